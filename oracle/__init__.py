@@ -1,0 +1,148 @@
+"""fp64 CPU oracle for Kimi Delta Attention -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never loads it, and
+the two share no code: this side is a plain C token loop in fp64
+(``kda_oracle.c``) plus this ctypes wrapper.
+
+Sources (page titles and sections):
+  * "Kimi K3 Open Weights: What Is Actually New In Its 2.8 Trillion Parameter
+    Architecture", section 1 "Kimi Delta Attention is a real new kernel
+    family": the delta-rule recurrence with o_t = S_t^T q_t, the bounded gate
+    g = -5 sigmoid(e^A z), alpha = e^g, and Q/K normalisation inside the op.
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` against closed
+forms, brute force and invariants that do not reuse this code.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kda_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+EPS = 1e-6
+G_MIN = -5.0
+
+
+def build(force: bool = False) -> str:
+    """Compile kda_oracle.c with gcc into oracle/_build/liboracle.so."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)) or (
+        os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+               "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = build()
+            lib = ctypes.CDLL(path)
+            dp = ctypes.POINTER(ctypes.c_double)
+            lib.kda_oracle_run.restype = ctypes.c_int
+            lib.kda_oracle_run.argtypes = [
+                dp, dp, dp, dp, dp, dp, dp,
+                ctypes.POINTER(ctypes.c_int64), ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
+                ctypes.c_double, ctypes.c_int, ctypes.POINTER(ctypes.c_int32),
+                ctypes.c_int64, dp, dp, ctypes.c_int]
+            lib.kda_oracle_gate.restype = ctypes.c_double
+            lib.kda_oracle_gate.argtypes = [ctypes.c_double, ctypes.c_double]
+            lib.kda_oracle_gate_vec.restype = None
+            lib.kda_oracle_gate_vec.argtypes = [dp, ctypes.c_int64, ctypes.c_double, dp]
+            _lib = lib
+    return _lib
+
+
+def _f64(x):
+    """Exact conversion of a bf16/fp32/fp64 array (numpy or torch) to fp64."""
+    if x is None:
+        return None
+    if hasattr(x, "detach"):  # torch tensor
+        x = x.detach().to("cpu")
+        import torch
+        x = x.to(torch.float64).numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a, ctype=ctypes.c_double):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def gate(z, A: float):
+    """g = -5 * sigmoid(e^A z), elementwise, in fp64."""
+    lib = _load()
+    zz = _f64(z)
+    out = np.empty_like(zz)
+    lib.kda_oracle_gate_vec(_ptr(zz), zz.size, float(A), _ptr(out))
+    return out
+
+
+def kda_reference(q, k, v, z, beta, A, initial_state=None, cu_seqlens=None,
+                  scale: float = 1.0, l2norm: bool = True, eps: float = EPS,
+                  chunk: int = 0, units=None, nthreads: int = 0):
+    """Run the oracle.
+
+    Layouts (token-major, packed):
+      q, k, z: [total_T, H, d_k];  v: [total_T, H, d_v];  beta: [total_T, H]
+      A: [H];  initial_state: [N, H, d_k, d_v] or None (zeros)
+      cu_seqlens: [N + 1] int, or None for one sequence of length total_T.
+    chunk: 0 = recurrent form (the oracle), C > 0 = the chunked form.
+    units: optional iterable of (n, h) pairs; only those are computed and the
+      other outputs are left as NaN.
+    Returns (o [total_T, H, d_v] fp64, final_state [N, H, d_k, d_v] fp64,
+    threads_used).
+    """
+    lib = _load()
+    q, k, v, z, beta, A = (_f64(t) for t in (q, k, v, z, beta, A))
+    if q.ndim == 4:  # [B, T, H, d] -> packed
+        B, T = q.shape[0], q.shape[1]
+        q, k, v, z = (t.reshape(B * T, *t.shape[2:]) for t in (q, k, v, z))
+        beta = beta.reshape(B * T, -1)
+        if cu_seqlens is None:
+            cu_seqlens = np.arange(B + 1, dtype=np.int64) * T
+    total_T, H, dk = q.shape
+    dv = v.shape[-1]
+    if cu_seqlens is None:
+        cu_seqlens = np.array([0, total_T], dtype=np.int64)
+    cu = np.ascontiguousarray(np.asarray(
+        cu_seqlens.cpu() if hasattr(cu_seqlens, "cpu") else cu_seqlens, dtype=np.int64))
+    N = cu.size - 1
+    if cu[0] != 0 or cu[-1] != total_T or np.any(np.diff(cu) < 0):
+        raise ValueError("cu_seqlens must be non-decreasing from 0 to total_T")
+    S0 = _f64(initial_state)
+    if S0 is not None and S0.shape != (N, H, dk, dv):
+        raise ValueError(f"initial_state shape {S0.shape} != {(N, H, dk, dv)}")
+    o = np.full((total_T, H, dv), np.nan)
+    S_out = np.full((N, H, dk, dv), np.nan)
+    if units is not None:
+        u = np.ascontiguousarray(np.asarray(list(units), dtype=np.int32).reshape(-1, 2))
+        n_units = u.shape[0]
+        uptr = _ptr(u, ctypes.c_int32)
+    else:
+        u, n_units, uptr = None, 0, None
+    rc = lib.kda_oracle_run(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(S0),
+        _ptr(cu, ctypes.c_int64), N, H, dk, dv, float(scale), int(bool(l2norm)),
+        float(eps), int(chunk), uptr, n_units, _ptr(o), _ptr(S_out), int(nthreads))
+    if rc <= 0:
+        raise RuntimeError(f"oracle failed with status {rc}")
+    return o, S_out, rc

@@ -1,0 +1,309 @@
+"""Pins of the fp64 oracle against facts that do not come from the oracle itself.
+
+Each test states where its expectation comes from: a closed form of the
+gate, the delta-rule overwrite property from the KDA row of the K3
+architecture census, an explicit product of transition matrices, a textbook
+special case, or an invariant that follows from the recurrence.  Together
+they fail on a dropped term, a wrong sign, a transposed operand or a read
+taken before instead of after the write.
+"""
+import json
+import math
+
+import numpy as np
+import pytest
+
+from conftest import golden_path
+
+RTOL = 1e-12
+
+
+def _rand_case(rng, T, H, dk, dv, N=1, nonzero_state=True, zscale=1.0):
+    q = rng.standard_normal((T, H, dk))
+    k = rng.standard_normal((T, H, dk))
+    v = rng.standard_normal((T, H, dv))
+    z = zscale * rng.standard_normal((T, H, dk))
+    beta = 1.0 / (1.0 + np.exp(-rng.standard_normal((T, H))))
+    A = 0.5 * rng.standard_normal(H)
+    S0 = 0.3 * rng.standard_normal((N, H, dk, dv)) if nonzero_state else None
+    return q, k, v, z, beta, A, S0
+
+
+def _unit(x, eps=1e-6):
+    return x / np.sqrt((x * x).sum(-1, keepdims=True) + eps)
+
+
+def _gate_test_side(z, A):
+    # Written independently of the oracle: g = -5 / (1 + exp(-e^A z)).
+    return -5.0 / (1.0 + np.exp(-np.exp(A) * z))
+
+
+def _close(a, b, tol=RTOL):
+    a = np.asarray(a)
+    b = np.asarray(b)
+    scale = max(1.0, float(np.max(np.abs(b))))
+    return float(np.max(np.abs(a - b))) <= tol * scale
+
+
+# --------------------------------------------------------------------- gate
+def test_gate_closed_forms(oracle_mod):
+    data = json.load(open(golden_path("gate_closed_forms.json")))
+    for c in data["cases"]:
+        g = oracle_mod.gate(np.array([c["z"]]), c["A"])[0]
+        assert abs(g - c["g"]) <= 1e-14, (c, g)
+
+
+def test_gate_range_and_alpha_bounds(oracle_mod):
+    rng = np.random.default_rng(1)
+    z = np.concatenate([rng.standard_normal(10000) * 5, [1e4, -1e4, 0.0, 1e308, -1e308]])
+    for A in (-3.0, -0.5, 0.0, 0.5, 2.0):
+        g = oracle_mod.gate(z, A)
+        assert np.all(g >= -5.0) and np.all(g <= 0.0)
+        alpha = np.exp(g)
+        assert np.all(alpha >= math.exp(-5.0)) and np.all(alpha <= 1.0)
+        # g is monotone non-increasing in z
+        order = np.argsort(z)
+        assert np.all(np.diff(g[order]) <= 1e-15)
+
+
+def test_tile_reciprocal_bound_fits_bf16():
+    """16 tokens at g >= -5 give 1/Gamma <= e^80, inside the BF16 range."""
+    data = json.load(open(golden_path("gate_closed_forms.json")))["tile_bound"]
+    worst_log = -data["g_min"] * data["tokens"]
+    assert worst_log == data["max_reciprocal_log"]
+    assert math.exp(worst_log) < data["bf16_max"]
+    # 17 tokens still fit, 18 do not: the bound is about tile length, not luck.
+    assert math.exp(5.0 * 17) < data["bf16_max"] < math.exp(5.0 * 18)
+
+
+# ---------------------------------------------------------------- overwrite
+def test_overwrite_golden(oracle_mod):
+    d = json.load(open(golden_path("overwrite_example.json")))
+    T, dk, dv = len(d["v"]), d["d_k"], d["d_v"]
+    q = np.array(d["q"]).reshape(T, 1, dk)
+    k = np.array(d["k"]).reshape(T, 1, dk)
+    v = np.array(d["v"]).reshape(T, 1, dv)
+    beta = np.array(d["beta"]).reshape(T, 1)
+    z = np.full((T, 1, dk), -1e4)          # sigmoid(-1e4) == 0 -> alpha == 1
+    A = np.zeros(1)
+    # k is exactly unit already; the in-op normalisation (with its 1e-6
+    # epsilon) is pinned separately in test_scale_and_normalisation.
+    o, S, _ = oracle_mod.kda_reference(q, k, v, z, beta, A, l2norm=False)
+    assert _close(o[:, 0], d["expected_o"], 1e-12)
+    assert not _close(o[1, 0], d["not_expected_o2"], 1e-3)
+    assert _close(S[0, 0], d["expected_final_state"], 1e-12)
+
+
+def test_delta_rule_readback(oracle_mod):
+    """k_hat^T S_t = (1 - beta_t) k_hat^T Diag(alpha_t) S_{t-1} + beta_t v_t^T.
+
+    With beta = 1 reading the key just written returns exactly v_t, whatever
+    the decay and the earlier content (the overwrite property in general)."""
+    rng = np.random.default_rng(2)
+    T, H, dk, dv = 7, 2, 6, 5
+    q, k, v, z, beta, A, S0 = _rand_case(rng, T, H, dk, dv)
+    k = _unit(k, eps=0.0)  # exactly unit keys; run without the in-op epsilon
+    for beta_mode in ("one", "random"):
+        b = np.ones_like(beta) if beta_mode == "one" else beta
+        for t in range(1, T + 1):
+            sl = slice(0, t)
+            _, S_t, _ = oracle_mod.kda_reference(q[sl], k[sl], v[sl], z[sl], b[sl], A, S0,
+                                                 l2norm=False)
+            if t == 1:
+                S_prev = S0
+            else:
+                _, S_prev, _ = oracle_mod.kda_reference(q[:t - 1], k[:t - 1], v[:t - 1],
+                                                        z[:t - 1], b[:t - 1], A, S0,
+                                                        l2norm=False)
+            for h in range(H):
+                kh = k[t - 1, h]
+                alpha = np.exp(_gate_test_side(z[t - 1, h], A[h]))
+                lhs = kh @ S_t[0, h]
+                rhs = (1 - b[t - 1, h]) * (kh @ (alpha[:, None] * S_prev[0, h])) \
+                    + b[t - 1, h] * v[t - 1, h]
+                assert _close(lhs, rhs, 1e-11)
+
+
+# ------------------------------------------------------------------ identity
+def test_identity_alpha1_beta0(oracle_mod):
+    rng = np.random.default_rng(3)
+    T, H, dk, dv = 9, 3, 5, 4
+    q, k, v, _, _, _, S0 = _rand_case(rng, T, H, dk, dv)
+    z = np.full((T, H, dk), -1e4)
+    A = np.zeros(H)
+    beta = np.zeros((T, H))
+    o, S, _ = oracle_mod.kda_reference(q, k, v, z, beta, A, S0)
+    assert np.array_equal(S, S0)
+    qh = _unit(q)
+    for t in range(T):
+        for h in range(H):
+            assert _close(o[t, h], S0[0, h].T @ qh[t, h], 1e-13)
+
+
+def test_decay_only_closed_form(oracle_mod):
+    """beta = 0: S_t = Diag(e^{sum_{i<=t} g_i}) S0 and o_t = S_t^T q_hat_t."""
+    rng = np.random.default_rng(4)
+    T, H, dk, dv = 11, 2, 6, 3
+    q, k, v, z, _, A, S0 = _rand_case(rng, T, H, dk, dv, zscale=2.0)
+    beta = np.zeros((T, H))
+    o, S, _ = oracle_mod.kda_reference(q, k, v, z, beta, A, S0)
+    qh = _unit(q)
+    for h in range(H):
+        gam = np.cumsum(_gate_test_side(z[:, h], A[h]), axis=0)  # [T, dk]
+        assert _close(S[0, h], np.exp(gam[-1])[:, None] * S0[0, h], 1e-12)
+        for t in range(T):
+            St = np.exp(gam[t])[:, None] * S0[0, h]
+            assert _close(o[t, h], St.T @ qh[t, h], 1e-12)
+
+
+# --------------------------------------------------------------- brute force
+@pytest.mark.parametrize("T,dk,dv", [(1, 4, 3), (5, 4, 3), (8, 6, 5), (8, 3, 7)])
+def test_brute_force_transition_products(oracle_mod, T, dk, dv):
+    """Explicit M_t = (I - beta_t k_t k_t^T) Diag(alpha_t), then
+    S_t = M_t...M_1 S0 + sum_i M_t...M_{i+1} beta_i k_i v_i^T,  o_t = S_t^T q_t."""
+    rng = np.random.default_rng(10 + T + dk)
+    H = 2
+    q, k, v, z, beta, A, S0 = _rand_case(rng, T, H, dk, dv)
+    o, S, _ = oracle_mod.kda_reference(q, k, v, z, beta, A, S0)
+    qh, kh = _unit(q), _unit(k)
+    for h in range(H):
+        M = []
+        for t in range(T):
+            alpha = np.exp(_gate_test_side(z[t, h], A[h]))
+            M.append((np.eye(dk) - beta[t, h] * np.outer(kh[t, h], kh[t, h])) @ np.diag(alpha))
+        for t in range(T):
+            P = np.eye(dk)
+            for s in range(t, -1, -1):
+                P = P @ M[s]
+            St = P @ S0[0, h]
+            for i in range(t + 1):
+                Pi = np.eye(dk)
+                for s in range(t, i, -1):
+                    Pi = Pi @ M[s]
+                St = St + Pi @ (beta[i, h] * np.outer(kh[i, h], v[i, h]))
+            assert _close(o[t, h], St.T @ qh[t, h], 1e-12)
+            if t == T - 1:
+                assert _close(S[0, h], St, 1e-12)
+
+
+# ------------------------------------------------------ chunked == recurrent
+@pytest.mark.parametrize("C", [1, 3, 16, 64])
+def test_chunked_form_equals_recurrent(oracle_mod, C):
+    rng = np.random.default_rng(20 + C)
+    lens = [50, 0, 37, 70]
+    T, H, dk, dv = sum(lens), 2, 8, 6
+    q, k, v, z, beta, A, S0 = _rand_case(rng, T, H, dk, dv, N=len(lens), zscale=2.0)
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    o_r, S_r, _ = oracle_mod.kda_reference(q, k, v, z, beta, A, S0, cu)
+    o_c, S_c, _ = oracle_mod.kda_reference(q, k, v, z, beta, A, S0, cu, chunk=C)
+    assert _close(o_c, o_r, 1e-10)
+    assert _close(S_c, S_r, 1e-10)
+    # the zero-length sequence returns its initial state
+    assert np.array_equal(S_r[1], S0[1])
+
+
+# ---------------------------------------------------------------- invariants
+def test_linearity_in_v_and_state(oracle_mod):
+    rng = np.random.default_rng(5)
+    T, H, dk, dv = 12, 2, 5, 4
+    q, k, v1, z, beta, A, S1 = _rand_case(rng, T, H, dk, dv)
+    v2 = rng.standard_normal(v1.shape)
+    S2 = rng.standard_normal(S1.shape)
+    a, b = 0.7, -1.9
+    o1, F1, _ = oracle_mod.kda_reference(q, k, v1, z, beta, A, S1)
+    o2, F2, _ = oracle_mod.kda_reference(q, k, v2, z, beta, A, S2)
+    o3, F3, _ = oracle_mod.kda_reference(q, k, a * v1 + b * v2, z, beta, A, a * S1 + b * S2)
+    assert _close(o3, a * o1 + b * o2, 1e-12)
+    assert _close(F3, a * F1 + b * F2, 1e-12)
+
+
+def test_value_column_permutation(oracle_mod):
+    rng = np.random.default_rng(6)
+    T, H, dk, dv = 10, 2, 4, 6
+    q, k, v, z, beta, A, S0 = _rand_case(rng, T, H, dk, dv)
+    perm = rng.permutation(dv)
+    o, S, _ = oracle_mod.kda_reference(q, k, v, z, beta, A, S0)
+    op, Sp, _ = oracle_mod.kda_reference(q, k, v[..., perm], z, beta, A, S0[..., perm])
+    assert _close(op, o[..., perm], 1e-13)
+    assert _close(Sp, S[..., perm], 1e-13)
+
+
+def test_textbook_causal_linear_attention(oracle_mod):
+    """alpha = 1, beta = 1, orthonormal keys, zero state: o_t = sum_{i<=t} (q.k_i) v_i."""
+    rng = np.random.default_rng(7)
+    T, H, dk, dv = 6, 1, 8, 3
+    Qm, _ = np.linalg.qr(rng.standard_normal((dk, dk)))
+    k = Qm[:T].reshape(T, H, dk)
+    q = rng.standard_normal((T, H, dk))
+    v = rng.standard_normal((T, H, dv))
+    z = np.full((T, H, dk), -1e4)
+    A = np.zeros(H)
+    beta = np.ones((T, H))
+    o, _, _ = oracle_mod.kda_reference(q, k, v, z, beta, A, l2norm=False)
+    for t in range(T):
+        ref = sum((q[t, 0] @ k[i, 0]) * v[i, 0] for i in range(t + 1))
+        assert _close(o[t, 0], ref, 1e-12)
+
+
+def test_contraction_bound(oracle_mod):
+    """||S_t||_2 <= ||S_{t-1}||_2 + beta_t ||v_t||: both factors of the
+    transition have spectral norm <= 1 for unit k and beta in [0, 1]."""
+    rng = np.random.default_rng(8)
+    T, H, dk, dv = 16, 1, 6, 6
+    q, k, v, z, beta, A, S0 = _rand_case(rng, T, H, dk, dv)
+    prev = np.linalg.norm(S0[0, 0], 2)
+    for t in range(1, T + 1):
+        _, S, _ = oracle_mod.kda_reference(q[:t], k[:t], v[:t], z[:t], beta[:t], A, S0)
+        cur = np.linalg.norm(S[0, 0], 2)
+        assert cur <= prev + beta[t - 1, 0] * np.linalg.norm(v[t - 1, 0]) + 1e-12
+        prev = cur
+
+
+def test_varlen_equals_separate_and_split_handoff(oracle_mod):
+    rng = np.random.default_rng(9)
+    lens = [13, 1, 20]
+    T, H, dk, dv = sum(lens), 2, 5, 4
+    q, k, v, z, beta, A, S0 = _rand_case(rng, T, H, dk, dv, N=len(lens))
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    o, S, _ = oracle_mod.kda_reference(q, k, v, z, beta, A, S0, cu)
+    for n in range(len(lens)):
+        sl = slice(cu[n], cu[n + 1])
+        on, Sn, _ = oracle_mod.kda_reference(q[sl], k[sl], v[sl], z[sl], beta[sl], A, S0[n:n + 1])
+        assert np.array_equal(on, o[sl])
+        assert np.array_equal(Sn[0], S[n])
+    # split the last sequence at 7 and hand the state over
+    sl = slice(cu[2], cu[3])
+    a = slice(cu[2], cu[2] + 7)
+    b = slice(cu[2] + 7, cu[3])
+    oa, Sa, _ = oracle_mod.kda_reference(q[a], k[a], v[a], z[a], beta[a], A, S0[2:3])
+    ob, Sb, _ = oracle_mod.kda_reference(q[b], k[b], v[b], z[b], beta[b], A, Sa)
+    assert np.array_equal(np.concatenate([oa, ob]), o[sl])
+    assert np.array_equal(Sb[0], S[2])
+
+
+def test_scale_and_normalisation(oracle_mod):
+    """o is linear in `scale`; positive rescaling of raw q, k does not matter
+    up to the 1e-6 epsilon under the root."""
+    rng = np.random.default_rng(11)
+    T, H, dk, dv = 9, 2, 7, 3
+    q, k, v, z, beta, A, S0 = _rand_case(rng, T, H, dk, dv)
+    o1, S1, _ = oracle_mod.kda_reference(q, k, v, z, beta, A, S0, scale=1.0)
+    o2, S2, _ = oracle_mod.kda_reference(q, k, v, z, beta, A, S0, scale=0.125)
+    assert _close(o2, 0.125 * o1, 1e-13)
+    assert np.array_equal(S1, S2)
+    o3, S3, _ = oracle_mod.kda_reference(3.0 * q, 0.5 * k, v, z, beta, A, S0)
+    assert _close(o3, o1, 1e-5) and _close(S3, S1, 1e-5)
+
+
+def test_units_subset_matches_full(oracle_mod):
+    rng = np.random.default_rng(12)
+    lens = [9, 14]
+    T, H, dk, dv = sum(lens), 3, 4, 4
+    q, k, v, z, beta, A, S0 = _rand_case(rng, T, H, dk, dv, N=2)
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    o, S, _ = oracle_mod.kda_reference(q, k, v, z, beta, A, S0, cu)
+    os_, Ss, _ = oracle_mod.kda_reference(q, k, v, z, beta, A, S0, cu, units=[(1, 2), (0, 0)])
+    assert np.array_equal(os_[cu[1]:, 2], o[cu[1]:, 2])
+    assert np.array_equal(os_[:cu[1], 0], o[:cu[1], 0])
+    assert np.array_equal(Ss[1, 2], S[1, 2]) and np.array_equal(Ss[0, 0], S[0, 0])
+    assert np.isnan(os_[:cu[1], 1]).all()
