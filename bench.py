@@ -1,0 +1,393 @@
+#!/usr/bin/env python3
+"""KDA benchmark on GB300: prefill tokens/s and decode state GB/s.
+
+Default workload (one "step" = one pass of the whole hot path):
+  kda_prefill on B=1, H=32, T=4096, d_k=d_v=128 (bf16 q/k/v/z/beta, fp32 A,
+  zero initial state) returning the fp32 final state, then one kda_decode_step
+  for each of the 32 heads from that final state (the decode handoff).
+The headline `value` is prefill tokens/s (B*T / step time).  The `decode`
+object times the decode workload B=256, H=96, d=128 (fp32 state ~1.6 GB resident
+in HBM, bf16 per-step inputs) over 64 consecutive steps, as state GB/s.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kda|reference]
+Under torchrun each rank runs an independent replica (the path needs no
+collective); rank 0 prints one JSON line with the whole-job throughput.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill tokens/s (% tensor peak); decode state GB/s (% HBM peak), 1 GB300"
+PREFILL_SHAPE = dict(B=1, H=32, T=4096, d=128)
+DECODE_SHAPE = dict(B=256, H=96, d=128, steps=64)
+L2_BYTES = 129 * 1024 * 1024
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured (MEASURED_PEAKS.json)")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0,
+                source="fallback")
+
+
+def prefill_algorithmic(B, H, T, d, C=64):
+    """Algorithmic bytes and flops of one prefill call (d_k = d_v = d, bf16 I/O).
+
+    bytes: q, k, v, z, o at 2 B per element, beta at 2 B per head-token, the fp32
+    final state once (zero initial state is not read).
+    flops: 6 d^2 per head-token for the three state contractions plus
+    (C+1)(3d+2d) - d for the causal halves of the intra-chunk products."""
+    ht = B * T * H
+    byts = ht * (5 * d * 2 + 2) + B * H * d * d * 4
+    flops = ht * (6 * d * d + (C + 1) * 5 * d - d)
+    return byts, flops
+
+
+def decode_algorithmic(B, H, d):
+    """Bytes of one decode step: fp32 state read + write, bf16 q,k,v,z in, o out, beta."""
+    return B * H * (2 * d * d * 4 + 5 * d * 2 + 2)
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def _barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def _max_over_ranks(pg, x: float) -> float:
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ oracle arm
+def run_oracle_sample(T_sample: int, H: int, d: int, seed: int = 0):
+    """Time the fp64 CPU oracle on the first T_sample tokens of the prefill
+    workload (all heads).  Returns (tokens/s, seconds, threads)."""
+    import torch
+    import oracle
+    from kimi_delta_attention_12_gb300 import inputs
+    x = inputs.make_prefill_inputs([T_sample], H, d, d, torch.bfloat16, seed=seed)
+    oracle.build()
+    t0 = time.perf_counter()
+    _, _, threads = oracle.kda_reference(x.q, x.k, x.v, x.z, x.beta, x.A, None, x.cu_seqlens)
+    dt = time.perf_counter() - t0
+    return T_sample / dt, dt, threads
+
+
+def reference_arm(args, world, rank, pg):
+    if rank != 0:
+        return
+    P = PREFILL_SHAPE
+    T_sample = 1024
+    # one warm-up and K timed samples; each sample is the first 1024 tokens of
+    # the prefill workload, all 32 heads
+    for _ in range(max(0, min(args.warmup, 1))):
+        run_oracle_sample(256, P["H"], P["d"])
+    vals, secs, threads = [], 0.0, 1
+    for _ in range(args.steps):
+        v, dt, threads = run_oracle_sample(T_sample, P["H"], P["d"])
+        vals.append(v)
+        secs += dt
+    value = statistics.median(vals)
+    sample = (f"first {T_sample} tokens of B=1 H=32 T=4096 d=128 (all 32 heads) per step, "
+              f"{args.steps} steps, fp64 C oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * secs / max(args.steps, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded torch CPU generator)",
+        "config": {"workload": "prefill B=1 H=32 T=4096 d_k=d_v=128 bf16 inputs", "B": 1,
+                   "H": 32, "T": 4096, "d": 128},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------- GPU arm
+def kda_arm(args, world, rank, local, pg):
+    import torch
+    import kimi_delta_attention_12_gb300 as kda
+    from kimi_delta_attention_12_gb300 import inputs
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    kda.lib()
+    stream = torch.cuda.current_stream()
+    peaks = _peaks()
+    P = PREFILL_SHAPE
+    B, H, T, d = P["B"], P["H"], P["T"], P["d"]
+    byts, flops = prefill_algorithmic(B, H, T, d)
+
+    # rotating input sets so that each step's inputs are not L2-resident
+    x_host = inputs.make_prefill_inputs([T] * B, H, d, d, torch.bfloat16, seed=rank)
+    set_bytes = byts
+    nsets = max(2, -(-3 * L2_BYTES // set_bytes))
+    sets = []
+    for i in range(nsets):
+        xi = x_host.to(dev) if i == 0 else inputs.PrefillInputs(
+            *(t.clone() if t is not None else None for t in
+              (sets[0].q, sets[0].k, sets[0].v, sets[0].z, sets[0].beta, sets[0].A,
+               sets[0].initial_state, sets[0].cu_seqlens)))
+        sets.append(xi)
+    o = torch.empty(B * T, H, d, dtype=torch.bfloat16, device=dev)
+    S = torch.empty(B, H, d, d, dtype=torch.float32, device=dev)
+    ws = kda.alloc_workspace(B, B * T, H, d, d, torch.bfloat16, dev)
+    o_dec = torch.empty(B, H, d, dtype=torch.bfloat16, device=dev)
+    cu_host = sets[0].cu_seqlens.cpu()
+
+    def step(i, ev=None):
+        x = sets[i % nsets]
+        if ev is not None:
+            ev[0].record(stream)
+        kda.kda_prefill(x.q, x.k, x.v, x.z, x.beta, x.A, None, x.cu_seqlens,
+                        cu_seqlens_host=cu_host, o=o, final_state=S, workspace=ws)
+        if ev is not None:
+            ev[1].record(stream)
+        # decode handoff: the next token of each head continues from S
+        kda.kda_decode_step(x.q[:B], x.k[:B], x.v[:B], x.z[:B], x.beta[:B], x.A, S, o=o_dec)
+
+    launches_per_step = 2
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    assert kda.workspace_status(ws) == kda.KDA_OK, "prefill kernel reported a timeout"
+
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    _barrier(pg)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(args.warmup + i, kev[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    _barrier(pg)
+    ms_total = t_start.elapsed_time(t_end)
+    ms_total = _max_over_ranks(pg, ms_total)
+    kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
+    ms_per_step = ms_total / args.steps
+    value = world * B * T / (ms_per_step / 1e3)
+    achieved_gbs = byts / (kernel_ms / 1e3) / 1e9
+    achieved_tf = flops / (kernel_ms / 1e3) / 1e12
+
+    # ---- end to end through the public API with host buffers ----
+    pin = lambda t: t.pin_memory()
+    hq, hk, hv, hz, hb = (pin(t) for t in (x_host.q, x_host.k, x_host.v, x_host.z, x_host.beta))
+    hA, hcu = pin(x_host.A), pin(x_host.cu_seqlens)
+    ho = torch.empty(B * T, H, d, dtype=torch.bfloat16).pin_memory()
+    hS = torch.empty(B, H, d, d, dtype=torch.float32).pin_memory()
+    dq, dk_, dv_, dz, db = (torch.empty_like(t, device=dev) for t in (hq, hk, hv, hz, hb))
+    dA, dcu = torch.empty_like(hA, device=dev), torch.empty_like(hcu, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hz, hb, hA, hcu))
+    d2h = ho.numel() * ho.element_size() + hS.numel() * hS.element_size()
+
+    def e2e_step():
+        for dst, src in ((dq, hq), (dk_, hk), (dv_, hv), (dz, hz), (db, hb), (dA, hA), (dcu, hcu)):
+            dst.copy_(src, non_blocking=True)
+        kda.kda_prefill(dq, dk_, dv_, dz, db, dA, None, dcu, cu_seqlens_host=cu_host,
+                        o=o, final_state=S, workspace=ws)
+        ho.copy_(o, non_blocking=True)
+        hS.copy_(S, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    _barrier(pg)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    _barrier(pg)
+    e2e_ms = _max_over_ranks(pg, e0.elapsed_time(e1)) / args.steps
+    e2e_value = world * B * T / (e2e_ms / 1e3)
+
+    # ---- decode workload: 64 consecutive steps on a resident 1.6 GB state ----
+    D = DECODE_SHAPE
+    g = torch.Generator(device=dev).manual_seed(1000 + rank)
+    Bd, Hd, dd = D["B"], D["H"], D["d"]
+    state = 0.02 * torch.randn(Bd, Hd, dd, dd, device=dev, generator=g)
+    Adec = 0.5 * torch.randn(Hd, device=dev, generator=g)
+    unit = lambda t: t / t.norm(dim=-1, keepdim=True)
+    dsteps = []
+    for s in range(D["steps"]):
+        dsteps.append((unit(torch.randn(Bd, Hd, dd, device=dev, generator=g)).bfloat16(),
+                       unit(torch.randn(Bd, Hd, dd, device=dev, generator=g)).bfloat16(),
+                       torch.randn(Bd, Hd, dd, device=dev, generator=g).bfloat16(),
+                       torch.randn(Bd, Hd, dd, device=dev, generator=g).bfloat16(),
+                       torch.sigmoid(torch.randn(Bd, Hd, device=dev, generator=g)).bfloat16()))
+    od = torch.empty(Bd, Hd, dd, dtype=torch.bfloat16, device=dev)
+    for s in range(3):
+        q_, k_, v_, z_, b_ = dsteps[s]
+        kda.kda_decode_step(q_, k_, v_, z_, b_, Adec, state, o=od)
+    torch.cuda.synchronize()
+    dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(D["steps"])]
+    with ClockSampler(local) as dclk:
+        for s in range(D["steps"]):
+            q_, k_, v_, z_, b_ = dsteps[s]
+            dev_ev[s][0].record(stream)
+            kda.kda_decode_step(q_, k_, v_, z_, b_, Adec, state, o=od)
+            dev_ev[s][1].record(stream)
+        torch.cuda.synchronize()
+    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dev_ev)
+    dec_bytes = decode_algorithmic(Bd, Hd, dd)
+    dec_gbs = dec_bytes / (dec_ms / 1e3) / 1e9
+
+    if rank != 0:
+        return
+    # CPU baseline: the oracle on a bounded sample of the prefill workload
+    cpu_tps, cpu_s, cpu_threads = run_oracle_sample(1024, H, d)
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof):
+        traffic = json.load(open(prof)).get("prefill_bytes_per_launch")
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded generators; inputs rotated over "
+                f"{nsets} sets of {set_bytes / 1e6:.0f} MB > L2)",
+        "config": {"workload": "prefill B=1 H=32 T=4096 d_k=d_v=128 bf16 + decode handoff",
+                   "B": B, "H": H, "T": T, "d": d, "chunk": 64,
+                   "l2": "inputs larger than L2 (rotating sets)", "parallelism": "replicas"},
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"],
+                     "traffic": traffic, "kernel_ms": kernel_ms,
+                     "algorithmic_bytes": byts, "peak_source": peaks["source"],
+                     "tensor_tflops": achieved_tf,
+                     "tensor_frac": achieved_tf / peaks["bf16_tflops"]},
+        "decode": {"metric": "decode state GB/s", "value": dec_gbs, "unit": "GB/s",
+                   "ms_per_step": dec_ms, "bytes_per_step": dec_bytes,
+                   "config": {"workload": "decode B=256 H=96 d=128 fp32 state, bf16 inputs",
+                              "steps": D["steps"]},
+                   "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm_gbs"],
+                                "unit": "GB/s", "frac": dec_gbs / peaks["hbm_gbs"]},
+                   "clocks": dclk.summary()},
+        "cpu_baseline": {"value": cpu_tps, "unit": "tokens/s", "cores": cpu_threads,
+                         "kind": "oracle",
+                         "sample": "first 1024 tokens of the prefill workload, all 32 heads, "
+                                   f"{cpu_s:.2f} s of fp64 C oracle"},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["kda", "reference"], default="kda")
+    args = ap.parse_args()
+    world, rank, local, pg = _dist_setup(args)
+    try:
+        if args.impl == "reference":
+            reference_arm(args, world, rank, pg)
+        else:
+            kda_arm(args, world, rank, local, pg)
+    finally:
+        if pg is not None:
+            pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

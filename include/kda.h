@@ -1,0 +1,178 @@
+/*
+ * kda.h -- C ABI of the Kimi Delta Attention (KDA) library for one GB300
+ * (sm_103a).
+ *
+ * The operation (per sequence n and head h, tokens t in order), from
+ * "Kimi K3 Open Weights: What Is Actually New In Its 2.8 Trillion Parameter
+ * Architecture", section 1 "Kimi Delta Attention is a real new kernel family":
+ *
+ *     g_t     = -5 * sigmoid(e^{A_h} * z_t)           (gate equation; per channel)
+ *     alpha_t = e^{g_t}                                in [e^-5, 1]
+ *     S_t     = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *     o_t     = S_t^T q_t                              (recurrence equation)
+ *
+ * with q_t, k_t L2-normalised inside the call ("Q/K normalization" in the
+ * section's prefill bullet) when KDA_FLAG_L2NORM_QK is set:
+ *     x_hat = x / sqrt(sum x^2 + 1e-6),   q_hat additionally times `scale`.
+ * S is d_k x d_v per (sequence, head), kept in fp32.  Prefill processes tokens
+ * "parallel within chunks, recurrent between"; decode advances one token with
+ * the state persistent in device memory (same section, runtime split).
+ *
+ * Conventions shared by every call
+ *   - Memory: every tensor pointer is a DEVICE pointer owned by the caller
+ *     (the library allocates nothing).  Layouts are token-major and dense:
+ *     x[token][head][channel].  States are [n][H][d_k][d_v] row-major fp32.
+ *   - Alignment: q, k, v, z, o, states: 16-byte aligned; beta: element
+ *     aligned; A, cu_seqlens, slots: 4-byte aligned.
+ *   - Sizes: d_k, d_v in {32, 64, 128}; other values -> KDA_ERR_UNSUPPORTED.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL = the legacy default stream).  A call validates its arguments on
+ *     the host, launches, and returns; host-detectable errors return a
+ *     negative status and launch nothing.  A CUDA launch failure returns
+ *     KDA_ERR_CUDA.  No exception or abort crosses this boundary.
+ *   - Calls are re-entrant; the library keeps no mutable global state apart
+ *     from lazily resolved driver entry points.
+ *   - Input buffers must not alias output buffers unless stated.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = -1,  /* null pointer, bad size, bad cu_seqlens mirror   */
+    KDA_ERR_UNSUPPORTED = -2,  /* head dim or dtype outside the supported set      */
+    KDA_ERR_ALIGNMENT = -3,    /* a pointer violates the alignment rule above       */
+    KDA_ERR_WORKSPACE = -4,    /* workspace missing or smaller than required        */
+    KDA_ERR_CUDA = -5,         /* a CUDA runtime/driver call failed                 */
+    KDA_ERR_TIMEOUT = -6       /* a kernel gave up a bounded wait (see kda_workspace_status) */
+} kda_status;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+enum {
+    KDA_FLAG_L2NORM_QK = 1,    /* L2-normalise q and k inside the call (default on)  */
+    KDA_FLAG_RECURRENT = 2     /* kda_prefill only: run the fused recurrent kernel
+                                  (fp32 arithmetic, one token at a time) even where
+                                  the chunked tensor-core kernel applies */
+};
+#define KDA_DEFAULT_FLAGS KDA_FLAG_L2NORM_QK
+
+/*
+ * Bytes of device workspace kda_prefill needs for these sizes (a status word,
+ * a work counter and the per-unit schedule).  Always > 0.  The workspace is
+ * scratch: its content on entry does not matter and it may be reused by the
+ * next call on the same stream.
+ */
+KDA_API size_t kda_prefill_workspace_bytes(int32_t N, int32_t total_T, int32_t H,
+                                   int32_t d_k, int32_t d_v, kda_dtype dt);
+
+/*
+ * kda_prefill -- chunked prefill over N packed sequences.
+ *
+ *  q, k, z        [total_T, H, d_k]  dt
+ *  v              [total_T, H, d_v]  dt
+ *  beta           [total_T, H]       dt, values in [0, 1]
+ *  A              [H]                fp32, log-scale of the gate (e^A multiplies z)
+ *  initial_state  [N, H, d_k, d_v]   fp32, or NULL for zeros
+ *  cu_seqlens     [N + 1] int32 DEVICE array of sequence starts (0 = first,
+ *                 total_T = last), or NULL for N equal sequences of total_T / N
+ *                 (total_T % N must be 0).
+ *  cu_seqlens_host  optional HOST mirror of cu_seqlens.  When given it is
+ *                 validated (starts at 0, non-decreasing, ends at total_T)
+ *                 and used to schedule long sequences first.
+ *  scale          multiplies q_hat (1.0 = none)
+ *  flags          KDA_FLAG_L2NORM_QK or 0
+ *  o              [total_T, H, d_v]  dt, output (o_t for every token)
+ *  final_state    [N, H, d_k, d_v] fp32, or NULL.  May alias initial_state
+ *                 (in-place update is allowed).
+ *  workspace      device scratch of at least kda_prefill_workspace_bytes()
+ *
+ * A zero-length sequence returns final_state = initial_state (or zeros).
+ * bf16 with d_k = d_v = 128 runs the tcgen05/TMEM chunked kernel; every other
+ * size/dtype runs the fused recurrent kernel (fp32 arithmetic throughout).
+ */
+KDA_API int kda_prefill(const void* q, const void* k, const void* v, const void* z,
+                const void* beta, const float* A, const float* initial_state,
+                const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                int32_t N, int32_t total_T, int32_t H, int32_t d_k, int32_t d_v,
+                kda_dtype dt, float scale, uint32_t flags,
+                void* o, float* final_state,
+                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * kda_workspace_status -- wait for `stream`, then read the status word a
+ * kda_prefill launch left in `workspace`.  Returns KDA_OK, KDA_ERR_TIMEOUT
+ * (a bounded wait inside the kernel ran out; its outputs are invalid) or
+ * KDA_ERR_CUDA.  Synchronising; meant for tests and diagnostics.
+ */
+KDA_API int kda_workspace_status(const void* workspace, void* stream);
+
+/*
+ * kda_decode_step -- one token for each of B sequences, state updated in
+ * place in a pool (section 1: "one recurrent-state update per layer and
+ * token, with ... recurrent state kept persistent").
+ *
+ *  q, k, z        [B, H, d_k]  dt;   v [B, H, d_v] dt;   beta [B, H] dt
+ *  A              [H] fp32
+ *  state          [pool_size, H, d_k, d_v] fp32, read and written in place
+ *  slots          [B] int32 device array: row b uses state[slots[b]]; NULL
+ *                 means slots[b] = b (then pool_size >= B is required).
+ *                 Slots must be distinct; a slot outside [0, pool_size)
+ *                 leaves that state untouched and writes NaN to its o row.
+ *  o              [B, H, d_v] dt
+ */
+KDA_API int kda_decode_step(const void* q, const void* k, const void* v, const void* z,
+                    const void* beta, const float* A, float* state,
+                    const int32_t* slots, int32_t pool_size,
+                    int32_t B, int32_t H, int32_t d_k, int32_t d_v,
+                    kda_dtype dt, float scale, uint32_t flags,
+                    void* o, void* stream);
+
+/*
+ * kda_state_io -- moves fp32 states of shape [H, d_k, d_v] each (the
+ * persistent KDA state that prefill hands to decode).
+ *
+ *  KDA_STATE_ZERO     dst[i] = 0 for i < n, or dst[slots[i]] = 0 when slots
+ *                     is given (then dst is a pool of pool_size states).
+ *  KDA_STATE_COPY     dst[0..n) = src[0..n); any direction (host or device
+ *                     pointers, cudaMemcpyDefault).  slots must be NULL.
+ *  KDA_STATE_GATHER   dst[i] = src[slots[i]]   (pool -> batch), i < n
+ *  KDA_STATE_SCATTER  dst[slots[i]] = src[i]   (batch -> pool), i < n
+ * Out-of-range slots skip their state.  For GATHER/SCATTER/ZERO the
+ * pointers are device pointers.
+ */
+typedef enum {
+    KDA_STATE_ZERO = 0,
+    KDA_STATE_COPY = 1,
+    KDA_STATE_GATHER = 2,
+    KDA_STATE_SCATTER = 3
+} kda_state_op;
+
+KDA_API int kda_state_io(kda_state_op op, float* dst, const float* src,
+                 const int32_t* slots, int32_t n, int32_t pool_size,
+                 int32_t H, int32_t d_k, int32_t d_v, void* stream);
+
+/* Human-readable name of a kda_status value (static storage). */
+KDA_API const char* kda_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+KDA_API int kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

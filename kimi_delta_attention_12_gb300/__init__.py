@@ -1,0 +1,243 @@
+"""Kimi Delta Attention (KDA) for one GB300 -- Python binding of libkda.so.
+
+This module only marshals arguments: torch supplies device memory and the
+current CUDA stream, and every step of the computation runs in the library's
+CUDA kernels behind the C ABI of ``include/kda.h``.  There is no CPU path:
+if the library is not built, or no CUDA device is present, calls raise.
+
+Entry points (same names as the C ABI):
+  kda_prefill(q, k, v, z, beta, A, ...)      chunked prefill over packed sequences
+  kda_decode_step(q, k, v, z, beta, A, state, ...)  one token per sequence, state in place
+  kda_state_io(op, dst, src, ...)            zero / copy / gather / scatter of states
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libkda.so")
+
+KDA_OK = 0
+KDA_ERR_INVALID_ARG = -1
+KDA_ERR_UNSUPPORTED = -2
+KDA_ERR_ALIGNMENT = -3
+KDA_ERR_WORKSPACE = -4
+KDA_ERR_CUDA = -5
+KDA_ERR_TIMEOUT = -6
+
+KDA_F32 = 0
+KDA_BF16 = 1
+
+KDA_FLAG_L2NORM_QK = 1
+KDA_FLAG_RECURRENT = 2
+
+KDA_STATE_ZERO = 0
+KDA_STATE_COPY = 1
+KDA_STATE_GATHER = 2
+KDA_STATE_SCATTER = 3
+
+# Every symbol include/kda.h declares.
+EXPORTED_SYMBOLS = (
+    "kda_prefill_workspace_bytes", "kda_prefill", "kda_workspace_status",
+    "kda_decode_step", "kda_state_io", "kda_status_string", "kda_version",
+)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class KDAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what} failed: {status_string(status)} ({status})")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libkda.so (built by ``__graft_entry__.build()``); raise if absent."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"KDA CUDA library not found at {LIB_PATH}; build it with "
+                    "`python -c 'import __graft_entry__ as g; g.build()'`")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i32, u32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32, ctypes.c_size_t
+            f32 = ctypes.c_float
+            L.kda_prefill_workspace_bytes.restype = sz
+            L.kda_prefill_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, ctypes.c_int]
+            L.kda_prefill.restype = ctypes.c_int
+            L.kda_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                      i32, i32, i32, i32, i32, ctypes.c_int, f32, u32,
+                                      vp, vp, vp, sz, vp]
+            L.kda_workspace_status.restype = ctypes.c_int
+            L.kda_workspace_status.argtypes = [vp, vp]
+            L.kda_decode_step.restype = ctypes.c_int
+            L.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32,
+                                          i32, i32, i32, i32, ctypes.c_int, f32, u32, vp, vp]
+            L.kda_state_io.restype = ctypes.c_int
+            L.kda_state_io.argtypes = [ctypes.c_int, vp, vp, vp, i32, i32, i32, i32, i32, vp]
+            L.kda_status_string.restype = ctypes.c_char_p
+            L.kda_status_string.argtypes = [ctypes.c_int]
+            L.kda_version.restype = ctypes.c_int
+            L.kda_version.argtypes = []
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().kda_status_string(int(status)).decode()
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream]):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float32:
+        return KDA_F32
+    if dt == torch.bfloat16:
+        return KDA_BF16
+    raise TypeError(f"unsupported dtype {dt}; KDA takes float32 or bfloat16")
+
+
+def _check_cuda(*ts):
+    for t in ts:
+        if t is not None:
+            if not t.is_cuda:
+                raise ValueError("KDA tensors must live on a CUDA device")
+            if not t.is_contiguous():
+                raise ValueError("KDA tensors must be contiguous")
+
+
+def prefill_workspace_bytes(N: int, total_T: int, H: int, d_k: int, d_v: int,
+                            dtype: torch.dtype) -> int:
+    return int(lib().kda_prefill_workspace_bytes(N, total_T, H, d_k, d_v, _dtype_code(dtype)))
+
+
+def alloc_workspace(N: int, total_T: int, H: int, d_k: int, d_v: int, dtype: torch.dtype,
+                    device=None) -> torch.Tensor:
+    nbytes = prefill_workspace_bytes(N, total_T, H, d_k, d_v, dtype)
+    return torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def kda_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: torch.Tensor,
+                beta: torch.Tensor, A: torch.Tensor,
+                initial_state: Optional[torch.Tensor] = None,
+                cu_seqlens: Optional[torch.Tensor] = None,
+                cu_seqlens_host: Optional[torch.Tensor] = None,
+                scale: float = 1.0, l2norm: bool = True, recurrent: bool = False,
+                output_final_state: bool = True,
+                o: Optional[torch.Tensor] = None, final_state: Optional[torch.Tensor] = None,
+                workspace: Optional[torch.Tensor] = None,
+                stream: Optional[torch.cuda.Stream] = None
+                ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Chunked KDA prefill.  Packed layout: q, k, z [total_T, H, d_k], v
+    [total_T, H, d_v], beta [total_T, H]; a 4-D [B, T, H, d] batch is accepted
+    and treated as B sequences of length T.  Returns (o, final_state)."""
+    batched = q.dim() == 4
+    if batched:
+        B, T = q.shape[:2]
+        q, k, v, z = (t.reshape(B * T, *t.shape[2:]) for t in (q, k, v, z))
+        beta = beta.reshape(B * T, -1)
+        N = B
+    else:
+        N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    total_T, H, d_k = q.shape
+    d_v = v.shape[-1]
+    dt = q.dtype
+    for t in (k, v, z, beta):
+        if t.dtype != dt:
+            raise TypeError("q, k, v, z and beta must share one dtype")
+    _check_cuda(q, k, v, z, beta, A, initial_state, cu_seqlens)
+    if A.dtype != torch.float32:
+        raise TypeError("A must be float32")
+    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    if initial_state is not None and initial_state.dtype != torch.float32:
+        raise TypeError("initial_state must be float32")
+    if o is None:
+        o = torch.empty(total_T, H, d_v, dtype=dt, device=q.device)
+    if final_state is None and output_final_state:
+        final_state = torch.empty(N, H, d_k, d_v, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(N, total_T, H, d_k, d_v, dt, q.device)
+    host_cu = None
+    if cu_seqlens_host is not None:
+        host_cu = cu_seqlens_host.to(torch.int32).contiguous()
+    flags = (KDA_FLAG_L2NORM_QK if l2norm else 0) | (KDA_FLAG_RECURRENT if recurrent else 0)
+    st = lib().kda_prefill(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(initial_state),
+        _ptr(cu_seqlens), None if host_cu is None else ctypes.c_void_p(host_cu.data_ptr()),
+        N, total_T, H, d_k, d_v, _dtype_code(dt), float(scale), flags,
+        _ptr(o), _ptr(final_state), _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_prefill")
+    if batched:
+        o = o.reshape(B, T, H, d_v)
+    return o, final_state
+
+
+def workspace_status(workspace: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> int:
+    return int(lib().kda_workspace_status(_ptr(workspace), _stream_ptr(stream)))
+
+
+def kda_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: torch.Tensor,
+                    beta: torch.Tensor, A: torch.Tensor, state: torch.Tensor,
+                    slots: Optional[torch.Tensor] = None, scale: float = 1.0,
+                    l2norm: bool = True, o: Optional[torch.Tensor] = None,
+                    stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """One decode token per sequence: q, k, z [B, H, d_k], v [B, H, d_v],
+    beta [B, H]; `state` [pool, H, d_k, d_v] fp32 is updated in place at
+    rows `slots` (default 0..B-1).  Returns o [B, H, d_v]."""
+    B, H, d_k = q.shape
+    d_v = v.shape[-1]
+    dt = q.dtype
+    _check_cuda(q, k, v, z, beta, A, state, slots)
+    if state.dtype != torch.float32:
+        raise TypeError("state must be float32")
+    if slots is not None and slots.dtype != torch.int32:
+        raise TypeError("slots must be int32")
+    if o is None:
+        o = torch.empty(B, H, d_v, dtype=dt, device=q.device)
+    flags = KDA_FLAG_L2NORM_QK if l2norm else 0
+    st = lib().kda_decode_step(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(state), _ptr(slots),
+        state.shape[0], B, H, d_k, d_v, _dtype_code(dt), float(scale), flags, _ptr(o),
+        _stream_ptr(stream))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_decode_step")
+    return o
+
+
+def kda_state_io(op: int, dst: torch.Tensor, src: Optional[torch.Tensor] = None,
+                 slots: Optional[torch.Tensor] = None, n: Optional[int] = None,
+                 stream: Optional[torch.cuda.Stream] = None) -> None:
+    """State movement; shapes [*, H, d_k, d_v] fp32.  n defaults to the
+    number of slots, or to the leading size of src (COPY) / dst (ZERO)."""
+    H, d_k, d_v = dst.shape[-3:]
+    if n is None:
+        if slots is not None:
+            n = slots.numel()
+        elif src is not None:
+            n = src.shape[0]
+        else:
+            n = dst.shape[0]
+    pool = dst.shape[0] if op in (KDA_STATE_ZERO, KDA_STATE_SCATTER) else (
+        src.shape[0] if op == KDA_STATE_GATHER else 0)
+    if op != KDA_STATE_COPY:
+        _check_cuda(dst, src, slots)
+    st = lib().kda_state_io(int(op), _ptr(dst), _ptr(src), _ptr(slots), int(n), int(pool),
+                            H, d_k, d_v, _stream_ptr(stream))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_state_io")

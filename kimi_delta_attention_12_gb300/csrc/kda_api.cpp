@@ -1,0 +1,206 @@
+// kda_api.cpp -- the C ABI declared in include/kda.h: argument validation,
+// kernel selection and launch on the caller's stream.  No allocation, no
+// exceptions across the boundary, no global mutable state.
+#include "../../include/kda.h"
+
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "kda_internal.h"
+
+namespace {
+
+inline bool aligned(const void* p, uintptr_t a) {
+    return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+inline bool supported_dim(int32_t d) { return d == 32 || d == 64 || d == 128; }
+
+inline size_t elem_bytes(kda_dtype dt) { return dt == KDA_F32 ? 4 : 2; }
+
+constexpr uint32_t kKnownFlags = KDA_FLAG_L2NORM_QK | KDA_FLAG_RECURRENT;
+constexpr uint32_t kFlagRecurrent = KDA_FLAG_RECURRENT;
+
+// status word + work counter, then the optional schedule (one int per unit)
+constexpr size_t kWsHeader = 256;
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+extern "C" {
+
+const char* kda_status_string(int status) {
+    switch (status) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+        case KDA_ERR_ALIGNMENT: return "KDA_ERR_ALIGNMENT";
+        case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+        case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
+        default: return "KDA_ERR_UNKNOWN";
+    }
+}
+
+int kda_version(void) { return 100; }
+
+size_t kda_prefill_workspace_bytes(int32_t N, int32_t total_T, int32_t H, int32_t d_k,
+                                   int32_t d_v, kda_dtype dt) {
+    (void)total_T; (void)d_k; (void)d_v; (void)dt;
+    const size_t units = (N > 0 && H > 0) ? (size_t)N * (size_t)H : 0;
+    return kWsHeader + round_up(units * sizeof(int32_t), 256);
+}
+
+int kda_workspace_status(const void* workspace, void* stream) {
+    if (!workspace) {
+        return KDA_ERR_INVALID_ARG;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) {
+        return KDA_ERR_CUDA;
+    }
+    int32_t st = 0;
+    if (cudaMemcpy(&st, workspace, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        return KDA_ERR_CUDA;
+    }
+    return st == 0 ? KDA_OK : KDA_ERR_TIMEOUT;
+}
+
+int kda_prefill(const void* q, const void* k, const void* v, const void* z,
+                const void* beta, const float* A, const float* initial_state,
+                const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                int32_t N, int32_t total_T, int32_t H, int32_t d_k, int32_t d_v,
+                kda_dtype dt, float scale, uint32_t flags,
+                void* o, float* final_state,
+                void* workspace, size_t workspace_bytes, void* stream) {
+    if (dt != KDA_F32 && dt != KDA_BF16) return KDA_ERR_UNSUPPORTED;
+    if (!supported_dim(d_k) || !supported_dim(d_v)) return KDA_ERR_UNSUPPORTED;
+    if (N < 1 || H < 1 || total_T < 0) return KDA_ERR_INVALID_ARG;
+    if ((flags & ~kKnownFlags) != 0) return KDA_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return KDA_ERR_INVALID_ARG;
+    if (!A) return KDA_ERR_INVALID_ARG;
+    if (total_T > 0 && (!q || !k || !v || !z || !beta || !o)) return KDA_ERR_INVALID_ARG;
+    if (!cu_seqlens && total_T % N != 0) return KDA_ERR_INVALID_ARG;
+    if (cu_seqlens_host) {
+        if (cu_seqlens_host[0] != 0 || cu_seqlens_host[N] != total_T) return KDA_ERR_INVALID_ARG;
+        for (int32_t n = 0; n < N; ++n) {
+            if (cu_seqlens_host[n + 1] < cu_seqlens_host[n]) return KDA_ERR_INVALID_ARG;
+        }
+    }
+    if (!workspace || workspace_bytes < kda_prefill_workspace_bytes(N, total_T, H, d_k, d_v, dt)) {
+        return KDA_ERR_WORKSPACE;
+    }
+    const size_t eb = elem_bytes(dt);
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(z, 16) ||
+        !aligned(o, 16) || !aligned(beta, eb) || !aligned(A, 4) ||
+        !aligned(initial_state, 16) || !aligned(final_state, 16) ||
+        !aligned(cu_seqlens, 4) || !aligned(workspace, 256)) {
+        return KDA_ERR_ALIGNMENT;
+    }
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t* ws = static_cast<int32_t*>(workspace);
+    if (cudaMemsetAsync(ws, 0, kWsHeader, s) != cudaSuccess) return KDA_ERR_CUDA;
+
+    const bool use_chunked = kda::kChunkedPrefillBuilt && dt == KDA_BF16 && d_k == 128 && d_v == 128 &&
+                             (flags & kFlagRecurrent) == 0 && total_T > 0;
+    cudaError_t err;
+    if (use_chunked) {
+        kda::ChunkedParams p;
+        memset(&p, 0, sizeof(p));
+        p.q = q; p.k = k; p.v = v; p.z = z; p.beta = beta; p.A = A;
+        p.initial_state = initial_state; p.final_state = final_state;
+        p.cu_seqlens = cu_seqlens; p.o = o;
+        p.status = ws; p.work_counter = ws + 1; p.schedule = nullptr;
+        p.N = N; p.total_T = total_T; p.H = H; p.scale = scale;
+        p.l2norm = (flags & KDA_FLAG_L2NORM_QK) ? 1 : 0;
+        err = kda::launch_chunked_prefill(p, s);
+    } else {
+        kda::RecurrentParams p;
+        memset(&p, 0, sizeof(p));
+        p.q = q; p.k = k; p.v = v; p.z = z; p.beta = beta; p.A = A;
+        p.state_in = initial_state; p.state_out = final_state;
+        p.slots = nullptr; p.cu_seqlens = cu_seqlens; p.o = o;
+        p.rows = N; p.total_T = total_T; p.H = H; p.pool_size = 0;
+        p.scale = scale; p.l2norm = (flags & KDA_FLAG_L2NORM_QK) ? 1 : 0; p.decode = 0;
+        if (total_T == 0 && !final_state) {
+            return KDA_OK;
+        }
+        err = kda::launch_recurrent(p, d_k, d_v, dt == KDA_F32 ? 0 : 1, s);
+    }
+    return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_decode_step(const void* q, const void* k, const void* v, const void* z,
+                    const void* beta, const float* A, float* state,
+                    const int32_t* slots, int32_t pool_size,
+                    int32_t B, int32_t H, int32_t d_k, int32_t d_v,
+                    kda_dtype dt, float scale, uint32_t flags,
+                    void* o, void* stream) {
+    if (dt != KDA_F32 && dt != KDA_BF16) return KDA_ERR_UNSUPPORTED;
+    if (!supported_dim(d_k) || !supported_dim(d_v)) return KDA_ERR_UNSUPPORTED;
+    if (B < 0 || H < 1 || pool_size < 0) return KDA_ERR_INVALID_ARG;
+    if ((flags & ~(uint32_t)KDA_FLAG_L2NORM_QK) != 0) return KDA_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return KDA_ERR_INVALID_ARG;
+    if (B == 0) return KDA_OK;
+    if (!q || !k || !v || !z || !beta || !A || !state || !o) return KDA_ERR_INVALID_ARG;
+    if (!slots && pool_size < B) return KDA_ERR_INVALID_ARG;
+    const size_t eb = elem_bytes(dt);
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(z, 16) ||
+        !aligned(o, 16) || !aligned(beta, eb) || !aligned(A, 4) || !aligned(state, 16) ||
+        !aligned(slots, 4)) {
+        return KDA_ERR_ALIGNMENT;
+    }
+    kda::RecurrentParams p;
+    memset(&p, 0, sizeof(p));
+    p.q = q; p.k = k; p.v = v; p.z = z; p.beta = beta; p.A = A;
+    p.state_in = state; p.state_out = state; p.slots = slots; p.cu_seqlens = nullptr;
+    p.o = o; p.rows = B; p.total_T = B; p.H = H; p.pool_size = pool_size;
+    p.scale = scale; p.l2norm = (flags & KDA_FLAG_L2NORM_QK) ? 1 : 0; p.decode = 1;
+    const cudaError_t err = kda::launch_recurrent(p, d_k, d_v, dt == KDA_F32 ? 0 : 1,
+                                                  static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_state_io(kda_state_op op, float* dst, const float* src,
+                 const int32_t* slots, int32_t n, int32_t pool_size,
+                 int32_t H, int32_t d_k, int32_t d_v, void* stream) {
+    if (!supported_dim(d_k) || !supported_dim(d_v)) return KDA_ERR_UNSUPPORTED;
+    if (n < 0 || H < 1 || pool_size < 0) return KDA_ERR_INVALID_ARG;
+    if (n == 0) return KDA_OK;
+    if (!dst) return KDA_ERR_INVALID_ARG;
+    if (!aligned(dst, 16) || !aligned(src, 16) || !aligned(slots, 4)) return KDA_ERR_ALIGNMENT;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t state_floats = (size_t)H * d_k * d_v;
+    cudaError_t err = cudaSuccess;
+    switch (op) {
+        case KDA_STATE_ZERO:
+            if (slots) {
+                err = kda::launch_state_zero_slots(dst, slots, n, pool_size, state_floats, s);
+            } else {
+                err = cudaMemsetAsync(dst, 0, (size_t)n * state_floats * sizeof(float), s);
+            }
+            break;
+        case KDA_STATE_COPY:
+            if (slots || !src) return KDA_ERR_INVALID_ARG;
+            err = cudaMemcpyAsync(dst, src, (size_t)n * state_floats * sizeof(float),
+                                  cudaMemcpyDefault, s);
+            break;
+        case KDA_STATE_GATHER:
+            if (!slots || !src) return KDA_ERR_INVALID_ARG;
+            err = kda::launch_state_gather(dst, src, slots, n, pool_size, state_floats, s);
+            break;
+        case KDA_STATE_SCATTER:
+            if (!slots || !src) return KDA_ERR_INVALID_ARG;
+            err = kda::launch_state_scatter(dst, src, slots, n, pool_size, state_floats, s);
+            break;
+        default:
+            return KDA_ERR_INVALID_ARG;
+    }
+    return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,83 @@
+// kda_internal.h -- declarations shared by the C-ABI layer (kda_api.cpp) and
+// the CUDA translation units.  Not part of the public interface.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kda {
+
+// Parameters of the fused recurrent kernel (one CTA per (row, head)).
+// Prefill: row = sequence n, tokens cu_seqlens[n] .. cu_seqlens[n+1]-1,
+//          state_in = initial_state (may be null), state_out = final_state
+//          (may be null), slots = null.
+// Decode:  row = batch entry b, one token (index b), state_in = state_out =
+//          the pool, state index = slots ? slots[b] : b.
+struct RecurrentParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* z;
+    const void* beta;
+    const float* A;
+    const float* state_in;
+    float* state_out;
+    const int32_t* slots;
+    const int32_t* cu_seqlens;
+    void* o;
+    int32_t rows;       // N (prefill) or B (decode)
+    int32_t total_T;
+    int32_t H;
+    int32_t pool_size;  // decode only
+    float scale;
+    int32_t l2norm;
+    int32_t decode;
+};
+
+// Launches the recurrent kernel for (d_k, d_v) in {32, 64, 128}^2 and
+// dtype (0 = fp32, 1 = bf16).  Returns a cudaError_t.
+cudaError_t launch_recurrent(const RecurrentParams& p, int d_k, int d_v, int dtype,
+                             cudaStream_t stream);
+
+// State movement kernels (kda_state_io.cu).
+cudaError_t launch_state_zero_slots(float* dst, const int32_t* slots, int32_t n,
+                                    int32_t pool_size, size_t state_floats,
+                                    cudaStream_t stream);
+cudaError_t launch_state_gather(float* dst, const float* src, const int32_t* slots,
+                                int32_t n, int32_t pool_size, size_t state_floats,
+                                cudaStream_t stream);
+cudaError_t launch_state_scatter(float* dst, const float* src, const int32_t* slots,
+                                 int32_t n, int32_t pool_size, size_t state_floats,
+                                 cudaStream_t stream);
+
+// Chunked tensor-core prefill (kda_prefill_sm103.cu): bf16, d_k = d_v = 128.
+struct ChunkedParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* z;
+    const void* beta;
+    const float* A;
+    const float* initial_state;
+    float* final_state;
+    const int32_t* cu_seqlens;   // device, [N+1]; null -> equal split
+    void* o;
+    int32_t* status;             // device status word (workspace)
+    int32_t* work_counter;       // device work counter (workspace)
+    const int32_t* schedule;     // optional device list of unit ids (workspace), or null
+    int32_t N;
+    int32_t total_T;
+    int32_t H;
+    float scale;
+    int32_t l2norm;
+};
+
+// True once the chunked kernel is compiled into the library.
+constexpr bool kChunkedPrefillBuilt = false;
+
+// Workspace layout for the chunked prefill.
+size_t chunked_workspace_bytes(int32_t N, int32_t H);
+cudaError_t launch_chunked_prefill(const ChunkedParams& p, cudaStream_t stream);
+
+}  // namespace kda

@@ -1,0 +1,287 @@
+// kda_recurrent.cu -- fused recurrent KDA kernel for sm_103a.
+//
+// One CTA owns one (row, head) state S (d_k x d_v, fp32) in registers and
+// walks that row's tokens in order.  Per token it fuses everything the
+// recurrence of "Kimi K3 Open Weights: What Is Actually New In Its 2.8
+// Trillion Parameter Architecture", section 1, asks for:
+//   gate     alpha = exp(-5 * sigmoid(e^A z))           (gate equation)
+//   decay    S'    = Diag(alpha) S
+//   erase    u     = beta (v - S'^T k_hat)
+//   write    S     = S' + k_hat u^T                     (delta-rule update)
+//   read     o     = S^T q_hat = S'^T q_hat + (k_hat . q_hat) u
+// q_hat/k_hat are the L2-normalised q/k (the section's "Q/K normalization").
+//
+// Decode (the section's "fused recurrent kernel" with the state kept
+// persistent) is the case of one token per row: the state streams from HBM
+// once, is updated in registers and streams back once, with 128-bit loads and
+// stores that are coalesced across each warp (a warp covers whole state rows).
+// The same kernel serves as the exact fp32 prefill path (any head dim, fp32
+// inputs).
+//
+// Thread layout: a state row of d_v floats is covered by LPR = d_v/4 lanes
+// holding one float4 each; a warp covers RPW = 32/LPR rows per pass; the CTA
+// covers RSTEP = 8*RPW rows per pass and each thread keeps RPT = d_k/RSTEP
+// float4 of the state.  Column sums over the d_k rows (S'^T k, S'^T q) are
+// reduced with warp shuffles inside a warp and through shared memory across
+// the 8 warps.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr float kGmin = -5.0f;
+constexpr float kNormEps = 1e-6f;
+
+__device__ __forceinline__ float load_elem(const float* p, size_t i) { return __ldg(p + i); }
+__device__ __forceinline__ float load_elem(const __nv_bfloat16* p, size_t i) {
+    return __bfloat162float(p[i]);
+}
+__device__ __forceinline__ void store_elem(float* p, size_t i, float x) { p[i] = x; }
+__device__ __forceinline__ void store_elem(__nv_bfloat16* p, size_t i, float x) {
+    p[i] = __float2bfloat16_rn(x);
+}
+
+// sigmoid on the branch that cannot overflow
+__device__ __forceinline__ float sigmoid_f(float x) {
+    if (x >= 0.0f) {
+        return 1.0f / (1.0f + expf(-x));
+    }
+    const float e = expf(x);
+    return e / (1.0f + e);
+}
+
+template <int DK, int DV, typename T>
+__global__ void __launch_bounds__(kThreads)
+kda_recurrent_kernel(const RecurrentParams p) {
+    constexpr int LPR = DV / 4;
+    constexpr int RPW = 32 / LPR;
+    constexpr int RSTEP = kWarps * RPW;
+    constexpr int RPT = DK / RSTEP;
+    static_assert(RPT >= 1 && RPT * RSTEP == DK, "bad state tiling");
+    static_assert(DK + DV <= kThreads, "stage-1 loaders need DK + DV threads");
+
+    __shared__ float s_q[DK];
+    __shared__ float s_k[DK];
+    __shared__ float s_a[DK];
+    __shared__ float s_v[DV];
+    __shared__ float s_u[DV];
+    __shared__ float s_red[kWarps][2][DV];
+    __shared__ float s_nrm[DK / 32][3];
+    __shared__ float s_beta;
+
+    const int tid = threadIdx.x;
+    const int w = tid >> 5;
+    const int lane = tid & 31;
+    const int cg = lane % LPR;
+    const int rs = lane / LPR;
+    const int h = blockIdx.x % p.H;
+    const int row = blockIdx.x / p.H;
+    const int H = p.H;
+
+    const T* q = static_cast<const T*>(p.q);
+    const T* k = static_cast<const T*>(p.k);
+    const T* v = static_cast<const T*>(p.v);
+    const T* z = static_cast<const T*>(p.z);
+    const T* beta = static_cast<const T*>(p.beta);
+    T* o = static_cast<T*>(p.o);
+
+    int64_t bos, eos;
+    int64_t sidx = row;  // index of this row's state in state_in / state_out
+    bool valid = true;
+    if (p.decode) {
+        bos = row;
+        eos = row + 1;
+        if (p.slots) {
+            sidx = p.slots[row];
+        }
+        valid = sidx >= 0 && sidx < p.pool_size;
+    } else if (p.cu_seqlens) {
+        bos = p.cu_seqlens[row];
+        eos = p.cu_seqlens[row + 1];
+    } else {
+        const int64_t len = p.total_T / p.rows;
+        bos = (int64_t)row * len;
+        eos = bos + len;
+    }
+    if (!valid) {
+        // Decode row with an out-of-range slot: state untouched, o = NaN.
+        for (int j = tid; j < DV; j += kThreads) {
+            store_elem(o, ((size_t)bos * H + h) * DV + j, __int_as_float(0x7fc00000));
+        }
+        return;
+    }
+
+    // ---- state load: 128-bit, each warp pass reads whole rows ----
+    float4 S[RPT];
+    const size_t soff = ((size_t)sidx * H + h) * DK * DV;
+    if (p.state_in) {
+        const float4* sp = reinterpret_cast<const float4*>(p.state_in + soff);
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            const int i = r * RSTEP + w * RPW + rs;
+            S[r] = __ldcs(sp + (i * DV) / 4 + cg);
+        }
+    } else {
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            S[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+
+    const float eA = expf(p.A[h]);
+    const float scale = p.scale;
+
+    for (int64_t t = bos; t < eos; ++t) {
+        // ---- stage 1: token inputs, gate, norm partial sums ----
+        const size_t rk = ((size_t)t * H + h) * DK;
+        if (tid < DK) {
+            const float qv = load_elem(q, rk + tid);
+            const float kv = load_elem(k, rk + tid);
+            const float zv = load_elem(z, rk + tid);
+            s_q[tid] = qv;
+            s_k[tid] = kv;
+            s_a[tid] = expf(kGmin * sigmoid_f(eA * zv));
+            float sq = qv * qv, sk = kv * kv, sqk = qv * kv;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                sq += __shfl_xor_sync(0xffffffffu, sq, off);
+                sk += __shfl_xor_sync(0xffffffffu, sk, off);
+                sqk += __shfl_xor_sync(0xffffffffu, sqk, off);
+            }
+            if (lane == 0) {
+                s_nrm[w][0] = sq;
+                s_nrm[w][1] = sk;
+                s_nrm[w][2] = sqk;
+            }
+        } else if (tid < DK + DV) {
+            const int j = tid - DK;
+            s_v[j] = load_elem(v, ((size_t)t * H + h) * DV + j);
+            if (j == 0) {
+                s_beta = load_elem(beta, (size_t)t * H + h);
+            }
+        }
+        __syncthreads();
+
+        float sq = 0.f, sk = 0.f, sqk = 0.f;
+#pragma unroll
+        for (int i = 0; i < DK / 32; ++i) {
+            sq += s_nrm[i][0];
+            sk += s_nrm[i][1];
+            sqk += s_nrm[i][2];
+        }
+        const float inv_q = p.l2norm ? rsqrtf(sq + kNormEps) : 1.0f;
+        const float inv_k = p.l2norm ? rsqrtf(sk + kNormEps) : 1.0f;
+        const float qscale = inv_q * scale;
+
+        // ---- stage 2: decay, and the two column sums of S' ----
+        float4 ak = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 aq = make_float4(0.f, 0.f, 0.f, 0.f);
+        float kreg[RPT];
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            const int i = r * RSTEP + w * RPW + rs;
+            const float a = s_a[i];
+            const float kk = s_k[i];
+            const float qq = s_q[i];
+            kreg[r] = kk * inv_k;
+            S[r].x *= a; S[r].y *= a; S[r].z *= a; S[r].w *= a;
+            ak.x += kk * S[r].x; ak.y += kk * S[r].y; ak.z += kk * S[r].z; ak.w += kk * S[r].w;
+            aq.x += qq * S[r].x; aq.y += qq * S[r].y; aq.z += qq * S[r].z; aq.w += qq * S[r].w;
+        }
+#pragma unroll
+        for (int off = LPR; off < 32; off <<= 1) {
+            ak.x += __shfl_xor_sync(0xffffffffu, ak.x, off);
+            ak.y += __shfl_xor_sync(0xffffffffu, ak.y, off);
+            ak.z += __shfl_xor_sync(0xffffffffu, ak.z, off);
+            ak.w += __shfl_xor_sync(0xffffffffu, ak.w, off);
+            aq.x += __shfl_xor_sync(0xffffffffu, aq.x, off);
+            aq.y += __shfl_xor_sync(0xffffffffu, aq.y, off);
+            aq.z += __shfl_xor_sync(0xffffffffu, aq.z, off);
+            aq.w += __shfl_xor_sync(0xffffffffu, aq.w, off);
+        }
+        if (rs == 0) {
+            *reinterpret_cast<float4*>(&s_red[w][0][4 * cg]) = ak;
+            *reinterpret_cast<float4*>(&s_red[w][1][4 * cg]) = aq;
+        }
+        __syncthreads();
+
+        // ---- stage 3: u and o per value column ----
+        if (tid < DV) {
+            float rkj = 0.f, rqj = 0.f;
+#pragma unroll
+            for (int ww = 0; ww < kWarps; ++ww) {
+                rkj += s_red[ww][0][tid];
+                rqj += s_red[ww][1][tid];
+            }
+            rkj *= inv_k;
+            rqj *= qscale;
+            const float u = s_beta * (s_v[tid] - rkj);
+            s_u[tid] = u;
+            const float dot = sqk * inv_k * qscale;  // k_hat . q_hat
+            store_elem(o, ((size_t)t * H + h) * DV + tid, rqj + dot * u);
+        }
+        __syncthreads();
+
+        // ---- stage 4: rank-1 write ----
+        const float4 u4 = *reinterpret_cast<const float4*>(&s_u[4 * cg]);
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            const float kk = kreg[r];
+            S[r].x += kk * u4.x; S[r].y += kk * u4.y; S[r].z += kk * u4.z; S[r].w += kk * u4.w;
+        }
+    }
+
+    if (p.state_out) {
+        float4* sp = reinterpret_cast<float4*>(p.state_out + soff);
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            const int i = r * RSTEP + w * RPW + rs;
+            __stcs(sp + (i * DV) / 4 + cg, S[r]);
+        }
+    }
+}
+
+template <int DK, int DV>
+cudaError_t launch_dims(const RecurrentParams& p, int dtype, cudaStream_t stream) {
+    const dim3 grid((unsigned)((int64_t)p.rows * p.H));
+    if (grid.x == 0) {
+        return cudaSuccess;
+    }
+    if (dtype == 0) {
+        kda_recurrent_kernel<DK, DV, float><<<grid, kThreads, 0, stream>>>(p);
+    } else {
+        kda_recurrent_kernel<DK, DV, __nv_bfloat16><<<grid, kThreads, 0, stream>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+template <int DK>
+cudaError_t launch_dk(const RecurrentParams& p, int d_v, int dtype, cudaStream_t stream) {
+    switch (d_v) {
+        case 32: return launch_dims<DK, 32>(p, dtype, stream);
+        case 64: return launch_dims<DK, 64>(p, dtype, stream);
+        case 128: return launch_dims<DK, 128>(p, dtype, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_recurrent(const RecurrentParams& p, int d_k, int d_v, int dtype,
+                             cudaStream_t stream) {
+    switch (d_k) {
+        case 32: return launch_dk<32>(p, d_v, dtype, stream);
+        case 64: return launch_dk<64>(p, d_v, dtype, stream);
+        case 128: return launch_dk<128>(p, d_v, dtype, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace kda

@@ -1,0 +1,174 @@
+"""Host-side checks of the C ABI (no GPU needed, nothing is launched).
+
+The library must load, export every symbol include/kda.h declares, and turn
+every host-detectable argument error into its status code before touching
+the device.  Fake device pointers are plain aligned integers: validation
+never dereferences device memory, and every call below fails validation.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+import kimi_delta_attention_12_gb300 as kda
+
+
+@pytest.fixture(scope="module")
+def L():
+    from kimi_delta_attention_12_gb300 import build
+    build.build()
+    return kda.lib()
+
+
+def _declared_symbols():
+    text = open(os.path.join(ROOT, "include", "kda.h")).read()
+    return sorted(set(re.findall(r"KDA_API\s+[\w\s\*]+?\b(kda_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(L):
+    declared = _declared_symbols()
+    assert set(declared) == set(kda.EXPORTED_SYMBOLS), declared
+    for name in declared:
+        assert hasattr(L, name), name
+        assert ctypes.cast(getattr(L, name), ctypes.c_void_p).value
+
+
+def test_status_strings(L):
+    for code, name in [(0, "KDA_OK"), (-1, "KDA_ERR_INVALID_ARG"), (-2, "KDA_ERR_UNSUPPORTED"),
+                       (-3, "KDA_ERR_ALIGNMENT"), (-4, "KDA_ERR_WORKSPACE"),
+                       (-5, "KDA_ERR_CUDA"), (-6, "KDA_ERR_TIMEOUT"), (7, "KDA_ERR_UNKNOWN")]:
+        assert kda.status_string(code) == name
+    assert L.kda_version() >= 100
+
+
+def test_workspace_bytes(L):
+    a = L.kda_prefill_workspace_bytes(1, 4096, 32, 128, 128, kda.KDA_BF16)
+    b = L.kda_prefill_workspace_bytes(16, 100000, 64, 128, 128, kda.KDA_BF16)
+    assert 0 < a < b
+    assert a % 256 == 0 and b % 256 == 0
+    assert b >= 16 * 64 * 4
+
+
+BASE = 0x7f0000000000  # a 256-byte aligned fake device address
+WS_BYTES = 1 << 20
+
+
+def _prefill_args(**over):
+    a = dict(q=BASE, k=BASE + 0x100000, v=BASE + 0x200000, z=BASE + 0x300000,
+             beta=BASE + 0x400000, A=BASE + 0x500000, S0=None, cu=None, cu_host=None,
+             N=1, T=64, H=2, dk=32, dv=32, dt=kda.KDA_F32, scale=1.0, flags=1,
+             o=BASE + 0x600000, Sf=None, ws=BASE + 0x700000, ws_bytes=WS_BYTES)
+    a.update(over)
+    return a
+
+
+def _call_prefill(L, a):
+    vp = ctypes.c_void_p
+    return L.kda_prefill(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["z"]), vp(a["beta"]),
+                         vp(a["A"]), vp(a["S0"]), vp(a["cu"]), a["cu_host"],
+                         a["N"], a["T"], a["H"], a["dk"], a["dv"], a["dt"], a["scale"],
+                         a["flags"], vp(a["o"]), vp(a["Sf"]), vp(a["ws"]), a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(dk=48), kda.KDA_ERR_UNSUPPORTED),
+    (dict(dv=256), kda.KDA_ERR_UNSUPPORTED),
+    (dict(dt=7), kda.KDA_ERR_UNSUPPORTED),
+    (dict(N=0), kda.KDA_ERR_INVALID_ARG),
+    (dict(H=0), kda.KDA_ERR_INVALID_ARG),
+    (dict(T=-1), kda.KDA_ERR_INVALID_ARG),
+    (dict(q=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(o=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(A=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(flags=8), kda.KDA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), kda.KDA_ERR_INVALID_ARG),
+    (dict(N=3, T=64), kda.KDA_ERR_INVALID_ARG),      # 64 % 3 != 0 without cu_seqlens
+    (dict(ws=None), kda.KDA_ERR_WORKSPACE),
+    (dict(ws_bytes=16), kda.KDA_ERR_WORKSPACE),
+    (dict(q=BASE + 8), kda.KDA_ERR_ALIGNMENT),
+    (dict(o=BASE + 0x600004), kda.KDA_ERR_ALIGNMENT),
+    (dict(Sf=BASE + 0x800008), kda.KDA_ERR_ALIGNMENT),
+    (dict(beta=BASE + 0x400002), kda.KDA_ERR_ALIGNMENT),   # fp32 beta must be 4-aligned
+    (dict(ws=BASE + 0x700010), kda.KDA_ERR_ALIGNMENT),
+])
+def test_prefill_validation(L, over, expect):
+    assert _call_prefill(L, _prefill_args(**over)) == expect
+
+
+@pytest.mark.parametrize("cu,expect", [
+    ([1, 64], kda.KDA_ERR_INVALID_ARG),        # must start at 0
+    ([0, 63], kda.KDA_ERR_INVALID_ARG),        # must end at total_T
+    ([0, 40, 30, 64], kda.KDA_ERR_INVALID_ARG),  # non-decreasing
+])
+def test_prefill_host_cu_seqlens_validation(L, cu, expect):
+    arr = (ctypes.c_int32 * len(cu))(*cu)
+    a = _prefill_args(N=len(cu) - 1, cu=BASE + 0x900000, cu_host=arr)
+    assert _call_prefill(L, a) == expect
+
+
+def _call_decode(L, **over):
+    a = dict(q=BASE, k=BASE + 0x100000, v=BASE + 0x200000, z=BASE + 0x300000,
+             beta=BASE + 0x400000, A=BASE + 0x500000, state=BASE + 0x600000, slots=None,
+             pool=4, B=4, H=2, dk=128, dv=128, dt=kda.KDA_BF16, scale=1.0, flags=1,
+             o=BASE + 0x700000)
+    a.update(over)
+    vp = ctypes.c_void_p
+    return L.kda_decode_step(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["z"]), vp(a["beta"]),
+                             vp(a["A"]), vp(a["state"]), vp(a["slots"]), a["pool"], a["B"],
+                             a["H"], a["dk"], a["dv"], a["dt"], a["scale"], a["flags"],
+                             vp(a["o"]), None)
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(dk=16), kda.KDA_ERR_UNSUPPORTED),
+    (dict(dt=3), kda.KDA_ERR_UNSUPPORTED),
+    (dict(H=0), kda.KDA_ERR_INVALID_ARG),
+    (dict(B=-1), kda.KDA_ERR_INVALID_ARG),
+    (dict(pool=2), kda.KDA_ERR_INVALID_ARG),    # identity slots need pool >= B
+    (dict(state=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(flags=2), kda.KDA_ERR_INVALID_ARG),   # the recurrent flag is prefill-only
+    (dict(k=BASE + 0x100004), kda.KDA_ERR_ALIGNMENT),
+    (dict(state=BASE + 0x600008), kda.KDA_ERR_ALIGNMENT),
+    (dict(slots=BASE + 0x800002), kda.KDA_ERR_ALIGNMENT),
+    (dict(B=0), kda.KDA_OK),                    # nothing to do, nothing launched
+])
+def test_decode_validation(L, over, expect):
+    assert _call_decode(L, **over) == expect
+
+
+def test_state_io_validation(L):
+    vp = ctypes.c_void_p
+    f = L.kda_state_io
+    assert f(kda.KDA_STATE_ZERO, vp(BASE), None, None, 1, 1, 2, 100, 128, None) == kda.KDA_ERR_UNSUPPORTED
+    assert f(kda.KDA_STATE_GATHER, vp(BASE), vp(BASE + 0x1000), None, 1, 1, 2, 128, 128, None) == kda.KDA_ERR_INVALID_ARG
+    assert f(kda.KDA_STATE_SCATTER, vp(BASE), None, vp(BASE + 0x2000), 1, 1, 2, 128, 128, None) == kda.KDA_ERR_INVALID_ARG
+    assert f(kda.KDA_STATE_COPY, vp(BASE), vp(BASE + 0x1000), vp(BASE + 0x2000), 1, 1, 2, 128, 128, None) == kda.KDA_ERR_INVALID_ARG
+    assert f(kda.KDA_STATE_COPY, vp(BASE + 4), vp(BASE + 0x1000), None, 1, 1, 2, 128, 128, None) == kda.KDA_ERR_ALIGNMENT
+    assert f(9, vp(BASE), vp(BASE + 0x1000), None, 1, 1, 2, 128, 128, None) == kda.KDA_ERR_INVALID_ARG
+    assert f(kda.KDA_STATE_ZERO, vp(BASE), None, None, 0, 0, 2, 128, 128, None) == kda.KDA_OK
+
+
+def test_product_path_has_no_cpu_fallback():
+    """The binding refuses CPU tensors instead of computing on the host."""
+    import torch
+    q = torch.zeros(4, 1, 32)
+    with pytest.raises((ValueError, RuntimeError)):
+        kda.kda_prefill(q, q, q, q, torch.zeros(4, 1), torch.zeros(1))
+
+
+def test_package_does_not_import_oracle():
+    """The product package never imports the test oracle."""
+    import ast
+    pkg = os.path.join(ROOT, "kimi_delta_attention_12_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith(".py"):
+                tree = ast.parse(open(os.path.join(dirpath, f)).read())
+                for node in ast.walk(tree):
+                    if isinstance(node, ast.Import):
+                        assert all(not a.name.startswith("oracle") for a in node.names), f
+                    if isinstance(node, ast.ImportFrom):
+                        assert not (node.module or "").startswith("oracle"), f

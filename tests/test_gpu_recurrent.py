@@ -1,0 +1,230 @@
+"""GPU parity of the fused recurrent kernel (decode and the fp32 prefill path)
+and of the state I/O kernels, through the C ABI, against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import kimi_delta_attention_12_gb300 as kda
+from kimi_delta_attention_12_gb300 import inputs
+from metrics import F32_TOL, max_rel, max_rel_stored
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    kda.lib()
+
+
+def _run_prefill(x, **kw):
+    xd = x.to(DEV)
+    o, S = kda.kda_prefill(xd.q, xd.k, xd.v, xd.z, xd.beta, xd.A, xd.initial_state,
+                           xd.cu_seqlens, **kw)
+    torch.cuda.synchronize()
+    return o, S
+
+
+def test_tiny_fp32_workload(oracle_mod):
+    """B=1, H=2, T=64, d=32, fp32, zero state: max relative error <= 1e-4."""
+    x = inputs.make_workload_inputs(inputs.TINY_F32, seed=0)
+    o, S = _run_prefill(x)
+    o_ref, S_ref, _ = oracle_mod.kda_reference(x.q, x.k, x.v, x.z, x.beta, x.A, None,
+                                               x.cu_seqlens)
+    assert max_rel(o, o_ref) <= F32_TOL
+    assert max_rel(S, S_ref) <= F32_TOL
+
+
+@pytest.mark.parametrize("dk,dv", [(32, 32), (32, 128), (64, 64), (64, 32), (128, 64),
+                                   (128, 128)])
+def test_recurrent_prefill_dims_fp32(oracle_mod, dk, dv):
+    x = inputs.make_prefill_inputs([37, 0, 90, 1], 3, dk, dv, torch.float32, seed=dk + dv,
+                                   nonzero_state=True)
+    o, S = _run_prefill(x, cu_seqlens_host=x.cu_seqlens)
+    o_ref, S_ref, _ = oracle_mod.kda_reference(x.q, x.k, x.v, x.z, x.beta, x.A,
+                                               x.initial_state, x.cu_seqlens)
+    assert max_rel(o, o_ref) <= F32_TOL
+    assert max_rel(S, S_ref) <= F32_TOL
+    # the zero-length sequence returns its initial state exactly
+    assert torch.equal(S[1].cpu(), x.initial_state[1])
+
+
+def test_recurrent_prefill_bf16_inputs(oracle_mod):
+    x = inputs.make_prefill_inputs([200, 57], 4, 128, 128, torch.bfloat16, seed=3,
+                                   nonzero_state=True)
+    o, S = _run_prefill(x, recurrent=True)
+    o_ref, S_ref, _ = oracle_mod.kda_reference(x.q, x.k, x.v, x.z, x.beta, x.A,
+                                               x.initial_state, x.cu_seqlens)
+    assert max_rel_stored(o, o_ref) <= F32_TOL
+    assert max_rel(S, S_ref) <= F32_TOL
+
+
+def test_prefill_scale_and_no_l2norm(oracle_mod):
+    x = inputs.make_prefill_inputs([50], 2, 64, 64, torch.float32, seed=4, nonzero_state=True)
+    for scale, l2 in [(0.125, True), (1.0, False)]:
+        o, S = _run_prefill(x, scale=scale, l2norm=l2)
+        o_ref, S_ref, _ = oracle_mod.kda_reference(x.q, x.k, x.v, x.z, x.beta, x.A,
+                                                   x.initial_state, x.cu_seqlens,
+                                                   scale=scale, l2norm=l2)
+        assert max_rel(o, o_ref) <= F32_TOL
+        assert max_rel(S, S_ref) <= F32_TOL
+
+
+def test_prefill_equals_decode_steps():
+    """prefill(T) == T consecutive decode steps (GPU against GPU, fp32)."""
+    T, H, d = 24, 3, 64
+    x = inputs.make_prefill_inputs([T], H, d, d, torch.float32, seed=5, nonzero_state=True)
+    o_p, S_p = _run_prefill(x)
+    xd = x.to(DEV)
+    state = xd.initial_state.clone()
+    outs = []
+    for t in range(T):
+        sl = slice(t, t + 1)
+        outs.append(kda.kda_decode_step(xd.q[sl], xd.k[sl], xd.v[sl], xd.z[sl], xd.beta[sl],
+                                        xd.A, state))
+    torch.cuda.synchronize()
+    o_d = torch.cat(outs)
+    assert max_rel(o_d, o_p) <= 1e-6
+    assert max_rel(state, S_p) <= 1e-6
+
+
+def test_split_prefill_handoff():
+    """prefill(T1) -> final state -> prefill(T2) equals prefill(T1 + T2)."""
+    H, d = 2, 128
+    x = inputs.make_prefill_inputs([150], H, d, d, torch.float32, seed=6, nonzero_state=True)
+    xd = x.to(DEV)
+    o_full, S_full = kda.kda_prefill(xd.q, xd.k, xd.v, xd.z, xd.beta, xd.A, xd.initial_state)
+    a, b = slice(0, 61), slice(61, 150)
+    o_a, S_a = kda.kda_prefill(xd.q[a], xd.k[a], xd.v[a], xd.z[a], xd.beta[a], xd.A,
+                               xd.initial_state)
+    o_b, S_b = kda.kda_prefill(xd.q[b], xd.k[b], xd.v[b], xd.z[b], xd.beta[b], xd.A, S_a)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat([o_a, o_b]), o_full)
+    assert torch.equal(S_b, S_full)
+
+
+def test_prefill_in_place_state():
+    """final_state may alias initial_state."""
+    x = inputs.make_prefill_inputs([40, 40], 2, 32, 32, torch.float32, seed=7,
+                                   nonzero_state=True)
+    xd = x.to(DEV)
+    _, S_ref = kda.kda_prefill(xd.q, xd.k, xd.v, xd.z, xd.beta, xd.A, xd.initial_state,
+                               xd.cu_seqlens)
+    S = xd.initial_state.clone()
+    kda.kda_prefill(xd.q, xd.k, xd.v, xd.z, xd.beta, xd.A, S, xd.cu_seqlens, final_state=S)
+    torch.cuda.synchronize()
+    assert torch.equal(S, S_ref)
+
+
+# ------------------------------------------------------------------ decode
+def _decode_oracle(oracle_mod, st, A, S0):
+    B, H, _ = st.q.shape
+    o, S, _ = oracle_mod.kda_reference(st.q.unsqueeze(1), st.k.unsqueeze(1), st.v.unsqueeze(1),
+                                       st.z.unsqueeze(1), st.beta.unsqueeze(1), A, S0)
+    return o.reshape(B, H, -1), S
+
+
+def test_decode_workload_two_steps(oracle_mod):
+    """B=256, H=96, d=128, fp32 state ~N(0,0.02) resident on the device, bf16
+    inputs: two consecutive steps on the device state, against the oracle run
+    over the same two tokens per sequence; every state and output compared."""
+    w = inputs.DECODE_256
+    A, S0 = inputs.make_decode_state(w.B, w.H, w.d_k, w.d_v, seed=0)
+    state = S0.to(DEV)
+    Ad = A.to(DEV)
+    steps = [inputs.make_decode_step(w.B, w.H, w.d_k, w.d_v, w.dtype, seed=0, step=s)
+             for s in range(2)]
+    outs = []
+    for st in steps:
+        sd = st.to(DEV)
+        outs.append(kda.kda_decode_step(sd.q, sd.k, sd.v, sd.z, sd.beta, Ad, state))
+    torch.cuda.synchronize()
+    cat = lambda name: torch.stack([getattr(s, name) for s in steps], dim=1)  # [B, 2, ...]
+    o_ref, S_ref, _ = oracle_mod.kda_reference(cat("q"), cat("k"), cat("v"), cat("z"),
+                                               cat("beta"), A, S0)
+    o_ref = o_ref.reshape(w.B, 2, w.H, w.d_v)
+    for s in range(2):
+        assert max_rel_stored(outs[s], o_ref[:, s]) <= F32_TOL
+    assert max_rel(state, S_ref) <= F32_TOL
+
+
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 32), (32, 128)])
+def test_decode_fp32_inputs(oracle_mod, dk, dv):
+    A, S0 = inputs.make_decode_state(8, 5, dk, dv, seed=1)
+    st = inputs.make_decode_step(8, 5, dk, dv, torch.float32, seed=1, step=0)
+    state = S0.to(DEV)
+    sd = st.to(DEV)
+    o = kda.kda_decode_step(sd.q, sd.k, sd.v, sd.z, sd.beta, A.to(DEV), state, scale=0.5)
+    torch.cuda.synchronize()
+    o_ref, S_ref, _ = oracle_mod.kda_reference(st.q.unsqueeze(1), st.k.unsqueeze(1),
+                                               st.v.unsqueeze(1), st.z.unsqueeze(1),
+                                               st.beta.unsqueeze(1), A, S0, scale=0.5)
+    assert max_rel(o, o_ref.reshape(8, 5, dv)) <= F32_TOL
+    assert max_rel(state, S_ref) <= F32_TOL
+
+
+def test_decode_slots_and_out_of_range(oracle_mod):
+    B, H, d, pool = 4, 2, 64, 7
+    A, P = inputs.make_decode_state(pool, H, d, d, seed=2)
+    st = inputs.make_decode_step(B, H, d, d, torch.float32, seed=2)
+    slots = torch.tensor([5, 0, 99, 3], dtype=torch.int32)
+    pool_d = P.to(DEV)
+    sd = st.to(DEV)
+    o = kda.kda_decode_step(sd.q, sd.k, sd.v, sd.z, sd.beta, A.to(DEV), pool_d,
+                            slots=slots.to(DEV))
+    torch.cuda.synchronize()
+    good = [0, 1, 3]
+    S0 = P[slots[good].long()]
+    o_ref, S_ref, _ = oracle_mod.kda_reference(
+        st.q[good].unsqueeze(1), st.k[good].unsqueeze(1), st.v[good].unsqueeze(1),
+        st.z[good].unsqueeze(1), st.beta[good].unsqueeze(1), A, S0)
+    assert max_rel(o[good], o_ref.reshape(3, H, d)) <= F32_TOL
+    assert torch.isnan(o[2]).all()
+    after = pool_d.cpu()
+    for i, b in enumerate(good):
+        assert max_rel(after[slots[b]], S_ref[i]) <= F32_TOL
+    untouched = [s for s in range(pool) if s not in (5, 0, 3)]
+    assert torch.equal(after[untouched], P[untouched])
+
+
+def test_decode_is_deterministic():
+    A, S0 = inputs.make_decode_state(16, 4, 128, 128, seed=3)
+    st = inputs.make_decode_step(16, 4, 128, 128, torch.bfloat16, seed=3).to(DEV)
+    outs = []
+    for _ in range(2):
+        state = S0.to(DEV)
+        o = kda.kda_decode_step(st.q, st.k, st.v, st.z, st.beta, A.to(DEV), state)
+        outs.append((o.clone(), state.clone()))
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+# ---------------------------------------------------------------- state io
+def test_state_io_roundtrip():
+    H, d, pool = 3, 32, 6
+    g = torch.Generator().manual_seed(0)
+    host = torch.randn(4, H, d, d, generator=g).pin_memory()
+    dev = torch.empty(4, H, d, d, device=DEV)
+    kda.kda_state_io(kda.KDA_STATE_COPY, dev, host)            # host -> device
+    P = torch.full((pool, H, d, d), 7.0, device=DEV)
+    slots = torch.tensor([4, 1, 0, 5], dtype=torch.int32, device=DEV)
+    kda.kda_state_io(kda.KDA_STATE_SCATTER, P, dev, slots)      # batch -> pool
+    back = torch.empty(4, H, d, d, device=DEV)
+    kda.kda_state_io(kda.KDA_STATE_GATHER, back, P, slots)      # pool -> batch
+    out = torch.empty(4, H, d, d).pin_memory()
+    kda.kda_state_io(kda.KDA_STATE_COPY, out, back)             # device -> host
+    torch.cuda.synchronize()
+    assert torch.equal(out, host)
+    Pc = P.cpu()
+    assert torch.equal(Pc[[4, 1, 0, 5]], host)
+    assert torch.all(Pc[[2, 3]] == 7.0)
+    kda.kda_state_io(kda.KDA_STATE_ZERO, P, slots=slots[:2])
+    torch.cuda.synchronize()
+    Pc = P.cpu()
+    assert torch.all(Pc[[4, 1]] == 0) and torch.equal(Pc[[0, 5]], host[[2, 3]])
+    kda.kda_state_io(kda.KDA_STATE_ZERO, P)
+    torch.cuda.synchronize()
+    assert torch.all(P == 0)
