@@ -205,6 +205,8 @@ def kda_arm(args, world, rank, local, pg):
     kda.lib()
     stream = torch.cuda.current_stream()
     peaks = _peaks()
+    if args.only == "decode":
+        return decode_only(args, rank, local, dev, stream, peaks)
     P = PREFILL_SHAPE
     B, H, T, d = P["B"], P["H"], P["T"], P["d"]
     byts, flops = prefill_algorithmic(B, H, T, d)
@@ -263,7 +265,66 @@ def kda_arm(args, world, rank, local, pg):
     value = world * B * T / (ms_per_step / 1e3)
     achieved_gbs = byts / (kernel_ms / 1e3) / 1e9
     achieved_tf = flops / (kernel_ms / 1e3) / 1e12
+    if args.only == "prefill":
+        if rank == 0:
+            print(json.dumps({"only": "prefill", "value": value, "unit": "tokens/s",
+                              "kernel_ms": kernel_ms, "achieved_gbs": achieved_gbs,
+                              "tensor_tflops": achieved_tf}), flush=True)
+        return
 
+    return finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops, nsets,
+                  set_bytes, x_host, o, S, ws, cu_host, value, ms_per_step, kernel_ms,
+                  achieved_gbs, achieved_tf, clk, launches_per_step, pg)
+
+
+def run_decode(dev, rank, local, stream):
+    """64 consecutive decode steps on a resident B=256, H=96, d=128 fp32 state."""
+    import torch
+    import kimi_delta_attention_12_gb300 as kda
+    D = DECODE_SHAPE
+    g = torch.Generator(device=dev).manual_seed(1000 + rank)
+    Bd, Hd, dd = D["B"], D["H"], D["d"]
+    state = 0.02 * torch.randn(Bd, Hd, dd, dd, device=dev, generator=g)
+    Adec = 0.5 * torch.randn(Hd, device=dev, generator=g)
+    unit = lambda t: t / t.norm(dim=-1, keepdim=True)
+    dsteps = []
+    for s in range(D["steps"]):
+        dsteps.append((unit(torch.randn(Bd, Hd, dd, device=dev, generator=g)).bfloat16(),
+                       unit(torch.randn(Bd, Hd, dd, device=dev, generator=g)).bfloat16(),
+                       torch.randn(Bd, Hd, dd, device=dev, generator=g).bfloat16(),
+                       torch.randn(Bd, Hd, dd, device=dev, generator=g).bfloat16(),
+                       torch.sigmoid(torch.randn(Bd, Hd, device=dev, generator=g)).bfloat16()))
+    od = torch.empty(Bd, Hd, dd, dtype=torch.bfloat16, device=dev)
+    for s in range(3):
+        q_, k_, v_, z_, b_ = dsteps[s]
+        kda.kda_decode_step(q_, k_, v_, z_, b_, Adec, state, o=od)
+    torch.cuda.synchronize()
+    dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(D["steps"])]
+    with ClockSampler(local) as dclk:
+        for s in range(D["steps"]):
+            q_, k_, v_, z_, b_ = dsteps[s]
+            dev_ev[s][0].record(stream)
+            kda.kda_decode_step(q_, k_, v_, z_, b_, Adec, state, o=od)
+            dev_ev[s][1].record(stream)
+        torch.cuda.synchronize()
+    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dev_ev)
+    dec_bytes = decode_algorithmic(Bd, Hd, dd)
+    return dec_ms, dec_bytes, dec_bytes / (dec_ms / 1e3) / 1e9, dclk.summary()
+
+
+def decode_only(args, rank, local, dev, stream, peaks):
+    dec_ms, dec_bytes, dec_gbs, clk = run_decode(dev, rank, local, stream)
+    if rank == 0:
+        print(json.dumps({"only": "decode", "value": dec_gbs, "unit": "GB/s", "ms_per_step": dec_ms,
+                          "frac": dec_gbs / peaks["hbm_gbs"], "clocks": clk}), flush=True)
+
+
+def finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops, nsets,
+           set_bytes, x_host, o, S, ws, cu_host, value, ms_per_step, kernel_ms, achieved_gbs,
+           achieved_tf, clk, launches_per_step, pg):
+    import torch
+    import kimi_delta_attention_12_gb300 as kda
     # ---- end to end through the public API with host buffers ----
     pin = lambda t: t.pin_memory()
     hq, hk, hv, hz, hb = (pin(t) for t in (x_host.q, x_host.k, x_host.v, x_host.z, x_host.beta))
@@ -299,35 +360,7 @@ def kda_arm(args, world, rank, local, pg):
 
     # ---- decode workload: 64 consecutive steps on a resident 1.6 GB state ----
     D = DECODE_SHAPE
-    g = torch.Generator(device=dev).manual_seed(1000 + rank)
-    Bd, Hd, dd = D["B"], D["H"], D["d"]
-    state = 0.02 * torch.randn(Bd, Hd, dd, dd, device=dev, generator=g)
-    Adec = 0.5 * torch.randn(Hd, device=dev, generator=g)
-    unit = lambda t: t / t.norm(dim=-1, keepdim=True)
-    dsteps = []
-    for s in range(D["steps"]):
-        dsteps.append((unit(torch.randn(Bd, Hd, dd, device=dev, generator=g)).bfloat16(),
-                       unit(torch.randn(Bd, Hd, dd, device=dev, generator=g)).bfloat16(),
-                       torch.randn(Bd, Hd, dd, device=dev, generator=g).bfloat16(),
-                       torch.randn(Bd, Hd, dd, device=dev, generator=g).bfloat16(),
-                       torch.sigmoid(torch.randn(Bd, Hd, device=dev, generator=g)).bfloat16()))
-    od = torch.empty(Bd, Hd, dd, dtype=torch.bfloat16, device=dev)
-    for s in range(3):
-        q_, k_, v_, z_, b_ = dsteps[s]
-        kda.kda_decode_step(q_, k_, v_, z_, b_, Adec, state, o=od)
-    torch.cuda.synchronize()
-    dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(D["steps"])]
-    with ClockSampler(local) as dclk:
-        for s in range(D["steps"]):
-            q_, k_, v_, z_, b_ = dsteps[s]
-            dev_ev[s][0].record(stream)
-            kda.kda_decode_step(q_, k_, v_, z_, b_, Adec, state, o=od)
-            dev_ev[s][1].record(stream)
-        torch.cuda.synchronize()
-    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dev_ev)
-    dec_bytes = decode_algorithmic(Bd, Hd, dd)
-    dec_gbs = dec_bytes / (dec_ms / 1e3) / 1e9
+    dec_ms, dec_bytes, dec_gbs, dclk_summary = run_decode(dev, rank, local, stream)
 
     if rank != 0:
         return
@@ -358,7 +391,7 @@ def kda_arm(args, world, rank, local, pg):
                               "steps": D["steps"]},
                    "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm_gbs"],
                                 "unit": "GB/s", "frac": dec_gbs / peaks["hbm_gbs"]},
-                   "clocks": dclk.summary()},
+                   "clocks": dclk_summary},
         "cpu_baseline": {"value": cpu_tps, "unit": "tokens/s", "cores": cpu_threads,
                          "kind": "oracle",
                          "sample": "first 1024 tokens of the prefill workload, all 32 heads, "
@@ -377,6 +410,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["kda", "reference"], default="kda")
+    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
+                    help="run one part only (for profiler captures); the default runs all")
     args = ap.parse_args()
     world, rank, local, pg = _dist_setup(args)
     try:

@@ -74,7 +74,7 @@ struct ChunkedParams {
 };
 
 // True once the chunked kernel is compiled into the library.
-constexpr bool kChunkedPrefillBuilt = false;
+constexpr bool kChunkedPrefillBuilt = true;
 
 // Workspace layout for the chunked prefill.
 size_t chunked_workspace_bytes(int32_t N, int32_t H);

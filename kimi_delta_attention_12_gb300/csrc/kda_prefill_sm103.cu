@@ -1,18 +1,726 @@
-// kda_prefill_sm103.cu -- chunked KDA prefill on tcgen05/TMEM (placeholder
-// until the tensor-core kernel lands; the API does not route here yet).
+// kda_prefill_sm103.cu -- chunked KDA prefill on tcgen05 tensor cores (sm_103a).
+//
+// The pages' prefill ("Kimi K3 Open Weights: What Is Actually New In Its 2.8
+// Trillion Parameter Architecture", section 1) processes tokens "parallel
+// within chunks, recurrent between", with decay products, triangular
+// intra-chunk interactions and dense matrix tiles; the bounded gate
+// (g >= -5) keeps the reciprocal decay factors of a 16-token tile inside the
+// bf16 range (e^80 < 3.4e38), so the diagonal tiles use dense matmuls too.
+//
+// Algebra used per chunk of C = 64 tokens (start state S0, d_k = d_v = 128),
+// derived by unrolling the recurrence; gamma_r = inclusive cumulative g:
+//   Akk[r,i] = beta_r <k_r e^{gamma_r - gamma_i}, k_i>   (i < r)
+//   Aqk[r,i] =        <q_r e^{gamma_r - gamma_i}, k_i>   (i <= r)
+//   Tm       = (I + Akk)^-1 Diag(beta)                    (UT solve, fp32)
+//   U        = Tm V - (Tm K+) S0,    K+ = k * e^{gamma}
+//   O        = Q+ S0 + Aqk U,        Q+ = q * e^{gamma}
+//   S_next   = Diag(e^{gamma_C}) S0 + Kend^T U,   Kend = k * e^{gamma_C - gamma}
+// The Gram products use one reference point per 16-token block a
+// (rho_a = gamma at the end of the previous block): the query/key side is
+// scaled by e^{gamma_r - rho_a} <= 1 and the key side of the products with
+// block a by e^{rho_a - gamma_i} (<= e^80 inside the block, <= 1 before it).
+//
+// Execution (one CTA of 8 warps per (sequence, head); one TMEM allocation of
+// 512 columns; fp32 state S^T kept in TMEM for the whole sequence):
+//   P0  TMA: raw q, k, z tiles [64 tok][128 ch]; v as a 128B-swizzled operand
+//   P1  prologue on the CUDA cores: L2 norms, gate, per-block cumulative
+//       decay, and the bf16 operand tiles (X~, K~^(a), K+, Q+, Kend)
+//   P2  tcgen05: Gram Aqk/Akk (two M=128 x N=64 x K=128 products)
+//   P3  Gram -> smem (masking, beta);  S^T -> bf16 operand; S^T *= Gamma
+//   P4  UT solve in shared memory (fp32): Tm
+//   P5  tcgen05: W^T = K+^T Tm^T, U^T = V^T Tm^T
+//   P6  W^T -> bf16 operand
+//   P7  tcgen05: U^T += S^T (-W^T), O^T = S^T Q+^T
+//   P8  U^T -> bf16 operand
+//   P9  tcgen05: O^T += U^T Aqk^T, S^T += U^T Kend
+//   P10 O^T -> o (bf16)
+// Every MMA is M=128 with the head dimension on M (the transposed form), so
+// the TMEM accumulator layout is row m -> lane m.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
 
 #include "kda_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace kda {
+namespace {
+
+using namespace sm103;
+
+constexpr int C = 64;          // chunk length
+constexpr int D = 128;         // head dim (d_k = d_v)
+constexpr int kThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kNormEps = 1e-6f;
+constexpr int kStatusTimeout = 1;
+
+// ---- shared memory map (byte offsets from a 1024-aligned base) ----
+// Region 1 (48 KB): raw q,k,z  ->  solve scratch  ->  W^T, U^T operands
+constexpr uint32_t OFF_RAWQ = 0;
+constexpr uint32_t OFF_RAWK = 16384;
+constexpr uint32_t OFF_RAWZ = 32768;
+constexpr uint32_t OFF_AKK = 0;             // fp32 [64][65]
+constexpr uint32_t OFF_NMAT = 16640;        // fp32 [64][65]
+constexpr uint32_t OFF_MSCR = 33280;        // fp32 [3][16][16]
+constexpr uint32_t OFF_WT = 0;              // bf16 [128 c][64 r]  (MN-major B)
+constexpr uint32_t OFF_UT = 16384;          // bf16 [128 j][64 i]  (K-major A)
+// Region 2 (96 KB): X~ and K~ (Gram operands) -> S^T bf16, Aqk, Tm
+constexpr uint32_t OFF_XT = 49152;          // 2 N-blocks x [128 c][64 e]  (MN-major B)
+constexpr uint32_t OFF_KT = 49152 + 32768;  // 4 M-blocks x [128 c][64 i] (MN-major A)
+constexpr uint32_t OFF_ST = 49152;          // [2 atoms][128 j][64 c]     (K-major A)
+constexpr uint32_t OFF_AQK = 49152 + 32768; // [64 r][64 i]               (K-major B)
+constexpr uint32_t OFF_TM = 49152 + 40960;  // [64 r][64 i]               (K-major B)
+// dedicated operand tiles
+constexpr uint32_t OFF_V = 147456;          // [2 blocks][64 i][64 j]     (MN-major A)
+constexpr uint32_t OFF_KP = 163840;         // [128 c][64 i]              (K-major A)
+constexpr uint32_t OFF_QP = 180224;         // [128 c][64 r]              (MN-major B)
+constexpr uint32_t OFF_KE = 196608;         // [128 c][64 i]              (K-major B)
+// small fp32 arrays
+constexpr uint32_t OFF_INVQ = 212992;       // [64]
+constexpr uint32_t OFF_INVK = OFF_INVQ + 256;
+constexpr uint32_t OFF_BETA = OFF_INVK + 256;
+constexpr uint32_t OFF_TOT = OFF_BETA + 256;  // [4][128]
+constexpr uint32_t OFF_GAM = OFF_TOT + 2048;  // [128]
+constexpr uint32_t SMEM_USED = OFF_GAM + 512;
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
+
+// TMEM columns
+constexpr uint32_t TM_S = 0;      // S^T  [128 j lanes][128 c]
+constexpr uint32_t TM_G1 = 128;   // Gram blocks 3, 2
+constexpr uint32_t TM_G2 = 192;   // Gram blocks 1, 0
+constexpr uint32_t TM_W = 256;    // W^T  [128 c][64 r]
+constexpr uint32_t TM_U = 320;    // U^T  [128 j][64 r]
+constexpr uint32_t TM_O = 384;    // O^T  [128 j][64 r]
+constexpr uint32_t TMEM_COLS = 512;
+
+struct ChunkedArgs {
+    CUtensorMap tm_q;
+    CUtensorMap tm_k;
+    CUtensorMap tm_z;
+    CUtensorMap tm_v;
+    ChunkedParams p;
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+// Store 16 consecutive fp32 values (tokens) of one operand row as bf16 into a
+// 128B-swizzled tile: row `row`, starting byte `byte0` (multiple of 32).
+__device__ __forceinline__ void store_row16(uint8_t* tile, uint32_t row, uint32_t byte0,
+                                            const float (&v)[16]) {
+    uint4 a, b;
+    a.x = pack_bf16x2(v[0], v[1]);   a.y = pack_bf16x2(v[2], v[3]);
+    a.z = pack_bf16x2(v[4], v[5]);   a.w = pack_bf16x2(v[6], v[7]);
+    b.x = pack_bf16x2(v[8], v[9]);   b.y = pack_bf16x2(v[10], v[11]);
+    b.z = pack_bf16x2(v[12], v[13]); b.w = pack_bf16x2(v[14], v[15]);
+    *reinterpret_cast<uint4*>(tile + sw128(row, byte0)) = a;
+    *reinterpret_cast<uint4*>(tile + sw128(row, byte0 + 16)) = b;
+}
+
+__device__ __forceinline__ float gate_log2(float eA, float z) {
+    // g = -5 sigmoid(e^A z), returned in log2 units (g * log2 e)
+    const float y = eA * z;
+    const float s = __fdividef(1.0f, 1.0f + exp2f(-y * kLog2e));
+    return -5.0f * kLog2e * s;
+}
+
+// CTA-wide barrier that also orders tcgen05 operations around it.
+__device__ __forceinline__ void cta_sync_tc() {
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+}
+
+__device__ void record_timeout(int32_t* status, volatile int* abort_flag) {
+    atomicExch(status, kStatusTimeout);
+    *abort_flag = 1;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
+    const ChunkedParams& p = args.p;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+    __shared__ uint64_t bar_tma;
+    __shared__ uint64_t bar_mma;
+    __shared__ uint32_t tmem_base_s;
+    __shared__ volatile int abort_flag;
+
+    float* s_invq = reinterpret_cast<float*>(sm + OFF_INVQ);
+    float* s_invk = reinterpret_cast<float*>(sm + OFF_INVK);
+    float* s_beta = reinterpret_cast<float*>(sm + OFF_BETA);
+    float* s_tot = reinterpret_cast<float*>(sm + OFF_TOT);
+    float* s_gam = reinterpret_cast<float*>(sm + OFF_GAM);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int H = p.H;
+    const int unit = blockIdx.x;
+    const int n = unit / H;
+    const int h = unit % H;
+
+    int64_t bos, eos;
+    if (p.cu_seqlens) {
+        bos = p.cu_seqlens[n];
+        eos = p.cu_seqlens[n + 1];
+    } else {
+        const int64_t len = p.total_T / p.N;
+        bos = (int64_t)n * len;
+        eos = bos + len;
+    }
+    const size_t state_off = (size_t)unit * D * D;
+
+    if (tid == 0) {
+        abort_flag = 0;
+        mbar_init(&bar_tma, 1);
+        mbar_init(&bar_mma, 1);
+        fence_mbar_init();
+        prefetch_tmap(&args.tm_q);
+        prefetch_tmap(&args.tm_k);
+        prefetch_tmap(&args.tm_z);
+        prefetch_tmap(&args.tm_v);
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_base_s, TMEM_COLS);
+        tmem_relinquish();
+    }
+    cta_sync_tc();
+    const uint32_t tbase = tmem_base_s;
+    const uint32_t smem_base = smem_u32(sm);
+
+    // ---- initial state -> TMEM: thread j (warps 0..3) owns lane j = column j of S ----
+    if (warp < 4) {
+        const int j = tid;
+        const uint32_t taddr = tbase + ((uint32_t)(32 * warp) << 16) + TM_S;
+        for (int c0 = 0; c0 < D; c0 += 16) {
+            uint32_t r[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float x = p.initial_state
+                                    ? __ldg(p.initial_state + state_off + (size_t)(c0 + i) * D + j)
+                                    : 0.0f;
+                r[i] = __float_as_uint(x);
+            }
+            tmem_st16(taddr + c0, r);
+        }
+        tmem_wait_st();
+    }
+    cta_sync_tc();
+
+    const float eA = expf(p.A[h]);
+    const __nv_bfloat16* beta_g = static_cast<const __nv_bfloat16*>(p.beta);
+    __nv_bfloat16* o_g = static_cast<__nv_bfloat16*>(p.o);
+
+    uint32_t ph_tma = 0, ph_mma = 0;
+    const int64_t len = eos - bos;
+    const int nchunks = (int)((len + C - 1) / C);
+
+    for (int ci = 0; ci < nchunks; ++ci) {
+        const int64_t t0 = bos + (int64_t)ci * C;
+        const int L = (int)((eos - t0) < C ? (eos - t0) : C);
+
+        // ---------------- P0: loads ----------------
+        if (tid == 0) {
+            mbar_arrive_expect_tx(&bar_tma, 4 * 16384);
+            tma_load_3d(sm + OFF_RAWQ, &args.tm_q, 0, h, (int)t0, &bar_tma);
+            tma_load_3d(sm + OFF_RAWK, &args.tm_k, 0, h, (int)t0, &bar_tma);
+            tma_load_3d(sm + OFF_RAWZ, &args.tm_z, 0, h, (int)t0, &bar_tma);
+            tma_load_3d(sm + OFF_V, &args.tm_v, 0, h, (int)t0, &bar_tma);
+            tma_load_3d(sm + OFF_V + 8192, &args.tm_v, 64, h, (int)t0, &bar_tma);
+        }
+        if (tid < C) {
+            s_beta[tid] = tid < L ? __bfloat162float(beta_g[(size_t)(t0 + tid) * H + h]) : 0.0f;
+        }
+        if (!mbar_wait(&bar_tma, ph_tma, &abort_flag)) {
+            record_timeout(p.status, &abort_flag);
+        }
+        ph_tma ^= 1;
+        __syncthreads();
+        if (abort_flag) {
+            break;
+        }
+
+        // ---------------- P1a: per-token L2 norms ----------------
+        {
+            const uint8_t* rq = sm + OFF_RAWQ;
+            const uint8_t* rk = sm + OFF_RAWK;
+#pragma unroll
+            for (int tt = 0; tt < 8; ++tt) {
+                const int r = warp * 8 + tt;
+                const uint2 qv = *reinterpret_cast<const uint2*>(rq + r * 256 + lane * 8);
+                const uint2 kv = *reinterpret_cast<const uint2*>(rk + r * 256 + lane * 8);
+                float q0 = bf16lo(qv.x), q1 = bf16hi(qv.x), q2 = bf16lo(qv.y), q3 = bf16hi(qv.y);
+                float k0 = bf16lo(kv.x), k1 = bf16hi(kv.x), k2 = bf16lo(kv.y), k3 = bf16hi(kv.y);
+                float sq = q0 * q0 + q1 * q1 + q2 * q2 + q3 * q3;
+                float sk = k0 * k0 + k1 * k1 + k2 * k2 + k3 * k3;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    sq += __shfl_xor_sync(0xffffffffu, sq, off);
+                    sk += __shfl_xor_sync(0xffffffffu, sk, off);
+                }
+                if (lane == 0) {
+                    const bool valid = r < L;
+                    s_invq[r] = valid ? (p.l2norm ? rsqrtf(sq + kNormEps) : 1.0f) * p.scale : 0.0f;
+                    s_invk[r] = valid ? (p.l2norm ? rsqrtf(sk + kNormEps) : 1.0f) : 0.0f;
+                }
+            }
+        }
+        __syncthreads();
+
+        // ---------------- P1b: gate, cumulative decay inside the 16-token block ----------------
+        const int cp = tid & 63;       // channel pair: channels 2cp, 2cp+1
+        const int ab = tid >> 6;       // token block: tokens 16ab .. 16ab+15
+        const int c0 = 2 * cp;
+        uint32_t qp[16], kp[16];
+        float lc0[16], lc1[16];        // inclusive cumulative log2-decay within the block
+        {
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) {
+                const int r = 16 * ab + rr;
+                qp[rr] = *reinterpret_cast<const uint32_t*>(sm + OFF_RAWQ + r * 256 + 4 * cp);
+                kp[rr] = *reinterpret_cast<const uint32_t*>(sm + OFF_RAWK + r * 256 + 4 * cp);
+                const uint32_t zp = *reinterpret_cast<const uint32_t*>(sm + OFF_RAWZ + r * 256 + 4 * cp);
+                const bool valid = r < L;
+                a0 += valid ? gate_log2(eA, bf16lo(zp)) : 0.0f;
+                a1 += valid ? gate_log2(eA, bf16hi(zp)) : 0.0f;
+                lc0[rr] = a0;
+                lc1[rr] = a1;
+            }
+            s_tot[ab * D + c0] = a0;
+            s_tot[ab * D + c0 + 1] = a1;
+        }
+        __syncthreads();
+
+        // ---------------- P1c: operand tiles ----------------
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int c = c0 + half;
+            const float* lcv = half ? lc1 : lc0;
+            float t[4];
+#pragma unroll
+            for (int b = 0; b < 4; ++b) t[b] = s_tot[b * D + c];
+            float rho[5];  // rho[b] = log2 decay before block b; rho[4] = chunk total
+            rho[0] = 0.f;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) rho[b + 1] = rho[b] + t[b];
+            if (ab == 0) {
+                s_gam[c] = exp2f(rho[4]);
+            }
+            const float rho_a = ab == 0 ? rho[0] : ab == 1 ? rho[1] : ab == 2 ? rho[2] : rho[3];
+            const float rho_a1 = ab == 0 ? rho[1] : ab == 1 ? rho[2] : ab == 2 ? rho[3] : rho[4];
+            const float tot_a = rho_a1 - rho_a;
+            const float eRa = exp2f(rho_a);               // e^{rho_a}          <= 1
+            const float eTa = exp2f(tot_a);               // e^{block total}    >= 2^-116
+            const float eEnd = exp2f(rho[4] - rho_a1);    // e^{gamma_C - rho_{a+1}} <= 1
+
+            float xq[16], xk[16], kown[16], kg[16];
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) {
+                const int r = 16 * ab + rr;
+                const float qv = (half ? bf16hi(qp[rr]) : bf16lo(qp[rr])) * s_invq[r];
+                const float kv = (half ? bf16hi(kp[rr]) : bf16lo(kp[rr])) * s_invk[r];
+                const float E = exp2f(lcv[rr]);           // e^{gamma_r - rho_a}  in [e^-80, 1]
+                const float F = exp2f(-lcv[rr]);          // e^{rho_a - gamma_r}  in [1, e^80]
+                xq[rr] = qv * E;
+                xk[rr] = kv * E;
+                kown[rr] = kv * F;
+                kg[rr] = kv * (F * eTa);                  // k e^{rho_{a+1} - gamma_r} <= 1
+            }
+            // X~ : Gram B operand; N-block 0 = [Q3 K3 Q2 K2], N-block 1 = [Q1 K1 Q0 K0]
+            {
+                const uint32_t nb = ab >= 2 ? 0u : 1u;
+                const uint32_t e0 = (ab >= 2 ? (3 - ab) : (1 - ab)) * 32;
+                uint8_t* xt = sm + OFF_XT + nb * 16384;
+                store_row16(xt, c, 2 * e0, xq);
+                store_row16(xt, c, 2 * (e0 + 16), xk);
+            }
+            // K~^(a') for a' >= ab: M-block (3 - a') of the Gram A operand
+            store_row16(sm + OFF_KT + (3 - ab) * 16384, c, 32 * ab, kown);
+#pragma unroll
+            for (int ap = 1; ap < 4; ++ap) {
+                if (ap > ab) {
+                    // e^{rho_{a'} - rho_{a+1}} <= 1
+                    const float f = exp2f((ap == 1 ? rho[1] : ap == 2 ? rho[2] : rho[3]) - rho_a1);
+                    float v[16];
+#pragma unroll
+                    for (int rr = 0; rr < 16; ++rr) v[rr] = kg[rr] * f;
+                    store_row16(sm + OFF_KT + (3 - ap) * 16384, c, 32 * ab, v);
+                }
+            }
+            // K+ = k e^{gamma}, Q+ = q e^{gamma}, Kend = k e^{gamma_C - gamma}
+            {
+                float v[16];
+#pragma unroll
+                for (int rr = 0; rr < 16; ++rr) v[rr] = xk[rr] * eRa;
+                store_row16(sm + OFF_KP, c, 32 * ab, v);
+#pragma unroll
+                for (int rr = 0; rr < 16; ++rr) v[rr] = xq[rr] * eRa;
+                store_row16(sm + OFF_QP, c, 32 * ab, v);
+#pragma unroll
+                for (int rr = 0; rr < 16; ++rr) v[rr] = kg[rr] * eEnd;
+                store_row16(sm + OFF_KE, c, 32 * ab, v);
+            }
+        }
+        fence_proxy_async();
+        cta_sync_tc();
+
+        // ---------------- P2: Gram products ----------------
+        if (tid == 0) {
+            const uint32_t idg = idesc_bf16(128, 64, 1, 1);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t a1 = smem_desc(smem_base + OFF_KT + kk * 2048, 16384, 1024);
+                const uint64_t b1 = smem_desc(smem_base + OFF_XT + kk * 2048, 16384, 1024);
+                mma_bf16(tbase + TM_G1, a1, b1, idg, kk > 0);
+                const uint64_t a2 = smem_desc(smem_base + OFF_KT + 32768 + kk * 2048, 16384, 1024);
+                const uint64_t b2 = smem_desc(smem_base + OFF_XT + 16384 + kk * 2048, 16384, 1024);
+                mma_bf16(tbase + TM_G2, a2, b2, idg, kk > 0);
+            }
+            mma_commit(&bar_mma);
+        }
+        if (!mbar_wait(&bar_mma, ph_mma, &abort_flag)) {
+            record_timeout(p.status, &abort_flag);
+        }
+        ph_mma ^= 1;
+        tc_fence_after();
+        __syncthreads();
+        if (abort_flag) {
+            break;
+        }
+
+        // ---------------- P3: Gram -> Akk (fp32), Aqk (bf16);  S^T -> bf16, S^T *= Gamma ----------------
+        if (warp < 4) {
+            const int q4 = warp;
+            const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+            float* akk = reinterpret_cast<float*>(sm + OFF_AKK);
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                const int blk = g == 0 ? (q4 < 2 ? 3 : 2) : (q4 < 2 ? 1 : 0);
+                const uint32_t col = (g == 0 ? TM_G1 : TM_G2) + (q4 < 2 ? 0 : 32);
+                const int i = (q4 < 2 ? 32 * q4 : 32 * (q4 - 2)) + lane;
+                uint32_t vq[16], vk[16];
+                tmem_ld16(tbase + lane_base + col, vq);
+                tmem_ld16(tbase + lane_base + col + 16, vk);
+                tmem_wait_ld();
+#pragma unroll
+                for (int rr = 0; rr < 16; ++rr) {
+                    const int r = 16 * blk + rr;
+                    const float aq = i <= r ? __uint_as_float(vq[rr]) : 0.0f;
+                    const float ak = i < r ? s_beta[r] * __uint_as_float(vk[rr]) : 0.0f;
+                    akk[r * 65 + i] = ak;
+                    *reinterpret_cast<__nv_bfloat16*>(sm + OFF_AQK + sw128(r, 2 * i)) =
+                        __float2bfloat16_rn(aq);
+                }
+            }
+        } else {
+            const int j = tid - 128;
+            const uint32_t taddr = tbase + ((uint32_t)(32 * (warp - 4)) << 16) + TM_S;
+#pragma unroll 1
+            for (int cb = 0; cb < D; cb += 16) {
+                uint32_t r[16];
+                tmem_ld16(taddr + cb, r);
+                tmem_wait_ld();
+                float v[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+                store_row16(sm + OFF_ST + (cb / 64) * 16384, j, 2 * (cb % 64), v);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(v[i] * s_gam[cb + i]);
+                tmem_st16(taddr + cb, r);
+            }
+            tmem_wait_st();
+        }
+        cta_sync_tc();
+
+        // ---------------- P4: UT solve  Tm = (I + Akk)^-1 Diag(beta) ----------------
+        {
+            const float* Lm = reinterpret_cast<const float*>(sm + OFF_AKK);
+            float* Nm = reinterpret_cast<float*>(sm + OFF_NMAT);
+            float* Ms = reinterpret_cast<float*>(sm + OFF_MSCR);
+            if (tid < 64) {
+                // diagonal 16x16 blocks by forward substitution, one column per thread
+                const int a = tid >> 4, jj = tid & 15;
+                const float* Lb = Lm + (16 * a) * 65 + 16 * a;
+                float x[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    float acc = (r == jj) ? 1.0f : 0.0f;
+#pragma unroll
+                    for (int i = 0; i < r; ++i) acc -= Lb[r * 65 + i] * x[i];
+                    x[r] = (r < jj) ? 0.0f : acc;
+                }
+#pragma unroll
+                for (int r = 0; r < 16; ++r) Nm[(16 * a + r) * 65 + 16 * a + jj] = x[r];
+            }
+            __syncthreads();
+            const int rr = tid >> 4, jj = tid & 15;
+#pragma unroll 1
+            for (int a = 1; a < 4; ++a) {
+                // M_ab = sum_{c=b}^{a-1} L_ac N_cb
+                for (int b = 0; b < a; ++b) {
+                    float m = 0.f;
+                    const float* Lrow = Lm + (16 * a + rr) * 65;
+                    for (int col = 16 * b; col < 16 * a; ++col) {
+                        m += Lrow[col] * Nm[col * 65 + 16 * b + jj];
+                    }
+                    Ms[(b * 16 + rr) * 16 + jj] = m;
+                }
+                __syncthreads();
+                // N_ab = -N_aa M_ab
+                for (int b = 0; b < a; ++b) {
+                    float acc = 0.f;
+                    const float* Nrow = Nm + (16 * a + rr) * 65 + 16 * a;
+                    for (int t = 0; t <= rr; ++t) {
+                        acc += Nrow[t] * Ms[(b * 16 + t) * 16 + jj];
+                    }
+                    Nm[(16 * a + rr) * 65 + 16 * b + jj] = -acc;
+                }
+                __syncthreads();
+            }
+            // Tm[r][i] = N[r][i] beta_i (lower triangle), bf16, rows of 64 -> K-major B tile
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int chunk = tid + e * kThreads;  // 512 chunks of 8 values
+                const int r = chunk >> 3, i0 = (chunk & 7) * 8;
+                uint4 w;
+                float v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int i = i0 + u;
+                    v[u] = i <= r ? Nm[r * 65 + i] * s_beta[i] : 0.0f;
+                }
+                w.x = pack_bf16x2(v[0], v[1]); w.y = pack_bf16x2(v[2], v[3]);
+                w.z = pack_bf16x2(v[4], v[5]); w.w = pack_bf16x2(v[6], v[7]);
+                *reinterpret_cast<uint4*>(sm + OFF_TM + sw128(r, 2 * i0)) = w;
+            }
+        }
+        fence_proxy_async();
+        cta_sync_tc();
+
+        // ---------------- P5: W^T = K+^T Tm^T,  U^T = V^T Tm^T ----------------
+        if (tid == 0) {
+            const uint32_t idw = idesc_bf16(128, 64, 0, 0);
+            const uint32_t idu = idesc_bf16(128, 64, 1, 0);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t bT = smem_desc(smem_base + OFF_TM + kk * 32, 16, 1024);
+                const uint64_t aK = smem_desc(smem_base + OFF_KP + kk * 32, 16, 1024);
+                mma_bf16(tbase + TM_W, aK, bT, idw, kk > 0);
+                const uint64_t aV = smem_desc(smem_base + OFF_V + kk * 2048, 8192, 1024);
+                mma_bf16(tbase + TM_U, aV, bT, idu, kk > 0);
+            }
+            mma_commit(&bar_mma);
+        }
+        if (!mbar_wait(&bar_mma, ph_mma, &abort_flag)) {
+            record_timeout(p.status, &abort_flag);
+        }
+        ph_mma ^= 1;
+        tc_fence_after();
+        __syncthreads();
+        if (abort_flag) {
+            break;
+        }
+
+        // ---------------- P6: W^T -> bf16 operand (row c = lane) ----------------
+        if (warp < 4) {
+            const int c = tid;
+            const uint32_t taddr = tbase + ((uint32_t)(32 * warp) << 16) + TM_W;
+#pragma unroll
+            for (int cb = 0; cb < C; cb += 16) {
+                uint32_t r[16];
+                tmem_ld16(taddr + cb, r);
+                tmem_wait_ld();
+                float v[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+                store_row16(sm + OFF_WT, c, 2 * cb, v);
+            }
+        }
+        fence_proxy_async();
+        cta_sync_tc();
+
+        // ---------------- P7: U^T += S^T (-W^T),  O^T = S^T Q+^T ----------------
+        if (tid == 0) {
+            const uint32_t idu = idesc_bf16(128, 64, 0, 1, /*neg_b=*/1);
+            const uint32_t ido = idesc_bf16(128, 64, 0, 1);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t aS =
+                    smem_desc(smem_base + OFF_ST + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                const uint64_t bW = smem_desc(smem_base + OFF_WT + kk * 2048, 16384, 1024);
+                mma_bf16(tbase + TM_U, aS, bW, idu, 1);
+                const uint64_t bQ = smem_desc(smem_base + OFF_QP + kk * 2048, 16384, 1024);
+                mma_bf16(tbase + TM_O, aS, bQ, ido, kk > 0);
+            }
+            mma_commit(&bar_mma);
+        }
+        if (!mbar_wait(&bar_mma, ph_mma, &abort_flag)) {
+            record_timeout(p.status, &abort_flag);
+        }
+        ph_mma ^= 1;
+        tc_fence_after();
+        __syncthreads();
+        if (abort_flag) {
+            break;
+        }
+
+        // ---------------- P8: U^T -> bf16 operand (row j = lane) ----------------
+        if (warp < 4) {
+            const int j = tid;
+            const uint32_t taddr = tbase + ((uint32_t)(32 * warp) << 16) + TM_U;
+#pragma unroll
+            for (int cb = 0; cb < C; cb += 16) {
+                uint32_t r[16];
+                tmem_ld16(taddr + cb, r);
+                tmem_wait_ld();
+                float v[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+                store_row16(sm + OFF_UT, j, 2 * cb, v);
+            }
+        }
+        fence_proxy_async();
+        cta_sync_tc();
+
+        // ---------------- P9: O^T += U^T Aqk^T,  S^T += U^T Kend ----------------
+        if (tid == 0) {
+            const uint32_t ido = idesc_bf16(128, 64, 0, 0);
+            const uint32_t ids = idesc_bf16(128, 128, 0, 0);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t aU = smem_desc(smem_base + OFF_UT + kk * 32, 16, 1024);
+                const uint64_t bA = smem_desc(smem_base + OFF_AQK + kk * 32, 16, 1024);
+                mma_bf16(tbase + TM_O, aU, bA, ido, 1);
+                const uint64_t bK = smem_desc(smem_base + OFF_KE + kk * 32, 16, 1024);
+                mma_bf16(tbase + TM_S, aU, bK, ids, 1);
+            }
+            mma_commit(&bar_mma);
+        }
+        if (!mbar_wait(&bar_mma, ph_mma, &abort_flag)) {
+            record_timeout(p.status, &abort_flag);
+        }
+        ph_mma ^= 1;
+        tc_fence_after();
+        __syncthreads();
+        if (abort_flag) {
+            break;
+        }
+
+        // ---------------- P10: O^T -> o ----------------
+        if (warp < 4) {
+            const int j = tid;
+            const uint32_t taddr = tbase + ((uint32_t)(32 * warp) << 16) + TM_O;
+#pragma unroll
+            for (int cb = 0; cb < C; cb += 16) {
+                uint32_t r[16];
+                tmem_ld16(taddr + cb, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int rtok = cb + i;
+                    if (rtok < L) {
+                        o_g[((size_t)(t0 + rtok) * H + h) * D + j] =
+                            __float2bfloat16_rn(__uint_as_float(r[i]));
+                    }
+                }
+            }
+        }
+        // all generic-proxy smem traffic of this chunk is ordered before the
+        // next chunk's TMA writes into the same regions
+        fence_proxy_async();
+        cta_sync_tc();
+    }
+
+    // ---- final state: TMEM S^T -> final_state (coalesced along j) ----
+    if (!abort_flag && p.final_state && warp < 4) {
+        const int j = tid;
+        const uint32_t taddr = tbase + ((uint32_t)(32 * warp) << 16) + TM_S;
+        for (int cb = 0; cb < D; cb += 16) {
+            uint32_t r[16];
+            tmem_ld16(taddr + cb, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                p.final_state[state_off + (size_t)(cb + i) * D + j] = __uint_as_float(r[i]);
+            }
+        }
+    }
+    cta_sync_tc();
+    if (warp == 0) {
+        tmem_dealloc(tbase, TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ host
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            return nullptr;
+        }
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    return fn;
+}
+
+bool make_map(CUtensorMap* map, const void* base, int total_T, int H, int box_c,
+              CUtensorMapSwizzle swz) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) {
+        return false;
+    }
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)total_T};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+    cuuint32_t box[3] = {(cuuint32_t)box_c, 1, (cuuint32_t)C};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+              box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
 
 size_t chunked_workspace_bytes(int32_t N, int32_t H) {
     return 256 + (size_t)N * H * sizeof(int32_t);
 }
 
 cudaError_t launch_chunked_prefill(const ChunkedParams& p, cudaStream_t stream) {
-    (void)p; (void)stream;
-    return cudaErrorNotSupported;
+    ChunkedArgs args;
+    memset(&args, 0, sizeof(args));
+    args.p = p;
+    if (!make_map(&args.tm_q, p.q, p.total_T, p.H, 128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&args.tm_k, p.k, p.total_T, p.H, 128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&args.tm_z, p.z, p.total_T, p.H, 128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&args.tm_v, p.v, p.total_T, p.H, 64, CU_TENSOR_MAP_SWIZZLE_128B)) {
+        return cudaErrorInvalidValue;
+    }
+    cudaError_t err = cudaFuncSetAttribute(kda_chunked_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)SMEM_BYTES);
+    if (err != cudaSuccess) {
+        return err;
+    }
+    const unsigned grid = (unsigned)((int64_t)p.N * p.H);
+    if (grid == 0) {
+        return cudaSuccess;
+    }
+    kda_chunked_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(args);
+    return cudaGetLastError();
 }
 
 }  // namespace kda

@@ -1,0 +1,141 @@
+"""GPU parity of the chunked tcgen05 prefill (bf16, d_k = d_v = 128) against
+the fp64 oracle, through the C ABI.  Bar: relative Frobenius error <= 2e-2 on
+o and on the final state, on the same seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+import kimi_delta_attention_12_gb300 as kda
+from kimi_delta_attention_12_gb300 import inputs
+from metrics import BF16_TOL, rel_fro
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    kda.lib()
+
+
+def _prefill(x, **kw):
+    xd = x.to(DEV)
+    ws = kda.alloc_workspace(x.cu_seqlens.numel() - 1, x.q.shape[0], x.q.shape[1], 128, 128,
+                             torch.bfloat16)
+    o, S = kda.kda_prefill(xd.q, xd.k, xd.v, xd.z, xd.beta, xd.A, xd.initial_state,
+                           xd.cu_seqlens, cu_seqlens_host=x.cu_seqlens, workspace=ws, **kw)
+    assert kda.workspace_status(ws) == kda.KDA_OK
+    return o, S
+
+
+def _check(x, o, S, units=None, tol=BF16_TOL):
+    import oracle
+    o_ref, S_ref, _ = oracle.kda_reference(x.q, x.k, x.v, x.z, x.beta, x.A, x.initial_state,
+                                           x.cu_seqlens, units=units)
+    o_c, S_c = o.float().cpu().numpy(), S.cpu().numpy()
+    if units is None:
+        eo, es = rel_fro(o_c, o_ref), rel_fro(S_c, S_ref)
+    else:
+        cu = x.cu_seqlens.numpy()
+        eo_num = eo_den = es_num = es_den = 0.0
+        for n, h in units:
+            sl = slice(cu[n], cu[n + 1])
+            eo_num += float(np.sum((o_c[sl, h] - o_ref[sl, h]) ** 2))
+            eo_den += float(np.sum(o_ref[sl, h] ** 2))
+            es_num += float(np.sum((S_c[n, h] - S_ref[n, h]) ** 2))
+            es_den += float(np.sum(S_ref[n, h] ** 2))
+        eo, es = (eo_num / max(eo_den, 1e-300)) ** 0.5, (es_num / max(es_den, 1e-300)) ** 0.5
+    assert np.isfinite(o_c).all() and np.isfinite(S_c).all()
+    assert eo <= tol, f"o relative Frobenius error {eo}"
+    assert es <= tol, f"final state relative Frobenius error {es}"
+    return eo, es
+
+
+@pytest.mark.parametrize("lens", [[64], [1], [17], [65], [200], [130, 0, 70, 5, 64]])
+def test_small_lengths_zero_state(lens):
+    x = inputs.make_prefill_inputs(lens, 3, 128, 128, torch.bfloat16, seed=len(lens) + sum(lens))
+    o, S = _prefill(x)
+    _check(x, o, S)
+
+
+def test_nonzero_state_and_scale():
+    x = inputs.make_prefill_inputs([300, 77], 4, 128, 128, torch.bfloat16, seed=11,
+                                   nonzero_state=True)
+    o, S = _prefill(x, scale=0.0883883)
+    import oracle
+    o_ref, S_ref, _ = oracle.kda_reference(x.q, x.k, x.v, x.z, x.beta, x.A, x.initial_state,
+                                           x.cu_seqlens, scale=0.0883883)
+    assert rel_fro(o, o_ref) <= BF16_TOL and rel_fro(S, S_ref) <= BF16_TOL
+
+
+def test_zero_length_sequences_return_initial_state():
+    x = inputs.make_prefill_inputs([0, 100, 0], 2, 128, 128, torch.bfloat16, seed=12,
+                                   nonzero_state=True)
+    o, S = _prefill(x)
+    assert torch.equal(S[0].cpu(), x.initial_state[0])
+    assert torch.equal(S[2].cpu(), x.initial_state[2])
+    _check(x, o, S)
+
+
+def test_prefill_4k_workload_all_heads():
+    """B=1, H=32, T=4096, d=128, bf16, zero state: every head compared."""
+    x = inputs.make_workload_inputs(inputs.PREFILL_4K, seed=0)
+    o, S = _prefill(x)
+    _check(x, o, S)
+
+
+def test_varlen_workload_sampled_units():
+    """16 packed sequences with lengths U[512, 16384], H=64, initial states
+    ~N(0, 0.02): the launch the benchmark would make, checked on a seeded
+    sample of (sequence, head) units (heads are independent)."""
+    x = inputs.make_workload_inputs(inputs.VARLEN_16, seed=0)
+    o, S = _prefill(x)
+    g = np.random.default_rng(0)
+    units = sorted({(int(n), int(h)) for n, h in zip(g.integers(0, 16, 12), g.integers(0, 64, 12))})
+    longest = int(np.argmax(x.cu_seqlens[1:].numpy() - x.cu_seqlens[:-1].numpy()))
+    units = sorted(set(units) | {(longest, 0), (longest, 63)})
+    _check(x, o, S, units=units)
+
+
+def test_long_prefill_workload_sampled_heads():
+    """B=1, H=96, T=65536, d=128: final state and outputs on sampled heads."""
+    x = inputs.make_workload_inputs(inputs.PREFILL_64K, seed=0)
+    o, S = _prefill(x)
+    _check(x, o, S, units=[(0, 0), (0, 37), (0, 95)])
+
+
+def test_chunked_matches_recurrent_kernel():
+    """The tensor-core path against the exact fp32 recurrent kernel on the GPU."""
+    x = inputs.make_prefill_inputs([1000, 333], 8, 128, 128, torch.bfloat16, seed=13,
+                                   nonzero_state=True)
+    o_c, S_c = _prefill(x)
+    o_r, S_r = _prefill(x, recurrent=True)
+    assert rel_fro(o_c, o_r.float()) <= BF16_TOL
+    assert rel_fro(S_c, S_r) <= BF16_TOL
+
+
+def test_split_handoff_consistent():
+    """prefill(T1) -> state -> prefill(T2) against one prefill(T1 + T2)."""
+    x = inputs.make_prefill_inputs([640], 4, 128, 128, torch.bfloat16, seed=14,
+                                   nonzero_state=True)
+    xd = x.to(DEV)
+    o_full, S_full = kda.kda_prefill(xd.q, xd.k, xd.v, xd.z, xd.beta, xd.A, xd.initial_state)
+    a, b = slice(0, 256), slice(256, 640)
+    o_a, S_a = kda.kda_prefill(xd.q[a], xd.k[a], xd.v[a], xd.z[a], xd.beta[a], xd.A,
+                               xd.initial_state)
+    o_b, S_b = kda.kda_prefill(xd.q[b], xd.k[b], xd.v[b], xd.z[b], xd.beta[b], xd.A, S_a)
+    torch.cuda.synchronize()
+    # a split on a chunk boundary reproduces the same arithmetic
+    assert torch.equal(torch.cat([o_a, o_b]), o_full)
+    assert torch.equal(S_b, S_full)
+
+
+def test_deterministic():
+    x = inputs.make_prefill_inputs([500, 12], 4, 128, 128, torch.bfloat16, seed=15,
+                                   nonzero_state=True)
+    o1, S1 = _prefill(x)
+    o2, S2 = _prefill(x)
+    assert torch.equal(o1, o2) and torch.equal(S1, S2)
