@@ -59,21 +59,23 @@ constexpr float kNormEps = 1e-6f;
 constexpr int kStatusTimeout = 1;
 
 // ---- shared memory map (byte offsets from a 1024-aligned base) ----
-// Region 1 (48 KB): raw q,k,z  ->  solve scratch  ->  W^T, U^T operands
+// Region 1 (48 KB): raw q, k, z tiles, dedicated so that the next chunk's
+// loads can be issued as soon as the prologue has consumed them.
 constexpr uint32_t OFF_RAWQ = 0;
 constexpr uint32_t OFF_RAWK = 16384;
 constexpr uint32_t OFF_RAWZ = 32768;
-constexpr uint32_t OFF_AKK = 0;             // fp32 [64][65]
-constexpr uint32_t OFF_NMAT = 16640;        // fp32 [64][65]
-constexpr uint32_t OFF_MSCR = 33280;        // fp32 [3][16][16]
-constexpr uint32_t OFF_WT = 0;              // bf16 [128 c][64 r]  (MN-major B)
-constexpr uint32_t OFF_UT = 16384;          // bf16 [128 j][64 i]  (K-major A)
-// Region 2 (96 KB): X~ and K~ (Gram operands) -> S^T bf16, Aqk, Tm
+// Region 2 (96 KB): X~ and K~ (Gram operands, P1-P2); then S^T bf16, Aqk, Tm
+// and the solve scratch (P3-P4); then W^T and U^T (P6-P9).
 constexpr uint32_t OFF_XT = 49152;          // 2 N-blocks x [128 c][64 e]  (MN-major B)
 constexpr uint32_t OFF_KT = 49152 + 32768;  // 4 M-blocks x [128 c][64 i] (MN-major A)
 constexpr uint32_t OFF_ST = 49152;          // [2 atoms][128 j][64 c]     (K-major A)
-constexpr uint32_t OFF_AQK = 49152 + 32768; // [64 r][64 i]               (K-major B)
-constexpr uint32_t OFF_TM = 49152 + 40960;  // [64 r][64 i]               (K-major B)
+constexpr uint32_t OFF_AQK = 81920;         // [64 r][64 i]               (K-major B)
+constexpr uint32_t OFF_TM = 90112;          // [64 r][64 i]               (K-major B)
+constexpr uint32_t OFF_AKK = 98304;         // fp32 [64][65]
+constexpr uint32_t OFF_NMAT = 114944;       // fp32 [64][65]
+constexpr uint32_t OFF_MSCR = 131584;       // fp32 [3][16][16]
+constexpr uint32_t OFF_WT = 98304;          // bf16 [128 c][64 r]  (MN-major B)
+constexpr uint32_t OFF_UT = 114688;         // bf16 [128 j][64 i]  (K-major A)
 // dedicated operand tiles
 constexpr uint32_t OFF_V = 147456;          // [2 blocks][64 i][64 j]     (MN-major A)
 constexpr uint32_t OFF_KP = 163840;         // [128 c][64 i]              (K-major A)
@@ -151,7 +153,8 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-    __shared__ uint64_t bar_tma;
+    __shared__ uint64_t bar_raw;   // raw q, k, z of a chunk landed
+    __shared__ uint64_t bar_v;     // v of a chunk landed
     __shared__ uint64_t bar_mma;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_flag;
@@ -183,7 +186,8 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
 
     if (tid == 0) {
         abort_flag = 0;
-        mbar_init(&bar_tma, 1);
+        mbar_init(&bar_raw, 1);
+        mbar_init(&bar_v, 1);
         mbar_init(&bar_mma, 1);
         fence_mbar_init();
         prefetch_tmap(&args.tm_q);
@@ -222,30 +226,41 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
     const __nv_bfloat16* beta_g = static_cast<const __nv_bfloat16*>(p.beta);
     __nv_bfloat16* o_g = static_cast<__nv_bfloat16*>(p.o);
 
-    uint32_t ph_tma = 0, ph_mma = 0;
+    uint32_t ph_raw = 0, ph_v = 0, ph_mma = 0;
     const int64_t len = eos - bos;
     const int nchunks = (int)((len + C - 1) / C);
+    // loads issued and not yet waited for (uniform across the CTA); drained
+    // before exit if the chunk loop is left early
+    bool raw_pending = nchunks > 0, v_pending = nchunks > 0;
+
+    // loads of chunk 0; later chunks are issued one chunk ahead
+    if (tid == 0 && nchunks > 0) {
+        mbar_arrive_expect_tx(&bar_raw, 3 * 16384);
+        tma_load_3d(sm + OFF_RAWQ, &args.tm_q, 0, h, (int)bos, &bar_raw);
+        tma_load_3d(sm + OFF_RAWK, &args.tm_k, 0, h, (int)bos, &bar_raw);
+        tma_load_3d(sm + OFF_RAWZ, &args.tm_z, 0, h, (int)bos, &bar_raw);
+        mbar_arrive_expect_tx(&bar_v, 16384);
+        tma_load_3d(sm + OFF_V, &args.tm_v, 0, h, (int)bos, &bar_v);
+        tma_load_3d(sm + OFF_V + 8192, &args.tm_v, 64, h, (int)bos, &bar_v);
+    }
 
     for (int ci = 0; ci < nchunks; ++ci) {
         const int64_t t0 = bos + (int64_t)ci * C;
         const int L = (int)((eos - t0) < C ? (eos - t0) : C);
 
-        // ---------------- P0: loads ----------------
-        if (tid == 0) {
-            mbar_arrive_expect_tx(&bar_tma, 4 * 16384);
-            tma_load_3d(sm + OFF_RAWQ, &args.tm_q, 0, h, (int)t0, &bar_tma);
-            tma_load_3d(sm + OFF_RAWK, &args.tm_k, 0, h, (int)t0, &bar_tma);
-            tma_load_3d(sm + OFF_RAWZ, &args.tm_z, 0, h, (int)t0, &bar_tma);
-            tma_load_3d(sm + OFF_V, &args.tm_v, 0, h, (int)t0, &bar_tma);
-            tma_load_3d(sm + OFF_V + 8192, &args.tm_v, 64, h, (int)t0, &bar_tma);
-        }
+        const bool has_next = ci + 1 < nchunks;
+        const int t_next = (int)(t0 + C);
+
+        // ---------------- P0: this chunk's raw tiles (issued one chunk ahead) ----------------
         if (tid < C) {
             s_beta[tid] = tid < L ? __bfloat162float(beta_g[(size_t)(t0 + tid) * H + h]) : 0.0f;
         }
-        if (!mbar_wait(&bar_tma, ph_tma, &abort_flag)) {
+        if (mbar_wait(&bar_raw, ph_raw, &abort_flag)) {
+            ph_raw ^= 1;
+            raw_pending = false;
+        } else {
             record_timeout(p.status, &abort_flag);
         }
-        ph_tma ^= 1;
         __syncthreads();
         if (abort_flag) {
             break;
@@ -377,7 +392,14 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
         cta_sync_tc();
 
         // ---------------- P2: Gram products ----------------
+        raw_pending = has_next;
         if (tid == 0) {
+            if (has_next) {  // raw tiles are consumed: fetch the next chunk's
+                mbar_arrive_expect_tx(&bar_raw, 3 * 16384);
+                tma_load_3d(sm + OFF_RAWQ, &args.tm_q, 0, h, t_next, &bar_raw);
+                tma_load_3d(sm + OFF_RAWK, &args.tm_k, 0, h, t_next, &bar_raw);
+                tma_load_3d(sm + OFF_RAWZ, &args.tm_z, 0, h, t_next, &bar_raw);
+            }
             const uint32_t idg = idesc_bf16(128, 64, 1, 1);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
@@ -510,7 +532,13 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
         cta_sync_tc();
 
         // ---------------- P5: W^T = K+^T Tm^T,  U^T = V^T Tm^T ----------------
-        if (tid == 0) {
+        if (mbar_wait(&bar_v, ph_v, &abort_flag)) {
+            ph_v ^= 1;
+            v_pending = false;
+        } else {
+            record_timeout(p.status, &abort_flag);
+        }
+        if (tid == 0 && !abort_flag) {
             const uint32_t idw = idesc_bf16(128, 64, 0, 0);
             const uint32_t idu = idesc_bf16(128, 64, 1, 0);
 #pragma unroll
@@ -531,6 +559,12 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
         __syncthreads();
         if (abort_flag) {
             break;
+        }
+        v_pending = has_next;
+        if (tid == 0 && has_next) {  // v tile consumed by the tensor core: fetch the next one
+            mbar_arrive_expect_tx(&bar_v, 16384);
+            tma_load_3d(sm + OFF_V, &args.tm_v, 0, h, t_next, &bar_v);
+            tma_load_3d(sm + OFF_V + 8192, &args.tm_v, 64, h, t_next, &bar_v);
         }
 
         // ---------------- P6: W^T -> bf16 operand (row c = lane) ----------------
@@ -637,10 +671,15 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
                 }
             }
         }
-        // all generic-proxy smem traffic of this chunk is ordered before the
-        // next chunk's TMA writes into the same regions
-        fence_proxy_async();
         cta_sync_tc();
+    }
+
+    // a loop left early may still have loads in flight into this CTA's smem
+    if (raw_pending) {
+        mbar_wait(&bar_raw, ph_raw, nullptr);
+    }
+    if (v_pending) {
+        mbar_wait(&bar_v, ph_v, nullptr);
     }
 
     // ---- final state: TMEM S^T -> final_state (coalesced along j) ----
