@@ -298,9 +298,9 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
         const int ab = tid >> 6;       // token block: tokens 16ab .. 16ab+15
         const int c0 = 2 * cp;
         uint32_t qp[16], kp[16];
-        float lc0[16], lc1[16];        // inclusive cumulative log2-decay within the block
+        float al0[16], al1[16];        // per-token decay alpha = e^g of the two channels
         {
-            float a0 = 0.f, a1 = 0.f;
+            float a0 = 0.f, a1 = 0.f;  // block totals of g, log2 units
 #pragma unroll
             for (int rr = 0; rr < 16; ++rr) {
                 const int r = 16 * ab + rr;
@@ -308,10 +308,12 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
                 kp[rr] = *reinterpret_cast<const uint32_t*>(sm + OFF_RAWK + r * 256 + 4 * cp);
                 const uint32_t zp = *reinterpret_cast<const uint32_t*>(sm + OFF_RAWZ + r * 256 + 4 * cp);
                 const bool valid = r < L;
-                a0 += valid ? gate_log2(eA, bf16lo(zp)) : 0.0f;
-                a1 += valid ? gate_log2(eA, bf16hi(zp)) : 0.0f;
-                lc0[rr] = a0;
-                lc1[rr] = a1;
+                const float g0 = valid ? gate_log2(eA, bf16lo(zp)) : 0.0f;
+                const float g1 = valid ? gate_log2(eA, bf16hi(zp)) : 0.0f;
+                a0 += g0;
+                a1 += g1;
+                al0[rr] = exp2f(g0);
+                al1[rr] = exp2f(g1);
             }
             s_tot[ab * D + c0] = a0;
             s_tot[ab * D + c0 + 1] = a1;
@@ -322,7 +324,7 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             const int c = c0 + half;
-            const float* lcv = half ? lc1 : lc0;
+            const float* alv = half ? al1 : al0;
             float t[4];
 #pragma unroll
             for (int b = 0; b < 4; ++b) t[b] = s_tot[b * D + c];
@@ -337,8 +339,20 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
             const float rho_a1 = ab == 0 ? rho[1] : ab == 1 ? rho[2] : ab == 2 ? rho[3] : rho[4];
             const float tot_a = rho_a1 - rho_a;
             const float eRa = exp2f(rho_a);               // e^{rho_a}          <= 1
-            const float eTa = exp2f(tot_a);               // e^{block total}    >= 2^-116
+            const float cF = exp2f(-tot_a);               // e^{-block total}   <= e^80
             const float eEnd = exp2f(rho[4] - rho_a1);    // e^{gamma_C - rho_{a+1}} <= 1
+
+            // In-block decay factors as running products of alpha:
+            //   E_r = e^{gamma_r - rho_a}      = prod_{t<=r} alpha_t        in [e^-80, 1]
+            //   G_r = e^{rho_{a+1} - gamma_r}  = prod_{t>r, t in block}     in [e^-80, 1]
+            //   F_r = e^{rho_a - gamma_r}      = G_r e^{-block total}       in [1, e^80]
+            float E[16], G[16];
+            E[0] = alv[0];
+#pragma unroll
+            for (int rr = 1; rr < 16; ++rr) E[rr] = E[rr - 1] * alv[rr];
+            G[15] = 1.0f;
+#pragma unroll
+            for (int rr = 14; rr >= 0; --rr) G[rr] = G[rr + 1] * alv[rr + 1];
 
             float xq[16], xk[16], kown[16], kg[16];
 #pragma unroll
@@ -346,12 +360,10 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
                 const int r = 16 * ab + rr;
                 const float qv = (half ? bf16hi(qp[rr]) : bf16lo(qp[rr])) * s_invq[r];
                 const float kv = (half ? bf16hi(kp[rr]) : bf16lo(kp[rr])) * s_invk[r];
-                const float E = exp2f(lcv[rr]);           // e^{gamma_r - rho_a}  in [e^-80, 1]
-                const float F = exp2f(-lcv[rr]);          // e^{rho_a - gamma_r}  in [1, e^80]
-                xq[rr] = qv * E;
-                xk[rr] = kv * E;
-                kown[rr] = kv * F;
-                kg[rr] = kv * (F * eTa);                  // k e^{rho_{a+1} - gamma_r} <= 1
+                xq[rr] = qv * E[rr];
+                xk[rr] = kv * E[rr];
+                kg[rr] = kv * G[rr];                      // k e^{rho_{a+1} - gamma_r} <= 1
+                kown[rr] = kg[rr] * cF;                   // k e^{rho_a - gamma_r}
             }
             // X~ : Gram B operand; N-block 0 = [Q3 K3 Q2 K2], N-block 1 = [Q1 K1 Q0 K0]
             {
