@@ -73,7 +73,7 @@ constexpr uint32_t OFF_AQK = 81920;         // [64 r][64 i]               (K-maj
 constexpr uint32_t OFF_TM = 90112;          // [64 r][64 i]               (K-major B)
 constexpr uint32_t OFF_AKK = 98304;         // fp32 [64][65]
 constexpr uint32_t OFF_NMAT = 114944;       // fp32 [64][65]
-constexpr uint32_t OFF_MSCR = 131584;       // fp32 [3][16][16]
+constexpr uint32_t OFF_MSCR = 131584;       // fp32 [3 x 16][65]
 constexpr uint32_t OFF_WT = 98304;          // bf16 [128 c][64 r]  (MN-major B)
 constexpr uint32_t OFF_UT = 114688;         // bf16 [128 j][64 i]  (K-major A)
 // dedicated operand tiles
@@ -133,6 +133,56 @@ __device__ __forceinline__ float gate_log2(float eA, float z) {
     const float y = eA * z;
     const float s = __fdividef(1.0f, 1.0f + exp2f(-y * kLog2e));
     return -5.0f * kLog2e * s;
+}
+
+// ---- UT-solve helpers: warp-level 16x16x16 products on fp32 [..][65] tiles ----
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], const uint32_t (&a)[4],
+                                                const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// acc (+)= X[xr0.., xc0..] * Y[yr0.., yc0..], all 16x16, row stride 65 floats.
+// acc holds the two 16x8 column halves in the m16n8 accumulator layout.
+__device__ __forceinline__ void warp_gemm16(float (&acc)[2][4], const float* X, int xr0, int xc0,
+                                            const float* Y, int yr0, int yc0, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int kb = 0; kb < 16; kb += 8) {
+        uint32_t a[4];
+        a[0] = to_tf32(X[(xr0 + g) * 65 + xc0 + kb + t]);
+        a[1] = to_tf32(X[(xr0 + g + 8) * 65 + xc0 + kb + t]);
+        a[2] = to_tf32(X[(xr0 + g) * 65 + xc0 + kb + t + 4]);
+        a[3] = to_tf32(X[(xr0 + g + 8) * 65 + xc0 + kb + t + 4]);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            uint32_t b[2];
+            b[0] = to_tf32(Y[(yr0 + kb + t) * 65 + yc0 + nt * 8 + g]);
+            b[1] = to_tf32(Y[(yr0 + kb + t + 4) * 65 + yc0 + nt * 8 + g]);
+            mma_tf32_16x8x8(acc[nt], a, b);
+        }
+    }
+}
+
+__device__ __forceinline__ void warp_store16(const float (&acc)[2][4], float* Z, int zr0, int zc0,
+                                             float sign, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        Z[(zr0 + g) * 65 + zc0 + nt * 8 + 2 * t] = sign * acc[nt][0];
+        Z[(zr0 + g) * 65 + zc0 + nt * 8 + 2 * t + 1] = sign * acc[nt][1];
+        Z[(zr0 + g + 8) * 65 + zc0 + nt * 8 + 2 * t] = sign * acc[nt][2];
+        Z[(zr0 + g + 8) * 65 + zc0 + nt * 8 + 2 * t + 1] = sign * acc[nt][3];
+    }
 }
 
 // CTA-wide barrier that also orders tcgen05 operations around it.
@@ -479,47 +529,45 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
         cta_sync_tc();
 
         // ---------------- P4: UT solve  Tm = (I + Akk)^-1 Diag(beta) ----------------
+        // N = (I + L)^-1, L = Akk strictly lower, in 16x16 blocks: the diagonal
+        // blocks by forward substitution (one column per thread), then the
+        // off-diagonal blocks by block rows, N_ab = -N_aa sum_{c=b}^{a-1} L_ac N_cb,
+        // in three waves of warp-level tf32 products.
         {
             const float* Lm = reinterpret_cast<const float*>(sm + OFF_AKK);
             float* Nm = reinterpret_cast<float*>(sm + OFF_NMAT);
             float* Ms = reinterpret_cast<float*>(sm + OFF_MSCR);
             if (tid < 64) {
-                // diagonal 16x16 blocks by forward substitution, one column per thread
                 const int a = tid >> 4, jj = tid & 15;
                 const float* Lb = Lm + (16 * a) * 65 + 16 * a;
-                float x[16];
+                float acc[16];
 #pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    float acc = (r == jj) ? 1.0f : 0.0f;
+                for (int r = 0; r < 16; ++r) acc[r] = (r == jj) ? 1.0f : 0.0f;
 #pragma unroll
-                    for (int i = 0; i < r; ++i) acc -= Lb[r * 65 + i] * x[i];
-                    x[r] = (r < jj) ? 0.0f : acc;
+                for (int i = 0; i < 16; ++i) {
+                    const float xi = (i < jj) ? 0.0f : acc[i];
+                    acc[i] = xi;
+#pragma unroll
+                    for (int r = i + 1; r < 16; ++r) acc[r] -= Lb[r * 65 + i] * xi;
                 }
 #pragma unroll
-                for (int r = 0; r < 16; ++r) Nm[(16 * a + r) * 65 + 16 * a + jj] = x[r];
+                for (int r = 0; r < 16; ++r) Nm[(16 * a + r) * 65 + 16 * a + jj] = acc[r];
             }
             __syncthreads();
-            const int rr = tid >> 4, jj = tid & 15;
 #pragma unroll 1
-            for (int a = 1; a < 4; ++a) {
-                // M_ab = sum_{c=b}^{a-1} L_ac N_cb
-                for (int b = 0; b < a; ++b) {
-                    float m = 0.f;
-                    const float* Lrow = Lm + (16 * a + rr) * 65;
-                    for (int col = 16 * b; col < 16 * a; ++col) {
-                        m += Lrow[col] * Nm[col * 65 + 16 * b + jj];
+            for (int wave = 1; wave < 4; ++wave) {
+                // wave w computes the blocks N_{a, a-w}, one warp per block
+                if (warp < 4 - wave) {
+                    const int a = warp + wave, b = a - wave;
+                    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    for (int c = b; c < a; ++c) {
+                        warp_gemm16(acc, Lm, 16 * a, 16 * c, Nm, 16 * c, 16 * b, lane);
                     }
-                    Ms[(b * 16 + rr) * 16 + jj] = m;
-                }
-                __syncthreads();
-                // N_ab = -N_aa M_ab
-                for (int b = 0; b < a; ++b) {
-                    float acc = 0.f;
-                    const float* Nrow = Nm + (16 * a + rr) * 65 + 16 * a;
-                    for (int t = 0; t <= rr; ++t) {
-                        acc += Nrow[t] * Ms[(b * 16 + t) * 16 + jj];
-                    }
-                    Nm[(16 * a + rr) * 65 + 16 * b + jj] = -acc;
+                    warp_store16(acc, Ms, 16 * warp, 0, 1.0f, lane);
+                    __syncwarp();
+                    float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    warp_gemm16(acc2, Nm, 16 * a, 16 * a, Ms, 16 * warp, 0, lane);
+                    warp_store16(acc2, Nm, 16 * a, 16 * b, -1.0f, lane);
                 }
                 __syncthreads();
             }
