@@ -18,12 +18,13 @@
 // The same kernel serves as the exact fp32 prefill path (any head dim, fp32
 // inputs).
 //
-// Thread layout: a state row of d_v floats is covered by LPR = d_v/4 lanes
-// holding one float4 each; a warp covers RPW = 32/LPR rows per pass; the CTA
-// covers RSTEP = 8*RPW rows per pass and each thread keeps RPT = d_k/RSTEP
-// float4 of the state.  Column sums over the d_k rows (S'^T k, S'^T q) are
-// reduced with warp shuffles inside a warp and through shared memory across
-// the 8 warps.
+// Thread layout: the value columns of a head are split over NSPLIT CTAs (the
+// columns of S are independent); a CTA's slice of DVS = d_v/NSPLIT columns
+// is covered by LPR = DVS/4 lanes holding one float4 each; a warp covers
+// RPW = 32/LPR rows per pass; the CTA covers RSTEP = 8*RPW rows per pass and
+// each thread keeps RPT = d_k/RSTEP float4 of the state.  Column sums over
+// the d_k rows (S'^T k, S'^T q) are reduced with warp shuffles inside a warp
+// and through shared memory across the 8 warps.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -57,22 +58,24 @@ __device__ __forceinline__ float sigmoid_f(float x) {
     return e / (1.0f + e);
 }
 
-template <int DK, int DV, typename T>
+template <int DK, int DV, int NSPLIT, typename T>
 __global__ void __launch_bounds__(kThreads)
 kda_recurrent_kernel(const RecurrentParams p) {
-    constexpr int LPR = DV / 4;
+    constexpr int DVS = DV / NSPLIT;
+    constexpr int LPR = DVS / 4;
     constexpr int RPW = 32 / LPR;
     constexpr int RSTEP = kWarps * RPW;
     constexpr int RPT = DK / RSTEP;
     static_assert(RPT >= 1 && RPT * RSTEP == DK, "bad state tiling");
-    static_assert(DK + DV <= kThreads, "stage-1 loaders need DK + DV threads");
+    static_assert(DK + DVS <= kThreads, "stage-1 loaders need DK + DVS threads");
+    static_assert(LPR >= 1 && LPR <= 32 && 32 % LPR == 0, "bad column split");
 
     __shared__ float s_q[DK];
     __shared__ float s_k[DK];
     __shared__ float s_a[DK];
-    __shared__ float s_v[DV];
-    __shared__ float s_u[DV];
-    __shared__ float s_red[kWarps][2][DV];
+    __shared__ float s_v[DVS];
+    __shared__ float s_u[DVS];
+    __shared__ float s_red[kWarps][2][DVS];
     __shared__ float s_nrm[DK / 32][3];
     __shared__ float s_beta;
 
@@ -81,8 +84,10 @@ kda_recurrent_kernel(const RecurrentParams p) {
     const int lane = tid & 31;
     const int cg = lane % LPR;
     const int rs = lane / LPR;
-    const int h = blockIdx.x % p.H;
-    const int row = blockIdx.x / p.H;
+    const int split = blockIdx.x % NSPLIT;
+    const int h = (blockIdx.x / NSPLIT) % p.H;
+    const int row = blockIdx.x / (NSPLIT * p.H);
+    const int col0 = split * DVS;
     const int H = p.H;
 
     const T* q = static_cast<const T*>(p.q);
@@ -112,8 +117,8 @@ kda_recurrent_kernel(const RecurrentParams p) {
     }
     if (!valid) {
         // Decode row with an out-of-range slot: state untouched, o = NaN.
-        for (int j = tid; j < DV; j += kThreads) {
-            store_elem(o, ((size_t)bos * H + h) * DV + j, __int_as_float(0x7fc00000));
+        for (int j = tid; j < DVS; j += kThreads) {
+            store_elem(o, ((size_t)bos * H + h) * DV + col0 + j, __int_as_float(0x7fc00000));
         }
         return;
     }
@@ -126,7 +131,7 @@ kda_recurrent_kernel(const RecurrentParams p) {
 #pragma unroll
         for (int r = 0; r < RPT; ++r) {
             const int i = r * RSTEP + w * RPW + rs;
-            S[r] = __ldcs(sp + (i * DV) / 4 + cg);
+            S[r] = __ldcs(sp + (i * DV + col0) / 4 + cg);
         }
     } else {
 #pragma unroll
@@ -160,9 +165,9 @@ kda_recurrent_kernel(const RecurrentParams p) {
                 s_nrm[w][1] = sk;
                 s_nrm[w][2] = sqk;
             }
-        } else if (tid < DK + DV) {
+        } else if (tid < DK + DVS) {
             const int j = tid - DK;
-            s_v[j] = load_elem(v, ((size_t)t * H + h) * DV + j);
+            s_v[j] = load_elem(v, ((size_t)t * H + h) * DV + col0 + j);
             if (j == 0) {
                 s_beta = load_elem(beta, (size_t)t * H + h);
             }
@@ -213,7 +218,7 @@ kda_recurrent_kernel(const RecurrentParams p) {
         __syncthreads();
 
         // ---- stage 3: u and o per value column ----
-        if (tid < DV) {
+        if (tid < DVS) {
             float rkj = 0.f, rqj = 0.f;
 #pragma unroll
             for (int ww = 0; ww < kWarps; ++ww) {
@@ -225,7 +230,7 @@ kda_recurrent_kernel(const RecurrentParams p) {
             const float u = s_beta * (s_v[tid] - rkj);
             s_u[tid] = u;
             const float dot = sqk * inv_k * qscale;  // k_hat . q_hat
-            store_elem(o, ((size_t)t * H + h) * DV + tid, rqj + dot * u);
+            store_elem(o, ((size_t)t * H + h) * DV + col0 + tid, rqj + dot * u);
         }
         __syncthreads();
 
@@ -243,21 +248,27 @@ kda_recurrent_kernel(const RecurrentParams p) {
 #pragma unroll
         for (int r = 0; r < RPT; ++r) {
             const int i = r * RSTEP + w * RPW + rs;
-            __stcs(sp + (i * DV) / 4 + cg, S[r]);
+            __stcs(sp + (i * DV + col0) / 4 + cg, S[r]);
         }
     }
 }
 
+// Value-column split per head: decode of d_v = 128 uses two CTAs per head
+// (half the registers per CTA, twice the state bytes in flight per SM).
+template <int DV>
+constexpr int column_split() { return DV == 128 ? 2 : 1; }
+
 template <int DK, int DV>
 cudaError_t launch_dims(const RecurrentParams& p, int dtype, cudaStream_t stream) {
-    const dim3 grid((unsigned)((int64_t)p.rows * p.H));
+    constexpr int NS = column_split<DV>();
+    const dim3 grid((unsigned)((int64_t)p.rows * p.H * NS));
     if (grid.x == 0) {
         return cudaSuccess;
     }
     if (dtype == 0) {
-        kda_recurrent_kernel<DK, DV, float><<<grid, kThreads, 0, stream>>>(p);
+        kda_recurrent_kernel<DK, DV, NS, float><<<grid, kThreads, 0, stream>>>(p);
     } else {
-        kda_recurrent_kernel<DK, DV, __nv_bfloat16><<<grid, kThreads, 0, stream>>>(p);
+        kda_recurrent_kernel<DK, DV, NS, __nv_bfloat16><<<grid, kThreads, 0, stream>>>(p);
     }
     return cudaGetLastError();
 }
