@@ -165,6 +165,34 @@ KDA_API int kda_state_io(kda_state_op op, float* dst, const float* src,
                  const int32_t* slots, int32_t n, int32_t pool_size,
                  int32_t H, int32_t d_k, int32_t d_v, void* stream);
 
+/*
+ * kda_prefill_noalloc -- kda_prefill without a caller-provided workspace.
+ *
+ * The pages have no counterpart to this call.  It exists for callers that
+ * are not allowed to allocate device memory themselves -- for example a
+ * plugin inside a host framework that owns all device memory and passes the
+ * plugin only its inputs and outputs, or a latency-critical loop that must
+ * not call into the CUDA allocator after start-up.  It allocates nothing:
+ * the workspace kda_prefill needs comes from a fixed array of
+ * 256 + 16384 * 4 bytes in the library's own device memory, held by every
+ * GPU that loads the library until the process exits.
+ *
+ * Arguments, layouts and results are those of kda_prefill.  Sizes whose
+ * workspace would exceed the array (N * H > 16384 (sequence, head) pairs)
+ * return KDA_ERR_WORKSPACE without launching.  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress, with that
+ * device current), so make that first call before any stream capture.
+ * Every call shares the one array: calls that overlap on the GPU (other
+ * streams, other threads) race on it.  The status word in the array is
+ * cleared by each call.
+ */
+KDA_API int kda_prefill_noalloc(const void* q, const void* k, const void* v, const void* z,
+                                const void* beta, const float* A, const float* initial_state,
+                                const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                                int32_t N, int32_t total_T, int32_t H, int32_t d_k, int32_t d_v,
+                                kda_dtype dt, float scale, uint32_t flags,
+                                void* o, float* final_state, void* stream);
+
 /* Human-readable name of a kda_status value (static storage). */
 KDA_API const char* kda_status_string(int status);
 

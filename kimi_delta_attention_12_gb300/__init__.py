@@ -45,6 +45,7 @@ KDA_STATE_SCATTER = 3
 EXPORTED_SYMBOLS = (
     "kda_prefill_workspace_bytes", "kda_prefill", "kda_workspace_status",
     "kda_decode_step", "kda_state_io", "kda_status_string", "kda_version",
+    "kda_prefill_noalloc",
 )
 
 _lock = threading.Lock()
@@ -86,6 +87,10 @@ def lib() -> ctypes.CDLL:
             L.kda_status_string.argtypes = [ctypes.c_int]
             L.kda_version.restype = ctypes.c_int
             L.kda_version.argtypes = []
+            L.kda_prefill_noalloc.restype = ctypes.c_int
+            L.kda_prefill_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                              i32, i32, i32, i32, i32, ctypes.c_int, f32, u32,
+                                              vp, vp, vp]
             _lib = L
     return _lib
 
