@@ -277,13 +277,13 @@ def kda_arm(args, world, rank, local, pg):
                   achieved_gbs, achieved_tf, clk, launches_per_step, pg)
 
 
-def run_decode(dev, rank, local, stream):
+def run_decode(dev, rank, local, stream, batch=None):
     """64 consecutive decode steps on a resident B=256, H=96, d=128 fp32 state."""
     import torch
     import kimi_delta_attention_12_gb300 as kda
     D = DECODE_SHAPE
     g = torch.Generator(device=dev).manual_seed(1000 + rank)
-    Bd, Hd, dd = D["B"], D["H"], D["d"]
+    Bd, Hd, dd = batch or D["B"], D["H"], D["d"]
     state = 0.02 * torch.randn(Bd, Hd, dd, dd, device=dev, generator=g)
     Adec = 0.5 * torch.randn(Hd, device=dev, generator=g)
     unit = lambda t: t / t.norm(dim=-1, keepdim=True)
@@ -314,9 +314,10 @@ def run_decode(dev, rank, local, stream):
 
 
 def decode_only(args, rank, local, dev, stream, peaks):
-    dec_ms, dec_bytes, dec_gbs, clk = run_decode(dev, rank, local, stream)
+    dec_ms, dec_bytes, dec_gbs, clk = run_decode(dev, rank, local, stream, args.decode_batch)
     if rank == 0:
-        print(json.dumps({"only": "decode", "value": dec_gbs, "unit": "GB/s", "ms_per_step": dec_ms,
+        print(json.dumps({"only": "decode", "batch": args.decode_batch, "value": dec_gbs,
+                          "unit": "GB/s", "ms_per_step": dec_ms,
                           "frac": dec_gbs / peaks["hbm_gbs"], "clocks": clk}), flush=True)
 
 
@@ -412,6 +413,8 @@ def main():
     ap.add_argument("--impl", choices=["kda", "reference"], default="kda")
     ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
                     help="run one part only (for profiler captures); the default runs all")
+    ap.add_argument("--decode-batch", type=int, default=DECODE_SHAPE["B"],
+                    help="decode batch for --only decode (smaller cases for profiler captures)")
     args = ap.parse_args()
     world, rank, local, pg = _dist_setup(args)
     try:

@@ -53,7 +53,7 @@ using namespace sm103;
 
 constexpr int C = 64;          // chunk length
 constexpr int D = 128;         // head dim (d_k = d_v)
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNormEps = 1e-6f;
 constexpr int kStatusTimeout = 1;
@@ -96,7 +96,7 @@ constexpr uint32_t TM_G1 = 128;   // Gram blocks 3, 2
 constexpr uint32_t TM_G2 = 192;   // Gram blocks 1, 0
 constexpr uint32_t TM_W = 256;    // W^T  [128 c][64 r]
 constexpr uint32_t TM_U = 320;    // U^T  [128 j][64 r]
-constexpr uint32_t TM_O = 384;    // O^T  [128 j][64 r]
+constexpr uint32_t TM_O = 384;    // O    [64 r][128 j]  (M = 64 layout)
 constexpr uint32_t TMEM_COLS = 512;
 
 struct ChunkedArgs {
@@ -128,11 +128,18 @@ __device__ __forceinline__ void store_row16(uint8_t* tile, uint32_t row, uint32_
     *reinterpret_cast<uint4*>(tile + sw128(row, byte0 + 16)) = b;
 }
 
-__device__ __forceinline__ float gate_log2(float eA, float z) {
-    // g = -5 sigmoid(e^A z), returned in log2 units (g * log2 e)
-    const float y = eA * z;
-    const float s = __fdividef(1.0f, 1.0f + exp2f(-y * kLog2e));
-    return -5.0f * kLog2e * s;
+// 2^x and 1/x with the hardware approximations (ex2.approx handles subnormal
+// results, so decay factors down to 2^-149 are kept).
+__device__ __forceinline__ float exp2_approx(float x) {
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // ---- UT-solve helpers: warp-level 16x16x16 products on fp32 [..][65] tiles ----
@@ -218,6 +225,9 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
+    const int qd = warp & 3;           // TMEM lane quadrant this warp may access
+    const int sub = warp >> 2;         // 0..3: which of the four warps of that quadrant
+    const uint32_t lane_base = (uint32_t)(32 * qd) << 16;
     const int H = p.H;
     const int unit = blockIdx.x;
     const int n = unit / H;
@@ -253,26 +263,27 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
     const uint32_t tbase = tmem_base_s;
     const uint32_t smem_base = smem_u32(sm);
 
-    // ---- initial state -> TMEM: thread j (warps 0..3) owns lane j = column j of S ----
-    if (warp < 4) {
-        const int j = tid;
-        const uint32_t taddr = tbase + ((uint32_t)(32 * warp) << 16) + TM_S;
-        for (int c0 = 0; c0 < D; c0 += 16) {
+    // ---- initial state -> TMEM: lane j holds column j of S (S^T row j) ----
+    {
+        const int j = 32 * qd + lane;
+        const uint32_t taddr = tbase + lane_base + TM_S;
+#pragma unroll 1
+        for (int cb = 32 * sub; cb < 32 * sub + 32; cb += 16) {
             uint32_t r[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const float x = p.initial_state
-                                    ? __ldg(p.initial_state + state_off + (size_t)(c0 + i) * D + j)
+                                    ? __ldg(p.initial_state + state_off + (size_t)(cb + i) * D + j)
                                     : 0.0f;
                 r[i] = __float_as_uint(x);
             }
-            tmem_st16(taddr + c0, r);
+            tmem_st16(taddr + cb, r);
         }
         tmem_wait_st();
     }
     cta_sync_tc();
 
-    const float eA = expf(p.A[h]);
+    const float eA_log2 = exp2_approx(p.A[h] * kLog2e) * kLog2e;  // e^A log2(e)
     const __nv_bfloat16* beta_g = static_cast<const __nv_bfloat16*>(p.beta);
     __nv_bfloat16* o_g = static_cast<__nv_bfloat16*>(p.o);
 
@@ -293,6 +304,11 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
         tma_load_3d(sm + OFF_V, &args.tm_v, 0, h, (int)bos, &bar_v);
         tma_load_3d(sm + OFF_V + 8192, &args.tm_v, 64, h, (int)bos, &bar_v);
     }
+    // beta of the next chunk is fetched one chunk ahead into a register
+    float beta_next = 0.0f;
+    if (tid < C && tid < len) {
+        beta_next = __bfloat162float(beta_g[(size_t)(bos + tid) * H + h]);
+    }
 
     for (int ci = 0; ci < nchunks; ++ci) {
         const int64_t t0 = bos + (int64_t)ci * C;
@@ -303,7 +319,11 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
 
         // ---------------- P0: this chunk's raw tiles (issued one chunk ahead) ----------------
         if (tid < C) {
-            s_beta[tid] = tid < L ? __bfloat162float(beta_g[(size_t)(t0 + tid) * H + h]) : 0.0f;
+            s_beta[tid] = beta_next;
+            beta_next = 0.0f;
+            if (has_next && t_next + tid < eos) {
+                beta_next = __bfloat162float(beta_g[(size_t)(t_next + tid) * H + h]);
+            }
         }
         if (mbar_wait(&bar_raw, ph_raw, &abort_flag)) {
             ph_raw ^= 1;
@@ -316,65 +336,69 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
             break;
         }
 
-        // ---------------- P1a: per-token L2 norms ----------------
+        // ---------------- P1a: per-token L2 norms (4 tokens per warp) ----------------
         {
             const uint8_t* rq = sm + OFF_RAWQ;
             const uint8_t* rk = sm + OFF_RAWK;
+            float sq[4], sk[4];
 #pragma unroll
-            for (int tt = 0; tt < 8; ++tt) {
-                const int r = warp * 8 + tt;
+            for (int tt = 0; tt < 4; ++tt) {
+                const int r = warp * 4 + tt;
                 const uint2 qv = *reinterpret_cast<const uint2*>(rq + r * 256 + lane * 8);
                 const uint2 kv = *reinterpret_cast<const uint2*>(rk + r * 256 + lane * 8);
-                float q0 = bf16lo(qv.x), q1 = bf16hi(qv.x), q2 = bf16lo(qv.y), q3 = bf16hi(qv.y);
-                float k0 = bf16lo(kv.x), k1 = bf16hi(kv.x), k2 = bf16lo(kv.y), k3 = bf16hi(kv.y);
-                float sq = q0 * q0 + q1 * q1 + q2 * q2 + q3 * q3;
-                float sk = k0 * k0 + k1 * k1 + k2 * k2 + k3 * k3;
+                const float q0 = bf16lo(qv.x), q1 = bf16hi(qv.x), q2 = bf16lo(qv.y), q3 = bf16hi(qv.y);
+                const float k0 = bf16lo(kv.x), k1 = bf16hi(kv.x), k2 = bf16lo(kv.y), k3 = bf16hi(kv.y);
+                sq[tt] = q0 * q0 + q1 * q1 + q2 * q2 + q3 * q3;
+                sk[tt] = k0 * k0 + k1 * k1 + k2 * k2 + k3 * k3;
+            }
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    sq += __shfl_xor_sync(0xffffffffu, sq, off);
-                    sk += __shfl_xor_sync(0xffffffffu, sk, off);
+            for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+                for (int tt = 0; tt < 4; ++tt) {
+                    sq[tt] += __shfl_xor_sync(0xffffffffu, sq[tt], off);
+                    sk[tt] += __shfl_xor_sync(0xffffffffu, sk[tt], off);
                 }
-                if (lane == 0) {
-                    const bool valid = r < L;
-                    s_invq[r] = valid ? (p.l2norm ? rsqrtf(sq + kNormEps) : 1.0f) * p.scale : 0.0f;
-                    s_invk[r] = valid ? (p.l2norm ? rsqrtf(sk + kNormEps) : 1.0f) : 0.0f;
-                }
+            }
+            if (lane < 4) {
+                const int r = warp * 4 + lane;
+                const float a = lane == 0 ? sq[0] : lane == 1 ? sq[1] : lane == 2 ? sq[2] : sq[3];
+                const float b = lane == 0 ? sk[0] : lane == 1 ? sk[1] : lane == 2 ? sk[2] : sk[3];
+                const bool valid = r < L;
+                s_invq[r] = valid ? (p.l2norm ? rsqrtf(a + kNormEps) : 1.0f) * p.scale : 0.0f;
+                s_invk[r] = valid ? (p.l2norm ? rsqrtf(b + kNormEps) : 1.0f) : 0.0f;
             }
         }
         __syncthreads();
 
-        // ---------------- P1b: gate, cumulative decay inside the 16-token block ----------------
-        const int cp = tid & 63;       // channel pair: channels 2cp, 2cp+1
-        const int ab = tid >> 6;       // token block: tokens 16ab .. 16ab+15
-        const int c0 = 2 * cp;
-        uint32_t qp[16], kp[16];
-        float al0[16], al1[16];        // per-token decay alpha = e^g of the two channels
+        // ---------------- P1b: gate and per-token decay (one channel, 16 tokens per thread) ----------------
+        const int c = tid & (D - 1);   // channel
+        const int ab = tid >> 7;       // token block: tokens 16ab .. 16ab+15
+        float qh[16], kh[16], al[16];
         {
-            float a0 = 0.f, a1 = 0.f;  // block totals of g, log2 units
+            float tot = 0.f;           // block total of g, log2 units
 #pragma unroll
             for (int rr = 0; rr < 16; ++rr) {
                 const int r = 16 * ab + rr;
-                qp[rr] = *reinterpret_cast<const uint32_t*>(sm + OFF_RAWQ + r * 256 + 4 * cp);
-                kp[rr] = *reinterpret_cast<const uint32_t*>(sm + OFF_RAWK + r * 256 + 4 * cp);
-                const uint32_t zp = *reinterpret_cast<const uint32_t*>(sm + OFF_RAWZ + r * 256 + 4 * cp);
-                const bool valid = r < L;
-                const float g0 = valid ? gate_log2(eA, bf16lo(zp)) : 0.0f;
-                const float g1 = valid ? gate_log2(eA, bf16hi(zp)) : 0.0f;
-                a0 += g0;
-                a1 += g1;
-                al0[rr] = exp2f(g0);
-                al1[rr] = exp2f(g1);
+                const float qv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                    sm + OFF_RAWQ + r * 256 + 2 * c));
+                const float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                    sm + OFF_RAWK + r * 256 + 2 * c));
+                const float zv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                    sm + OFF_RAWZ + r * 256 + 2 * c));
+                // g = -5 sigmoid(e^A z) in log2 units; invalid tokens: g = 0
+                const float sg = rcp_approx(1.0f + exp2_approx(-eA_log2 * zv));
+                const float g = r < L ? -5.0f * kLog2e * sg : 0.0f;
+                tot += g;
+                al[rr] = exp2_approx(g);
+                qh[rr] = qv * s_invq[r];
+                kh[rr] = kv * s_invk[r];
             }
-            s_tot[ab * D + c0] = a0;
-            s_tot[ab * D + c0 + 1] = a1;
+            s_tot[ab * D + c] = tot;
         }
         __syncthreads();
 
         // ---------------- P1c: operand tiles ----------------
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int c = c0 + half;
-            const float* alv = half ? al1 : al0;
+        {
             float t[4];
 #pragma unroll
             for (int b = 0; b < 4; ++b) t[b] = s_tot[b * D + c];
@@ -383,71 +407,65 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
 #pragma unroll
             for (int b = 0; b < 4; ++b) rho[b + 1] = rho[b] + t[b];
             if (ab == 0) {
-                s_gam[c] = exp2f(rho[4]);
+                s_gam[c] = exp2_approx(rho[4]);
             }
             const float rho_a = ab == 0 ? rho[0] : ab == 1 ? rho[1] : ab == 2 ? rho[2] : rho[3];
             const float rho_a1 = ab == 0 ? rho[1] : ab == 1 ? rho[2] : ab == 2 ? rho[3] : rho[4];
-            const float tot_a = rho_a1 - rho_a;
-            const float eRa = exp2f(rho_a);               // e^{rho_a}          <= 1
-            const float cF = exp2f(-tot_a);               // e^{-block total}   <= e^80
-            const float eEnd = exp2f(rho[4] - rho_a1);    // e^{gamma_C - rho_{a+1}} <= 1
+            const float eRa = exp2_approx(rho_a);               // e^{rho_a}          <= 1
+            const float cF = exp2_approx(rho_a - rho_a1);       // e^{-block total}   <= e^80
+            const float eEnd = exp2_approx(rho[4] - rho_a1);    // e^{gamma_C - rho_{a+1}} <= 1
 
             // In-block decay factors as running products of alpha:
             //   E_r = e^{gamma_r - rho_a}      = prod_{t<=r} alpha_t        in [e^-80, 1]
             //   G_r = e^{rho_{a+1} - gamma_r}  = prod_{t>r, t in block}     in [e^-80, 1]
             //   F_r = e^{rho_a - gamma_r}      = G_r e^{-block total}       in [1, e^80]
             float E[16], G[16];
-            E[0] = alv[0];
+            E[0] = al[0];
 #pragma unroll
-            for (int rr = 1; rr < 16; ++rr) E[rr] = E[rr - 1] * alv[rr];
+            for (int rr = 1; rr < 16; ++rr) E[rr] = E[rr - 1] * al[rr];
             G[15] = 1.0f;
 #pragma unroll
-            for (int rr = 14; rr >= 0; --rr) G[rr] = G[rr + 1] * alv[rr + 1];
+            for (int rr = 14; rr >= 0; --rr) G[rr] = G[rr + 1] * al[rr + 1];
 
-            float xq[16], xk[16], kown[16], kg[16];
-#pragma unroll
-            for (int rr = 0; rr < 16; ++rr) {
-                const int r = 16 * ab + rr;
-                const float qv = (half ? bf16hi(qp[rr]) : bf16lo(qp[rr])) * s_invq[r];
-                const float kv = (half ? bf16hi(kp[rr]) : bf16lo(kp[rr])) * s_invk[r];
-                xq[rr] = qv * E[rr];
-                xk[rr] = kv * E[rr];
-                kg[rr] = kv * G[rr];                      // k e^{rho_{a+1} - gamma_r} <= 1
-                kown[rr] = kg[rr] * cF;                   // k e^{rho_a - gamma_r}
-            }
+            float v[16];
             // X~ : Gram B operand; N-block 0 = [Q3 K3 Q2 K2], N-block 1 = [Q1 K1 Q0 K0]
-            {
-                const uint32_t nb = ab >= 2 ? 0u : 1u;
-                const uint32_t e0 = (ab >= 2 ? (3 - ab) : (1 - ab)) * 32;
-                uint8_t* xt = sm + OFF_XT + nb * 16384;
-                store_row16(xt, c, 2 * e0, xq);
-                store_row16(xt, c, 2 * (e0 + 16), xk);
-            }
-            // K~^(a') for a' >= ab: M-block (3 - a') of the Gram A operand
-            store_row16(sm + OFF_KT + (3 - ab) * 16384, c, 32 * ab, kown);
+            const uint32_t nb = ab >= 2 ? 0u : 1u;
+            const uint32_t e0 = (ab >= 2 ? (3 - ab) : (1 - ab)) * 32;
+            uint8_t* xt = sm + OFF_XT + nb * 16384;
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) v[rr] = qh[rr] * E[rr];
+            store_row16(xt, c, 2 * e0, v);
+            // Q+ = q e^{gamma} = (q e^{gamma - rho_a}) e^{rho_a}
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) v[rr] *= eRa;
+            store_row16(sm + OFF_QP, c, 32 * ab, v);
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) v[rr] = kh[rr] * E[rr];
+            store_row16(xt, c, 2 * (e0 + 16), v);
+            // K+ = k e^{gamma}
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) v[rr] *= eRa;
+            store_row16(sm + OFF_KP, c, 32 * ab, v);
+            // key side with the end-of-block reference: k e^{rho_{a+1} - gamma_r} <= 1
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) G[rr] *= kh[rr];
+            // Kend = k e^{gamma_C - gamma}
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) v[rr] = G[rr] * eEnd;
+            store_row16(sm + OFF_KE, c, 32 * ab, v);
+            // K~^(ab) = k e^{rho_a - gamma}: M-block (3 - ab) of the Gram A operand
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) v[rr] = G[rr] * cF;
+            store_row16(sm + OFF_KT + (3 - ab) * 16384, c, 32 * ab, v);
+            // K~^(a') for a' > ab: k e^{rho_{a'} - gamma} = (k e^{rho_{a+1} - gamma}) e^{rho_{a'} - rho_{a+1}}
 #pragma unroll
             for (int ap = 1; ap < 4; ++ap) {
                 if (ap > ab) {
-                    // e^{rho_{a'} - rho_{a+1}} <= 1
-                    const float f = exp2f((ap == 1 ? rho[1] : ap == 2 ? rho[2] : rho[3]) - rho_a1);
-                    float v[16];
+                    const float f = exp2_approx((ap == 1 ? rho[1] : ap == 2 ? rho[2] : rho[3]) - rho_a1);
 #pragma unroll
-                    for (int rr = 0; rr < 16; ++rr) v[rr] = kg[rr] * f;
+                    for (int rr = 0; rr < 16; ++rr) v[rr] = G[rr] * f;
                     store_row16(sm + OFF_KT + (3 - ap) * 16384, c, 32 * ab, v);
                 }
-            }
-            // K+ = k e^{gamma}, Q+ = q e^{gamma}, Kend = k e^{gamma_C - gamma}
-            {
-                float v[16];
-#pragma unroll
-                for (int rr = 0; rr < 16; ++rr) v[rr] = xk[rr] * eRa;
-                store_row16(sm + OFF_KP, c, 32 * ab, v);
-#pragma unroll
-                for (int rr = 0; rr < 16; ++rr) v[rr] = xq[rr] * eRa;
-                store_row16(sm + OFF_QP, c, 32 * ab, v);
-#pragma unroll
-                for (int rr = 0; rr < 16; ++rr) v[rr] = kg[rr] * eEnd;
-                store_row16(sm + OFF_KE, c, 32 * ab, v);
             }
         }
         fence_proxy_async();
@@ -485,44 +503,53 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
         }
 
         // ---------------- P3: Gram -> Akk (fp32), Aqk (bf16);  S^T -> bf16, S^T *= Gamma ----------------
-        if (warp < 4) {
-            const int q4 = warp;
-            const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+        if (warp < 8) {
+            // warps 0-3: Gram blocks 3 (lanes 0-63) and 2 (lanes 64-127) in TM_G1;
+            // warps 4-7: Gram blocks 1 and 0 in TM_G2
+            const int g = warp >> 2;
             float* akk = reinterpret_cast<float*>(sm + OFF_AKK);
+            const int blk = g == 0 ? (qd < 2 ? 3 : 2) : (qd < 2 ? 1 : 0);
+            const uint32_t col = (g == 0 ? TM_G1 : TM_G2) + (qd < 2 ? 0 : 32);
+            const int i = (qd < 2 ? 32 * qd : 32 * (qd - 2)) + lane;
+            uint32_t vq[16], vk[16];
+            tmem_ld16(tbase + lane_base + col, vq);
+            tmem_ld16(tbase + lane_base + col + 16, vk);
+            tmem_wait_ld();
 #pragma unroll
-            for (int g = 0; g < 2; ++g) {
-                const int blk = g == 0 ? (q4 < 2 ? 3 : 2) : (q4 < 2 ? 1 : 0);
-                const uint32_t col = (g == 0 ? TM_G1 : TM_G2) + (q4 < 2 ? 0 : 32);
-                const int i = (q4 < 2 ? 32 * q4 : 32 * (q4 - 2)) + lane;
-                uint32_t vq[16], vk[16];
-                tmem_ld16(tbase + lane_base + col, vq);
-                tmem_ld16(tbase + lane_base + col + 16, vk);
-                tmem_wait_ld();
-#pragma unroll
-                for (int rr = 0; rr < 16; ++rr) {
-                    const int r = 16 * blk + rr;
-                    const float aq = i <= r ? __uint_as_float(vq[rr]) : 0.0f;
-                    const float ak = i < r ? s_beta[r] * __uint_as_float(vk[rr]) : 0.0f;
-                    akk[r * 65 + i] = ak;
-                    *reinterpret_cast<__nv_bfloat16*>(sm + OFF_AQK + sw128(r, 2 * i)) =
-                        __float2bfloat16_rn(aq);
-                }
+            for (int rr = 0; rr < 16; ++rr) {
+                const int r = 16 * blk + rr;
+                const float aq = i <= r ? __uint_as_float(vq[rr]) : 0.0f;
+                const float ak = i < r ? s_beta[r] * __uint_as_float(vk[rr]) : 0.0f;
+                akk[r * 65 + i] = ak;
+                *reinterpret_cast<__nv_bfloat16*>(sm + OFF_AQK + sw128(r, 2 * i)) =
+                    __float2bfloat16_rn(aq);
             }
         } else {
-            const int j = tid - 128;
-            const uint32_t taddr = tbase + ((uint32_t)(32 * (warp - 4)) << 16) + TM_S;
+            // warps 8-15: S^T row j = lane, columns [64 half, 64 half + 64)
+            const int j = 32 * qd + lane;
+            const int half = sub - 2;
+            const uint32_t taddr = tbase + lane_base + TM_S;
 #pragma unroll 1
-            for (int cb = 0; cb < D; cb += 16) {
-                uint32_t r[16];
-                tmem_ld16(taddr + cb, r);
+            for (int cb = 64 * half; cb < 64 * half + 64; cb += 32) {
+                uint32_t r0[16], r1[16];
+                tmem_ld16(taddr + cb, r0);
+                tmem_ld16(taddr + cb + 16, r1);
                 tmem_wait_ld();
-                float v[16];
+                float v0[16], v1[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-                store_row16(sm + OFF_ST + (cb / 64) * 16384, j, 2 * (cb % 64), v);
+                for (int i = 0; i < 16; ++i) {
+                    v0[i] = __uint_as_float(r0[i]);
+                    v1[i] = __uint_as_float(r1[i]);
+                }
+                store_row16(sm + OFF_ST + half * 16384, j, 2 * (cb % 64), v0);
+                store_row16(sm + OFF_ST + half * 16384, j, 2 * (cb % 64) + 32, v1);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(v[i] * s_gam[cb + i]);
-                tmem_st16(taddr + cb, r);
+                for (int i = 0; i < 16; ++i) {
+                    r0[i] = __float_as_uint(v0[i] * s_gam[cb + i]);
+                    r1[i] = __float_as_uint(v1[i] * s_gam[cb + 16 + i]);
+                }
+                tmem_st16(taddr + cb, r0);
+                tmem_st16(taddr + cb + 16, r1);
             }
             tmem_wait_st();
         }
@@ -560,8 +587,8 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
                 if (warp < 4 - wave) {
                     const int a = warp + wave, b = a - wave;
                     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                    for (int c = b; c < a; ++c) {
-                        warp_gemm16(acc, Lm, 16 * a, 16 * c, Nm, 16 * c, 16 * b, lane);
+                    for (int cc = b; cc < a; ++cc) {
+                        warp_gemm16(acc, Lm, 16 * a, 16 * cc, Nm, 16 * cc, 16 * b, lane);
                     }
                     warp_store16(acc, Ms, 16 * warp, 0, 1.0f, lane);
                     __syncwarp();
@@ -572,10 +599,8 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
                 __syncthreads();
             }
             // Tm[r][i] = N[r][i] beta_i (lower triangle), bf16, rows of 64 -> K-major B tile
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int chunk = tid + e * kThreads;  // 512 chunks of 8 values
-                const int r = chunk >> 3, i0 = (chunk & 7) * 8;
+            {
+                const int r = tid >> 3, i0 = (tid & 7) * 8;  // 512 chunks of 8 values
                 uint4 w;
                 float v[8];
 #pragma unroll
@@ -627,36 +652,36 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
             tma_load_3d(sm + OFF_V + 8192, &args.tm_v, 64, h, t_next, &bar_v);
         }
 
-        // ---------------- P6: W^T -> bf16 operand (row c = lane) ----------------
-        if (warp < 4) {
-            const int c = tid;
-            const uint32_t taddr = tbase + ((uint32_t)(32 * warp) << 16) + TM_W;
+        // ---------------- P6: W^T -> bf16 operand (row c = lane, 16 tokens per warp) ----------------
+        {
+            uint32_t r[16];
+            tmem_ld16(tbase + lane_base + TM_W + 16 * sub, r);
+            tmem_wait_ld();
+            float v[16];
 #pragma unroll
-            for (int cb = 0; cb < C; cb += 16) {
-                uint32_t r[16];
-                tmem_ld16(taddr + cb, r);
-                tmem_wait_ld();
-                float v[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-                store_row16(sm + OFF_WT, c, 2 * cb, v);
-            }
+            for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+            store_row16(sm + OFF_WT, 32 * qd + lane, 32 * sub, v);
         }
         fence_proxy_async();
         cta_sync_tc();
 
-        // ---------------- P7: U^T += S^T (-W^T),  O^T = S^T Q+^T ----------------
+        // ---------------- P7: U^T += S^T (-W^T),  O = Q+ S ----------------
         if (tid == 0) {
             const uint32_t idu = idesc_bf16(128, 64, 0, 1, /*neg_b=*/1);
-            const uint32_t ido = idesc_bf16(128, 64, 0, 1);
+            const uint32_t ido = idesc_bf16(64, 128, 1, 0);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const uint64_t aS =
                     smem_desc(smem_base + OFF_ST + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
                 const uint64_t bW = smem_desc(smem_base + OFF_WT + kk * 2048, 16384, 1024);
                 mma_bf16(tbase + TM_U, aS, bW, idu, 1);
-                const uint64_t bQ = smem_desc(smem_base + OFF_QP + kk * 2048, 16384, 1024);
-                mma_bf16(tbase + TM_O, aS, bQ, ido, kk > 0);
+            }
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t aQ = smem_desc(smem_base + OFF_QP + kk * 2048, 16384, 1024);
+                const uint64_t bS =
+                    smem_desc(smem_base + OFF_ST + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                mma_bf16(tbase + TM_O, aQ, bS, ido, kk > 0);
             }
             mma_commit(&bar_mma);
         }
@@ -670,33 +695,29 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
             break;
         }
 
-        // ---------------- P8: U^T -> bf16 operand (row j = lane) ----------------
-        if (warp < 4) {
-            const int j = tid;
-            const uint32_t taddr = tbase + ((uint32_t)(32 * warp) << 16) + TM_U;
+        // ---------------- P8: U^T -> bf16 operand (row j = lane, 16 tokens per warp) ----------------
+        {
+            uint32_t r[16];
+            tmem_ld16(tbase + lane_base + TM_U + 16 * sub, r);
+            tmem_wait_ld();
+            float v[16];
 #pragma unroll
-            for (int cb = 0; cb < C; cb += 16) {
-                uint32_t r[16];
-                tmem_ld16(taddr + cb, r);
-                tmem_wait_ld();
-                float v[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-                store_row16(sm + OFF_UT, j, 2 * cb, v);
-            }
+            for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+            store_row16(sm + OFF_UT, 32 * qd + lane, 32 * sub, v);
         }
         fence_proxy_async();
         cta_sync_tc();
 
-        // ---------------- P9: O^T += U^T Aqk^T,  S^T += U^T Kend ----------------
+        // ---------------- P9: O += Aqk U,  S^T += U^T Kend ----------------
         if (tid == 0) {
-            const uint32_t ido = idesc_bf16(128, 64, 0, 0);
+            const uint32_t ido = idesc_bf16(64, 128, 0, 0);
             const uint32_t ids = idesc_bf16(128, 128, 0, 0);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t aA = smem_desc(smem_base + OFF_AQK + kk * 32, 16, 1024);
+                const uint64_t bU = smem_desc(smem_base + OFF_UT + kk * 32, 16, 1024);
+                mma_bf16(tbase + TM_O, aA, bU, ido, 1);
                 const uint64_t aU = smem_desc(smem_base + OFF_UT + kk * 32, 16, 1024);
-                const uint64_t bA = smem_desc(smem_base + OFF_AQK + kk * 32, 16, 1024);
-                mma_bf16(tbase + TM_O, aU, bA, ido, 1);
                 const uint64_t bK = smem_desc(smem_base + OFF_KE + kk * 32, 16, 1024);
                 mma_bf16(tbase + TM_S, aU, bK, ids, 1);
             }
@@ -712,23 +733,26 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
             break;
         }
 
-        // ---------------- P10: O^T -> o ----------------
-        if (warp < 4) {
-            const int j = tid;
-            const uint32_t taddr = tbase + ((uint32_t)(32 * warp) << 16) + TM_O;
+        // ---------------- P10: O -> o ----------------
+        // O (M = 64 tokens) sits in TMEM lanes 32q .. 32q+15 for tokens
+        // 16q .. 16q+15; each warp stores 32 value columns of its 16 tokens.
+        {
+            uint32_t r0[16], r1[16];
+            tmem_ld16(tbase + lane_base + TM_O + 32 * sub, r0);
+            tmem_ld16(tbase + lane_base + TM_O + 32 * sub + 16, r1);
+            tmem_wait_ld();
+            const int rtok = 16 * qd + lane;
+            if (lane < 16 && rtok < L) {
+                uint4 w[4];
+                uint32_t* wp = reinterpret_cast<uint32_t*>(w);
 #pragma unroll
-            for (int cb = 0; cb < C; cb += 16) {
-                uint32_t r[16];
-                tmem_ld16(taddr + cb, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int rtok = cb + i;
-                    if (rtok < L) {
-                        o_g[((size_t)(t0 + rtok) * H + h) * D + j] =
-                            __float2bfloat16_rn(__uint_as_float(r[i]));
-                    }
+                for (int i = 0; i < 8; ++i) {
+                    wp[i] = pack_bf16x2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
+                    wp[8 + i] = pack_bf16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
                 }
+                uint4* dst = reinterpret_cast<uint4*>(o_g + ((size_t)(t0 + rtok) * H + h) * D + 32 * sub);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) dst[i] = w[i];
             }
         }
         cta_sync_tc();
@@ -743,10 +767,11 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
     }
 
     // ---- final state: TMEM S^T -> final_state (coalesced along j) ----
-    if (!abort_flag && p.final_state && warp < 4) {
-        const int j = tid;
-        const uint32_t taddr = tbase + ((uint32_t)(32 * warp) << 16) + TM_S;
-        for (int cb = 0; cb < D; cb += 16) {
+    if (!abort_flag && p.final_state) {
+        const int j = 32 * qd + lane;
+        const uint32_t taddr = tbase + lane_base + TM_S;
+#pragma unroll 1
+        for (int cb = 32 * sub; cb < 32 * sub + 32; cb += 16) {
             uint32_t r[16];
             tmem_ld16(taddr + cb, r);
             tmem_wait_ld();
