@@ -368,9 +368,11 @@ def finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops
     # CPU baseline: the oracle on a bounded sample of the prefill workload
     cpu_tps, cpu_s, cpu_threads = run_oracle_sample(1024, H, d)
     traffic = None
-    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    prof = os.path.join(ROOT, "profiles", "kda_chunked_prefill_4k.md")
     if os.path.exists(prof):
-        traffic = json.load(open(prof)).get("prefill_bytes_per_launch")
+        for line in open(prof):
+            if line.startswith("| traffic_bytes_per_launch |"):
+                traffic = int(line.split("|")[2].strip())
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
