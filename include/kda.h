@@ -71,10 +71,17 @@ enum {
 #define KDA_DEFAULT_FLAGS KDA_FLAG_L2NORM_QK
 
 /*
- * Bytes of device workspace kda_prefill needs for these sizes (a status word,
- * a work counter and the per-unit schedule).  Always > 0.  The workspace is
- * scratch: its content on entry does not matter and it may be reused by the
- * next call on the same stream.
+ * Bytes of device workspace that let kda_prefill pick its fastest kernel for
+ * these sizes on the current device.  Always > 0 and a multiple of 256.
+ *
+ * Any workspace of at least 256 + 4 * N * H bytes (rounded up to 256) is
+ * accepted.  With bf16, d_k = d_v = 128 and few (sequence, head) pairs (at
+ * most a third of the SMs), a larger workspace -- the size returned here,
+ * about 66 KB per (64-token chunk, head) -- selects the split kernel, which
+ * spreads each pair's chunks over all SMs and stages every chunk's operand
+ * tiles in the workspace; a smaller one selects the single-pass kernel.  The
+ * workspace is scratch: its content on entry does not matter and it may be
+ * reused by the next call on the same stream.
  */
 KDA_API size_t kda_prefill_workspace_bytes(int32_t N, int32_t total_T, int32_t H,
                                    int32_t d_k, int32_t d_v, kda_dtype dt);
@@ -98,11 +105,12 @@ KDA_API size_t kda_prefill_workspace_bytes(int32_t N, int32_t total_T, int32_t H
  *  o              [total_T, H, d_v]  dt, output (o_t for every token)
  *  final_state    [N, H, d_k, d_v] fp32, or NULL.  May alias initial_state
  *                 (in-place update is allowed).
- *  workspace      device scratch of at least kda_prefill_workspace_bytes()
+ *  workspace      device scratch, 256-byte aligned; see kda_prefill_workspace_bytes()
  *
  * A zero-length sequence returns final_state = initial_state (or zeros).
- * bf16 with d_k = d_v = 128 runs the tcgen05/TMEM chunked kernel; every other
- * size/dtype runs the fused recurrent kernel (fp32 arithmetic throughout).
+ * bf16 with d_k = d_v = 128 runs a tcgen05/TMEM chunked kernel (single-pass,
+ * or split when the workspace allows it; both give bit-identical results);
+ * every other size/dtype runs the fused recurrent kernel (fp32 arithmetic).
  */
 KDA_API int kda_prefill(const void* q, const void* k, const void* v, const void* z,
                 const void* beta, const float* A, const float* initial_state,

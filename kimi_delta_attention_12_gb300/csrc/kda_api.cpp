@@ -28,7 +28,35 @@ constexpr size_t kWsHeader = 256;
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Minimum workspace: the header and one int per (sequence, head) unit.
+size_t basic_workspace_bytes(int32_t N, int32_t H) {
+    const size_t units = (N > 0 && H > 0) ? (size_t)N * (size_t)H : 0;
+    return kWsHeader + round_up(units * sizeof(int32_t), 256);
+}
+
+// SMs of the current device, 0 if there is none.
+int current_sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return sms;
+}
+
+// Few (sequence, head) units leave most SMs idle in the single-pass kernel;
+// the split kernel spreads each unit's chunks over producer CTAs.
+bool split_eligible(int32_t N, int32_t H, kda_dtype dt, int32_t d_k, int32_t d_v, int sms) {
+    return dt == KDA_BF16 && d_k == 128 && d_v == 128 && sms > 0 &&
+           (int64_t)N * H <= kda::split_max_units(sms);
+}
+
 }  // namespace
+
+namespace kda {
+size_t min_prefill_workspace_bytes(int32_t N, int32_t H) { return basic_workspace_bytes(N, H); }
+}  // namespace kda
 
 extern "C" {
 
@@ -49,9 +77,12 @@ int kda_version(void) { return 100; }
 
 size_t kda_prefill_workspace_bytes(int32_t N, int32_t total_T, int32_t H, int32_t d_k,
                                    int32_t d_v, kda_dtype dt) {
-    (void)total_T; (void)d_k; (void)d_v; (void)dt;
-    const size_t units = (N > 0 && H > 0) ? (size_t)N * (size_t)H : 0;
-    return kWsHeader + round_up(units * sizeof(int32_t), 256);
+    const size_t basic = basic_workspace_bytes(N, H);
+    if (N > 0 && H > 0 && total_T > 0 && split_eligible(N, H, dt, d_k, d_v, current_sm_count())) {
+        const size_t split = kda::split_workspace_bytes(N, total_T, H);
+        return split > basic ? split : basic;
+    }
+    return basic;
 }
 
 int kda_workspace_status(const void* workspace, void* stream) {
@@ -90,7 +121,7 @@ int kda_prefill(const void* q, const void* k, const void* v, const void* z,
             if (cu_seqlens_host[n + 1] < cu_seqlens_host[n]) return KDA_ERR_INVALID_ARG;
         }
     }
-    if (!workspace || workspace_bytes < kda_prefill_workspace_bytes(N, total_T, H, d_k, d_v, dt)) {
+    if (!workspace || workspace_bytes < basic_workspace_bytes(N, H)) {
         return KDA_ERR_WORKSPACE;
     }
     const size_t eb = elem_bytes(dt);
@@ -117,7 +148,16 @@ int kda_prefill(const void* q, const void* k, const void* v, const void* z,
         p.status = ws; p.work_counter = ws + 1; p.schedule = nullptr;
         p.N = N; p.total_T = total_T; p.H = H; p.scale = scale;
         p.l2norm = (flags & KDA_FLAG_L2NORM_QK) ? 1 : 0;
-        err = kda::launch_chunked_prefill(p, s);
+        const int sms = current_sm_count();
+        if (split_eligible(N, H, dt, d_k, d_v, sms) &&
+            workspace_bytes >= kda::split_workspace_bytes(N, total_T, H)) {
+            uint8_t* wsb = static_cast<uint8_t*>(workspace);
+            p.flags = reinterpret_cast<int32_t*>(wsb + 256);
+            p.handoff = wsb + kda::split_handoff_offset(N, total_T, H);
+            err = kda::launch_split_prefill(p, sms, s);
+        } else {
+            err = kda::launch_chunked_prefill(p, s);
+        }
     } else {
         kda::RecurrentParams p;
         memset(&p, 0, sizeof(p));

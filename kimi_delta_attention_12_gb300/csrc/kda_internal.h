@@ -66,6 +66,8 @@ struct ChunkedParams {
     int32_t* status;             // device status word (workspace)
     int32_t* work_counter;       // device work counter (workspace)
     const int32_t* schedule;     // optional device list of unit ids (workspace), or null
+    int32_t* flags;              // split mode: one ready flag per (chunk, head) slot
+    uint8_t* handoff;            // split mode: one published chunk per slot
     int32_t N;
     int32_t total_T;
     int32_t H;
@@ -76,8 +78,19 @@ struct ChunkedParams {
 // True once the chunked kernel is compiled into the library.
 constexpr bool kChunkedPrefillBuilt = true;
 
-// Workspace layout for the chunked prefill.
+// Workspace layout for the chunked prefill.  Single pass: a 256-byte header
+// (status word, work counter) and one int per unit.  Split mode: the header,
+// then ready flags, then one published chunk per (chunk, head) slot.
 size_t chunked_workspace_bytes(int32_t N, int32_t H);
+size_t split_slots_bound(int32_t N, int32_t total_T, int32_t H);
+size_t split_handoff_offset(int32_t N, int32_t total_T, int32_t H);
+size_t split_workspace_bytes(int32_t N, int32_t total_T, int32_t H);
+// Smallest workspace kda_prefill accepts (it then runs the single-pass kernel).
+size_t min_prefill_workspace_bytes(int32_t N, int32_t H);
+// Largest number of (sequence, head) units that runs in split mode on a GPU
+// with num_sms SMs.
+int split_max_units(int num_sms);
 cudaError_t launch_chunked_prefill(const ChunkedParams& p, cudaStream_t stream);
+cudaError_t launch_split_prefill(const ChunkedParams& p, int num_sms, cudaStream_t stream);
 
 }  // namespace kda

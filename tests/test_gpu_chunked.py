@@ -139,3 +139,26 @@ def test_deterministic():
     o1, S1 = _prefill(x)
     o2, S2 = _prefill(x)
     assert torch.equal(o1, o2) and torch.equal(S1, S2)
+
+
+def test_split_mode_matches_single_pass_bitwise():
+    """Few (sequence, head) units run the split kernel (producer CTAs publish
+    each chunk's operand tiles, one consumer CTA per unit runs the state
+    chain); with only the minimal workspace the single-pass kernel runs.  Both
+    execute the same per-chunk arithmetic, so the results agree bit for bit."""
+    x = inputs.make_prefill_inputs([700, 0, 129, 64], 5, 128, 128, torch.bfloat16, seed=16,
+                                   nonzero_state=True)
+    xd = x.to(DEV)
+    N, T, H = 4, x.q.shape[0], 5
+    big = kda.alloc_workspace(N, T, H, 128, 128, torch.bfloat16)
+    small = torch.empty(256 + 256, dtype=torch.uint8, device=DEV)
+    assert big.numel() > small.numel()  # split mode is available for these sizes
+    outs = []
+    for ws in (big, small):
+        o, S = kda.kda_prefill(xd.q, xd.k, xd.v, xd.z, xd.beta, xd.A, xd.initial_state,
+                               xd.cu_seqlens, cu_seqlens_host=x.cu_seqlens, workspace=ws)
+        assert kda.workspace_status(ws) == kda.KDA_OK
+        outs.append((o, S))
+    assert torch.equal(outs[0][0], outs[1][0])
+    assert torch.equal(outs[0][1], outs[1][1])
+    _check(x, outs[0][0], outs[0][1])
