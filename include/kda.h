@@ -185,9 +185,10 @@ KDA_API int kda_state_io(kda_state_op op, float* dst, const float* src,
  * 256 + 16384 * 4 bytes in the library's own device memory, held by every
  * GPU that loads the library until the process exits.
  *
- * Arguments, layouts and results are those of kda_prefill.  Sizes whose
- * workspace would exceed the array (N * H > 16384 (sequence, head) pairs)
- * return KDA_ERR_WORKSPACE without launching.  The first call on a device
+ * Arguments, layouts and results are those of kda_prefill, which it calls
+ * with the array as its workspace (so bf16 d=128 runs the single-pass
+ * kernel).  More than 16384 (sequence, head) pairs return KDA_ERR_WORKSPACE
+ * without launching.  The first call on a device
  * looks up the array's device address (cudaGetSymbolAddress, with that
  * device current), so make that first call before any stream capture.
  * Every call shares the one array: calls that overlap on the GPU (other

@@ -17,6 +17,8 @@
 
 #include <cuda_runtime.h>
 
+#include "kda_internal.h"
+
 #include <mutex>
 
 namespace {
@@ -59,7 +61,9 @@ extern "C" KDA_API int kda_prefill_noalloc(const void* q, const void* k, const v
                                            int32_t d_v, kda_dtype dt, float scale,
                                            uint32_t flags, void* o, float* final_state,
                                            void* stream) {
-    if (kda_prefill_workspace_bytes(N, total_T, H, d_k, d_v, dt) > kNoAllocScratchBytes) {
+    // the array always holds the smallest workspace kda_prefill accepts for
+    // up to 16384 (sequence, head) pairs (which then runs its single-pass kernel)
+    if (N < 0 || H < 0 || kda::min_prefill_workspace_bytes(N, H) > kNoAllocScratchBytes) {
         return KDA_ERR_WORKSPACE;
     }
     void* scratch = scratch_on_current_device();
