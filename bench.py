@@ -56,6 +56,40 @@ def prefill_algorithmic(B, H, T, d, C=64):
     return byts, flops
 
 
+# Sources of the chunked prefill kernels; a profile summary records their
+# digest so that its DRAM traffic is only reported for the kernel it measured.
+PREFILL_SOURCES = ("kda_prefill_sm103.cu", "kda_chunk_phases.cuh", "sm103_ptx.cuh",
+                   "kda_internal.h")
+
+
+def prefill_source_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in PREFILL_SOURCES:
+        with open(os.path.join(ROOT, "kimi_delta_attention_12_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str):
+    """dram bytes read + written per launch of `kernel` from its committed ncu
+    summary, or None when there is none for the current sources."""
+    prof = os.path.join(ROOT, "profiles", f"{kernel}_b1_h32_t4096.md")
+    if not os.path.exists(prof):
+        return None
+    rows = {}
+    for line in open(prof):
+        cells = [c.strip() for c in line.split("|")]
+        if len(cells) >= 4 and cells[0] == "":
+            rows[cells[1]] = cells[2]
+    if rows.get("source_digest") != prefill_source_digest():
+        return None
+    try:
+        return int(rows["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 def decode_algorithmic(B, H, d):
     """Bytes of one decode step: fp32 state read + write, bf16 q,k,v,z in, o out, beta."""
     return B * H * (2 * d * d * 4 + 5 * d * 2 + 2)
@@ -161,13 +195,27 @@ def run_oracle_sample(T_sample: int, H: int, d: int, seed: int = 0):
     return T_sample / dt, dt, threads
 
 
+def cpu_baseline(H: int, T: int, d: int, cpu_seconds: float = 12.0):
+    """The oracle on the whole prefill workload, repeated until about
+    cpu_seconds of CPU work (wall time x threads) are spent."""
+    runs, wall, threads = 0, 0.0, 1
+    while runs == 0 or wall * threads < cpu_seconds:
+        _, dt, threads = run_oracle_sample(T, H, d)
+        runs += 1
+        wall += dt
+    value = runs * T / wall
+    sample = (f"whole prefill workload (B=1 T={T}, all {H} heads) x {runs} runs, "
+              f"{wall:.1f} s wall on {threads} threads, fp64 C oracle")
+    return value, threads, sample
+
+
 def reference_arm(args, world, rank, pg):
     if rank != 0:
         return
     P = PREFILL_SHAPE
-    T_sample = 1024
-    # one warm-up and K timed samples; each sample is the first 1024 tokens of
-    # the prefill workload, all 32 heads
+    T_sample = P["T"]
+    # one warm-up and K timed steps; each step is the whole prefill workload
+    # (B=1, T=4096, all 32 heads)
     for _ in range(max(0, min(args.warmup, 1))):
         run_oracle_sample(256, P["H"], P["d"])
     vals, secs, threads = [], 0.0, 1
@@ -176,7 +224,7 @@ def reference_arm(args, world, rank, pg):
         vals.append(v)
         secs += dt
     value = statistics.median(vals)
-    sample = (f"first {T_sample} tokens of B=1 H=32 T=4096 d=128 (all 32 heads) per step, "
+    sample = (f"whole workload B=1 T={T_sample} d=128, all 32 heads, per step; "
               f"{args.steps} steps, fp64 C oracle")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
@@ -225,6 +273,10 @@ def kda_arm(args, world, rank, local, pg):
     o = torch.empty(B * T, H, d, dtype=torch.bfloat16, device=dev)
     S = torch.empty(B, H, d, d, dtype=torch.float32, device=dev)
     ws = kda.alloc_workspace(B, B * T, H, d, d, torch.bfloat16, dev)
+    # the library asks for more than the minimal workspace (256 B header + one
+    # int32 per sequence-head, rounded to 256 B) exactly when it runs the split kernel
+    minimal_ws = 256 + -(-4 * B * H // 256) * 256
+    kernel_name = "kda_split_kernel" if ws.numel() > minimal_ws else "kda_chunked_kernel"
     o_dec = torch.empty(B, H, d, dtype=torch.bfloat16, device=dev)
     cu_host = sets[0].cu_seqlens.cpu()
 
@@ -274,7 +326,7 @@ def kda_arm(args, world, rank, local, pg):
 
     return finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops, nsets,
                   set_bytes, x_host, o, S, ws, cu_host, value, ms_per_step, kernel_ms,
-                  achieved_gbs, achieved_tf, clk, launches_per_step, pg)
+                  achieved_gbs, achieved_tf, clk, launches_per_step, kernel_name, pg)
 
 
 def run_decode(dev, rank, local, stream, batch=None):
@@ -323,7 +375,7 @@ def decode_only(args, rank, local, dev, stream, peaks):
 
 def finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops, nsets,
            set_bytes, x_host, o, S, ws, cu_host, value, ms_per_step, kernel_ms, achieved_gbs,
-           achieved_tf, clk, launches_per_step, pg):
+           achieved_tf, clk, launches_per_step, kernel_name, pg):
     import torch
     import kimi_delta_attention_12_gb300 as kda
     # ---- end to end through the public API with host buffers ----
@@ -365,14 +417,9 @@ def finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops
 
     if rank != 0:
         return
-    # CPU baseline: the oracle on a bounded sample of the prefill workload
-    cpu_tps, cpu_s, cpu_threads = run_oracle_sample(1024, H, d)
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "kda_chunked_prefill_4k.md")
-    if os.path.exists(prof):
-        for line in open(prof):
-            if line.startswith("| traffic_bytes_per_launch |"):
-                traffic = int(line.split("|")[2].strip())
+    # CPU baseline: the oracle on the same workload
+    cpu_tps, cpu_threads, cpu_sample = cpu_baseline(H, T, d)
+    traffic = profiled_traffic(kernel_name)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -384,7 +431,7 @@ def finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops
                    "l2": "inputs larger than L2 (rotating sets)", "parallelism": "replicas"},
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"],
-                     "traffic": traffic, "kernel_ms": kernel_ms,
+                     "traffic": traffic, "kernel": kernel_name, "kernel_ms": kernel_ms,
                      "algorithmic_bytes": byts, "peak_source": peaks["source"],
                      "tensor_tflops": achieved_tf,
                      "tensor_frac": achieved_tf / peaks["bf16_tflops"]},
@@ -396,9 +443,7 @@ def finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops
                                 "unit": "GB/s", "frac": dec_gbs / peaks["hbm_gbs"]},
                    "clocks": dclk_summary},
         "cpu_baseline": {"value": cpu_tps, "unit": "tokens/s", "cores": cpu_threads,
-                         "kind": "oracle",
-                         "sample": "first 1024 tokens of the prefill workload, all 32 heads, "
-                                   f"{cpu_s:.2f} s of fp64 C oracle"},
+                         "kind": "oracle", "sample": cpu_sample},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,

@@ -134,10 +134,16 @@ int kda_prefill(const void* q, const void* k, const void* v, const void* z,
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int32_t* ws = static_cast<int32_t*>(workspace);
-    if (cudaMemsetAsync(ws, 0, kWsHeader, s) != cudaSuccess) return KDA_ERR_CUDA;
-
     const bool use_chunked = kda::kChunkedPrefillBuilt && dt == KDA_BF16 && d_k == 128 && d_v == 128 &&
                              (flags & kFlagRecurrent) == 0 && total_T > 0;
+    const int sms = use_chunked ? current_sm_count() : 0;
+    const bool use_split = use_chunked && split_eligible(N, H, dt, d_k, d_v, sms) &&
+                           workspace_bytes >= kda::split_workspace_bytes(N, total_T, H);
+    // the header (status, work counter) and, for the split kernel, the
+    // per-slot ready flags that follow it start at zero on every call
+    const size_t zero_bytes = use_split ? kda::split_handoff_offset(N, total_T, H) : kWsHeader;
+    if (cudaMemsetAsync(ws, 0, zero_bytes, s) != cudaSuccess) return KDA_ERR_CUDA;
+
     cudaError_t err;
     if (use_chunked) {
         kda::ChunkedParams p;
@@ -148,9 +154,7 @@ int kda_prefill(const void* q, const void* k, const void* v, const void* z,
         p.status = ws; p.work_counter = ws + 1; p.schedule = nullptr;
         p.N = N; p.total_T = total_T; p.H = H; p.scale = scale;
         p.l2norm = (flags & KDA_FLAG_L2NORM_QK) ? 1 : 0;
-        const int sms = current_sm_count();
-        if (split_eligible(N, H, dt, d_k, d_v, sms) &&
-            workspace_bytes >= kda::split_workspace_bytes(N, total_T, H)) {
+        if (use_split) {
             uint8_t* wsb = static_cast<uint8_t*>(workspace);
             p.flags = reinterpret_cast<int32_t*>(wsb + 256);
             p.handoff = wsb + kda::split_handoff_offset(N, total_T, H);

@@ -796,12 +796,7 @@ cudaError_t launch_split_prefill(const ChunkedParams& p, int num_sms, cudaStream
     if (err != cudaSuccess) {
         return err;
     }
-    // flags start at zero for every call
-    err = cudaMemsetAsync(p.flags, 0, split_slots_bound(p.N, p.total_T, p.H) * sizeof(int32_t),
-                          stream);
-    if (err != cudaSuccess) {
-        return err;
-    }
+    // p.flags was zeroed by the caller on this stream
     kda_split_kernel<<<(unsigned)num_sms, kThreads, SMEM_BYTES, stream>>>(args);
     return cudaGetLastError();
 }
