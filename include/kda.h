@@ -75,13 +75,17 @@ enum {
  * these sizes on the current device.  Always > 0 and a multiple of 256.
  *
  * Any workspace of at least 256 + 4 * N * H bytes (rounded up to 256) is
- * accepted.  With bf16, d_k = d_v = 128 and few (sequence, head) pairs (at
- * most a third of the SMs), a larger workspace -- the size returned here,
- * about 66 KB per (64-token chunk, head) -- selects the split kernel, which
- * spreads each pair's chunks over all SMs and stages every chunk's operand
- * tiles in the workspace; a smaller one selects the single-pass kernel.  The
- * workspace is scratch: its content on entry does not matter and it may be
- * reused by the next call on the same stream.
+ * accepted.  With bf16 and d_k = d_v = 128 (up to 1024 sequences and 256
+ * heads), a larger workspace -- the size returned here, about 0.5 MB per
+ * consumer CTA (a quarter of the SMs at most, ~20 MB on 152 SMs) whatever the
+ * sequence lengths -- selects the split kernel, which spreads each
+ * (sequence, head) pair's chunks over all SMs and passes every chunk's
+ * operand tiles through a ring of slots in the workspace; a smaller one
+ * selects the single-pass kernel.  The split kernel expects one CTA on every
+ * SM at once: with other work on the GPU its waits may run out and the call
+ * then reports KDA_ERR_TIMEOUT through kda_workspace_status.  The workspace
+ * is scratch: its content on entry does not matter and it may be reused by
+ * the next call on the same stream.
  */
 KDA_API size_t kda_prefill_workspace_bytes(int32_t N, int32_t total_T, int32_t H,
                                    int32_t d_k, int32_t d_v, kda_dtype dt);

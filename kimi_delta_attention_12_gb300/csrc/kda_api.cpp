@@ -45,11 +45,11 @@ int current_sm_count() {
     return sms;
 }
 
-// Few (sequence, head) units leave most SMs idle in the single-pass kernel;
-// the split kernel spreads each unit's chunks over producer CTAs.
-bool split_eligible(int32_t N, int32_t H, kda_dtype dt, int32_t d_k, int32_t d_v, int sms) {
-    return dt == KDA_BF16 && d_k == 128 && d_v == 128 && sms > 0 &&
-           (int64_t)N * H <= kda::split_max_units(sms);
+// bf16 at d = 128 runs the split kernel when its tables can describe the
+// sizes (the single-pass kernel otherwise, or with a minimal workspace).
+bool split_eligible(int32_t N, int32_t H, kda_dtype dt, int32_t d_k, int32_t d_v, int sms,
+                    kda::SplitPlan* plan) {
+    return dt == KDA_BF16 && d_k == 128 && d_v == 128 && kda::split_plan(N, H, sms, plan);
 }
 
 }  // namespace
@@ -78,8 +78,10 @@ int kda_version(void) { return 100; }
 size_t kda_prefill_workspace_bytes(int32_t N, int32_t total_T, int32_t H, int32_t d_k,
                                    int32_t d_v, kda_dtype dt) {
     const size_t basic = basic_workspace_bytes(N, H);
-    if (N > 0 && H > 0 && total_T > 0 && split_eligible(N, H, dt, d_k, d_v, current_sm_count())) {
-        const size_t split = kda::split_workspace_bytes(N, total_T, H);
+    kda::SplitPlan plan;
+    if (N > 0 && H > 0 && total_T > 0 &&
+        split_eligible(N, H, dt, d_k, d_v, current_sm_count(), &plan)) {
+        const size_t split = kda::split_workspace_bytes(plan);
         return split > basic ? split : basic;
     }
     return basic;
@@ -137,11 +139,12 @@ int kda_prefill(const void* q, const void* k, const void* v, const void* z,
     const bool use_chunked = kda::kChunkedPrefillBuilt && dt == KDA_BF16 && d_k == 128 && d_v == 128 &&
                              (flags & kFlagRecurrent) == 0 && total_T > 0;
     const int sms = use_chunked ? current_sm_count() : 0;
-    const bool use_split = use_chunked && split_eligible(N, H, dt, d_k, d_v, sms) &&
-                           workspace_bytes >= kda::split_workspace_bytes(N, total_T, H);
-    // the header (status, work counter) and, for the split kernel, the
-    // per-slot ready flags that follow it start at zero on every call
-    const size_t zero_bytes = use_split ? kda::split_handoff_offset(N, total_T, H) : kWsHeader;
+    kda::SplitPlan plan;
+    const bool use_split = use_chunked && split_eligible(N, H, dt, d_k, d_v, sms, &plan) &&
+                           workspace_bytes >= kda::split_workspace_bytes(plan);
+    // the header (status, work counter) and, for the split kernel, the ring
+    // flags and consumer counters that follow it start at zero on every call
+    const size_t zero_bytes = use_split ? kda::split_zeroed_bytes(plan) : kWsHeader;
     if (cudaMemsetAsync(ws, 0, zero_bytes, s) != cudaSuccess) return KDA_ERR_CUDA;
 
     cudaError_t err;
@@ -155,9 +158,7 @@ int kda_prefill(const void* q, const void* k, const void* v, const void* z,
         p.N = N; p.total_T = total_T; p.H = H; p.scale = scale;
         p.l2norm = (flags & KDA_FLAG_L2NORM_QK) ? 1 : 0;
         if (use_split) {
-            uint8_t* wsb = static_cast<uint8_t*>(workspace);
-            p.flags = reinterpret_cast<int32_t*>(wsb + 256);
-            p.handoff = wsb + kda::split_handoff_offset(N, total_T, H);
+            kda::split_bind(plan, workspace, &p);
             err = kda::launch_split_prefill(p, sms, s);
         } else {
             err = kda::launch_chunked_prefill(p, s);

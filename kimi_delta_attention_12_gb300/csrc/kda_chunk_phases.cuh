@@ -9,7 +9,7 @@
 //   Aqk[r,i] =        <q_r e^{gamma_r - gamma_i}, k_i>   (i <= r)
 //   Tm       = (I + Akk)^-1 Diag(beta)                    (UT solve, fp32)
 //   U        = Tm V - (Tm K+) S0,    K+ = k * e^{gamma}
-//   O        = Q+ S0 + Aqk U,        Q+ = q * e^{gamma}
+//   O        = Q+ S0 + Aqk U,        Q+ = q * e^{gamma}  (computed as O^T)
 //   S_next   = Diag(e^{gamma_C}) S0 + Kend^T U,   Kend = k * e^{gamma_C - gamma}
 // The Gram products use one reference point per 16-token block a (rho_a =
 // gamma at the end of the previous block): the query/key side is scaled by
@@ -78,13 +78,13 @@ constexpr uint32_t TM_G1 = 128;   // Gram blocks 3, 2
 constexpr uint32_t TM_G2 = 192;   // Gram blocks 1, 0
 constexpr uint32_t TM_W = 256;    // W^T  [128 c][64 r]
 constexpr uint32_t TM_U = 320;    // U^T  [128 j][64 r]
-constexpr uint32_t TM_O = 384;    // O    [64 r][128 j]  (M = 64 layout)
+constexpr uint32_t TM_O = 384;    // O^T  [128 j][64 r]
 constexpr uint32_t TMEM_COLS = 512;
 
 // Where the state-side phases find a chunk's operand tiles.
 struct StateTiles {
     uint32_t wt;   // W^T  bf16 [128 c][64 r]  MN-major B
-    uint32_t qp;   // Q+   bf16 [128 c][64 r]  MN-major A (M = 64)
+    uint32_t qp;   // Q+   bf16 [128 c][64 r]  MN-major B
     uint32_t ke;   // Kend bf16 [128 c][64 i]  K-major B
     uint32_t aqk;  // Aqk  bf16 [64 r][64 i]   K-major A
     uint32_t tm;   // Tm   bf16 [64 r][64 i]   K-major B
@@ -429,6 +429,43 @@ __device__ __forceinline__ void phase_state_epilogue(const Ctx& x, const float* 
     tmem_wait_st();
 }
 
+// The two halves of phase_state_epilogue for the split kernel's consumer, all
+// 16 warps, 32 columns each: S^T (TMEM) -> bf16 A-operand tile (no barrier) ...
+__device__ __forceinline__ void phase_state_to_operand(const Ctx& x, uint32_t st_tile) {
+    const int j = 32 * x.qd + x.lane;
+    const int cb = 32 * x.sub;
+    uint32_t r0[16], r1[16];
+    tmem_ld16(x.tbase + x.lane_base + TM_S + cb, r0);
+    tmem_ld16(x.tbase + x.lane_base + TM_S + cb + 16, r1);
+    tmem_wait_ld();
+    float v0[16], v1[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        v0[i] = __uint_as_float(r0[i]);
+        v1[i] = __uint_as_float(r1[i]);
+    }
+    store_row16(x.sm + st_tile + (cb / 64) * 16384, j, 2 * (cb % 64), v0);
+    store_row16(x.sm + st_tile + (cb / 64) * 16384, j, 2 * (cb % 64) + 32, v1);
+}
+
+// ... and S^T *= Gamma_C in TMEM (no barrier; waits for its own stores).
+__device__ __forceinline__ void phase_state_decay(const Ctx& x, const float* gam) {
+    const int cb = 32 * x.sub;
+    const uint32_t taddr = x.tbase + x.lane_base + TM_S + cb;
+    uint32_t r0[16], r1[16];
+    tmem_ld16(taddr, r0);
+    tmem_ld16(taddr + 16, r1);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        r0[i] = __float_as_uint(__uint_as_float(r0[i]) * gam[cb + i]);
+        r1[i] = __float_as_uint(__uint_as_float(r1[i]) * gam[cb + 16 + i]);
+    }
+    tmem_st16(taddr, r0);
+    tmem_st16(taddr + 16, r1);
+    tmem_wait_st();
+}
+
 // ---------------------------------------------------------------- P4
 // UT solve  Tm = (I + Akk)^-1 Diag(beta) -> bf16 tile at OFF_TM.
 // N = (I + L)^-1, L = Akk strictly lower, in 16x16 blocks:
@@ -547,15 +584,15 @@ __device__ __forceinline__ void issue_u(const Ctx& x, const StateTiles& st) {
     }
 }
 
-// O = Q+ S   (S^T bf16 tile at st.st).
+// O^T = S^T Q+^T   (S^T bf16 tile at st.st; Q+ [128 c][64 r] is the MN-major B).
 __device__ __forceinline__ void issue_o(const Ctx& x, const StateTiles& st) {
-    const uint32_t ido = idesc_bf16(64, 128, 1, 0);
+    const uint32_t ido = idesc_bf16(128, 64, 0, 1);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t aQ = smem_desc(x.smem_base + st.qp + kk * 2048, 16384, 1024);
-        const uint64_t bS =
+        const uint64_t aS =
             smem_desc(x.smem_base + st.st + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-        mma_bf16(x.tbase + TM_O, aQ, bS, ido, kk > 0);
+        const uint64_t bQ = smem_desc(x.smem_base + st.qp + kk * 2048, 16384, 1024);
+        mma_bf16(x.tbase + TM_O, aS, bQ, ido, kk > 0);
     }
 }
 
@@ -565,52 +602,42 @@ __device__ __forceinline__ void issue_uo(const Ctx& x, const StateTiles& st) {
 }
 
 // ---------------------------------------------------------------- P9 (one thread)
-// O += Aqk U;  S^T += U^T Kend   (U^T bf16 tile at st.ut).
+// S^T += U^T Kend (first: the next chunk waits for it);  O^T += U^T Aqk^T
+// (U^T bf16 tile at st.ut; Kend [128 c][64 i] and Aqk [64 r][64 i] K-major B).
 __device__ __forceinline__ void issue_os(const Ctx& x, const StateTiles& st) {
-    const uint32_t ido = idesc_bf16(64, 128, 0, 0);
     const uint32_t ids = idesc_bf16(128, 128, 0, 0);
+    const uint32_t ido = idesc_bf16(128, 64, 0, 0);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t aA = smem_desc(x.smem_base + st.aqk + kk * 32, 16, 1024);
-        const uint64_t bU = smem_desc(x.smem_base + st.ut + kk * 32, 16, 1024);
-        mma_bf16(x.tbase + TM_O, aA, bU, ido, 1);
         const uint64_t aU = smem_desc(x.smem_base + st.ut + kk * 32, 16, 1024);
         const uint64_t bK = smem_desc(x.smem_base + st.ke + kk * 32, 16, 1024);
         mma_bf16(x.tbase + TM_S, aU, bK, ids, 1);
     }
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t aU = smem_desc(x.smem_base + st.ut + kk * 32, 16, 1024);
+        const uint64_t bA = smem_desc(x.smem_base + st.aqk + kk * 32, 16, 1024);
+        mma_bf16(x.tbase + TM_O, aU, bA, ido, 1);
+    }
 }
 
 // ---------------------------------------------------------------- P10
-// O (M = 64 tokens) sits in TMEM lanes 32q .. 32q+15 for tokens 16q .. 16q+15.
-// Warps with sub in [sub0, sub0 + nsub) take part; each stores 128 / nsub
-// value columns of its 16 tokens as 16-byte vectors.
+// O^T (TMEM lane j = value column, column r = token) -> o (bf16).  Each warp
+// stores 16 tokens of its 32 value columns; for a token the warp's lanes
+// cover 64 contiguous bytes of o.  No barrier.
 __device__ __forceinline__ void phase_o_epilogue(const Ctx& x, __nv_bfloat16* o_g, int64_t t0,
-                                                 int L, int h, int H, int sub0 = 0,
-                                                 int nsub = 4) {
-    const int part = x.sub - sub0;
-    if (part < 0 || part >= nsub) {
-        return;
-    }
-    const int ncol = D / nsub;
-    const int rtok = 16 * x.qd + x.lane;
-#pragma unroll 1
-    for (int cb = part * ncol; cb < (part + 1) * ncol; cb += 32) {
-        uint32_t r0[16], r1[16];
-        tmem_ld16(x.tbase + x.lane_base + TM_O + cb, r0);
-        tmem_ld16(x.tbase + x.lane_base + TM_O + cb + 16, r1);
-        tmem_wait_ld();
-        if (x.lane < 16 && rtok < L) {
-            uint4 w[4];
-            uint32_t* wp = reinterpret_cast<uint32_t*>(w);
+                                                 int L, int h, int H) {
+    const int j = 32 * x.qd + x.lane;
+    const int r0 = 16 * x.sub;
+    uint32_t r[16];
+    tmem_ld16(x.tbase + x.lane_base + TM_O + r0, r);
+    tmem_wait_ld();
+    __nv_bfloat16* dst = o_g + ((size_t)(t0 + r0) * H + h) * D + j;
+    const size_t row = (size_t)H * D;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                wp[i] = pack_bf16x2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
-                wp[8 + i] =
-                    pack_bf16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
-            }
-            uint4* dst = reinterpret_cast<uint4*>(o_g + ((size_t)(t0 + rtok) * H + h) * D + cb);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = w[i];
+    for (int i = 0; i < 16; ++i) {
+        if (r0 + i < L) {
+            dst[i * row] = __float2bfloat16_rn(__uint_as_float(r[i]));
         }
     }
 }

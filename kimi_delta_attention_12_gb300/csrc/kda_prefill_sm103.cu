@@ -20,24 +20,28 @@
 //     P4  UT solve in shared memory (fp32): Tm
 //     P5  tcgen05: W^T = K+^T Tm^T, U^T = V^T Tm^T
 //     P6  W^T -> bf16 operand
-//     P7  tcgen05: U^T += S^T (-W^T), O = Q+ S
+//     P7  tcgen05: U^T += S^T (-W^T), O^T = S^T Q+^T
 //     P8  U^T -> bf16 operand
-//     P9  tcgen05: O += Aqk U, S^T += U^T Kend
+//     P9  tcgen05: S^T += U^T Kend, O^T += U^T Aqk^T
 //     P10 O -> o (bf16)
 //   with the fp32 state S^T in TMEM for the whole sequence.
 //
-// kda_split_kernel (few (sequence, head) units, e.g. 32 heads of one
-//   sequence on 152 SMs): one launch of one CTA per SM.  CTAs 0..U-1 are
-//   consumers, one per unit, and run only the sequential part of every chunk
-//   (P3 state half, P5 U', P7..P10).  The other CTAs are producers: they take
-//   (chunk, unit) tasks in chunk-major order from an atomic counter and run
-//   the state-independent part (P0..P6) of each, then publish the chunk's
-//   operand tiles (W^T, Q+, Kend, Aqk, Tm, Gamma) to a workspace slot and
-//   raise the slot's flag (release).  A consumer waits for the flag of its
-//   next chunk (acquire, bounded), copies the slot into shared memory with
-//   one bulk copy and its v tile with TMA, one chunk ahead of use.
-//   Producers never wait for consumers, so progress needs only that every
-//   CTA is resident: the grid is one CTA per SM.
+// kda_split_kernel: one launch of one CTA per SM.  The (sequence, head)
+//   units are cut into batches of at most a quarter of the SMs.  CTA i < the
+//   batch size is a consumer: it carries the state of the i-th unit of each
+//   batch in turn and runs only the sequential part of every chunk (the
+//   state epilogue, U', U, O, the state update and o).  The other CTAs are
+//   producers: they take (chunk, unit) tasks in batch-major, then chunk-major
+//   order from an atomic counter, run the state-independent part of each
+//   (prologue, Gram, UT solve, W) and store the chunk's operand tiles
+//   (Aqk, Tm, W^T, Q+, Kend, Gamma) with bulk copies into a ring of slots
+//   that belongs to the chunk's consumer, then raise the slot's flag
+//   (release).  A consumer waits for its next chunk's flag (acquire,
+//   bounded), copies the slot into shared memory with one bulk copy and the
+//   v tile with TMA, one chunk ahead of use, and reports every chunk it has
+//   copied out so that producers may refill the slot.  Tasks are taken in
+//   the order consumers need them and every CTA is resident (the grid is
+//   one CTA per SM), so each wait ends.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -64,12 +68,18 @@ struct ChunkedArgs {
 };
 
 // ---- split mode: one published chunk (a workspace slot), byte offsets ----
-constexpr uint32_t HO_WT = 0;
-constexpr uint32_t HO_QP = 16384;
-constexpr uint32_t HO_KE = 32768;
-constexpr uint32_t HO_AQK = 49152;
-constexpr uint32_t HO_TM = 57344;
+// The slot mirrors two contiguous runs of the producer's shared memory
+// (Aqk | Tm | W^T and Q+ | Kend) plus Gamma_C, so three bulk copies store it.
+constexpr uint32_t HO_AQK = 0;
+constexpr uint32_t HO_TM = 8192;
+constexpr uint32_t HO_WT = 16384;
+constexpr uint32_t HO_QP = 32768;
+constexpr uint32_t HO_KE = 49152;
 constexpr uint32_t HO_GAM = 65536;
+static_assert(OFF_TM == OFF_AQK + 8192 && OFF_WT == OFF_TM + 8192 && OFF_KE == OFF_QP + 16384,
+              "slot runs must be contiguous in the producer's shared memory");
+static_assert(OFF_GAM % 16 == 0 && OFF_AQK % 16 == 0 && OFF_QP % 16 == 0,
+              "bulk copies need 16-byte aligned sources");
 constexpr uint32_t HO_BYTES = 66048;           // multiple of 256
 // consumer shared memory: two buffers of [slot | v tile], then S^T and U^T
 constexpr uint32_t CB_V = 66560;               // v tile inside a buffer (1024-aligned)
@@ -287,7 +297,7 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
         fence_proxy_async();
         cta_sync_tc();
 
-        // ---------------- P7: U^T += S^T (-W^T),  O = Q+ S ----------------
+        // ---------------- P7: U^T += S^T (-W^T),  O^T = S^T Q+^T ----------------
         if (tid == 0) {
             issue_uo(x, lt);
             mma_commit(&bar_mma);
@@ -307,7 +317,7 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
         fence_proxy_async();
         cta_sync_tc();
 
-        // ---------------- P9: O += Aqk U,  S^T += U^T Kend ----------------
+        // ---------------- P9: S^T += U^T Kend,  O^T += U^T Aqk^T ----------------
         if (tid == 0) {
             issue_os(x, lt);
             mma_commit(&bar_mma);
@@ -344,31 +354,36 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
 }
 
 // ====================================================================== split mode
-// Bounded wait for a release-published flag (acquire, one thread).
-__device__ __forceinline__ bool wait_flag(const int32_t* flag, const volatile int* abort_flag) {
+__device__ __forceinline__ int32_t ld_acquire(const int32_t* ptr) {
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release(int32_t* ptr, int32_t v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+}
+
+// Bounded wait (one thread) until *ptr >= target.  False on timeout or when
+// another thread of the CTA raised the abort flag.
+__device__ __forceinline__ bool wait_at_least(const int32_t* ptr, int32_t target,
+                                              const volatile int* abort_flag) {
     for (uint32_t i = 0; i < (1u << 25); ++i) {
-        int32_t v;
-        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
-        if (v != 0) {
+        if (ld_acquire(ptr) >= target) {
             return true;
         }
         if (*abort_flag) {
             return false;
         }
-        __nanosleep(128);
+        __nanosleep(64);
     }
     return false;
 }
 
-// chunk index base of sequence n: sum over earlier sequences of ceil(len / C)
-__device__ __forceinline__ int64_t chunk_base(const ChunkedParams& p, int n) {
-    int64_t base = 0;
-    for (int m = 0; m < n; ++m) {
-        int64_t b, e;
-        seq_bounds(p, m, b, e);
-        base += (e - b + C - 1) / C;
-    }
-    return base;
+// orders this thread's generic-proxy global accesses with its later (or
+// earlier) async-proxy ones
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes,
@@ -380,16 +395,83 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint
         : "memory");
 }
 
+__device__ __forceinline__ void bulk_store(void* gdst, const void* smem_src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                     reinterpret_cast<uint64_t>(gdst)),
+                 "r"(smem_u32(smem_src)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// this thread's bulk stores are complete
+__device__ __forceinline__ void bulk_wait() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Sequence and batch tables, built by every CTA at start.
+struct SplitMeta {
+    int32_t cu[kSplitMaxSeqs + 1];       // token start of each sequence (and total_T)
+    float eA[kSplitMaxHeads];            // e^{A_h} log2(e)
+    int32_t task0[kSplitMaxBatches + 1]; // first task of each batch
+    int32_t g0[kSplitMaxBatches + 1];    // first consumer-stream index of each batch
+};
+
+// One producer task: chunk c of unit `unit` (the i-th unit of its batch).
+// Task t of batch b is chunk (t - task0[b]) / nu of unit (t - task0[b]) % nu
+// (chunk-major), nu the batch's units; in consumer i's stream of chunks it is
+// number g = g0[b] + c, and it goes through ring slot i * ring + g % ring.
+struct SplitTask {
+    int i, unit, h, c, L;
+    int32_t t0, g;
+};
+
+// False if the task's chunk lies past the end of its sequence.
+__device__ __forceinline__ bool decode_task(const SplitMeta& m, const ChunkedParams& p, int t,
+                                            SplitTask& o) {
+    int lo = 0, hi = p.n_batches - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (m.task0[mid] <= t) {
+            lo = mid;
+        } else {
+            hi = mid - 1;
+        }
+    }
+    const int U = p.N * p.H;
+    const int u0 = lo * p.n_cons;
+    const int nu = min(U - u0, p.n_cons);
+    const int local = t - m.task0[lo];
+    const int c = local / nu;
+    o.i = local - c * nu;
+    o.unit = u0 + o.i;
+    const int n = o.unit / p.H;
+    o.h = o.unit - n * p.H;
+    o.c = c;
+    const int32_t bos = m.cu[n];
+    const int32_t len = m.cu[n + 1] - bos;
+    o.t0 = bos + c * C;
+    o.L = min(C, len - c * C);
+    o.g = m.g0[lo] + c;
+    return c * C < len;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
     const ChunkedParams& p = args.p;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
-    __shared__ uint64_t bar_raw;
-    __shared__ uint64_t bar_full[2];
-    __shared__ uint64_t bar_mma;
+    __shared__ SplitMeta meta;
+    __shared__ uint64_t bar_raw;       // producer: raw q, k, z landed
+    __shared__ uint64_t bar_mma;       // producer: MMA group done
+    __shared__ uint64_t bar_full[2];   // consumer: a buffer's slot and v tile landed
+    __shared__ uint64_t bar_u;         // consumer: U^T done
+    __shared__ uint64_t bar_os;        // consumer: O and the state update done
+    __shared__ uint64_t bar_fin;       // every MMA of this CTA done
     __shared__ uint32_t tmem_base_s;
-    __shared__ int s_task;
+    __shared__ int s_next;
     __shared__ int s_issued;
     __shared__ volatile int abort_flag;
 
@@ -400,9 +482,12 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
     if (tid == 0) {
         abort_flag = 0;
         mbar_init(&bar_raw, 1);
+        mbar_init(&bar_mma, 1);
         mbar_init(&bar_full[0], 1);
         mbar_init(&bar_full[1], 1);
-        mbar_init(&bar_mma, 1);
+        mbar_init(&bar_u, 1);
+        mbar_init(&bar_os, 1);
+        mbar_init(&bar_fin, 1);
         fence_mbar_init();
         prefetch_tmap(&args.tm_q);
         prefetch_tmap(&args.tm_k);
@@ -413,201 +498,273 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
         tmem_alloc(&tmem_base_s, TMEM_COLS);
         tmem_relinquish();
     }
+    // sequence starts and gate constants
+    for (int n = tid; n <= p.N; n += kThreads) {
+        meta.cu[n] = p.cu_seqlens ? p.cu_seqlens[n] : n * (p.total_T / p.N);
+    }
+    for (int h = tid; h < H; h += kThreads) {
+        meta.eA[h] = exp2_approx(p.A[h] * kLog2e) * kLog2e;
+    }
+    __syncthreads();
+    // per batch: tasks (its longest sequence's chunks x its units) and stream length
+    for (int b = tid; b < p.n_batches; b += kThreads) {
+        const int u0 = b * p.n_cons;
+        const int u1 = min(U, u0 + p.n_cons);
+        int maxc = 0;
+        for (int n = u0 / H; n <= (u1 - 1) / H; ++n) {
+            maxc = max(maxc, (meta.cu[n + 1] - meta.cu[n] + C - 1) / C);
+        }
+        meta.task0[b + 1] = maxc * (u1 - u0);
+        meta.g0[b + 1] = maxc;
+    }
+    __syncthreads();
+    if (tid < 32) {  // exclusive prefix sums over the batches (one warp)
+        const int nb = p.n_batches;
+        const int per = (nb + 31) >> 5;
+        const int b0 = tid * per;
+        int a = 0, g = 0;
+        for (int j = 0; j < per; ++j) {
+            if (b0 + j < nb) {
+                a += meta.task0[b0 + j + 1];
+                g += meta.g0[b0 + j + 1];
+            }
+        }
+        int ai = a, gi = g;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int ta = __shfl_up_sync(0xffffffffu, ai, off);
+            const int tg = __shfl_up_sync(0xffffffffu, gi, off);
+            if (tid >= off) {
+                ai += ta;
+                gi += tg;
+            }
+        }
+        int ra = ai - a, rg = gi - g;
+        for (int j = 0; j < per; ++j) {
+            if (b0 + j < nb) {
+                ra += meta.task0[b0 + j + 1];
+                meta.task0[b0 + j + 1] = ra;
+                rg += meta.g0[b0 + j + 1];
+                meta.g0[b0 + j + 1] = rg;
+            }
+        }
+        if (tid == 0) {
+            meta.task0[0] = 0;
+            meta.g0[0] = 0;
+        }
+    }
     cta_sync_tc();
     const Ctx x = make_ctx(sm, tmem_base_s);
     const __nv_bfloat16* beta_g = static_cast<const __nv_bfloat16*>(p.beta);
-    uint32_t ph_mma = 0;
 
-    if ((int)blockIdx.x < U) {
+    if ((int)blockIdx.x < p.n_cons) {
         // ------------------------------------------------------------ consumer
-        const int unit = blockIdx.x;
-        const int n = unit / H;
-        const int h = unit % H;
-        int64_t bos, eos;
-        seq_bounds(p, n, bos, eos);
-        const int nchunks = (int)((eos - bos + C - 1) / C);
-        const int64_t base = chunk_base(p, n);
-        const size_t state_off = (size_t)unit * D * D;
+        const int i = blockIdx.x;
         __nv_bfloat16* o_g = static_cast<__nv_bfloat16*>(p.o);
-
-        load_state(x, p.initial_state ? p.initial_state + state_off : nullptr);
-        cta_sync_tc();
-
-        // one thread: wait for chunk c's slot and copy it (and the v tile) into buffer c & 1
-        auto fetch = [&](int c) -> bool {
-            const int64_t slot = (base + c) * H + h;
-            if (!wait_flag(p.flags + slot, &abort_flag)) {
-                return false;
-            }
-            // order the acquire (and this CTA's earlier generic accesses to the
-            // buffer) before the async-proxy copies below
-            asm volatile("fence.proxy.async.global;" ::: "memory");
-            fence_proxy_async();
-            uint8_t* buf = sm + (c & 1) * CB_BYTES;
-            uint64_t* bar = &bar_full[c & 1];
-            const int t0 = (int)(bos + (int64_t)c * C);
-            mbar_arrive_expect_tx(bar, HO_BYTES + 16384);
-            bulk_load(buf, p.handoff + slot * HO_BYTES, HO_BYTES, bar);
-            tma_load_3d(buf + CB_V, &args.tm_v, 0, h, t0, bar);
-            tma_load_3d(buf + CB_V + 8192, &args.tm_v, 64, h, t0, bar);
-            return true;
-        };
-        // number of chunks whose copies were issued (thread 0's count)
-        int issued = 0;
-        if (tid == 0 && nchunks > 0) {
-            if (fetch(0)) {
-                issued = 1;
-            } else {
-                record_timeout(p.status, &abort_flag);
-            }
-        }
-        __syncthreads();
-        int waited = 0;
-        for (int c = 0; c < nchunks && !abort_flag; ++c) {
-            const int b = c & 1;
-            const int64_t t0 = bos + (int64_t)c * C;
-            const int L = (int)((eos - t0) < C ? (eos - t0) : C);
+        auto tiles = [&](uint32_t b) -> StateTiles {
             const uint32_t cb = b * CB_BYTES;
-            const StateTiles st{cb + HO_WT, cb + HO_QP, cb + HO_KE, cb + HO_AQK, cb + HO_TM,
-                                cb + HO_GAM, cb + CB_V, CB_ST, CB_UT};
-            if (!mbar_wait(&bar_full[b], (c >> 1) & 1, &abort_flag)) {
-                record_timeout(p.status, &abort_flag);
-            }
-            waited = c + 1;
-            tc_fence_after();
-            __syncthreads();
-            if (abort_flag) {
+            return StateTiles{cb + HO_WT, cb + HO_QP,  cb + HO_KE, cb + HO_AQK, cb + HO_TM,
+                              cb + HO_GAM, cb + CB_V, CB_ST,      CB_UT};
+        };
+        uint32_t cnt = 0;  // buffer fills so far (buffer = count & 1, parity = (count >> 1) & 1)
+        uint32_t ph_u = 0, ph_os = 0;
+        for (int bt = 0; bt < p.n_batches && !abort_flag; ++bt) {
+            const int unit = bt * p.n_cons + i;
+            if (unit >= U) {
                 break;
             }
-            if (tid == 0) {
-                issue_u_prime(x, st);          // U'^T = V^T Tm^T, independent of S
-                mma_commit(&bar_mma);
-                if (c + 1 < nchunks) {         // buffer b^1 was released by chunk c-1
-                    if (fetch(c + 1)) {
-                        issued = c + 2;
-                    } else {
+            const int n = unit / H;
+            const int h = unit - n * H;
+            const int32_t bos = meta.cu[n];
+            const int32_t len = meta.cu[n + 1] - bos;
+            const int nch = (len + C - 1) / C;
+            const int32_t g0 = meta.g0[bt];
+            const size_t state_off = (size_t)unit * D * D;
+
+            load_state(x, p.initial_state ? p.initial_state + state_off : nullptr);
+            cta_sync_tc();
+
+            int fetched = 0;  // thread 0: chunks of this unit whose copies are issued
+            int waited = 0;   // chunks of this unit every thread has waited for
+            // thread 0: copy chunk c's slot and v tile into buffer (cnt + c) & 1
+            auto fetch = [&](int c, bool block) -> bool {
+                const int32_t g = g0 + c;
+                const int32_t slot = i * p.ring + g % p.ring;
+                if (block) {
+                    if (!wait_at_least(p.flags + slot, g + 1, &abort_flag)) {
                         record_timeout(p.status, &abort_flag);
+                        return false;
+                    }
+                } else if (ld_acquire(p.flags + slot) < g + 1) {
+                    return false;
+                }
+                // the acquire (and this CTA's earlier use of the buffer) before the copies
+                fence_proxy_async_global();
+                fence_proxy_async();
+                const uint32_t b = (cnt + c) & 1;
+                uint8_t* buf = sm + b * CB_BYTES;
+                mbar_arrive_expect_tx(&bar_full[b], HO_BYTES + 16384);
+                bulk_load(buf, p.handoff + (size_t)slot * HO_BYTES, HO_BYTES, &bar_full[b]);
+                tma_load_3d(buf + CB_V, &args.tm_v, 0, h, bos + c * C, &bar_full[b]);
+                tma_load_3d(buf + CB_V + 8192, &args.tm_v, 64, h, bos + c * C, &bar_full[b]);
+                fetched = c + 1;
+                return true;
+            };
+            // every thread: wait for chunk c's buffer; then its slot may be reused
+            auto wait_full = [&](int c) {
+                const uint32_t r = cnt + c;
+                if (!mbar_wait(&bar_full[r & 1], (r >> 1) & 1, &abort_flag)) {
+                    record_timeout(p.status, &abort_flag);
+                }
+                waited = c + 1;
+                if (tid == 32 && !abort_flag) {
+                    st_release(p.cons_done + i, g0 + c + 1);
+                }
+            };
+
+            if (nch > 0) {
+                if (tid == 0 && fetch(0, true) && nch > 1) {
+                    fetch(1, false);
+                }
+                wait_full(0);
+                tc_fence_after();
+                if (tid == 0 && !abort_flag) {
+                    issue_u_prime(x, tiles(cnt & 1));   // U'^T = V^T Tm^T into TM_U
+                }
+                phase_state_to_operand(x, CB_ST);
+                fence_proxy_async();
+                cta_sync_tc();
+            }
+            for (int c = 0; c < nch && !abort_flag; ++c) {
+                const StateTiles st = tiles((cnt + c) & 1);
+                // U^T += S^T (-W^T) (after U'), then O^T = S^T Q+^T
+                if (tid == 0) {
+                    issue_u(x, st);
+                    mma_commit(&bar_u);
+                }
+                // S^T *= Gamma_C while the tensor core works
+                phase_state_decay(x, reinterpret_cast<const float*>(sm + st.gam));
+                if (tid == 0) {
+                    issue_o(x, st);
+                    if (fetched == c + 1 && c + 1 < nch) {
+                        fetch(c + 1, false);
                     }
                 }
+                if (!mbar_wait(&bar_u, ph_u, &abort_flag)) {
+                    record_timeout(p.status, &abort_flag);
+                }
+                ph_u ^= 1;
+                tc_fence_after();
+                phase_tile_from_tmem(x, TM_U, CB_UT);
+                fence_proxy_async();
+                cta_sync_tc();
+                if (abort_flag) {
+                    break;
+                }
+                // S^T += U^T Kend, O^T += U^T Aqk^T; then the next chunk's U'
+                if (tid == 0) {
+                    issue_os(x, st);
+                    mma_commit(&bar_os);
+                    if (c + 1 < nch && (fetched >= c + 2 || fetch(c + 1, true))) {
+                        const uint32_t r = cnt + c + 1;
+                        if (mbar_wait(&bar_full[r & 1], (r >> 1) & 1, &abort_flag)) {
+                            tc_fence_after();
+                            issue_u_prime(x, tiles(r & 1));
+                        } else {
+                            record_timeout(p.status, &abort_flag);
+                        }
+                    }
+                }
+                if (!mbar_wait(&bar_os, ph_os, &abort_flag)) {
+                    record_timeout(p.status, &abort_flag);
+                }
+                ph_os ^= 1;
+                tc_fence_after();
+                // this chunk's buffer is free: copy chunk c + 2 into it if it is ready
+                if (tid == 0 && c + 2 < nch && fetched == c + 2) {
+                    fetch(c + 2, false);
+                }
+                if (c + 1 < nch) {
+                    wait_full(c + 1);
+                }
+                // O^T -> o, and the next chunk's S^T -> bf16 operand (the loop
+                // condition, read after the barrier below, handles an abort)
+                phase_o_epilogue(x, o_g, bos + c * C, min(C, len - c * C), h, H);
+                if (c + 1 < nch) {
+                    phase_state_to_operand(x, CB_ST);
+                }
+                fence_proxy_async();
+                cta_sync_tc();
             }
-            // S^T -> bf16 operand, S^T *= Gamma_C (all 16 warps, 32 columns each)
-            phase_state_epilogue(x, reinterpret_cast<const float*>(sm + st.gam), st.st, 0, 4);
-            fence_proxy_async();
-            tc_fence_before();
-            if (!mbar_wait(&bar_mma, ph_mma, &abort_flag)) {
-                record_timeout(p.status, &abort_flag);
-            }
-            ph_mma ^= 1;
-            tc_fence_after();
-            __syncthreads();
-            if (abort_flag) {
-                break;
-            }
+            // copies still in flight into this CTA's buffers (a loop left early)
             if (tid == 0) {
-                issue_uo(x, st);
-                mma_commit(&bar_mma);
+                s_issued = fetched;
             }
-            if (!mbar_wait(&bar_mma, ph_mma, &abort_flag)) {
-                record_timeout(p.status, &abort_flag);
-            }
-            ph_mma ^= 1;
-            tc_fence_after();
             __syncthreads();
-            if (abort_flag) {
-                break;
+            const int issued = s_issued;
+            for (int c = waited; c < issued; ++c) {
+                const uint32_t r = cnt + c;
+                mbar_wait(&bar_full[r & 1], (r >> 1) & 1, nullptr);
             }
-            phase_tile_from_tmem(x, TM_U, st.ut);
-            fence_proxy_async();
+            cnt += issued;
+            if (!abort_flag && p.final_state) {
+                store_state(x, p.final_state + state_off);
+            }
             cta_sync_tc();
-            if (tid == 0) {
-                issue_os(x, st);
-                mma_commit(&bar_mma);
+            if (tid == 32 && !abort_flag) {  // skip the stream positions this unit leaves unused
+                st_release(p.cons_done + i, meta.g0[bt + 1]);
             }
-            if (!mbar_wait(&bar_mma, ph_mma, &abort_flag)) {
-                record_timeout(p.status, &abort_flag);
-            }
-            ph_mma ^= 1;
-            tc_fence_after();
-            __syncthreads();
-            if (abort_flag) {
-                break;
-            }
-            phase_o_epilogue(x, o_g, t0, L, h, H);
-            cta_sync_tc();
-        }
-        // drain copies still in flight into this CTA's smem (early exit only)
-        if (tid == 0) {
-            s_issued = issued;
-        }
-        __syncthreads();
-        for (int c = waited; c < s_issued; ++c) {
-            mbar_wait(&bar_full[c & 1], (c >> 1) & 1, nullptr);
-        }
-        if (!abort_flag && p.final_state) {
-            store_state(x, p.final_state + state_off);
         }
     } else {
         // ------------------------------------------------------------ producer
-        int max_chunks = 0;
-        for (int m = 0; m < p.N; ++m) {
-            int64_t b, e;
-            seq_bounds(p, m, b, e);
-            const int nc = (int)((e - b + C - 1) / C);
-            max_chunks = nc > max_chunks ? nc : max_chunks;
-        }
-        const int ntasks = max_chunks * U;
+        const int total = meta.task0[p.n_batches];
         float* s_beta = reinterpret_cast<float*>(sm + OFF_BETA);
-        // task t = (chunk t / U, unit t % U), chunk-major; tasks past the end of
-        // their sequence are skipped.  Thread 0 only.
-        auto grab_valid = [&]() -> int {
-            for (;;) {
-                const int t = atomicAdd(p.work_counter, 1);
-                if (t >= ntasks) {
-                    return ntasks;
-                }
-                int64_t b, e;
-                seq_bounds(p, (t % U) / H, b, e);
-                if (t / U < (int)((e - b + C - 1) / C)) {
-                    return t;
-                }
-            }
-        };
-        auto issue_raw = [&](int t) {
-            const int hh = (t % U) % H;
-            int64_t b, e;
-            seq_bounds(p, (t % U) / H, b, e);
-            const int tt0 = (int)(b + (int64_t)(t / U) * C);
+        int32_t* ctr = p.work_counter;
+        auto issue_raw = [&](const SplitTask& tk) {
             mbar_arrive_expect_tx(&bar_raw, 3 * 16384);
-            tma_load_3d(sm + OFF_RAWQ, &args.tm_q, 0, hh, tt0, &bar_raw);
-            tma_load_3d(sm + OFF_RAWK, &args.tm_k, 0, hh, tt0, &bar_raw);
-            tma_load_3d(sm + OFF_RAWZ, &args.tm_z, 0, hh, tt0, &bar_raw);
+            tma_load_3d(sm + OFF_RAWQ, &args.tm_q, 0, tk.h, tk.t0, &bar_raw);
+            tma_load_3d(sm + OFF_RAWK, &args.tm_k, 0, tk.h, tk.t0, &bar_raw);
+            tma_load_3d(sm + OFF_RAWZ, &args.tm_z, 0, tk.h, tk.t0, &bar_raw);
         };
-        uint32_t ph_raw = 0;
-        bool raw_pending = false;      // a raw load is in flight (uniform after each barrier)
+        // thread 0: the first valid task at or after counter value t
+        auto next_valid = [&](int t) -> int {
+            SplitTask tk;
+            while (t < total && !decode_task(meta, p, t, tk)) {
+                t = atomicAdd(ctr, 1);
+            }
+            return t;
+        };
         if (tid == 0) {
-            s_task = grab_valid();
-            if (s_task < ntasks) {
-                issue_raw(s_task);
+            const int t = next_valid(atomicAdd(ctr, 1));
+            s_next = t;
+            if (t < total) {
+                SplitTask tk;
+                decode_task(meta, p, t, tk);
+                issue_raw(tk);
             }
         }
         __syncthreads();
-        int task = s_task;
-        raw_pending = task < ntasks;
-        while (task < ntasks && !abort_flag) {
-            const int c = task / U;
-            const int unit = task % U;
-            const int n = unit / H;
-            const int h = unit % H;
-            int64_t bos, eos;
-            seq_bounds(p, n, bos, eos);
-            const int64_t t0 = bos + (int64_t)c * C;
-            const int L = (int)((eos - t0) < C ? (eos - t0) : C);
-            const int64_t slot = (chunk_base(p, n) + c) * H + h;
-            const float eA_log2 = exp2_approx(p.A[h] * kLog2e) * kLog2e;
-            // beta: loaded now, stored to shared memory once the prologue is done
-            float beta_r = 0.0f;
-            if (tid < L) {
-                beta_r = __bfloat162float(beta_g[(size_t)(t0 + tid) * H + h]);
+        int t = s_next;
+        bool raw_pending = t < total;
+        uint32_t ph_raw = 0, ph_mma = 0;
+        float beta_r = 0.0f;   // this thread's beta of the current task (tid < 64)
+        if (t < total) {
+            SplitTask tk;
+            decode_task(meta, p, t, tk);
+            if (tid < tk.L) {
+                beta_r = __bfloat162float(beta_g[(size_t)(tk.t0 + tid) * H + tk.h]);
+            }
+        }
+        // thread 0: the last published slot, flagged once its bulk store completes
+        bool store_pending = false;
+        int32_t pend_slot = 0, pend_val = 0;
+        while (t < total && !abort_flag) {
+            SplitTask cur;
+            decode_task(meta, p, t, cur);
+            // candidate for the next task; its latency hides behind the prologue
+            int t_ahead = 0;
+            if (tid == 0) {
+                t_ahead = atomicAdd(ctr, 1);
             }
             if (mbar_wait(&bar_raw, ph_raw, &abort_flag)) {
                 ph_raw ^= 1;
@@ -615,19 +772,27 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
             } else {
                 record_timeout(p.status, &abort_flag);
             }
+            if (tid == 0 && store_pending) {  // publish the last slot
+                bulk_wait();
+                fence_proxy_async_global();
+                st_release(p.flags + pend_slot, pend_val);
+                store_pending = false;
+            }
             __syncthreads();
             if (abort_flag) {
                 break;
             }
-            phase_norms(x, L, p.scale, p.l2norm);
+            phase_norms(x, cur.L, p.scale, p.l2norm);
             __syncthreads();
-            phase_prologue(x, L, eA_log2);
-            // every thread has passed the prologue's barrier: the raw tiles are
-            // consumed, fetch the next task's
+            phase_prologue(x, cur.L, meta.eA[cur.h]);
+            // the raw tiles are consumed: fetch the next task's
             if (tid == 0) {
-                s_task = grab_valid();
-                if (s_task < ntasks) {
-                    issue_raw(s_task);
+                const int tn = next_valid(t_ahead);
+                s_next = tn;
+                if (tn < total) {
+                    SplitTask nt;
+                    decode_task(meta, p, tn, nt);
+                    issue_raw(nt);
                 }
             }
             if (tid < C) {
@@ -635,7 +800,16 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
             }
             fence_proxy_async();
             cta_sync_tc();
-            raw_pending = s_task < ntasks;
+            const int tn = s_next;
+            raw_pending = tn < total;
+            beta_r = 0.0f;
+            if (tn < total) {
+                SplitTask nt;
+                decode_task(meta, p, tn, nt);
+                if (tid < nt.L) {
+                    beta_r = __bfloat162float(beta_g[(size_t)(nt.t0 + tid) * H + nt.h]);
+                }
+            }
             if (tid == 0) {
                 issue_gram(x);
                 mma_commit(&bar_mma);
@@ -670,32 +844,44 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 break;
             }
             phase_tile_from_tmem(x, TM_W, OFF_WT);
+            fence_proxy_async();
             __syncthreads();
-            // publish: the slot is an image of the operand tiles
-            uint4* dst = reinterpret_cast<uint4*>(p.handoff + slot * HO_BYTES);
-            const uint32_t src_off[6] = {OFF_WT, OFF_QP, OFF_KE, OFF_AQK, OFF_TM, OFF_GAM};
-            const uint32_t dst_off[6] = {HO_WT, HO_QP, HO_KE, HO_AQK, HO_TM, HO_GAM};
-            const uint32_t nbytes[6] = {16384, 16384, 16384, 8192, 8192, 512};
-#pragma unroll
-            for (int t = 0; t < 6; ++t) {
-                const uint4* src = reinterpret_cast<const uint4*>(sm + src_off[t]);
-                uint4* d = dst + dst_off[t] / 16;
-                for (uint32_t e = tid; e < nbytes[t] / 16; e += kThreads) {
-                    d[e] = src[e];
+            // store the slot once the consumer has copied out the chunk that was in it
+            if (tid == 0) {
+                const int32_t slot = cur.i * p.ring + cur.g % p.ring;
+                if (wait_at_least(p.cons_done + cur.i, cur.g - p.ring + 1, &abort_flag)) {
+                    fence_proxy_async_global();
+                    uint8_t* dst = p.handoff + (size_t)slot * HO_BYTES;
+                    bulk_store(dst + HO_AQK, sm + OFF_AQK, 32768);  // Aqk | Tm | W^T
+                    bulk_store(dst + HO_QP, sm + OFF_QP, 32768);    // Q+ | Kend
+                    bulk_store(dst + HO_GAM, sm + OFF_GAM, 512);
+                    bulk_commit();
+                    store_pending = true;
+                    pend_slot = slot;
+                    pend_val = cur.g + 1;
+                } else {
+                    record_timeout(p.status, &abort_flag);
                 }
             }
-            __threadfence();
-            __syncthreads();
-            if (tid == 0) {
-                asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.flags + slot), "r"(1)
-                             : "memory");
+            t = tn;
+        }
+        if (tid == 0 && store_pending) {
+            bulk_wait();
+            if (!abort_flag) {
+                fence_proxy_async_global();
+                st_release(p.flags + pend_slot, pend_val);
             }
-            task = s_task;
         }
         // a loop left early may still have a raw load in flight into this CTA's smem
         if (raw_pending) {
             mbar_wait(&bar_raw, ph_raw, nullptr);
         }
+    }
+    // no MMA of this CTA may still be running when its TMEM is freed
+    cta_sync_tc();
+    if (tid == 0) {
+        mma_commit(&bar_fin);
+        mbar_wait(&bar_fin, 0, nullptr);
     }
     cta_sync_tc();
     if (x.warp == 0) {
@@ -748,22 +934,50 @@ size_t chunked_workspace_bytes(int32_t N, int32_t H) {
     return 256 + (size_t)N * H * sizeof(int32_t);
 }
 
-size_t split_slots_bound(int32_t N, int32_t total_T, int32_t H) {
-    return (size_t)H * ((size_t)(total_T + C - 1) / C + (size_t)N);
+namespace {
+constexpr int32_t kSplitRing = 8;  // slots per consumer
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+size_t split_flags_offset() { return 256; }
+size_t split_done_offset(const SplitPlan& plan) {
+    return split_flags_offset() + round256((size_t)plan.consumers * plan.ring * sizeof(int32_t));
+}
+}  // namespace
+
+bool split_plan(int32_t N, int32_t H, int num_sms, SplitPlan* plan) {
+    if (num_sms < 8 || N < 1 || H < 1 || N > kSplitMaxSeqs || H > kSplitMaxHeads) {
+        return false;
+    }
+    // producers need most of the GPU: at most a quarter of the SMs are consumers
+    const int64_t U = (int64_t)N * H;
+    const int64_t max_cons = num_sms / 4;
+    int64_t batches = (U + max_cons - 1) / max_cons;
+    if (batches > kSplitMaxBatches) {
+        return false;
+    }
+    const int64_t cons = (U + batches - 1) / batches;  // even batches
+    batches = (U + cons - 1) / cons;                    // none left empty
+    plan->consumers = (int32_t)cons;
+    plan->batches = (int32_t)batches;
+    plan->ring = kSplitRing;
+    return true;
 }
 
-size_t split_handoff_offset(int32_t N, int32_t total_T, int32_t H) {
-    const size_t flags = split_slots_bound(N, total_T, H) * sizeof(int32_t);
-    return 256 + (flags + 255) / 256 * 256;
+size_t split_zeroed_bytes(const SplitPlan& plan) {
+    return split_done_offset(plan) + round256((size_t)plan.consumers * sizeof(int32_t));
 }
 
-size_t split_workspace_bytes(int32_t N, int32_t total_T, int32_t H) {
-    return split_handoff_offset(N, total_T, H) + split_slots_bound(N, total_T, H) * HO_BYTES;
+size_t split_workspace_bytes(const SplitPlan& plan) {
+    return split_zeroed_bytes(plan) + (size_t)plan.consumers * plan.ring * HO_BYTES;
 }
 
-int split_max_units(int num_sms) {
-    // producers need most of the GPU: at most a third of the SMs are consumers
-    return num_sms / 3;
+void split_bind(const SplitPlan& plan, void* workspace, ChunkedParams* p) {
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p->flags = reinterpret_cast<int32_t*>(ws + split_flags_offset());
+    p->cons_done = reinterpret_cast<int32_t*>(ws + split_done_offset(plan));
+    p->handoff = ws + split_zeroed_bytes(plan);
+    p->n_cons = plan.consumers;
+    p->n_batches = plan.batches;
+    p->ring = plan.ring;
 }
 
 cudaError_t launch_chunked_prefill(const ChunkedParams& p, cudaStream_t stream) {
@@ -796,7 +1010,7 @@ cudaError_t launch_split_prefill(const ChunkedParams& p, int num_sms, cudaStream
     if (err != cudaSuccess) {
         return err;
     }
-    // p.flags was zeroed by the caller on this stream
+    // the ring flags and consumer counters were zeroed by the caller on this stream
     kda_split_kernel<<<(unsigned)num_sms, kThreads, SMEM_BYTES, stream>>>(args);
     return cudaGetLastError();
 }
