@@ -76,8 +76,8 @@ enum {
  *
  * Any workspace of at least 256 + 4 * N * H bytes (rounded up to 256) is
  * accepted.  With bf16 and d_k = d_v = 128 (up to 1024 sequences and 256
- * heads), a larger workspace -- the size returned here, about 0.5 MB per
- * consumer CTA (a quarter of the SMs at most, ~20 MB on 152 SMs) whatever the
+ * heads), a larger workspace -- the size returned here, about 0.8 MB per
+ * consumer CTA (a quarter of the SMs at most, ~30 MB on 152 SMs) whatever the
  * sequence lengths -- selects the split kernel, which spreads each
  * (sequence, head) pair's chunks over all SMs and passes every chunk's
  * operand tiles through a ring of slots in the workspace; a smaller one

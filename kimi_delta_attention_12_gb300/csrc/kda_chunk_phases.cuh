@@ -72,6 +72,18 @@ constexpr uint32_t OFF_GAM = OFF_TOT + 2048;  // [128]
 constexpr uint32_t SMEM_USED = OFF_GAM + 512;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
 
+// A published chunk (split mode): the operand tiles the state chain needs,
+// laid out as the shared-memory tiles are, so one bulk copy loads it.
+// Q+ and -W^T are adjacent MN-major N-blocks (one N = 128 B operand), and so
+// are the K-major rows of Kend and Aqk (one N = 192 B operand).
+constexpr uint32_t HO_QP = 0;        // Q+    bf16 [128 c][64 r]
+constexpr uint32_t HO_WT = 16384;    // -W^T  bf16 [128 c][64 r]
+constexpr uint32_t HO_KE = 32768;    // Kend  bf16 [128 c][64 i]
+constexpr uint32_t HO_AQK = 49152;   // Aqk   bf16 [64 r][64 i]
+constexpr uint32_t HO_TM = 57344;    // Tm    bf16 [64 r][64 i]
+constexpr uint32_t HO_GAM = 65536;   // Gamma_C fp32 [128]
+constexpr uint32_t HO_BYTES = 66048; // multiple of 256
+
 // TMEM columns
 constexpr uint32_t TM_S = 0;      // S^T  [128 j lanes][128 c]
 constexpr uint32_t TM_G1 = 128;   // Gram blocks 3, 2
@@ -248,12 +260,24 @@ __device__ __forceinline__ void phase_norms(const Ctx& x, int L, float scale, in
 // Q+, Kend, plus Gamma_C = e^{gamma_C} (fp32, OFF_GAM).  Each thread owns one
 // channel and 16 tokens.  Contains one CTA barrier; the caller must have
 // synchronised after phase_norms.
-__device__ __forceinline__ void phase_prologue(const Ctx& x, int L, float eA_log2) {
+// kPub (split producer): Q+, Kend and Gamma_C go straight to the published
+// chunk at `pub` (global memory) instead of shared memory.  after_gate() runs
+// right after the barrier (every thread).
+struct NoHook {
+    __device__ void operator()() const {}
+};
+template <bool kPub = false, typename Hook = NoHook>
+__device__ __forceinline__ void phase_prologue(const Ctx& x, int L, float eA_log2,
+                                               uint8_t* pub = nullptr,
+                                               Hook after_gate = Hook()) {
     uint8_t* sm = x.sm;
     const float* s_invq = reinterpret_cast<const float*>(sm + OFF_INVQ);
     const float* s_invk = reinterpret_cast<const float*>(sm + OFF_INVK);
     float* s_tot = reinterpret_cast<float*>(sm + OFF_TOT);
-    float* s_gam = reinterpret_cast<float*>(sm + OFF_GAM);
+    float* s_gam = kPub ? reinterpret_cast<float*>(pub + HO_GAM)
+                        : reinterpret_cast<float*>(sm + OFF_GAM);
+    uint8_t* qp_tile = kPub ? pub + HO_QP : sm + OFF_QP;
+    uint8_t* ke_tile = kPub ? pub + HO_KE : sm + OFF_KE;
     const int c = x.tid & (D - 1);   // channel
     const int ab = x.tid >> 7;       // token block: tokens 16ab .. 16ab+15
     float qh[16], kh[16], al[16];
@@ -279,6 +303,7 @@ __device__ __forceinline__ void phase_prologue(const Ctx& x, int L, float eA_log
         s_tot[ab * D + c] = tot;
     }
     __syncthreads();
+    after_gate();
 
     float t[4];
 #pragma unroll
@@ -319,7 +344,7 @@ __device__ __forceinline__ void phase_prologue(const Ctx& x, int L, float eA_log
     // Q+ = q e^{gamma} = (q e^{gamma - rho_a}) e^{rho_a}
 #pragma unroll
     for (int rr = 0; rr < 16; ++rr) v[rr] *= eRa;
-    store_row16(sm + OFF_QP, c, 32 * ab, v);
+    store_row16(qp_tile, c, 32 * ab, v);
 #pragma unroll
     for (int rr = 0; rr < 16; ++rr) v[rr] = kh[rr] * E[rr];
     store_row16(xt, c, 2 * (e0 + 16), v);
@@ -333,7 +358,7 @@ __device__ __forceinline__ void phase_prologue(const Ctx& x, int L, float eA_log
     // Kend = k e^{gamma_C - gamma}
 #pragma unroll
     for (int rr = 0; rr < 16; ++rr) v[rr] = G[rr] * eEnd;
-    store_row16(sm + OFF_KE, c, 32 * ab, v);
+    store_row16(ke_tile, c, 32 * ab, v);
     // K~^(ab) = k e^{rho_a - gamma}: M-block (3 - ab) of the Gram A operand
 #pragma unroll
     for (int rr = 0; rr < 16; ++rr) v[rr] = G[rr] * cF;
@@ -368,7 +393,10 @@ __device__ __forceinline__ void issue_gram(const Ctx& x) {
 // Gram -> Akk (fp32, beta-scaled, strictly lower) and Aqk (bf16 tile, lower).
 // Warps 0-3: blocks 3 (lanes 0-63) and 2 (lanes 64-127) of TM_G1; warps 4-7:
 // blocks 1 and 0 of TM_G2.
-__device__ __forceinline__ void phase_gram_epilogue(const Ctx& x) {
+// kPub: Aqk goes straight to the published chunk at `pub`.
+template <bool kPub = false>
+__device__ __forceinline__ void phase_gram_epilogue(const Ctx& x, uint8_t* pub = nullptr) {
+    uint8_t* aqk_tile = kPub ? pub + HO_AQK : x.sm + OFF_AQK;
     const float* s_beta = reinterpret_cast<const float*>(x.sm + OFF_BETA);
     float* akk = reinterpret_cast<float*>(x.sm + OFF_AKK);
     const int g = x.warp >> 2;
@@ -386,7 +414,7 @@ __device__ __forceinline__ void phase_gram_epilogue(const Ctx& x) {
         const float aq = i <= r ? __uint_as_float(vq[rr]) : 0.0f;
         const float ak = i < r ? s_beta[r] * __uint_as_float(vk[rr]) : 0.0f;
         akk[r * 65 + i] = ak;
-        *reinterpret_cast<__nv_bfloat16*>(x.sm + OFF_AQK + sw128(r, 2 * i)) =
+        *reinterpret_cast<__nv_bfloat16*>(aqk_tile + sw128(r, 2 * i)) =
             __float2bfloat16_rn(aq);
     }
 }
@@ -429,29 +457,39 @@ __device__ __forceinline__ void phase_state_epilogue(const Ctx& x, const float* 
     tmem_wait_st();
 }
 
-// The two halves of phase_state_epilogue for the split kernel's consumer, all
-// 16 warps, 32 columns each: S^T (TMEM) -> bf16 A-operand tile (no barrier) ...
-__device__ __forceinline__ void phase_state_to_operand(const Ctx& x, uint32_t st_tile) {
-    const int j = 32 * x.qd + x.lane;
+// ---------------------------------------------------------------- split consumer
+// The split kernel's consumer keeps the bf16 copies of S^T and U^T that feed
+// the tensor core in TMEM (A operands read from TMEM: lane = row, two K
+// elements per column) and places its accumulators so that one instruction
+// computes two products: [O^T | U^T] += S^T [Q+^T | -W^T] (N = 128) and
+// [S^T | O^T] += U^T [Kend ; Aqk] (N = 192).
+constexpr uint32_t TC_S = 0;      // S^T  fp32 [128 j][128 c]
+constexpr uint32_t TC_O = 128;    // O^T  fp32 [128 j][64 r]
+constexpr uint32_t TC_U = 192;    // U^T  fp32 [128 j][64 r]
+constexpr uint32_t TC_SB = 256;   // S^T  bf16, 64 columns
+constexpr uint32_t TC_UB = 320;   // U^T  bf16, 32 columns
+
+// S^T (TMEM, fp32) -> bf16 at TC_SB; all 16 warps, 32 c each.  No barrier.
+__device__ __forceinline__ void phase_state_to_tmem(const Ctx& x) {
     const int cb = 32 * x.sub;
     uint32_t r0[16], r1[16];
-    tmem_ld16(x.tbase + x.lane_base + TM_S + cb, r0);
-    tmem_ld16(x.tbase + x.lane_base + TM_S + cb + 16, r1);
+    tmem_ld16(x.tbase + x.lane_base + TC_S + cb, r0);
+    tmem_ld16(x.tbase + x.lane_base + TC_S + cb + 16, r1);
     tmem_wait_ld();
-    float v0[16], v1[16];
+    uint32_t w[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        v0[i] = __uint_as_float(r0[i]);
-        v1[i] = __uint_as_float(r1[i]);
+    for (int i = 0; i < 8; ++i) {
+        w[i] = pack_bf16x2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
+        w[8 + i] = pack_bf16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
     }
-    store_row16(x.sm + st_tile + (cb / 64) * 16384, j, 2 * (cb % 64), v0);
-    store_row16(x.sm + st_tile + (cb / 64) * 16384, j, 2 * (cb % 64) + 32, v1);
+    tmem_st16(x.tbase + x.lane_base + TC_SB + cb / 2, w);
+    tmem_wait_st();
 }
 
-// ... and S^T *= Gamma_C in TMEM (no barrier; waits for its own stores).
+// S^T *= Gamma_C in TMEM; all 16 warps, 32 c each.  No barrier.
 __device__ __forceinline__ void phase_state_decay(const Ctx& x, const float* gam) {
     const int cb = 32 * x.sub;
-    const uint32_t taddr = x.tbase + x.lane_base + TM_S + cb;
+    const uint32_t taddr = x.tbase + x.lane_base + TC_S + cb;
     uint32_t r0[16], r1[16];
     tmem_ld16(taddr, r0);
     tmem_ld16(taddr + 16, r1);
@@ -466,6 +504,75 @@ __device__ __forceinline__ void phase_state_decay(const Ctx& x, const float* gam
     tmem_wait_st();
 }
 
+// U^T (TMEM, fp32) -> bf16 at TC_UB; all 16 warps, 16 r each.  No barrier.
+__device__ __forceinline__ void phase_u_to_tmem(const Ctx& x) {
+    uint32_t r[16];
+    tmem_ld16(x.tbase + x.lane_base + TC_U + 16 * x.sub, r);
+    tmem_wait_ld();
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        w[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+    }
+    tmem_st8(x.tbase + x.lane_base + TC_UB + 8 * x.sub, w);
+    tmem_wait_st();
+}
+
+// O^T (TMEM lane j, column r) -> o (bf16), then O^T = 0 for the next chunk's
+// accumulation.  Each warp handles 16 tokens of its 32 value columns; for a
+// token the warp's lanes cover 64 contiguous bytes of o.  No barrier.
+__device__ __forceinline__ void phase_ot_epilogue_zero(const Ctx& x, __nv_bfloat16* o_g,
+                                                       int64_t t0, int L, int h, int H) {
+    const int j = 32 * x.qd + x.lane;
+    const int r0 = 16 * x.sub;
+    const uint32_t taddr = x.tbase + x.lane_base + TC_O + r0;
+    uint32_t r[16];
+    tmem_ld16(taddr, r);
+    tmem_wait_ld();
+    __nv_bfloat16* dst = o_g + ((size_t)(t0 + r0) * H + h) * D + j;
+    const size_t row = (size_t)H * D;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        if (r0 + i < L) {
+            dst[i * row] = __float2bfloat16_rn(__uint_as_float(r[i]));
+        }
+        r[i] = 0u;
+    }
+    tmem_st16(taddr, r);
+    tmem_wait_st();
+}
+
+// (one thread) O^T = 0 in TMEM is the caller's; U'^T = V^T Tm^T into TC_U.
+__device__ __forceinline__ void issue_u_prime_tc(const Ctx& x, const StateTiles& st) {
+    const uint32_t idu = idesc_bf16(128, 64, 1, 0);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t bT = smem_desc(x.smem_base + st.tm + kk * 32, 16, 1024);
+        const uint64_t aV = smem_desc(x.smem_base + st.v + kk * 2048, 8192, 1024);
+        mma_bf16(x.tbase + TC_U, aV, bT, idu, kk > 0);
+    }
+}
+
+// (one thread) [O^T | U^T] += S^T [Q+^T | -W^T]: st.qp holds Q+ then -W^T.
+__device__ __forceinline__ void issue_ou_tc(const Ctx& x, const StateTiles& st) {
+    const uint32_t id = idesc_bf16(128, 128, 0, 1);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint64_t b = smem_desc(x.smem_base + st.qp + kk * 2048, 16384, 1024);
+        mma_bf16_ta(x.tbase + TC_O, x.tbase + TC_SB + kk * 8, b, id, 1);
+    }
+}
+
+// (one thread) [S^T | O^T] += U^T [Kend ; Aqk]: st.ke holds Kend then Aqk rows.
+__device__ __forceinline__ void issue_so_tc(const Ctx& x, const StateTiles& st) {
+    const uint32_t id = idesc_bf16(128, 192, 0, 0);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t b = smem_desc(x.smem_base + st.ke + kk * 32, 16, 1024);
+        mma_bf16_ta(x.tbase + TC_S, x.tbase + TC_UB + kk * 8, b, id, 1);
+    }
+}
+
 // ---------------------------------------------------------------- P4
 // UT solve  Tm = (I + Akk)^-1 Diag(beta) -> bf16 tile at OFF_TM.
 // N = (I + L)^-1, L = Akk strictly lower, in 16x16 blocks:
@@ -476,7 +583,9 @@ __device__ __forceinline__ void phase_state_decay(const Ctx& x, const float* gam
 //   waves 1..3: N_ab = -sum_{c=b}^{a-1} B_ac N_cb for a - b = wave.
 // All products are warp-level tf32 MMAs.  Contains CTA barriers; the caller
 // must have synchronised after phase_gram_epilogue.
-__device__ __forceinline__ void phase_solve(const Ctx& x) {
+// kPub: Tm is also copied to the published chunk at `pub`.
+template <bool kPub = false>
+__device__ __forceinline__ void phase_solve(const Ctx& x, uint8_t* pub = nullptr) {
     const float* s_beta = reinterpret_cast<const float*>(x.sm + OFF_BETA);
     float* Lm = reinterpret_cast<float*>(x.sm + OFF_AKK);
     float* Nm = reinterpret_cast<float*>(x.sm + OFF_NMAT);
@@ -532,6 +641,9 @@ __device__ __forceinline__ void phase_solve(const Ctx& x) {
         w.x = pack_bf16x2(v[0], v[1]); w.y = pack_bf16x2(v[2], v[3]);
         w.z = pack_bf16x2(v[4], v[5]); w.w = pack_bf16x2(v[6], v[7]);
         *reinterpret_cast<uint4*>(x.sm + OFF_TM + sw128(r, 2 * i0)) = w;
+        if (kPub) {
+            *reinterpret_cast<uint4*>(pub + HO_TM + sw128(r, 2 * i0)) = w;
+        }
     }
 }
 
@@ -561,6 +673,17 @@ __device__ __forceinline__ void issue_u_prime(const Ctx& x, const StateTiles& st
 // ---------------------------------------------------------------- P6 / P8
 // A 128-lane x 64-token fp32 TMEM block -> bf16 tile rows (lane = row), 16
 // tokens per warp (all 16 warps).  No barrier.
+__device__ __forceinline__ void phase_tile_from_tmem_to(const Ctx& x, uint32_t tm_col,
+                                                        uint8_t* tile, float sign = 1.0f) {
+    uint32_t r[16];
+    tmem_ld16(x.tbase + x.lane_base + tm_col + 16 * x.sub, r);
+    tmem_wait_ld();
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = sign * __uint_as_float(r[i]);
+    store_row16(tile, 32 * x.qd + x.lane, 32 * x.sub, v);
+}
+
 __device__ __forceinline__ void phase_tile_from_tmem(const Ctx& x, uint32_t tm_col, uint32_t tile) {
     uint32_t r[16];
     tmem_ld16(x.tbase + x.lane_base + tm_col + 16 * x.sub, r);

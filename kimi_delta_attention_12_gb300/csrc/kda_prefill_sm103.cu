@@ -67,26 +67,11 @@ struct ChunkedArgs {
     ChunkedParams p;
 };
 
-// ---- split mode: one published chunk (a workspace slot), byte offsets ----
-// The slot mirrors two contiguous runs of the producer's shared memory
-// (Aqk | Tm | W^T and Q+ | Kend) plus Gamma_C, so three bulk copies store it.
-constexpr uint32_t HO_AQK = 0;
-constexpr uint32_t HO_TM = 8192;
-constexpr uint32_t HO_WT = 16384;
-constexpr uint32_t HO_QP = 32768;
-constexpr uint32_t HO_KE = 49152;
-constexpr uint32_t HO_GAM = 65536;
-static_assert(OFF_TM == OFF_AQK + 8192 && OFF_WT == OFF_TM + 8192 && OFF_KE == OFF_QP + 16384,
-              "slot runs must be contiguous in the producer's shared memory");
-static_assert(OFF_GAM % 16 == 0 && OFF_AQK % 16 == 0 && OFF_QP % 16 == 0,
-              "bulk copies need 16-byte aligned sources");
-constexpr uint32_t HO_BYTES = 66048;           // multiple of 256
-// consumer shared memory: two buffers of [slot | v tile], then S^T and U^T
+// consumer shared memory: two buffers of [slot | v tile] (its bf16 S^T and
+// U^T operands live in TMEM)
 constexpr uint32_t CB_V = 66560;               // v tile inside a buffer (1024-aligned)
 constexpr uint32_t CB_BYTES = CB_V + 16384;    // 82944
-constexpr uint32_t CB_ST = 2 * CB_BYTES;       // 165888
-constexpr uint32_t CB_UT = CB_ST + 32768;      // 198656
-static_assert(CB_UT + 16384 <= SMEM_USED, "consumer layout exceeds the shared memory budget");
+static_assert(2 * CB_BYTES <= SMEM_USED, "consumer layout exceeds the shared memory budget");
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) &
@@ -395,22 +380,6 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint
         : "memory");
 }
 
-__device__ __forceinline__ void bulk_store(void* gdst, const void* smem_src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
-                     reinterpret_cast<uint64_t>(gdst)),
-                 "r"(smem_u32(smem_src)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() {
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-// this thread's bulk stores are complete
-__device__ __forceinline__ void bulk_wait() {
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
 // Sequence and batch tables, built by every CTA at start.
 struct SplitMeta {
     int32_t cu[kSplitMaxSeqs + 1];       // token start of each sequence (and total_T)
@@ -473,6 +442,7 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
     __shared__ uint32_t tmem_base_s;
     __shared__ int s_next;
     __shared__ int s_issued;
+    __shared__ int s_slot_free;
     __shared__ volatile int abort_flag;
 
     const int tid = threadIdx.x;
@@ -564,10 +534,17 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
         auto tiles = [&](uint32_t b) -> StateTiles {
             const uint32_t cb = b * CB_BYTES;
             return StateTiles{cb + HO_WT, cb + HO_QP,  cb + HO_KE, cb + HO_AQK, cb + HO_TM,
-                              cb + HO_GAM, cb + CB_V, CB_ST,      CB_UT};
+                              cb + HO_GAM, cb + CB_V, 0,          0};
         };
         uint32_t cnt = 0;  // buffer fills so far (buffer = count & 1, parity = (count >> 1) & 1)
         uint32_t ph_u = 0, ph_os = 0;
+        {   // O^T starts at zero; every chunk's output epilogue zeroes it again
+            uint32_t z[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) z[k] = 0u;
+            tmem_st16(x.tbase + x.lane_base + TC_O + 16 * x.sub, z);
+            tmem_wait_st();
+        }
         for (int bt = 0; bt < p.n_batches && !abort_flag; ++bt) {
             const int unit = bt * p.n_cons + i;
             if (unit >= U) {
@@ -629,47 +606,42 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 wait_full(0);
                 tc_fence_after();
                 if (tid == 0 && !abort_flag) {
-                    issue_u_prime(x, tiles(cnt & 1));   // U'^T = V^T Tm^T into TM_U
+                    issue_u_prime_tc(x, tiles(cnt & 1));   // U'^T = V^T Tm^T
                 }
-                phase_state_to_operand(x, CB_ST);
-                fence_proxy_async();
+                phase_state_to_tmem(x);
                 cta_sync_tc();
             }
             for (int c = 0; c < nch && !abort_flag; ++c) {
                 const StateTiles st = tiles((cnt + c) & 1);
-                // U^T += S^T (-W^T) (after U'), then O^T = S^T Q+^T
+                // [O^T | U^T] += S^T [Q+^T | -W^T]  (U^T holds U', O^T zero)
                 if (tid == 0) {
-                    issue_u(x, st);
+                    issue_ou_tc(x, st);
                     mma_commit(&bar_u);
-                }
-                // S^T *= Gamma_C while the tensor core works
-                phase_state_decay(x, reinterpret_cast<const float*>(sm + st.gam));
-                if (tid == 0) {
-                    issue_o(x, st);
                     if (fetched == c + 1 && c + 1 < nch) {
                         fetch(c + 1, false);
                     }
                 }
+                // S^T *= Gamma_C while the tensor core works
+                phase_state_decay(x, reinterpret_cast<const float*>(sm + st.gam));
                 if (!mbar_wait(&bar_u, ph_u, &abort_flag)) {
                     record_timeout(p.status, &abort_flag);
                 }
                 ph_u ^= 1;
                 tc_fence_after();
-                phase_tile_from_tmem(x, TM_U, CB_UT);
-                fence_proxy_async();
+                phase_u_to_tmem(x);
                 cta_sync_tc();
                 if (abort_flag) {
                     break;
                 }
-                // S^T += U^T Kend, O^T += U^T Aqk^T; then the next chunk's U'
+                // [S^T | O^T] += U^T [Kend ; Aqk]; then the next chunk's U'
                 if (tid == 0) {
-                    issue_os(x, st);
+                    issue_so_tc(x, st);
                     mma_commit(&bar_os);
                     if (c + 1 < nch && (fetched >= c + 2 || fetch(c + 1, true))) {
                         const uint32_t r = cnt + c + 1;
                         if (mbar_wait(&bar_full[r & 1], (r >> 1) & 1, &abort_flag)) {
                             tc_fence_after();
-                            issue_u_prime(x, tiles(r & 1));
+                            issue_u_prime_tc(x, tiles(r & 1));
                         } else {
                             record_timeout(p.status, &abort_flag);
                         }
@@ -689,11 +661,10 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 }
                 // O^T -> o, and the next chunk's S^T -> bf16 operand (the loop
                 // condition, read after the barrier below, handles an abort)
-                phase_o_epilogue(x, o_g, bos + c * C, min(C, len - c * C), h, H);
+                phase_ot_epilogue_zero(x, o_g, bos + c * C, min(C, len - c * C), h, H);
                 if (c + 1 < nch) {
-                    phase_state_to_operand(x, CB_ST);
+                    phase_state_to_tmem(x);
                 }
-                fence_proxy_async();
                 cta_sync_tc();
             }
             // copies still in flight into this CTA's buffers (a loop left early)
@@ -717,9 +688,13 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
         }
     } else {
         // ------------------------------------------------------------ producer
+        // Each task writes the tiles it does not need itself (Q+, Kend, Gamma,
+        // Aqk, a copy of Tm and W^T) straight into its ring slot; the slot's
+        // flag is raised one task later, after every thread has fenced.
         const int total = meta.task0[p.n_batches];
         float* s_beta = reinterpret_cast<float*>(sm + OFF_BETA);
         int32_t* ctr = p.work_counter;
+        constexpr int kPublisher = 256;  // idle while warps 0-7 run the Gram epilogue
         auto issue_raw = [&](const SplitTask& tk) {
             mbar_arrive_expect_tx(&bar_raw, 3 * 16384);
             tma_load_3d(sm + OFF_RAWQ, &args.tm_q, 0, tk.h, tk.t0, &bar_raw);
@@ -755,16 +730,27 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 beta_r = __bfloat162float(beta_g[(size_t)(tk.t0 + tid) * H + tk.h]);
             }
         }
-        // thread 0: the last published slot, flagged once its bulk store completes
-        bool store_pending = false;
-        int32_t pend_slot = 0, pend_val = 0;
+        // the last written slot, not yet flagged.  Every thread wrote its part
+        // of it before the barriers since; the publisher's gpu-scope fence
+        // orders all of those writes (cumulativity) before the flag.
+        int32_t pend_slot = -1, pend_val = 0;
+        int32_t cons_seen = 0;  // publisher: the next task's consumer counter, read ahead
         while (t < total && !abort_flag) {
             SplitTask cur;
             decode_task(meta, p, t, cur);
+            const int32_t slot = cur.i * p.ring + cur.g % p.ring;
+            uint8_t* pub = p.handoff + (size_t)slot * HO_BYTES;
             // candidate for the next task; its latency hides behind the prologue
             int t_ahead = 0;
             if (tid == 0) {
                 t_ahead = atomicAdd(ctr, 1);
+            }
+            // the slot is free once its consumer has copied out the chunk that was in it
+            if (tid == kPublisher) {
+                if (cons_seen < cur.g - p.ring + 1) {
+                    cons_seen = ld_acquire(p.cons_done + cur.i);
+                }
+                s_slot_free = cons_seen >= cur.g - p.ring + 1;
             }
             if (mbar_wait(&bar_raw, ph_raw, &abort_flag)) {
                 ph_raw ^= 1;
@@ -772,19 +758,35 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
             } else {
                 record_timeout(p.status, &abort_flag);
             }
-            if (tid == 0 && store_pending) {  // publish the last slot
-                bulk_wait();
-                fence_proxy_async_global();
-                st_release(p.flags + pend_slot, pend_val);
-                store_pending = false;
-            }
             __syncthreads();
+            if (!s_slot_free) {
+                // about to wait on a consumer: first raise the flag still held,
+                // which that consumer may need
+                if (tid == kPublisher) {
+                    if (pend_slot >= 0 && !abort_flag) {
+                        __threadfence();
+                        st_release(p.flags + pend_slot, pend_val);
+                    }
+                    pend_slot = -1;
+                    if (!wait_at_least(p.cons_done + cur.i, cur.g - p.ring + 1, &abort_flag)) {
+                        record_timeout(p.status, &abort_flag);
+                    }
+                }
+                __syncthreads();
+            }
             if (abort_flag) {
                 break;
             }
             phase_norms(x, cur.L, p.scale, p.l2norm);
             __syncthreads();
-            phase_prologue(x, cur.L, meta.eA[cur.h]);
+            // the last slot's writes finished a prologue ago: raise its flag
+            phase_prologue<true>(x, cur.L, meta.eA[cur.h], pub, [&]() {
+                if (tid == kPublisher && pend_slot >= 0) {
+                    __threadfence();
+                    st_release(p.flags + pend_slot, pend_val);
+                    pend_slot = -1;
+                }
+            });
             // the raw tiles are consumed: fetch the next task's
             if (tid == 0) {
                 const int tn = next_valid(t_ahead);
@@ -824,10 +826,16 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 break;
             }
             if (x.warp < 8) {
-                phase_gram_epilogue(x);
+                phase_gram_epilogue<true>(x, pub);
+            } else if (tid == kPublisher) {
+                if (tn < total) {  // read the next task's consumer counter ahead of use
+                    SplitTask nt;
+                    decode_task(meta, p, tn, nt);
+                    cons_seen = ld_acquire(p.cons_done + nt.i);
+                }
             }
             cta_sync_tc();
-            phase_solve(x);
+            phase_solve<true>(x, pub);
             fence_proxy_async();
             cta_sync_tc();
             if (tid == 0) {
@@ -843,34 +851,16 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
             if (abort_flag) {
                 break;
             }
-            phase_tile_from_tmem(x, TM_W, OFF_WT);
-            fence_proxy_async();
-            __syncthreads();
-            // store the slot once the consumer has copied out the chunk that was in it
-            if (tid == 0) {
-                const int32_t slot = cur.i * p.ring + cur.g % p.ring;
-                if (wait_at_least(p.cons_done + cur.i, cur.g - p.ring + 1, &abort_flag)) {
-                    fence_proxy_async_global();
-                    uint8_t* dst = p.handoff + (size_t)slot * HO_BYTES;
-                    bulk_store(dst + HO_AQK, sm + OFF_AQK, 32768);  // Aqk | Tm | W^T
-                    bulk_store(dst + HO_QP, sm + OFF_QP, 32768);    // Q+ | Kend
-                    bulk_store(dst + HO_GAM, sm + OFF_GAM, 512);
-                    bulk_commit();
-                    store_pending = true;
-                    pend_slot = slot;
-                    pend_val = cur.g + 1;
-                } else {
-                    record_timeout(p.status, &abort_flag);
-                }
-            }
+            phase_tile_from_tmem_to(x, TM_W, pub + HO_WT, -1.0f);
+            pend_slot = slot;
+            pend_val = cur.g + 1;
             t = tn;
         }
-        if (tid == 0 && store_pending) {
-            bulk_wait();
-            if (!abort_flag) {
-                fence_proxy_async_global();
-                st_release(p.flags + pend_slot, pend_val);
-            }
+        // flag the last slot
+        __syncthreads();
+        if (tid == kPublisher && pend_slot >= 0 && !abort_flag) {
+            __threadfence();
+            st_release(p.flags + pend_slot, pend_val);
         }
         // a loop left early may still have a raw load in flight into this CTA's smem
         if (raw_pending) {
@@ -935,7 +925,7 @@ size_t chunked_workspace_bytes(int32_t N, int32_t H) {
 }
 
 namespace {
-constexpr int32_t kSplitRing = 8;  // slots per consumer
+constexpr int32_t kSplitRing = 12;  // slots per consumer
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 size_t split_flags_offset() { return 256; }
 size_t split_done_offset(const SplitPlan& plan) {
