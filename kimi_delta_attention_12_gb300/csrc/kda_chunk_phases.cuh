@@ -258,10 +258,11 @@ __device__ __forceinline__ void phase_norms(const Ctx& x, int L, float scale, in
 // ---------------------------------------------------------------- P1b + P1c
 // Gate, in-block decay products and the bf16 operand tiles X~, K~^(a), K+,
 // Q+, Kend, plus Gamma_C = e^{gamma_C} (fp32, OFF_GAM).  Each thread owns one
-// channel and 16 tokens.  Contains one CTA barrier; the caller must have
-// synchronised after phase_norms.
+// channel and 16 tokens.  Contains one CTA barrier, which also publishes the
+// norms phase_norms wrote just before (no barrier needed between the two).
 // kPub (split producer): Q+, Kend and Gamma_C go straight to the published
-// chunk at `pub` (global memory) instead of shared memory.  after_gate() runs
+// chunk at `pub` (global memory) instead of shared memory, after the
+// thread's shared-memory tiles and their proxy fence.  after_gate() runs
 // right after the barrier (every thread).
 struct NoHook {
     __device__ void operator()() const {}
@@ -297,13 +298,19 @@ __device__ __forceinline__ void phase_prologue(const Ctx& x, int L, float eA_log
             const float g = r < L ? -5.0f * kLog2e * sg : 0.0f;
             tot += g;
             al[rr] = exp2_approx(g);
-            qh[rr] = qv * s_invq[r];
-            kh[rr] = kv * s_invk[r];
+            qh[rr] = qv;
+            kh[rr] = kv;
         }
         s_tot[ab * D + c] = tot;
     }
     __syncthreads();
     after_gate();
+    // the norms (written before the barrier) are applied now
+#pragma unroll
+    for (int rr = 0; rr < 16; ++rr) {
+        qh[rr] *= s_invq[16 * ab + rr];
+        kh[rr] *= s_invk[16 * ab + rr];
+    }
 
     float t[4];
 #pragma unroll
@@ -344,7 +351,13 @@ __device__ __forceinline__ void phase_prologue(const Ctx& x, int L, float eA_log
     // Q+ = q e^{gamma} = (q e^{gamma - rho_a}) e^{rho_a}
 #pragma unroll
     for (int rr = 0; rr < 16; ++rr) v[rr] *= eRa;
-    store_row16(qp_tile, c, 32 * ab, v);
+    uint32_t qp_w[8];
+    if (kPub) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) qp_w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+    } else {
+        store_row16(qp_tile, c, 32 * ab, v);
+    }
 #pragma unroll
     for (int rr = 0; rr < 16; ++rr) v[rr] = kh[rr] * E[rr];
     store_row16(xt, c, 2 * (e0 + 16), v);
@@ -358,7 +371,13 @@ __device__ __forceinline__ void phase_prologue(const Ctx& x, int L, float eA_log
     // Kend = k e^{gamma_C - gamma}
 #pragma unroll
     for (int rr = 0; rr < 16; ++rr) v[rr] = G[rr] * eEnd;
-    store_row16(ke_tile, c, 32 * ab, v);
+    uint32_t ke_w[8];
+    if (kPub) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ke_w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+    } else {
+        store_row16(ke_tile, c, 32 * ab, v);
+    }
     // K~^(ab) = k e^{rho_a - gamma}: M-block (3 - ab) of the Gram A operand
 #pragma unroll
     for (int rr = 0; rr < 16; ++rr) v[rr] = G[rr] * cF;
@@ -372,6 +391,19 @@ __device__ __forceinline__ void phase_prologue(const Ctx& x, int L, float eA_log
             for (int rr = 0; rr < 16; ++rr) v[rr] = G[rr] * f;
             store_row16(sm + OFF_KT + (3 - ap) * 16384, c, 32 * ab, v);
         }
+    }
+    if (kPub) {
+        // shared-memory tiles before the tensor core reads them; then the
+        // published tiles (global stores the fence need not wait for)
+        fence_proxy_async();
+        uint4* q4 = reinterpret_cast<uint4*>(qp_tile + sw128(c, 32 * ab));
+        uint4* q5 = reinterpret_cast<uint4*>(qp_tile + sw128(c, 32 * ab + 16));
+        uint4* k4 = reinterpret_cast<uint4*>(ke_tile + sw128(c, 32 * ab));
+        uint4* k5 = reinterpret_cast<uint4*>(ke_tile + sw128(c, 32 * ab + 16));
+        *q4 = make_uint4(qp_w[0], qp_w[1], qp_w[2], qp_w[3]);
+        *q5 = make_uint4(qp_w[4], qp_w[5], qp_w[6], qp_w[7]);
+        *k4 = make_uint4(ke_w[0], ke_w[1], ke_w[2], ke_w[3]);
+        *k5 = make_uint4(ke_w[4], ke_w[5], ke_w[6], ke_w[7]);
     }
 }
 

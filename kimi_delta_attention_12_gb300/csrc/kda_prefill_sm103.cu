@@ -204,8 +204,7 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
         }
 
         // ---------------- P1a: per-token L2 norms ----------------
-        phase_norms(x, L, p.scale, p.l2norm);
-        __syncthreads();
+        phase_norms(x, L, p.scale, p.l2norm);  // published by the prologue's barrier
 
         // ---------------- P1b: gate, decay products and operand tiles ----------------
         phase_prologue(x, L, eA_log2);
@@ -440,7 +439,6 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
     __shared__ uint64_t bar_os;        // consumer: O and the state update done
     __shared__ uint64_t bar_fin;       // every MMA of this CTA done
     __shared__ uint32_t tmem_base_s;
-    __shared__ int s_next;
     __shared__ int s_issued;
     __shared__ int s_slot_free;
     __shared__ volatile int abort_flag;
@@ -688,12 +686,14 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
         }
     } else {
         // ------------------------------------------------------------ producer
-        // Each task writes the tiles it does not need itself (Q+, Kend, Gamma,
-        // Aqk, a copy of Tm and W^T) straight into its ring slot; the slot's
-        // flag is raised one task later, after every thread has fenced.
+        // Producer k takes tasks k, k + P, k + 2P, ... (P producers; tasks past
+        // the end of their sequence are skipped).  Each task writes the tiles it
+        // does not need itself (Q+, Kend, Gamma, Aqk, a copy of Tm and -W^T)
+        // straight into its ring slot; the slot's flag is raised during the
+        // next task, after the publishing thread's fence.
         const int total = meta.task0[p.n_batches];
+        const int P = (int)gridDim.x - p.n_cons;
         float* s_beta = reinterpret_cast<float*>(sm + OFF_BETA);
-        int32_t* ctr = p.work_counter;
         constexpr int kPublisher = 256;  // idle while warps 0-7 run the Gram epilogue
         auto issue_raw = [&](const SplitTask& tk) {
             mbar_arrive_expect_tx(&bar_raw, 3 * 16384);
@@ -701,49 +701,39 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
             tma_load_3d(sm + OFF_RAWK, &args.tm_k, 0, tk.h, tk.t0, &bar_raw);
             tma_load_3d(sm + OFF_RAWZ, &args.tm_z, 0, tk.h, tk.t0, &bar_raw);
         };
-        // thread 0: the first valid task at or after counter value t
-        auto next_valid = [&](int t) -> int {
-            SplitTask tk;
+        // the first of this producer's tasks at or after t (every thread)
+        auto next_task = [&](int t, SplitTask& tk) -> int {
             while (t < total && !decode_task(meta, p, t, tk)) {
-                t = atomicAdd(ctr, 1);
+                t += P;
             }
             return t;
         };
-        if (tid == 0) {
-            const int t = next_valid(atomicAdd(ctr, 1));
-            s_next = t;
-            if (t < total) {
-                SplitTask tk;
-                decode_task(meta, p, t, tk);
-                issue_raw(tk);
-            }
+        SplitTask cur;
+        int t = next_task((int)blockIdx.x - p.n_cons, cur);
+        if (tid == 0 && t < total) {
+            issue_raw(cur);
         }
-        __syncthreads();
-        int t = s_next;
         bool raw_pending = t < total;
         uint32_t ph_raw = 0, ph_mma = 0;
         float beta_r = 0.0f;   // this thread's beta of the current task (tid < 64)
-        if (t < total) {
-            SplitTask tk;
-            decode_task(meta, p, t, tk);
-            if (tid < tk.L) {
-                beta_r = __bfloat162float(beta_g[(size_t)(tk.t0 + tid) * H + tk.h]);
-            }
+        if (t < total && tid < cur.L) {
+            beta_r = __bfloat162float(beta_g[(size_t)(cur.t0 + tid) * H + cur.h]);
         }
         // the last written slot, not yet flagged.  Every thread wrote its part
         // of it before the barriers since; the publisher's gpu-scope fence
         // orders all of those writes (cumulativity) before the flag.
         int32_t pend_slot = -1, pend_val = 0;
-        int32_t cons_seen = 0;  // publisher: the next task's consumer counter, read ahead
+        int32_t cons_seen = 0;  // publisher: the current task's consumer counter, read ahead
         while (t < total && !abort_flag) {
-            SplitTask cur;
-            decode_task(meta, p, t, cur);
+            SplitTask nt;
+            const int tn = next_task(t + P, nt);
+            const bool has_next = tn < total;
             const int32_t slot = cur.i * p.ring + cur.g % p.ring;
             uint8_t* pub = p.handoff + (size_t)slot * HO_BYTES;
-            // candidate for the next task; its latency hides behind the prologue
-            int t_ahead = 0;
-            if (tid == 0) {
-                t_ahead = atomicAdd(ctr, 1);
+            // beta of the next task, used one task from now
+            float beta_n = 0.0f;
+            if (has_next && tid < nt.L) {
+                beta_n = __bfloat162float(beta_g[(size_t)(nt.t0 + tid) * H + nt.h]);
             }
             // the slot is free once its consumer has copied out the chunk that was in it
             if (tid == kPublisher) {
@@ -777,41 +767,24 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
             if (abort_flag) {
                 break;
             }
-            phase_norms(x, cur.L, p.scale, p.l2norm);
-            __syncthreads();
-            // the last slot's writes finished a prologue ago: raise its flag
+            phase_norms(x, cur.L, p.scale, p.l2norm);  // published by the prologue's barrier
             phase_prologue<true>(x, cur.L, meta.eA[cur.h], pub, [&]() {
+                // the last slot's writes finished a prologue ago: raise its flag
                 if (tid == kPublisher && pend_slot >= 0) {
                     __threadfence();
                     st_release(p.flags + pend_slot, pend_val);
                     pend_slot = -1;
                 }
-            });
-            // the raw tiles are consumed: fetch the next task's
-            if (tid == 0) {
-                const int tn = next_valid(t_ahead);
-                s_next = tn;
-                if (tn < total) {
-                    SplitTask nt;
-                    decode_task(meta, p, tn, nt);
+                // the raw tiles are consumed: fetch the next task's
+                if (tid == 0 && has_next) {
                     issue_raw(nt);
                 }
-            }
+            });
+            raw_pending = has_next;
             if (tid < C) {
                 s_beta[tid] = beta_r;
             }
-            fence_proxy_async();
-            cta_sync_tc();
-            const int tn = s_next;
-            raw_pending = tn < total;
-            beta_r = 0.0f;
-            if (tn < total) {
-                SplitTask nt;
-                decode_task(meta, p, tn, nt);
-                if (tid < nt.L) {
-                    beta_r = __bfloat162float(beta_g[(size_t)(nt.t0 + tid) * H + nt.h]);
-                }
-            }
+            cta_sync_tc();  // (the prologue fenced its shared-memory tiles)
             if (tid == 0) {
                 issue_gram(x);
                 mma_commit(&bar_mma);
@@ -827,12 +800,8 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
             }
             if (x.warp < 8) {
                 phase_gram_epilogue<true>(x, pub);
-            } else if (tid == kPublisher) {
-                if (tn < total) {  // read the next task's consumer counter ahead of use
-                    SplitTask nt;
-                    decode_task(meta, p, tn, nt);
-                    cons_seen = ld_acquire(p.cons_done + nt.i);
-                }
+            } else if (tid == kPublisher && has_next) {
+                cons_seen = ld_acquire(p.cons_done + nt.i);  // read ahead of use
             }
             cta_sync_tc();
             phase_solve<true>(x, pub);
@@ -854,7 +823,9 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
             phase_tile_from_tmem_to(x, TM_W, pub + HO_WT, -1.0f);
             pend_slot = slot;
             pend_val = cur.g + 1;
+            beta_r = beta_n;
             t = tn;
+            cur = nt;
         }
         // flag the last slot
         __syncthreads();
