@@ -258,60 +258,67 @@ __device__ __forceinline__ void phase_norms(const Ctx& x, int L, float scale, in
 // ---------------------------------------------------------------- P1b + P1c
 // Gate, in-block decay products and the bf16 operand tiles X~, K~^(a), K+,
 // Q+, Kend, plus Gamma_C = e^{gamma_C} (fp32, OFF_GAM).  Each thread owns one
-// channel and 16 tokens.  Contains one CTA barrier, which also publishes the
-// norms phase_norms wrote just before (no barrier needed between the two).
+// (channel c = tid % 128, 16-token block ab = tid / 128) unit.  Two halves:
+// phase_prologue_gate (gate, alpha, block totals; raw q, k kept in the
+// thread's registers) and, after a CTA barrier that also publishes the norms
+// phase_norms wrote, phase_prologue_operands (the tiles).  The same thread
+// must run both halves of its unit.
 // kPub (split producer): Q+, Kend and Gamma_C go straight to the published
 // chunk at `pub` (global memory) instead of shared memory, after the
-// thread's shared-memory tiles and their proxy fence.  after_gate() runs
-// right after the barrier (every thread).
-struct NoHook {
-    __device__ void operator()() const {}
+// thread's shared-memory tiles and their proxy fence.
+struct GateRegs {
+    float qh[16], kh[16], al[16];
 };
-template <bool kPub = false, typename Hook = NoHook>
-__device__ __forceinline__ void phase_prologue(const Ctx& x, int L, float eA_log2,
-                                               uint8_t* pub = nullptr,
-                                               Hook after_gate = Hook()) {
+
+__device__ __forceinline__ void phase_prologue_gate(const Ctx& x, int L, float eA_log2,
+                                                    GateRegs& gr) {
+    uint8_t* sm = x.sm;
+    float* s_tot = reinterpret_cast<float*>(sm + OFF_TOT);
+    const int c = x.tid & (D - 1);   // channel
+    const int ab = (x.tid >> 7) & 3; // token block: tokens 16ab .. 16ab+15
+    float tot = 0.f;                 // block total of g, log2 units
+#pragma unroll
+    for (int rr = 0; rr < 16; ++rr) {
+        const int r = 16 * ab + rr;
+        const float qv = __bfloat162float(
+            *reinterpret_cast<const __nv_bfloat16*>(sm + OFF_RAWQ + r * 256 + 2 * c));
+        const float kv = __bfloat162float(
+            *reinterpret_cast<const __nv_bfloat16*>(sm + OFF_RAWK + r * 256 + 2 * c));
+        const float zv = __bfloat162float(
+            *reinterpret_cast<const __nv_bfloat16*>(sm + OFF_RAWZ + r * 256 + 2 * c));
+        // g = -5 sigmoid(e^A z) in log2 units; invalid tokens: g = 0
+        const float sg = rcp_approx(1.0f + exp2_approx(-eA_log2 * zv));
+        const float g = r < L ? -5.0f * kLog2e * sg : 0.0f;
+        tot += g;
+        gr.al[rr] = exp2_approx(g);
+        gr.qh[rr] = qv;
+        gr.kh[rr] = kv;
+    }
+    s_tot[ab * D + c] = tot;
+}
+
+template <bool kPub = false>
+__device__ __forceinline__ void phase_prologue_operands(const Ctx& x, int L, GateRegs& gr,
+                                                        uint8_t* pub = nullptr) {
     uint8_t* sm = x.sm;
     const float* s_invq = reinterpret_cast<const float*>(sm + OFF_INVQ);
     const float* s_invk = reinterpret_cast<const float*>(sm + OFF_INVK);
-    float* s_tot = reinterpret_cast<float*>(sm + OFF_TOT);
+    const float* s_tot = reinterpret_cast<const float*>(sm + OFF_TOT);
     float* s_gam = kPub ? reinterpret_cast<float*>(pub + HO_GAM)
                         : reinterpret_cast<float*>(sm + OFF_GAM);
     uint8_t* qp_tile = kPub ? pub + HO_QP : sm + OFF_QP;
     uint8_t* ke_tile = kPub ? pub + HO_KE : sm + OFF_KE;
-    const int c = x.tid & (D - 1);   // channel
-    const int ab = x.tid >> 7;       // token block: tokens 16ab .. 16ab+15
-    float qh[16], kh[16], al[16];
-    {
-        float tot = 0.f;           // block total of g, log2 units
-#pragma unroll
-        for (int rr = 0; rr < 16; ++rr) {
-            const int r = 16 * ab + rr;
-            const float qv = __bfloat162float(
-                *reinterpret_cast<const __nv_bfloat16*>(sm + OFF_RAWQ + r * 256 + 2 * c));
-            const float kv = __bfloat162float(
-                *reinterpret_cast<const __nv_bfloat16*>(sm + OFF_RAWK + r * 256 + 2 * c));
-            const float zv = __bfloat162float(
-                *reinterpret_cast<const __nv_bfloat16*>(sm + OFF_RAWZ + r * 256 + 2 * c));
-            // g = -5 sigmoid(e^A z) in log2 units; invalid tokens: g = 0
-            const float sg = rcp_approx(1.0f + exp2_approx(-eA_log2 * zv));
-            const float g = r < L ? -5.0f * kLog2e * sg : 0.0f;
-            tot += g;
-            al[rr] = exp2_approx(g);
-            qh[rr] = qv;
-            kh[rr] = kv;
-        }
-        s_tot[ab * D + c] = tot;
-    }
-    __syncthreads();
-    after_gate();
+    const int c = x.tid & (D - 1);
+    const int ab = (x.tid >> 7) & 3;
+    float* qh = gr.qh;
+    float* kh = gr.kh;
+    const float* al = gr.al;
     // the norms (written before the barrier) are applied now
 #pragma unroll
     for (int rr = 0; rr < 16; ++rr) {
         qh[rr] *= s_invq[16 * ab + rr];
         kh[rr] *= s_invk[16 * ab + rr];
     }
-
     float t[4];
 #pragma unroll
     for (int b = 0; b < 4; ++b) t[b] = s_tot[b * D + c];
@@ -405,6 +412,23 @@ __device__ __forceinline__ void phase_prologue(const Ctx& x, int L, float eA_log
         *k4 = make_uint4(ke_w[0], ke_w[1], ke_w[2], ke_w[3]);
         *k5 = make_uint4(ke_w[4], ke_w[5], ke_w[6], ke_w[7]);
     }
+}
+
+
+// Both halves with the barrier between them; after_gate() runs right after
+// the barrier (every thread).
+struct NoHook {
+    __device__ void operator()() const {}
+};
+template <bool kPub = false, typename Hook = NoHook>
+__device__ __forceinline__ void phase_prologue(const Ctx& x, int L, float eA_log2,
+                                               uint8_t* pub = nullptr,
+                                               Hook after_gate = Hook()) {
+    GateRegs gr;
+    phase_prologue_gate(x, L, eA_log2, gr);
+    __syncthreads();
+    after_gate();
+    phase_prologue_operands<kPub>(x, L, gr, pub);
 }
 
 // ---------------------------------------------------------------- P2 (one thread)
@@ -794,6 +818,140 @@ __device__ __forceinline__ void phase_o_epilogue(const Ctx& x, __nv_bfloat16* o_
         if (r0 + i < L) {
             dst[i * row] = __float2bfloat16_rn(__uint_as_float(r[i]));
         }
+    }
+}
+
+// ---------------------------------------------------------------- half-CTA variants
+// The split kernel's producer runs the tail of a chunk (Gram epilogue, UT
+// solve, W) on warps 0-7 while warps 8-15 start the next chunk (norms, gate).
+// These variants cover one half (256 threads) and synchronise it with a
+// named barrier; their arithmetic is that of the full-CTA phases.
+constexpr int kHalfThreads = 256;
+constexpr int kBarLow = 1;   // named barrier of warps 0-7
+
+__device__ __forceinline__ void half_sync(int id) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(kHalfThreads) : "memory");
+}
+
+// Per-token L2 norms, 8 tokens per warp; lw = warp index within the half.
+__device__ __forceinline__ void phase_norms_half(const Ctx& x, int lw, int L, float scale,
+                                                 int l2norm) {
+    const uint8_t* rq = x.sm + OFF_RAWQ;
+    const uint8_t* rk = x.sm + OFF_RAWK;
+    float* s_invq = reinterpret_cast<float*>(x.sm + OFF_INVQ);
+    float* s_invk = reinterpret_cast<float*>(x.sm + OFF_INVK);
+    float sq[8], sk[8];
+#pragma unroll
+    for (int tt = 0; tt < 8; ++tt) {
+        const int r = lw * 8 + tt;
+        const uint2 qv = *reinterpret_cast<const uint2*>(rq + r * 256 + x.lane * 8);
+        const uint2 kv = *reinterpret_cast<const uint2*>(rk + r * 256 + x.lane * 8);
+        const float q0 = bf16lo(qv.x), q1 = bf16hi(qv.x), q2 = bf16lo(qv.y), q3 = bf16hi(qv.y);
+        const float k0 = bf16lo(kv.x), k1 = bf16hi(kv.x), k2 = bf16lo(kv.y), k3 = bf16hi(kv.y);
+        sq[tt] = q0 * q0 + q1 * q1 + q2 * q2 + q3 * q3;
+        sk[tt] = k0 * k0 + k1 * k1 + k2 * k2 + k3 * k3;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+        for (int tt = 0; tt < 8; ++tt) {
+            sq[tt] += __shfl_xor_sync(0xffffffffu, sq[tt], off);
+            sk[tt] += __shfl_xor_sync(0xffffffffu, sk[tt], off);
+        }
+    }
+    if (x.lane < 8) {
+        float a = sq[0], b = sk[0];
+#pragma unroll
+        for (int tt = 1; tt < 8; ++tt) {
+            if (x.lane == tt) {
+                a = sq[tt];
+                b = sk[tt];
+            }
+        }
+        const int r = lw * 8 + x.lane;
+        const bool valid = r < L;
+        s_invq[r] = valid ? (l2norm ? rsqrtf(a + kNormEps) : 1.0f) * scale : 0.0f;
+        s_invk[r] = valid ? (l2norm ? rsqrtf(b + kNormEps) : 1.0f) : 0.0f;
+    }
+}
+
+// phase_solve on warps 0-7 (named barrier kBarLow); Tm also to `pub` when
+// kPub.  The caller must have synchronised the half after the Gram epilogue.
+template <bool kPub>
+__device__ __forceinline__ void phase_solve_half(const Ctx& x, uint8_t* pub) {
+    const float* s_beta = reinterpret_cast<const float*>(x.sm + OFF_BETA);
+    float* Lm = reinterpret_cast<float*>(x.sm + OFF_AKK);
+    float* Nm = reinterpret_cast<float*>(x.sm + OFF_NMAT);
+    if (x.tid < 64) {
+        const int a = x.tid >> 4, jj = x.tid & 15;
+        const float* Lb = Lm + (16 * a) * 65 + 16 * a;
+        float acc[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) acc[r] = (r == jj) ? 1.0f : 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float xi = (i < jj) ? 0.0f : acc[i];
+            acc[i] = xi;
+#pragma unroll
+            for (int r = i + 1; r < 16; ++r) acc[r] -= Lb[r * 65 + i] * xi;
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) Nm[(16 * a + r) * 65 + 16 * a + jj] = acc[r];
+    }
+    half_sync(kBarLow);
+    if (x.warp < 6) {
+        // (a, c) = (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
+        const int a = x.warp < 1 ? 1 : x.warp < 3 ? 2 : 3;
+        const int c = x.warp < 1 ? 0 : x.warp < 3 ? x.warp - 1 : x.warp - 3;
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        warp_gemm16(acc, Nm, 16 * a, 16 * a, Lm, 16 * a, 16 * c, x.lane);
+        warp_store16(acc, Lm, 16 * a, 16 * c, 1.0f, x.lane);
+    }
+    half_sync(kBarLow);
+#pragma unroll 1
+    for (int wave = 1; wave < 4; ++wave) {
+        if (x.warp < 4 - wave) {
+            const int a = x.warp + wave, b = x.warp;
+            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            for (int cc = b; cc < a; ++cc) {
+                warp_gemm16(acc, Lm, 16 * a, 16 * cc, Nm, 16 * cc, 16 * b, x.lane);
+            }
+            warp_store16(acc, Nm, 16 * a, 16 * b, -1.0f, x.lane);
+        }
+        half_sync(kBarLow);
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int r = (x.tid >> 3) + 32 * h, i0 = (x.tid & 7) * 8;
+        uint4 w;
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u;
+            v[u] = i <= r ? Nm[r * 65 + i] * s_beta[i] : 0.0f;
+        }
+        w.x = pack_bf16x2(v[0], v[1]); w.y = pack_bf16x2(v[2], v[3]);
+        w.z = pack_bf16x2(v[4], v[5]); w.w = pack_bf16x2(v[6], v[7]);
+        *reinterpret_cast<uint4*>(x.sm + OFF_TM + sw128(r, 2 * i0)) = w;
+        if (kPub) {
+            *reinterpret_cast<uint4*>(pub + HO_TM + sw128(r, 2 * i0)) = w;
+        }
+    }
+}
+
+// -W^T (TMEM TM_W) -> tile, warps 0-7: each covers 32 of the 64 token
+// columns of its lane quadrant.  No barrier.
+__device__ __forceinline__ void phase_neg_w_tile_half(const Ctx& x, uint8_t* tile) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int sub = 2 * (x.warp >> 2) + h;
+        uint32_t r[16];
+        tmem_ld16(x.tbase + x.lane_base + TM_W + 16 * sub, r);
+        tmem_wait_ld();
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = -1.0f * __uint_as_float(r[i]);
+        store_row16(tile, 32 * x.qd + x.lane, 32 * sub, v);
     }
 }
 

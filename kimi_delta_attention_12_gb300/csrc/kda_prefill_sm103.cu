@@ -687,21 +687,26 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
     } else {
         // ------------------------------------------------------------ producer
         // Producer k takes tasks k, k + P, k + 2P, ... (P producers; tasks past
-        // the end of their sequence are skipped).  Each task writes the tiles it
-        // does not need itself (Q+, Kend, Gamma, Aqk, a copy of Tm and -W^T)
-        // straight into its ring slot; the slot's flag is raised during the
-        // next task, after the publishing thread's fence.
+        // the end of their sequence are skipped).  Per task: the operand tiles
+        // (all warps), the Gram products, then warps 0-7 finish the task (Gram
+        // epilogue, UT solve, W) while warps 8-15 run the next task's norms and
+        // gate; warps 0-7 then run their own gate units of the next task.  The
+        // tiles the task does not keep (Q+, Kend, Gamma, Aqk, a copy of Tm,
+        // -W^T) go straight into its ring slot; the slot's flag is raised right
+        // after the next task's gate barrier by one thread's release store,
+        // which is cumulative over the CTA's writes ordered before it by that
+        // barrier, and before any wait for a consumer.
         const int total = meta.task0[p.n_batches];
         const int P = (int)gridDim.x - p.n_cons;
         float* s_beta = reinterpret_cast<float*>(sm + OFF_BETA);
-        constexpr int kPublisher = 256;  // idle while warps 0-7 run the Gram epilogue
+        constexpr int kPublisher = 256;  // a thread of warps 8-15 (idle at the hand-offs)
+        const bool low = x.warp < 8;
         auto issue_raw = [&](const SplitTask& tk) {
             mbar_arrive_expect_tx(&bar_raw, 3 * 16384);
             tma_load_3d(sm + OFF_RAWQ, &args.tm_q, 0, tk.h, tk.t0, &bar_raw);
             tma_load_3d(sm + OFF_RAWK, &args.tm_k, 0, tk.h, tk.t0, &bar_raw);
             tma_load_3d(sm + OFF_RAWZ, &args.tm_z, 0, tk.h, tk.t0, &bar_raw);
         };
-        // the first of this producer's tasks at or after t (every thread)
         auto next_task = [&](int t, SplitTask& tk) -> int {
             while (t < total && !decode_task(meta, p, t, tk)) {
                 t += P;
@@ -716,111 +721,120 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
         bool raw_pending = t < total;
         uint32_t ph_raw = 0, ph_mma = 0;
         float beta_r = 0.0f;   // this thread's beta of the current task (tid < 64)
-        if (t < total && tid < cur.L) {
-            beta_r = __bfloat162float(beta_g[(size_t)(cur.t0 + tid) * H + cur.h]);
+        GateRegs gr;           // this thread's gate unit of the current task
+        if (t < total) {
+            if (tid < cur.L) {
+                beta_r = __bfloat162float(beta_g[(size_t)(cur.t0 + tid) * H + cur.h]);
+            }
+            if (mbar_wait(&bar_raw, ph_raw, &abort_flag)) {
+                raw_pending = false;
+            } else {
+                record_timeout(p.status, &abort_flag);
+            }
+            ph_raw ^= 1;
+            phase_norms(x, cur.L, p.scale, p.l2norm);
+            phase_prologue_gate(x, cur.L, meta.eA[cur.h], gr);
         }
-        // the last written slot, not yet flagged.  Every thread wrote its part
-        // of it before the barriers since; the publisher's gpu-scope fence
-        // orders all of those writes (cumulativity) before the flag.
-        int32_t pend_slot = -1, pend_val = 0;
-        int32_t cons_seen = 0;  // publisher: the current task's consumer counter, read ahead
-        while (t < total && !abort_flag) {
+        int32_t pend_slot = -1, pend_val = 0;  // publisher: the last written slot, not yet flagged
+        int32_t cons_seen = 0;                 // publisher: the current task's consumer counter
+        while (t < total) {
             SplitTask nt;
             const int tn = next_task(t + P, nt);
             const bool has_next = tn < total;
             const int32_t slot = cur.i * p.ring + cur.g % p.ring;
             uint8_t* pub = p.handoff + (size_t)slot * HO_BYTES;
-            // beta of the next task, used one task from now
-            float beta_n = 0.0f;
-            if (has_next && tid < nt.L) {
-                beta_n = __bfloat162float(beta_g[(size_t)(nt.t0 + tid) * H + nt.h]);
-            }
-            // the slot is free once its consumer has copied out the chunk that was in it
+            // is the slot free (its consumer has copied out the chunk that was in
+            // it)?  cons_seen was read while warps 8-15 waited for the last task.
             if (tid == kPublisher) {
                 if (cons_seen < cur.g - p.ring + 1) {
                     cons_seen = ld_acquire(p.cons_done + cur.i);
                 }
                 s_slot_free = cons_seen >= cur.g - p.ring + 1;
             }
-            if (mbar_wait(&bar_raw, ph_raw, &abort_flag)) {
-                ph_raw ^= 1;
-                raw_pending = false;
-            } else {
-                record_timeout(p.status, &abort_flag);
+            // every gate unit and the norms of this task are done; the last
+            // task's slot writes too
+            if (__syncthreads_or(abort_flag != 0)) {
+                break;
             }
-            __syncthreads();
-            if (!s_slot_free) {
-                // about to wait on a consumer: first raise the flag still held,
-                // which that consumer may need
-                if (tid == kPublisher) {
-                    if (pend_slot >= 0 && !abort_flag) {
-                        __threadfence();
-                        st_release(p.flags + pend_slot, pend_val);
-                    }
-                    pend_slot = -1;
-                    if (!wait_at_least(p.cons_done + cur.i, cur.g - p.ring + 1, &abort_flag)) {
-                        record_timeout(p.status, &abort_flag);
-                    }
+            // the last task's slot writes are ordered before this barrier
+            if (tid == kPublisher && pend_slot >= 0) {
+                st_release(p.flags + pend_slot, pend_val);
+                pend_slot = -1;
+            }
+            if (tid == 0 && has_next) {  // the raw tiles are consumed: fetch the next task's
+                issue_raw(nt);
+            }
+            raw_pending = has_next;   // (every thread waits for it below)
+            if (!s_slot_free) {  // wait for the consumer (no flag is held now)
+                if (tid == kPublisher &&
+                    !wait_at_least(p.cons_done + cur.i, cur.g - p.ring + 1, &abort_flag)) {
+                    record_timeout(p.status, &abort_flag);
                 }
                 __syncthreads();
             }
-            if (abort_flag) {
-                break;
-            }
-            phase_norms(x, cur.L, p.scale, p.l2norm);  // published by the prologue's barrier
-            phase_prologue<true>(x, cur.L, meta.eA[cur.h], pub, [&]() {
-                // the last slot's writes finished a prologue ago: raise its flag
-                if (tid == kPublisher && pend_slot >= 0) {
-                    __threadfence();
-                    st_release(p.flags + pend_slot, pend_val);
-                    pend_slot = -1;
-                }
-                // the raw tiles are consumed: fetch the next task's
-                if (tid == 0 && has_next) {
-                    issue_raw(nt);
-                }
-            });
-            raw_pending = has_next;
+            phase_prologue_operands<true>(x, cur.L, gr, pub);
             if (tid < C) {
                 s_beta[tid] = beta_r;
             }
-            cta_sync_tc();  // (the prologue fenced its shared-memory tiles)
+            cta_sync_tc();  // (the operands half fenced its shared-memory tiles)
             if (tid == 0) {
                 issue_gram(x);
                 mma_commit(&bar_mma);
             }
-            if (!mbar_wait(&bar_mma, ph_mma, &abort_flag)) {
-                record_timeout(p.status, &abort_flag);
+            float beta_n = 0.0f;   // beta of the next task, used one task from now
+            if (has_next && tid < nt.L) {
+                beta_n = __bfloat162float(beta_g[(size_t)(nt.t0 + tid) * H + nt.h]);
             }
-            ph_mma ^= 1;
-            tc_fence_after();
-            __syncthreads();
-            if (abort_flag) {
-                break;
-            }
-            if (x.warp < 8) {
+            if (low) {
+                // ---- warps 0-7: the rest of this task
+                if (!mbar_wait(&bar_mma, ph_mma, &abort_flag)) {
+                    record_timeout(p.status, &abort_flag);
+                }
+                ph_mma ^= 1;
+                tc_fence_after();
                 phase_gram_epilogue<true>(x, pub);
-            } else if (tid == kPublisher && has_next) {
-                cons_seen = ld_acquire(p.cons_done + nt.i);  // read ahead of use
+                tc_fence_before();
+                half_sync(kBarLow);
+                phase_solve_half<true>(x, pub);
+                fence_proxy_async();
+                tc_fence_before();
+                half_sync(kBarLow);
+                tc_fence_after();
+                if (tid == 0) {
+                    issue_w(x);
+                    mma_commit(&bar_mma);
+                }
+                if (!mbar_wait(&bar_mma, ph_mma, &abort_flag)) {
+                    record_timeout(p.status, &abort_flag);
+                }
+                ph_mma ^= 1;
+                tc_fence_after();
+                phase_neg_w_tile_half(x, pub + HO_WT);
+                // then this half's gate units of the next task
+                if (has_next) {
+                    if (mbar_wait(&bar_raw, ph_raw, &abort_flag)) {
+                        raw_pending = false;
+                    } else {
+                        record_timeout(p.status, &abort_flag);
+                    }
+                    phase_prologue_gate(x, nt.L, meta.eA[nt.h], gr);
+                }
+            } else if (has_next) {
+                // ---- warps 8-15: the next task's norms and their gate units
+                if (mbar_wait(&bar_raw, ph_raw, &abort_flag)) {
+                    raw_pending = false;
+                } else {
+                    record_timeout(p.status, &abort_flag);
+                }
+                phase_norms_half(x, x.warp - 8, nt.L, p.scale, p.l2norm);
+                phase_prologue_gate(x, nt.L, meta.eA[nt.h], gr);
+                if (tid == kPublisher) {
+                    cons_seen = ld_acquire(p.cons_done + nt.i);  // read ahead of use
+                }
             }
-            cta_sync_tc();
-            phase_solve<true>(x, pub);
-            fence_proxy_async();
-            cta_sync_tc();
-            if (tid == 0) {
-                issue_w(x);
-                mma_commit(&bar_mma);
+            if (has_next) {
+                ph_raw ^= 1;
             }
-            if (!mbar_wait(&bar_mma, ph_mma, &abort_flag)) {
-                record_timeout(p.status, &abort_flag);
-            }
-            ph_mma ^= 1;
-            tc_fence_after();
-            __syncthreads();
-            if (abort_flag) {
-                break;
-            }
-            phase_tile_from_tmem_to(x, TM_W, pub + HO_WT, -1.0f);
             pend_slot = slot;
             pend_val = cur.g + 1;
             beta_r = beta_n;
@@ -830,7 +844,6 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
         // flag the last slot
         __syncthreads();
         if (tid == kPublisher && pend_slot >= 0 && !abort_flag) {
-            __threadfence();
             st_release(p.flags + pend_slot, pend_val);
         }
         // a loop left early may still have a raw load in flight into this CTA's smem
@@ -896,7 +909,7 @@ size_t chunked_workspace_bytes(int32_t N, int32_t H) {
 }
 
 namespace {
-constexpr int32_t kSplitRing = 12;  // slots per consumer
+constexpr int32_t kSplitRing = 16;  // slots per consumer
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 size_t split_flags_offset() { return 256; }
 size_t split_done_offset(const SplitPlan& plan) {
