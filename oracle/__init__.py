@@ -62,6 +62,13 @@ def _load():
                 ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
                 ctypes.c_double, ctypes.c_int, ctypes.POINTER(ctypes.c_int32),
                 ctypes.c_int64, dp, dp, ctypes.c_int]
+            lib.kda_oracle_run_ckpt.restype = ctypes.c_int
+            lib.kda_oracle_run_ckpt.argtypes = [
+                dp, dp, dp, dp, dp, dp, dp,
+                ctypes.POINTER(ctypes.c_int64), ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
+                ctypes.c_double, ctypes.POINTER(ctypes.c_int32), ctypes.c_int64, dp, dp,
+                ctypes.c_int64, ctypes.POINTER(ctypes.c_int64), dp, ctypes.c_int]
             lib.kda_oracle_gate.restype = ctypes.c_double
             lib.kda_oracle_gate.argtypes = [ctypes.c_double, ctypes.c_double]
             lib.kda_oracle_gate_vec.restype = None
@@ -146,3 +153,59 @@ def kda_reference(q, k, v, z, beta, A, initial_state=None, cu_seqlens=None,
     if rc <= 0:
         raise RuntimeError(f"oracle failed with status {rc}")
     return o, S_out, rc
+
+
+def checkpoint_counts(cu_seqlens, interval: int):
+    """Checkpoints per sequence (floor(length / interval)) and the index of
+    each sequence's first one (exclusive prefix sum), for the state
+    checkpoints of kda_reference_checkpoints."""
+    cu = np.asarray(cu_seqlens.cpu() if hasattr(cu_seqlens, "cpu") else cu_seqlens,
+                    dtype=np.int64)
+    counts = np.diff(cu) // int(interval)
+    base = np.concatenate([[0], np.cumsum(counts)[:-1]]).astype(np.int64)
+    return counts, base
+
+
+def kda_reference_checkpoints(q, k, v, z, beta, A, initial_state=None, cu_seqlens=None,
+                              interval: int = 64, scale: float = 1.0, l2norm: bool = True,
+                              eps: float = EPS, units=None, nthreads: int = 0):
+    """The oracle (recurrent form) plus state checkpoints: for every sequence n
+    and m = 1, 2, ... with m * interval <= its length, the state after its
+    first m * interval tokens, at index base[n] + m - 1 (checkpoint_counts).
+
+    Layouts as kda_reference (packed only).  Returns (o, final_state,
+    checkpoints [n_checkpoints, H, d_k, d_v] fp64, threads_used); entries of
+    pairs not listed in `units` stay NaN.
+    """
+    lib = _load()
+    q, k, v, z, beta, A = (_f64(t) for t in (q, k, v, z, beta, A))
+    total_T, H, dk = q.shape
+    dv = v.shape[-1]
+    if cu_seqlens is None:
+        cu_seqlens = np.array([0, total_T], dtype=np.int64)
+    cu = np.ascontiguousarray(np.asarray(
+        cu_seqlens.cpu() if hasattr(cu_seqlens, "cpu") else cu_seqlens, dtype=np.int64))
+    N = cu.size - 1
+    if cu[0] != 0 or cu[-1] != total_T or np.any(np.diff(cu) < 0):
+        raise ValueError("cu_seqlens must be non-decreasing from 0 to total_T")
+    if int(interval) <= 0:
+        raise ValueError("interval must be positive")
+    counts, base = checkpoint_counts(cu, interval)
+    base = np.ascontiguousarray(base)
+    S0 = _f64(initial_state)
+    o = np.full((total_T, H, dv), np.nan)
+    S_out = np.full((N, H, dk, dv), np.nan)
+    ck = np.full((max(int(counts.sum()), 1), H, dk, dv), np.nan)
+    if units is not None:
+        u = np.ascontiguousarray(np.asarray(list(units), dtype=np.int32).reshape(-1, 2))
+        n_units, uptr = u.shape[0], _ptr(u, ctypes.c_int32)
+    else:
+        u, n_units, uptr = None, 0, None
+    rc = lib.kda_oracle_run_ckpt(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(S0),
+        _ptr(cu, ctypes.c_int64), N, H, dk, dv, float(scale), int(bool(l2norm)),
+        float(eps), uptr, n_units, _ptr(o), _ptr(S_out), int(interval),
+        _ptr(base, ctypes.c_int64), _ptr(ck), int(nthreads))
+    if rc <= 0:
+        raise RuntimeError(f"oracle failed with status {rc}")
+    return o, S_out, ck[:int(counts.sum())], rc

@@ -106,6 +106,9 @@ typedef struct {
     double* o;            /* [total_T, H, dv] */
     double* S_out;        /* [N, H, dk, dv] or NULL */
     const int32_t* units; /* optional list of (n, h) pairs; NULL = all */
+    int64_t ckpt_interval;       /* > 0: record S after every this many tokens of a sequence */
+    const int64_t* ckpt_base;    /* [N]: index of each sequence's first checkpoint */
+    double* ckpt;                /* [n_checkpoints, H, dk, dv] */
     int64_t n_units;
     int64_t next;         /* work counter, guarded by mu */
     pthread_mutex_t mu;
@@ -167,6 +170,12 @@ static int oracle_unit_recurrent(oracle_job* J, int n, int h)
                 acc += S[(size_t)c * dv + j] * qh[c];
             }
             J->o[rowv + j] = acc;
+        }
+        /* checkpoint: the state after the first m * ckpt_interval tokens */
+        const int64_t done = t - J->cu[n] + 1;
+        if (J->ckpt && J->ckpt_interval > 0 && done % J->ckpt_interval == 0) {
+            const int64_t idx = J->ckpt_base[n] + done / J->ckpt_interval - 1;
+            memcpy(J->ckpt + ((size_t)idx * H + h) * dk * dv, S, sizeof(double) * dk * dv);
         }
     }
     if (J->S_out) {
@@ -375,5 +384,29 @@ int kda_oracle_run(const double* q, const double* k, const double* v, const doub
     J.cu = cu_seqlens; J.N = N; J.H = H; J.dk = dk; J.dv = dv;
     J.scale = scale; J.eps = eps; J.l2norm = l2norm; J.chunk = chunk;
     J.o = o; J.S_out = S_out; J.units = units; J.n_units = n_units;
+    return oracle_run(&J, nthreads);
+}
+
+/* kda_oracle_run plus state checkpoints (recurrent form only): for every
+ * sequence n and m >= 1 with m * ckpt_interval <= its length, the state after
+ * its first m * ckpt_interval tokens goes to ckpt[(ckpt_base[n] + m - 1), h]. */
+int kda_oracle_run_ckpt(const double* q, const double* k, const double* v, const double* z,
+                        const double* beta, const double* A, const double* S0,
+                        const int64_t* cu_seqlens, int N, int H, int dk, int dv,
+                        double scale, int l2norm, double eps,
+                        const int32_t* units, int64_t n_units,
+                        double* o, double* S_out, int64_t ckpt_interval,
+                        const int64_t* ckpt_base, double* ckpt, int nthreads)
+{
+    if (ckpt_interval <= 0 || !ckpt_base || !ckpt) {
+        return -1;
+    }
+    oracle_job J;
+    memset(&J, 0, sizeof(J));
+    J.q = q; J.k = k; J.v = v; J.z = z; J.beta = beta; J.A = A; J.S0 = S0;
+    J.cu = cu_seqlens; J.N = N; J.H = H; J.dk = dk; J.dv = dv;
+    J.scale = scale; J.eps = eps; J.l2norm = l2norm; J.chunk = 0;
+    J.o = o; J.S_out = S_out; J.units = units; J.n_units = n_units;
+    J.ckpt_interval = ckpt_interval; J.ckpt_base = ckpt_base; J.ckpt = ckpt;
     return oracle_run(&J, nthreads);
 }

@@ -307,3 +307,39 @@ def test_units_subset_matches_full(oracle_mod):
     assert np.array_equal(os_[:cu[1], 0], o[:cu[1], 0])
     assert np.array_equal(Ss[1, 2], S[1, 2]) and np.array_equal(Ss[0, 0], S[0, 0])
     assert np.isnan(os_[:cu[1], 1]).all()
+
+
+# ------------------------------------------------------------ state checkpoints
+def test_checkpoints_are_prefix_final_states(oracle_mod):
+    """Checkpoint m of sequence n is the final state of a run on its first
+    m * interval tokens (a separate oracle run from the same initial state),
+    and resuming from it reproduces the rest of the sequence; sequences
+    shorter than the interval have none; a length that is a multiple of the
+    interval ends with its final state."""
+    rng = np.random.default_rng(21)
+    lens = [13, 5, 8, 0, 17]
+    interval = 4
+    T, H, dk, dv = sum(lens), 2, 5, 3
+    q, k, v, z, beta, A, S0 = _rand_case(rng, T, H, dk, dv, N=len(lens))
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    counts, base = oracle_mod.checkpoint_counts(cu, interval)
+    assert counts.tolist() == [3, 1, 2, 0, 4]
+    assert base.tolist() == [0, 3, 4, 6, 6]
+    o, S, ck, _ = oracle_mod.kda_reference_checkpoints(q, k, v, z, beta, A, S0, cu,
+                                                       interval=interval)
+    o_ref, S_ref, _ = oracle_mod.kda_reference(q, k, v, z, beta, A, S0, cu)
+    assert np.array_equal(o, o_ref) and np.array_equal(S, S_ref)
+    assert ck.shape == (int(counts.sum()), H, dk, dv)
+    for n in range(len(lens)):
+        for m in range(1, counts[n] + 1):
+            pre = slice(cu[n], cu[n] + m * interval)
+            _, Sp, _ = oracle_mod.kda_reference(q[pre], k[pre], v[pre], z[pre], beta[pre], A,
+                                                S0[n:n + 1])
+            assert np.array_equal(ck[base[n] + m - 1], Sp[0]), (n, m)
+            rest = slice(cu[n] + m * interval, cu[n + 1])
+            if rest.stop > rest.start:
+                orr, Srr, _ = oracle_mod.kda_reference(q[rest], k[rest], v[rest], z[rest],
+                                                       beta[rest], A, ck[base[n] + m - 1][None])
+                assert np.array_equal(orr, o[rest]) and np.array_equal(Srr[0], S[n])
+    # length 8 = 2 intervals: the last checkpoint is the final state
+    assert np.array_equal(ck[base[2] + 1], S[2])
