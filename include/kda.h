@@ -125,6 +125,51 @@ KDA_API int kda_prefill(const void* q, const void* k, const void* v, const void*
                 void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * kda_prefill_checkpointed -- kda_prefill that also saves the state at
+ * chunk-aligned token boundaries: for sequence n and every m >= 1 with
+ * m * ckpt_interval <= its length, the state after its first
+ * m * ckpt_interval tokens.  This is what prefix reuse needs: a later request
+ * that shares those first tokens can start its prefill or decode from that
+ * state ("Kimi K3 Open Weights: What Is Actually New In Its 2.8 Trillion
+ * Parameter Architecture", section "Why 104B active still understates the
+ * systems problem": reuse is valid only where the prefix and the KDA state
+ * checkpoint agree at the same token boundary).
+ *
+ *  ckpt_interval   tokens between checkpoints, a positive multiple of 64
+ *  ckpt_pool       [ckpt_pool_size, H, d_k, d_v] fp32 state pool (the layout
+ *                  kda_decode_step and kda_state_io use), 16-byte aligned,
+ *                  not overlapping any other output
+ *  ckpt_slots      device [n_checkpoints] int32: the pool row of each
+ *                  checkpoint, or NULL for row = checkpoint index.  The
+ *                  checkpoints of sequence n follow those of sequences
+ *                  0 .. n-1 (see kda_checkpoint_count); checkpoint m of
+ *                  sequence n has index (checkpoints before n) + m - 1.  Rows
+ *                  outside [0, ckpt_pool_size) are skipped.
+ *  ckpt_pool_size  rows in the pool (>= 1)
+ * Every other argument and result is that of kda_prefill; ckpt_interval == 0
+ * (with a NULL pool) is exactly kda_prefill.  Errors: KDA_ERR_INVALID_ARG for
+ * an interval that is negative or not a multiple of 64, or a missing pool;
+ * KDA_ERR_ALIGNMENT for a misaligned pool or slot array.
+ */
+KDA_API int kda_prefill_checkpointed(const void* q, const void* k, const void* v,
+                const void* z, const void* beta, const float* A,
+                const float* initial_state, const int32_t* cu_seqlens,
+                const int32_t* cu_seqlens_host, int32_t N, int32_t total_T, int32_t H,
+                int32_t d_k, int32_t d_v, kda_dtype dt, float scale, uint32_t flags,
+                void* o, float* final_state, int32_t ckpt_interval, float* ckpt_pool,
+                const int32_t* ckpt_slots, int32_t ckpt_pool_size,
+                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * kda_checkpoint_count -- how many checkpoints kda_prefill_checkpointed writes
+ * (before slot mapping): the sum over sequences of floor(length /
+ * ckpt_interval).  cu_seqlens_host: HOST array [N + 1] of sequence starts, or
+ * NULL for N equal sequences of total_T / N.  Negative on invalid arguments.
+ */
+KDA_API int64_t kda_checkpoint_count(const int32_t* cu_seqlens_host, int32_t N,
+                                     int32_t total_T, int32_t ckpt_interval);
+
+/*
  * kda_workspace_status -- wait for `stream`, then read the status word a
  * kda_prefill launch left in `workspace`.  Returns KDA_OK, KDA_ERR_TIMEOUT
  * (a bounded wait inside the kernel ran out; its outputs are invalid) or

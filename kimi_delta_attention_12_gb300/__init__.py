@@ -45,7 +45,7 @@ KDA_STATE_SCATTER = 3
 EXPORTED_SYMBOLS = (
     "kda_prefill_workspace_bytes", "kda_prefill", "kda_workspace_status",
     "kda_decode_step", "kda_state_io", "kda_status_string", "kda_version",
-    "kda_prefill_noalloc",
+    "kda_prefill_noalloc", "kda_prefill_checkpointed", "kda_checkpoint_count",
 )
 
 _lock = threading.Lock()
@@ -91,6 +91,12 @@ def lib() -> ctypes.CDLL:
             L.kda_prefill_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                               i32, i32, i32, i32, i32, ctypes.c_int, f32, u32,
                                               vp, vp, vp]
+            L.kda_prefill_checkpointed.restype = ctypes.c_int
+            L.kda_prefill_checkpointed.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                   i32, i32, i32, i32, i32, ctypes.c_int, f32,
+                                                   u32, vp, vp, i32, vp, vp, i32, vp, sz, vp]
+            L.kda_checkpoint_count.restype = ctypes.c_int64
+            L.kda_checkpoint_count.argtypes = [vp, i32, i32, i32]
             _lib = L
     return _lib
 
@@ -145,11 +151,18 @@ def kda_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: torch.Tens
                 output_final_state: bool = True,
                 o: Optional[torch.Tensor] = None, final_state: Optional[torch.Tensor] = None,
                 workspace: Optional[torch.Tensor] = None,
+                ckpt_interval: int = 0, ckpt_pool: Optional[torch.Tensor] = None,
+                ckpt_slots: Optional[torch.Tensor] = None,
                 stream: Optional[torch.cuda.Stream] = None
                 ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """Chunked KDA prefill.  Packed layout: q, k, z [total_T, H, d_k], v
     [total_T, H, d_v], beta [total_T, H]; a 4-D [B, T, H, d] batch is accepted
-    and treated as B sequences of length T.  Returns (o, final_state)."""
+    and treated as B sequences of length T.  Returns (o, final_state).
+
+    With ckpt_interval > 0 (a multiple of 64) the state after every
+    ckpt_interval tokens of each sequence is also written into ckpt_pool
+    [pool, H, d_k, d_v] fp32, at row ckpt_slots[i] (int32, default i) for
+    checkpoint i (kda_prefill_checkpointed in include/kda.h)."""
     batched = q.dim() == 4
     if batched:
         B, T = q.shape[:2]
@@ -181,16 +194,43 @@ def kda_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: torch.Tens
     if cu_seqlens_host is not None:
         host_cu = cu_seqlens_host.to(torch.int32).contiguous()
     flags = (KDA_FLAG_L2NORM_QK if l2norm else 0) | (KDA_FLAG_RECURRENT if recurrent else 0)
-    st = lib().kda_prefill(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(initial_state),
-        _ptr(cu_seqlens), None if host_cu is None else ctypes.c_void_p(host_cu.data_ptr()),
-        N, total_T, H, d_k, d_v, _dtype_code(dt), float(scale), flags,
-        _ptr(o), _ptr(final_state), _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    host_ptr = None if host_cu is None else ctypes.c_void_p(host_cu.data_ptr())
+    if ckpt_interval:
+        _check_cuda(ckpt_pool, ckpt_slots)
+        if ckpt_pool is None or ckpt_pool.dtype != torch.float32:
+            raise TypeError("ckpt_pool must be a float32 tensor")
+        if ckpt_slots is not None and ckpt_slots.dtype != torch.int32:
+            raise TypeError("ckpt_slots must be int32")
+        st = lib().kda_prefill_checkpointed(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(initial_state),
+            _ptr(cu_seqlens), host_ptr, N, total_T, H, d_k, d_v, _dtype_code(dt),
+            float(scale), flags, _ptr(o), _ptr(final_state), int(ckpt_interval),
+            _ptr(ckpt_pool), _ptr(ckpt_slots), ckpt_pool.shape[0], _ptr(workspace),
+            workspace.numel(), _stream_ptr(stream))
+        name = "kda_prefill_checkpointed"
+    else:
+        st = lib().kda_prefill(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(initial_state),
+            _ptr(cu_seqlens), host_ptr, N, total_T, H, d_k, d_v, _dtype_code(dt),
+            float(scale), flags, _ptr(o), _ptr(final_state), _ptr(workspace), workspace.numel(),
+            _stream_ptr(stream))
+        name = "kda_prefill"
     if st != KDA_OK:
-        raise KDAError(st, "kda_prefill")
+        raise KDAError(st, name)
     if batched:
         o = o.reshape(B, T, H, d_v)
     return o, final_state
+
+
+def checkpoint_count(cu_seqlens_host: Optional[torch.Tensor], N: int, total_T: int,
+                     ckpt_interval: int) -> int:
+    """Checkpoints kda_prefill writes with this interval (sum of floor(len / interval))."""
+    host = None if cu_seqlens_host is None else cu_seqlens_host.to(torch.int32).contiguous()
+    n = int(lib().kda_checkpoint_count(None if host is None else ctypes.c_void_p(host.data_ptr()),
+                                       N, total_T, ckpt_interval))
+    if n < 0:
+        raise KDAError(n, "kda_checkpoint_count")
+    return n
 
 
 def workspace_status(workspace: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> int:

@@ -22,6 +22,7 @@ inline size_t elem_bytes(kda_dtype dt) { return dt == KDA_F32 ? 4 : 2; }
 
 constexpr uint32_t kKnownFlags = KDA_FLAG_L2NORM_QK | KDA_FLAG_RECURRENT;
 constexpr uint32_t kFlagRecurrent = KDA_FLAG_RECURRENT;
+constexpr int32_t kCheckpointGrain = 64;  // checkpoints fall on chunk boundaries
 
 // status word + work counter, then the optional schedule (one int per unit)
 constexpr size_t kWsHeader = 256;
@@ -109,6 +110,42 @@ int kda_prefill(const void* q, const void* k, const void* v, const void* z,
                 kda_dtype dt, float scale, uint32_t flags,
                 void* o, float* final_state,
                 void* workspace, size_t workspace_bytes, void* stream) {
+    return kda_prefill_checkpointed(q, k, v, z, beta, A, initial_state, cu_seqlens,
+                                    cu_seqlens_host, N, total_T, H, d_k, d_v, dt, scale, flags,
+                                    o, final_state, 0, nullptr, nullptr, 0, workspace,
+                                    workspace_bytes, stream);
+}
+
+int64_t kda_checkpoint_count(const int32_t* cu_seqlens_host, int32_t N, int32_t total_T,
+                             int32_t ckpt_interval) {
+    if (N < 1 || total_T < 0 || ckpt_interval <= 0) return KDA_ERR_INVALID_ARG;
+    if (!cu_seqlens_host) {
+        if (total_T % N != 0) return KDA_ERR_INVALID_ARG;
+        return (int64_t)N * ((total_T / N) / ckpt_interval);
+    }
+    if (cu_seqlens_host[0] != 0 || cu_seqlens_host[N] != total_T) return KDA_ERR_INVALID_ARG;
+    int64_t count = 0;
+    for (int32_t n = 0; n < N; ++n) {
+        const int32_t len = cu_seqlens_host[n + 1] - cu_seqlens_host[n];
+        if (len < 0) return KDA_ERR_INVALID_ARG;
+        count += len / ckpt_interval;
+    }
+    return count;
+}
+
+int kda_prefill_checkpointed(const void* q, const void* k, const void* v, const void* z,
+                             const void* beta, const float* A, const float* initial_state,
+                             const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                             int32_t N, int32_t total_T, int32_t H, int32_t d_k, int32_t d_v,
+                             kda_dtype dt, float scale, uint32_t flags, void* o,
+                             float* final_state, int32_t ckpt_interval, float* ckpt_pool,
+                             const int32_t* ckpt_slots, int32_t ckpt_pool_size,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+    if (ckpt_interval < 0 || ckpt_interval % kCheckpointGrain != 0) return KDA_ERR_INVALID_ARG;
+    if (ckpt_interval > 0 && (!ckpt_pool || ckpt_pool_size < 1)) return KDA_ERR_INVALID_ARG;
+    if (ckpt_interval > 0 && (!aligned(ckpt_pool, 16) || !aligned(ckpt_slots, 4))) {
+        return KDA_ERR_ALIGNMENT;
+    }
     if (dt != KDA_F32 && dt != KDA_BF16) return KDA_ERR_UNSUPPORTED;
     if (!supported_dim(d_k) || !supported_dim(d_v)) return KDA_ERR_UNSUPPORTED;
     if (N < 1 || H < 1 || total_T < 0) return KDA_ERR_INVALID_ARG;
@@ -157,6 +194,8 @@ int kda_prefill(const void* q, const void* k, const void* v, const void* z,
         p.status = ws; p.work_counter = ws + 1; p.schedule = nullptr;
         p.N = N; p.total_T = total_T; p.H = H; p.scale = scale;
         p.l2norm = (flags & KDA_FLAG_L2NORM_QK) ? 1 : 0;
+        p.ckpt_interval = ckpt_interval; p.ckpt_pool = ckpt_pool;
+        p.ckpt_slots = ckpt_slots; p.ckpt_pool_size = ckpt_pool_size;
         if (use_split) {
             kda::split_bind(plan, workspace, &p);
             err = kda::launch_split_prefill(p, sms, s);
@@ -171,6 +210,8 @@ int kda_prefill(const void* q, const void* k, const void* v, const void* z,
         p.slots = nullptr; p.cu_seqlens = cu_seqlens; p.o = o;
         p.rows = N; p.total_T = total_T; p.H = H; p.pool_size = 0;
         p.scale = scale; p.l2norm = (flags & KDA_FLAG_L2NORM_QK) ? 1 : 0; p.decode = 0;
+        p.ckpt_interval = ckpt_interval; p.ckpt_pool = ckpt_pool;
+        p.ckpt_slots = ckpt_slots; p.ckpt_pool_size = ckpt_pool_size;
         if (total_T == 0 && !final_state) {
             return KDA_OK;
         }

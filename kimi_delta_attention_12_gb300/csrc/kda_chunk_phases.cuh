@@ -955,6 +955,29 @@ __device__ __forceinline__ void phase_neg_w_tile_half(const Ctx& x, uint8_t* til
     }
 }
 
+// ---------------------------------------------------------------- state checkpoints
+// Index of sequence n's first checkpoint: the sum over earlier sequences of
+// floor(length / interval).  `len_of(m)` gives sequence m's length; every
+// thread of the CTA calls this (one CTA barrier inside, two with the reset).
+template <typename LenOf>
+__device__ __forceinline__ int64_t ckpt_base(int n, int interval, LenOf len_of, int* s_acc) {
+    if (threadIdx.x == 0) {
+        *s_acc = 0;
+    }
+    __syncthreads();
+    int part = 0;
+    for (int m = threadIdx.x; m < n; m += blockDim.x) {
+        part += len_of(m) / interval;
+    }
+    if (part) {
+        atomicAdd(s_acc, part);
+    }
+    __syncthreads();
+    const int64_t r = *s_acc;
+    __syncthreads();
+    return r;
+}
+
 // ---------------------------------------------------------------- state load / store
 // initial state -> TMEM: lane j holds column j of S (S^T row j).
 __device__ __forceinline__ void load_state(const Ctx& x, const float* src) {

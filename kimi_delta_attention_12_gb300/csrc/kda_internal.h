@@ -33,6 +33,11 @@ struct RecurrentParams {
     float scale;
     int32_t l2norm;
     int32_t decode;
+    // prefill only: state checkpoints every ckpt_interval tokens (0 = none)
+    int32_t ckpt_interval;
+    float* ckpt_pool;
+    const int32_t* ckpt_slots;
+    int32_t ckpt_pool_size;
 };
 
 // Launches the recurrent kernel for (d_k, d_v) in {32, 64, 128}^2 and
@@ -78,6 +83,11 @@ struct ChunkedParams {
     int32_t H;
     float scale;
     int32_t l2norm;
+    // state checkpoints every ckpt_interval tokens (a multiple of the chunk; 0 = none)
+    int32_t ckpt_interval;
+    float* ckpt_pool;
+    const int32_t* ckpt_slots;
+    int32_t ckpt_pool_size;
 };
 
 // Split mode: the N*H (sequence, head) units are cut into `batches` batches of

@@ -149,6 +149,17 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
 
     load_state(x, p.initial_state ? p.initial_state + state_off : nullptr);
     cta_sync_tc();
+    __shared__ int s_ck;
+    const int64_t ck_base =
+        p.ckpt_interval > 0
+            ? ckpt_base(n, p.ckpt_interval,
+                        [&](int m) {
+                            int64_t b, e;
+                            seq_bounds(p, m, b, e);
+                            return (int)(e - b);
+                        },
+                        &s_ck)
+            : 0;
 
     const float eA_log2 = exp2_approx(p.A[h] * kLog2e) * kLog2e;  // e^A log2(e)
     const __nv_bfloat16* beta_g = static_cast<const __nv_bfloat16*>(p.beta);
@@ -318,6 +329,17 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
 
         // ---------------- P10: O -> o ----------------
         phase_o_epilogue(x, o_g, t0, L, h, H);
+        // state checkpoint after this chunk (S^T in TMEM is the state after it)
+        if (p.ckpt_interval > 0) {
+            const int64_t done = (int64_t)(ci + 1) * C;
+            if (done % p.ckpt_interval == 0 && done <= len) {
+                const int64_t idx = ck_base + done / p.ckpt_interval - 1;
+                const int64_t row = p.ckpt_slots ? (int64_t)p.ckpt_slots[idx] : idx;
+                if (row >= 0 && row < p.ckpt_pool_size) {
+                    store_state(x, p.ckpt_pool + ((size_t)row * H + h) * D * D);
+                }
+            }
+        }
         cta_sync_tc();
     }
 
@@ -441,6 +463,7 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
     __shared__ uint32_t tmem_base_s;
     __shared__ int s_issued;
     __shared__ int s_slot_free;
+    __shared__ int s_ck;
     __shared__ volatile int abort_flag;
 
     const int tid = threadIdx.x;
@@ -558,6 +581,12 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
 
             load_state(x, p.initial_state ? p.initial_state + state_off : nullptr);
             cta_sync_tc();
+            const int64_t ck_base =
+                p.ckpt_interval > 0
+                    ? ckpt_base(n, p.ckpt_interval,
+                                [&](int m) { return (int)(meta.cu[m + 1] - meta.cu[m]); },
+                                &s_ck)
+                    : 0;
 
             int fetched = 0;  // thread 0: chunks of this unit whose copies are issued
             int waited = 0;   // chunks of this unit every thread has waited for
@@ -659,6 +688,17 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 }
                 // O^T -> o, and the next chunk's S^T -> bf16 operand (the loop
                 // condition, read after the barrier below, handles an abort)
+                // state checkpoint after this chunk (S^T in TMEM is the state after it)
+                if (p.ckpt_interval > 0) {
+                    const int64_t done = (int64_t)(c + 1) * C;
+                    if (done % p.ckpt_interval == 0 && done <= len) {
+                        const int64_t idx = ck_base + done / p.ckpt_interval - 1;
+                        const int64_t row = p.ckpt_slots ? (int64_t)p.ckpt_slots[idx] : idx;
+                        if (row >= 0 && row < p.ckpt_pool_size) {
+                            store_state(x, p.ckpt_pool + ((size_t)row * H + h) * D * D);
+                        }
+                    }
+                }
                 phase_ot_epilogue_zero(x, o_g, bos + c * C, min(C, len - c * C), h, H);
                 if (c + 1 < nch) {
                     phase_state_to_tmem(x);

@@ -143,6 +143,28 @@ kda_recurrent_kernel(const RecurrentParams p) {
     const float eA = expf(p.A[h]);
     const float scale = p.scale;
 
+    // prefill state checkpoints: index of this row's first one (the sum over
+    // earlier sequences of floor(length / interval))
+    __shared__ int s_ck;
+    int64_t ck_base = 0;
+    if (!p.decode && p.ckpt_interval > 0) {
+        if (tid == 0) {
+            s_ck = 0;
+        }
+        __syncthreads();
+        int part = 0;
+        for (int m = tid; m < row; m += kThreads) {
+            const int64_t len = p.cu_seqlens ? (int64_t)(p.cu_seqlens[m + 1] - p.cu_seqlens[m])
+                                             : p.total_T / p.rows;
+            part += (int)(len / p.ckpt_interval);
+        }
+        if (part) {
+            atomicAdd(&s_ck, part);
+        }
+        __syncthreads();
+        ck_base = s_ck;
+    }
+
     for (int64_t t = bos; t < eos; ++t) {
         // ---- stage 1: token inputs, gate, norm partial sums ----
         const size_t rk = ((size_t)t * H + h) * DK;
@@ -240,6 +262,20 @@ kda_recurrent_kernel(const RecurrentParams p) {
         for (int r = 0; r < RPT; ++r) {
             const float kk = kreg[r];
             S[r].x += kk * u4.x; S[r].y += kk * u4.y; S[r].z += kk * u4.z; S[r].w += kk * u4.w;
+        }
+
+        // ---- state checkpoint after every ckpt_interval tokens of the row ----
+        if (!p.decode && p.ckpt_interval > 0 && (t - bos + 1) % p.ckpt_interval == 0) {
+            const int64_t idx = ck_base + (t - bos + 1) / p.ckpt_interval - 1;
+            const int64_t prow = p.ckpt_slots ? (int64_t)p.ckpt_slots[idx] : idx;
+            if (prow >= 0 && prow < p.ckpt_pool_size) {
+                float4* cp = reinterpret_cast<float4*>(p.ckpt_pool + ((size_t)prow * H + h) * DK * DV);
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) {
+                    const int i = r * RSTEP + w * RPW + rs;
+                    __stcs(cp + (i * DV + col0) / 4 + cg, S[r]);
+                }
+            }
         }
     }
 

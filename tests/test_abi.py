@@ -176,3 +176,40 @@ def test_package_does_not_import_oracle():
                         assert all(not a.name.startswith("oracle") for a in node.names), f
                     if isinstance(node, ast.ImportFrom):
                         assert not (node.module or "").startswith("oracle"), f
+
+
+def test_checkpoint_count(L):
+    cu = (ctypes.c_int32 * 5)(0, 300, 300, 377, 633)
+    assert L.kda_checkpoint_count(cu, 4, 633, 64) == 4 + 0 + 1 + 4
+    assert L.kda_checkpoint_count(cu, 4, 633, 128) == 2 + 0 + 0 + 2
+    assert L.kda_checkpoint_count(None, 2, 256, 64) == 4
+    assert L.kda_checkpoint_count(None, 3, 256, 64) < 0      # 256 % 3 != 0
+    assert L.kda_checkpoint_count(cu, 4, 633, 0) < 0
+    assert L.kda_checkpoint_count(cu, 4, 600, 64) < 0        # does not end at total_T
+
+
+def _call_ckpt(L, interval, pool, slots=None, pool_size=4, **over):
+    a = _prefill_args(**over)
+    vp = ctypes.c_void_p
+    return L.kda_prefill_checkpointed(
+        vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["z"]), vp(a["beta"]), vp(a["A"]),
+        vp(a["S0"]), vp(a["cu"]), a["cu_host"], a["N"], a["T"], a["H"], a["dk"], a["dv"],
+        a["dt"], a["scale"], a["flags"], vp(a["o"]), vp(a["Sf"]), interval, vp(pool),
+        vp(slots), pool_size, vp(a["ws"]), a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("interval,pool,slots,pool_size,expect", [
+    (32, BASE + 0xA00000, None, 4, kda.KDA_ERR_INVALID_ARG),       # not a multiple of 64
+    (-64, BASE + 0xA00000, None, 4, kda.KDA_ERR_INVALID_ARG),
+    (64, None, None, 4, kda.KDA_ERR_INVALID_ARG),                  # no pool
+    (64, BASE + 0xA00000, None, 0, kda.KDA_ERR_INVALID_ARG),       # empty pool
+    (64, BASE + 0xA00008, None, 4, kda.KDA_ERR_ALIGNMENT),
+    (64, BASE + 0xA00000, BASE + 0xB00002, 4, kda.KDA_ERR_ALIGNMENT),
+])
+def test_checkpoint_validation(L, interval, pool, slots, pool_size, expect):
+    assert _call_ckpt(L, interval, pool, slots, pool_size) == expect
+
+
+def test_checkpoint_zero_interval_is_plain_prefill_validation(L):
+    # interval 0 takes the plain path: the other arguments are validated as usual
+    assert _call_ckpt(L, 0, None, None, 0, dk=48) == kda.KDA_ERR_UNSUPPORTED
