@@ -323,10 +323,35 @@ def kda_arm(args, world, rank, local, pg):
                               "kernel_ms": kernel_ms, "achieved_gbs": achieved_gbs,
                               "tensor_tflops": achieved_tf}), flush=True)
         return
+    ckpt = measure_checkpointed(sets, ws, o, S, cu_host, B, H, T, d, args, stream)
 
     return finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops, nsets,
                   set_bytes, x_host, o, S, ws, cu_host, value, ms_per_step, kernel_ms,
-                  achieved_gbs, achieved_tf, clk, launches_per_step, kernel_name, pg)
+                  achieved_gbs, achieved_tf, clk, launches_per_step, kernel_name, pg, ckpt)
+
+
+def measure_checkpointed(sets, ws, o, S, cu_host, B, H, T, d, args, stream, interval=1024):
+    """The same prefill with a state checkpoint every `interval` tokens
+    (kda_prefill_checkpointed): kernel time and the checkpoint bytes written."""
+    import torch
+    import kimi_delta_attention_12_gb300 as kda
+    count = kda.checkpoint_count(cu_host, B, B * T, interval)
+    pool = torch.empty(count, H, d, d, dtype=torch.float32, device=o.device)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    for i in range(args.warmup + args.steps):
+        x = sets[i % len(sets)]
+        if i >= args.warmup:
+            ev[i - args.warmup][0].record(stream)
+        kda.kda_prefill(x.q, x.k, x.v, x.z, x.beta, x.A, None, x.cu_seqlens,
+                        cu_seqlens_host=cu_host, o=o, final_state=S, workspace=ws,
+                        ckpt_interval=interval, ckpt_pool=pool)
+        if i >= args.warmup:
+            ev[i - args.warmup][1].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    return {"interval": interval, "checkpoints": count,
+            "checkpoint_bytes": count * H * d * d * 4, "kernel_ms": ms}
 
 
 def run_decode(dev, rank, local, stream, batch=None):
@@ -375,7 +400,7 @@ def decode_only(args, rank, local, dev, stream, peaks):
 
 def finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops, nsets,
            set_bytes, x_host, o, S, ws, cu_host, value, ms_per_step, kernel_ms, achieved_gbs,
-           achieved_tf, clk, launches_per_step, kernel_name, pg):
+           achieved_tf, clk, launches_per_step, kernel_name, pg, ckpt):
     import torch
     import kimi_delta_attention_12_gb300 as kda
     # ---- end to end through the public API with host buffers ----
@@ -442,6 +467,7 @@ def finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops
                    "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm_gbs"],
                                 "unit": "GB/s", "frac": dec_gbs / peaks["hbm_gbs"]},
                    "clocks": dclk_summary},
+        "prefill_checkpointed": dict(ckpt, kernel_ms_plain=kernel_ms),
         "cpu_baseline": {"value": cpu_tps, "unit": "tokens/s", "cores": cpu_threads,
                          "kind": "oracle", "sample": cpu_sample},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
