@@ -69,9 +69,11 @@ struct ChunkedArgs {
 
 // consumer shared memory: two buffers of [slot | v tile] (its bf16 S^T and
 // U^T operands live in TMEM)
-constexpr uint32_t CB_V = 66560;               // v tile inside a buffer (1024-aligned)
-constexpr uint32_t CB_BYTES = CB_V + 16384;    // 82944
-static_assert(2 * CB_BYTES <= SMEM_USED, "consumer layout exceeds the shared memory budget");
+constexpr uint32_t CB_BYTES = 66560;          // one slot buffer (HO_BYTES, 1024-aligned)
+constexpr uint32_t CB_VRING = 2 * CB_BYTES;    // then a ring of v tiles, prefetched ahead
+constexpr int kVRing = 4;
+static_assert(CB_VRING + kVRing * 16384 <= SMEM_USED,
+              "consumer layout exceeds the shared memory budget");
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) &
@@ -456,12 +458,14 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
     __shared__ SplitMeta meta;
     __shared__ uint64_t bar_raw;       // producer: raw q, k, z landed
     __shared__ uint64_t bar_mma;       // producer: MMA group done
-    __shared__ uint64_t bar_full[2];   // consumer: a buffer's slot and v tile landed
+    __shared__ uint64_t bar_full[2];   // consumer: a buffer's slot landed
+    __shared__ uint64_t bar_v[kVRing]; // consumer: a v tile landed
     __shared__ uint64_t bar_u;         // consumer: U^T done
     __shared__ uint64_t bar_os;        // consumer: O and the state update done
     __shared__ uint64_t bar_fin;       // every MMA of this CTA done
     __shared__ uint32_t tmem_base_s;
     __shared__ int s_issued;
+    __shared__ int s_vissued;
     __shared__ int s_slot_free;
     __shared__ int s_ck;
     __shared__ volatile int abort_flag;
@@ -476,6 +480,9 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
         mbar_init(&bar_mma, 1);
         mbar_init(&bar_full[0], 1);
         mbar_init(&bar_full[1], 1);
+        for (int j = 0; j < kVRing; ++j) {
+            mbar_init(&bar_v[j], 1);
+        }
         mbar_init(&bar_u, 1);
         mbar_init(&bar_os, 1);
         mbar_init(&bar_fin, 1);
@@ -552,12 +559,13 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
         // ------------------------------------------------------------ consumer
         const int i = blockIdx.x;
         __nv_bfloat16* o_g = static_cast<__nv_bfloat16*>(p.o);
-        auto tiles = [&](uint32_t b) -> StateTiles {
+        auto tiles = [&](uint32_t b, uint32_t vb) -> StateTiles {
             const uint32_t cb = b * CB_BYTES;
             return StateTiles{cb + HO_WT, cb + HO_QP,  cb + HO_KE, cb + HO_AQK, cb + HO_TM,
-                              cb + HO_GAM, cb + CB_V, 0,          0};
+                              cb + HO_GAM, CB_VRING + vb * 16384, 0, 0};
         };
         uint32_t cnt = 0;  // buffer fills so far (buffer = count & 1, parity = (count >> 1) & 1)
+        uint32_t vcnt = 0; // v tiles loaded so far (ring slot = count % 4, parity = (count / 4) & 1)
         uint32_t ph_u = 0, ph_os = 0;
         {   // O^T starts at zero; every chunk's output epilogue zeroes it again
             uint32_t z[16];
@@ -590,7 +598,27 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
 
             int fetched = 0;  // thread 0: chunks of this unit whose copies are issued
             int waited = 0;   // chunks of this unit every thread has waited for
-            // thread 0: copy chunk c's slot and v tile into buffer (cnt + c) & 1
+            int v_issued = 0, v_waited = 0;   // thread 0: v tiles of this unit
+            // thread 0: load chunk c's v tile (an input, independent of the
+            // producers) into the v ring, up to kVRing chunks ahead of use
+            auto issue_v = [&](int c) {
+                const uint32_t vb = (vcnt + c) % kVRing;
+                uint8_t* vbuf = sm + CB_VRING + vb * 16384;
+                mbar_arrive_expect_tx(&bar_v[vb], 16384);
+                tma_load_3d(vbuf, &args.tm_v, 0, h, bos + c * C, &bar_v[vb]);
+                tma_load_3d(vbuf + 8192, &args.tm_v, 64, h, bos + c * C, &bar_v[vb]);
+                v_issued = c + 1;
+            };
+            // thread 0: wait for chunk c's v tile
+            auto wait_v = [&](int c) -> bool {
+                const uint32_t r = vcnt + c;
+                const bool ok = mbar_wait(&bar_v[r % kVRing], (r / kVRing) & 1, &abort_flag);
+                if (ok) {
+                    v_waited = c + 1;
+                }
+                return ok;
+            };
+            // thread 0: copy chunk c's slot into buffer (cnt + c) & 1
             auto fetch = [&](int c, bool block) -> bool {
                 const int32_t g = g0 + c;
                 const int32_t slot = i * p.ring + g % p.ring;
@@ -607,10 +635,8 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 fence_proxy_async();
                 const uint32_t b = (cnt + c) & 1;
                 uint8_t* buf = sm + b * CB_BYTES;
-                mbar_arrive_expect_tx(&bar_full[b], HO_BYTES + 16384);
+                mbar_arrive_expect_tx(&bar_full[b], HO_BYTES);
                 bulk_load(buf, p.handoff + (size_t)slot * HO_BYTES, HO_BYTES, &bar_full[b]);
-                tma_load_3d(buf + CB_V, &args.tm_v, 0, h, bos + c * C, &bar_full[b]);
-                tma_load_3d(buf + CB_V + 8192, &args.tm_v, 64, h, bos + c * C, &bar_full[b]);
                 fetched = c + 1;
                 return true;
             };
@@ -627,19 +653,29 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
             };
 
             if (nch > 0) {
-                if (tid == 0 && fetch(0, true) && nch > 1) {
-                    fetch(1, false);
+                if (tid == 0) {
+                    for (int c = 0; c < nch && c < kVRing; ++c) {
+                        issue_v(c);
+                    }
+                    if (fetch(0, true) && nch > 1) {
+                        fetch(1, false);
+                    }
                 }
                 wait_full(0);
                 tc_fence_after();
                 if (tid == 0 && !abort_flag) {
-                    issue_u_prime_tc(x, tiles(cnt & 1));   // U'^T = V^T Tm^T
+                    if (wait_v(0)) {
+                        tc_fence_after();
+                        issue_u_prime_tc(x, tiles(cnt & 1, vcnt % kVRing));   // U'^T = V^T Tm^T
+                    } else {
+                        record_timeout(p.status, &abort_flag);
+                    }
                 }
                 phase_state_to_tmem(x);
                 cta_sync_tc();
             }
             for (int c = 0; c < nch && !abort_flag; ++c) {
-                const StateTiles st = tiles((cnt + c) & 1);
+                const StateTiles st = tiles((cnt + c) & 1, (vcnt + c) % kVRing);
                 // [O^T | U^T] += S^T [Q+^T | -W^T]  (U^T holds U', O^T zero)
                 if (tid == 0) {
                     issue_ou_tc(x, st);
@@ -664,11 +700,16 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 if (tid == 0) {
                     issue_so_tc(x, st);
                     mma_commit(&bar_os);
+                    // U'(c) is done (before U^T): its v slot takes chunk c + kVRing
+                    if (c + kVRing < nch) {
+                        issue_v(c + kVRing);
+                    }
                     if (c + 1 < nch && (fetched >= c + 2 || fetch(c + 1, true))) {
                         const uint32_t r = cnt + c + 1;
-                        if (mbar_wait(&bar_full[r & 1], (r >> 1) & 1, &abort_flag)) {
+                        if (mbar_wait(&bar_full[r & 1], (r >> 1) & 1, &abort_flag) &&
+                            wait_v(c + 1)) {
                             tc_fence_after();
-                            issue_u_prime_tc(x, tiles(r & 1));
+                            issue_u_prime_tc(x, tiles(r & 1, (vcnt + c + 1) % kVRing));
                         } else {
                             record_timeout(p.status, &abort_flag);
                         }
@@ -708,6 +749,11 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
             // copies still in flight into this CTA's buffers (a loop left early)
             if (tid == 0) {
                 s_issued = fetched;
+                for (int c = v_waited; c < v_issued; ++c) {
+                    const uint32_t r = vcnt + c;
+                    mbar_wait(&bar_v[r % kVRing], (r / kVRing) & 1, nullptr);
+                }
+                s_vissued = v_issued;
             }
             __syncthreads();
             const int issued = s_issued;
@@ -716,6 +762,7 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 mbar_wait(&bar_full[r & 1], (r >> 1) & 1, nullptr);
             }
             cnt += issued;
+            vcnt += s_vissued;
             if (!abort_flag && p.final_state) {
                 store_state(x, p.final_state + state_off);
             }
