@@ -69,6 +69,8 @@ def _load():
                 ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
                 ctypes.c_double, ctypes.POINTER(ctypes.c_int32), ctypes.c_int64, dp, dp,
                 ctypes.c_int64, ctypes.POINTER(ctypes.c_int64), dp, ctypes.c_int]
+            lib.kda_oracle_gate_softplus.restype = ctypes.c_double
+            lib.kda_oracle_gate_softplus.argtypes = [ctypes.c_double, ctypes.c_double]
             lib.kda_oracle_gate.restype = ctypes.c_double
             lib.kda_oracle_gate.argtypes = [ctypes.c_double, ctypes.c_double]
             lib.kda_oracle_gate_vec.restype = None
@@ -94,6 +96,13 @@ def _ptr(a, ctype=ctypes.c_double):
     return a.ctypes.data_as(ctypes.POINTER(ctype))
 
 
+def gate_softplus(z, A: float):
+    """Kimi Linear's negative-softplus gate g = -softplus(e^A z), elementwise (fp64)."""
+    lib = _load()
+    zz = np.asarray(z, dtype=np.float64)
+    return np.vectorize(lambda v: lib.kda_oracle_gate_softplus(float(v), float(A)))(zz)
+
+
 def gate(z, A: float):
     """g = -5 * sigmoid(e^A z), elementwise, in fp64."""
     lib = _load()
@@ -105,7 +114,7 @@ def gate(z, A: float):
 
 def kda_reference(q, k, v, z, beta, A, initial_state=None, cu_seqlens=None,
                   scale: float = 1.0, l2norm: bool = True, eps: float = EPS,
-                  chunk: int = 0, units=None, nthreads: int = 0):
+                  chunk: int = 0, units=None, nthreads: int = 0, softplus_gate: bool = False):
     """Run the oracle.
 
     Layouts (token-major, packed):
@@ -115,6 +124,8 @@ def kda_reference(q, k, v, z, beta, A, initial_state=None, cu_seqlens=None,
     chunk: 0 = recurrent form (the oracle), C > 0 = the chunked form.
     units: optional iterable of (n, h) pairs; only those are computed and the
       other outputs are left as NaN.
+    softplus_gate: Kimi Linear's unbounded gate g = -softplus(e^A z) instead of
+      K3's g = -5 sigmoid(e^A z).
     Returns (o [total_T, H, d_v] fp64, final_state [N, H, d_k, d_v] fp64,
     threads_used).
     """
@@ -148,7 +159,8 @@ def kda_reference(q, k, v, z, beta, A, initial_state=None, cu_seqlens=None,
         u, n_units, uptr = None, 0, None
     rc = lib.kda_oracle_run(
         _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(S0),
-        _ptr(cu, ctypes.c_int64), N, H, dk, dv, float(scale), int(bool(l2norm)),
+        _ptr(cu, ctypes.c_int64), N, H, dk, dv, float(scale),
+        int(bool(l2norm)) | (2 if softplus_gate else 0),
         float(eps), int(chunk), uptr, n_units, _ptr(o), _ptr(S_out), int(nthreads))
     if rc <= 0:
         raise RuntimeError(f"oracle failed with status {rc}")

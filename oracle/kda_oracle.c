@@ -60,6 +60,20 @@ static double oracle_sigmoid(double x)
     return e / (1.0 + e);
 }
 
+/* Kimi Linear's unbounded negative-softplus decay, which the same section
+ * says K3 replaced: g = -softplus(e^A * z) = -log(1 + e^{e^A z}) (the pages
+ * give its name, not its argument; the argument e^A z of the K3 gate is the
+ * reading).  Evaluated without overflow: softplus(x) = max(x, 0) + log1p(e^-|x|). */
+static double oracle_neg_softplus(double x)
+{
+    return -((x > 0.0 ? x : 0.0) + log1p(exp(-fabs(x))));
+}
+
+double kda_oracle_gate_softplus(double z, double A)
+{
+    return oracle_neg_softplus(exp(A) * z);
+}
+
 /* Gate equation of section 1: g = g_min * sigmoid(e^A * z). */
 double kda_oracle_gate(double z, double A)
 {
@@ -102,6 +116,7 @@ typedef struct {
     int N, H, dk, dv;
     double scale, eps;
     int l2norm;
+    int softplus;         /* 1: Kimi Linear's negative-softplus gate instead of the K3 one */
     int chunk;            /* 0 = recurrent form, >0 = chunked form with this C */
     double* o;            /* [total_T, H, dv] */
     double* S_out;        /* [N, H, dk, dv] or NULL */
@@ -141,7 +156,9 @@ static int oracle_unit_recurrent(oracle_job* J, int n, int h)
         oracle_normalise(J->k + rowk, dk, J->l2norm, J->eps, 1.0, kh);
         for (int c = 0; c < dk; ++c) {
             /* gate equation (same as kda_oracle_gate, with e^A hoisted) */
-            alpha[c] = exp(KDA_ORACLE_GMIN * oracle_sigmoid(eA * J->z[rowk + c]));
+            const double x = eA * J->z[rowk + c];
+            alpha[c] = exp(J->softplus ? oracle_neg_softplus(x)
+                                       : KDA_ORACLE_GMIN * oracle_sigmoid(x));
         }
         const double b = J->beta[(size_t)t * H + h];
         /* S' = Diag(alpha) S */
@@ -226,7 +243,8 @@ static int oracle_unit_chunked(oracle_job* J, int n, int h)
             oracle_normalise(J->q + rowk, dk, J->l2norm, J->eps, J->scale, Q + (size_t)r * dk);
             oracle_normalise(J->k + rowk, dk, J->l2norm, J->eps, 1.0, K + (size_t)r * dk);
             for (int c = 0; c < dk; ++c) {
-                const double g = kda_oracle_gate(J->z[rowk + c], J->A[h]);
+                const double g = J->softplus ? kda_oracle_gate_softplus(J->z[rowk + c], J->A[h])
+                                             : kda_oracle_gate(J->z[rowk + c], J->A[h]);
                 G[(size_t)r * dk + c] = (r == 0 ? 0.0 : G[(size_t)(r - 1) * dk + c]) + g;
             }
             bet[r] = J->beta[(size_t)(t0 + r) * H + h];
@@ -369,6 +387,7 @@ static int oracle_run(oracle_job* J, int nthreads)
 }
 
 /* Returns the number of threads used (> 0), or a negative value on error.
+ * `l2norm`: bit 0 = L2-normalise q and k, bit 1 = the negative-softplus gate.
  * `units`: NULL for every (sequence, head) pair, else n_units (n, h) pairs;
  * outputs are written only for the listed pairs. */
 int kda_oracle_run(const double* q, const double* k, const double* v, const double* z,
@@ -382,7 +401,8 @@ int kda_oracle_run(const double* q, const double* k, const double* v, const doub
     memset(&J, 0, sizeof(J));
     J.q = q; J.k = k; J.v = v; J.z = z; J.beta = beta; J.A = A; J.S0 = S0;
     J.cu = cu_seqlens; J.N = N; J.H = H; J.dk = dk; J.dv = dv;
-    J.scale = scale; J.eps = eps; J.l2norm = l2norm; J.chunk = chunk;
+    J.scale = scale; J.eps = eps; J.l2norm = l2norm & 1; J.softplus = (l2norm >> 1) & 1;
+    J.chunk = chunk;
     J.o = o; J.S_out = S_out; J.units = units; J.n_units = n_units;
     return oracle_run(&J, nthreads);
 }
@@ -405,7 +425,8 @@ int kda_oracle_run_ckpt(const double* q, const double* k, const double* v, const
     memset(&J, 0, sizeof(J));
     J.q = q; J.k = k; J.v = v; J.z = z; J.beta = beta; J.A = A; J.S0 = S0;
     J.cu = cu_seqlens; J.N = N; J.H = H; J.dk = dk; J.dv = dv;
-    J.scale = scale; J.eps = eps; J.l2norm = l2norm; J.chunk = 0;
+    J.scale = scale; J.eps = eps; J.l2norm = l2norm & 1; J.softplus = (l2norm >> 1) & 1;
+    J.chunk = 0;
     J.o = o; J.S_out = S_out; J.units = units; J.n_units = n_units;
     J.ckpt_interval = ckpt_interval; J.ckpt_base = ckpt_base; J.ckpt = ckpt;
     return oracle_run(&J, nthreads);

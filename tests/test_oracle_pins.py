@@ -343,3 +343,51 @@ def test_checkpoints_are_prefix_final_states(oracle_mod):
                 assert np.array_equal(orr, o[rest]) and np.array_equal(Srr[0], S[n])
     # length 8 = 2 intervals: the last checkpoint is the final state
     assert np.array_equal(ck[base[2] + 1], S[2])
+
+
+# ------------------------------------------------- Kimi Linear softplus gate
+def test_softplus_gate_closed_forms(oracle_mod):
+    """g = -softplus(e^A z): g(0) = -ln 2 for any A (alpha = 1/2); alpha is the
+    logistic function of -e^A z; the gate is unbounded below (about -x for
+    large x) and tends to 0 for large negative arguments."""
+    for A in (-1.3, 0.0, 0.7):
+        assert abs(oracle_mod.gate_softplus(0.0, A) + math.log(2.0)) < 1e-15
+    for z, A in ((0.3, 0.2), (-2.0, 0.5), (5.0, -0.4), (40.0, 1.0)):
+        x = math.exp(A) * z
+        alpha = math.exp(float(oracle_mod.gate_softplus(z, A)))
+        assert abs(alpha - 1.0 / (1.0 + math.exp(x))) <= 1e-15 * max(1.0, alpha) + 1e-300
+    g = float(oracle_mod.gate_softplus(1000.0, 0.0))
+    assert abs(g + 1000.0) < 1e-9                  # unbounded: no -5 floor
+    assert float(oracle_mod.gate_softplus(-800.0, 0.0)) > -1e-300
+
+
+@pytest.mark.parametrize("T,dk,dv", [(5, 3, 2), (8, 4, 4)])
+def test_softplus_gate_brute_force_products(oracle_mod, T, dk, dv):
+    """The recurrence with the softplus gate equals the explicit product of the
+    transition matrices (I - beta k k^T) Diag(alpha) on tiny inputs."""
+    rng = np.random.default_rng(40 + T)
+    q, k, v, z, beta, A, S0 = _rand_case(rng, T, 1, dk, dv, zscale=3.0)
+    o, S, _ = oracle_mod.kda_reference(q, k, v, z, beta, A, S0, softplus_gate=True)
+    St = S0[0, 0].copy()
+    for t in range(T):
+        kh = _unit(k[t, 0]); qh = _unit(q[t, 0])
+        x = math.exp(A[0]) * z[t, 0]
+        alpha = 1.0 / (1.0 + np.exp(x))          # e^{-softplus(x)}
+        St = (np.eye(dk) - beta[t, 0] * np.outer(kh, kh)) @ np.diag(alpha) @ St \
+            + beta[t, 0] * np.outer(kh, v[t, 0])
+        assert _close(o[t, 0], St.T @ qh, 1e-12)
+    assert _close(S[0, 0], St, 1e-12)
+
+
+def test_softplus_gate_chunked_equals_recurrent(oracle_mod):
+    rng = np.random.default_rng(44)
+    lens = [70, 3, 33]
+    T, H, dk, dv = sum(lens), 2, 6, 5
+    q, k, v, z, beta, A, S0 = _rand_case(rng, T, H, dk, dv, N=len(lens), zscale=2.0)
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    o_r, S_r, _ = oracle_mod.kda_reference(q, k, v, z, beta, A, S0, cu, softplus_gate=True)
+    o_c, S_c, _ = oracle_mod.kda_reference(q, k, v, z, beta, A, S0, cu, chunk=16,
+                                           softplus_gate=True)
+    assert _close(o_c, o_r, 1e-10) and _close(S_c, S_r, 1e-10)
+    o_k3, _, _ = oracle_mod.kda_reference(q, k, v, z, beta, A, S0, cu)
+    assert not _close(o_k3, o_r, 1e-3)             # the two gates really differ
