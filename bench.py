@@ -324,10 +324,13 @@ def kda_arm(args, world, rank, local, pg):
                               "tensor_tflops": achieved_tf}), flush=True)
         return
     ckpt = measure_checkpointed(sets, ws, o, S, cu_host, B, H, T, d, args, stream)
+    softplus = measure_softplus(sets, ws, o, S, cu_host, args, stream)
+    softplus["tokens_per_s"] = B * T / (softplus["kernel_ms"] / 1e3)
 
     return finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops, nsets,
                   set_bytes, x_host, o, S, ws, cu_host, value, ms_per_step, kernel_ms,
-                  achieved_gbs, achieved_tf, clk, launches_per_step, kernel_name, pg, ckpt)
+                  achieved_gbs, achieved_tf, clk, launches_per_step, kernel_name, pg, ckpt,
+                  softplus)
 
 
 def measure_checkpointed(sets, ws, o, S, cu_host, B, H, T, d, args, stream, interval=1024):
@@ -354,7 +357,29 @@ def measure_checkpointed(sets, ws, o, S, cu_host, B, H, T, d, args, stream, inte
             "checkpoint_bytes": count * H * d * d * 4, "kernel_ms": ms}
 
 
-def run_decode(dev, rank, local, stream, batch=None):
+def measure_softplus(sets, ws, o, S, cu_host, args, stream):
+    """The same prefill with the softplus-decay gate (KDA_FLAG_SOFTPLUS_GATE), which
+    runs on the fp32 recurrent kernel: its kernel time."""
+    import torch
+    import kimi_delta_attention_12_gb300 as kda
+    n = min(args.steps, 5)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    for i in range(args.warmup + n):
+        x = sets[i % len(sets)]
+        if i >= args.warmup:
+            ev[i - args.warmup][0].record(stream)
+        kda.kda_prefill(x.q, x.k, x.v, x.z, x.beta, x.A, None, x.cu_seqlens,
+                        cu_seqlens_host=cu_host, o=o, final_state=S, workspace=ws,
+                        softplus_gate=True)
+        if i >= args.warmup:
+            ev[i - args.warmup][1].record(stream)
+    torch.cuda.synchronize()
+    return {"kernel": "kda_recurrent_kernel",
+            "kernel_ms": statistics.mean(a.elapsed_time(b) for a, b in ev), "steps": n}
+
+
+def run_decode(dev, rank, local, stream, batch=None, softplus_gate=False):
     """64 consecutive decode steps on a resident B=256, H=96, d=128 fp32 state."""
     import torch
     import kimi_delta_attention_12_gb300 as kda
@@ -374,7 +399,8 @@ def run_decode(dev, rank, local, stream, batch=None):
     od = torch.empty(Bd, Hd, dd, dtype=torch.bfloat16, device=dev)
     for s in range(3):
         q_, k_, v_, z_, b_ = dsteps[s]
-        kda.kda_decode_step(q_, k_, v_, z_, b_, Adec, state, o=od)
+        kda.kda_decode_step(q_, k_, v_, z_, b_, Adec, state, o=od,
+                            softplus_gate=softplus_gate)
     torch.cuda.synchronize()
     dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(D["steps"])]
@@ -382,7 +408,8 @@ def run_decode(dev, rank, local, stream, batch=None):
         for s in range(D["steps"]):
             q_, k_, v_, z_, b_ = dsteps[s]
             dev_ev[s][0].record(stream)
-            kda.kda_decode_step(q_, k_, v_, z_, b_, Adec, state, o=od)
+            kda.kda_decode_step(q_, k_, v_, z_, b_, Adec, state, o=od,
+                            softplus_gate=softplus_gate)
             dev_ev[s][1].record(stream)
         torch.cuda.synchronize()
     dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dev_ev)
@@ -400,7 +427,7 @@ def decode_only(args, rank, local, dev, stream, peaks):
 
 def finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops, nsets,
            set_bytes, x_host, o, S, ws, cu_host, value, ms_per_step, kernel_ms, achieved_gbs,
-           achieved_tf, clk, launches_per_step, kernel_name, pg, ckpt):
+           achieved_tf, clk, launches_per_step, kernel_name, pg, ckpt, softplus):
     import torch
     import kimi_delta_attention_12_gb300 as kda
     # ---- end to end through the public API with host buffers ----
@@ -439,6 +466,9 @@ def finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops
     # ---- decode workload: 64 consecutive steps on a resident 1.6 GB state ----
     D = DECODE_SHAPE
     dec_ms, dec_bytes, dec_gbs, dclk_summary = run_decode(dev, rank, local, stream)
+    sp_ms, _, sp_gbs, _ = run_decode(dev, rank, local, stream, softplus_gate=True)
+    softplus.update({"decode_ms_per_step": sp_ms, "decode_gbs": sp_gbs,
+                     "decode_frac": sp_gbs / peaks["hbm_gbs"]})
 
     if rank != 0:
         return
@@ -468,6 +498,7 @@ def finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops
                                 "unit": "GB/s", "frac": dec_gbs / peaks["hbm_gbs"]},
                    "clocks": dclk_summary},
         "prefill_checkpointed": dict(ckpt, kernel_ms_plain=kernel_ms),
+        "softplus_gate": softplus,
         "cpu_baseline": {"value": cpu_tps, "unit": "tokens/s", "cores": cpu_threads,
                          "kind": "oracle", "sample": cpu_sample},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,

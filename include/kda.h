@@ -64,9 +64,16 @@ typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
 
 enum {
     KDA_FLAG_L2NORM_QK = 1,    /* L2-normalise q and k inside the call (default on)  */
-    KDA_FLAG_RECURRENT = 2     /* kda_prefill only: run the fused recurrent kernel
+    KDA_FLAG_RECURRENT = 2,    /* kda_prefill only: run the fused recurrent kernel
                                   (fp32 arithmetic, one token at a time) even where
                                   the chunked tensor-core kernel applies */
+    KDA_FLAG_SOFTPLUS_GATE = 4 /* Kimi Linear's unbounded gate g = -softplus(e^A z),
+                                  alpha = e^g = sigmoid(-e^A z), in place of
+                                  g = -5 sigmoid(e^A z) (the pages' section 1 names it
+                                  as the decay K3 replaced).  Its decay has no lower
+                                  bound, so the 16-token reciprocal tiles of the
+                                  chunked kernels do not apply: prefill runs the fused
+                                  recurrent kernel (fp32), decode is unchanged. */
 };
 #define KDA_DEFAULT_FLAGS KDA_FLAG_L2NORM_QK
 
@@ -105,7 +112,7 @@ KDA_API size_t kda_prefill_workspace_bytes(int32_t N, int32_t total_T, int32_t H
  *                 validated (starts at 0, non-decreasing, ends at total_T)
  *                 and used to schedule long sequences first.
  *  scale          multiplies q_hat (1.0 = none)
- *  flags          KDA_FLAG_L2NORM_QK or 0
+ *  flags          KDA_FLAG_L2NORM_QK, KDA_FLAG_RECURRENT, KDA_FLAG_SOFTPLUS_GATE (or 0)
  *  o              [total_T, H, d_v]  dt, output (o_t for every token)
  *  final_state    [N, H, d_k, d_v] fp32, or NULL.  May alias initial_state
  *                 (in-place update is allowed).

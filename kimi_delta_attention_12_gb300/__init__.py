@@ -35,6 +35,7 @@ KDA_BF16 = 1
 
 KDA_FLAG_L2NORM_QK = 1
 KDA_FLAG_RECURRENT = 2
+KDA_FLAG_SOFTPLUS_GATE = 4
 
 KDA_STATE_ZERO = 0
 KDA_STATE_COPY = 1
@@ -148,7 +149,7 @@ def kda_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: torch.Tens
                 cu_seqlens: Optional[torch.Tensor] = None,
                 cu_seqlens_host: Optional[torch.Tensor] = None,
                 scale: float = 1.0, l2norm: bool = True, recurrent: bool = False,
-                output_final_state: bool = True,
+                softplus_gate: bool = False, output_final_state: bool = True,
                 o: Optional[torch.Tensor] = None, final_state: Optional[torch.Tensor] = None,
                 workspace: Optional[torch.Tensor] = None,
                 ckpt_interval: int = 0, ckpt_pool: Optional[torch.Tensor] = None,
@@ -162,7 +163,10 @@ def kda_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: torch.Tens
     With ckpt_interval > 0 (a multiple of 64) the state after every
     ckpt_interval tokens of each sequence is also written into ckpt_pool
     [pool, H, d_k, d_v] fp32, at row ckpt_slots[i] (int32, default i) for
-    checkpoint i (kda_prefill_checkpointed in include/kda.h)."""
+    checkpoint i (kda_prefill_checkpointed in include/kda.h).
+
+    softplus_gate=True selects Kimi Linear's unbounded gate -softplus(e^A z)
+    (KDA_FLAG_SOFTPLUS_GATE; runs the fused recurrent kernel)."""
     batched = q.dim() == 4
     if batched:
         B, T = q.shape[:2]
@@ -193,7 +197,8 @@ def kda_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: torch.Tens
     host_cu = None
     if cu_seqlens_host is not None:
         host_cu = cu_seqlens_host.to(torch.int32).contiguous()
-    flags = (KDA_FLAG_L2NORM_QK if l2norm else 0) | (KDA_FLAG_RECURRENT if recurrent else 0)
+    flags = ((KDA_FLAG_L2NORM_QK if l2norm else 0) | (KDA_FLAG_RECURRENT if recurrent else 0)
+             | (KDA_FLAG_SOFTPLUS_GATE if softplus_gate else 0))
     host_ptr = None if host_cu is None else ctypes.c_void_p(host_cu.data_ptr())
     if ckpt_interval:
         _check_cuda(ckpt_pool, ckpt_slots)
@@ -241,7 +246,7 @@ def kda_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: torch.
                     beta: torch.Tensor, A: torch.Tensor, state: torch.Tensor,
                     slots: Optional[torch.Tensor] = None, scale: float = 1.0,
                     l2norm: bool = True, o: Optional[torch.Tensor] = None,
-                    stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+                    stream: Optional[torch.cuda.Stream] = None, softplus_gate: bool = False) -> torch.Tensor:
     """One decode token per sequence: q, k, z [B, H, d_k], v [B, H, d_v],
     beta [B, H]; `state` [pool, H, d_k, d_v] fp32 is updated in place at
     rows `slots` (default 0..B-1).  Returns o [B, H, d_v]."""
@@ -255,7 +260,7 @@ def kda_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: torch.
         raise TypeError("slots must be int32")
     if o is None:
         o = torch.empty(B, H, d_v, dtype=dt, device=q.device)
-    flags = KDA_FLAG_L2NORM_QK if l2norm else 0
+    flags = (KDA_FLAG_L2NORM_QK if l2norm else 0) | (KDA_FLAG_SOFTPLUS_GATE if softplus_gate else 0)
     st = lib().kda_decode_step(
         _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(state), _ptr(slots),
         state.shape[0], B, H, d_k, d_v, _dtype_code(dt), float(scale), flags, _ptr(o),

@@ -20,7 +20,7 @@ inline bool supported_dim(int32_t d) { return d == 32 || d == 64 || d == 128; }
 
 inline size_t elem_bytes(kda_dtype dt) { return dt == KDA_F32 ? 4 : 2; }
 
-constexpr uint32_t kKnownFlags = KDA_FLAG_L2NORM_QK | KDA_FLAG_RECURRENT;
+constexpr uint32_t kKnownFlags = KDA_FLAG_L2NORM_QK | KDA_FLAG_RECURRENT | KDA_FLAG_SOFTPLUS_GATE;
 constexpr uint32_t kFlagRecurrent = KDA_FLAG_RECURRENT;
 constexpr int32_t kCheckpointGrain = 64;  // checkpoints fall on chunk boundaries
 
@@ -174,7 +174,8 @@ int kda_prefill_checkpointed(const void* q, const void* k, const void* v, const 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int32_t* ws = static_cast<int32_t*>(workspace);
     const bool use_chunked = kda::kChunkedPrefillBuilt && dt == KDA_BF16 && d_k == 128 && d_v == 128 &&
-                             (flags & kFlagRecurrent) == 0 && total_T > 0;
+                             (flags & (kFlagRecurrent | KDA_FLAG_SOFTPLUS_GATE)) == 0 &&
+                             total_T > 0;
     const int sms = use_chunked ? current_sm_count() : 0;
     kda::SplitPlan plan;
     const bool use_split = use_chunked && split_eligible(N, H, dt, d_k, d_v, sms, &plan) &&
@@ -210,6 +211,7 @@ int kda_prefill_checkpointed(const void* q, const void* k, const void* v, const 
         p.slots = nullptr; p.cu_seqlens = cu_seqlens; p.o = o;
         p.rows = N; p.total_T = total_T; p.H = H; p.pool_size = 0;
         p.scale = scale; p.l2norm = (flags & KDA_FLAG_L2NORM_QK) ? 1 : 0; p.decode = 0;
+        p.softplus_gate = (flags & KDA_FLAG_SOFTPLUS_GATE) ? 1 : 0;
         p.ckpt_interval = ckpt_interval; p.ckpt_pool = ckpt_pool;
         p.ckpt_slots = ckpt_slots; p.ckpt_pool_size = ckpt_pool_size;
         if (total_T == 0 && !final_state) {
@@ -229,7 +231,9 @@ int kda_decode_step(const void* q, const void* k, const void* v, const void* z,
     if (dt != KDA_F32 && dt != KDA_BF16) return KDA_ERR_UNSUPPORTED;
     if (!supported_dim(d_k) || !supported_dim(d_v)) return KDA_ERR_UNSUPPORTED;
     if (B < 0 || H < 1 || pool_size < 0) return KDA_ERR_INVALID_ARG;
-    if ((flags & ~(uint32_t)KDA_FLAG_L2NORM_QK) != 0) return KDA_ERR_INVALID_ARG;
+    if ((flags & ~(uint32_t)(KDA_FLAG_L2NORM_QK | KDA_FLAG_SOFTPLUS_GATE)) != 0) {
+        return KDA_ERR_INVALID_ARG;
+    }
     if (!isfinite(scale)) return KDA_ERR_INVALID_ARG;
     if (B == 0) return KDA_OK;
     if (!q || !k || !v || !z || !beta || !A || !state || !o) return KDA_ERR_INVALID_ARG;
@@ -246,6 +250,7 @@ int kda_decode_step(const void* q, const void* k, const void* v, const void* z,
     p.state_in = state; p.state_out = state; p.slots = slots; p.cu_seqlens = nullptr;
     p.o = o; p.rows = B; p.total_T = B; p.H = H; p.pool_size = pool_size;
     p.scale = scale; p.l2norm = (flags & KDA_FLAG_L2NORM_QK) ? 1 : 0; p.decode = 1;
+    p.softplus_gate = (flags & KDA_FLAG_SOFTPLUS_GATE) ? 1 : 0;
     const cudaError_t err = kda::launch_recurrent(p, d_k, d_v, dt == KDA_F32 ? 0 : 1,
                                                   static_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;

@@ -33,6 +33,7 @@ struct RecurrentParams {
     float scale;
     int32_t l2norm;
     int32_t decode;
+    int32_t softplus_gate;  // Kimi Linear's gate -softplus(e^A z) instead of -5 sigmoid(e^A z)
     // prefill only: state checkpoints every ckpt_interval tokens (0 = none)
     int32_t ckpt_interval;
     float* ckpt_pool;

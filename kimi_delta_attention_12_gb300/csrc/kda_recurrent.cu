@@ -4,7 +4,9 @@
 // walks that row's tokens in order.  Per token it fuses everything the
 // recurrence of "Kimi K3 Open Weights: What Is Actually New In Its 2.8
 // Trillion Parameter Architecture", section 1, asks for:
-//   gate     alpha = exp(-5 * sigmoid(e^A z))           (gate equation)
+//   gate     alpha = exp(-5 * sigmoid(e^A z))           (gate equation; or
+//            sigmoid(-e^A z) = exp(-softplus(e^A z)), the unbounded gate the
+//            section says K3 replaced)
 //   decay    S'    = Diag(alpha) S
 //   erase    u     = beta (v - S'^T k_hat)
 //   write    S     = S' + k_hat u^T                     (delta-rule update)
@@ -174,7 +176,9 @@ kda_recurrent_kernel(const RecurrentParams p) {
             const float zv = load_elem(z, rk + tid);
             s_q[tid] = qv;
             s_k[tid] = kv;
-            s_a[tid] = expf(kGmin * sigmoid_f(eA * zv));
+            // alpha = e^g: K3's g = -5 sigmoid(e^A z), or Kimi Linear's
+            // g = -softplus(e^A z), for which e^g = sigmoid(-e^A z)
+            s_a[tid] = p.softplus_gate ? sigmoid_f(-eA * zv) : expf(kGmin * sigmoid_f(eA * zv));
             float sq = qv * qv, sk = kv * kv, sqk = qv * kv;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) {

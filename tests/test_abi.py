@@ -88,6 +88,7 @@ def _call_prefill(L, a):
     (dict(o=None), kda.KDA_ERR_INVALID_ARG),
     (dict(A=None), kda.KDA_ERR_INVALID_ARG),
     (dict(flags=8), kda.KDA_ERR_INVALID_ARG),
+    (dict(flags=16), kda.KDA_ERR_INVALID_ARG),
     (dict(scale=float("nan")), kda.KDA_ERR_INVALID_ARG),
     (dict(N=3, T=64), kda.KDA_ERR_INVALID_ARG),      # 64 % 3 != 0 without cu_seqlens
     (dict(ws=None), kda.KDA_ERR_WORKSPACE),
@@ -134,6 +135,7 @@ def _call_decode(L, **over):
     (dict(pool=2), kda.KDA_ERR_INVALID_ARG),    # identity slots need pool >= B
     (dict(state=None), kda.KDA_ERR_INVALID_ARG),
     (dict(flags=2), kda.KDA_ERR_INVALID_ARG),   # the recurrent flag is prefill-only
+    (dict(flags=8), kda.KDA_ERR_INVALID_ARG),
     (dict(k=BASE + 0x100004), kda.KDA_ERR_ALIGNMENT),
     (dict(state=BASE + 0x600008), kda.KDA_ERR_ALIGNMENT),
     (dict(slots=BASE + 0x800002), kda.KDA_ERR_ALIGNMENT),
