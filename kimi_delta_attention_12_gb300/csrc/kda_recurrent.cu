@@ -60,9 +60,18 @@ __device__ __forceinline__ float sigmoid_f(float x) {
     return e / (1.0f + e);
 }
 
-template <int DK, int DV, int NSPLIT, typename T>
+// Launch modes.  Each is its own instantiation so that the decode kernel,
+// whose occupancy (and so its HBM bandwidth) depends on its register count,
+// carries none of the prefill bookkeeping.
+constexpr int kModeDecode = 0;    // one token per row, state pool with slots
+constexpr int kModePrefill = 1;   // a sequence per row
+constexpr int kModeCkpt = 2;      // prefill that also stores state checkpoints
+
+template <int DK, int DV, int NSPLIT, typename T, int kMode>
 __global__ void __launch_bounds__(kThreads)
 kda_recurrent_kernel(const RecurrentParams p) {
+    constexpr bool kDecode = kMode == kModeDecode;
+    constexpr bool kCkpt = kMode == kModeCkpt;
     constexpr int DVS = DV / NSPLIT;
     constexpr int LPR = DVS / 4;
     constexpr int RPW = 32 / LPR;
@@ -102,7 +111,7 @@ kda_recurrent_kernel(const RecurrentParams p) {
     int64_t bos, eos;
     int64_t sidx = row;  // index of this row's state in state_in / state_out
     bool valid = true;
-    if (p.decode) {
+    if constexpr (kDecode) {
         bos = row;
         eos = row + 1;
         if (p.slots) {
@@ -147,9 +156,10 @@ kda_recurrent_kernel(const RecurrentParams p) {
 
     // prefill state checkpoints: index of this row's first one (the sum over
     // earlier sequences of floor(length / interval))
-    __shared__ int s_ck;
-    int64_t ck_base = 0;
-    if (!p.decode && p.ckpt_interval > 0) {
+    int64_t ck_idx = 0;               // pool index of the row's next checkpoint
+    int64_t ck_next = INT64_MAX;      // token after which it is taken
+    if constexpr (kCkpt) {
+        __shared__ int s_ck;
         if (tid == 0) {
             s_ck = 0;
         }
@@ -164,7 +174,8 @@ kda_recurrent_kernel(const RecurrentParams p) {
             atomicAdd(&s_ck, part);
         }
         __syncthreads();
-        ck_base = s_ck;
+        ck_idx = s_ck;
+        ck_next = bos + p.ckpt_interval - 1;
     }
 
     for (int64_t t = bos; t < eos; ++t) {
@@ -178,7 +189,8 @@ kda_recurrent_kernel(const RecurrentParams p) {
             s_k[tid] = kv;
             // alpha = e^g: K3's g = -5 sigmoid(e^A z), or Kimi Linear's
             // g = -softplus(e^A z), for which e^g = sigmoid(-e^A z)
-            s_a[tid] = p.softplus_gate ? sigmoid_f(-eA * zv) : expf(kGmin * sigmoid_f(eA * zv));
+            const float sg = sigmoid_f(p.softplus_gate ? -eA * zv : eA * zv);
+            s_a[tid] = p.softplus_gate ? sg : expf(kGmin * sg);
             float sq = qv * qv, sk = kv * kv, sqk = qv * kv;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) {
@@ -269,15 +281,19 @@ kda_recurrent_kernel(const RecurrentParams p) {
         }
 
         // ---- state checkpoint after every ckpt_interval tokens of the row ----
-        if (!p.decode && p.ckpt_interval > 0 && (t - bos + 1) % p.ckpt_interval == 0) {
-            const int64_t idx = ck_base + (t - bos + 1) / p.ckpt_interval - 1;
-            const int64_t prow = p.ckpt_slots ? (int64_t)p.ckpt_slots[idx] : idx;
-            if (prow >= 0 && prow < p.ckpt_pool_size) {
-                float4* cp = reinterpret_cast<float4*>(p.ckpt_pool + ((size_t)prow * H + h) * DK * DV);
+        if constexpr (kCkpt) {
+            if (t == ck_next) {
+                const int64_t idx = ck_idx++;
+                ck_next += p.ckpt_interval;
+                const int64_t prow = p.ckpt_slots ? (int64_t)p.ckpt_slots[idx] : idx;
+                if (prow >= 0 && prow < p.ckpt_pool_size) {
+                    float4* cp = reinterpret_cast<float4*>(p.ckpt_pool +
+                                                           ((size_t)prow * H + h) * DK * DV);
 #pragma unroll
-                for (int r = 0; r < RPT; ++r) {
-                    const int i = r * RSTEP + w * RPW + rs;
-                    __stcs(cp + (i * DV + col0) / 4 + cg, S[r]);
+                    for (int r = 0; r < RPT; ++r) {
+                        const int i = r * RSTEP + w * RPW + rs;
+                        __stcs(cp + (i * DV + col0) / 4 + cg, S[r]);
+                    }
                 }
             }
         }
@@ -298,6 +314,21 @@ kda_recurrent_kernel(const RecurrentParams p) {
 template <int DV>
 constexpr int column_split() { return DV == 128 ? 2 : 1; }
 
+template <int DK, int DV, int NS, typename T>
+void launch_mode(int mode, dim3 grid, const RecurrentParams& p, cudaStream_t stream) {
+    switch (mode) {
+        case kModeDecode:
+            kda_recurrent_kernel<DK, DV, NS, T, kModeDecode><<<grid, kThreads, 0, stream>>>(p);
+            break;
+        case kModeCkpt:
+            kda_recurrent_kernel<DK, DV, NS, T, kModeCkpt><<<grid, kThreads, 0, stream>>>(p);
+            break;
+        default:
+            kda_recurrent_kernel<DK, DV, NS, T, kModePrefill><<<grid, kThreads, 0, stream>>>(p);
+            break;
+    }
+}
+
 template <int DK, int DV>
 cudaError_t launch_dims(const RecurrentParams& p, int dtype, cudaStream_t stream) {
     constexpr int NS = column_split<DV>();
@@ -305,10 +336,11 @@ cudaError_t launch_dims(const RecurrentParams& p, int dtype, cudaStream_t stream
     if (grid.x == 0) {
         return cudaSuccess;
     }
+    const int mode = p.decode ? kModeDecode : p.ckpt_interval > 0 ? kModeCkpt : kModePrefill;
     if (dtype == 0) {
-        kda_recurrent_kernel<DK, DV, NS, float><<<grid, kThreads, 0, stream>>>(p);
+        launch_mode<DK, DV, NS, float>(mode, grid, p, stream);
     } else {
-        kda_recurrent_kernel<DK, DV, NS, __nv_bfloat16><<<grid, kThreads, 0, stream>>>(p);
+        launch_mode<DK, DV, NS, __nv_bfloat16>(mode, grid, p, stream);
     }
     return cudaGetLastError();
 }
