@@ -9,7 +9,9 @@ Sources (page titles and sections):
   * "Kimi K3 Open Weights: What Is Actually New In Its 2.8 Trillion Parameter
     Architecture", section 1 "Kimi Delta Attention is a real new kernel
     family": the delta-rule recurrence with o_t = S_t^T q_t, the bounded gate
-    g = -5 sigmoid(e^A z), alpha = e^g, and Q/K normalisation inside the op.
+    g = -5 sigmoid(e^A z), alpha = e^g, and Q/K normalisation inside the op;
+    the short convolutions before it and their persistent conv state (the
+    prefill and decode bullets of the same section).
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against closed
 forms, brute force and invariants that do not reuse this code.
@@ -73,6 +75,10 @@ def _load():
             lib.kda_oracle_gate_softplus.argtypes = [ctypes.c_double, ctypes.c_double]
             lib.kda_oracle_gate.restype = ctypes.c_double
             lib.kda_oracle_gate.argtypes = [ctypes.c_double, ctypes.c_double]
+            lib.kda_oracle_short_conv.restype = ctypes.c_int
+            lib.kda_oracle_short_conv.argtypes = [
+                dp, ctypes.c_int64, ctypes.c_int64, ctypes.POINTER(ctypes.c_int64), ctypes.c_int,
+                dp, ctypes.c_int, dp, ctypes.c_int, dp, dp]
             lib.kda_oracle_gate_vec.restype = None
             lib.kda_oracle_gate_vec.argtypes = [dp, ctypes.c_int64, ctypes.c_double, dp]
             _lib = lib
@@ -221,3 +227,80 @@ def kda_reference_checkpoints(q, k, v, z, beta, A, initial_state=None, cu_seqlen
     if rc <= 0:
         raise RuntimeError(f"oracle failed with status {rc}")
     return o, S_out, ck[:int(counts.sum())], rc
+
+
+def _cu(cu_seqlens, total_T):
+    if cu_seqlens is None:
+        cu_seqlens = np.array([0, total_T], dtype=np.int64)
+    cu = np.ascontiguousarray(np.asarray(
+        cu_seqlens.cpu() if hasattr(cu_seqlens, "cpu") else cu_seqlens, dtype=np.int64))
+    if cu[0] != 0 or cu[-1] != total_T or np.any(np.diff(cu) < 0):
+        raise ValueError("cu_seqlens must be non-decreasing from 0 to total_T")
+    return cu
+
+
+def short_conv(x, w, cu_seqlens=None, state_in=None, silu: bool = False):
+    """Causal depthwise convolution along time (the short convolution).
+
+    x: [total_T, C]; w: [C, W] (w[:, W-1] weights the current token);
+    state_in: [N, W-1, C] or None (zeros), row r = the input W-1-r tokens
+    before the sequence's first one.  Returns (y [total_T, C],
+    state_out [N, W-1, C]): y_t = sum_j w[:, j] x_{t-W+1+j} (then y*sigmoid(y)
+    if silu) and the last W-1 inputs of every sequence, all fp64."""
+    lib = _load()
+    x, w = _f64(x), _f64(w)
+    total_T, C = x.shape
+    W = w.shape[1]
+    if w.shape[0] != C:
+        raise ValueError("w must be [C, W]")
+    cu = _cu(cu_seqlens, total_T)
+    N = cu.size - 1
+    s_in = _f64(state_in)
+    if s_in is not None and s_in.shape != (N, W - 1, C):
+        raise ValueError(f"state_in shape {s_in.shape} != {(N, W - 1, C)}")
+    y = np.empty((total_T, C))
+    s_out = np.empty((N, W - 1, C))
+    rc = lib.kda_oracle_short_conv(_ptr(x), total_T, C, _ptr(cu, ctypes.c_int64), N,
+                                   _ptr(w), W, _ptr(s_in), int(bool(silu)), _ptr(y),
+                                   _ptr(s_out))
+    if rc != 0:
+        raise RuntimeError(f"oracle short_conv failed with status {rc}")
+    return y, s_out
+
+
+def short_conv_qkv(q, k, v, conv_w, cu_seqlens=None, conv_state=None, silu: bool = False):
+    """The short convolutions of q, k and v with the per-head packed layouts
+    of the library: conv_w [H, 2 d_k + d_v, W] fp32 and conv_state
+    [N, H, W-1, 2 d_k + d_v], channels of a head ordered q | k | v.
+
+    Returns (q_c, k_c, v_c, conv_state_out), fp64."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    total_T, H, dk = q.shape
+    dv = v.shape[-1]
+    Cc = 2 * dk + dv
+    w = _f64(conv_w)
+    W = w.shape[-1]
+    x = np.concatenate([q, k, v], axis=-1).reshape(total_T, H * Cc)
+    st = _f64(conv_state)
+    if st is not None:
+        st = np.ascontiguousarray(st.transpose(0, 2, 1, 3).reshape(st.shape[0], W - 1, H * Cc))
+    y, s_out = short_conv(x, w.reshape(H * Cc, W), cu_seqlens, st, silu)
+    y = y.reshape(total_T, H, Cc)
+    s_out = s_out.reshape(-1, W - 1, H, Cc).transpose(0, 2, 1, 3)
+    return (np.ascontiguousarray(y[..., :dk]), np.ascontiguousarray(y[..., dk:2 * dk]),
+            np.ascontiguousarray(y[..., 2 * dk:]), np.ascontiguousarray(s_out))
+
+
+def kda_reference_conv(q, k, v, z, beta, A, conv_w, conv_state=None, initial_state=None,
+                       cu_seqlens=None, silu: bool = False, scale: float = 1.0,
+                       l2norm: bool = True, eps: float = EPS, softplus_gate: bool = False,
+                       nthreads: int = 0):
+    """Short convolutions of q, k, v (short_conv_qkv) followed by the KDA
+    recurrence (kda_reference) on the convolved q, k, v.
+
+    Returns (o, final_state, conv_state_out), fp64."""
+    qc, kc, vc, cs = short_conv_qkv(q, k, v, conv_w, cu_seqlens, conv_state, silu)
+    o, S, _ = kda_reference(qc, kc, vc, z, beta, A, initial_state, cu_seqlens, scale=scale,
+                            l2norm=l2norm, eps=eps, softplus_gate=softplus_gate,
+                            nthreads=nthreads)
+    return o, S, cs

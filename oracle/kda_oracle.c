@@ -431,3 +431,58 @@ int kda_oracle_run_ckpt(const double* q, const double* k, const double* v, const
     J.ckpt_interval = ckpt_interval; J.ckpt_base = ckpt_base; J.ckpt = ckpt;
     return oracle_run(&J, nthreads);
 }
+
+/* ---- short convolution ---------------------------------------------------
+ * Section 1 lists "short convolutions" first among the prefill steps and
+ * keeps a "convolution state" persistent through decode; the section "Why
+ * 104B active still understates the systems problem" counts a fixed-size
+ * short-convolution state per request and layer.  The pages give no formula.  Reading: a causal,
+ * depthwise convolution along time of width W on every channel,
+ *     y_t[c] = sum_{j=0}^{W-1} w[c][j] * x_{t-(W-1)+j}[c]
+ * (w[c][W-1] weights the current token), optionally followed by SiLU,
+ * y * sigmoid(y).  Inputs before a sequence's first token come from that
+ * sequence's conv state, whose row r (0 <= r < W-1) holds the input at
+ * position bos - (W-1) + r (oldest first); with no state they are zero.  The
+ * final conv state is the last W-1 inputs of the sequence, taking rows of
+ * the initial state where the sequence is shorter than W-1.
+ *
+ * Layouts: x, y [total_T, C]; w [C, W]; state_in, state_out [N, W-1, C]
+ * (state_in may be NULL = zeros; state_out may be NULL).  Returns 0, or -1
+ * on a bad argument. */
+int kda_oracle_short_conv(const double* x, int64_t total_T, int64_t C,
+                          const int64_t* cu_seqlens, int N, const double* w, int W,
+                          const double* state_in, int silu, double* y, double* state_out)
+{
+    if (W < 1 || C < 0 || N < 0 || !cu_seqlens || cu_seqlens[0] != 0 ||
+        cu_seqlens[N] != total_T) {
+        return -1;
+    }
+    const int R = W - 1;  /* rows of conv state */
+    for (int n = 0; n < N; ++n) {
+        const int64_t bos = cu_seqlens[n], eos = cu_seqlens[n + 1];
+        if (eos < bos) {
+            return -1;
+        }
+        for (int64_t c = 0; c < C; ++c) {
+            /* input at absolute position tau of this sequence (tau < eos) */
+#define ORACLE_CONV_IN(tau)                                                        \
+    ((tau) >= bos ? x[(tau) * C + c]                                               \
+                  : (state_in ? state_in[((int64_t)n * R + ((tau) - bos + R)) * C + c] \
+                              : 0.0))
+            for (int64_t t = bos; t < eos; ++t) {
+                double acc = 0.0;
+                for (int j = 0; j < W; ++j) {
+                    acc += w[c * W + j] * ORACLE_CONV_IN(t - R + j);
+                }
+                y[t * C + c] = silu ? acc * oracle_sigmoid(acc) : acc;
+            }
+            if (state_out) {
+                for (int r = 0; r < R; ++r) {
+                    state_out[((int64_t)n * R + r) * C + c] = ORACLE_CONV_IN(eos - R + r);
+                }
+            }
+#undef ORACLE_CONV_IN
+        }
+    }
+    return 0;
+}

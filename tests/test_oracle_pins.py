@@ -391,3 +391,139 @@ def test_softplus_gate_chunked_equals_recurrent(oracle_mod):
     assert _close(o_c, o_r, 1e-10) and _close(S_c, S_r, 1e-10)
     o_k3, _, _ = oracle_mod.kda_reference(q, k, v, z, beta, A, S0, cu)
     assert not _close(o_k3, o_r, 1e-3)             # the two gates really differ
+
+
+# ------------------------------------------------ short convolution + state
+# Reading of the pages' "short convolutions" / "convolution state": a causal
+# depthwise convolution along time, y_t = sum_j w[:, j] x_{t-W+1+j}, whose
+# state is the last W-1 inputs (oldest first).
+
+@pytest.mark.parametrize("W", [1, 2, 3, 4])
+def test_short_conv_is_numpy_convolve(oracle_mod, W):
+    """With a zero state every channel is the textbook full convolution with
+    the reversed taps, truncated to the sequence (numpy.convolve)."""
+    rng = np.random.default_rng(60 + W)
+    T, C = 11, 5
+    x = rng.standard_normal((T, C))
+    w = rng.standard_normal((C, W))
+    y, s = oracle_mod.short_conv(x, w)
+    for c in range(C):
+        assert _close(y[:, c], np.convolve(x[:, c], w[c, ::-1])[:T], 1e-14)
+    # final state: the last W-1 inputs, oldest first
+    assert np.array_equal(s[0], x[T - (W - 1):] if W > 1 else np.zeros((0, C)))
+
+
+def test_short_conv_impulse_response(oracle_mod):
+    """A unit impulse at t0 in one channel gives the taps in reverse order
+    at t0, t0+1, ..., t0+W-1 and zero everywhere else."""
+    T, C, W, t0, c0 = 9, 3, 4, 2, 1
+    w = np.arange(1.0, 1.0 + C * W).reshape(C, W)
+    x = np.zeros((T, C))
+    x[t0, c0] = 1.0
+    y, _ = oracle_mod.short_conv(x, w)
+    want = np.zeros((T, C))
+    for m in range(W):
+        want[t0 + m, c0] = w[c0, W - 1 - m]
+    assert np.array_equal(y, want)
+
+
+@pytest.mark.parametrize("W", [2, 4])
+def test_short_conv_state_is_prepended_input(oracle_mod, W):
+    """A conv state acts as the W-1 inputs just before the sequence: running
+    with state s equals running on [s; x] from a zero state and dropping the
+    first W-1 outputs; the final state is the last W-1 rows of [s; x], also
+    for sequences shorter than W-1."""
+    rng = np.random.default_rng(70 + W)
+    C = 4
+    w = rng.standard_normal((C, W))
+    for T in (0, 1, W - 1, 7):
+        x = rng.standard_normal((T, C))
+        s = rng.standard_normal((1, W - 1, C))
+        y, s_out = oracle_mod.short_conv(x, w, state_in=s)
+        xx = np.concatenate([s[0], x])
+        yy, ss = oracle_mod.short_conv(xx, w)
+        assert y.shape == (T, C) and (T == 0 or _close(y, yy[W - 1:], 1e-14))
+        assert np.array_equal(s_out[0], xx[len(xx) - (W - 1):])
+        assert np.array_equal(s_out, ss)
+
+
+def test_short_conv_split_and_varlen(oracle_mod):
+    """Packed sequences are independent (varlen = separate calls), and a
+    sequence cut anywhere and resumed from the first part's conv state gives
+    the same outputs and final state as one pass (prefill then decode)."""
+    rng = np.random.default_rng(80)
+    C, W = 6, 4
+    w = rng.standard_normal((C, W))
+    lens = [9, 0, 2, 13]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    x = rng.standard_normal((cu[-1], C))
+    s0 = rng.standard_normal((len(lens), W - 1, C))
+    y, s = oracle_mod.short_conv(x, w, cu, s0, silu=True)
+    for n, L in enumerate(lens):
+        sl = slice(cu[n], cu[n + 1])
+        yn, sn = oracle_mod.short_conv(x[sl], w, None, s0[n:n + 1], silu=True)
+        assert np.array_equal(yn, y[sl]) and np.array_equal(sn[0], s[n])
+    x1 = x[cu[3]:cu[4]]
+    for cut in (0, 1, 2, 5, 13):
+        ya, sa = oracle_mod.short_conv(x1[:cut], w, None, s0[3:4])
+        parts = [ya]                 # the first part as one prefill
+        st = sa
+        for t in range(cut, 13):     # the rest one token at a time, as decode
+            yt, st = oracle_mod.short_conv(x1[t:t + 1], w, None, st)
+            parts.append(yt)
+        yf, sf = oracle_mod.short_conv(x1, w, None, s0[3:4])
+        assert _close(np.concatenate(parts), yf, 1e-14) and np.array_equal(st, sf)
+
+
+def test_short_conv_silu_closed_forms(oracle_mod):
+    """SiLU after the convolution: silu(0) = 0, silu(ln 3) = (3/4) ln 3,
+    silu(-ln 3) = -(1/4) ln 3, silu(40) = 40 to rounding."""
+    x = np.array([[1.0], [0.0], [0.0], [0.0]])
+    for val, want in ((0.0, 0.0), (math.log(3.0), 0.75 * math.log(3.0)),
+                      (-math.log(3.0), -0.25 * math.log(3.0)), (40.0, 40.0)):
+        w = np.array([[0.0, val]])           # y_t = val * x_t
+        y, _ = oracle_mod.short_conv(x, w, silu=True)
+        assert abs(y[0, 0] - want) <= 1e-15 * max(1.0, abs(want))
+        assert y[1, 0] == 0.0
+
+
+def test_short_conv_qkv_packing(oracle_mod):
+    """The per-head packed layouts (weights [H, 2dk+dv, W], state
+    [N, H, W-1, 2dk+dv], channels q | k | v) address the same channels as
+    convolving q, k and v one channel at a time."""
+    rng = np.random.default_rng(90)
+    T, H, dk, dv, W = 7, 2, 3, 2, 4
+    q, k, v = (rng.standard_normal((T, H, d)) for d in (dk, dk, dv))
+    cw = rng.standard_normal((H, 2 * dk + dv, W))
+    st = rng.standard_normal((1, H, W - 1, 2 * dk + dv))
+    qc, kc, vc, so = oracle_mod.short_conv_qkv(q, k, v, cw, None, st)
+    for h in range(H):
+        for name, xin, out, off, d in (("q", q, qc, 0, dk), ("k", k, kc, dk, dk),
+                                       ("v", v, vc, 2 * dk, dv)):
+            for c in range(d):
+                xs = np.concatenate([st[0, h, :, off + c], xin[:, h, c]])
+                want = np.convolve(xs, cw[h, off + c, ::-1])[W - 1:W - 1 + T]
+                assert _close(out[:, h, c], want, 1e-14), name
+                assert np.array_equal(so[0, h, :, off + c], xs[-(W - 1):])
+
+
+def test_conv_kda_prefill_equals_decode_steps(oracle_mod):
+    """Convolution + KDA over a sequence equals the same sequence fed one
+    token at a time with both states (recurrent and conv) carried between
+    steps: the decode loop with persistent states."""
+    rng = np.random.default_rng(95)
+    T, H, dk, dv, W = 6, 2, 4, 3, 4
+    q, k, v, z, beta, A, S0 = _rand_case(rng, T, H, dk, dv)
+    cw = 0.5 * rng.standard_normal((H, 2 * dk + dv, W))
+    cs0 = rng.standard_normal((1, H, W - 1, 2 * dk + dv))
+    o, S, cs = oracle_mod.kda_reference_conv(q, k, v, z, beta, A, cw, cs0, S0, silu=True)
+    St, ct = S0, cs0
+    for t in range(T):
+        sl = slice(t, t + 1)
+        ot, St, ct = oracle_mod.kda_reference_conv(q[sl], k[sl], v[sl], z[sl], beta[sl], A,
+                                                   cw, ct, St, silu=True)
+        assert _close(ot, o[sl], 1e-12)
+    assert _close(St, S, 1e-12) and np.array_equal(ct, cs)
+    # and the convolution really acts: without it the output differs
+    o_plain, _, _ = oracle_mod.kda_reference(q, k, v, z, beta, A, S0)
+    assert not _close(o_plain, o, 1e-3)
