@@ -286,7 +286,7 @@ def short_conv_qkv(q, k, v, conv_w, cu_seqlens=None, conv_state=None, silu: bool
         st = np.ascontiguousarray(st.transpose(0, 2, 1, 3).reshape(st.shape[0], W - 1, H * Cc))
     y, s_out = short_conv(x, w.reshape(H * Cc, W), cu_seqlens, st, silu)
     y = y.reshape(total_T, H, Cc)
-    s_out = s_out.reshape(-1, W - 1, H, Cc).transpose(0, 2, 1, 3)
+    s_out = s_out.reshape(s_out.shape[0], W - 1, H, Cc).transpose(0, 2, 1, 3)
     return (np.ascontiguousarray(y[..., :dk]), np.ascontiguousarray(y[..., dk:2 * dk]),
             np.ascontiguousarray(y[..., 2 * dk:]), np.ascontiguousarray(s_out))
 

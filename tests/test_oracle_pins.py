@@ -487,12 +487,13 @@ def test_short_conv_silu_closed_forms(oracle_mod):
         assert y[1, 0] == 0.0
 
 
-def test_short_conv_qkv_packing(oracle_mod):
+@pytest.mark.parametrize("W", [1, 4])
+def test_short_conv_qkv_packing(oracle_mod, W):
     """The per-head packed layouts (weights [H, 2dk+dv, W], state
     [N, H, W-1, 2dk+dv], channels q | k | v) address the same channels as
     convolving q, k and v one channel at a time."""
     rng = np.random.default_rng(90)
-    T, H, dk, dv, W = 7, 2, 3, 2, 4
+    T, H, dk, dv = 7, 2, 3, 2
     q, k, v = (rng.standard_normal((T, H, d)) for d in (dk, dk, dv))
     cw = rng.standard_normal((H, 2 * dk + dv, W))
     st = rng.standard_normal((1, H, W - 1, 2 * dk + dv))
@@ -504,7 +505,7 @@ def test_short_conv_qkv_packing(oracle_mod):
                 xs = np.concatenate([st[0, h, :, off + c], xin[:, h, c]])
                 want = np.convolve(xs, cw[h, off + c, ::-1])[W - 1:W - 1 + T]
                 assert _close(out[:, h, c], want, 1e-14), name
-                assert np.array_equal(so[0, h, :, off + c], xs[-(W - 1):])
+                assert np.array_equal(so[0, h, :, off + c], xs[len(xs) - (W - 1):])
 
 
 def test_conv_kda_prefill_equals_decode_steps(oracle_mod):
