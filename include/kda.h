@@ -67,13 +67,15 @@ enum {
     KDA_FLAG_RECURRENT = 2,    /* kda_prefill only: run the fused recurrent kernel
                                   (fp32 arithmetic, one token at a time) even where
                                   the chunked tensor-core kernel applies */
-    KDA_FLAG_SOFTPLUS_GATE = 4 /* Kimi Linear's unbounded gate g = -softplus(e^A z),
-                                  alpha = e^g = sigmoid(-e^A z), in place of
-                                  g = -5 sigmoid(e^A z) (the pages' section 1 names it
-                                  as the decay K3 replaced).  Its decay has no lower
-                                  bound, so the 16-token reciprocal tiles of the
-                                  chunked kernels do not apply: prefill runs the fused
-                                  recurrent kernel (fp32), decode is unchanged. */
+    KDA_FLAG_SOFTPLUS_GATE = 4, /* Kimi Linear's unbounded gate g = -softplus(e^A z),
+                                   alpha = e^g = sigmoid(-e^A z), in place of
+                                   g = -5 sigmoid(e^A z) (section 1 names it as the
+                                   decay K3 replaced).  Its decay has no lower bound,
+                                   so the 16-token reciprocal tiles of the chunked
+                                   kernels do not apply: prefill runs the fused
+                                   recurrent kernel (fp32), decode is unchanged. */
+    KDA_FLAG_CONV_SILU = 8      /* kda_short_conv, kda_decode_step_conv: SiLU,
+                                   y * sigmoid(y), after each short convolution */
 };
 #define KDA_DEFAULT_FLAGS KDA_FLAG_L2NORM_QK
 
@@ -204,6 +206,69 @@ KDA_API int kda_decode_step(const void* q, const void* k, const void* v, const v
                     int32_t B, int32_t H, int32_t d_k, int32_t d_v,
                     kda_dtype dt, float scale, uint32_t flags,
                     void* o, void* stream);
+
+/*
+ * kda_short_conv -- the short convolutions of q, k and v that precede the KDA
+ * step in prefill (section 1, prefill bullet: "short convolutions"; decode
+ * bullet: the convolution state kept persistent; section "Why 104B active
+ * still understates the systems problem": a fixed-size short-convolution
+ * state per request and layer).  The pages give no formula; the library reads
+ * it as a causal depthwise convolution along time of width W on every
+ * channel,
+ *     y_t[c] = sum_{j < W} w[c][j] * x_{t-W+1+j}[c],
+ * then y * sigmoid(y) when KDA_FLAG_CONV_SILU is set.  Inputs before a
+ * sequence's first token are rows of its conv state (zeros without one).
+ * Feed q_out, k_out, v_out to kda_prefill; hand conv_state_out to
+ * kda_decode_step_conv.
+ *
+ *  q, k            [total_T, H, d_k] dt;  v [total_T, H, d_v] dt
+ *  conv_w          [H, 2 d_k + d_v, W] fp32: per head the taps of the q
+ *                  channels, then k, then v; tap W-1 weights the current token
+ *  conv_state_in   [N, H, W-1, 2 d_k + d_v] dt, or NULL for zeros: row r is
+ *                  the input W-1-r tokens before the sequence's first one
+ *  conv_state_out  same shape, or NULL: the last W-1 inputs of each sequence
+ *                  (taken from conv_state_in where a sequence is shorter)
+ *  cu_seqlens      as kda_prefill (device [N + 1], or NULL for equal lengths)
+ *  W               1 .. 4;  flags: 0 or KDA_FLAG_CONV_SILU
+ *  q_out, k_out, v_out   the convolved tensors, layouts of q, k, v, rounded
+ *                  to dt (round to nearest even)
+ * Buffers are device memory owned by the caller, 16-byte aligned (conv_w:
+ * 4-byte).  Errors (nothing is launched): KDA_ERR_INVALID_ARG for a missing
+ * buffer, W outside 1 .. 4, an unknown flag, bad cu_seqlens_host, an output
+ * overlapping an input or another output, or conv_state_out overlapping
+ * conv_state_in; KDA_ERR_UNSUPPORTED / KDA_ERR_ALIGNMENT as kda_prefill.
+ */
+KDA_API int kda_short_conv(const void* q, const void* k, const void* v, const float* conv_w,
+                           const void* conv_state_in, void* conv_state_out,
+                           const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                           int32_t N, int32_t total_T, int32_t H, int32_t d_k, int32_t d_v,
+                           int32_t W, kda_dtype dt, uint32_t flags,
+                           void* q_out, void* k_out, void* v_out, void* stream);
+
+/*
+ * kda_decode_step_conv -- kda_decode_step with the short convolutions of q,
+ * k and v (as kda_short_conv, width W) fused in front of the state update:
+ * one launch reads each row's conv state, convolves the token's q, k, v in
+ * fp32 (no rounding to dt in between), runs the decode step on the result and
+ * shifts the conv state by the token (section 1, decode bullet: convolution
+ * state and recurrent state both kept persistent).
+ *
+ *  conv_w       [H, 2 d_k + d_v, W] fp32, as kda_short_conv
+ *  conv_state   [pool_size, H, W-1, 2 d_k + d_v] dt; row slots[b] (or b) is
+ *               read and rewritten in place; may be NULL when W == 1
+ *  W            1 .. 4
+ *  flags        KDA_FLAG_L2NORM_QK, KDA_FLAG_SOFTPLUS_GATE, KDA_FLAG_CONV_SILU
+ * Every other argument is that of kda_decode_step; a slot outside
+ * [0, pool_size) leaves both of its states untouched.  For d_v = 128 the two
+ * CTAs that share a head run as one thread-block cluster.
+ */
+KDA_API int kda_decode_step_conv(const void* q, const void* k, const void* v, const void* z,
+                                 const void* beta, const float* A, float* state,
+                                 const int32_t* slots, int32_t pool_size,
+                                 const float* conv_w, void* conv_state, int32_t W,
+                                 int32_t B, int32_t H, int32_t d_k, int32_t d_v,
+                                 kda_dtype dt, float scale, uint32_t flags,
+                                 void* o, void* stream);
 
 /*
  * kda_state_io -- moves fp32 states of shape [H, d_k, d_v] each (the

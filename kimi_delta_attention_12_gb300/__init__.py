@@ -36,6 +36,7 @@ KDA_BF16 = 1
 KDA_FLAG_L2NORM_QK = 1
 KDA_FLAG_RECURRENT = 2
 KDA_FLAG_SOFTPLUS_GATE = 4
+KDA_FLAG_CONV_SILU = 8
 
 KDA_STATE_ZERO = 0
 KDA_STATE_COPY = 1
@@ -47,6 +48,7 @@ EXPORTED_SYMBOLS = (
     "kda_prefill_workspace_bytes", "kda_prefill", "kda_workspace_status",
     "kda_decode_step", "kda_state_io", "kda_status_string", "kda_version",
     "kda_prefill_noalloc", "kda_prefill_checkpointed", "kda_checkpoint_count",
+    "kda_short_conv", "kda_decode_step_conv",
 )
 
 _lock = threading.Lock()
@@ -96,6 +98,14 @@ def lib() -> ctypes.CDLL:
             L.kda_prefill_checkpointed.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                                    i32, i32, i32, i32, i32, ctypes.c_int, f32,
                                                    u32, vp, vp, i32, vp, vp, i32, vp, sz, vp]
+            L.kda_short_conv.restype = ctypes.c_int
+            L.kda_short_conv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                         i32, i32, ctypes.c_int, ctypes.c_uint32, vp, vp, vp,
+                                         vp]
+            L.kda_decode_step_conv.restype = ctypes.c_int
+            L.kda_decode_step_conv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i32,
+                                               i32, i32, i32, i32, ctypes.c_int,
+                                               ctypes.c_float, ctypes.c_uint32, vp, vp]
             L.kda_checkpoint_count.restype = ctypes.c_int64
             L.kda_checkpoint_count.argtypes = [vp, i32, i32, i32]
             _lib = L
@@ -267,6 +277,90 @@ def kda_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: torch.
         _stream_ptr(stream))
     if st != KDA_OK:
         raise KDAError(st, "kda_decode_step")
+    return o
+
+
+def kda_short_conv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, conv_w: torch.Tensor,
+                   conv_state_in: Optional[torch.Tensor] = None,
+                   conv_state_out: Optional[torch.Tensor] = None,
+                   cu_seqlens: Optional[torch.Tensor] = None,
+                   cu_seqlens_host: Optional[torch.Tensor] = None, silu: bool = False,
+                   outputs: Optional[Tuple[torch.Tensor, torch.Tensor, torch.Tensor]] = None,
+                   stream: Optional[torch.cuda.Stream] = None
+                   ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """Short convolutions of q, k [total_T, H, d_k] and v [total_T, H, d_v]
+    (a 4-D [B, T, H, d] batch is taken as B sequences of length T).
+    conv_w [H, 2 d_k + d_v, W] fp32; conv states [N, H, W-1, 2 d_k + d_v] in
+    the dtype of q.  Returns the convolved (q, k, v); the final conv states go
+    to conv_state_out when given (kda_short_conv in include/kda.h)."""
+    batched = q.dim() == 4
+    if batched:
+        B, T = q.shape[:2]
+        q, k, v = (t.reshape(B * T, *t.shape[2:]) for t in (q, k, v))
+        N = B
+    else:
+        N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    total_T, H, d_k = q.shape
+    d_v = v.shape[-1]
+    dt = q.dtype
+    if k.dtype != dt or v.dtype != dt:
+        raise TypeError("q, k and v must share one dtype")
+    _check_cuda(q, k, v, conv_w, conv_state_in, conv_state_out, cu_seqlens)
+    if conv_w.dtype != torch.float32 or conv_w.dim() != 3:
+        raise TypeError("conv_w must be a float32 [H, 2 d_k + d_v, W] tensor")
+    for st_ in (conv_state_in, conv_state_out):
+        if st_ is not None and st_.dtype != dt:
+            raise TypeError("conv states must have the dtype of q")
+    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    if outputs is None:
+        outputs = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+    qo, ko, vo = outputs
+    host_cu = None if cu_seqlens_host is None else cu_seqlens_host.to(torch.int32).contiguous()
+    host_ptr = None if host_cu is None else ctypes.c_void_p(host_cu.data_ptr())
+    st = lib().kda_short_conv(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(conv_w), _ptr(conv_state_in), _ptr(conv_state_out),
+        _ptr(cu_seqlens), host_ptr, N, total_T, H, d_k, d_v, conv_w.shape[-1], _dtype_code(dt),
+        KDA_FLAG_CONV_SILU if silu else 0, _ptr(qo), _ptr(ko), _ptr(vo), _stream_ptr(stream))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_short_conv")
+    if batched:
+        qo, ko, vo = (t.reshape(B, T, *t.shape[1:]) for t in (qo, ko, vo))
+    return qo, ko, vo
+
+
+def kda_decode_step_conv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: torch.Tensor,
+                         beta: torch.Tensor, A: torch.Tensor, state: torch.Tensor,
+                         conv_w: torch.Tensor, conv_state: Optional[torch.Tensor],
+                         slots: Optional[torch.Tensor] = None, scale: float = 1.0,
+                         l2norm: bool = True, silu: bool = False, softplus_gate: bool = False,
+                         o: Optional[torch.Tensor] = None,
+                         stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """kda_decode_step with the short convolutions of q, k, v fused in front:
+    conv_state [pool, H, W-1, 2 d_k + d_v] (dtype of q) is read and shifted in
+    place at rows `slots`, like `state`.  Returns o [B, H, d_v]."""
+    B, H, d_k = q.shape
+    d_v = v.shape[-1]
+    dt = q.dtype
+    _check_cuda(q, k, v, z, beta, A, state, conv_w, conv_state, slots)
+    if state.dtype != torch.float32:
+        raise TypeError("state must be float32")
+    if conv_w.dtype != torch.float32 or conv_w.dim() != 3:
+        raise TypeError("conv_w must be a float32 [H, 2 d_k + d_v, W] tensor")
+    if conv_state is not None and conv_state.dtype != dt:
+        raise TypeError("conv_state must have the dtype of q")
+    if slots is not None and slots.dtype != torch.int32:
+        raise TypeError("slots must be int32")
+    if o is None:
+        o = torch.empty(B, H, d_v, dtype=dt, device=q.device)
+    flags = ((KDA_FLAG_L2NORM_QK if l2norm else 0) | (KDA_FLAG_SOFTPLUS_GATE if softplus_gate else 0)
+             | (KDA_FLAG_CONV_SILU if silu else 0))
+    st = lib().kda_decode_step_conv(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(state), _ptr(slots),
+        state.shape[0], _ptr(conv_w), _ptr(conv_state), conv_w.shape[-1], B, H, d_k, d_v,
+        _dtype_code(dt), float(scale), flags, _ptr(o), _stream_ptr(stream))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_decode_step_conv")
     return o
 
 

@@ -29,6 +29,15 @@ constexpr size_t kWsHeader = 256;
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Whether the byte ranges [a, a + na) and [b, b + nb) share a byte.
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+constexpr int32_t kMaxConvWidth = 4;
+
 // Minimum workspace: the header and one int per (sequence, head) unit.
 size_t basic_workspace_bytes(int32_t N, int32_t H) {
     const size_t units = (N > 0 && H > 0) ? (size_t)N * (size_t)H : 0;
@@ -222,21 +231,86 @@ int kda_prefill_checkpointed(const void* q, const void* k, const void* v, const 
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
-int kda_decode_step(const void* q, const void* k, const void* v, const void* z,
-                    const void* beta, const float* A, float* state,
-                    const int32_t* slots, int32_t pool_size,
-                    int32_t B, int32_t H, int32_t d_k, int32_t d_v,
-                    kda_dtype dt, float scale, uint32_t flags,
-                    void* o, void* stream) {
+int kda_short_conv(const void* q, const void* k, const void* v, const float* conv_w,
+                   const void* conv_state_in, void* conv_state_out,
+                   const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                   int32_t N, int32_t total_T, int32_t H, int32_t d_k, int32_t d_v,
+                   int32_t W, kda_dtype dt, uint32_t flags,
+                   void* q_out, void* k_out, void* v_out, void* stream) {
+    if (dt != KDA_F32 && dt != KDA_BF16) return KDA_ERR_UNSUPPORTED;
+    if (!supported_dim(d_k) || !supported_dim(d_v)) return KDA_ERR_UNSUPPORTED;
+    if (N < 1 || H < 1 || total_T < 0) return KDA_ERR_INVALID_ARG;
+    if (W < 1 || W > kMaxConvWidth) return KDA_ERR_INVALID_ARG;
+    if ((flags & ~(uint32_t)KDA_FLAG_CONV_SILU) != 0) return KDA_ERR_INVALID_ARG;
+    if (!conv_w) return KDA_ERR_INVALID_ARG;
+    if (total_T > 0 && (!q || !k || !v || !q_out || !k_out || !v_out)) {
+        return KDA_ERR_INVALID_ARG;
+    }
+    if (!cu_seqlens && total_T % N != 0) return KDA_ERR_INVALID_ARG;
+    if (cu_seqlens_host) {
+        if (cu_seqlens_host[0] != 0 || cu_seqlens_host[N] != total_T) return KDA_ERR_INVALID_ARG;
+        for (int32_t n = 0; n < N; ++n) {
+            if (cu_seqlens_host[n + 1] < cu_seqlens_host[n]) return KDA_ERR_INVALID_ARG;
+        }
+    }
+    const size_t eb = elem_bytes(dt);
+    const size_t nqk = (size_t)total_T * H * d_k * eb, nv = (size_t)total_T * H * d_v * eb;
+    const size_t nst = (size_t)N * H * (W - 1) * (2 * d_k + d_v) * eb;
+    const void* ins[3] = {q, k, v};
+    const void* outs[3] = {q_out, k_out, v_out};
+    const size_t sz[3] = {nqk, nqk, nv};
+    for (int i = 0; i < 3; ++i) {
+        for (int j = 0; j < 3; ++j) {
+            if (overlaps(outs[i], sz[i], ins[j], sz[j])) return KDA_ERR_INVALID_ARG;
+            if (j != i && overlaps(outs[i], sz[i], outs[j], sz[j])) return KDA_ERR_INVALID_ARG;
+        }
+        if (overlaps(outs[i], sz[i], conv_state_out, nst) ||
+            overlaps(outs[i], sz[i], conv_state_in, nst)) {
+            return KDA_ERR_INVALID_ARG;
+        }
+    }
+    if (overlaps(conv_state_in, nst, conv_state_out, nst)) return KDA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(q_out, 16) ||
+        !aligned(k_out, 16) || !aligned(v_out, 16) || !aligned(conv_w, 4) ||
+        !aligned(conv_state_in, 16) || !aligned(conv_state_out, 16) ||
+        !aligned(cu_seqlens, 4)) {
+        return KDA_ERR_ALIGNMENT;
+    }
+    kda::ShortConvParams p;
+    memset(&p, 0, sizeof(p));
+    p.x[0] = q; p.x[1] = k; p.x[2] = v;
+    p.y[0] = q_out; p.y[1] = k_out; p.y[2] = v_out;
+    p.w = conv_w;
+    p.state_in = W > 1 ? conv_state_in : nullptr;
+    p.state_out = W > 1 ? conv_state_out : nullptr;
+    p.cu_seqlens = cu_seqlens;
+    p.N = N; p.total_T = total_T; p.H = H; p.d_k = d_k; p.d_v = d_v; p.W = W;
+    p.silu = (flags & KDA_FLAG_CONV_SILU) ? 1 : 0;
+    const cudaError_t err = kda::launch_short_conv(p, dt == KDA_F32 ? 0 : 1,
+                                                   static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+// kda_decode_step and kda_decode_step_conv (W = 0: no convolution)
+static int decode_step_impl(const void* q, const void* k, const void* v, const void* z,
+                     const void* beta, const float* A, float* state,
+                     const int32_t* slots, int32_t pool_size, const float* conv_w,
+                     void* conv_state, int32_t W, int32_t B, int32_t H, int32_t d_k,
+                     int32_t d_v, kda_dtype dt, float scale, uint32_t flags, void* o,
+                     void* stream) {
     if (dt != KDA_F32 && dt != KDA_BF16) return KDA_ERR_UNSUPPORTED;
     if (!supported_dim(d_k) || !supported_dim(d_v)) return KDA_ERR_UNSUPPORTED;
     if (B < 0 || H < 1 || pool_size < 0) return KDA_ERR_INVALID_ARG;
-    if ((flags & ~(uint32_t)(KDA_FLAG_L2NORM_QK | KDA_FLAG_SOFTPLUS_GATE)) != 0) {
-        return KDA_ERR_INVALID_ARG;
-    }
+    const uint32_t known = KDA_FLAG_L2NORM_QK | KDA_FLAG_SOFTPLUS_GATE |
+                           (W > 0 ? (uint32_t)KDA_FLAG_CONV_SILU : 0u);
+    if ((flags & ~known) != 0) return KDA_ERR_INVALID_ARG;
+    if (W < 0 || W > kMaxConvWidth) return KDA_ERR_INVALID_ARG;
+    if (W > 0 && (!conv_w || (W > 1 && !conv_state))) return KDA_ERR_INVALID_ARG;
     if (!isfinite(scale)) return KDA_ERR_INVALID_ARG;
     if (B == 0) return KDA_OK;
     if (!q || !k || !v || !z || !beta || !A || !state || !o) return KDA_ERR_INVALID_ARG;
+    if (W > 0 && !aligned(conv_w, 4)) return KDA_ERR_ALIGNMENT;
+    if (W > 1 && !aligned(conv_state, elem_bytes(dt))) return KDA_ERR_ALIGNMENT;
     if (!slots && pool_size < B) return KDA_ERR_INVALID_ARG;
     const size_t eb = elem_bytes(dt);
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(z, 16) ||
@@ -251,9 +325,35 @@ int kda_decode_step(const void* q, const void* k, const void* v, const void* z,
     p.o = o; p.rows = B; p.total_T = B; p.H = H; p.pool_size = pool_size;
     p.scale = scale; p.l2norm = (flags & KDA_FLAG_L2NORM_QK) ? 1 : 0; p.decode = 1;
     p.softplus_gate = (flags & KDA_FLAG_SOFTPLUS_GATE) ? 1 : 0;
+    p.conv_width = W;
+    p.conv_silu = (flags & KDA_FLAG_CONV_SILU) ? 1 : 0;
+    p.conv_w = conv_w;
+    p.conv_state = conv_state;
     const cudaError_t err = kda::launch_recurrent(p, d_k, d_v, dt == KDA_F32 ? 0 : 1,
                                                   static_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_decode_step(const void* q, const void* k, const void* v, const void* z,
+                    const void* beta, const float* A, float* state,
+                    const int32_t* slots, int32_t pool_size,
+                    int32_t B, int32_t H, int32_t d_k, int32_t d_v,
+                    kda_dtype dt, float scale, uint32_t flags,
+                    void* o, void* stream) {
+    return decode_step_impl(q, k, v, z, beta, A, state, slots, pool_size, nullptr, nullptr, 0,
+                            B, H, d_k, d_v, dt, scale, flags, o, stream);
+}
+
+int kda_decode_step_conv(const void* q, const void* k, const void* v, const void* z,
+                         const void* beta, const float* A, float* state,
+                         const int32_t* slots, int32_t pool_size,
+                         const float* conv_w, void* conv_state, int32_t W,
+                         int32_t B, int32_t H, int32_t d_k, int32_t d_v,
+                         kda_dtype dt, float scale, uint32_t flags,
+                         void* o, void* stream) {
+    if (W < 1) return KDA_ERR_INVALID_ARG;
+    return decode_step_impl(q, k, v, z, beta, A, state, slots, pool_size, conv_w, conv_state, W,
+                            B, H, d_k, d_v, dt, scale, flags, o, stream);
 }
 
 int kda_state_io(kda_state_op op, float* dst, const float* src,

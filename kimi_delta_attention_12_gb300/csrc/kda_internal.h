@@ -39,7 +39,34 @@ struct RecurrentParams {
     float* ckpt_pool;
     const int32_t* ckpt_slots;
     int32_t ckpt_pool_size;
+    // decode only: short convolutions of q, k, v fused in front of the step
+    // (conv_width 0 = none); conv_state [pool_size, H, W-1, 2 d_k + d_v] in
+    // the input dtype, read and rewritten in place at the row's slot
+    int32_t conv_width;
+    int32_t conv_silu;
+    const float* conv_w;         // [H, 2 d_k + d_v, W] fp32
+    void* conv_state;
 };
+
+// Short convolutions of q, k and v (kda_short_conv.cu).  Conv weights and
+// states use the per-head packed channel order q | k | v (Cc = 2 d_k + d_v):
+// w [H, Cc, W] fp32, states [N, H, W-1, Cc] in the input dtype.
+struct ShortConvParams {
+    const void* x[3];            // q, k [total_T, H, d_k]; v [total_T, H, d_v]
+    void* y[3];                  // convolved q, k, v, same layouts
+    const float* w;
+    const void* state_in;        // or null (zeros)
+    void* state_out;             // or null
+    const int32_t* cu_seqlens;   // device [N + 1], or null for equal lengths
+    int32_t N;
+    int32_t total_T;
+    int32_t H;
+    int32_t d_k;
+    int32_t d_v;
+    int32_t W;                   // 1 .. 4
+    int32_t silu;
+};
+cudaError_t launch_short_conv(const ShortConvParams& p, int dtype, cudaStream_t stream);
 
 // Launches the recurrent kernel for (d_k, d_v) in {32, 64, 128}^2 and
 // dtype (0 = fp32, 1 = bf16).  Returns a cudaError_t.

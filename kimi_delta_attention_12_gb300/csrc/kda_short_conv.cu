@@ -1,0 +1,309 @@
+// kda_short_conv.cu -- the short convolutions of q, k and v for prefill.
+//
+// "Kimi K3 Open Weights: What Is Actually New In Its 2.8 Trillion Parameter
+// Architecture", section 1, lists short convolutions first among the KDA
+// prefill steps and keeps a convolution state persistent through decode.
+// The operation (the pages give no formula; this is the plain reading): a
+// causal depthwise convolution along time of width W on every channel,
+//     y_t[c] = sum_{j<W} w[c][j] * x_{t-W+1+j}[c],   optionally y * sigmoid(y),
+// where inputs before a sequence's first token are the rows of its conv state
+// (the W-1 inputs that preceded it, oldest first) and the final conv state is
+// the last W-1 inputs of the sequence.
+//
+// Memory-bound: every input element is read once from HBM (plus W-1 halo rows
+// per block of tokens, from L2) and every output written once.  A thread owns
+// one 16-byte vector of channels of one tensor (8 bf16 or 4 fp32 channels) for
+// a block of TB consecutive tokens and slides a window of the last W-1 rows
+// through registers.  Consecutive threads own consecutive vectors of the same
+// token row, so a warp reads and writes 512 contiguous bytes per token.
+// Loads are issued eight rows ahead of their use.
+//
+// Grid: x = token blocks, then one block per sequence that writes that
+// sequence's final conv state; y = groups of 256 channel vectors.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+constexpr int kConvThreads = 256;
+constexpr int kConvTB = 32;     // tokens per block
+constexpr int kConvAhead = 8;   // rows loaded ahead
+
+template <typename T>
+struct VecTraits;
+template <>
+struct VecTraits<float> {
+    static constexpr int kN = 4;
+    __device__ static void unpack(const uint4& r, float* f) {
+        f[0] = __uint_as_float(r.x); f[1] = __uint_as_float(r.y);
+        f[2] = __uint_as_float(r.z); f[3] = __uint_as_float(r.w);
+    }
+    __device__ static uint4 pack(const float* f) {
+        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
+                          __float_as_uint(f[2]), __float_as_uint(f[3]));
+    }
+};
+template <>
+struct VecTraits<__nv_bfloat16> {
+    static constexpr int kN = 8;
+    __device__ static void unpack(const uint4& r, float* f) {
+        const uint32_t u[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(u[i] << 16);
+            f[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+        }
+    }
+    __device__ static uint4 pack(const float* f) {
+        uint32_t u[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 b = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+            u[i] = *reinterpret_cast<const uint32_t*>(&b);
+        }
+        return make_uint4(u[0], u[1], u[2], u[3]);
+    }
+};
+
+__device__ __forceinline__ float silu_f(float y) {
+    // y * sigmoid(y) on the branch that cannot overflow
+    if (y >= 0.0f) {
+        return y / (1.0f + expf(-y));
+    }
+    const float e = expf(y);
+    return y * e / (1.0f + e);
+}
+
+__device__ __forceinline__ uint4 ld16(const void* base, size_t elem_off, int eb) {
+    return __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(base) +
+                                                elem_off * eb));
+}
+
+// Which tensor, head and channel a channel vector is.
+struct ChanVec {
+    int tensor;      // 0 q, 1 k, 2 v
+    int h;
+    int c0;          // first channel within the tensor's head
+    int d;           // head dim of the tensor
+    int off;         // first channel within the head's packed q | k | v channels
+};
+
+template <int VEC>
+__device__ __forceinline__ bool chan_vec(const ShortConvParams& p, int gv, ChanVec* cv) {
+    const int vq = p.H * p.d_k / VEC;
+    const int vv = p.H * p.d_v / VEC;
+    int lin = gv;
+    if (lin < vq) {
+        cv->tensor = 0; cv->d = p.d_k;
+    } else if (lin < 2 * vq) {
+        lin -= vq; cv->tensor = 1; cv->d = p.d_k;
+    } else if (lin < 2 * vq + vv) {
+        lin -= 2 * vq; cv->tensor = 2; cv->d = p.d_v;
+    } else {
+        return false;
+    }
+    const int per_head = cv->d / VEC;
+    cv->h = lin / per_head;
+    cv->c0 = (lin % per_head) * VEC;
+    cv->off = (cv->tensor == 0 ? 0 : cv->tensor == 1 ? p.d_k : 2 * p.d_k) + cv->c0;
+    return true;
+}
+
+__device__ __forceinline__ void seq_bounds(const ShortConvParams& p, int n, int64_t* bos,
+                                           int64_t* eos) {
+    if (p.cu_seqlens) {
+        *bos = p.cu_seqlens[n];
+        *eos = p.cu_seqlens[n + 1];
+    } else {
+        const int64_t len = p.total_T / p.N;
+        *bos = (int64_t)n * len;
+        *eos = *bos + len;
+    }
+}
+
+// The sequence that holds token t (t < total_T): the last n with start <= t.
+__device__ __forceinline__ int seq_of(const ShortConvParams& p, int64_t t) {
+    if (!p.cu_seqlens) {
+        return (int)(t / (p.total_T / p.N));
+    }
+    int lo = 0, hi = p.N - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.cu_seqlens[mid] <= t) {
+            lo = mid;
+        } else {
+            hi = mid - 1;
+        }
+    }
+    return lo;
+}
+
+template <typename T, int W>
+__global__ void __launch_bounds__(kConvThreads)
+short_conv_kernel(const ShortConvParams p, int n_token_blocks) {
+    using VT = VecTraits<T>;
+    constexpr int VEC = VT::kN;
+    constexpr int R = W - 1;
+    constexpr int EB = sizeof(T);
+
+    ChanVec cv;
+    if (!chan_vec<VEC>(p, blockIdx.y * kConvThreads + threadIdx.x, &cv)) {
+        return;
+    }
+    const int Cc = 2 * p.d_k + p.d_v;
+    // (selected, not indexed: a dynamic index into the parameter block would
+    // copy it to local memory)
+    const void* x = cv.tensor == 0 ? p.x[0] : cv.tensor == 1 ? p.x[1] : p.x[2];
+    const int H = p.H;
+    // element offset of (token t, this vector) in x / y
+    auto xoff = [=](int64_t t) { return ((size_t)t * H + cv.h) * cv.d + cv.c0; };
+    // element offset of (sequence n, row r, this vector) in a conv state
+    auto soff = [=](int n, int r) { return (((size_t)n * H + cv.h) * R + r) * Cc + cv.off; };
+
+    if ((int)blockIdx.x >= n_token_blocks) {
+        // final conv state of sequence n: its last W-1 inputs, oldest first
+        const int n = blockIdx.x - n_token_blocks;
+        if (R == 0 || !p.state_out) {
+            return;
+        }
+        int64_t bos, eos;
+        seq_bounds(p, n, &bos, &eos);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int64_t tau = eos - R + r;
+            uint4 val = make_uint4(0u, 0u, 0u, 0u);
+            if (tau >= bos) {
+                val = ld16(x, xoff(tau), EB);
+            } else if (p.state_in) {
+                val = ld16(p.state_in, soff(n, (int)(tau - bos + R)), EB);
+            }
+            *reinterpret_cast<uint4*>(static_cast<char*>(p.state_out) + soff(n, r) * EB) = val;
+        }
+        return;
+    }
+
+    const int64_t t0 = (int64_t)blockIdx.x * kConvTB;
+    const int64_t t1 = min((int64_t)p.total_T, t0 + kConvTB);
+
+    // taps of this vector's channels: w[h][off + i][j]
+    float wt[W][VEC];
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+        const float* wr = p.w + ((size_t)cv.h * Cc + cv.off + i) * W;
+#pragma unroll
+        for (int j = 0; j < W; ++j) {
+            wt[j][i] = __ldg(wr + j);
+        }
+    }
+
+    int n = seq_of(p, t0);
+    int64_t bos, eos;
+    seq_bounds(p, n, &bos, &eos);
+    float win[R > 0 ? R : 1][VEC];   // inputs t-R .. t-1
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int64_t tau = t0 - R + r;
+        uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+        if (tau >= bos) {
+            raw = ld16(x, xoff(tau), EB);
+        } else if (p.state_in) {
+            raw = ld16(p.state_in, soff(n, (int)(tau - bos + R)), EB);
+        }
+        VT::unpack(raw, win[r]);
+    }
+
+    void* y = cv.tensor == 0 ? p.y[0] : cv.tensor == 1 ? p.y[1] : p.y[2];
+    for (int64_t tb = t0; tb < t1; tb += kConvAhead) {
+        uint4 raw[kConvAhead];
+#pragma unroll
+        for (int i = 0; i < kConvAhead; ++i) {
+            if (tb + i < t1) {
+                raw[i] = ld16(x, xoff(tb + i), EB);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kConvAhead; ++i) {
+            const int64_t t = tb + i;
+            if (t >= t1) {
+                continue;
+            }
+            if (t >= eos) {
+                // first token of a later sequence (skipping empty ones): the
+                // window restarts from that sequence's conv state
+                do {
+                    ++n;
+                    seq_bounds(p, n, &bos, &eos);
+                } while (t >= eos);
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    uint4 s = make_uint4(0u, 0u, 0u, 0u);
+                    if (p.state_in) {
+                        s = ld16(p.state_in, soff(n, r), EB);
+                    }
+                    VT::unpack(s, win[r]);
+                }
+            }
+            float cur[VEC], out[VEC];
+            VT::unpack(raw[i], cur);
+#pragma unroll
+            for (int c = 0; c < VEC; ++c) {
+                float acc = 0.0f;
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    acc = fmaf(wt[r][c], win[r][c], acc);
+                }
+                acc = fmaf(wt[R][c], cur[c], acc);
+                out[c] = p.silu ? silu_f(acc) : acc;
+            }
+            *reinterpret_cast<uint4*>(static_cast<char*>(y) + xoff(t) * EB) = VT::pack(out);
+#pragma unroll
+            for (int r = 0; r + 1 < R; ++r) {
+#pragma unroll
+                for (int c = 0; c < VEC; ++c) {
+                    win[r][c] = win[r + 1][c];
+                }
+            }
+            if (R > 0) {
+#pragma unroll
+                for (int c = 0; c < VEC; ++c) {
+                    win[R > 0 ? R - 1 : 0][c] = cur[c];
+                }
+            }
+        }
+    }
+}
+
+template <typename T>
+cudaError_t launch_typed(const ShortConvParams& p, cudaStream_t stream) {
+    constexpr int VEC = VecTraits<T>::kN;
+    const int64_t vecs = (int64_t)p.H * (2 * p.d_k + p.d_v) / VEC;
+    const int64_t ntb = ((int64_t)p.total_T + kConvTB - 1) / kConvTB;
+    const int64_t gx = ntb + (p.state_out ? p.N : 0);
+    if (gx == 0 || vecs == 0) {
+        return cudaSuccess;
+    }
+    if (gx > 0x7fffffffLL) {
+        return cudaErrorInvalidValue;
+    }
+    const dim3 grid((unsigned)gx, (unsigned)((vecs + kConvThreads - 1) / kConvThreads));
+    switch (p.W) {
+        case 1: short_conv_kernel<T, 1><<<grid, kConvThreads, 0, stream>>>(p, (int)ntb); break;
+        case 2: short_conv_kernel<T, 2><<<grid, kConvThreads, 0, stream>>>(p, (int)ntb); break;
+        case 3: short_conv_kernel<T, 3><<<grid, kConvThreads, 0, stream>>>(p, (int)ntb); break;
+        case 4: short_conv_kernel<T, 4><<<grid, kConvThreads, 0, stream>>>(p, (int)ntb); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_short_conv(const ShortConvParams& p, int dtype, cudaStream_t stream) {
+    return dtype == 0 ? launch_typed<float>(p, stream) : launch_typed<__nv_bfloat16>(p, stream);
+}
+
+}  // namespace kda

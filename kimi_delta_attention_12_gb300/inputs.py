@@ -155,5 +155,22 @@ def make_decode_step(B: int, H: int, d_k: int, d_v: int, dtype: torch.dtype,
     return DecodeStepInputs(q, k, v, z, beta)
 
 
+def make_conv_params(N: int, H: int, d_k: int, d_v: int, W: int, dtype: torch.dtype,
+                     seed: int = 0, with_state: bool = True):
+    """Short-convolution weights [H, 2 d_k + d_v, W] fp32 ~ N(0, 0.5) and a
+    conv state [N, H, W-1, 2 d_k + d_v] in `dtype` (or None): N(0, 1) draws,
+    the q and k channels scaled by 1 / sqrt(d_k) to the size of unit-norm
+    rows.  Drawn in that order from generator(seed + 7)."""
+    g = torch.Generator().manual_seed(seed + 7)
+    Cc = 2 * d_k + d_v
+    w = (0.5 * torch.randn(H, Cc, W, generator=g)).float()
+    state = None
+    if with_state:
+        state = torch.randn(N, H, W - 1, Cc, generator=g)
+        state[..., :2 * d_k] *= d_k ** -0.5
+        state = state.to(dtype)
+    return w, state
+
+
 def list_workloads() -> List[str]:
     return list(WORKLOADS) + [DECODE_256.name]

@@ -215,3 +215,77 @@ def test_checkpoint_validation(L, interval, pool, slots, pool_size, expect):
 def test_checkpoint_zero_interval_is_plain_prefill_validation(L):
     # interval 0 takes the plain path: the other arguments are validated as usual
     assert _call_ckpt(L, 0, None, None, 0, dk=48) == kda.KDA_ERR_UNSUPPORTED
+
+
+def _call_conv(L, **over):
+    # q, k, v, outputs and states far apart; T=64, H=2, d=32 (bf16): 8 KB each
+    a = dict(q=BASE, k=BASE + 0x100000, v=BASE + 0x200000, w=BASE + 0x300000,
+             s_in=BASE + 0x400000, s_out=BASE + 0x500000, cu=None, cu_host=None, N=1, T=64,
+             H=2, dk=32, dv=32, W=4, dt=kda.KDA_BF16, flags=0, qo=BASE + 0x600000,
+             ko=BASE + 0x700000, vo=BASE + 0x800000)
+    a.update(over)
+    vp = ctypes.c_void_p
+    return L.kda_short_conv(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["w"]), vp(a["s_in"]),
+                            vp(a["s_out"]), vp(a["cu"]), a["cu_host"], a["N"], a["T"], a["H"],
+                            a["dk"], a["dv"], a["W"], a["dt"], a["flags"], vp(a["qo"]),
+                            vp(a["ko"]), vp(a["vo"]), None)
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(dk=48), kda.KDA_ERR_UNSUPPORTED),
+    (dict(dt=5), kda.KDA_ERR_UNSUPPORTED),
+    (dict(W=0), kda.KDA_ERR_INVALID_ARG),
+    (dict(W=5), kda.KDA_ERR_INVALID_ARG),
+    (dict(flags=1), kda.KDA_ERR_INVALID_ARG),          # only KDA_FLAG_CONV_SILU applies
+    (dict(N=0), kda.KDA_ERR_INVALID_ARG),
+    (dict(T=-1), kda.KDA_ERR_INVALID_ARG),
+    (dict(w=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(vo=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(N=3), kda.KDA_ERR_INVALID_ARG),              # 64 % 3 without cu_seqlens
+    (dict(qo=BASE), kda.KDA_ERR_INVALID_ARG),          # output on top of its input
+    (dict(ko=BASE + 0x201000), kda.KDA_ERR_INVALID_ARG),   # output inside v
+    (dict(vo=BASE + 0x601000), kda.KDA_ERR_INVALID_ARG),   # two outputs overlap
+    (dict(s_out=BASE + 0x400100), kda.KDA_ERR_INVALID_ARG),  # state out overlaps state in
+    (dict(s_out=BASE + 0x800100), kda.KDA_ERR_INVALID_ARG),  # state out overlaps an output
+    (dict(q=BASE + 8), kda.KDA_ERR_ALIGNMENT),
+    (dict(s_in=BASE + 0x400008), kda.KDA_ERR_ALIGNMENT),
+    (dict(w=BASE + 0x300002), kda.KDA_ERR_ALIGNMENT),
+])
+def test_short_conv_validation(L, over, expect):
+    assert _call_conv(L, **over) == expect
+
+
+def test_short_conv_host_cu_seqlens_validation(L):
+    arr = (ctypes.c_int32 * 3)(0, 70, 64)
+    assert _call_conv(L, N=2, cu=BASE + 0x900000, cu_host=arr) == kda.KDA_ERR_INVALID_ARG
+
+
+def _call_decode_conv(L, **over):
+    a = dict(q=BASE, k=BASE + 0x100000, v=BASE + 0x200000, z=BASE + 0x300000,
+             beta=BASE + 0x400000, A=BASE + 0x500000, state=BASE + 0x600000, slots=None,
+             pool=4, w=BASE + 0x800000, cs=BASE + 0x900000, W=4, B=4, H=2, dk=128, dv=128,
+             dt=kda.KDA_BF16, scale=1.0, flags=1, o=BASE + 0x700000)
+    a.update(over)
+    vp = ctypes.c_void_p
+    return L.kda_decode_step_conv(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["z"]),
+                                  vp(a["beta"]), vp(a["A"]), vp(a["state"]), vp(a["slots"]),
+                                  a["pool"], vp(a["w"]), vp(a["cs"]), a["W"], a["B"], a["H"],
+                                  a["dk"], a["dv"], a["dt"], a["scale"], a["flags"], vp(a["o"]),
+                                  None)
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(W=0), kda.KDA_ERR_INVALID_ARG),
+    (dict(W=5), kda.KDA_ERR_INVALID_ARG),
+    (dict(w=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(cs=None), kda.KDA_ERR_INVALID_ARG),          # W > 1 needs a conv state
+    (dict(flags=2), kda.KDA_ERR_INVALID_ARG),          # the recurrent flag is prefill-only
+    (dict(flags=16), kda.KDA_ERR_INVALID_ARG),
+    (dict(dk=16), kda.KDA_ERR_UNSUPPORTED),
+    (dict(pool=2), kda.KDA_ERR_INVALID_ARG),
+    (dict(w=BASE + 0x800002), kda.KDA_ERR_ALIGNMENT),
+    (dict(cs=BASE + 0x900001), kda.KDA_ERR_ALIGNMENT),
+    (dict(B=0, flags=1 | 4 | 8), kda.KDA_OK),          # nothing to do, nothing launched
+])
+def test_decode_conv_validation(L, over, expect):
+    assert _call_decode_conv(L, **over) == expect
