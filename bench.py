@@ -59,7 +59,7 @@ def prefill_algorithmic(B, H, T, d, C=64):
 # Sources of the chunked prefill kernels; a profile summary records their
 # digest so that its DRAM traffic is only reported for the kernel it measured.
 PREFILL_SOURCES = ("kda_prefill_sm103.cu", "kda_chunk_phases.cuh", "sm103_ptx.cuh",
-                   "kda_internal.h")
+                   "kda_chunked.h")
 
 
 def prefill_source_digest() -> str:
@@ -93,6 +93,20 @@ def profiled_traffic(kernel: str):
 def decode_algorithmic(B, H, d):
     """Bytes of one decode step: fp32 state read + write, bf16 q,k,v,z in, o out, beta."""
     return B * H * (2 * d * d * 4 + 5 * d * 2 + 2)
+
+
+def conv_algorithmic(N, H, T, d, W):
+    """Bytes of one kda_short_conv call (d_k = d_v = d, bf16): q, k, v read and
+    their convolved copies written, conv states read and written, fp32 taps."""
+    Cc = 3 * d
+    return 2 * N * T * H * Cc * 2 + 2 * N * H * (W - 1) * Cc * 2 + H * Cc * W * 4
+
+
+def conv_decode_extra(B, H, d, W):
+    """Bytes a decode step with fused short convolutions moves on top of
+    decode_algorithmic: the bf16 conv state read and written, the fp32 taps."""
+    Cc = 3 * d
+    return 2 * B * H * (W - 1) * Cc * 2 + H * Cc * W * 4
 
 
 class ClockSampler:
@@ -317,6 +331,12 @@ def kda_arm(args, world, rank, local, pg):
     value = world * B * T / (ms_per_step / 1e3)
     achieved_gbs = byts / (kernel_ms / 1e3) / 1e9
     achieved_tf = flops / (kernel_ms / 1e3) / 1e12
+    if args.only == "conv":
+        conv = measure_conv(sets, ws, o, S, cu_host, B, H, T, d, args, stream)
+        if rank == 0:
+            print(json.dumps(dict(conv, only="conv",
+                                  frac=conv["achieved_gbs"] / peaks["hbm_gbs"])), flush=True)
+        return
     if args.only == "prefill":
         if rank == 0:
             print(json.dumps({"only": "prefill", "value": value, "unit": "tokens/s",
@@ -324,13 +344,14 @@ def kda_arm(args, world, rank, local, pg):
                               "tensor_tflops": achieved_tf}), flush=True)
         return
     ckpt = measure_checkpointed(sets, ws, o, S, cu_host, B, H, T, d, args, stream)
+    conv = measure_conv(sets, ws, o, S, cu_host, B, H, T, d, args, stream)
     softplus = measure_softplus(sets, ws, o, S, cu_host, args, stream)
     softplus["tokens_per_s"] = B * T / (softplus["kernel_ms"] / 1e3)
 
     return finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops, nsets,
                   set_bytes, x_host, o, S, ws, cu_host, value, ms_per_step, kernel_ms,
                   achieved_gbs, achieved_tf, clk, launches_per_step, kernel_name, pg, ckpt,
-                  softplus)
+                  softplus, conv)
 
 
 def measure_checkpointed(sets, ws, o, S, cu_host, B, H, T, d, args, stream, interval=1024):
@@ -357,6 +378,47 @@ def measure_checkpointed(sets, ws, o, S, cu_host, B, H, T, d, args, stream, inte
             "checkpoint_bytes": count * H * d * d * 4, "kernel_ms": ms}
 
 
+CONV_WIDTH = 4
+
+
+def measure_conv(sets, ws, o, S, cu_host, B, H, T, d, args, stream):
+    """The short convolutions (width 4, SiLU, conv states in and out) on the
+    prefill workload: kda_short_conv kernel time and bandwidth, and the time
+    of kda_short_conv followed by kda_prefill on its outputs."""
+    import torch
+    import kimi_delta_attention_12_gb300 as kda
+    from kimi_delta_attention_12_gb300 import inputs
+    dev = o.device
+    W = CONV_WIDTH
+    w, cs0 = inputs.make_conv_params(B, H, d, d, W, torch.bfloat16, seed=11)
+    w, cs_in = w.to(dev), cs0.to(dev)
+    cs_out = torch.empty_like(cs_in)
+    outs = tuple(torch.empty(B * T, H, d, dtype=torch.bfloat16, device=dev) for _ in range(3))
+    n = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    for i in range(args.warmup + n):
+        x = sets[i % len(sets)]
+        e = ev[i - args.warmup] if i >= args.warmup else None
+        if e:
+            e[0].record(stream)
+        qc, kc, vc = kda.kda_short_conv(x.q, x.k, x.v, w, cs_in, cs_out, x.cu_seqlens, cu_host,
+                                        silu=True, outputs=outs)
+        if e:
+            e[1].record(stream)
+        kda.kda_prefill(qc, kc, vc, x.z, x.beta, x.A, None, x.cu_seqlens,
+                        cu_seqlens_host=cu_host, o=o, final_state=S, workspace=ws)
+        if e:
+            e[2].record(stream)
+    torch.cuda.synchronize()
+    conv_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    both_ms = statistics.mean(e[0].elapsed_time(e[2]) for e in ev)
+    byts = conv_algorithmic(B, H, T, d, W)
+    return {"kernel": "short_conv_kernel", "width": W, "silu": True, "kernel_ms": conv_ms,
+            "algorithmic_bytes": byts, "achieved_gbs": byts / (conv_ms / 1e3) / 1e9,
+            "conv_then_prefill_ms": both_ms,
+            "conv_then_prefill_tokens_per_s": B * T / (both_ms / 1e3)}
+
+
 def measure_softplus(sets, ws, o, S, cu_host, args, stream):
     """The same prefill with the softplus-decay gate (KDA_FLAG_SOFTPLUS_GATE), which
     runs on the fp32 recurrent kernel: its kernel time."""
@@ -379,8 +441,10 @@ def measure_softplus(sets, ws, o, S, cu_host, args, stream):
             "kernel_ms": statistics.mean(a.elapsed_time(b) for a, b in ev), "steps": n}
 
 
-def run_decode(dev, rank, local, stream, batch=None, softplus_gate=False):
-    """64 consecutive decode steps on a resident B=256, H=96, d=128 fp32 state."""
+def run_decode(dev, rank, local, stream, batch=None, softplus_gate=False, conv=False):
+    """64 consecutive decode steps on a resident B=256, H=96, d=128 fp32 state
+    (with conv: short convolutions of width 4 and SiLU fused into each step,
+    on a resident bf16 conv state)."""
     import torch
     import kimi_delta_attention_12_gb300 as kda
     D = DECODE_SHAPE
@@ -397,37 +461,51 @@ def run_decode(dev, rank, local, stream, batch=None, softplus_gate=False):
                        torch.randn(Bd, Hd, dd, device=dev, generator=g).bfloat16(),
                        torch.sigmoid(torch.randn(Bd, Hd, device=dev, generator=g)).bfloat16()))
     od = torch.empty(Bd, Hd, dd, dtype=torch.bfloat16, device=dev)
-    for s in range(3):
+    if conv:
+        from kimi_delta_attention_12_gb300 import inputs
+        cw, cst = inputs.make_conv_params(Bd, Hd, dd, dd, CONV_WIDTH, torch.bfloat16,
+                                          seed=1000 + rank)
+        cw, cst = cw.to(dev), cst.to(dev)
+
+    def one(s):
         q_, k_, v_, z_, b_ = dsteps[s]
-        kda.kda_decode_step(q_, k_, v_, z_, b_, Adec, state, o=od,
-                            softplus_gate=softplus_gate)
+        if conv:
+            kda.kda_decode_step_conv(q_, k_, v_, z_, b_, Adec, state, cw, cst, o=od, silu=True,
+                                     softplus_gate=softplus_gate)
+        else:
+            kda.kda_decode_step(q_, k_, v_, z_, b_, Adec, state, o=od,
+                                softplus_gate=softplus_gate)
+    for s in range(3):
+        one(s)
     torch.cuda.synchronize()
     dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(D["steps"])]
     with ClockSampler(local) as dclk:
         for s in range(D["steps"]):
-            q_, k_, v_, z_, b_ = dsteps[s]
             dev_ev[s][0].record(stream)
-            kda.kda_decode_step(q_, k_, v_, z_, b_, Adec, state, o=od,
-                            softplus_gate=softplus_gate)
+            one(s)
             dev_ev[s][1].record(stream)
         torch.cuda.synchronize()
     dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dev_ev)
     dec_bytes = decode_algorithmic(Bd, Hd, dd)
+    if conv:
+        dec_bytes += conv_decode_extra(Bd, Hd, dd, CONV_WIDTH)
     return dec_ms, dec_bytes, dec_bytes / (dec_ms / 1e3) / 1e9, dclk.summary()
 
 
 def decode_only(args, rank, local, dev, stream, peaks):
-    dec_ms, dec_bytes, dec_gbs, clk = run_decode(dev, rank, local, stream, args.decode_batch)
+    dec_ms, dec_bytes, dec_gbs, clk = run_decode(dev, rank, local, stream, args.decode_batch,
+                                                 conv=args.decode_conv)
     if rank == 0:
-        print(json.dumps({"only": "decode", "batch": args.decode_batch, "value": dec_gbs,
+        print(json.dumps({"only": "decode", "batch": args.decode_batch,
+                          "conv": args.decode_conv, "value": dec_gbs,
                           "unit": "GB/s", "ms_per_step": dec_ms,
                           "frac": dec_gbs / peaks["hbm_gbs"], "clocks": clk}), flush=True)
 
 
 def finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops, nsets,
            set_bytes, x_host, o, S, ws, cu_host, value, ms_per_step, kernel_ms, achieved_gbs,
-           achieved_tf, clk, launches_per_step, kernel_name, pg, ckpt, softplus):
+           achieved_tf, clk, launches_per_step, kernel_name, pg, ckpt, softplus, conv):
     import torch
     import kimi_delta_attention_12_gb300 as kda
     # ---- end to end through the public API with host buffers ----
@@ -469,6 +547,11 @@ def finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops
     sp_ms, _, sp_gbs, _ = run_decode(dev, rank, local, stream, softplus_gate=True)
     softplus.update({"decode_ms_per_step": sp_ms, "decode_gbs": sp_gbs,
                      "decode_frac": sp_gbs / peaks["hbm_gbs"]})
+    cv_ms, cv_bytes, cv_gbs, _ = run_decode(dev, rank, local, stream, conv=True)
+    conv["frac"] = conv["achieved_gbs"] / peaks["hbm_gbs"]
+    conv.update({"decode_kernel": "kda_recurrent_kernel (conv fused, 2-CTA clusters)",
+                 "decode_ms_per_step": cv_ms, "decode_bytes_per_step": cv_bytes,
+                 "decode_gbs": cv_gbs, "decode_frac": cv_gbs / peaks["hbm_gbs"]})
 
     if rank != 0:
         return
@@ -499,6 +582,7 @@ def finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops
                    "clocks": dclk_summary},
         "prefill_checkpointed": dict(ckpt, kernel_ms_plain=kernel_ms),
         "softplus_gate": softplus,
+        "short_conv": conv,
         "cpu_baseline": {"value": cpu_tps, "unit": "tokens/s", "cores": cpu_threads,
                          "kind": "oracle", "sample": cpu_sample},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
@@ -515,10 +599,12 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["kda", "reference"], default="kda")
-    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "conv"], default="all",
                     help="run one part only (for profiler captures); the default runs all")
     ap.add_argument("--decode-batch", type=int, default=DECODE_SHAPE["B"],
                     help="decode batch for --only decode (smaller cases for profiler captures)")
+    ap.add_argument("--decode-conv", action="store_true",
+                    help="--only decode: short convolutions fused into each step")
     args = ap.parse_args()
     world, rank, local, pg = _dist_setup(args)
     try:

@@ -232,8 +232,8 @@ KDA_API int kda_decode_step(const void* q, const void* k, const void* v, const v
  *  W               1 .. 4;  flags: 0 or KDA_FLAG_CONV_SILU
  *  q_out, k_out, v_out   the convolved tensors, layouts of q, k, v, rounded
  *                  to dt (round to nearest even)
- * Buffers are device memory owned by the caller, 16-byte aligned (conv_w:
- * 4-byte).  Errors (nothing is launched): KDA_ERR_INVALID_ARG for a missing
+ * Buffers are device memory owned by the caller, 16-byte aligned (conv_w
+ * too).  Errors (nothing is launched): KDA_ERR_INVALID_ARG for a missing
  * buffer, W outside 1 .. 4, an unknown flag, bad cu_seqlens_host, an output
  * overlapping an input or another output, or conv_state_out overlapping
  * conv_state_in; KDA_ERR_UNSUPPORTED / KDA_ERR_ALIGNMENT as kda_prefill.
@@ -253,7 +253,7 @@ KDA_API int kda_short_conv(const void* q, const void* k, const void* v, const fl
  * shifts the conv state by the token (section 1, decode bullet: convolution
  * state and recurrent state both kept persistent).
  *
- *  conv_w       [H, 2 d_k + d_v, W] fp32, as kda_short_conv
+ *  conv_w       [H, 2 d_k + d_v, W] fp32, as kda_short_conv (16-byte aligned)
  *  conv_state   [pool_size, H, W-1, 2 d_k + d_v] dt; row slots[b] (or b) is
  *               read and rewritten in place; may be NULL when W == 1
  *  W            1 .. 4

@@ -271,7 +271,7 @@ int kda_short_conv(const void* q, const void* k, const void* v, const float* con
     }
     if (overlaps(conv_state_in, nst, conv_state_out, nst)) return KDA_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(q_out, 16) ||
-        !aligned(k_out, 16) || !aligned(v_out, 16) || !aligned(conv_w, 4) ||
+        !aligned(k_out, 16) || !aligned(v_out, 16) || !aligned(conv_w, 16) ||
         !aligned(conv_state_in, 16) || !aligned(conv_state_out, 16) ||
         !aligned(cu_seqlens, 4)) {
         return KDA_ERR_ALIGNMENT;
@@ -309,7 +309,7 @@ static int decode_step_impl(const void* q, const void* k, const void* v, const v
     if (!isfinite(scale)) return KDA_ERR_INVALID_ARG;
     if (B == 0) return KDA_OK;
     if (!q || !k || !v || !z || !beta || !A || !state || !o) return KDA_ERR_INVALID_ARG;
-    if (W > 0 && !aligned(conv_w, 4)) return KDA_ERR_ALIGNMENT;
+    if (W > 0 && !aligned(conv_w, 16)) return KDA_ERR_ALIGNMENT;
     if (W > 1 && !aligned(conv_state, elem_bytes(dt))) return KDA_ERR_ALIGNMENT;
     if (!slots && pool_size < B) return KDA_ERR_INVALID_ARG;
     const size_t eb = elem_bytes(dt);

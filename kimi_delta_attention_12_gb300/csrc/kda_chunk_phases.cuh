@@ -27,7 +27,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "kda_internal.h"
+#include "kda_chunked.h"
 #include "sm103_ptx.cuh"
 
 namespace kda {

@@ -50,7 +50,7 @@
 #include <string.h>
 
 #include "kda_chunk_phases.cuh"
-#include "kda_internal.h"
+#include "kda_chunked.h"
 #include "sm103_ptx.cuh"
 
 namespace kda {

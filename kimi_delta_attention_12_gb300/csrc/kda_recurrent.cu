@@ -70,8 +70,12 @@ constexpr int kModeDecodeConv = 3;  // decode with the short convolutions fused 
 
 // Cluster barrier between the two column-split CTAs of a head (decode with
 // short convolutions): every thread of both CTAs arrives once and waits once.
+// The arrive is relaxed: what it orders is the reads of the shared conv rows,
+// whose values each thread has already consumed (stored to shared memory
+// ahead of a __syncthreads) when it arrives; a release would also make the
+// thread wait for its in-flight state loads.
 __device__ __forceinline__ void cluster_arrive() {
-    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
@@ -81,19 +85,49 @@ __device__ __forceinline__ void cluster_wait() {
 // inputs (rows of the conv state, oldest first) and the current input x
 // against the channel's W = R + 1 taps; SiLU if asked.  nxt[0 .. R-1]
 // receives the shifted rows (the R most recent inputs, x last).
+// The W taps of a channel are contiguous: one 16-byte load for W = 4 and one
+// 8-byte load for W = 2 (the weights are 16-byte aligned), so that a warp's
+// tap loads touch no more sectors than the taps occupy.
+__device__ __forceinline__ void load_taps(const float* taps, int W, float tp[4]) {
+    if (W == 4) {
+        const float4 t = __ldg(reinterpret_cast<const float4*>(taps));
+        tp[0] = t.x; tp[1] = t.y; tp[2] = t.z; tp[3] = t.w;
+    } else if (W == 2) {
+        const float2 t = __ldg(reinterpret_cast<const float2*>(taps));
+        tp[0] = t.x; tp[1] = t.y;
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (j < W) {
+                tp[j] = __ldg(taps + j);
+            }
+        }
+    }
+}
+
 template <typename T>
 __device__ __forceinline__ float conv_channel(const T* rows, int Cc, int ch, const float* taps,
                                               int R, int silu, float x, float nxt[3]) {
+    float tp[4];
+    load_taps(taps, R + 1, tp);
     float acc = 0.0f;
     float prev[3];
 #pragma unroll
     for (int r = 0; r < 3; ++r) {
         if (r < R) {
             prev[r] = load_elem(rows, (size_t)r * Cc + ch);
-            acc = fmaf(__ldg(taps + r), prev[r], acc);
+            acc = fmaf(tp[r], prev[r], acc);
         }
     }
-    acc = fmaf(__ldg(taps + R), x, acc);
+#pragma unroll
+    for (int j = 1; j < 4; ++j) {
+        if (j == R) {
+            acc = fmaf(tp[j], x, acc);
+        }
+    }
+    if (R == 0) {
+        acc = tp[0] * x;
+    }
 #pragma unroll
     for (int r = 0; r < 3; ++r) {
         if (r < R) {

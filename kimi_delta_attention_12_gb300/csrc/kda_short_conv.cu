@@ -12,11 +12,12 @@
 //
 // Memory-bound: every input element is read once from HBM (plus W-1 halo rows
 // per block of tokens, from L2) and every output written once.  A thread owns
-// one 16-byte vector of channels of one tensor (8 bf16 or 4 fp32 channels) for
+// one 8-byte vector of channels of one tensor (4 bf16 or 2 fp32 channels) for
 // a block of TB consecutive tokens and slides a window of the last W-1 rows
 // through registers.  Consecutive threads own consecutive vectors of the same
-// token row, so a warp reads and writes 512 contiguous bytes per token.
-// Loads are issued eight rows ahead of their use.
+// token row, so a warp reads and writes 256 contiguous bytes per token.
+// Loads are issued eight rows ahead of their use; at 64 registers four CTAs
+// of 256 threads share an SM, which keeps enough loads in flight.
 //
 // Grid: x = token blocks, then one block per sequence that writes that
 // sequence's final conv state; y = groups of 256 channel vectors.
@@ -33,53 +34,49 @@ constexpr int kConvThreads = 256;
 constexpr int kConvTB = 32;     // tokens per block
 constexpr int kConvAhead = 8;   // rows loaded ahead
 
+// An 8-byte vector of channels: 4 bf16 or 2 fp32.
 template <typename T>
 struct VecTraits;
 template <>
 struct VecTraits<float> {
-    static constexpr int kN = 4;
-    __device__ static void unpack(const uint4& r, float* f) {
-        f[0] = __uint_as_float(r.x); f[1] = __uint_as_float(r.y);
-        f[2] = __uint_as_float(r.z); f[3] = __uint_as_float(r.w);
+    static constexpr int kN = 2;
+    __device__ static void unpack(const uint2& r, float* f) {
+        f[0] = __uint_as_float(r.x);
+        f[1] = __uint_as_float(r.y);
     }
-    __device__ static uint4 pack(const float* f) {
-        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
-                          __float_as_uint(f[2]), __float_as_uint(f[3]));
+    __device__ static uint2 pack(const float* f) {
+        return make_uint2(__float_as_uint(f[0]), __float_as_uint(f[1]));
     }
 };
 template <>
 struct VecTraits<__nv_bfloat16> {
-    static constexpr int kN = 8;
-    __device__ static void unpack(const uint4& r, float* f) {
-        const uint32_t u[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            f[2 * i] = __uint_as_float(u[i] << 16);
-            f[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
-        }
+    static constexpr int kN = 4;
+    __device__ static void unpack(const uint2& r, float* f) {
+        f[0] = __uint_as_float(r.x << 16);
+        f[1] = __uint_as_float(r.x & 0xffff0000u);
+        f[2] = __uint_as_float(r.y << 16);
+        f[3] = __uint_as_float(r.y & 0xffff0000u);
     }
-    __device__ static uint4 pack(const float* f) {
-        uint32_t u[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const __nv_bfloat162 b = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
-            u[i] = *reinterpret_cast<const uint32_t*>(&b);
-        }
-        return make_uint4(u[0], u[1], u[2], u[3]);
+    __device__ static uint2 pack(const float* f) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(f[0], f[1]);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(f[2], f[3]);
+        return make_uint2(*reinterpret_cast<const uint32_t*>(&lo),
+                          *reinterpret_cast<const uint32_t*>(&hi));
     }
 };
 
+// y * sigmoid(y) without a branch: with t = e^-|y| (never overflows),
+// sigmoid(y) = 1 / (1 + t) for y >= 0 and t / (1 + t) otherwise.  The fast
+// exponential and reciprocal keep the relative error near 1e-7, far below
+// the bf16 rounding of the stored result.
 __device__ __forceinline__ float silu_f(float y) {
-    // y * sigmoid(y) on the branch that cannot overflow
-    if (y >= 0.0f) {
-        return y / (1.0f + expf(-y));
-    }
-    const float e = expf(y);
-    return y * e / (1.0f + e);
+    const float t = __expf(-fabsf(y));
+    const float r = __fdividef(1.0f, 1.0f + t);
+    return y * (y >= 0.0f ? r : t * r);
 }
 
-__device__ __forceinline__ uint4 ld16(const void* base, size_t elem_off, int eb) {
-    return __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(base) +
+__device__ __forceinline__ uint2 ld8(const void* base, size_t elem_off, int eb) {
+    return __ldg(reinterpret_cast<const uint2*>(static_cast<const char*>(base) +
                                                 elem_off * eb));
 }
 
@@ -142,8 +139,8 @@ __device__ __forceinline__ int seq_of(const ShortConvParams& p, int64_t t) {
     return lo;
 }
 
-template <typename T, int W>
-__global__ void __launch_bounds__(kConvThreads)
+template <typename T, int W, bool kSilu>
+__global__ void __launch_bounds__(kConvThreads, 4)
 short_conv_kernel(const ShortConvParams p, int n_token_blocks) {
     using VT = VecTraits<T>;
     constexpr int VEC = VT::kN;
@@ -175,13 +172,13 @@ short_conv_kernel(const ShortConvParams p, int n_token_blocks) {
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const int64_t tau = eos - R + r;
-            uint4 val = make_uint4(0u, 0u, 0u, 0u);
+            uint2 val = make_uint2(0u, 0u);
             if (tau >= bos) {
-                val = ld16(x, xoff(tau), EB);
+                val = ld8(x, xoff(tau), EB);
             } else if (p.state_in) {
-                val = ld16(p.state_in, soff(n, (int)(tau - bos + R)), EB);
+                val = ld8(p.state_in, soff(n, (int)(tau - bos + R)), EB);
             }
-            *reinterpret_cast<uint4*>(static_cast<char*>(p.state_out) + soff(n, r) * EB) = val;
+            *reinterpret_cast<uint2*>(static_cast<char*>(p.state_out) + soff(n, r) * EB) = val;
         }
         return;
     }
@@ -189,14 +186,21 @@ short_conv_kernel(const ShortConvParams p, int n_token_blocks) {
     const int64_t t0 = (int64_t)blockIdx.x * kConvTB;
     const int64_t t1 = min((int64_t)p.total_T, t0 + kConvTB);
 
-    // taps of this vector's channels: w[h][off + i][j]
+    // taps of this vector's channels, w[h][off + i][j]: VEC * W contiguous
+    // floats, read as 16-byte vectors when W = 4 (the weights are 16-byte
+    // aligned and off is a multiple of VEC)
     float wt[W][VEC];
+    const float* wbase = p.w + ((size_t)cv.h * Cc + cv.off) * W;
 #pragma unroll
     for (int i = 0; i < VEC; ++i) {
-        const float* wr = p.w + ((size_t)cv.h * Cc + cv.off + i) * W;
+        if constexpr (W == 4) {
+            const float4 t = __ldg(reinterpret_cast<const float4*>(wbase) + i);
+            wt[0][i] = t.x; wt[1][i] = t.y; wt[2][i] = t.z; wt[3][i] = t.w;
+        } else {
 #pragma unroll
-        for (int j = 0; j < W; ++j) {
-            wt[j][i] = __ldg(wr + j);
+            for (int j = 0; j < W; ++j) {
+                wt[j][i] = __ldg(wbase + i * W + j);
+            }
         }
     }
 
@@ -207,22 +211,26 @@ short_conv_kernel(const ShortConvParams p, int n_token_blocks) {
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         const int64_t tau = t0 - R + r;
-        uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+        uint2 raw = make_uint2(0u, 0u);
         if (tau >= bos) {
-            raw = ld16(x, xoff(tau), EB);
+            raw = ld8(x, xoff(tau), EB);
         } else if (p.state_in) {
-            raw = ld16(p.state_in, soff(n, (int)(tau - bos + R)), EB);
+            raw = ld8(p.state_in, soff(n, (int)(tau - bos + R)), EB);
         }
         VT::unpack(raw, win[r]);
     }
 
     void* y = cv.tensor == 0 ? p.y[0] : cv.tensor == 1 ? p.y[1] : p.y[2];
+    // row pointers of this vector, advanced one token (H * d elements) at a time
+    const size_t row_bytes = (size_t)H * cv.d * EB;
+    const char* xr = static_cast<const char*>(x) + xoff(t0) * EB;
+    char* yr = static_cast<char*>(y) + xoff(t0) * EB;
     for (int64_t tb = t0; tb < t1; tb += kConvAhead) {
-        uint4 raw[kConvAhead];
+        uint2 raw[kConvAhead];
 #pragma unroll
         for (int i = 0; i < kConvAhead; ++i) {
             if (tb + i < t1) {
-                raw[i] = ld16(x, xoff(tb + i), EB);
+                raw[i] = __ldg(reinterpret_cast<const uint2*>(xr + i * row_bytes));
             }
         }
 #pragma unroll
@@ -240,9 +248,9 @@ short_conv_kernel(const ShortConvParams p, int n_token_blocks) {
                 } while (t >= eos);
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    uint4 s = make_uint4(0u, 0u, 0u, 0u);
+                    uint2 s = make_uint2(0u, 0u);
                     if (p.state_in) {
-                        s = ld16(p.state_in, soff(n, r), EB);
+                        s = ld8(p.state_in, soff(n, r), EB);
                     }
                     VT::unpack(s, win[r]);
                 }
@@ -251,15 +259,14 @@ short_conv_kernel(const ShortConvParams p, int n_token_blocks) {
             VT::unpack(raw[i], cur);
 #pragma unroll
             for (int c = 0; c < VEC; ++c) {
-                float acc = 0.0f;
+                float acc = wt[R][c] * cur[c];
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     acc = fmaf(wt[r][c], win[r][c], acc);
                 }
-                acc = fmaf(wt[R][c], cur[c], acc);
-                out[c] = p.silu ? silu_f(acc) : acc;
+                out[c] = kSilu ? silu_f(acc) : acc;
             }
-            *reinterpret_cast<uint4*>(static_cast<char*>(y) + xoff(t) * EB) = VT::pack(out);
+            *reinterpret_cast<uint2*>(yr + i * row_bytes) = VT::pack(out);
 #pragma unroll
             for (int r = 0; r + 1 < R; ++r) {
 #pragma unroll
@@ -274,6 +281,18 @@ short_conv_kernel(const ShortConvParams p, int n_token_blocks) {
                 }
             }
         }
+        xr += kConvAhead * row_bytes;
+        yr += kConvAhead * row_bytes;
+    }
+}
+
+template <typename T, bool kSilu>
+void launch_width(const ShortConvParams& p, dim3 grid, int ntb, cudaStream_t stream) {
+    switch (p.W) {
+        case 1: short_conv_kernel<T, 1, kSilu><<<grid, kConvThreads, 0, stream>>>(p, ntb); break;
+        case 2: short_conv_kernel<T, 2, kSilu><<<grid, kConvThreads, 0, stream>>>(p, ntb); break;
+        case 3: short_conv_kernel<T, 3, kSilu><<<grid, kConvThreads, 0, stream>>>(p, ntb); break;
+        default: short_conv_kernel<T, 4, kSilu><<<grid, kConvThreads, 0, stream>>>(p, ntb); break;
     }
 }
 
@@ -286,16 +305,14 @@ cudaError_t launch_typed(const ShortConvParams& p, cudaStream_t stream) {
     if (gx == 0 || vecs == 0) {
         return cudaSuccess;
     }
-    if (gx > 0x7fffffffLL) {
+    if (gx > 0x7fffffffLL || p.W < 1 || p.W > 4) {
         return cudaErrorInvalidValue;
     }
     const dim3 grid((unsigned)gx, (unsigned)((vecs + kConvThreads - 1) / kConvThreads));
-    switch (p.W) {
-        case 1: short_conv_kernel<T, 1><<<grid, kConvThreads, 0, stream>>>(p, (int)ntb); break;
-        case 2: short_conv_kernel<T, 2><<<grid, kConvThreads, 0, stream>>>(p, (int)ntb); break;
-        case 3: short_conv_kernel<T, 3><<<grid, kConvThreads, 0, stream>>>(p, (int)ntb); break;
-        case 4: short_conv_kernel<T, 4><<<grid, kConvThreads, 0, stream>>>(p, (int)ntb); break;
-        default: return cudaErrorInvalidValue;
+    if (p.silu) {
+        launch_width<T, true>(p, grid, (int)ntb, stream);
+    } else {
+        launch_width<T, false>(p, grid, (int)ntb, stream);
     }
     return cudaGetLastError();
 }

@@ -250,6 +250,7 @@ def _call_conv(L, **over):
     (dict(q=BASE + 8), kda.KDA_ERR_ALIGNMENT),
     (dict(s_in=BASE + 0x400008), kda.KDA_ERR_ALIGNMENT),
     (dict(w=BASE + 0x300002), kda.KDA_ERR_ALIGNMENT),
+    (dict(w=BASE + 0x300004), kda.KDA_ERR_ALIGNMENT),      # taps are read as 16-byte vectors
 ])
 def test_short_conv_validation(L, over, expect):
     assert _call_conv(L, **over) == expect
@@ -284,6 +285,7 @@ def _call_decode_conv(L, **over):
     (dict(dk=16), kda.KDA_ERR_UNSUPPORTED),
     (dict(pool=2), kda.KDA_ERR_INVALID_ARG),
     (dict(w=BASE + 0x800002), kda.KDA_ERR_ALIGNMENT),
+    (dict(w=BASE + 0x800008), kda.KDA_ERR_ALIGNMENT),
     (dict(cs=BASE + 0x900001), kda.KDA_ERR_ALIGNMENT),
     (dict(B=0, flags=1 | 4 | 8), kda.KDA_OK),          # nothing to do, nothing launched
 ])
