@@ -103,8 +103,9 @@ def conv_algorithmic(N, H, T, d, W):
 
 
 def conv_decode_extra(B, H, d, W):
-    """Bytes a decode step with fused short convolutions moves on top of
-    decode_algorithmic: the bf16 conv state read and written, the fp32 taps."""
+    """Bytes a decode step with short convolutions moves on top of
+    decode_algorithmic: the bf16 conv state read and written, the fp32 taps
+    (the convolved token passes through a scratch buffer, not counted)."""
     Cc = 3 * d
     return 2 * B * H * (W - 1) * Cc * 2 + H * Cc * W * 4
 
@@ -443,8 +444,8 @@ def measure_softplus(sets, ws, o, S, cu_host, args, stream):
 
 def run_decode(dev, rank, local, stream, batch=None, softplus_gate=False, conv=False):
     """64 consecutive decode steps on a resident B=256, H=96, d=128 fp32 state
-    (with conv: short convolutions of width 4 and SiLU fused into each step,
-    on a resident bf16 conv state)."""
+    (with conv: each step preceded by the token's short convolutions, width 4
+    and SiLU, on a resident bf16 conv state: kda_decode_step_conv)."""
     import torch
     import kimi_delta_attention_12_gb300 as kda
     D = DECODE_SHAPE
@@ -466,12 +467,14 @@ def run_decode(dev, rank, local, stream, batch=None, softplus_gate=False, conv=F
         cw, cst = inputs.make_conv_params(Bd, Hd, dd, dd, CONV_WIDTH, torch.bfloat16,
                                           seed=1000 + rank)
         cw, cst = cw.to(dev), cst.to(dev)
+        cws = torch.empty(kda.decode_conv_workspace_bytes(Bd, Hd, dd, dd, torch.bfloat16),
+                          dtype=torch.uint8, device=dev)
 
     def one(s):
         q_, k_, v_, z_, b_ = dsteps[s]
         if conv:
             kda.kda_decode_step_conv(q_, k_, v_, z_, b_, Adec, state, cw, cst, o=od, silu=True,
-                                     softplus_gate=softplus_gate)
+                                     softplus_gate=softplus_gate, workspace=cws)
         else:
             kda.kda_decode_step(q_, k_, v_, z_, b_, Adec, state, o=od,
                                 softplus_gate=softplus_gate)
@@ -549,7 +552,7 @@ def finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops
                      "decode_frac": sp_gbs / peaks["hbm_gbs"]})
     cv_ms, cv_bytes, cv_gbs, _ = run_decode(dev, rank, local, stream, conv=True)
     conv["frac"] = conv["achieved_gbs"] / peaks["hbm_gbs"]
-    conv.update({"decode_kernel": "kda_recurrent_kernel (conv fused, 2-CTA clusters)",
+    conv.update({"decode_kernels": "short_conv_decode_kernel + kda_recurrent_kernel",
                  "decode_ms_per_step": cv_ms, "decode_bytes_per_step": cv_bytes,
                  "decode_gbs": cv_gbs, "decode_frac": cv_gbs / peaks["hbm_gbs"]})
 
@@ -604,7 +607,7 @@ def main():
     ap.add_argument("--decode-batch", type=int, default=DECODE_SHAPE["B"],
                     help="decode batch for --only decode (smaller cases for profiler captures)")
     ap.add_argument("--decode-conv", action="store_true",
-                    help="--only decode: short convolutions fused into each step")
+                    help="--only decode: each step preceded by the short convolutions")
     args = ap.parse_args()
     world, rank, local, pg = _dist_setup(args)
     try:

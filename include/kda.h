@@ -246,21 +246,26 @@ KDA_API int kda_short_conv(const void* q, const void* k, const void* v, const fl
                            void* q_out, void* k_out, void* v_out, void* stream);
 
 /*
- * kda_decode_step_conv -- kda_decode_step with the short convolutions of q,
- * k and v (as kda_short_conv, width W) fused in front of the state update:
- * one launch reads each row's conv state, convolves the token's q, k, v in
- * fp32 (no rounding to dt in between), runs the decode step on the result and
- * shifts the conv state by the token (section 1, decode bullet: convolution
- * state and recurrent state both kept persistent).
+ * kda_decode_step_conv -- kda_decode_step preceded by the token's short
+ * convolutions of q, k and v (as kda_short_conv, width W) with the conv
+ * state kept persistent beside the recurrent state (section 1, decode
+ * bullet).  Two launches on `stream`: a memory-bound pass convolves the
+ * token of every row into `workspace` (rounded to dt, as kda_short_conv's
+ * outputs) and shifts each row's conv state by the token in place; the
+ * decode step then runs on the convolved q, k, v.
  *
  *  conv_w       [H, 2 d_k + d_v, W] fp32, as kda_short_conv (16-byte aligned)
  *  conv_state   [pool_size, H, W-1, 2 d_k + d_v] dt; row slots[b] (or b) is
  *               read and rewritten in place; may be NULL when W == 1
  *  W            1 .. 4
  *  flags        KDA_FLAG_L2NORM_QK, KDA_FLAG_SOFTPLUS_GATE, KDA_FLAG_CONV_SILU
+ *  workspace    device scratch of kda_decode_conv_workspace_bytes(B, H, d_k,
+ *               d_v, dt) bytes, 16-byte aligned, overlapping none of the
+ *               other buffers; its contents need no initialisation
  * Every other argument is that of kda_decode_step; a slot outside
- * [0, pool_size) leaves both of its states untouched.  For d_v = 128 the two
- * CTAs that share a head run as one thread-block cluster.
+ * [0, pool_size) leaves both of its states untouched and writes NaN to its
+ * o row.  Errors as kda_decode_step, plus KDA_ERR_WORKSPACE for a missing or
+ * short workspace and KDA_ERR_UNSUPPORTED for B > 65535.
  */
 KDA_API int kda_decode_step_conv(const void* q, const void* k, const void* v, const void* z,
                                  const void* beta, const float* A, float* state,
@@ -268,7 +273,13 @@ KDA_API int kda_decode_step_conv(const void* q, const void* k, const void* v, co
                                  const float* conv_w, void* conv_state, int32_t W,
                                  int32_t B, int32_t H, int32_t d_k, int32_t d_v,
                                  kda_dtype dt, float scale, uint32_t flags,
-                                 void* o, void* stream);
+                                 void* o, void* workspace, size_t workspace_bytes,
+                                 void* stream);
+
+/* kda_decode_conv_workspace_bytes -- the scratch kda_decode_step_conv needs:
+ * the convolved q, k, v of one token per row (0 for negative sizes). */
+KDA_API size_t kda_decode_conv_workspace_bytes(int32_t B, int32_t H, int32_t d_k, int32_t d_v,
+                                               kda_dtype dt);
 
 /*
  * kda_state_io -- moves fp32 states of shape [H, d_k, d_v] each (the

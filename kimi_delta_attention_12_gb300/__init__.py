@@ -48,7 +48,7 @@ EXPORTED_SYMBOLS = (
     "kda_prefill_workspace_bytes", "kda_prefill", "kda_workspace_status",
     "kda_decode_step", "kda_state_io", "kda_status_string", "kda_version",
     "kda_prefill_noalloc", "kda_prefill_checkpointed", "kda_checkpoint_count",
-    "kda_short_conv", "kda_decode_step_conv",
+    "kda_short_conv", "kda_decode_step_conv", "kda_decode_conv_workspace_bytes",
 )
 
 _lock = threading.Lock()
@@ -105,7 +105,9 @@ def lib() -> ctypes.CDLL:
             L.kda_decode_step_conv.restype = ctypes.c_int
             L.kda_decode_step_conv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i32,
                                                i32, i32, i32, i32, ctypes.c_int,
-                                               ctypes.c_float, ctypes.c_uint32, vp, vp]
+                                               ctypes.c_float, ctypes.c_uint32, vp, vp, sz, vp]
+            L.kda_decode_conv_workspace_bytes.restype = sz
+            L.kda_decode_conv_workspace_bytes.argtypes = [i32, i32, i32, i32, ctypes.c_int]
             L.kda_checkpoint_count.restype = ctypes.c_int64
             L.kda_checkpoint_count.argtypes = [vp, i32, i32, i32]
             _lib = L
@@ -329,16 +331,23 @@ def kda_short_conv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, conv_w: to
     return qo, ko, vo
 
 
+def decode_conv_workspace_bytes(B: int, H: int, d_k: int, d_v: int, dtype: torch.dtype) -> int:
+    return int(lib().kda_decode_conv_workspace_bytes(B, H, d_k, d_v, _dtype_code(dtype)))
+
+
 def kda_decode_step_conv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: torch.Tensor,
                          beta: torch.Tensor, A: torch.Tensor, state: torch.Tensor,
                          conv_w: torch.Tensor, conv_state: Optional[torch.Tensor],
                          slots: Optional[torch.Tensor] = None, scale: float = 1.0,
                          l2norm: bool = True, silu: bool = False, softplus_gate: bool = False,
                          o: Optional[torch.Tensor] = None,
+                         workspace: Optional[torch.Tensor] = None,
                          stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
-    """kda_decode_step with the short convolutions of q, k, v fused in front:
+    """kda_decode_step preceded by the token's short convolutions of q, k, v:
     conv_state [pool, H, W-1, 2 d_k + d_v] (dtype of q) is read and shifted in
-    place at rows `slots`, like `state`.  Returns o [B, H, d_v]."""
+    place at rows `slots`, like `state`.  `workspace` (uint8, at least
+    decode_conv_workspace_bytes) is allocated when not given.
+    Returns o [B, H, d_v]."""
     B, H, d_k = q.shape
     d_v = v.shape[-1]
     dt = q.dtype
@@ -353,12 +362,16 @@ def kda_decode_step_conv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: t
         raise TypeError("slots must be int32")
     if o is None:
         o = torch.empty(B, H, d_v, dtype=dt, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(decode_conv_workspace_bytes(B, H, d_k, d_v, dt),
+                                dtype=torch.uint8, device=q.device)
     flags = ((KDA_FLAG_L2NORM_QK if l2norm else 0) | (KDA_FLAG_SOFTPLUS_GATE if softplus_gate else 0)
              | (KDA_FLAG_CONV_SILU if silu else 0))
     st = lib().kda_decode_step_conv(
         _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(state), _ptr(slots),
         state.shape[0], _ptr(conv_w), _ptr(conv_state), conv_w.shape[-1], B, H, d_k, d_v,
-        _dtype_code(dt), float(scale), flags, _ptr(o), _stream_ptr(stream))
+        _dtype_code(dt), float(scale), flags, _ptr(o), _ptr(workspace), workspace.numel(),
+        _stream_ptr(stream))
     if st != KDA_OK:
         raise KDAError(st, "kda_decode_step_conv")
     return o

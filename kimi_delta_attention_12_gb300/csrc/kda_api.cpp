@@ -291,13 +291,24 @@ int kda_short_conv(const void* q, const void* k, const void* v, const float* con
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+// One of the three convolved tensors in the decode-conv workspace.
+static size_t conv_ws_part(int32_t B, int32_t H, int32_t d, kda_dtype dt) {
+    return round_up((size_t)B * H * d * elem_bytes(dt), 256);
+}
+
+size_t kda_decode_conv_workspace_bytes(int32_t B, int32_t H, int32_t d_k, int32_t d_v,
+                                       kda_dtype dt) {
+    if (B < 0 || H < 0 || d_k < 0 || d_v < 0) return 0;
+    return 2 * conv_ws_part(B, H, d_k, dt) + conv_ws_part(B, H, d_v, dt);
+}
+
 // kda_decode_step and kda_decode_step_conv (W = 0: no convolution)
 static int decode_step_impl(const void* q, const void* k, const void* v, const void* z,
                      const void* beta, const float* A, float* state,
                      const int32_t* slots, int32_t pool_size, const float* conv_w,
                      void* conv_state, int32_t W, int32_t B, int32_t H, int32_t d_k,
                      int32_t d_v, kda_dtype dt, float scale, uint32_t flags, void* o,
-                     void* stream) {
+                     void* workspace, size_t workspace_bytes, void* stream) {
     if (dt != KDA_F32 && dt != KDA_BF16) return KDA_ERR_UNSUPPORTED;
     if (!supported_dim(d_k) || !supported_dim(d_v)) return KDA_ERR_UNSUPPORTED;
     if (B < 0 || H < 1 || pool_size < 0) return KDA_ERR_INVALID_ARG;
@@ -309,8 +320,23 @@ static int decode_step_impl(const void* q, const void* k, const void* v, const v
     if (!isfinite(scale)) return KDA_ERR_INVALID_ARG;
     if (B == 0) return KDA_OK;
     if (!q || !k || !v || !z || !beta || !A || !state || !o) return KDA_ERR_INVALID_ARG;
-    if (W > 0 && !aligned(conv_w, 16)) return KDA_ERR_ALIGNMENT;
-    if (W > 1 && !aligned(conv_state, elem_bytes(dt))) return KDA_ERR_ALIGNMENT;
+    if (W > 0) {
+        if (B > 65535) return KDA_ERR_UNSUPPORTED;
+        if (!workspace || workspace_bytes < kda_decode_conv_workspace_bytes(B, H, d_k, d_v, dt)) {
+            return KDA_ERR_WORKSPACE;
+        }
+        const size_t wsb = kda_decode_conv_workspace_bytes(B, H, d_k, d_v, dt);
+        const size_t eb = elem_bytes(dt);
+        const size_t nqk = (size_t)B * H * d_k * eb, nv = (size_t)B * H * d_v * eb;
+        const size_t ncs = (size_t)pool_size * H * (W - 1) * (2 * d_k + d_v) * eb;
+        if (overlaps(workspace, wsb, q, nqk) || overlaps(workspace, wsb, k, nqk) ||
+            overlaps(workspace, wsb, v, nv) || overlaps(workspace, wsb, o, nv) ||
+            overlaps(workspace, wsb, conv_state, ncs)) {
+            return KDA_ERR_INVALID_ARG;
+        }
+        if (!aligned(conv_w, 16) || !aligned(workspace, 16)) return KDA_ERR_ALIGNMENT;
+        if (W > 1 && !aligned(conv_state, 16)) return KDA_ERR_ALIGNMENT;
+    }
     if (!slots && pool_size < B) return KDA_ERR_INVALID_ARG;
     const size_t eb = elem_bytes(dt);
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(z, 16) ||
@@ -325,12 +351,25 @@ static int decode_step_impl(const void* q, const void* k, const void* v, const v
     p.o = o; p.rows = B; p.total_T = B; p.H = H; p.pool_size = pool_size;
     p.scale = scale; p.l2norm = (flags & KDA_FLAG_L2NORM_QK) ? 1 : 0; p.decode = 1;
     p.softplus_gate = (flags & KDA_FLAG_SOFTPLUS_GATE) ? 1 : 0;
-    p.conv_width = W;
-    p.conv_silu = (flags & KDA_FLAG_CONV_SILU) ? 1 : 0;
-    p.conv_w = conv_w;
-    p.conv_state = conv_state;
-    const cudaError_t err = kda::launch_recurrent(p, d_k, d_v, dt == KDA_F32 ? 0 : 1,
-                                                  static_cast<cudaStream_t>(stream));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (W > 0) {
+        // the token's short convolutions into the workspace, conv state
+        // shifted in place; the decode step then reads the convolved q, k, v
+        kda::ShortConvDecodeParams c;
+        memset(&c, 0, sizeof(c));
+        char* ws = static_cast<char*>(workspace);
+        c.x[0] = q; c.x[1] = k; c.x[2] = v;
+        c.y[0] = ws;
+        c.y[1] = ws + conv_ws_part(B, H, d_k, dt);
+        c.y[2] = ws + 2 * conv_ws_part(B, H, d_k, dt);
+        c.w = conv_w; c.state = conv_state; c.slots = slots;
+        c.B = B; c.pool_size = pool_size; c.H = H; c.d_k = d_k; c.d_v = d_v; c.W = W;
+        c.silu = (flags & KDA_FLAG_CONV_SILU) ? 1 : 0;
+        const cudaError_t ce = kda::launch_short_conv_decode(c, dt == KDA_F32 ? 0 : 1, s);
+        if (ce != cudaSuccess) return KDA_ERR_CUDA;
+        p.q = c.y[0]; p.k = c.y[1]; p.v = c.y[2];
+    }
+    const cudaError_t err = kda::launch_recurrent(p, d_k, d_v, dt == KDA_F32 ? 0 : 1, s);
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -341,7 +380,7 @@ int kda_decode_step(const void* q, const void* k, const void* v, const void* z,
                     kda_dtype dt, float scale, uint32_t flags,
                     void* o, void* stream) {
     return decode_step_impl(q, k, v, z, beta, A, state, slots, pool_size, nullptr, nullptr, 0,
-                            B, H, d_k, d_v, dt, scale, flags, o, stream);
+                            B, H, d_k, d_v, dt, scale, flags, o, nullptr, 0, stream);
 }
 
 int kda_decode_step_conv(const void* q, const void* k, const void* v, const void* z,
@@ -350,10 +389,11 @@ int kda_decode_step_conv(const void* q, const void* k, const void* v, const void
                          const float* conv_w, void* conv_state, int32_t W,
                          int32_t B, int32_t H, int32_t d_k, int32_t d_v,
                          kda_dtype dt, float scale, uint32_t flags,
-                         void* o, void* stream) {
+                         void* o, void* workspace, size_t workspace_bytes, void* stream) {
     if (W < 1) return KDA_ERR_INVALID_ARG;
     return decode_step_impl(q, k, v, z, beta, A, state, slots, pool_size, conv_w, conv_state, W,
-                            B, H, d_k, d_v, dt, scale, flags, o, stream);
+                            B, H, d_k, d_v, dt, scale, flags, o, workspace, workspace_bytes,
+                            stream);
 }
 
 int kda_state_io(kda_state_op op, float* dst, const float* src,

@@ -39,13 +39,6 @@ struct RecurrentParams {
     float* ckpt_pool;
     const int32_t* ckpt_slots;
     int32_t ckpt_pool_size;
-    // decode only: short convolutions of q, k, v fused in front of the step
-    // (conv_width 0 = none); conv_state [pool_size, H, W-1, 2 d_k + d_v] in
-    // the input dtype, read and rewritten in place at the row's slot
-    int32_t conv_width;
-    int32_t conv_silu;
-    const float* conv_w;         // [H, 2 d_k + d_v, W] fp32
-    void* conv_state;
 };
 
 // Short convolutions of q, k and v (kda_short_conv.cu).  Conv weights and
@@ -67,6 +60,27 @@ struct ShortConvParams {
     int32_t silu;
 };
 cudaError_t launch_short_conv(const ShortConvParams& p, int dtype, cudaStream_t stream);
+
+// One decode token of short convolutions per batch row: y = the convolved q,
+// k, v (layouts [B, H, d]); the row's conv state (pool row slots[b], or b) is
+// shifted by the token in place.  Rows with a slot outside [0, pool_size)
+// are skipped (their y is left unwritten).
+struct ShortConvDecodeParams {
+    const void* x[3];            // q, k [B, H, d_k]; v [B, H, d_v]
+    void* y[3];
+    const float* w;              // [H, 2 d_k + d_v, W] fp32
+    void* state;                 // [pool_size, H, W-1, 2 d_k + d_v]
+    const int32_t* slots;        // or null (identity)
+    int32_t B;
+    int32_t pool_size;
+    int32_t H;
+    int32_t d_k;
+    int32_t d_v;
+    int32_t W;                   // 1 .. 4
+    int32_t silu;
+};
+cudaError_t launch_short_conv_decode(const ShortConvDecodeParams& p, int dtype,
+                                     cudaStream_t stream);
 
 // Launches the recurrent kernel for (d_k, d_v) in {32, 64, 128}^2 and
 // dtype (0 = fp32, 1 = bf16).  Returns a cudaError_t.

@@ -66,96 +66,11 @@ __device__ __forceinline__ float sigmoid_f(float x) {
 constexpr int kModeDecode = 0;    // one token per row, state pool with slots
 constexpr int kModePrefill = 1;   // a sequence per row
 constexpr int kModeCkpt = 2;      // prefill that also stores state checkpoints
-constexpr int kModeDecodeConv = 3;  // decode with the short convolutions fused in
-
-// Cluster barrier between the two column-split CTAs of a head (decode with
-// short convolutions): every thread of both CTAs arrives once and waits once.
-// The arrive is relaxed: what it orders is the reads of the shared conv rows,
-// whose values each thread has already consumed (stored to shared memory
-// ahead of a __syncthreads) when it arrives; a release would also make the
-// thread wait for its in-flight state loads.
-__device__ __forceinline__ void cluster_arrive() {
-    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
-}
-
-// Short convolution of one channel for one decode token: the R stored
-// inputs (rows of the conv state, oldest first) and the current input x
-// against the channel's W = R + 1 taps; SiLU if asked.  nxt[0 .. R-1]
-// receives the shifted rows (the R most recent inputs, x last).
-// The W taps of a channel are contiguous: one 16-byte load for W = 4 and one
-// 8-byte load for W = 2 (the weights are 16-byte aligned), so that a warp's
-// tap loads touch no more sectors than the taps occupy.
-__device__ __forceinline__ void load_taps(const float* taps, int W, float tp[4]) {
-    if (W == 4) {
-        const float4 t = __ldg(reinterpret_cast<const float4*>(taps));
-        tp[0] = t.x; tp[1] = t.y; tp[2] = t.z; tp[3] = t.w;
-    } else if (W == 2) {
-        const float2 t = __ldg(reinterpret_cast<const float2*>(taps));
-        tp[0] = t.x; tp[1] = t.y;
-    } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            if (j < W) {
-                tp[j] = __ldg(taps + j);
-            }
-        }
-    }
-}
-
-template <typename T>
-__device__ __forceinline__ float conv_channel(const T* rows, int Cc, int ch, const float* taps,
-                                              int R, int silu, float x, float nxt[3]) {
-    float tp[4];
-    load_taps(taps, R + 1, tp);
-    float acc = 0.0f;
-    float prev[3];
-#pragma unroll
-    for (int r = 0; r < 3; ++r) {
-        if (r < R) {
-            prev[r] = load_elem(rows, (size_t)r * Cc + ch);
-            acc = fmaf(tp[r], prev[r], acc);
-        }
-    }
-#pragma unroll
-    for (int j = 1; j < 4; ++j) {
-        if (j == R) {
-            acc = fmaf(tp[j], x, acc);
-        }
-    }
-    if (R == 0) {
-        acc = tp[0] * x;
-    }
-#pragma unroll
-    for (int r = 0; r < 3; ++r) {
-        if (r < R) {
-            nxt[r] = r + 1 < R ? prev[r + 1] : x;
-        }
-    }
-    if (silu) {
-        acc = acc * sigmoid_f(acc);
-    }
-    return acc;
-}
-
-template <typename T>
-__device__ __forceinline__ void conv_store_rows(T* rows, int Cc, int ch, int R,
-                                                const float nxt[3]) {
-#pragma unroll
-    for (int r = 0; r < 3; ++r) {
-        if (r < R) {
-            store_elem(rows, (size_t)r * Cc + ch, nxt[r]);
-        }
-    }
-}
 
 template <int DK, int DV, int NSPLIT, typename T, int kMode>
-__global__ void __launch_bounds__(kThreads, 4)
+__global__ void __launch_bounds__(kThreads)
 kda_recurrent_kernel(const RecurrentParams p) {
-    constexpr bool kConv = kMode == kModeDecodeConv;
-    constexpr bool kDecode = kMode == kModeDecode || kConv;
+    constexpr bool kDecode = kMode == kModeDecode;
     constexpr bool kCkpt = kMode == kModeCkpt;
     constexpr int DVS = DV / NSPLIT;
     constexpr int LPR = DVS / 4;
@@ -263,32 +178,13 @@ kda_recurrent_kernel(const RecurrentParams p) {
         ck_next = bos + p.ckpt_interval - 1;
     }
 
-    // decode with short convolutions: this row's conv state and taps
-    T* conv_rows = nullptr;
-    const float* conv_w = nullptr;
-    int conv_R = 0, Cc = 0;
-    float nq[3], nk[3], nv[3];
-    if constexpr (kConv) {
-        Cc = 2 * DK + DV;
-        conv_R = p.conv_width - 1;
-        conv_rows = static_cast<T*>(p.conv_state) + ((size_t)sidx * H + h) * conv_R * Cc;
-        conv_w = p.conv_w + (size_t)h * Cc * p.conv_width;
-    }
-
     for (int64_t t = bos; t < eos; ++t) {
         // ---- stage 1: token inputs, gate, norm partial sums ----
         const size_t rk = ((size_t)t * H + h) * DK;
         if (tid < DK) {
-            float qv = load_elem(q, rk + tid);
-            float kv = load_elem(k, rk + tid);
+            const float qv = load_elem(q, rk + tid);
+            const float kv = load_elem(k, rk + tid);
             const float zv = load_elem(z, rk + tid);
-            if constexpr (kConv) {
-                qv = conv_channel(conv_rows, Cc, tid, conv_w + (size_t)tid * p.conv_width,
-                                  conv_R, p.conv_silu, qv, nq);
-                kv = conv_channel(conv_rows, Cc, DK + tid,
-                                  conv_w + (size_t)(DK + tid) * p.conv_width, conv_R,
-                                  p.conv_silu, kv, nk);
-            }
             s_q[tid] = qv;
             s_k[tid] = kv;
             // alpha = e^g: K3's g = -5 sigmoid(e^A z), or Kimi Linear's
@@ -309,22 +205,12 @@ kda_recurrent_kernel(const RecurrentParams p) {
             }
         } else if (tid < DK + DVS) {
             const int j = tid - DK;
-            float vv = load_elem(v, ((size_t)t * H + h) * DV + col0 + j);
-            if constexpr (kConv) {
-                const int ch = 2 * DK + col0 + j;
-                vv = conv_channel(conv_rows, Cc, ch, conv_w + (size_t)ch * p.conv_width, conv_R,
-                                  p.conv_silu, vv, nv);
-            }
-            s_v[j] = vv;
+            s_v[j] = load_elem(v, ((size_t)t * H + h) * DV + col0 + j);
             if (j == 0) {
                 s_beta = load_elem(beta, (size_t)t * H + h);
             }
         }
         __syncthreads();
-        if constexpr (kConv && NSPLIT > 1) {
-            // this CTA has read the q / k conv rows that its partner rewrites
-            cluster_arrive();
-        }
 
         float sq = 0.f, sk = 0.f, sqk = 0.f;
 #pragma unroll
@@ -421,22 +307,6 @@ kda_recurrent_kernel(const RecurrentParams p) {
             __stcs(sp + (i * DV + col0) / 4 + cg, S[r]);
         }
     }
-
-    if constexpr (kConv) {
-        // shift the conv state: v columns belong to this CTA alone; the q and
-        // k rows are shared by the column-split CTAs of the head and are
-        // rewritten by split 0 once both have read them
-        if (tid >= DK && tid < DK + DVS) {
-            conv_store_rows(conv_rows, Cc, 2 * DK + col0 + (tid - DK), conv_R, nv);
-        }
-        if constexpr (NSPLIT > 1) {
-            cluster_wait();
-        }
-        if (split == 0 && tid < DK) {
-            conv_store_rows(conv_rows, Cc, tid, conv_R, nq);
-            conv_store_rows(conv_rows, Cc, DK + tid, conv_R, nk);
-        }
-    }
 }
 
 // Value-column split per head: decode of d_v = 128 uses two CTAs per head
@@ -445,28 +315,11 @@ template <int DV>
 constexpr int column_split() { return DV == 128 ? 2 : 1; }
 
 template <int DK, int DV, int NS, typename T>
-cudaError_t launch_mode(int mode, dim3 grid, const RecurrentParams& p, cudaStream_t stream) {
+void launch_mode(int mode, dim3 grid, const RecurrentParams& p, cudaStream_t stream) {
     switch (mode) {
         case kModeDecode:
             kda_recurrent_kernel<DK, DV, NS, T, kModeDecode><<<grid, kThreads, 0, stream>>>(p);
             break;
-        case kModeDecodeConv: {
-            // the NS column-split CTAs of a head form one cluster
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = grid;
-            cfg.blockDim = dim3(kThreads);
-            cfg.dynamicSmemBytes = 0;
-            cfg.stream = stream;
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = NS;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            return cudaLaunchKernelEx(&cfg, kda_recurrent_kernel<DK, DV, NS, T, kModeDecodeConv>,
-                                      p);
-        }
         case kModeCkpt:
             kda_recurrent_kernel<DK, DV, NS, T, kModeCkpt><<<grid, kThreads, 0, stream>>>(p);
             break;
@@ -474,7 +327,6 @@ cudaError_t launch_mode(int mode, dim3 grid, const RecurrentParams& p, cudaStrea
             kda_recurrent_kernel<DK, DV, NS, T, kModePrefill><<<grid, kThreads, 0, stream>>>(p);
             break;
     }
-    return cudaSuccess;
 }
 
 template <int DK, int DV>
@@ -484,13 +336,11 @@ cudaError_t launch_dims(const RecurrentParams& p, int dtype, cudaStream_t stream
     if (grid.x == 0) {
         return cudaSuccess;
     }
-    const int mode = p.decode ? (p.conv_width > 0 ? kModeDecodeConv : kModeDecode)
-                     : p.ckpt_interval > 0 ? kModeCkpt : kModePrefill;
-    const cudaError_t err = dtype == 0 ? launch_mode<DK, DV, NS, float>(mode, grid, p, stream)
-                                       : launch_mode<DK, DV, NS, __nv_bfloat16>(mode, grid, p,
-                                                                                stream);
-    if (err != cudaSuccess) {
-        return err;
+    const int mode = p.decode ? kModeDecode : p.ckpt_interval > 0 ? kModeCkpt : kModePrefill;
+    if (dtype == 0) {
+        launch_mode<DK, DV, NS, float>(mode, grid, p, stream);
+    } else {
+        launch_mode<DK, DV, NS, __nv_bfloat16>(mode, grid, p, stream);
     }
     return cudaGetLastError();
 }

@@ -90,24 +90,42 @@ struct ChanVec {
 };
 
 template <int VEC>
-__device__ __forceinline__ bool chan_vec(const ShortConvParams& p, int gv, ChanVec* cv) {
-    const int vq = p.H * p.d_k / VEC;
-    const int vv = p.H * p.d_v / VEC;
+__device__ __forceinline__ bool chan_vec(int H, int d_k, int d_v, int gv, ChanVec* cv) {
+    const int vq = H * d_k / VEC;
+    const int vv = H * d_v / VEC;
     int lin = gv;
     if (lin < vq) {
-        cv->tensor = 0; cv->d = p.d_k;
+        cv->tensor = 0; cv->d = d_k;
     } else if (lin < 2 * vq) {
-        lin -= vq; cv->tensor = 1; cv->d = p.d_k;
+        lin -= vq; cv->tensor = 1; cv->d = d_k;
     } else if (lin < 2 * vq + vv) {
-        lin -= 2 * vq; cv->tensor = 2; cv->d = p.d_v;
+        lin -= 2 * vq; cv->tensor = 2; cv->d = d_v;
     } else {
         return false;
     }
     const int per_head = cv->d / VEC;
     cv->h = lin / per_head;
     cv->c0 = (lin % per_head) * VEC;
-    cv->off = (cv->tensor == 0 ? 0 : cv->tensor == 1 ? p.d_k : 2 * p.d_k) + cv->c0;
+    cv->off = (cv->tensor == 0 ? 0 : cv->tensor == 1 ? d_k : 2 * d_k) + cv->c0;
     return true;
+}
+
+// The taps of VEC consecutive channels, w[h][off + i][j] (VEC * W contiguous
+// floats, 16-byte aligned when W = 4), as wt[j][i].
+template <int VEC, int W>
+__device__ __forceinline__ void load_taps(const float* wbase, float (&wt)[W][VEC]) {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+        if constexpr (W == 4) {
+            const float4 t = __ldg(reinterpret_cast<const float4*>(wbase) + i);
+            wt[0][i] = t.x; wt[1][i] = t.y; wt[2][i] = t.z; wt[3][i] = t.w;
+        } else {
+#pragma unroll
+            for (int j = 0; j < W; ++j) {
+                wt[j][i] = __ldg(wbase + i * W + j);
+            }
+        }
+    }
 }
 
 __device__ __forceinline__ void seq_bounds(const ShortConvParams& p, int n, int64_t* bos,
@@ -148,7 +166,7 @@ short_conv_kernel(const ShortConvParams p, int n_token_blocks) {
     constexpr int EB = sizeof(T);
 
     ChanVec cv;
-    if (!chan_vec<VEC>(p, blockIdx.y * kConvThreads + threadIdx.x, &cv)) {
+    if (!chan_vec<VEC>(p.H, p.d_k, p.d_v, blockIdx.y * kConvThreads + threadIdx.x, &cv)) {
         return;
     }
     const int Cc = 2 * p.d_k + p.d_v;
@@ -186,23 +204,8 @@ short_conv_kernel(const ShortConvParams p, int n_token_blocks) {
     const int64_t t0 = (int64_t)blockIdx.x * kConvTB;
     const int64_t t1 = min((int64_t)p.total_T, t0 + kConvTB);
 
-    // taps of this vector's channels, w[h][off + i][j]: VEC * W contiguous
-    // floats, read as 16-byte vectors when W = 4 (the weights are 16-byte
-    // aligned and off is a multiple of VEC)
     float wt[W][VEC];
-    const float* wbase = p.w + ((size_t)cv.h * Cc + cv.off) * W;
-#pragma unroll
-    for (int i = 0; i < VEC; ++i) {
-        if constexpr (W == 4) {
-            const float4 t = __ldg(reinterpret_cast<const float4*>(wbase) + i);
-            wt[0][i] = t.x; wt[1][i] = t.y; wt[2][i] = t.z; wt[3][i] = t.w;
-        } else {
-#pragma unroll
-            for (int j = 0; j < W; ++j) {
-                wt[j][i] = __ldg(wbase + i * W + j);
-            }
-        }
-    }
+    load_taps<VEC, W>(p.w + ((size_t)cv.h * Cc + cv.off) * W, wt);
 
     int n = seq_of(p, t0);
     int64_t bos, eos;
@@ -317,7 +320,109 @@ cudaError_t launch_typed(const ShortConvParams& p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// One decode token per batch row: thread = one 8-byte channel vector of one
+// tensor of row b (grid y = b).  It reads the vector's W-1 conv-state rows
+// and the token, writes the convolved vector to y and the shifted rows back
+// in place; no other thread touches those channels of that row.
+template <typename T, int W, bool kSilu>
+__global__ void __launch_bounds__(kConvThreads)
+short_conv_decode_kernel(const ShortConvDecodeParams p) {
+    using VT = VecTraits<T>;
+    constexpr int VEC = VT::kN;
+    constexpr int R = W - 1;
+    constexpr int EB = sizeof(T);
+    ChanVec cv;
+    if (!chan_vec<VEC>(p.H, p.d_k, p.d_v, blockIdx.x * kConvThreads + threadIdx.x, &cv)) {
+        return;
+    }
+    const int b = blockIdx.y;
+    const int slot = p.slots ? p.slots[b] : b;
+    if (slot < 0 || slot >= p.pool_size) {
+        return;
+    }
+    const int Cc = 2 * p.d_k + p.d_v;
+    const void* x = cv.tensor == 0 ? p.x[0] : cv.tensor == 1 ? p.x[1] : p.x[2];
+    void* y = cv.tensor == 0 ? p.y[0] : cv.tensor == 1 ? p.y[1] : p.y[2];
+    const size_t xo = ((size_t)b * p.H + cv.h) * cv.d + cv.c0;
+    char* rows = R > 0 ? static_cast<char*>(p.state) +
+                             ((((size_t)slot * p.H + cv.h) * R) * Cc + cv.off) * EB
+                       : nullptr;
+    const size_t row_bytes = (size_t)Cc * EB;
+
+    uint2 raw[R > 0 ? R : 1];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        raw[r] = *reinterpret_cast<const uint2*>(rows + r * row_bytes);
+    }
+    const uint2 xr = ld8(x, xo, EB);
+    float wt[W][VEC];
+    load_taps<VEC, W>(p.w + ((size_t)cv.h * Cc + cv.off) * W, wt);
+
+    float cur[VEC], out[VEC];
+    VT::unpack(xr, cur);
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) {
+        out[c] = wt[R][c] * cur[c];
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        float prev[VEC];
+        VT::unpack(raw[r], prev);
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) {
+            out[c] = fmaf(wt[r][c], prev[c], out[c]);
+        }
+    }
+    if constexpr (kSilu) {
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) {
+            out[c] = silu_f(out[c]);
+        }
+    }
+    *reinterpret_cast<uint2*>(static_cast<char*>(y) + xo * EB) = VT::pack(out);
+    // shift: row r takes row r + 1, the last row takes the token
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        *reinterpret_cast<uint2*>(rows + r * row_bytes) = r + 1 < R ? raw[r + 1 < R ? r + 1 : 0] : xr;
+    }
+}
+
+template <typename T, bool kSilu>
+void launch_decode_width(const ShortConvDecodeParams& p, dim3 grid, cudaStream_t stream) {
+    switch (p.W) {
+        case 1: short_conv_decode_kernel<T, 1, kSilu><<<grid, kConvThreads, 0, stream>>>(p); break;
+        case 2: short_conv_decode_kernel<T, 2, kSilu><<<grid, kConvThreads, 0, stream>>>(p); break;
+        case 3: short_conv_decode_kernel<T, 3, kSilu><<<grid, kConvThreads, 0, stream>>>(p); break;
+        default: short_conv_decode_kernel<T, 4, kSilu><<<grid, kConvThreads, 0, stream>>>(p); break;
+    }
+}
+
+template <typename T>
+cudaError_t launch_decode_typed(const ShortConvDecodeParams& p, cudaStream_t stream) {
+    constexpr int VEC = VecTraits<T>::kN;
+    const int64_t vecs = (int64_t)p.H * (2 * p.d_k + p.d_v) / VEC;
+    if (p.B == 0 || vecs == 0) {
+        return cudaSuccess;
+    }
+    if (p.B > 65535 || p.W < 1 || p.W > 4) {
+        return cudaErrorInvalidValue;
+    }
+    const dim3 grid((unsigned)((vecs + kConvThreads - 1) / kConvThreads), (unsigned)p.B);
+    if (p.silu) {
+        launch_decode_width<T, true>(p, grid, stream);
+    } else {
+        launch_decode_width<T, false>(p, grid, stream);
+    }
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_short_conv_decode(const ShortConvDecodeParams& p, int dtype,
+                                     cudaStream_t stream) {
+    return dtype == 0 ? launch_decode_typed<float>(p, stream)
+                      : launch_decode_typed<__nv_bfloat16>(p, stream);
+}
 
 cudaError_t launch_short_conv(const ShortConvParams& p, int dtype, cudaStream_t stream) {
     return dtype == 0 ? launch_typed<float>(p, stream) : launch_typed<__nv_bfloat16>(p, stream);

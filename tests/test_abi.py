@@ -265,14 +265,15 @@ def _call_decode_conv(L, **over):
     a = dict(q=BASE, k=BASE + 0x100000, v=BASE + 0x200000, z=BASE + 0x300000,
              beta=BASE + 0x400000, A=BASE + 0x500000, state=BASE + 0x600000, slots=None,
              pool=4, w=BASE + 0x800000, cs=BASE + 0x900000, W=4, B=4, H=2, dk=128, dv=128,
-             dt=kda.KDA_BF16, scale=1.0, flags=1, o=BASE + 0x700000)
+             dt=kda.KDA_BF16, scale=1.0, flags=1, o=BASE + 0x700000, ws=BASE + 0xa00000,
+             ws_bytes=1 << 20)
     a.update(over)
     vp = ctypes.c_void_p
     return L.kda_decode_step_conv(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["z"]),
                                   vp(a["beta"]), vp(a["A"]), vp(a["state"]), vp(a["slots"]),
                                   a["pool"], vp(a["w"]), vp(a["cs"]), a["W"], a["B"], a["H"],
                                   a["dk"], a["dv"], a["dt"], a["scale"], a["flags"], vp(a["o"]),
-                                  None)
+                                  vp(a["ws"]), a["ws_bytes"], None)
 
 
 @pytest.mark.parametrize("over,expect", [
@@ -286,8 +287,20 @@ def _call_decode_conv(L, **over):
     (dict(pool=2), kda.KDA_ERR_INVALID_ARG),
     (dict(w=BASE + 0x800002), kda.KDA_ERR_ALIGNMENT),
     (dict(w=BASE + 0x800008), kda.KDA_ERR_ALIGNMENT),
-    (dict(cs=BASE + 0x900001), kda.KDA_ERR_ALIGNMENT),
+    (dict(cs=BASE + 0x900008), kda.KDA_ERR_ALIGNMENT),
+    (dict(ws=None), kda.KDA_ERR_WORKSPACE),
+    (dict(ws_bytes=1024), kda.KDA_ERR_WORKSPACE),     # 3 x 4 x 2 x 128 bf16 = 6 KB needed
+    (dict(ws=BASE + 0xa00008), kda.KDA_ERR_ALIGNMENT),
+    (dict(ws=BASE + 0x700100), kda.KDA_ERR_INVALID_ARG),   # workspace overlapping o
+    (dict(B=70000, pool=70000), kda.KDA_ERR_UNSUPPORTED),
     (dict(B=0, flags=1 | 4 | 8), kda.KDA_OK),          # nothing to do, nothing launched
 ])
 def test_decode_conv_validation(L, over, expect):
     assert _call_decode_conv(L, **over) == expect
+
+
+def test_decode_conv_workspace_bytes(L):
+    f = L.kda_decode_conv_workspace_bytes
+    assert f(4, 2, 128, 128, kda.KDA_BF16) == 3 * 4 * 2 * 128 * 2
+    assert f(3, 1, 32, 64, kda.KDA_F32) == 512 + 512 + 768     # each part rounded up to 256 B
+    assert f(-1, 2, 128, 128, kda.KDA_BF16) == 0

@@ -1,7 +1,7 @@
 """GPU parity of the short convolutions and their persistent conv state
 against the fp64 oracle, through the C ABI: kda_short_conv alone, short conv
-followed by kda_prefill, kda_decode_step_conv (conv fused into the decode
-step), and prefill handing both states to decode.
+followed by kda_prefill, kda_decode_step_conv (the token's convolutions, then
+the decode step), and prefill handing both states to decode.
 
 Bars: the convolved tensors within their storage rounding (bf16: 2^-8 of
 each value, plus 1e-5 of the tensor's largest value for fp32 accumulation;
@@ -145,8 +145,7 @@ def _decode_case(oracle_mod, dtype, d, W, silu, softplus, seed):
 
 @pytest.mark.parametrize("W,silu", [(4, True), (2, False), (1, True)])
 def test_decode_conv_bf16_d128(oracle_mod, W, silu):
-    """d_v = 128: the head's two column-split CTAs run as one cluster and
-    share the q / k conv rows."""
+    """d_v = 128 (the decode step's two column-split CTAs per head)."""
     _decode_case(oracle_mod, torch.bfloat16, 128, W, silu, False, seed=330 + W)
 
 
