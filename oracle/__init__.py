@@ -11,7 +11,8 @@ Sources (page titles and sections):
     family": the delta-rule recurrence with o_t = S_t^T q_t, the bounded gate
     g = -5 sigmoid(e^A z), alpha = e^g, and Q/K normalisation inside the op;
     the short convolutions before it and their persistent conv state (the
-    prefill and decode bullets of the same section).
+    prefill and decode bullets of the same section); and the gradients of a
+    loss through the recurrence (reverse mode, for the training form).
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against closed
 forms, brute force and invariants that do not reuse this code.
@@ -79,6 +80,11 @@ def _load():
             lib.kda_oracle_short_conv.argtypes = [
                 dp, ctypes.c_int64, ctypes.c_int64, ctypes.POINTER(ctypes.c_int64), ctypes.c_int,
                 dp, ctypes.c_int, dp, ctypes.c_int, dp, dp]
+            lib.kda_oracle_backward.restype = ctypes.c_int
+            lib.kda_oracle_backward.argtypes = [
+                dp, dp, dp, dp, dp, dp, dp, ctypes.POINTER(ctypes.c_int64), ctypes.c_int,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
+                ctypes.c_double, dp, dp, dp, dp, dp, dp, dp, dp, dp, ctypes.c_int]
             lib.kda_oracle_gate_vec.restype = None
             lib.kda_oracle_gate_vec.argtypes = [dp, ctypes.c_int64, ctypes.c_double, dp]
             _lib = lib
@@ -304,3 +310,39 @@ def kda_reference_conv(q, k, v, z, beta, A, conv_w, conv_state=None, initial_sta
                             l2norm=l2norm, eps=eps, softplus_gate=softplus_gate,
                             nthreads=nthreads)
     return o, S, cs
+
+
+def kda_reference_backward(q, k, v, z, beta, A, initial_state=None, cu_seqlens=None, dO=None,
+                           dS_final=None, scale: float = 1.0, l2norm: bool = True,
+                           eps: float = EPS, softplus_gate: bool = False, nthreads: int = 0):
+    """Gradients of L = sum(dO * o) + sum(dS_final * S_T) with respect to every
+    input of kda_reference (reverse mode of the recurrent form, fp64).
+
+    Layouts as kda_reference (packed); dO [total_T, H, d_v]; dS_final
+    [N, H, d_k, d_v] or None.  Returns a dict with dq, dk, dz [total_T, H, d_k],
+    dv [total_T, H, d_v], dbeta [total_T, H], dA [H], dS0 [N, H, d_k, d_v]."""
+    lib = _load()
+    q, k, v, z, beta, A = (_f64(t) for t in (q, k, v, z, beta, A))
+    total_T, H, dk = q.shape
+    dv = v.shape[-1]
+    cu = _cu(cu_seqlens, total_T)
+    N = cu.size - 1
+    S0 = _f64(initial_state)
+    dO = _f64(dO)
+    dSf = _f64(dS_final)
+    if dO is None or dO.shape != (total_T, H, dv):
+        raise ValueError("dO must be [total_T, H, d_v]")
+    out = dict(dq=np.empty((total_T, H, dk)), dk=np.empty((total_T, H, dk)),
+               dv=np.empty((total_T, H, dv)), dz=np.empty((total_T, H, dk)),
+               dbeta=np.empty((total_T, H)), dS0=np.empty((N, H, dk, dv)))
+    gA = np.empty((N, H))
+    rc = lib.kda_oracle_backward(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(S0),
+        _ptr(cu, ctypes.c_int64), N, H, dk, dv, float(scale),
+        int(bool(l2norm)) | (2 if softplus_gate else 0), float(eps), _ptr(dO), _ptr(dSf),
+        _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dz"]),
+        _ptr(out["dbeta"]), _ptr(gA), _ptr(out["dS0"]), int(nthreads))
+    if rc <= 0:
+        raise RuntimeError(f"oracle backward failed with status {rc}")
+    out["dA"] = gA.sum(axis=0)
+    return out

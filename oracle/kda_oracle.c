@@ -40,6 +40,10 @@
  *                           reciprocal rescaling.
  * Both are fp64 throughout; every input arrives already converted exactly
  * from its stored bf16/fp32 value.
+ *
+ * kda_oracle_backward is reverse mode of the token loop (the gradients of a
+ * loss through every step, in reverse), kda_oracle_short_conv the short
+ * convolutions that precede the step.
  */
 #include <math.h>
 #include <pthread.h>
@@ -125,6 +129,17 @@ typedef struct {
     const int64_t* ckpt_base;    /* [N]: index of each sequence's first checkpoint */
     double* ckpt;                /* [n_checkpoints, H, dk, dv] */
     int64_t n_units;
+    /* reverse mode (kda_oracle_backward): upstream gradients in, gradients out */
+    int backward;
+    const double* dO;     /* [total_T, H, dv] */
+    const double* dSf;    /* [N, H, dk, dv] or NULL */
+    double* gq;           /* [total_T, H, dk] */
+    double* gk;
+    double* gv;           /* [total_T, H, dv] */
+    double* gz;           /* [total_T, H, dk] */
+    double* gbeta;        /* [total_T, H] */
+    double* gA_part;      /* [N, H]: this pair's share of dL/dA_h */
+    double* gS0;          /* [N, H, dk, dv] */
     int64_t next;         /* work counter, guarded by mu */
     pthread_mutex_t mu;
     int failed;
@@ -314,6 +329,198 @@ static int oracle_unit_chunked(oracle_job* J, int n, int h)
     return 0;
 }
 
+/* ---- reverse mode of the recurrent form: one (sequence, head) pair ------
+ * Given dL/do_t for every token and dL/dS_T, the gradients of L with respect
+ * to q, k, v, z, beta, A (this pair's share) and S_0, by the chain rule taken
+ * through the forward steps in reverse order.  With G = dL/dS_t:
+ *   o_t = S_t^T qh          G += qh do^T;          dqh = S_t do
+ *   S_t = S' + kh u^T       du = G^T kh;           dkh = G u;      dS' = G
+ *   u = b (v - S'^T kh)     dv = b du;  db = du . (v - S'^T kh);
+ *                           dS' -= b kh du^T;      dkh -= b S' du
+ *   S' = Diag(a) S_{t-1}    da[c] = sum_j dS'[c][j] S_{t-1}[c][j];  G = Diag(a) dS'
+ * then through the gate (a = e^g, x = e^A z; g = -5 sigma(x): dx = da a (-5)
+ * sigma(x) (1 - sigma(x)); g = -softplus(x), a = sigma(-x): dx = -da a (1 - a);
+ * dz = dx e^A, dA += dx x) and the normalisation (xh = m rho x with rho =
+ * (sum x^2 + eps)^(-1/2): dx = m (rho dxh - rho^3 (x . dxh) x)).  The forward
+ * pass keeps every state S_0 .. S_T of the pair. */
+static void oracle_normalise_backward(const double* x, const double* dxh, int d, int l2norm,
+                                      double eps, double mult, double* dx)
+{
+    if (!l2norm) {
+        for (int c = 0; c < d; ++c) {
+            dx[c] = mult * dxh[c];
+        }
+        return;
+    }
+    double ss = 0.0, xd = 0.0;
+    for (int c = 0; c < d; ++c) {
+        ss += x[c] * x[c];
+        xd += x[c] * dxh[c];
+    }
+    const double rho = 1.0 / sqrt(ss + eps);
+    for (int c = 0; c < d; ++c) {
+        dx[c] = mult * (rho * dxh[c] - rho * rho * rho * xd * x[c]);
+    }
+}
+
+static int oracle_unit_backward(oracle_job* J, int n, int h)
+{
+    const int dk = J->dk, dv = J->dv, H = J->H;
+    const int64_t bos = J->cu[n], T = J->cu[n + 1] - bos;
+    const size_t SS = (size_t)dk * dv;
+    double* Sall = (double*)malloc(sizeof(double) * SS * (size_t)(T + 1));
+    double* qh = (double*)malloc(sizeof(double) * dk * (size_t)(T > 0 ? T : 1));
+    double* kh = (double*)malloc(sizeof(double) * dk * (size_t)(T > 0 ? T : 1));
+    double* al = (double*)malloc(sizeof(double) * dk * (size_t)(T > 0 ? T : 1));
+    double* uu = (double*)malloc(sizeof(double) * dv * (size_t)(T > 0 ? T : 1));
+    double* G = (double*)malloc(sizeof(double) * SS);
+    double* Sp = (double*)malloc(sizeof(double) * SS);
+    double* du = (double*)malloc(sizeof(double) * dv);
+    double* dqh = (double*)malloc(sizeof(double) * dk);
+    double* dkh = (double*)malloc(sizeof(double) * dk);
+    double* da = (double*)malloc(sizeof(double) * dk);
+    if (!Sall || !qh || !kh || !al || !uu || !G || !Sp || !du || !dqh || !dkh || !da) {
+        free(Sall); free(qh); free(kh); free(al); free(uu); free(G); free(Sp);
+        free(du); free(dqh); free(dkh); free(da);
+        return -1;
+    }
+    const double eA = exp(J->A[h]);
+    /* forward, keeping S_0 .. S_T */
+    if (J->S0) {
+        memcpy(Sall, J->S0 + ((size_t)n * H + h) * SS, sizeof(double) * SS);
+    } else {
+        memset(Sall, 0, sizeof(double) * SS);
+    }
+    for (int64_t i = 0; i < T; ++i) {
+        const int64_t t = bos + i;
+        const size_t rowk = ((size_t)t * H + h) * dk, rowv = ((size_t)t * H + h) * dv;
+        oracle_normalise(J->q + rowk, dk, J->l2norm, J->eps, J->scale, qh + i * dk);
+        oracle_normalise(J->k + rowk, dk, J->l2norm, J->eps, 1.0, kh + i * dk);
+        for (int c = 0; c < dk; ++c) {
+            const double x = eA * J->z[rowk + c];
+            al[i * dk + c] = exp(J->softplus ? oracle_neg_softplus(x)
+                                             : KDA_ORACLE_GMIN * oracle_sigmoid(x));
+        }
+        const double b = J->beta[(size_t)t * H + h];
+        const double* Sprev = Sall + (size_t)i * SS;
+        double* Snext = Sall + (size_t)(i + 1) * SS;
+        for (int c = 0; c < dk; ++c) {
+            for (int j = 0; j < dv; ++j) {
+                Snext[(size_t)c * dv + j] = al[i * dk + c] * Sprev[(size_t)c * dv + j];
+            }
+        }
+        for (int j = 0; j < dv; ++j) {
+            double r = 0.0;
+            for (int c = 0; c < dk; ++c) {
+                r += Snext[(size_t)c * dv + j] * kh[i * dk + c];
+            }
+            uu[i * dv + j] = b * (J->v[rowv + j] - r);
+        }
+        for (int c = 0; c < dk; ++c) {
+            for (int j = 0; j < dv; ++j) {
+                Snext[(size_t)c * dv + j] += kh[i * dk + c] * uu[i * dv + j];
+            }
+        }
+    }
+    /* reverse */
+    if (J->dSf) {
+        memcpy(G, J->dSf + ((size_t)n * H + h) * SS, sizeof(double) * SS);
+    } else {
+        memset(G, 0, sizeof(double) * SS);
+    }
+    double gA = 0.0;
+    for (int64_t i = T - 1; i >= 0; --i) {
+        const int64_t t = bos + i;
+        const size_t rowk = ((size_t)t * H + h) * dk, rowv = ((size_t)t * H + h) * dv;
+        const double* dO = J->dO + rowv;
+        const double* Sprev = Sall + (size_t)i * SS;
+        const double* St = Sall + (size_t)(i + 1) * SS;
+        const double* q_ = qh + i * dk;
+        const double* k_ = kh + i * dk;
+        const double* a_ = al + i * dk;
+        const double* u_ = uu + i * dv;
+        const double b = J->beta[(size_t)t * H + h];
+        /* o_t = S_t^T qh */
+        for (int c = 0; c < dk; ++c) {
+            double acc = 0.0;
+            for (int j = 0; j < dv; ++j) {
+                G[(size_t)c * dv + j] += q_[c] * dO[j];
+                acc += St[(size_t)c * dv + j] * dO[j];
+            }
+            dqh[c] = acc;
+        }
+        /* S_t = S' + kh u^T */
+        for (int j = 0; j < dv; ++j) {
+            double acc = 0.0;
+            for (int c = 0; c < dk; ++c) {
+                acc += G[(size_t)c * dv + j] * k_[c];
+            }
+            du[j] = acc;
+        }
+        for (int c = 0; c < dk; ++c) {
+            double acc = 0.0;
+            for (int j = 0; j < dv; ++j) {
+                acc += G[(size_t)c * dv + j] * u_[j];
+            }
+            dkh[c] = acc;
+        }
+        /* u = b (v - S'^T kh) */
+        for (int c = 0; c < dk; ++c) {
+            for (int j = 0; j < dv; ++j) {
+                Sp[(size_t)c * dv + j] = a_[c] * Sprev[(size_t)c * dv + j];
+            }
+        }
+        double db = 0.0;
+        for (int j = 0; j < dv; ++j) {
+            double r = 0.0;
+            for (int c = 0; c < dk; ++c) {
+                r += Sp[(size_t)c * dv + j] * k_[c];
+            }
+            J->gv[rowv + j] = b * du[j];
+            db += du[j] * (J->v[rowv + j] - r);
+        }
+        J->gbeta[(size_t)t * H + h] = db;
+        for (int c = 0; c < dk; ++c) {
+            double acc = 0.0;
+            for (int j = 0; j < dv; ++j) {
+                G[(size_t)c * dv + j] -= b * k_[c] * du[j];
+                acc += Sp[(size_t)c * dv + j] * du[j];
+            }
+            dkh[c] -= b * acc;
+        }
+        /* S' = Diag(a) S_{t-1} */
+        for (int c = 0; c < dk; ++c) {
+            double acc = 0.0;
+            for (int j = 0; j < dv; ++j) {
+                acc += G[(size_t)c * dv + j] * Sprev[(size_t)c * dv + j];
+                G[(size_t)c * dv + j] *= a_[c];
+            }
+            da[c] = acc;
+        }
+        /* gate and normalisation */
+        for (int c = 0; c < dk; ++c) {
+            const double x = eA * J->z[rowk + c];
+            double dx;
+            if (J->softplus) {
+                dx = -da[c] * a_[c] * (1.0 - a_[c]);
+            } else {
+                const double sg = oracle_sigmoid(x);
+                dx = da[c] * a_[c] * KDA_ORACLE_GMIN * sg * (1.0 - sg);
+            }
+            J->gz[rowk + c] = dx * eA;
+            gA += dx * x;
+        }
+        oracle_normalise_backward(J->q + rowk, dqh, dk, J->l2norm, J->eps, J->scale,
+                                  J->gq + rowk);
+        oracle_normalise_backward(J->k + rowk, dkh, dk, J->l2norm, J->eps, 1.0, J->gk + rowk);
+    }
+    memcpy(J->gS0 + ((size_t)n * H + h) * SS, G, sizeof(double) * SS);
+    J->gA_part[(size_t)n * H + h] = gA;
+    free(Sall); free(qh); free(kh); free(al); free(uu); free(G); free(Sp);
+    free(du); free(dqh); free(dkh); free(da);
+    return 0;
+}
+
 static void* oracle_worker(void* arg)
 {
     oracle_job* J = (oracle_job*)arg;
@@ -333,7 +540,9 @@ static void* oracle_worker(void* arg)
             n = (int)(w / J->H);
             h = (int)(w % J->H);
         }
-        const int rc = J->chunk > 0 ? oracle_unit_chunked(J, n, h) : oracle_unit_recurrent(J, n, h);
+        const int rc = J->backward ? oracle_unit_backward(J, n, h)
+                       : J->chunk > 0 ? oracle_unit_chunked(J, n, h)
+                                      : oracle_unit_recurrent(J, n, h);
         if (rc != 0) {
             pthread_mutex_lock(&J->mu);
             J->failed = 1;
@@ -485,4 +694,32 @@ int kda_oracle_short_conv(const double* x, int64_t total_T, int64_t C,
         }
     }
     return 0;
+}
+
+/* Gradients of L = sum_t do_t . o_t + dSf . S_T (reverse mode of the
+ * recurrent form, oracle_unit_backward) for every (sequence, head) pair:
+ * gq, gk, gz [total_T, H, dk]; gv [total_T, H, dv]; gbeta [total_T, H];
+ * gA_part [N, H] (dL/dA_h is the sum over n); gS0 [N, H, dk, dv].
+ * `flags` as kda_oracle_run's `l2norm` (bit 0 normalise, bit 1 softplus
+ * gate); dSf may be NULL (zero).  Returns the threads used or a negative
+ * value on error. */
+int kda_oracle_backward(const double* q, const double* k, const double* v, const double* z,
+                        const double* beta, const double* A, const double* S0,
+                        const int64_t* cu_seqlens, int N, int H, int dk, int dv,
+                        double scale, int flags, double eps, const double* dO,
+                        const double* dSf, double* gq, double* gk, double* gv, double* gz,
+                        double* gbeta, double* gA_part, double* gS0, int nthreads)
+{
+    if (!dO || !gq || !gk || !gv || !gz || !gbeta || !gA_part || !gS0) {
+        return -1;
+    }
+    oracle_job J;
+    memset(&J, 0, sizeof(J));
+    J.q = q; J.k = k; J.v = v; J.z = z; J.beta = beta; J.A = A; J.S0 = S0;
+    J.cu = cu_seqlens; J.N = N; J.H = H; J.dk = dk; J.dv = dv;
+    J.scale = scale; J.eps = eps; J.l2norm = flags & 1; J.softplus = (flags >> 1) & 1;
+    J.backward = 1; J.dO = dO; J.dSf = dSf;
+    J.gq = gq; J.gk = gk; J.gv = gv; J.gz = gz; J.gbeta = gbeta; J.gA_part = gA_part;
+    J.gS0 = gS0;
+    return oracle_run(&J, nthreads);
 }

@@ -528,3 +528,94 @@ def test_conv_kda_prefill_equals_decode_steps(oracle_mod):
     # and the convolution really acts: without it the output differs
     o_plain, _, _ = oracle_mod.kda_reference(q, k, v, z, beta, A, S0)
     assert not _close(o_plain, o, 1e-3)
+
+
+# ------------------------------------------- reverse mode (training backward)
+def _loss(oracle_mod, dO, dSf, cu, flags, **x):
+    o, S, _ = oracle_mod.kda_reference(x["q"], x["k"], x["v"], x["z"], x["beta"], x["A"],
+                                       x["S0"], cu, **flags)
+    return float((o * dO).sum() + (0.0 if dSf is None else (S * dSf).sum()))
+
+
+@pytest.mark.parametrize("softplus,l2norm,with_state", [(False, True, True), (True, True, False),
+                                                        (False, False, True)])
+def test_backward_matches_finite_differences(oracle_mod, softplus, l2norm, with_state):
+    """Directional derivatives of L = sum(dO * o) + sum(dSf * S_T), taken by
+    central differences of the forward oracle (step 1e-6 in fp64), equal the
+    reverse-mode gradients contracted with the same directions, for every
+    input; varlen with an empty sequence."""
+    rng = np.random.default_rng(500 + 2 * softplus + l2norm)
+    lens = [5, 0, 3]
+    T, H, dk, dv = sum(lens), 2, 4, 3
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    q, k, v, z, beta, A, S0 = _rand_case(rng, T, H, dk, dv, N=len(lens), zscale=2.0)
+    if not with_state:
+        S0 = None
+    dO = rng.standard_normal((T, H, dv))
+    dSf = rng.standard_normal((len(lens), H, dk, dv)) if with_state else None
+    flags = dict(softplus_gate=softplus, l2norm=l2norm, scale=0.7)
+    g = oracle_mod.kda_reference_backward(q, k, v, z, beta, A, S0, cu, dO, dSf, **flags)
+    x = dict(q=q, k=k, v=v, z=z, beta=beta, A=A, S0=S0)
+    keys = dict(q="dq", k="dk", v="dv", z="dz", beta="dbeta", A="dA", S0="dS0")
+    eps = 1e-6
+    for name, key in keys.items():
+        if x[name] is None:
+            continue
+        d = rng.standard_normal(x[name].shape)
+        xp, xm = dict(x), dict(x)
+        xp[name] = x[name] + eps * d
+        xm[name] = x[name] - eps * d
+        fd = (_loss(oracle_mod, dO, dSf, cu, flags, **xp) -
+              _loss(oracle_mod, dO, dSf, cu, flags, **xm)) / (2 * eps)
+        an = float((g[key] * d).sum())
+        assert abs(fd - an) <= 1e-7 * max(1.0, abs(an)), (name, fd, an)
+
+
+def test_backward_matches_autograd(oracle_mod):
+    """The reverse-mode gradients equal torch.autograd of a separate fp64
+    torch restatement of the recurrence (gate, normalisation, delta rule,
+    read after write) on one sequence."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(510)
+    T, H, dk, dv = 6, 2, 5, 4
+    q, k, v, z, beta, A, S0 = _rand_case(rng, T, H, dk, dv)
+    dO = rng.standard_normal((T, H, dv))
+    dSf = rng.standard_normal((1, H, dk, dv))
+    g = oracle_mod.kda_reference_backward(q, k, v, z, beta, A, S0, None, dO, dSf, scale=1.3)
+    tt = {n: torch.tensor(a, dtype=torch.float64, requires_grad=True)
+          for n, a in dict(q=q, k=k, v=v, z=z, beta=beta, A=A, S0=S0).items()}
+    L = 0.0
+    for h in range(H):
+        S = tt["S0"][0, h]
+        for t in range(T):
+            qh = 1.3 * tt["q"][t, h] / torch.sqrt((tt["q"][t, h] ** 2).sum() + 1e-6)
+            kh = tt["k"][t, h] / torch.sqrt((tt["k"][t, h] ** 2).sum() + 1e-6)
+            alpha = torch.exp(-5.0 * torch.sigmoid(torch.exp(tt["A"][h]) * tt["z"][t, h]))
+            b = tt["beta"][t, h]
+            Sd = alpha[:, None] * S
+            S = Sd - b * torch.outer(kh, kh @ Sd) + b * torch.outer(kh, tt["v"][t, h])
+            L = L + (S.T @ qh * torch.tensor(dO[t, h])).sum()
+        L = L + (S * torch.tensor(dSf[0, h])).sum()
+    L.backward()
+    for n, key in dict(q="dq", k="dk", v="dv", z="dz", beta="dbeta", A="dA", S0="dS0").items():
+        assert _close(g[key], tt[n].grad.numpy(), 1e-10), n
+
+
+def test_backward_identity_closed_form(oracle_mod):
+    """alpha = 1 (saturated gate), beta = 0: o_t = S0^T qh_t and S_T = S0, so
+    dS0 = sum_t qh_t dO_t^T + dSf, dv = 0, dz = 0, dA = 0, and dqh_t = S0 dO_t
+    (no normalisation here, scale 1)."""
+    rng = np.random.default_rng(520)
+    T, H, dk, dv = 4, 1, 3, 2
+    q, k, v, _, _, _, S0 = _rand_case(rng, T, H, dk, dv)
+    z = np.full((T, H, dk), -1e4)
+    A = np.zeros(H)
+    beta = np.zeros((T, H))
+    dO = rng.standard_normal((T, H, dv))
+    dSf = rng.standard_normal((1, H, dk, dv))
+    g = oracle_mod.kda_reference_backward(q, k, v, z, beta, A, S0, None, dO, dSf, l2norm=False)
+    want = dSf[0, 0] + sum(np.outer(q[t, 0], dO[t, 0]) for t in range(T))
+    assert _close(g["dS0"][0, 0], want, 1e-13)
+    assert np.all(g["dv"] == 0.0) and np.all(g["dz"] == 0.0) and g["dA"][0] == 0.0
+    for t in range(T):
+        assert _close(g["dq"][t, 0], S0[0, 0] @ dO[t, 0], 1e-13)
