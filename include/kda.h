@@ -282,6 +282,48 @@ KDA_API size_t kda_decode_conv_workspace_bytes(int32_t B, int32_t H, int32_t d_k
                                                kda_dtype dt);
 
 /*
+ * kda_backward -- gradients of the KDA recurrence for training: given
+ * dL/do for every token and dL/dS_T (optional), the gradients of L with
+ * respect to q, k, v, z, beta, A and the initial state, through the
+ * delta-rule step, the gate (K3's or, with KDA_FLAG_SOFTPLUS_GATE, Kimi
+ * Linear's) and the Q/K normalisation (section 1 of the K3 architecture
+ * page gives the forward step; the backward is its reverse mode).
+ *
+ * Recurrent form, fp32 arithmetic, one CTA per (sequence, head): a forward
+ * pass stores the state at every 64-token chunk start; the chunks are then
+ * walked last to first, each recomputed forward into a scratch and its
+ * tokens walked in reverse.
+ *
+ *  q, k, v, z, beta, A, initial_state, cu_seqlens, cu_seqlens_host, N,
+ *  total_T, H, d_k, d_v, dt, scale: as kda_prefill (the forward's inputs)
+ *  flags       KDA_FLAG_L2NORM_QK, KDA_FLAG_SOFTPLUS_GATE (as the forward)
+ *  dO          [total_T, H, d_v] dt: dL/do
+ *  dS_final    [N, H, d_k, d_v] fp32 or NULL (zero): dL/dS_T
+ *  dq, dk, dz  [total_T, H, d_k] fp32;  dv [total_T, H, d_v] fp32;
+ *  dbeta       [total_T, H] fp32;  dA [H] fp32;  dS0 [N, H, d_k, d_v] fp32
+ *              (written, not accumulated; dS0 is written also when
+ *              initial_state is NULL)
+ *  workspace   kda_backward_workspace_bytes(N, total_T, H, d_k, d_v) bytes,
+ *              16-byte aligned, no initialisation needed
+ * Errors: as kda_prefill (KDA_ERR_WORKSPACE for a short workspace), and
+ * KDA_ERR_INVALID_ARG for a missing gradient buffer.
+ */
+KDA_API int kda_backward(const void* q, const void* k, const void* v, const void* z,
+                         const void* beta, const float* A, const float* initial_state,
+                         const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                         int32_t N, int32_t total_T, int32_t H, int32_t d_k, int32_t d_v,
+                         kda_dtype dt, float scale, uint32_t flags,
+                         const void* dO, const float* dS_final,
+                         float* dq, float* dk, float* dv, float* dz, float* dbeta, float* dA,
+                         float* dS0, void* workspace, size_t workspace_bytes, void* stream);
+
+/* kda_backward_workspace_bytes -- the workspace kda_backward needs: chunk-
+ * start states, a 64-state scratch per (sequence, head), per-pair dA shares
+ * (0 for invalid sizes). */
+KDA_API size_t kda_backward_workspace_bytes(int32_t N, int32_t total_T, int32_t H, int32_t d_k,
+                                            int32_t d_v);
+
+/*
  * kda_state_io -- moves fp32 states of shape [H, d_k, d_v] each (the
  * persistent KDA state that prefill hands to decode).
  *

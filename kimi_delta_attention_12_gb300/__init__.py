@@ -49,6 +49,7 @@ EXPORTED_SYMBOLS = (
     "kda_decode_step", "kda_state_io", "kda_status_string", "kda_version",
     "kda_prefill_noalloc", "kda_prefill_checkpointed", "kda_checkpoint_count",
     "kda_short_conv", "kda_decode_step_conv", "kda_decode_conv_workspace_bytes",
+    "kda_backward", "kda_backward_workspace_bytes",
 )
 
 _lock = threading.Lock()
@@ -108,6 +109,12 @@ def lib() -> ctypes.CDLL:
                                                ctypes.c_float, ctypes.c_uint32, vp, vp, sz, vp]
             L.kda_decode_conv_workspace_bytes.restype = sz
             L.kda_decode_conv_workspace_bytes.argtypes = [i32, i32, i32, i32, ctypes.c_int]
+            L.kda_backward.restype = ctypes.c_int
+            L.kda_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                       i32, ctypes.c_int, ctypes.c_float, ctypes.c_uint32, vp,
+                                       vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+            L.kda_backward_workspace_bytes.restype = sz
+            L.kda_backward_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
             L.kda_checkpoint_count.restype = ctypes.c_int64
             L.kda_checkpoint_count.argtypes = [vp, i32, i32, i32]
             _lib = L
@@ -375,6 +382,57 @@ def kda_decode_step_conv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: t
     if st != KDA_OK:
         raise KDAError(st, "kda_decode_step_conv")
     return o
+
+
+def backward_workspace_bytes(N: int, total_T: int, H: int, d_k: int, d_v: int) -> int:
+    return int(lib().kda_backward_workspace_bytes(N, total_T, H, d_k, d_v))
+
+
+def kda_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: torch.Tensor,
+                 beta: torch.Tensor, A: torch.Tensor, dO: torch.Tensor,
+                 initial_state: Optional[torch.Tensor] = None,
+                 cu_seqlens: Optional[torch.Tensor] = None,
+                 cu_seqlens_host: Optional[torch.Tensor] = None,
+                 dS_final: Optional[torch.Tensor] = None, scale: float = 1.0,
+                 l2norm: bool = True, softplus_gate: bool = False,
+                 workspace: Optional[torch.Tensor] = None,
+                 stream: Optional[torch.cuda.Stream] = None) -> dict:
+    """Gradients of the recurrence (kda_backward in include/kda.h) for packed
+    inputs as kda_prefill takes them; dO [total_T, H, d_v] in the inputs'
+    dtype, dS_final [N, H, d_k, d_v] fp32 or None.  Returns a dict of fp32
+    tensors dq, dk, dz [total_T, H, d_k], dv [total_T, H, d_v],
+    dbeta [total_T, H], dA [H], dS0 [N, H, d_k, d_v]."""
+    N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    total_T, H, d_k = q.shape
+    d_v = v.shape[-1]
+    dt = q.dtype
+    for t in (k, v, z, beta, dO):
+        if t.dtype != dt:
+            raise TypeError("q, k, v, z, beta and dO must share one dtype")
+    _check_cuda(q, k, v, z, beta, A, dO, initial_state, cu_seqlens, dS_final)
+    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    dev = q.device
+    f32 = dict(dtype=torch.float32, device=dev)
+    g = dict(dq=torch.empty(total_T, H, d_k, **f32), dk=torch.empty(total_T, H, d_k, **f32),
+             dv=torch.empty(total_T, H, d_v, **f32), dz=torch.empty(total_T, H, d_k, **f32),
+             dbeta=torch.empty(total_T, H, **f32), dA=torch.empty(H, **f32),
+             dS0=torch.empty(N, H, d_k, d_v, **f32))
+    if workspace is None:
+        workspace = torch.empty(backward_workspace_bytes(N, total_T, H, d_k, d_v),
+                                dtype=torch.uint8, device=dev)
+    host_cu = None if cu_seqlens_host is None else cu_seqlens_host.to(torch.int32).contiguous()
+    host_ptr = None if host_cu is None else ctypes.c_void_p(host_cu.data_ptr())
+    flags = (KDA_FLAG_L2NORM_QK if l2norm else 0) | (KDA_FLAG_SOFTPLUS_GATE if softplus_gate else 0)
+    st = lib().kda_backward(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(initial_state),
+        _ptr(cu_seqlens), host_ptr, N, total_T, H, d_k, d_v, _dtype_code(dt), float(scale),
+        flags, _ptr(dO), _ptr(dS_final), _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]),
+        _ptr(g["dz"]), _ptr(g["dbeta"]), _ptr(g["dA"]), _ptr(g["dS0"]), _ptr(workspace),
+        workspace.numel(), _stream_ptr(stream))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_backward")
+    return g
 
 
 def kda_state_io(op: int, dst: torch.Tensor, src: Optional[torch.Tensor] = None,

@@ -22,7 +22,8 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC]
 SOURCES = ["kda_api.cpp", "kda_recurrent.cu", "kda_state_io.cu", "kda_prefill_sm103.cu",
-           "kda_noalloc.cu", "kda_short_conv.cu"]
+           "kda_noalloc.cu", "kda_short_conv.cu",
+           "kda_backward.cu"]
 
 
 def _nvcc() -> str:

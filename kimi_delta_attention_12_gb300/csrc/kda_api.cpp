@@ -396,6 +396,79 @@ int kda_decode_step_conv(const void* q, const void* k, const void* v, const void
                             stream);
 }
 
+// Backward workspace: chunk-start states, per-pair scratch, per-pair dA.
+static void backward_layout(int32_t N, int32_t total_T, int32_t H, int32_t d_k, int32_t d_v,
+                            size_t* ckpt, size_t* scratch, size_t* part) {
+    const size_t SS = (size_t)d_k * d_v * sizeof(float);
+    *ckpt = round_up(((size_t)total_T / kda::kBwChunk + N) * H * SS, 256);
+    *scratch = round_up((size_t)N * H * kda::kBwChunk * SS, 256);
+    *part = round_up((size_t)N * H * sizeof(float), 256);
+}
+
+size_t kda_backward_workspace_bytes(int32_t N, int32_t total_T, int32_t H, int32_t d_k,
+                                    int32_t d_v) {
+    if (N < 1 || H < 1 || total_T < 0 || !supported_dim(d_k) || !supported_dim(d_v)) return 0;
+    size_t a, b, c;
+    backward_layout(N, total_T, H, d_k, d_v, &a, &b, &c);
+    return a + b + c;
+}
+
+int kda_backward(const void* q, const void* k, const void* v, const void* z,
+                 const void* beta, const float* A, const float* initial_state,
+                 const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                 int32_t N, int32_t total_T, int32_t H, int32_t d_k, int32_t d_v,
+                 kda_dtype dt, float scale, uint32_t flags,
+                 const void* dO, const float* dS_final,
+                 float* dq, float* dk, float* dv, float* dz, float* dbeta, float* dA,
+                 float* dS0, void* workspace, size_t workspace_bytes, void* stream) {
+    if (dt != KDA_F32 && dt != KDA_BF16) return KDA_ERR_UNSUPPORTED;
+    if (!supported_dim(d_k) || !supported_dim(d_v)) return KDA_ERR_UNSUPPORTED;
+    if (N < 1 || H < 1 || total_T < 0) return KDA_ERR_INVALID_ARG;
+    if ((flags & ~(uint32_t)(KDA_FLAG_L2NORM_QK | KDA_FLAG_SOFTPLUS_GATE)) != 0) {
+        return KDA_ERR_INVALID_ARG;
+    }
+    if (!isfinite(scale)) return KDA_ERR_INVALID_ARG;
+    if (!A || !dA || !dS0) return KDA_ERR_INVALID_ARG;
+    if (total_T > 0 && (!q || !k || !v || !z || !beta || !dO || !dq || !dk || !dv || !dz ||
+                        !dbeta)) {
+        return KDA_ERR_INVALID_ARG;
+    }
+    if (!cu_seqlens && total_T % N != 0) return KDA_ERR_INVALID_ARG;
+    if (cu_seqlens_host) {
+        if (cu_seqlens_host[0] != 0 || cu_seqlens_host[N] != total_T) return KDA_ERR_INVALID_ARG;
+        for (int32_t n = 0; n < N; ++n) {
+            if (cu_seqlens_host[n + 1] < cu_seqlens_host[n]) return KDA_ERR_INVALID_ARG;
+        }
+    }
+    size_t wc, wsr, wp;
+    backward_layout(N, total_T, H, d_k, d_v, &wc, &wsr, &wp);
+    if (!workspace || workspace_bytes < wc + wsr + wp) return KDA_ERR_WORKSPACE;
+    const size_t eb = elem_bytes(dt);
+    if (!aligned(q, eb) || !aligned(k, eb) || !aligned(v, eb) || !aligned(z, eb) ||
+        !aligned(beta, eb) || !aligned(dO, eb) || !aligned(A, 4) || !aligned(dq, 4) ||
+        !aligned(dk, 4) || !aligned(dv, 4) || !aligned(dz, 4) || !aligned(dbeta, 4) ||
+        !aligned(dA, 4) || !aligned(initial_state, 16) || !aligned(dS_final, 16) ||
+        !aligned(dS0, 16) || !aligned(cu_seqlens, 4) || !aligned(workspace, 16)) {
+        return KDA_ERR_ALIGNMENT;
+    }
+    kda::BackwardParams p;
+    memset(&p, 0, sizeof(p));
+    p.q = q; p.k = k; p.v = v; p.z = z; p.beta = beta; p.A = A;
+    p.initial_state = initial_state; p.cu_seqlens = cu_seqlens;
+    p.dO = dO; p.dS_final = dS_final;
+    p.dq = dq; p.dk = dk; p.dv = dv; p.dz = dz; p.dbeta = dbeta; p.dA = dA; p.dS0 = dS0;
+    char* ws = static_cast<char*>(workspace);
+    p.ckpt = reinterpret_cast<float*>(ws);
+    p.scratch = reinterpret_cast<float*>(ws + wc);
+    p.dA_part = reinterpret_cast<float*>(ws + wc + wsr);
+    p.N = N; p.total_T = total_T; p.H = H; p.scale = scale;
+    p.l2norm = (flags & KDA_FLAG_L2NORM_QK) ? 1 : 0;
+    p.softplus_gate = (flags & KDA_FLAG_SOFTPLUS_GATE) ? 1 : 0;
+    const cudaError_t err = kda::launch_backward(p, d_k, d_v, dt == KDA_F32 ? 0 : 1,
+                                                 static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 int kda_state_io(kda_state_op op, float* dst, const float* src,
                  const int32_t* slots, int32_t n, int32_t pool_size,
                  int32_t H, int32_t d_k, int32_t d_v, void* stream) {

@@ -1,0 +1,472 @@
+// kda_backward.cu -- gradients of the KDA recurrence (training backward),
+// recurrent form, fp32, for sm_103a.
+//
+// The forward step of "Kimi K3 Open Weights: What Is Actually New In Its 2.8
+// Trillion Parameter Architecture", section 1 (per head, per token):
+//   qh = scale q / |q|, kh = k / |k|,  a = e^g (g = -5 sigmoid(e^A z), or
+//   -softplus(e^A z)),  S' = Diag(a) S_{t-1},  u = b (v - S'^T kh),
+//   S_t = S' + kh u^T,  o_t = S_t^T qh.
+// With G = dL/dS_t carried backwards from dL/dS_T, each token in reverse:
+//   G += qh do^T;  dqh = S_t do;  du = G^T kh;  dkh = G u - b S' du;
+//   dv = b du;  db = du . (v - S'^T kh);  G' = G - b kh du^T;
+//   da[c] = sum_j G'[c][j] S_{t-1}[c][j];  G = Diag(a) G'
+// followed by the gate and normalisation derivatives, written out per token.
+//
+// One CTA per (sequence, head) holds the whole d_k x d_v state and its
+// gradient G in registers (so every sum over the value columns stays inside
+// the CTA).  The reverse pass needs S_{t-1} for every token; phase 1 runs the
+// forward recurrence and stores the state at the start of every 64-token
+// chunk; phase 2 walks the chunks last to first, recomputes each chunk's
+// states forward into a scratch buffer (S_{t-1} of its 64 tokens), then walks
+// its tokens backwards.  The forward recomputation doubles the token-serial
+// work; the scratch keeps memory at 64 states per (sequence, head).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+constexpr int kBwThreads = 256;
+constexpr int kBwWarps = kBwThreads / 32;
+constexpr float kBwGmin = -5.0f;
+constexpr float kBwEps = 1e-6f;
+
+__device__ __forceinline__ float ldf(const float* p, size_t i) { return __ldg(p + i); }
+__device__ __forceinline__ float ldf(const __nv_bfloat16* p, size_t i) {
+    return __bfloat162float(p[i]);
+}
+
+__device__ __forceinline__ float bw_sigmoid(float x) {
+    if (x >= 0.0f) {
+        return 1.0f / (1.0f + expf(-x));
+    }
+    const float e = expf(x);
+    return e / (1.0f + e);
+}
+
+// Sum over the CTA of one value per thread of warps 0 .. nw-1 (the others
+// pass 0); every thread gets the total.  Uses red[kBwWarps] and two barriers.
+__device__ __forceinline__ float block_sum(float x, float* red) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        x += __shfl_xor_sync(0xffffffffu, x, off);
+    }
+    if (lane == 0) {
+        red[w] = x;
+    }
+    __syncthreads();
+    float t = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kBwWarps; ++i) {
+        t += red[i];
+    }
+    __syncthreads();
+    return t;
+}
+
+template <int DK, int DV>
+struct BwShared {
+    float q[DK];        // raw q, k of the token
+    float k[DK];
+    float a[DK];        // decay a = e^g
+    float v[DV];
+    float dO[DV];
+    float u[DV];
+    float du[DV];
+    float red[kBwWarps][2][DV];
+    float nrm[DK / 32][3];
+    float dqh[DK];
+    float dkh[DK];
+    float da[DK];
+    float red1[kBwWarps];
+    float beta;
+};
+
+template <int DK, int DV, typename T>
+__global__ void __launch_bounds__(kBwThreads, 1)
+kda_backward_kernel(const BackwardParams p) {
+    constexpr int LPR = DV / 4;            // lanes per state row (one float4 each)
+    constexpr int RPW = 32 / LPR;          // rows per warp pass
+    constexpr int RSTEP = kBwWarps * RPW;  // rows per CTA pass
+    constexpr int RPT = DK / RSTEP;        // rows per thread
+    constexpr int C = kBwChunk;
+    static_assert(RPT >= 1 && RPT * RSTEP == DK, "bad state tiling");
+    static_assert(DK + DV <= kBwThreads, "token loaders need DK + DV threads");
+
+    __shared__ BwShared<DK, DV> sh;
+
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    const int cg = lane % LPR, rs = lane / LPR;
+    const int h = blockIdx.x % p.H;
+    const int n = blockIdx.x / p.H;
+    const int H = p.H;
+    const T* q = static_cast<const T*>(p.q);
+    const T* k = static_cast<const T*>(p.k);
+    const T* v = static_cast<const T*>(p.v);
+    const T* z = static_cast<const T*>(p.z);
+    const T* beta = static_cast<const T*>(p.beta);
+    const T* dO = static_cast<const T*>(p.dO);
+
+    int64_t bos, eos;
+    if (p.cu_seqlens) {
+        bos = p.cu_seqlens[n];
+        eos = p.cu_seqlens[n + 1];
+    } else {
+        const int64_t len = p.total_T / p.N;
+        bos = (int64_t)n * len;
+        eos = bos + len;
+    }
+    const int64_t len = eos - bos;
+    const int64_t nchunks = (len + C - 1) / C;
+    const size_t SS = (size_t)DK * DV;
+    // this pair's chunk-start states and its chunk scratch
+    float* ckpt = p.ckpt + ((size_t)(bos / C + n) * H + h) * SS;
+    const size_t ckpt_stride = (size_t)H * SS;       // consecutive chunks of the pair
+    float* scratch = p.scratch + ((size_t)n * H + h) * C * SS;
+    const float eA = expf(p.A[h]);
+    const float scale = p.scale;
+
+    auto row_of = [&](int r) { return r * RSTEP + w * RPW + rs; };
+    auto st_idx = [&](int r) { return ((size_t)row_of(r) * DV) / 4 + cg; };   // float4 index
+
+    // ---- one token's inputs into shared memory, and the norm partials ----
+    auto load_token = [&](int64_t t, bool with_do) {
+        const size_t rk = ((size_t)t * H + h) * DK;
+        if (tid < DK) {
+            const float qv = ldf(q, rk + tid), kv = ldf(k, rk + tid), zv = ldf(z, rk + tid);
+            sh.q[tid] = qv;
+            sh.k[tid] = kv;
+            const float sg = bw_sigmoid(p.softplus_gate ? -eA * zv : eA * zv);
+            sh.a[tid] = p.softplus_gate ? sg : expf(kBwGmin * sg);
+            float sq = qv * qv, sk = kv * kv, sqk = qv * kv;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                sq += __shfl_xor_sync(0xffffffffu, sq, off);
+                sk += __shfl_xor_sync(0xffffffffu, sk, off);
+                sqk += __shfl_xor_sync(0xffffffffu, sqk, off);
+            }
+            if (lane == 0) {
+                sh.nrm[w][0] = sq;
+                sh.nrm[w][1] = sk;
+                sh.nrm[w][2] = sqk;
+            }
+        } else if (tid < DK + DV) {
+            const int j = tid - DK;
+            const size_t rv = ((size_t)t * H + h) * DV + j;
+            sh.v[j] = ldf(v, rv);
+            if (with_do) {
+                sh.dO[j] = ldf(dO, rv);
+            }
+            if (j == 0) {
+                sh.beta = ldf(beta, (size_t)t * H + h);
+            }
+        }
+    };
+    struct Norms { float rq, rk, qk; };   // 1/|q|, 1/|k| (or 1), q . k raw
+    auto norms = [&]() {
+        float sq = 0.f, sk = 0.f, sqk = 0.f;
+#pragma unroll
+        for (int i = 0; i < DK / 32; ++i) {
+            sq += sh.nrm[i][0];
+            sk += sh.nrm[i][1];
+            sqk += sh.nrm[i][2];
+        }
+        Norms m;
+        m.rq = p.l2norm ? rsqrtf(sq + kBwEps) : 1.0f;
+        m.rk = p.l2norm ? rsqrtf(sk + kBwEps) : 1.0f;
+        m.qk = sqk;
+        return m;
+    };
+
+    // ---- one forward step on S (registers); token inputs already loaded ----
+    float4 S[RPT];
+    auto forward_step = [&]() {
+        const Norms m = norms();
+        float4 ak = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            const int i = row_of(r);
+            const float a = sh.a[i], kk = sh.k[i];
+            S[r].x *= a; S[r].y *= a; S[r].z *= a; S[r].w *= a;
+            ak.x += kk * S[r].x; ak.y += kk * S[r].y; ak.z += kk * S[r].z; ak.w += kk * S[r].w;
+        }
+#pragma unroll
+        for (int off = LPR; off < 32; off <<= 1) {
+            ak.x += __shfl_xor_sync(0xffffffffu, ak.x, off);
+            ak.y += __shfl_xor_sync(0xffffffffu, ak.y, off);
+            ak.z += __shfl_xor_sync(0xffffffffu, ak.z, off);
+            ak.w += __shfl_xor_sync(0xffffffffu, ak.w, off);
+        }
+        if (rs == 0) {
+            *reinterpret_cast<float4*>(&sh.red[w][0][4 * cg]) = ak;
+        }
+        __syncthreads();
+        if (tid < DV) {
+            float r = 0.f;
+#pragma unroll
+            for (int ww = 0; ww < kBwWarps; ++ww) {
+                r += sh.red[ww][0][tid];
+            }
+            sh.u[tid] = sh.beta * (sh.v[tid] - r * m.rk);
+        }
+        __syncthreads();
+        const float4 u4 = *reinterpret_cast<const float4*>(&sh.u[4 * cg]);
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            const float kk = sh.k[row_of(r)] * m.rk;
+            S[r].x += kk * u4.x; S[r].y += kk * u4.y; S[r].z += kk * u4.z; S[r].w += kk * u4.w;
+        }
+    };
+    auto load_state = [&](const float* src) {
+        const float4* sp = reinterpret_cast<const float4*>(src);
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            S[r] = sp[st_idx(r)];
+        }
+    };
+    auto store_state = [&](float* dst, const float4* X) {
+        float4* dp = reinterpret_cast<float4*>(dst);
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            dp[st_idx(r)] = X[r];
+        }
+    };
+
+    // ---- phase 1: forward, storing the state at every chunk start ----
+    if (p.initial_state) {
+        load_state(p.initial_state + ((size_t)n * H + h) * SS);
+    } else {
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            S[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    for (int64_t i = 0; i < len; ++i) {
+        if (i % C == 0) {
+            store_state(ckpt + (size_t)(i / C) * ckpt_stride, S);
+        }
+        load_token(bos + i, false);
+        __syncthreads();
+        forward_step();
+        __syncthreads();   // the next token's loads overwrite what this one read
+    }
+
+    // ---- phase 2: chunks last to first ----
+    float4 G[RPT];
+    if (p.dS_final) {
+        const float4* gp = reinterpret_cast<const float4*>(p.dS_final + ((size_t)n * H + h) * SS);
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            G[r] = gp[st_idx(r)];
+        }
+    } else {
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            G[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    float dA_acc = 0.0f;   // thread 0: this pair's share of dL/dA_h
+    for (int64_t c = nchunks - 1; c >= 0; --c) {
+        const int64_t i0 = c * C;
+        const int64_t cl = min((int64_t)C, len - i0);
+        // 2a: the chunk's states S_{t-1} into the scratch
+        __syncthreads();
+        load_state(ckpt + (size_t)c * ckpt_stride);
+        for (int64_t j = 0; j < cl; ++j) {
+            store_state(scratch + (size_t)j * SS, S);
+            if (j + 1 == cl) {
+                break;   // the state after the chunk's last token is not needed
+            }
+            load_token(bos + i0 + j, false);
+            __syncthreads();
+            forward_step();
+            __syncthreads();
+        }
+        // 2b: the chunk's tokens in reverse
+        for (int64_t j = cl - 1; j >= 0; --j) {
+            const int64_t t = bos + i0 + j;
+            __syncthreads();   // the scratch stores (and the previous token's reads) are done
+            load_state(scratch + (size_t)j * SS);        // S = S_{t-1}
+            load_token(t, true);
+            __syncthreads();
+            const Norms m = norms();
+            const float qs = m.rq * scale;
+            // column sums: r = S'^T kh and gk = G^T kh (G = dL/dS_t from the future)
+            float4 ar = make_float4(0.f, 0.f, 0.f, 0.f), ag = ar;
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) {
+                const int i = row_of(r);
+                const float a = sh.a[i], kk = sh.k[i] * m.rk;
+                ar.x += kk * a * S[r].x; ar.y += kk * a * S[r].y;
+                ar.z += kk * a * S[r].z; ar.w += kk * a * S[r].w;
+                ag.x += kk * G[r].x; ag.y += kk * G[r].y; ag.z += kk * G[r].z; ag.w += kk * G[r].w;
+            }
+#pragma unroll
+            for (int off = LPR; off < 32; off <<= 1) {
+                ar.x += __shfl_xor_sync(0xffffffffu, ar.x, off);
+                ar.y += __shfl_xor_sync(0xffffffffu, ar.y, off);
+                ar.z += __shfl_xor_sync(0xffffffffu, ar.z, off);
+                ar.w += __shfl_xor_sync(0xffffffffu, ar.w, off);
+                ag.x += __shfl_xor_sync(0xffffffffu, ag.x, off);
+                ag.y += __shfl_xor_sync(0xffffffffu, ag.y, off);
+                ag.z += __shfl_xor_sync(0xffffffffu, ag.z, off);
+                ag.w += __shfl_xor_sync(0xffffffffu, ag.w, off);
+            }
+            if (rs == 0) {
+                *reinterpret_cast<float4*>(&sh.red[w][0][4 * cg]) = ar;
+                *reinterpret_cast<float4*>(&sh.red[w][1][4 * cg]) = ag;
+            }
+            __syncthreads();
+            // per value column: u, du, dv and the column's share of db
+            float dbj = 0.0f;
+            if (tid < DV) {
+                float rr = 0.f, gk = 0.f;
+#pragma unroll
+                for (int ww = 0; ww < kBwWarps; ++ww) {
+                    rr += sh.red[ww][0][tid];
+                    gk += sh.red[ww][1][tid];
+                }
+                const float b = sh.beta;
+                const float wv = sh.v[tid] - rr;                   // v - S'^T kh
+                const float qk = m.qk * m.rk * qs;                 // qh . kh
+                const float duj = gk + qk * sh.dO[tid];
+                sh.u[tid] = b * wv;
+                sh.du[tid] = duj;
+                p.dv[((size_t)t * H + h) * DV + tid] = b * duj;
+                dbj = duj * wv;
+            }
+            const float db = block_sum(dbj, sh.red1);   // two barriers: u, du visible after
+            if (tid == 0) {
+                p.dbeta[(size_t)t * H + h] = db;
+            }
+            // per state row: dqh, dkh, da and the new G
+            const float4 u4 = *reinterpret_cast<const float4*>(&sh.u[4 * cg]);
+            const float4 du4 = *reinterpret_cast<const float4*>(&sh.du[4 * cg]);
+            const float4 do4 = *reinterpret_cast<const float4*>(&sh.dO[4 * cg]);
+            const float b = sh.beta;
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) {
+                const int i = row_of(r);
+                const float a = sh.a[i], kk = sh.k[i] * m.rk, qq = sh.q[i] * qs;
+                const float4 sp = make_float4(a * S[r].x, a * S[r].y, a * S[r].z, a * S[r].w);
+                const float4 st = make_float4(sp.x + kk * u4.x, sp.y + kk * u4.y,
+                                              sp.z + kk * u4.z, sp.w + kk * u4.w);
+                float dq_i = st.x * do4.x + st.y * do4.y + st.z * do4.z + st.w * do4.w;
+                float4 g = make_float4(G[r].x + qq * do4.x, G[r].y + qq * do4.y,
+                                       G[r].z + qq * do4.z, G[r].w + qq * do4.w);
+                float dk_i = g.x * u4.x + g.y * u4.y + g.z * u4.z + g.w * u4.w -
+                             b * (sp.x * du4.x + sp.y * du4.y + sp.z * du4.z + sp.w * du4.w);
+                g.x -= b * kk * du4.x; g.y -= b * kk * du4.y;
+                g.z -= b * kk * du4.z; g.w -= b * kk * du4.w;
+                float da_i = g.x * S[r].x + g.y * S[r].y + g.z * S[r].z + g.w * S[r].w;
+                G[r] = make_float4(a * g.x, a * g.y, a * g.z, a * g.w);
+#pragma unroll
+                for (int off = 1; off < LPR; off <<= 1) {
+                    dq_i += __shfl_xor_sync(0xffffffffu, dq_i, off);
+                    dk_i += __shfl_xor_sync(0xffffffffu, dk_i, off);
+                    da_i += __shfl_xor_sync(0xffffffffu, da_i, off);
+                }
+                if (cg == 0) {
+                    sh.dqh[i] = dq_i;
+                    sh.dkh[i] = dk_i;
+                    sh.da[i] = da_i;
+                }
+            }
+            __syncthreads();
+            // per key channel: gate and normalisation derivatives
+            float pq = 0.f, pk = 0.f, pa = 0.f, dx = 0.f, x = 0.f;
+            if (tid < DK) {
+                const float a = sh.a[tid];
+                x = eA * ldf(z, ((size_t)t * H + h) * DK + tid);
+                if (p.softplus_gate) {
+                    dx = -sh.da[tid] * a * (1.0f - a);
+                } else {
+                    const float sg = bw_sigmoid(x);
+                    dx = sh.da[tid] * a * kBwGmin * sg * (1.0f - sg);
+                }
+                pq = sh.q[tid] * sh.dqh[tid];
+                pk = sh.k[tid] * sh.dkh[tid];
+                pa = dx * x;
+            }
+            const float xq = block_sum(pq, sh.red1);
+            const float xk = block_sum(pk, sh.red1);
+            const float xa = block_sum(pa, sh.red1);
+            if (tid < DK) {
+                const size_t o = ((size_t)t * H + h) * DK + tid;
+                p.dz[o] = dx * eA;
+                const float rq3 = p.l2norm ? m.rq * m.rq * m.rq : 0.0f;
+                const float rk3 = p.l2norm ? m.rk * m.rk * m.rk : 0.0f;
+                p.dq[o] = scale * (m.rq * sh.dqh[tid] - rq3 * xq * sh.q[tid]);
+                p.dk[o] = m.rk * sh.dkh[tid] - rk3 * xk * sh.k[tid];
+            }
+            if (tid == 0) {
+                dA_acc += xa;
+            }
+        }
+    }
+    // dL/dS_0 and this pair's share of dL/dA_h
+    store_state(p.dS0 + ((size_t)n * H + h) * SS, G);
+    if (tid == 0) {
+        p.dA_part[(size_t)n * H + h] = dA_acc;
+    }
+}
+
+// dA[h] = sum over sequences of the pairs' shares, in sequence order.
+__global__ void kda_backward_dA_kernel(const float* part, float* dA, int N, int H) {
+    const int h = blockIdx.x * blockDim.x + threadIdx.x;
+    if (h < H) {
+        float s = 0.0f;
+        for (int n = 0; n < N; ++n) {
+            s += part[(size_t)n * H + h];
+        }
+        dA[h] = s;
+    }
+}
+
+template <int DK, int DV>
+cudaError_t launch_dims(const BackwardParams& p, int dtype, cudaStream_t stream) {
+    const dim3 grid((unsigned)((int64_t)p.N * p.H));
+    if (dtype == 0) {
+        kda_backward_kernel<DK, DV, float><<<grid, kBwThreads, 0, stream>>>(p);
+    } else {
+        kda_backward_kernel<DK, DV, __nv_bfloat16><<<grid, kBwThreads, 0, stream>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+template <int DK>
+cudaError_t launch_dk(const BackwardParams& p, int d_v, int dtype, cudaStream_t stream) {
+    switch (d_v) {
+        case 32: return launch_dims<DK, 32>(p, dtype, stream);
+        case 64: return launch_dims<DK, 64>(p, dtype, stream);
+        case 128: return launch_dims<DK, 128>(p, dtype, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_backward(const BackwardParams& p, int d_k, int d_v, int dtype,
+                            cudaStream_t stream) {
+    if (p.N > 0) {
+        cudaError_t err;
+        switch (d_k) {
+            case 32: err = launch_dk<32>(p, d_v, dtype, stream); break;
+            case 64: err = launch_dk<64>(p, d_v, dtype, stream); break;
+            case 128: err = launch_dk<128>(p, d_v, dtype, stream); break;
+            default: return cudaErrorInvalidValue;
+        }
+        if (err != cudaSuccess) {
+            return err;
+        }
+    }
+    kda_backward_dA_kernel<<<(p.H + 127) / 128, 128, 0, stream>>>(p.dA_part, p.dA, p.N, p.H);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

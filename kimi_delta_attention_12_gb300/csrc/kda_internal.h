@@ -82,6 +82,42 @@ struct ShortConvDecodeParams {
 cudaError_t launch_short_conv_decode(const ShortConvDecodeParams& p, int dtype,
                                      cudaStream_t stream);
 
+// Training backward of the recurrence (kda_backward.cu): one CTA per
+// (sequence, head); chunk-start states every kBwChunk tokens in `ckpt` (the
+// pair of sequence n, head h, chunk c at row (floor(cu[n] / kBwChunk) + n + c)
+// * H + h), per-pair scratch of kBwChunk states, per-pair dA shares.
+constexpr int kBwChunk = 64;
+struct BackwardParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* z;
+    const void* beta;
+    const float* A;
+    const float* initial_state;  // or null
+    const int32_t* cu_seqlens;   // or null (equal lengths)
+    const void* dO;              // [total_T, H, d_v]
+    const float* dS_final;       // [N, H, d_k, d_v] or null
+    float* dq;                   // [total_T, H, d_k] fp32
+    float* dk;
+    float* dv;                   // [total_T, H, d_v]
+    float* dz;
+    float* dbeta;                // [total_T, H]
+    float* dA;                   // [H]
+    float* dS0;                  // [N, H, d_k, d_v]
+    float* ckpt;                 // workspace
+    float* scratch;
+    float* dA_part;              // [N, H]
+    int32_t N;
+    int32_t total_T;
+    int32_t H;
+    float scale;
+    int32_t l2norm;
+    int32_t softplus_gate;
+};
+cudaError_t launch_backward(const BackwardParams& p, int d_k, int d_v, int dtype,
+                            cudaStream_t stream);
+
 // Launches the recurrent kernel for (d_k, d_v) in {32, 64, 128}^2 and
 // dtype (0 = fp32, 1 = bf16).  Returns a cudaError_t.
 cudaError_t launch_recurrent(const RecurrentParams& p, int d_k, int d_v, int dtype,

@@ -172,5 +172,16 @@ def make_conv_params(N: int, H: int, d_k: int, d_v: int, W: int, dtype: torch.dt
     return w, state
 
 
+def make_upstream_grads(total_T: int, N: int, H: int, d_k: int, d_v: int, dtype: torch.dtype,
+                        seed: int = 0, with_state: bool = True):
+    """Upstream gradients for the backward: dO [total_T, H, d_v] ~ N(0, 1) in
+    `dtype` and dL/dS_T [N, H, d_k, d_v] ~ N(0, 0.1) fp32 (or None), drawn in
+    that order from generator(seed + 13)."""
+    g = torch.Generator().manual_seed(seed + 13)
+    dO = torch.randn(total_T, H, d_v, generator=g).to(dtype)
+    dSf = (0.1 * torch.randn(N, H, d_k, d_v, generator=g)).float() if with_state else None
+    return dO, dSf
+
+
 def list_workloads() -> List[str]:
     return list(WORKLOADS) + [DECODE_256.name]

@@ -304,3 +304,50 @@ def test_decode_conv_workspace_bytes(L):
     assert f(4, 2, 128, 128, kda.KDA_BF16) == 3 * 4 * 2 * 128 * 2
     assert f(3, 1, 32, 64, kda.KDA_F32) == 512 + 512 + 768     # each part rounded up to 256 B
     assert f(-1, 2, 128, 128, kda.KDA_BF16) == 0
+
+
+def _call_backward(L, **over):
+    a = dict(q=BASE, k=BASE + 0x100000, v=BASE + 0x200000, z=BASE + 0x300000,
+             beta=BASE + 0x400000, A=BASE + 0x500000, S0=None, cu=None, cu_host=None, N=1, T=64,
+             H=2, dk=32, dv=32, dt=kda.KDA_F32, scale=1.0, flags=1, dO=BASE + 0x600000,
+             dSf=None, dq=BASE + 0x700000, dk_=BASE + 0x800000, dv_=BASE + 0x900000,
+             dz=BASE + 0xa00000, db=BASE + 0xb00000, dA=BASE + 0xc00000, dS0=BASE + 0xd00000,
+             ws=BASE + 0x1000000, ws_bytes=64 << 20)
+    a.update(over)
+    vp = ctypes.c_void_p
+    return L.kda_backward(vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["z"]), vp(a["beta"]),
+                          vp(a["A"]), vp(a["S0"]), vp(a["cu"]), a["cu_host"], a["N"], a["T"],
+                          a["H"], a["dk"], a["dv"], a["dt"], a["scale"], a["flags"], vp(a["dO"]),
+                          vp(a["dSf"]), vp(a["dq"]), vp(a["dk_"]), vp(a["dv_"]), vp(a["dz"]),
+                          vp(a["db"]), vp(a["dA"]), vp(a["dS0"]), vp(a["ws"]), a["ws_bytes"],
+                          None)
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(dk=48), kda.KDA_ERR_UNSUPPORTED),
+    (dict(dt=4), kda.KDA_ERR_UNSUPPORTED),
+    (dict(N=0), kda.KDA_ERR_INVALID_ARG),
+    (dict(flags=2), kda.KDA_ERR_INVALID_ARG),      # the recurrent flag is a forward choice
+    (dict(flags=8), kda.KDA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), kda.KDA_ERR_INVALID_ARG),
+    (dict(dO=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(dA=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(dS0=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(db=None), kda.KDA_ERR_INVALID_ARG),
+    (dict(N=3), kda.KDA_ERR_INVALID_ARG),          # 64 % 3 without cu_seqlens
+    (dict(ws=None), kda.KDA_ERR_WORKSPACE),
+    (dict(ws_bytes=4096), kda.KDA_ERR_WORKSPACE),
+    (dict(dS0=BASE + 0xd00008), kda.KDA_ERR_ALIGNMENT),
+    (dict(dq=BASE + 0x700002), kda.KDA_ERR_ALIGNMENT),
+    (dict(ws=BASE + 0x1000008), kda.KDA_ERR_ALIGNMENT),
+])
+def test_backward_validation(L, over, expect):
+    assert _call_backward(L, **over) == expect
+
+
+def test_backward_workspace_bytes(L):
+    f = L.kda_backward_workspace_bytes
+    SS = 32 * 32 * 4
+    # (64 / 64 + 1) chunk states, 64 scratch states, 2 dA shares, per head
+    assert f(1, 64, 2, 32, 32) == 2 * 2 * SS + 2 * 64 * SS + 256
+    assert f(0, 64, 2, 32, 32) == 0 and f(1, 64, 2, 48, 32) == 0
