@@ -332,6 +332,12 @@ def kda_arm(args, world, rank, local, pg):
     value = world * B * T / (ms_per_step / 1e3)
     achieved_gbs = byts / (kernel_ms / 1e3) / 1e9
     achieved_tf = flops / (kernel_ms / 1e3) / 1e12
+    if args.only == "backward":
+        bw = measure_backward(sets, B, H, T, d, args, stream)
+        if rank == 0:
+            print(json.dumps(dict(bw, only="backward",
+                                  frac=bw["achieved_gbs"] / peaks["hbm_gbs"])), flush=True)
+        return
     if args.only == "conv":
         conv = measure_conv(sets, ws, o, S, cu_host, B, H, T, d, args, stream)
         if rank == 0:
@@ -345,14 +351,16 @@ def kda_arm(args, world, rank, local, pg):
                               "tensor_tflops": achieved_tf}), flush=True)
         return
     ckpt = measure_checkpointed(sets, ws, o, S, cu_host, B, H, T, d, args, stream)
-    conv = measure_conv(sets, ws, o, S, cu_host, B, H, T, d, args, stream)
     softplus = measure_softplus(sets, ws, o, S, cu_host, args, stream)
     softplus["tokens_per_s"] = B * T / (softplus["kernel_ms"] / 1e3)
+    extras = {"prefill_checkpointed": dict(ckpt, kernel_ms_plain=kernel_ms),
+              "softplus_gate": softplus,
+              "short_conv": measure_conv(sets, ws, o, S, cu_host, B, H, T, d, args, stream),
+              "backward": measure_backward(sets, B, H, T, d, args, stream)}
 
     return finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops, nsets,
                   set_bytes, x_host, o, S, ws, cu_host, value, ms_per_step, kernel_ms,
-                  achieved_gbs, achieved_tf, clk, launches_per_step, kernel_name, pg, ckpt,
-                  softplus, conv)
+                  achieved_gbs, achieved_tf, clk, launches_per_step, kernel_name, pg, extras)
 
 
 def measure_checkpointed(sets, ws, o, S, cu_host, B, H, T, d, args, stream, interval=1024):
@@ -380,6 +388,43 @@ def measure_checkpointed(sets, ws, o, S, cu_host, B, H, T, d, args, stream, inte
 
 
 CONV_WIDTH = 4
+
+
+def backward_algorithmic(B, H, T, d):
+    """Bytes of one kda_backward call (d_k = d_v = d, bf16 inputs): q, k, v, z,
+    dO and beta read; fp32 dq, dk, dv, dz, dbeta, dS0 and dA written."""
+    ht = B * T * H
+    return ht * (5 * d * 2 + 2) + ht * (4 * d * 4 + 4) + B * H * d * d * 4 + H * 4
+
+
+def measure_backward(sets, B, H, T, d, args, stream):
+    """kda_backward on the prefill workload with seeded upstream gradients:
+    kernel time (both launches) and bandwidth on its algorithmic bytes."""
+    import torch
+    import kimi_delta_attention_12_gb300 as kda
+    from kimi_delta_attention_12_gb300 import inputs
+    x0 = sets[0]
+    dO, dSf = inputs.make_upstream_grads(B * T, B, H, d, d, torch.bfloat16, seed=21)
+    dO, dSf = dO.to(x0.q.device), dSf.to(x0.q.device)
+    ws = torch.empty(kda.backward_workspace_bytes(B, B * T, H, d, d), dtype=torch.uint8,
+                     device=x0.q.device)
+    n = min(args.steps, 3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    for i in range(1 + n):
+        x = sets[i % len(sets)]
+        if i >= 1:
+            ev[i - 1][0].record(stream)
+        kda.kda_backward(x.q, x.k, x.v, x.z, x.beta, x.A, dO, None, x.cu_seqlens,
+                         dS_final=dSf, workspace=ws)
+        if i >= 1:
+            ev[i - 1][1].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    byts = backward_algorithmic(B, H, T, d)
+    return {"kernel": "kda_backward_kernel", "form": "recurrent, fp32", "kernel_ms": ms,
+            "steps": n, "tokens_per_s": B * T / (ms / 1e3), "algorithmic_bytes": byts,
+            "achieved_gbs": byts / (ms / 1e3) / 1e9}
 
 
 def measure_conv(sets, ws, o, S, cu_host, B, H, T, d, args, stream):
@@ -508,7 +553,7 @@ def decode_only(args, rank, local, dev, stream, peaks):
 
 def finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops, nsets,
            set_bytes, x_host, o, S, ws, cu_host, value, ms_per_step, kernel_ms, achieved_gbs,
-           achieved_tf, clk, launches_per_step, kernel_name, pg, ckpt, softplus, conv):
+           achieved_tf, clk, launches_per_step, kernel_name, pg, extras):
     import torch
     import kimi_delta_attention_12_gb300 as kda
     # ---- end to end through the public API with host buffers ----
@@ -548,10 +593,12 @@ def finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops
     D = DECODE_SHAPE
     dec_ms, dec_bytes, dec_gbs, dclk_summary = run_decode(dev, rank, local, stream)
     sp_ms, _, sp_gbs, _ = run_decode(dev, rank, local, stream, softplus_gate=True)
-    softplus.update({"decode_ms_per_step": sp_ms, "decode_gbs": sp_gbs,
-                     "decode_frac": sp_gbs / peaks["hbm_gbs"]})
+    extras["softplus_gate"].update({"decode_ms_per_step": sp_ms, "decode_gbs": sp_gbs,
+                                    "decode_frac": sp_gbs / peaks["hbm_gbs"]})
     cv_ms, cv_bytes, cv_gbs, _ = run_decode(dev, rank, local, stream, conv=True)
+    conv = extras["short_conv"]
     conv["frac"] = conv["achieved_gbs"] / peaks["hbm_gbs"]
+    extras["backward"]["frac"] = extras["backward"]["achieved_gbs"] / peaks["hbm_gbs"]
     conv.update({"decode_kernels": "short_conv_decode_kernel + kda_recurrent_kernel",
                  "decode_ms_per_step": cv_ms, "decode_bytes_per_step": cv_bytes,
                  "decode_gbs": cv_gbs, "decode_frac": cv_gbs / peaks["hbm_gbs"]})
@@ -583,9 +630,7 @@ def finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops
                    "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm_gbs"],
                                 "unit": "GB/s", "frac": dec_gbs / peaks["hbm_gbs"]},
                    "clocks": dclk_summary},
-        "prefill_checkpointed": dict(ckpt, kernel_ms_plain=kernel_ms),
-        "softplus_gate": softplus,
-        "short_conv": conv,
+        **extras,
         "cpu_baseline": {"value": cpu_tps, "unit": "tokens/s", "cores": cpu_threads,
                          "kind": "oracle", "sample": cpu_sample},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
@@ -602,7 +647,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["kda", "reference"], default="kda")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "conv"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "conv", "backward"],
+                    default="all",
                     help="run one part only (for profiler captures); the default runs all")
     ap.add_argument("--decode-batch", type=int, default=DECODE_SHAPE["B"],
                     help="decode batch for --only decode (smaller cases for profiler captures)")

@@ -396,21 +396,23 @@ int kda_decode_step_conv(const void* q, const void* k, const void* v, const void
                             stream);
 }
 
-// Backward workspace: chunk-start states, per-pair scratch, per-pair dA.
+// Backward workspace: chunk-start states, per-pair scratch, per-CTA column
+// partials, per-token dA shares.
 static void backward_layout(int32_t N, int32_t total_T, int32_t H, int32_t d_k, int32_t d_v,
-                            size_t* ckpt, size_t* scratch, size_t* part) {
+                            size_t* ckpt, size_t* scratch, size_t* part, size_t* dA_tok) {
     const size_t SS = (size_t)d_k * d_v * sizeof(float);
     *ckpt = round_up(((size_t)total_T / kda::kBwChunk + N) * H * SS, 256);
     *scratch = round_up((size_t)N * H * kda::kBwChunk * SS, 256);
-    *part = round_up((size_t)N * H * sizeof(float), 256);
+    *part = round_up((size_t)(d_v / 32) * total_T * H * (3 * d_k + 1) * sizeof(float), 256);
+    *dA_tok = round_up((size_t)total_T * H * sizeof(float), 256);
 }
 
 size_t kda_backward_workspace_bytes(int32_t N, int32_t total_T, int32_t H, int32_t d_k,
                                     int32_t d_v) {
     if (N < 1 || H < 1 || total_T < 0 || !supported_dim(d_k) || !supported_dim(d_v)) return 0;
-    size_t a, b, c;
-    backward_layout(N, total_T, H, d_k, d_v, &a, &b, &c);
-    return a + b + c;
+    size_t a, b, c, d;
+    backward_layout(N, total_T, H, d_k, d_v, &a, &b, &c, &d);
+    return a + b + c + d;
 }
 
 int kda_backward(const void* q, const void* k, const void* v, const void* z,
@@ -440,9 +442,13 @@ int kda_backward(const void* q, const void* k, const void* v, const void* z,
             if (cu_seqlens_host[n + 1] < cu_seqlens_host[n]) return KDA_ERR_INVALID_ARG;
         }
     }
-    size_t wc, wsr, wp;
-    backward_layout(N, total_T, H, d_k, d_v, &wc, &wsr, &wp);
-    if (!workspace || workspace_bytes < wc + wsr + wp) return KDA_ERR_WORKSPACE;
+    // one finalize CTA per (token, head) and d_v / 32 main CTAs per (sequence, head)
+    if ((int64_t)total_T * H >= ((int64_t)1 << 31) || (int64_t)N * H * (d_v / 32) >= ((int64_t)1 << 31)) {
+        return KDA_ERR_UNSUPPORTED;
+    }
+    size_t wc, wsr, wp, wt;
+    backward_layout(N, total_T, H, d_k, d_v, &wc, &wsr, &wp, &wt);
+    if (!workspace || workspace_bytes < wc + wsr + wp + wt) return KDA_ERR_WORKSPACE;
     const size_t eb = elem_bytes(dt);
     if (!aligned(q, eb) || !aligned(k, eb) || !aligned(v, eb) || !aligned(z, eb) ||
         !aligned(beta, eb) || !aligned(dO, eb) || !aligned(A, 4) || !aligned(dq, 4) ||
@@ -460,7 +466,8 @@ int kda_backward(const void* q, const void* k, const void* v, const void* z,
     char* ws = static_cast<char*>(workspace);
     p.ckpt = reinterpret_cast<float*>(ws);
     p.scratch = reinterpret_cast<float*>(ws + wc);
-    p.dA_part = reinterpret_cast<float*>(ws + wc + wsr);
+    p.part = reinterpret_cast<float*>(ws + wc + wsr);
+    p.dA_tok = reinterpret_cast<float*>(ws + wc + wsr + wp);
     p.N = N; p.total_T = total_T; p.H = H; p.scale = scale;
     p.l2norm = (flags & KDA_FLAG_L2NORM_QK) ? 1 : 0;
     p.softplus_gate = (flags & KDA_FLAG_SOFTPLUS_GATE) ? 1 : 0;

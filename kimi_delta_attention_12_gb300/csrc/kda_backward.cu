@@ -12,14 +12,18 @@
 //   da[c] = sum_j G'[c][j] S_{t-1}[c][j];  G = Diag(a) G'
 // followed by the gate and normalisation derivatives, written out per token.
 //
-// One CTA per (sequence, head) holds the whole d_k x d_v state and its
-// gradient G in registers (so every sum over the value columns stays inside
-// the CTA).  The reverse pass needs S_{t-1} for every token; phase 1 runs the
-// forward recurrence and stores the state at the start of every 64-token
-// chunk; phase 2 walks the chunks last to first, recomputes each chunk's
-// states forward into a scratch buffer (S_{t-1} of its 64 tokens), then walks
-// its tokens backwards.  The forward recomputation doubles the token-serial
-// work; the scratch keeps memory at 64 states per (sequence, head).
+// The value columns of a head are independent in the recurrence (column j of
+// S, G, u, du only meets column j), so each (sequence, head) runs as NS =
+// d_v / 32 CTAs of 32 columns, each holding its d_k x 32 slices of the state
+// and of G in registers.  What sums over the columns (dqh, dkh, da, db) is
+// written per token as one partial per CTA; kda_backward_finalize_kernel adds
+// the partials and applies the gate and normalisation derivatives.  The
+// reverse pass needs S_{t-1} for every token: phase 1 runs the forward
+// recurrence and stores the state at the start of every 64-token chunk;
+// phase 2 walks the chunks last to first, recomputes each chunk's states
+// forward into a scratch buffer (S_{t-1} of its 64 tokens), then walks its
+// tokens backwards.  The forward recomputation doubles the token-serial work;
+// the scratch keeps memory at 64 states per (sequence, head).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -69,41 +73,45 @@ __device__ __forceinline__ float block_sum(float x, float* red) {
     return t;
 }
 
-template <int DK, int DV>
+constexpr int kBwCols = 32;   // value columns per CTA
+
+template <int DK>
 struct BwShared {
     float q[DK];        // raw q, k of the token
     float k[DK];
     float a[DK];        // decay a = e^g
-    float v[DV];
-    float dO[DV];
-    float u[DV];
-    float du[DV];
-    float red[kBwWarps][2][DV];
+    float v[kBwCols];
+    float dO[kBwCols];
+    float u[kBwCols];
+    float du[kBwCols];
+    float red[kBwWarps][2][kBwCols];
     float nrm[DK / 32][3];
-    float dqh[DK];
-    float dkh[DK];
-    float da[DK];
     float red1[kBwWarps];
     float beta;
 };
 
 template <int DK, int DV, typename T>
-__global__ void __launch_bounds__(kBwThreads, 1)
+__global__ void __launch_bounds__(kBwThreads)
 kda_backward_kernel(const BackwardParams p) {
-    constexpr int LPR = DV / 4;            // lanes per state row (one float4 each)
+    constexpr int NS = DV / kBwCols;       // CTAs per (sequence, head)
+    constexpr int DVS = kBwCols;
+    constexpr int LPR = DVS / 4;           // lanes per state row (one float4 each)
     constexpr int RPW = 32 / LPR;          // rows per warp pass
     constexpr int RSTEP = kBwWarps * RPW;  // rows per CTA pass
     constexpr int RPT = DK / RSTEP;        // rows per thread
     constexpr int C = kBwChunk;
+    constexpr int PW = 3 * DK + 1;         // partials per (split, token, head)
     static_assert(RPT >= 1 && RPT * RSTEP == DK, "bad state tiling");
-    static_assert(DK + DV <= kBwThreads, "token loaders need DK + DV threads");
+    static_assert(DK + DVS <= kBwThreads, "token loaders need DK + 32 threads");
 
-    __shared__ BwShared<DK, DV> sh;
+    __shared__ BwShared<DK> sh;
 
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     const int cg = lane % LPR, rs = lane / LPR;
-    const int h = blockIdx.x % p.H;
-    const int n = blockIdx.x / p.H;
+    const int split = blockIdx.x % NS;
+    const int h = (blockIdx.x / NS) % p.H;
+    const int n = blockIdx.x / (NS * p.H);
+    const int col0 = split * DVS;
     const int H = p.H;
     const T* q = static_cast<const T*>(p.q);
     const T* k = static_cast<const T*>(p.k);
@@ -132,7 +140,8 @@ kda_backward_kernel(const BackwardParams p) {
     const float scale = p.scale;
 
     auto row_of = [&](int r) { return r * RSTEP + w * RPW + rs; };
-    auto st_idx = [&](int r) { return ((size_t)row_of(r) * DV) / 4 + cg; };   // float4 index
+    // float4 index of this thread's part of row r in a full d_k x d_v state
+    auto st_idx = [&](int r) { return ((size_t)row_of(r) * DV + col0) / 4 + cg; };
 
     // ---- one token's inputs into shared memory, and the norm partials ----
     auto load_token = [&](int64_t t, bool with_do) {
@@ -155,9 +164,9 @@ kda_backward_kernel(const BackwardParams p) {
                 sh.nrm[w][1] = sk;
                 sh.nrm[w][2] = sqk;
             }
-        } else if (tid < DK + DV) {
+        } else if (tid < DK + DVS) {
             const int j = tid - DK;
-            const size_t rv = ((size_t)t * H + h) * DV + j;
+            const size_t rv = ((size_t)t * H + h) * DV + col0 + j;
             sh.v[j] = ldf(v, rv);
             if (with_do) {
                 sh.dO[j] = ldf(dO, rv);
@@ -206,7 +215,7 @@ kda_backward_kernel(const BackwardParams p) {
             *reinterpret_cast<float4*>(&sh.red[w][0][4 * cg]) = ak;
         }
         __syncthreads();
-        if (tid < DV) {
+        if (tid < DVS) {
             float r = 0.f;
 #pragma unroll
             for (int ww = 0; ww < kBwWarps; ++ww) {
@@ -270,7 +279,6 @@ kda_backward_kernel(const BackwardParams p) {
             G[r] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
-    float dA_acc = 0.0f;   // thread 0: this pair's share of dL/dA_h
     for (int64_t c = nchunks - 1; c >= 0; --c) {
         const int64_t i0 = c * C;
         const int64_t cl = min((int64_t)C, len - i0);
@@ -324,7 +332,7 @@ kda_backward_kernel(const BackwardParams p) {
             __syncthreads();
             // per value column: u, du, dv and the column's share of db
             float dbj = 0.0f;
-            if (tid < DV) {
+            if (tid < DVS) {
                 float rr = 0.f, gk = 0.f;
 #pragma unroll
                 for (int ww = 0; ww < kBwWarps; ++ww) {
@@ -337,12 +345,13 @@ kda_backward_kernel(const BackwardParams p) {
                 const float duj = gk + qk * sh.dO[tid];
                 sh.u[tid] = b * wv;
                 sh.du[tid] = duj;
-                p.dv[((size_t)t * H + h) * DV + tid] = b * duj;
+                p.dv[((size_t)t * H + h) * DV + col0 + tid] = b * duj;
                 dbj = duj * wv;
             }
             const float db = block_sum(dbj, sh.red1);   // two barriers: u, du visible after
+            float* part = p.part + (((size_t)split * p.total_T + t) * H + h) * PW;
             if (tid == 0) {
-                p.dbeta[(size_t)t * H + h] = db;
+                part[3 * DK] = db;
             }
             // per state row: dqh, dkh, da and the new G
             const float4 u4 = *reinterpret_cast<const float4*>(&sh.u[4 * cg]);
@@ -372,69 +381,134 @@ kda_backward_kernel(const BackwardParams p) {
                     da_i += __shfl_xor_sync(0xffffffffu, da_i, off);
                 }
                 if (cg == 0) {
-                    sh.dqh[i] = dq_i;
-                    sh.dkh[i] = dk_i;
-                    sh.da[i] = da_i;
+                    part[i] = dq_i;
+                    part[DK + i] = dk_i;
+                    part[2 * DK + i] = da_i;
                 }
-            }
-            __syncthreads();
-            // per key channel: gate and normalisation derivatives
-            float pq = 0.f, pk = 0.f, pa = 0.f, dx = 0.f, x = 0.f;
-            if (tid < DK) {
-                const float a = sh.a[tid];
-                x = eA * ldf(z, ((size_t)t * H + h) * DK + tid);
-                if (p.softplus_gate) {
-                    dx = -sh.da[tid] * a * (1.0f - a);
-                } else {
-                    const float sg = bw_sigmoid(x);
-                    dx = sh.da[tid] * a * kBwGmin * sg * (1.0f - sg);
-                }
-                pq = sh.q[tid] * sh.dqh[tid];
-                pk = sh.k[tid] * sh.dkh[tid];
-                pa = dx * x;
-            }
-            const float xq = block_sum(pq, sh.red1);
-            const float xk = block_sum(pk, sh.red1);
-            const float xa = block_sum(pa, sh.red1);
-            if (tid < DK) {
-                const size_t o = ((size_t)t * H + h) * DK + tid;
-                p.dz[o] = dx * eA;
-                const float rq3 = p.l2norm ? m.rq * m.rq * m.rq : 0.0f;
-                const float rk3 = p.l2norm ? m.rk * m.rk * m.rk : 0.0f;
-                p.dq[o] = scale * (m.rq * sh.dqh[tid] - rq3 * xq * sh.q[tid]);
-                p.dk[o] = m.rk * sh.dkh[tid] - rk3 * xk * sh.k[tid];
-            }
-            if (tid == 0) {
-                dA_acc += xa;
             }
         }
     }
-    // dL/dS_0 and this pair's share of dL/dA_h
+    // dL/dS_0 (this CTA's columns)
     store_state(p.dS0 + ((size_t)n * H + h) * SS, G);
-    if (tid == 0) {
-        p.dA_part[(size_t)n * H + h] = dA_acc;
+}
+
+// Per (token, head): the column partials of dqh, dkh, da and db added up,
+// then the gate derivative (a = e^g, x = e^A z; g = -5 sigmoid(x): dx = da a
+// (-5) sigmoid(x) (1 - sigmoid(x)); g = -softplus(x), a = sigmoid(-x): dx = -da
+// a (1 - a)), dz = dx e^A, the token's share dx . x of dL/dA, and the
+// normalisation derivative (xh = m x / sqrt(sum x^2 + eps): dx = m (rho dxh -
+// rho^3 (x . dxh) x)).  One thread per key channel.
+template <int DK, int NS, typename T>
+__global__ void __launch_bounds__(DK)
+kda_backward_finalize_kernel(const BackwardParams p) {
+    constexpr int PW = 3 * DK + 1;
+    constexpr int NW = DK / 32;
+    __shared__ float red[NW][5];
+    const int c = threadIdx.x, lane = c & 31, w = c >> 5;
+    const int64_t th = blockIdx.x;               // t * H + h
+    const int h = (int)(th % p.H);
+    float dqh = 0.f, dkh = 0.f, da = 0.f, db = 0.f;
+#pragma unroll
+    for (int s = 0; s < NS; ++s) {
+        const float* part = p.part + ((size_t)s * p.total_T * p.H + th) * PW;
+        dqh += part[c];
+        dkh += part[DK + c];
+        da += part[2 * DK + c];
+        if (c == 0) {
+            db += part[3 * DK];
+        }
+    }
+    const size_t o = (size_t)th * DK + c;
+    const float qv = ldf(static_cast<const T*>(p.q), o);
+    const float kv = ldf(static_cast<const T*>(p.k), o);
+    const float eA = expf(p.A[h]);
+    const float x = eA * ldf(static_cast<const T*>(p.z), o);
+    float dx;
+    if (p.softplus_gate) {
+        const float a = bw_sigmoid(-x);
+        dx = -da * a * (1.0f - a);
+    } else {
+        const float sg = bw_sigmoid(x);
+        const float a = expf(kBwGmin * sg);
+        dx = da * a * kBwGmin * sg * (1.0f - sg);
+    }
+    float v5[5] = {qv * qv, kv * kv, qv * dqh, kv * dkh, dx * x};
+#pragma unroll
+    for (int i = 0; i < 5; ++i) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            v5[i] += __shfl_xor_sync(0xffffffffu, v5[i], off);
+        }
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < 5; ++i) {
+            red[w][i] = v5[i];
+        }
+    }
+    __syncthreads();
+    float t5[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ww = 0; ww < NW; ++ww) {
+#pragma unroll
+        for (int i = 0; i < 5; ++i) {
+            t5[i] += red[ww][i];
+        }
+    }
+    p.dz[o] = dx * eA;
+    if (p.l2norm) {
+        const float rq = rsqrtf(t5[0] + kBwEps), rk = rsqrtf(t5[1] + kBwEps);
+        p.dq[o] = p.scale * (rq * dqh - rq * rq * rq * t5[2] * qv);
+        p.dk[o] = rk * dkh - rk * rk * rk * t5[3] * kv;
+    } else {
+        p.dq[o] = p.scale * dqh;
+        p.dk[o] = dkh;
+    }
+    if (c == 0) {
+        p.dbeta[th] = db;
+        p.dA_tok[th] = t5[4];
     }
 }
 
-// dA[h] = sum over sequences of the pairs' shares, in sequence order.
-__global__ void kda_backward_dA_kernel(const float* part, float* dA, int N, int H) {
-    const int h = blockIdx.x * blockDim.x + threadIdx.x;
-    if (h < H) {
-        float s = 0.0f;
-        for (int n = 0; n < N; ++n) {
-            s += part[(size_t)n * H + h];
+// dA[h] = the sum over all tokens of their shares, as a fixed tree (the same
+// order on every call).  One CTA of 256 threads per head.
+__global__ void __launch_bounds__(256)
+kda_backward_dA_kernel(const float* dA_tok, float* dA, int64_t total_T, int H) {
+    __shared__ float red[256];
+    const int h = blockIdx.x;
+    float s = 0.0f;
+    for (int64_t t = threadIdx.x; t < total_T; t += 256) {
+        s += dA_tok[(size_t)t * H + h];
+    }
+    red[threadIdx.x] = s;
+    __syncthreads();
+    for (int width = 128; width > 0; width >>= 1) {
+        if ((int)threadIdx.x < width) {
+            red[threadIdx.x] += red[threadIdx.x + width];
         }
-        dA[h] = s;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        dA[h] = red[0];
     }
 }
 
 template <int DK, int DV>
 cudaError_t launch_dims(const BackwardParams& p, int dtype, cudaStream_t stream) {
-    const dim3 grid((unsigned)((int64_t)p.N * p.H));
+    constexpr int NS = DV / kBwCols;
+    const dim3 grid((unsigned)((int64_t)p.N * p.H * NS));
+    const int64_t tokens = (int64_t)p.total_T * p.H;
     if (dtype == 0) {
         kda_backward_kernel<DK, DV, float><<<grid, kBwThreads, 0, stream>>>(p);
+        if (tokens > 0) {
+            kda_backward_finalize_kernel<DK, NS, float><<<(unsigned)tokens, DK, 0, stream>>>(p);
+        }
     } else {
         kda_backward_kernel<DK, DV, __nv_bfloat16><<<grid, kBwThreads, 0, stream>>>(p);
+        if (tokens > 0) {
+            kda_backward_finalize_kernel<DK, NS, __nv_bfloat16>
+                <<<(unsigned)tokens, DK, 0, stream>>>(p);
+        }
     }
     return cudaGetLastError();
 }
@@ -465,7 +539,7 @@ cudaError_t launch_backward(const BackwardParams& p, int d_k, int d_v, int dtype
             return err;
         }
     }
-    kda_backward_dA_kernel<<<(p.H + 127) / 128, 128, 0, stream>>>(p.dA_part, p.dA, p.N, p.H);
+    kda_backward_dA_kernel<<<p.H, 256, 0, stream>>>(p.dA_tok, p.dA, p.total_T, p.H);
     return cudaGetLastError();
 }
 

@@ -82,10 +82,11 @@ struct ShortConvDecodeParams {
 cudaError_t launch_short_conv_decode(const ShortConvDecodeParams& p, int dtype,
                                      cudaStream_t stream);
 
-// Training backward of the recurrence (kda_backward.cu): one CTA per
+// Training backward of the recurrence (kda_backward.cu): d_v / 32 CTAs per
 // (sequence, head); chunk-start states every kBwChunk tokens in `ckpt` (the
 // pair of sequence n, head h, chunk c at row (floor(cu[n] / kBwChunk) + n + c)
-// * H + h), per-pair scratch of kBwChunk states, per-pair dA shares.
+// * H + h), per-pair scratch of kBwChunk states, per-CTA column partials
+// [d_v / 32][total_T][H][3 d_k + 1] of dqh, dkh, da, db, per-token dA shares.
 constexpr int kBwChunk = 64;
 struct BackwardParams {
     const void* q;
@@ -107,7 +108,8 @@ struct BackwardParams {
     float* dS0;                  // [N, H, d_k, d_v]
     float* ckpt;                 // workspace
     float* scratch;
-    float* dA_part;              // [N, H]
+    float* part;
+    float* dA_tok;               // [total_T, H]
     int32_t N;
     int32_t total_T;
     int32_t H;

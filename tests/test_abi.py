@@ -348,6 +348,9 @@ def test_backward_validation(L, over, expect):
 def test_backward_workspace_bytes(L):
     f = L.kda_backward_workspace_bytes
     SS = 32 * 32 * 4
-    # (64 / 64 + 1) chunk states, 64 scratch states, 2 dA shares, per head
-    assert f(1, 64, 2, 32, 32) == 2 * 2 * SS + 2 * 64 * SS + 256
+    # per head: (64 / 64 + 1) chunk states and 64 scratch states; one column
+    # group of partials (3 * 32 + 1 floats per token and head); per-token dA shares
+    part = 64 * 2 * 97 * 4
+    assert f(1, 64, 2, 32, 32) == (2 * 2 * SS + 2 * 64 * SS + (part + 255) // 256 * 256
+                                   + 64 * 2 * 4)
     assert f(0, 64, 2, 32, 32) == 0 and f(1, 64, 2, 48, 32) == 0
