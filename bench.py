@@ -399,15 +399,16 @@ def backward_algorithmic(B, H, T, d):
 
 def measure_backward(sets, B, H, T, d, args, stream):
     """kda_backward on the prefill workload with seeded upstream gradients:
-    kernel time (both launches) and bandwidth on its algorithmic bytes."""
+    the call's time (its checkpointed forward prefill, the backward and the
+    finalize kernels) and bandwidth on its algorithmic bytes."""
     import torch
     import kimi_delta_attention_12_gb300 as kda
     from kimi_delta_attention_12_gb300 import inputs
     x0 = sets[0]
     dO, dSf = inputs.make_upstream_grads(B * T, B, H, d, d, torch.bfloat16, seed=21)
     dO, dSf = dO.to(x0.q.device), dSf.to(x0.q.device)
-    ws = torch.empty(kda.backward_workspace_bytes(B, B * T, H, d, d), dtype=torch.uint8,
-                     device=x0.q.device)
+    ws = torch.empty(kda.backward_workspace_bytes(B, B * T, H, d, d, torch.bfloat16),
+                     dtype=torch.uint8, device=x0.q.device)
     n = min(args.steps, 3)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(n)]

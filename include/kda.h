@@ -289,10 +289,13 @@ KDA_API size_t kda_decode_conv_workspace_bytes(int32_t B, int32_t H, int32_t d_k
  * Linear's) and the Q/K normalisation (section 1 of the K3 architecture
  * page gives the forward step; the backward is its reverse mode).
  *
- * Recurrent form, fp32 arithmetic, one CTA per (sequence, head): a forward
- * pass stores the state at every 64-token chunk start; the chunks are then
- * walked last to first, each recomputed forward into a scratch and its
- * tokens walked in reverse.
+ * Recurrent form, fp32 arithmetic, d_v / 32 CTAs per (sequence, head): the
+ * states at every 64-token chunk start come from the forward prefill
+ * (kda_prefill_checkpointed, on the chunked tensor-core kernel where it
+ * applies, launched by this call on `stream`); the chunks are then walked
+ * last to first, each recomputed forward in fp32 into a scratch and its
+ * tokens walked in reverse; a second kernel adds the per-CTA column sums and
+ * applies the gate and normalisation derivatives.
  *
  *  q, k, v, z, beta, A, initial_state, cu_seqlens, cu_seqlens_host, N,
  *  total_T, H, d_k, d_v, dt, scale: as kda_prefill (the forward's inputs)
@@ -303,8 +306,10 @@ KDA_API size_t kda_decode_conv_workspace_bytes(int32_t B, int32_t H, int32_t d_k
  *  dbeta       [total_T, H] fp32;  dA [H] fp32;  dS0 [N, H, d_k, d_v] fp32
  *              (written, not accumulated; dS0 is written also when
  *              initial_state is NULL)
- *  workspace   kda_backward_workspace_bytes(N, total_T, H, d_k, d_v) bytes,
- *              16-byte aligned, no initialisation needed
+ *  workspace   kda_backward_workspace_bytes(N, total_T, H, d_k, d_v, dt) bytes,
+ *              256-byte aligned, no initialisation needed; it begins with the
+ *              forward prefill's workspace, so kda_workspace_status on it
+ *              reports that prefill's bounded waits
  * Errors: as kda_prefill (KDA_ERR_WORKSPACE for a short workspace), and
  * KDA_ERR_INVALID_ARG for a missing gradient buffer.
  */
@@ -317,11 +322,12 @@ KDA_API int kda_backward(const void* q, const void* k, const void* v, const void
                          float* dq, float* dk, float* dv, float* dz, float* dbeta, float* dA,
                          float* dS0, void* workspace, size_t workspace_bytes, void* stream);
 
-/* kda_backward_workspace_bytes -- the workspace kda_backward needs: chunk-
- * start states, a 64-state scratch per (sequence, head), per-pair dA shares
+/* kda_backward_workspace_bytes -- the workspace kda_backward needs: the
+ * forward prefill's workspace and outputs, the chunk-start states, a 64-state
+ * scratch per (sequence, head), the column partials and per-token dA shares
  * (0 for invalid sizes). */
 KDA_API size_t kda_backward_workspace_bytes(int32_t N, int32_t total_T, int32_t H, int32_t d_k,
-                                            int32_t d_v);
+                                            int32_t d_v, kda_dtype dt);
 
 /*
  * kda_state_io -- moves fp32 states of shape [H, d_k, d_v] each (the

@@ -114,7 +114,7 @@ def lib() -> ctypes.CDLL:
                                        i32, ctypes.c_int, ctypes.c_float, ctypes.c_uint32, vp,
                                        vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
             L.kda_backward_workspace_bytes.restype = sz
-            L.kda_backward_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+            L.kda_backward_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, ctypes.c_int]
             L.kda_checkpoint_count.restype = ctypes.c_int64
             L.kda_checkpoint_count.argtypes = [vp, i32, i32, i32]
             _lib = L
@@ -384,8 +384,9 @@ def kda_decode_step_conv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: t
     return o
 
 
-def backward_workspace_bytes(N: int, total_T: int, H: int, d_k: int, d_v: int) -> int:
-    return int(lib().kda_backward_workspace_bytes(N, total_T, H, d_k, d_v))
+def backward_workspace_bytes(N: int, total_T: int, H: int, d_k: int, d_v: int,
+                             dtype: torch.dtype) -> int:
+    return int(lib().kda_backward_workspace_bytes(N, total_T, H, d_k, d_v, _dtype_code(dtype)))
 
 
 def kda_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: torch.Tensor,
@@ -419,7 +420,7 @@ def kda_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: torch.Ten
              dbeta=torch.empty(total_T, H, **f32), dA=torch.empty(H, **f32),
              dS0=torch.empty(N, H, d_k, d_v, **f32))
     if workspace is None:
-        workspace = torch.empty(backward_workspace_bytes(N, total_T, H, d_k, d_v),
+        workspace = torch.empty(backward_workspace_bytes(N, total_T, H, d_k, d_v, dt),
                                 dtype=torch.uint8, device=dev)
     host_cu = None if cu_seqlens_host is None else cu_seqlens_host.to(torch.int32).contiguous()
     host_ptr = None if host_cu is None else ctypes.c_void_p(host_cu.data_ptr())

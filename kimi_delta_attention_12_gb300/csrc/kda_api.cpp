@@ -396,23 +396,36 @@ int kda_decode_step_conv(const void* q, const void* k, const void* v, const void
                             stream);
 }
 
-// Backward workspace: chunk-start states, per-pair scratch, per-CTA column
-// partials, per-token dA shares.
-static void backward_layout(int32_t N, int32_t total_T, int32_t H, int32_t d_k, int32_t d_v,
-                            size_t* ckpt, size_t* scratch, size_t* part, size_t* dA_tok) {
+// Backward workspace, in order: the workspace of the checkpointed prefill
+// that provides the chunk-start states (first, so that kda_workspace_status
+// reads its status word), that prefill's output o (not used), the checkpoint
+// pool (at most floor(total_T / 64) states), the per-pair scratch, the
+// per-CTA column partials and the per-token dA shares.
+struct BackwardLayout {
+    size_t prefill, o, pool, scratch, part, dA_tok;
+    size_t total() const { return prefill + o + pool + scratch + part + dA_tok; }
+};
+
+static BackwardLayout backward_layout(int32_t N, int32_t total_T, int32_t H, int32_t d_k,
+                                      int32_t d_v, kda_dtype dt) {
     const size_t SS = (size_t)d_k * d_v * sizeof(float);
-    *ckpt = round_up(((size_t)total_T / kda::kBwChunk + N) * H * SS, 256);
-    *scratch = round_up((size_t)N * H * kda::kBwChunk * SS, 256);
-    *part = round_up((size_t)(d_v / 32) * total_T * H * (3 * d_k + 1) * sizeof(float), 256);
-    *dA_tok = round_up((size_t)total_T * H * sizeof(float), 256);
+    BackwardLayout l;
+    l.prefill = round_up(kda_prefill_workspace_bytes(N, total_T, H, d_k, d_v, dt), 256);
+    l.o = round_up((size_t)total_T * H * d_v * elem_bytes(dt), 256);
+    l.pool = round_up((size_t)(total_T / kda::kBwChunk) * H * SS, 256);
+    l.scratch = round_up((size_t)N * H * kda::kBwChunk * SS, 256);
+    l.part = round_up((size_t)(d_v / 32) * total_T * H * (3 * d_k + 1) * sizeof(float), 256);
+    l.dA_tok = round_up((size_t)total_T * H * sizeof(float), 256);
+    return l;
 }
 
 size_t kda_backward_workspace_bytes(int32_t N, int32_t total_T, int32_t H, int32_t d_k,
-                                    int32_t d_v) {
-    if (N < 1 || H < 1 || total_T < 0 || !supported_dim(d_k) || !supported_dim(d_v)) return 0;
-    size_t a, b, c, d;
-    backward_layout(N, total_T, H, d_k, d_v, &a, &b, &c, &d);
-    return a + b + c + d;
+                                    int32_t d_v, kda_dtype dt) {
+    if (N < 1 || H < 1 || total_T < 0 || !supported_dim(d_k) || !supported_dim(d_v) ||
+        (dt != KDA_F32 && dt != KDA_BF16)) {
+        return 0;
+    }
+    return backward_layout(N, total_T, H, d_k, d_v, dt).total();
 }
 
 int kda_backward(const void* q, const void* k, const void* v, const void* z,
@@ -446,16 +459,27 @@ int kda_backward(const void* q, const void* k, const void* v, const void* z,
     if ((int64_t)total_T * H >= ((int64_t)1 << 31) || (int64_t)N * H * (d_v / 32) >= ((int64_t)1 << 31)) {
         return KDA_ERR_UNSUPPORTED;
     }
-    size_t wc, wsr, wp, wt;
-    backward_layout(N, total_T, H, d_k, d_v, &wc, &wsr, &wp, &wt);
-    if (!workspace || workspace_bytes < wc + wsr + wp + wt) return KDA_ERR_WORKSPACE;
+    const BackwardLayout wl = backward_layout(N, total_T, H, d_k, d_v, dt);
+    if (!workspace || workspace_bytes < wl.total()) return KDA_ERR_WORKSPACE;
     const size_t eb = elem_bytes(dt);
     if (!aligned(q, eb) || !aligned(k, eb) || !aligned(v, eb) || !aligned(z, eb) ||
         !aligned(beta, eb) || !aligned(dO, eb) || !aligned(A, 4) || !aligned(dq, 4) ||
         !aligned(dk, 4) || !aligned(dv, 4) || !aligned(dz, 4) || !aligned(dbeta, 4) ||
         !aligned(dA, 4) || !aligned(initial_state, 16) || !aligned(dS_final, 16) ||
-        !aligned(dS0, 16) || !aligned(cu_seqlens, 4) || !aligned(workspace, 16)) {
+        !aligned(dS0, 16) || !aligned(cu_seqlens, 4) || !aligned(workspace, 256)) {
         return KDA_ERR_ALIGNMENT;
+    }
+    char* ws = static_cast<char*>(workspace);
+    char* ws_o = ws + wl.prefill;
+    float* pool = reinterpret_cast<float*>(ws_o + wl.o);
+    // the states after every 64 tokens of each sequence, from the forward
+    const int32_t pool_rows = total_T / kda::kBwChunk;
+    if (pool_rows > 0) {
+        const int st = kda_prefill_checkpointed(
+            q, k, v, z, beta, A, initial_state, cu_seqlens, cu_seqlens_host, N, total_T, H,
+            d_k, d_v, dt, scale, flags, ws_o, nullptr, kda::kBwChunk, pool, nullptr, pool_rows,
+            ws, wl.prefill, stream);
+        if (st != KDA_OK) return st;
     }
     kda::BackwardParams p;
     memset(&p, 0, sizeof(p));
@@ -463,11 +487,10 @@ int kda_backward(const void* q, const void* k, const void* v, const void* z,
     p.initial_state = initial_state; p.cu_seqlens = cu_seqlens;
     p.dO = dO; p.dS_final = dS_final;
     p.dq = dq; p.dk = dk; p.dv = dv; p.dz = dz; p.dbeta = dbeta; p.dA = dA; p.dS0 = dS0;
-    char* ws = static_cast<char*>(workspace);
-    p.ckpt = reinterpret_cast<float*>(ws);
-    p.scratch = reinterpret_cast<float*>(ws + wc);
-    p.part = reinterpret_cast<float*>(ws + wc + wsr);
-    p.dA_tok = reinterpret_cast<float*>(ws + wc + wsr + wp);
+    p.pool = pool;
+    p.scratch = reinterpret_cast<float*>(ws_o + wl.o + wl.pool);
+    p.part = reinterpret_cast<float*>(ws_o + wl.o + wl.pool + wl.scratch);
+    p.dA_tok = reinterpret_cast<float*>(ws_o + wl.o + wl.pool + wl.scratch + wl.part);
     p.N = N; p.total_T = total_T; p.H = H; p.scale = scale;
     p.l2norm = (flags & KDA_FLAG_L2NORM_QK) ? 1 : 0;
     p.softplus_gate = (flags & KDA_FLAG_SOFTPLUS_GATE) ? 1 : 0;

@@ -18,12 +18,14 @@
 // and of G in registers.  What sums over the columns (dqh, dkh, da, db) is
 // written per token as one partial per CTA; kda_backward_finalize_kernel adds
 // the partials and applies the gate and normalisation derivatives.  The
-// reverse pass needs S_{t-1} for every token: phase 1 runs the forward
-// recurrence and stores the state at the start of every 64-token chunk;
-// phase 2 walks the chunks last to first, recomputes each chunk's states
+// reverse pass needs S_{t-1} for every token.  The states at the 64-token
+// chunk starts come from the library's checkpointed prefill (run by the host
+// before this kernel: checkpoint m of sequence n, the state after its first
+// 64 m tokens, at pool row (checkpoints of earlier sequences) + m - 1); the
+// kernel walks the chunks last to first, recomputes each chunk's states
 // forward into a scratch buffer (S_{t-1} of its 64 tokens), then walks its
-// tokens backwards.  The forward recomputation doubles the token-serial work;
-// the scratch keeps memory at 64 states per (sequence, head).
+// tokens backwards.  The scratch keeps memory at 64 states per (sequence,
+// head).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -132,9 +134,7 @@ kda_backward_kernel(const BackwardParams p) {
     const int64_t len = eos - bos;
     const int64_t nchunks = (len + C - 1) / C;
     const size_t SS = (size_t)DK * DV;
-    // this pair's chunk-start states and its chunk scratch
-    float* ckpt = p.ckpt + ((size_t)(bos / C + n) * H + h) * SS;
-    const size_t ckpt_stride = (size_t)H * SS;       // consecutive chunks of the pair
+    // this pair's chunk scratch
     float* scratch = p.scratch + ((size_t)n * H + h) * C * SS;
     const float eA = expf(p.A[h]);
     const float scale = p.scale;
@@ -246,24 +246,26 @@ kda_backward_kernel(const BackwardParams p) {
         }
     };
 
-    // ---- phase 1: forward, storing the state at every chunk start ----
-    if (p.initial_state) {
-        load_state(p.initial_state + ((size_t)n * H + h) * SS);
-    } else {
-#pragma unroll
-        for (int r = 0; r < RPT; ++r) {
-            S[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+    // index of this sequence's first checkpoint in the pool: the sum over
+    // earlier sequences of floor(length / 64)
+    __shared__ int s_base;
+    if (tid == 0) {
+        s_base = 0;
+    }
+    __syncthreads();
+    {
+        int part = 0;
+        for (int m = tid; m < n; m += kBwThreads) {
+            const int64_t lm = p.cu_seqlens ? (int64_t)(p.cu_seqlens[m + 1] - p.cu_seqlens[m])
+                                            : p.total_T / p.N;
+            part += (int)(lm / C);
+        }
+        if (part) {
+            atomicAdd(&s_base, part);
         }
     }
-    for (int64_t i = 0; i < len; ++i) {
-        if (i % C == 0) {
-            store_state(ckpt + (size_t)(i / C) * ckpt_stride, S);
-        }
-        load_token(bos + i, false);
-        __syncthreads();
-        forward_step();
-        __syncthreads();   // the next token's loads overwrite what this one read
-    }
+    __syncthreads();
+    const int64_t ck_base = s_base;
 
     // ---- phase 2: chunks last to first ----
     float4 G[RPT];
@@ -282,9 +284,19 @@ kda_backward_kernel(const BackwardParams p) {
     for (int64_t c = nchunks - 1; c >= 0; --c) {
         const int64_t i0 = c * C;
         const int64_t cl = min((int64_t)C, len - i0);
-        // 2a: the chunk's states S_{t-1} into the scratch
+        // 2a: the chunk's states S_{t-1} into the scratch, from the state at
+        // the chunk start (the initial state for chunk 0, else checkpoint c)
         __syncthreads();
-        load_state(ckpt + (size_t)c * ckpt_stride);
+        if (c > 0) {
+            load_state(p.pool + ((size_t)(ck_base + c - 1) * H + h) * SS);
+        } else if (p.initial_state) {
+            load_state(p.initial_state + ((size_t)n * H + h) * SS);
+        } else {
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) {
+                S[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
         for (int64_t j = 0; j < cl; ++j) {
             store_state(scratch + (size_t)j * SS, S);
             if (j + 1 == cl) {

@@ -83,10 +83,11 @@ cudaError_t launch_short_conv_decode(const ShortConvDecodeParams& p, int dtype,
                                      cudaStream_t stream);
 
 // Training backward of the recurrence (kda_backward.cu): d_v / 32 CTAs per
-// (sequence, head); chunk-start states every kBwChunk tokens in `ckpt` (the
-// pair of sequence n, head h, chunk c at row (floor(cu[n] / kBwChunk) + n + c)
-// * H + h), per-pair scratch of kBwChunk states, per-CTA column partials
-// [d_v / 32][total_T][H][3 d_k + 1] of dqh, dkh, da, db, per-token dA shares.
+// (sequence, head); the states every kBwChunk tokens in `pool` (the layout of
+// the checkpointed prefill: checkpoint m >= 1 of sequence n at row
+// (checkpoints of sequences before n) + m - 1), per-pair scratch of kBwChunk
+// states, per-CTA column partials [d_v / 32][total_T][H][3 d_k + 1] of dqh,
+// dkh, da, db, per-token dA shares.
 constexpr int kBwChunk = 64;
 struct BackwardParams {
     const void* q;
@@ -106,7 +107,7 @@ struct BackwardParams {
     float* dbeta;                // [total_T, H]
     float* dA;                   // [H]
     float* dS0;                  // [N, H, d_k, d_v]
-    float* ckpt;                 // workspace
+    const float* pool;           // workspace
     float* scratch;
     float* part;
     float* dA_tok;               // [total_T, H]

@@ -340,6 +340,7 @@ def _call_backward(L, **over):
     (dict(dS0=BASE + 0xd00008), kda.KDA_ERR_ALIGNMENT),
     (dict(dq=BASE + 0x700002), kda.KDA_ERR_ALIGNMENT),
     (dict(ws=BASE + 0x1000008), kda.KDA_ERR_ALIGNMENT),
+    (dict(ws=BASE + 0x1000080), kda.KDA_ERR_ALIGNMENT),   # the forward's part needs 256 B
 ])
 def test_backward_validation(L, over, expect):
     assert _call_backward(L, **over) == expect
@@ -347,10 +348,13 @@ def test_backward_validation(L, over, expect):
 
 def test_backward_workspace_bytes(L):
     f = L.kda_backward_workspace_bytes
+    r256 = lambda x: (x + 255) // 256 * 256
     SS = 32 * 32 * 4
-    # per head: (64 / 64 + 1) chunk states and 64 scratch states; one column
-    # group of partials (3 * 32 + 1 floats per token and head); per-token dA shares
-    part = 64 * 2 * 97 * 4
-    assert f(1, 64, 2, 32, 32) == (2 * 2 * SS + 2 * 64 * SS + (part + 255) // 256 * 256
-                                   + 64 * 2 * 4)
-    assert f(0, 64, 2, 32, 32) == 0 and f(1, 64, 2, 48, 32) == 0
+    prefill = r256(L.kda_prefill_workspace_bytes(1, 64, 2, 32, 32, kda.KDA_F32))
+    want = (prefill + r256(64 * 2 * 32 * 4)        # forward o
+            + 1 * 2 * SS                           # one checkpoint (64 tokens) per head
+            + 2 * 64 * SS                          # 64 scratch states per head
+            + r256(64 * 2 * 97 * 4)                # one column group of partials
+            + 64 * 2 * 4)                          # per-token dA shares
+    assert f(1, 64, 2, 32, 32, kda.KDA_F32) == want
+    assert f(0, 64, 2, 32, 32, kda.KDA_F32) == 0 and f(1, 64, 2, 48, 32, kda.KDA_F32) == 0
