@@ -309,38 +309,42 @@ kda_recurrent_kernel(const RecurrentParams p) {
     }
 }
 
-// Value-column split per head: decode of d_v = 128 uses two CTAs per head
-// (half the registers per CTA, twice the state bytes in flight per SM).
+// Value-column split per head.  Decode of d_v = 128 uses two CTAs per head
+// (half the registers per CTA, twice the state bytes in flight per SM; more
+// CTAs per head would shrink the 128-bit rows each warp streams).  Prefill,
+// token-serial and latency-bound, uses 32-column CTAs: a quarter of the
+// per-token work of each CTA at d_v = 128, on four times the SMs.
 template <int DV>
-constexpr int column_split() { return DV == 128 ? 2 : 1; }
+constexpr int decode_split() { return DV == 128 ? 2 : 1; }
+template <int DV>
+constexpr int prefill_split() { return DV / 32; }
 
-template <int DK, int DV, int NS, typename T>
-void launch_mode(int mode, dim3 grid, const RecurrentParams& p, cudaStream_t stream) {
+template <int DK, int DV, int NS, typename T, int kMode>
+void launch_one(const RecurrentParams& p, cudaStream_t stream) {
+    const dim3 grid((unsigned)((int64_t)p.rows * p.H * NS));
+    if (grid.x > 0) {
+        kda_recurrent_kernel<DK, DV, NS, T, kMode><<<grid, kThreads, 0, stream>>>(p);
+    }
+}
+
+template <int DK, int DV, typename T>
+void launch_mode(int mode, const RecurrentParams& p, cudaStream_t stream) {
+    constexpr int NSD = decode_split<DV>();
+    constexpr int NSP = prefill_split<DV>();
     switch (mode) {
-        case kModeDecode:
-            kda_recurrent_kernel<DK, DV, NS, T, kModeDecode><<<grid, kThreads, 0, stream>>>(p);
-            break;
-        case kModeCkpt:
-            kda_recurrent_kernel<DK, DV, NS, T, kModeCkpt><<<grid, kThreads, 0, stream>>>(p);
-            break;
-        default:
-            kda_recurrent_kernel<DK, DV, NS, T, kModePrefill><<<grid, kThreads, 0, stream>>>(p);
-            break;
+        case kModeDecode: launch_one<DK, DV, NSD, T, kModeDecode>(p, stream); break;
+        case kModeCkpt: launch_one<DK, DV, NSP, T, kModeCkpt>(p, stream); break;
+        default: launch_one<DK, DV, NSP, T, kModePrefill>(p, stream); break;
     }
 }
 
 template <int DK, int DV>
 cudaError_t launch_dims(const RecurrentParams& p, int dtype, cudaStream_t stream) {
-    constexpr int NS = column_split<DV>();
-    const dim3 grid((unsigned)((int64_t)p.rows * p.H * NS));
-    if (grid.x == 0) {
-        return cudaSuccess;
-    }
     const int mode = p.decode ? kModeDecode : p.ckpt_interval > 0 ? kModeCkpt : kModePrefill;
     if (dtype == 0) {
-        launch_mode<DK, DV, NS, float>(mode, grid, p, stream);
+        launch_mode<DK, DV, float>(mode, p, stream);
     } else {
-        launch_mode<DK, DV, NS, __nv_bfloat16>(mode, grid, p, stream);
+        launch_mode<DK, DV, __nv_bfloat16>(mode, p, stream);
     }
     return cudaGetLastError();
 }
