@@ -462,8 +462,8 @@ int kda_backward(const void* q, const void* k, const void* v, const void* z,
     const BackwardLayout wl = backward_layout(N, total_T, H, d_k, d_v, dt);
     if (!workspace || workspace_bytes < wl.total()) return KDA_ERR_WORKSPACE;
     const size_t eb = elem_bytes(dt);
-    if (!aligned(q, eb) || !aligned(k, eb) || !aligned(v, eb) || !aligned(z, eb) ||
-        !aligned(beta, eb) || !aligned(dO, eb) || !aligned(A, 4) || !aligned(dq, 4) ||
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(z, 16) ||
+        !aligned(beta, eb) || !aligned(dO, 16) || !aligned(A, 4) || !aligned(dq, 4) ||
         !aligned(dk, 4) || !aligned(dv, 4) || !aligned(dz, 4) || !aligned(dbeta, 4) ||
         !aligned(dA, 4) || !aligned(initial_state, 16) || !aligned(dS_final, 16) ||
         !aligned(dS0, 16) || !aligned(cu_seqlens, 4) || !aligned(workspace, 256)) {

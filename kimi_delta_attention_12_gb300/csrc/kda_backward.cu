@@ -25,7 +25,9 @@
 // kernel walks the chunks last to first, recomputes each chunk's states
 // forward into a scratch buffer (S_{t-1} of its 64 tokens), then walks its
 // tokens backwards.  The scratch keeps memory at 64 states per (sequence,
-// head).
+// head).  Both walks over a chunk read its tokens' inputs (q, k, z, the CTA's
+// v and dO columns, beta) from shared memory, staged once at the chunk start
+// with 16-byte loads, so no token waits on a global load.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -45,6 +47,10 @@ __device__ __forceinline__ float ldf(const float* p, size_t i) { return __ldg(p 
 __device__ __forceinline__ float ldf(const __nv_bfloat16* p, size_t i) {
     return __bfloat162float(p[i]);
 }
+
+// A value of the input dtype as float (any memory space).
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
 
 __device__ __forceinline__ float bw_sigmoid(float x) {
     if (x >= 0.0f) {
@@ -91,6 +97,12 @@ struct BwShared {
     float red1[kBwWarps];
     float beta;
 };
+
+// Dynamic shared memory of the chunk's token inputs (in the input dtype).
+template <int DK, typename T>
+constexpr size_t chunk_stage_bytes() {
+    return (size_t)kBwChunk * (3 * DK + 2 * kBwCols + 1) * sizeof(T);
+}
 
 template <int DK, int DV, typename T>
 __global__ void __launch_bounds__(kBwThreads)
@@ -143,11 +155,47 @@ kda_backward_kernel(const BackwardParams p) {
     // float4 index of this thread's part of row r in a full d_k x d_v state
     auto st_idx = [&](int r) { return ((size_t)row_of(r) * DV + col0) / 4 + cg; };
 
-    // ---- one token's inputs into shared memory, and the norm partials ----
+    // ---- the chunk's token inputs, staged in shared memory ----
+    extern __shared__ __align__(16) unsigned char bw_stage[];
+    T* cq = reinterpret_cast<T*>(bw_stage);       // [C][DK]
+    T* ck = cq + C * DK;
+    T* cz = ck + C * DK;
+    T* cv = cz + C * DK;                          // [C][DVS]
+    T* cdo = cv + C * DVS;
+    T* cb = cdo + C * DVS;                        // [C]
+    constexpr int VE = 16 / sizeof(T);            // elements per 16-byte vector
+    int64_t stage_t0 = 0;
+    auto stage_chunk = [&](int64_t t0, int cl) {
+        constexpr int RK = DK / VE, RV = DVS / VE;
+        for (int e = tid; e < cl * RK; e += kBwThreads) {
+            const int j = e / RK, c4 = e - j * RK;
+            const size_t g = ((size_t)(t0 + j) * H + h) * DK + (size_t)c4 * VE;
+            const int l = j * DK + c4 * VE;
+            *reinterpret_cast<uint4*>(cq + l) = __ldg(reinterpret_cast<const uint4*>(q + g));
+            *reinterpret_cast<uint4*>(ck + l) = __ldg(reinterpret_cast<const uint4*>(k + g));
+            *reinterpret_cast<uint4*>(cz + l) = __ldg(reinterpret_cast<const uint4*>(z + g));
+        }
+        for (int e = tid; e < cl * RV; e += kBwThreads) {
+            const int j = e / RV, c4 = e - j * RV;
+            const size_t g = ((size_t)(t0 + j) * H + h) * DV + col0 + (size_t)c4 * VE;
+            const int l = j * DVS + c4 * VE;
+            *reinterpret_cast<uint4*>(cv + l) = __ldg(reinterpret_cast<const uint4*>(v + g));
+            *reinterpret_cast<uint4*>(cdo + l) = __ldg(reinterpret_cast<const uint4*>(dO + g));
+        }
+        if (tid < cl) {
+            cb[tid] = beta[(size_t)(t0 + tid) * H + h];
+        }
+        stage_t0 = t0;
+        __syncthreads();
+    };
+    auto sf = [](const T* a, int i) { return to_f(a[i]); };   // a staged (shared) value
+
+    // ---- one token's inputs into the working arrays, and the norm partials ----
     auto load_token = [&](int64_t t, bool with_do) {
-        const size_t rk = ((size_t)t * H + h) * DK;
+        const int jt = (int)(t - stage_t0);
         if (tid < DK) {
-            const float qv = ldf(q, rk + tid), kv = ldf(k, rk + tid), zv = ldf(z, rk + tid);
+            const int e = jt * DK + tid;
+            const float qv = sf(cq, e), kv = sf(ck, e), zv = sf(cz, e);
             sh.q[tid] = qv;
             sh.k[tid] = kv;
             const float sg = bw_sigmoid(p.softplus_gate ? -eA * zv : eA * zv);
@@ -166,13 +214,12 @@ kda_backward_kernel(const BackwardParams p) {
             }
         } else if (tid < DK + DVS) {
             const int j = tid - DK;
-            const size_t rv = ((size_t)t * H + h) * DV + col0 + j;
-            sh.v[j] = ldf(v, rv);
+            sh.v[j] = sf(cv, jt * DVS + j);
             if (with_do) {
-                sh.dO[j] = ldf(dO, rv);
+                sh.dO[j] = sf(cdo, jt * DVS + j);
             }
             if (j == 0) {
-                sh.beta = ldf(beta, (size_t)t * H + h);
+                sh.beta = sf(cb, jt);
             }
         }
     };
@@ -287,6 +334,7 @@ kda_backward_kernel(const BackwardParams p) {
         // 2a: the chunk's states S_{t-1} into the scratch, from the state at
         // the chunk start (the initial state for chunk 0, else checkpoint c)
         __syncthreads();
+        stage_chunk(bos + i0, (int)cl);
         if (c > 0) {
             load_state(p.pool + ((size_t)(ck_base + c - 1) * H + h) * SS);
         } else if (p.initial_state) {
@@ -505,18 +553,41 @@ kda_backward_dA_kernel(const float* dA_tok, float* dA, int64_t total_T, int H) {
     }
 }
 
+template <int DK, int DV, typename T>
+cudaError_t launch_main(const BackwardParams& p, dim3 grid, cudaStream_t stream) {
+    constexpr size_t smem = chunk_stage_bytes<DK, T>();
+    static bool configured = false;   // the attribute is per kernel; setting it again is harmless
+    if (!configured) {
+        const cudaError_t e = cudaFuncSetAttribute(kda_backward_kernel<DK, DV, T>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)smem);
+        if (e != cudaSuccess) {
+            return e;
+        }
+        configured = true;
+    }
+    kda_backward_kernel<DK, DV, T><<<grid, kBwThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
 template <int DK, int DV>
 cudaError_t launch_dims(const BackwardParams& p, int dtype, cudaStream_t stream) {
     constexpr int NS = DV / kBwCols;
     const dim3 grid((unsigned)((int64_t)p.N * p.H * NS));
     const int64_t tokens = (int64_t)p.total_T * p.H;
     if (dtype == 0) {
-        kda_backward_kernel<DK, DV, float><<<grid, kBwThreads, 0, stream>>>(p);
+        const cudaError_t e = launch_main<DK, DV, float>(p, grid, stream);
+        if (e != cudaSuccess) {
+            return e;
+        }
         if (tokens > 0) {
             kda_backward_finalize_kernel<DK, NS, float><<<(unsigned)tokens, DK, 0, stream>>>(p);
         }
     } else {
-        kda_backward_kernel<DK, DV, __nv_bfloat16><<<grid, kBwThreads, 0, stream>>>(p);
+        const cudaError_t e = launch_main<DK, DV, __nv_bfloat16>(p, grid, stream);
+        if (e != cudaSuccess) {
+            return e;
+        }
         if (tokens > 0) {
             kda_backward_finalize_kernel<DK, NS, __nv_bfloat16>
                 <<<(unsigned)tokens, DK, 0, stream>>>(p);
