@@ -47,6 +47,18 @@ __device__ __forceinline__ float load_elem(const __nv_bfloat16* p, size_t i) {
     return __bfloat162float(p[i]);
 }
 __device__ __forceinline__ void store_elem(float* p, size_t i, float x) { p[i] = x; }
+// a value of the input dtype as float (any memory space)
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// Prefill stages the next kStage tokens' inputs (q, k, z, the CTA's v
+// columns, beta) in dynamic shared memory with 16-byte loads, so that no
+// token of the serial loop waits on a global load round trip.
+constexpr int kStage = 64;
+template <int DK, int DVS, typename T>
+constexpr size_t stage_bytes() {
+    return (size_t)kStage * (3 * DK + DVS + 1) * sizeof(T);
+}
 __device__ __forceinline__ void store_elem(__nv_bfloat16* p, size_t i, float x) {
     p[i] = __float2bfloat16_rn(x);
 }
@@ -178,13 +190,49 @@ kda_recurrent_kernel(const RecurrentParams p) {
         ck_next = bos + p.ckpt_interval - 1;
     }
 
+    extern __shared__ __align__(16) unsigned char rc_stage[];
+    T* cq = reinterpret_cast<T*>(rc_stage);   // [kStage][DK]
+    T* ck = cq + kStage * DK;
+    T* cz = ck + kStage * DK;
+    T* cv = cz + kStage * DK;                 // [kStage][DVS]
+    T* cb = cv + kStage * DVS;                // [kStage]
+    int jt = kStage;                          // position in the staged tokens
+    auto stage = [&](int64_t t0, int n) {
+        constexpr int VE = 16 / sizeof(T);
+        constexpr int RK = DK / VE, RV = DVS / VE;
+        for (int e = tid; e < n * RK; e += kThreads) {
+            const int j = e / RK, c4 = e - j * RK;
+            const size_t g = ((size_t)(t0 + j) * H + h) * DK + (size_t)c4 * VE;
+            const int l = j * DK + c4 * VE;
+            *reinterpret_cast<uint4*>(cq + l) = __ldg(reinterpret_cast<const uint4*>(q + g));
+            *reinterpret_cast<uint4*>(ck + l) = __ldg(reinterpret_cast<const uint4*>(k + g));
+            *reinterpret_cast<uint4*>(cz + l) = __ldg(reinterpret_cast<const uint4*>(z + g));
+        }
+        for (int e = tid; e < n * RV; e += kThreads) {
+            const int j = e / RV, c4 = e - j * RV;
+            const size_t g = ((size_t)(t0 + j) * H + h) * DV + col0 + (size_t)c4 * VE;
+            *reinterpret_cast<uint4*>(cv + j * DVS + c4 * VE) =
+                __ldg(reinterpret_cast<const uint4*>(v + g));
+        }
+        if (tid < n) {
+            cb[tid] = beta[(size_t)(t0 + tid) * H + h];
+        }
+        __syncthreads();
+    };
+
     for (int64_t t = bos; t < eos; ++t) {
+        if constexpr (!kDecode) {
+            if (jt == kStage) {
+                stage(t, (int)min((int64_t)kStage, eos - t));
+                jt = 0;
+            }
+        }
         // ---- stage 1: token inputs, gate, norm partial sums ----
         const size_t rk = ((size_t)t * H + h) * DK;
         if (tid < DK) {
-            const float qv = load_elem(q, rk + tid);
-            const float kv = load_elem(k, rk + tid);
-            const float zv = load_elem(z, rk + tid);
+            const float qv = kDecode ? load_elem(q, rk + tid) : to_f(cq[jt * DK + tid]);
+            const float kv = kDecode ? load_elem(k, rk + tid) : to_f(ck[jt * DK + tid]);
+            const float zv = kDecode ? load_elem(z, rk + tid) : to_f(cz[jt * DK + tid]);
             s_q[tid] = qv;
             s_k[tid] = kv;
             // alpha = e^g: K3's g = -5 sigmoid(e^A z), or Kimi Linear's
@@ -205,11 +253,13 @@ kda_recurrent_kernel(const RecurrentParams p) {
             }
         } else if (tid < DK + DVS) {
             const int j = tid - DK;
-            s_v[j] = load_elem(v, ((size_t)t * H + h) * DV + col0 + j);
+            s_v[j] = kDecode ? load_elem(v, ((size_t)t * H + h) * DV + col0 + j)
+                             : to_f(cv[jt * DVS + j]);
             if (j == 0) {
-                s_beta = load_elem(beta, (size_t)t * H + h);
+                s_beta = kDecode ? load_elem(beta, (size_t)t * H + h) : to_f(cb[jt]);
             }
         }
+        ++jt;
         __syncthreads();
 
         float sq = 0.f, sk = 0.f, sqk = 0.f;
@@ -322,9 +372,23 @@ constexpr int prefill_split() { return DV / 32; }
 template <int DK, int DV, int NS, typename T, int kMode>
 void launch_one(const RecurrentParams& p, cudaStream_t stream) {
     const dim3 grid((unsigned)((int64_t)p.rows * p.H * NS));
-    if (grid.x > 0) {
-        kda_recurrent_kernel<DK, DV, NS, T, kMode><<<grid, kThreads, 0, stream>>>(p);
+    if (grid.x == 0) {
+        return;
     }
+    // decode has one token per row: no staging, no dynamic shared memory
+    constexpr size_t smem = kMode == kModeDecode ? 0 : stage_bytes<DK, DV / NS, T>();
+    if (smem > 0) {
+        static bool configured = false;   // per instantiation; setting it again is harmless
+        if (!configured) {
+            if (cudaFuncSetAttribute(kda_recurrent_kernel<DK, DV, NS, T, kMode>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem) != cudaSuccess) {
+                return;   // the launch error below reports it
+            }
+            configured = true;
+        }
+    }
+    kda_recurrent_kernel<DK, DV, NS, T, kMode><<<grid, kThreads, smem, stream>>>(p);
 }
 
 template <int DK, int DV, typename T>
