@@ -210,6 +210,29 @@ def run_oracle_sample(T_sample: int, H: int, d: int, seed: int = 0):
     return T_sample / dt, dt, threads
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (from /proc/cpuinfo, else the platform)."""
+    import platform
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                key = line.split(":", 1)[0].strip().lower()
+                if key in ("model name", "cpu model"):
+                    return line.split(":", 1)[1].strip()
+        with open("/proc/cpuinfo") as fh:   # Arm: implementer / part numbers
+            fields = {}
+            for line in fh:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip(), v.strip())
+            if "CPU part" in fields:
+                return (f"{platform.machine()} implementer {fields.get('CPU implementer', '?')} "
+                        f"part {fields['CPU part']}")
+    except OSError:
+        pass
+    return platform.machine() or "unknown"
+
+
 def cpu_baseline(H: int, T: int, d: int, cpu_seconds: float = 12.0):
     """The oracle on the whole prefill workload, repeated until about
     cpu_seconds of CPU work (wall time x threads) are spent."""
@@ -250,7 +273,7 @@ def reference_arm(args, world, rank, pg):
         "config": {"workload": "prefill B=1 H=32 T=4096 d_k=d_v=128 bf16 inputs", "B": 1,
                    "H": 32, "T": 4096, "d": 128},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": sample, "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -633,7 +656,7 @@ def finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops
                    "clocks": dclk_summary},
         **extras,
         "cpu_baseline": {"value": cpu_tps, "unit": "tokens/s", "cores": cpu_threads,
-                         "kind": "oracle", "sample": cpu_sample},
+                         "kind": "oracle", "sample": cpu_sample, "cpu_model": cpu_model()},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
