@@ -355,6 +355,12 @@ def kda_arm(args, world, rank, local, pg):
     value = world * B * T / (ms_per_step / 1e3)
     achieved_gbs = byts / (kernel_ms / 1e3) / 1e9
     achieved_tf = flops / (kernel_ms / 1e3) / 1e12
+    if args.only == "softplus":
+        sp = measure_softplus(sets, ws, o, S, cu_host, args, stream)
+        if rank == 0:
+            print(json.dumps(dict(sp, only="softplus",
+                                  tokens_per_s=B * T / (sp["kernel_ms"] / 1e3))), flush=True)
+        return
     if args.only == "backward":
         bw = measure_backward(sets, B, H, T, d, args, stream)
         if rank == 0:
@@ -671,7 +677,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["kda", "reference"], default="kda")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "conv", "backward"],
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "conv", "backward", "softplus"],
                     default="all",
                     help="run one part only (for profiler captures); the default runs all")
     ap.add_argument("--decode-batch", type=int, default=DECODE_SHAPE["B"],
