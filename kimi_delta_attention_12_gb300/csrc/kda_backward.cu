@@ -556,15 +556,12 @@ kda_backward_dA_kernel(const float* dA_tok, float* dA, int64_t total_T, int H) {
 template <int DK, int DV, typename T>
 cudaError_t launch_main(const BackwardParams& p, dim3 grid, cudaStream_t stream) {
     constexpr size_t smem = chunk_stage_bytes<DK, T>();
-    static bool configured = false;   // the attribute is per kernel; setting it again is harmless
-    if (!configured) {
-        const cudaError_t e = cudaFuncSetAttribute(kda_backward_kernel<DK, DV, T>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   (int)smem);
-        if (e != cudaSuccess) {
-            return e;
-        }
-        configured = true;
+    // the attribute belongs to the current device: set on every launch
+    const cudaError_t e = cudaFuncSetAttribute(kda_backward_kernel<DK, DV, T>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)smem);
+    if (e != cudaSuccess) {
+        return e;
     }
     kda_backward_kernel<DK, DV, T><<<grid, kBwThreads, smem, stream>>>(p);
     return cudaGetLastError();

@@ -370,47 +370,42 @@ template <int DV>
 constexpr int prefill_split() { return DV / 32; }
 
 template <int DK, int DV, int NS, typename T, int kMode>
-void launch_one(const RecurrentParams& p, cudaStream_t stream) {
+cudaError_t launch_one(const RecurrentParams& p, cudaStream_t stream) {
     const dim3 grid((unsigned)((int64_t)p.rows * p.H * NS));
     if (grid.x == 0) {
-        return;
+        return cudaSuccess;
     }
-    // decode has one token per row: no staging, no dynamic shared memory
+    // decode has one token per row: no staging, no dynamic shared memory.
+    // The attribute belongs to the current device, so it is set on every launch.
     constexpr size_t smem = kMode == kModeDecode ? 0 : stage_bytes<DK, DV / NS, T>();
     if (smem > 0) {
-        static bool configured = false;   // per instantiation; setting it again is harmless
-        if (!configured) {
-            if (cudaFuncSetAttribute(kda_recurrent_kernel<DK, DV, NS, T, kMode>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)smem) != cudaSuccess) {
-                return;   // the launch error below reports it
-            }
-            configured = true;
+        const cudaError_t e = cudaFuncSetAttribute(kda_recurrent_kernel<DK, DV, NS, T, kMode>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)smem);
+        if (e != cudaSuccess) {
+            return e;
         }
     }
     kda_recurrent_kernel<DK, DV, NS, T, kMode><<<grid, kThreads, smem, stream>>>(p);
+    return cudaGetLastError();
 }
 
 template <int DK, int DV, typename T>
-void launch_mode(int mode, const RecurrentParams& p, cudaStream_t stream) {
+cudaError_t launch_mode(int mode, const RecurrentParams& p, cudaStream_t stream) {
     constexpr int NSD = decode_split<DV>();
     constexpr int NSP = prefill_split<DV>();
     switch (mode) {
-        case kModeDecode: launch_one<DK, DV, NSD, T, kModeDecode>(p, stream); break;
-        case kModeCkpt: launch_one<DK, DV, NSP, T, kModeCkpt>(p, stream); break;
-        default: launch_one<DK, DV, NSP, T, kModePrefill>(p, stream); break;
+        case kModeDecode: return launch_one<DK, DV, NSD, T, kModeDecode>(p, stream);
+        case kModeCkpt: return launch_one<DK, DV, NSP, T, kModeCkpt>(p, stream);
+        default: return launch_one<DK, DV, NSP, T, kModePrefill>(p, stream);
     }
 }
 
 template <int DK, int DV>
 cudaError_t launch_dims(const RecurrentParams& p, int dtype, cudaStream_t stream) {
     const int mode = p.decode ? kModeDecode : p.ckpt_interval > 0 ? kModeCkpt : kModePrefill;
-    if (dtype == 0) {
-        launch_mode<DK, DV, float>(mode, p, stream);
-    } else {
-        launch_mode<DK, DV, __nv_bfloat16>(mode, p, stream);
-    }
-    return cudaGetLastError();
+    return dtype == 0 ? launch_mode<DK, DV, float>(mode, p, stream)
+                      : launch_mode<DK, DV, __nv_bfloat16>(mode, p, stream);
 }
 
 template <int DK>
