@@ -151,6 +151,23 @@ def _check_cuda(*ts):
                 raise ValueError("KDA tensors must be contiguous")
 
 
+def _expect(t: Optional[torch.Tensor], shape, name: str, dtype: Optional[torch.dtype] = None):
+    """The kernels index raw pointers with the sizes they are given: a tensor
+    of another shape (or dtype) would be read or written out of bounds, so it
+    is refused here."""
+    if t is None:
+        return
+    if tuple(t.shape) != tuple(int(x) for x in shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _nbytes(t: torch.Tensor) -> int:
+    _check_cuda(t)
+    return t.numel() * t.element_size()
+
+
 def prefill_workspace_bytes(N: int, total_T: int, H: int, d_k: int, d_v: int,
                             dtype: torch.dtype) -> int:
     return int(lib().kda_prefill_workspace_bytes(N, total_T, H, d_k, d_v, _dtype_code(dtype)))
@@ -200,13 +217,16 @@ def kda_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: torch.Tens
     for t in (k, v, z, beta):
         if t.dtype != dt:
             raise TypeError("q, k, v, z and beta must share one dtype")
-    _check_cuda(q, k, v, z, beta, A, initial_state, cu_seqlens)
-    if A.dtype != torch.float32:
-        raise TypeError("A must be float32")
-    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
-        raise TypeError("cu_seqlens must be int32")
-    if initial_state is not None and initial_state.dtype != torch.float32:
-        raise TypeError("initial_state must be float32")
+    _check_cuda(q, k, v, z, beta, A, initial_state, cu_seqlens, o, final_state)
+    for name, t in (("k", k), ("z", z)):
+        _expect(t, (total_T, H, d_k), name)
+    _expect(v, (total_T, H, d_v), "v")
+    _expect(beta, (total_T, H), "beta")
+    _expect(A, (H,), "A", torch.float32)
+    _expect(cu_seqlens, (N + 1,), "cu_seqlens", torch.int32)
+    _expect(initial_state, (N, H, d_k, d_v), "initial_state", torch.float32)
+    _expect(o, (total_T, H, d_v), "o", dt)
+    _expect(final_state, (N, H, d_k, d_v), "final_state", torch.float32)
     if o is None:
         o = torch.empty(total_T, H, d_v, dtype=dt, device=q.device)
     if final_state is None and output_final_state:
@@ -223,20 +243,28 @@ def kda_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: torch.Tens
         _check_cuda(ckpt_pool, ckpt_slots)
         if ckpt_pool is None or ckpt_pool.dtype != torch.float32:
             raise TypeError("ckpt_pool must be a float32 tensor")
-        if ckpt_slots is not None and ckpt_slots.dtype != torch.int32:
-            raise TypeError("ckpt_slots must be int32")
+        _expect(ckpt_pool, (ckpt_pool.shape[0], H, d_k, d_v), "ckpt_pool", torch.float32)
+        if ckpt_slots is not None:
+            if ckpt_slots.dtype != torch.int32 or ckpt_slots.dim() != 1:
+                raise TypeError("ckpt_slots must be a 1-D int32 tensor")
+            cu_h = host_cu if host_cu is not None else (
+                None if cu_seqlens is None else cu_seqlens.to("cpu", torch.int32))
+            need = checkpoint_count(cu_h, N, total_T, int(ckpt_interval))
+            if need >= 0 and ckpt_slots.numel() < need:
+                raise ValueError(f"ckpt_slots has {ckpt_slots.numel()} entries for {need} "
+                                 "checkpoints")
         st = lib().kda_prefill_checkpointed(
             _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(initial_state),
             _ptr(cu_seqlens), host_ptr, N, total_T, H, d_k, d_v, _dtype_code(dt),
             float(scale), flags, _ptr(o), _ptr(final_state), int(ckpt_interval),
             _ptr(ckpt_pool), _ptr(ckpt_slots), ckpt_pool.shape[0], _ptr(workspace),
-            workspace.numel(), _stream_ptr(stream))
+            _nbytes(workspace), _stream_ptr(stream))
         name = "kda_prefill_checkpointed"
     else:
         st = lib().kda_prefill(
             _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(initial_state),
             _ptr(cu_seqlens), host_ptr, N, total_T, H, d_k, d_v, _dtype_code(dt),
-            float(scale), flags, _ptr(o), _ptr(final_state), _ptr(workspace), workspace.numel(),
+            float(scale), flags, _ptr(o), _ptr(final_state), _ptr(workspace), _nbytes(workspace),
             _stream_ptr(stream))
         name = "kda_prefill"
     if st != KDA_OK:
@@ -261,6 +289,19 @@ def workspace_status(workspace: torch.Tensor, stream: Optional[torch.cuda.Stream
     return int(lib().kda_workspace_status(_ptr(workspace), _stream_ptr(stream)))
 
 
+def _expect_decode(q, k, v, z, beta, A, state, slots, o):
+    B, H, d_k = q.shape
+    d_v = v.shape[-1]
+    for name, t in (("k", k), ("z", z)):
+        _expect(t, (B, H, d_k), name, q.dtype)
+    _expect(v, (B, H, d_v), "v", q.dtype)
+    _expect(beta, (B, H), "beta", q.dtype)
+    _expect(A, (H,), "A", torch.float32)
+    _expect(state, (state.shape[0], H, d_k, d_v), "state", torch.float32)
+    _expect(slots, (B,), "slots", torch.int32)
+    _expect(o, (B, H, d_v), "o", q.dtype)
+
+
 def kda_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: torch.Tensor,
                     beta: torch.Tensor, A: torch.Tensor, state: torch.Tensor,
                     slots: Optional[torch.Tensor] = None, scale: float = 1.0,
@@ -272,11 +313,8 @@ def kda_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: torch.
     B, H, d_k = q.shape
     d_v = v.shape[-1]
     dt = q.dtype
-    _check_cuda(q, k, v, z, beta, A, state, slots)
-    if state.dtype != torch.float32:
-        raise TypeError("state must be float32")
-    if slots is not None and slots.dtype != torch.int32:
-        raise TypeError("slots must be int32")
+    _check_cuda(q, k, v, z, beta, A, state, slots, o)
+    _expect_decode(q, k, v, z, beta, A, state, slots, o)
     if o is None:
         o = torch.empty(B, H, d_v, dtype=dt, device=q.device)
     flags = (KDA_FLAG_L2NORM_QK if l2norm else 0) | (KDA_FLAG_SOFTPLUS_GATE if softplus_gate else 0)
@@ -317,14 +355,20 @@ def kda_short_conv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, conv_w: to
     _check_cuda(q, k, v, conv_w, conv_state_in, conv_state_out, cu_seqlens)
     if conv_w.dtype != torch.float32 or conv_w.dim() != 3:
         raise TypeError("conv_w must be a float32 [H, 2 d_k + d_v, W] tensor")
-    for st_ in (conv_state_in, conv_state_out):
-        if st_ is not None and st_.dtype != dt:
-            raise TypeError("conv states must have the dtype of q")
-    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
-        raise TypeError("cu_seqlens must be int32")
+    W = conv_w.shape[-1]
+    Cc = 2 * d_k + d_v
+    _expect(k, (total_T, H, d_k), "k")
+    _expect(v, (total_T, H, d_v), "v")
+    _expect(conv_w, (H, Cc, W), "conv_w", torch.float32)
+    _expect(conv_state_in, (N, H, W - 1, Cc), "conv_state_in", dt)
+    _expect(conv_state_out, (N, H, W - 1, Cc), "conv_state_out", dt)
+    _expect(cu_seqlens, (N + 1,), "cu_seqlens", torch.int32)
     if outputs is None:
         outputs = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
     qo, ko, vo = outputs
+    _check_cuda(qo, ko, vo)
+    for name, t, ref in (("q_out", qo, q), ("k_out", ko, k), ("v_out", vo, v)):
+        _expect(t, tuple(ref.shape), name, dt)
     host_cu = None if cu_seqlens_host is None else cu_seqlens_host.to(torch.int32).contiguous()
     host_ptr = None if host_cu is None else ctypes.c_void_p(host_cu.data_ptr())
     st = lib().kda_short_conv(
@@ -358,15 +402,13 @@ def kda_decode_step_conv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: t
     B, H, d_k = q.shape
     d_v = v.shape[-1]
     dt = q.dtype
-    _check_cuda(q, k, v, z, beta, A, state, conv_w, conv_state, slots)
-    if state.dtype != torch.float32:
-        raise TypeError("state must be float32")
+    _check_cuda(q, k, v, z, beta, A, state, conv_w, conv_state, slots, o)
+    _expect_decode(q, k, v, z, beta, A, state, slots, o)
     if conv_w.dtype != torch.float32 or conv_w.dim() != 3:
         raise TypeError("conv_w must be a float32 [H, 2 d_k + d_v, W] tensor")
-    if conv_state is not None and conv_state.dtype != dt:
-        raise TypeError("conv_state must have the dtype of q")
-    if slots is not None and slots.dtype != torch.int32:
-        raise TypeError("slots must be int32")
+    W = conv_w.shape[-1]
+    _expect(conv_w, (H, 2 * d_k + d_v, W), "conv_w", torch.float32)
+    _expect(conv_state, (state.shape[0], H, W - 1, 2 * d_k + d_v), "conv_state", dt)
     if o is None:
         o = torch.empty(B, H, d_v, dtype=dt, device=q.device)
     if workspace is None:
@@ -377,7 +419,7 @@ def kda_decode_step_conv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: t
     st = lib().kda_decode_step_conv(
         _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(state), _ptr(slots),
         state.shape[0], _ptr(conv_w), _ptr(conv_state), conv_w.shape[-1], B, H, d_k, d_v,
-        _dtype_code(dt), float(scale), flags, _ptr(o), _ptr(workspace), workspace.numel(),
+        _dtype_code(dt), float(scale), flags, _ptr(o), _ptr(workspace), _nbytes(workspace),
         _stream_ptr(stream))
     if st != KDA_OK:
         raise KDAError(st, "kda_decode_step_conv")
@@ -411,8 +453,15 @@ def kda_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: torch.Ten
         if t.dtype != dt:
             raise TypeError("q, k, v, z, beta and dO must share one dtype")
     _check_cuda(q, k, v, z, beta, A, dO, initial_state, cu_seqlens, dS_final)
-    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
-        raise TypeError("cu_seqlens must be int32")
+    for name, t in (("k", k), ("z", z)):
+        _expect(t, (total_T, H, d_k), name)
+    _expect(v, (total_T, H, d_v), "v")
+    _expect(beta, (total_T, H), "beta")
+    _expect(dO, (total_T, H, d_v), "dO")
+    _expect(A, (H,), "A", torch.float32)
+    _expect(cu_seqlens, (N + 1,), "cu_seqlens", torch.int32)
+    _expect(initial_state, (N, H, d_k, d_v), "initial_state", torch.float32)
+    _expect(dS_final, (N, H, d_k, d_v), "dS_final", torch.float32)
     dev = q.device
     f32 = dict(dtype=torch.float32, device=dev)
     g = dict(dq=torch.empty(total_T, H, d_k, **f32), dk=torch.empty(total_T, H, d_k, **f32),
@@ -430,7 +479,7 @@ def kda_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: torch.Ten
         _ptr(cu_seqlens), host_ptr, N, total_T, H, d_k, d_v, _dtype_code(dt), float(scale),
         flags, _ptr(dO), _ptr(dS_final), _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]),
         _ptr(g["dz"]), _ptr(g["dbeta"]), _ptr(g["dA"]), _ptr(g["dS0"]), _ptr(workspace),
-        workspace.numel(), _stream_ptr(stream))
+        _nbytes(workspace), _stream_ptr(stream))
     if st != KDA_OK:
         raise KDAError(st, "kda_backward")
     return g
@@ -453,6 +502,20 @@ def kda_state_io(op: int, dst: torch.Tensor, src: Optional[torch.Tensor] = None,
         src.shape[0] if op == KDA_STATE_GATHER else 0)
     if op != KDA_STATE_COPY:
         _check_cuda(dst, src, slots)
+    elif not dst.is_contiguous() or (src is not None and not src.is_contiguous()):
+        raise ValueError("KDA tensors must be contiguous")
+    # the kernels and copies move n whole states: every operand must hold them
+    for name, t in (("dst", dst), ("src", src)):
+        if t is not None:
+            if t.dtype != torch.float32 or t.dim() != 4 or tuple(t.shape[1:]) != (H, d_k, d_v):
+                raise ValueError(f"{name} must be a float32 [*, {H}, {d_k}, {d_v}] tensor")
+    _expect(slots, (int(n),), "slots", torch.int32)
+    if slots is None and dst.shape[0] < n:
+        raise ValueError(f"dst holds {dst.shape[0]} states, {n} are written")
+    if op in (KDA_STATE_COPY, KDA_STATE_SCATTER) and src is not None and src.shape[0] < n:
+        raise ValueError(f"src holds {src.shape[0]} states, {n} are read")
+    if op == KDA_STATE_GATHER and dst.shape[0] < n:
+        raise ValueError(f"dst holds {dst.shape[0]} states, {n} are written")
     st = lib().kda_state_io(int(op), _ptr(dst), _ptr(src), _ptr(slots), int(n), int(pool),
                             H, d_k, d_v, _stream_ptr(stream))
     if st != KDA_OK:
