@@ -47,17 +47,16 @@ __device__ __forceinline__ float load_elem(const __nv_bfloat16* p, size_t i) {
     return __bfloat162float(p[i]);
 }
 __device__ __forceinline__ void store_elem(float* p, size_t i, float x) { p[i] = x; }
-// a value of the input dtype as float (any memory space)
-__device__ __forceinline__ float to_f(float x) { return x; }
-__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
 
-// Prefill stages the next kStage tokens' inputs (q, k, z, the CTA's v
-// columns, beta) in dynamic shared memory with 16-byte loads, so that no
-// token of the serial loop waits on a global load round trip.
+// Prefill prepares the next kStage tokens at once, in dynamic shared memory
+// (fp32): the normalised and scaled q_hat, k_hat, the decay alpha, the CTA's
+// v columns, beta and q_hat . k_hat.  These depend on the inputs only, so the
+// whole CTA computes them in parallel (one warp per token); the token-serial
+// loop is then left with the state update and two CTA barriers per token.
 constexpr int kStage = 64;
 template <int DK, int DVS, typename T>
 constexpr size_t stage_bytes() {
-    return (size_t)kStage * (3 * DK + DVS + 1) * sizeof(T);
+    return (size_t)kStage * (3 * DK + DVS + 2) * sizeof(float);
 }
 __device__ __forceinline__ void store_elem(__nv_bfloat16* p, size_t i, float x) {
     p[i] = __float2bfloat16_rn(x);
@@ -191,48 +190,150 @@ kda_recurrent_kernel(const RecurrentParams p) {
     }
 
     extern __shared__ __align__(16) unsigned char rc_stage[];
-    T* cq = reinterpret_cast<T*>(rc_stage);   // [kStage][DK]
-    T* ck = cq + kStage * DK;
-    T* cz = ck + kStage * DK;
-    T* cv = cz + kStage * DK;                 // [kStage][DVS]
-    T* cb = cv + kStage * DVS;                // [kStage]
-    int jt = kStage;                          // position in the staged tokens
-    auto stage = [&](int64_t t0, int n) {
-        constexpr int VE = 16 / sizeof(T);
-        constexpr int RK = DK / VE, RV = DVS / VE;
-        for (int e = tid; e < n * RK; e += kThreads) {
-            const int j = e / RK, c4 = e - j * RK;
-            const size_t g = ((size_t)(t0 + j) * H + h) * DK + (size_t)c4 * VE;
-            const int l = j * DK + c4 * VE;
-            *reinterpret_cast<uint4*>(cq + l) = __ldg(reinterpret_cast<const uint4*>(q + g));
-            *reinterpret_cast<uint4*>(ck + l) = __ldg(reinterpret_cast<const uint4*>(k + g));
-            *reinterpret_cast<uint4*>(cz + l) = __ldg(reinterpret_cast<const uint4*>(z + g));
-        }
-        for (int e = tid; e < n * RV; e += kThreads) {
-            const int j = e / RV, c4 = e - j * RV;
-            const size_t g = ((size_t)(t0 + j) * H + h) * DV + col0 + (size_t)c4 * VE;
-            *reinterpret_cast<uint4*>(cv + j * DVS + c4 * VE) =
-                __ldg(reinterpret_cast<const uint4*>(v + g));
-        }
-        if (tid < n) {
-            cb[tid] = beta[(size_t)(t0 + tid) * H + h];
+    float* sq_h = reinterpret_cast<float*>(rc_stage);   // [kStage][DK] scale q / |q|
+    float* sk_h = sq_h + kStage * DK;                   // [kStage][DK] k / |k|
+    float* sa_h = sk_h + kStage * DK;                   // [kStage][DK] alpha
+    float* sv_h = sa_h + kStage * DK;                   // [kStage][DVS]
+    float* sb_h = sv_h + kStage * DVS;                  // [kStage] beta
+    float* sd_h = sb_h + kStage;                        // [kStage] q_hat . k_hat
+    // tokens t0 .. t0+n-1: warp w prepares tokens w, w + 8, ...; lane l holds
+    // channels l, l + 32, ... of q, k, z (and column l of v when l < DVS)
+    auto prepare = [&](int64_t t0, int n) {
+        constexpr int CPL = DK / 32;
+        for (int j = w; j < n; j += kWarps) {
+            const int64_t t = t0 + j;
+            const size_t rk = ((size_t)t * H + h) * DK;
+            float qv[CPL], kv[CPL], zv[CPL];
+            float sq = 0.f, sk = 0.f, sqk = 0.f;
+#pragma unroll
+            for (int m = 0; m < CPL; ++m) {
+                qv[m] = load_elem(q, rk + lane + 32 * m);
+                kv[m] = load_elem(k, rk + lane + 32 * m);
+                zv[m] = load_elem(z, rk + lane + 32 * m);
+                sq += qv[m] * qv[m];
+                sk += kv[m] * kv[m];
+                sqk += qv[m] * kv[m];
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                sq += __shfl_xor_sync(0xffffffffu, sq, off);
+                sk += __shfl_xor_sync(0xffffffffu, sk, off);
+                sqk += __shfl_xor_sync(0xffffffffu, sqk, off);
+            }
+            const float iq = p.l2norm ? rsqrtf(sq + kNormEps) : 1.0f;
+            const float ik = p.l2norm ? rsqrtf(sk + kNormEps) : 1.0f;
+#pragma unroll
+            for (int m = 0; m < CPL; ++m) {
+                const int c = lane + 32 * m;
+                sq_h[j * DK + c] = qv[m] * iq * scale;
+                sk_h[j * DK + c] = kv[m] * ik;
+                // alpha = e^g: K3's g = -5 sigmoid(e^A z), or Kimi Linear's
+                // g = -softplus(e^A z), for which e^g = sigmoid(-e^A z)
+                const float sg = sigmoid_f(p.softplus_gate ? -eA * zv[m] : eA * zv[m]);
+                sa_h[j * DK + c] = p.softplus_gate ? sg : expf(kGmin * sg);
+            }
+            if (lane < DVS) {
+                sv_h[j * DVS + lane] = load_elem(v, ((size_t)t * H + h) * DV + col0 + lane);
+            }
+            if (lane == 0) {
+                sb_h[j] = load_elem(beta, (size_t)t * H + h);
+                sd_h[j] = sqk * iq * ik * scale;
+            }
         }
         __syncthreads();
     };
 
-    for (int64_t t = bos; t < eos; ++t) {
-        if constexpr (!kDecode) {
-            if (jt == kStage) {
-                stage(t, (int)min((int64_t)kStage, eos - t));
-                jt = 0;
+    if constexpr (!kDecode) {
+        static_assert(DVS <= 32, "prefill CTAs hold at most 32 value columns");
+        for (int64_t t0 = bos; t0 < eos; t0 += kStage) {
+            const int n = (int)min((int64_t)kStage, eos - t0);
+            __syncthreads();   // the previous stretch's last token has been read
+            prepare(t0, n);
+            for (int jt = 0; jt < n; ++jt) {
+                const int64_t t = t0 + jt;
+                // ---- decay, and the two column sums of S' ----
+                float4 ak = make_float4(0.f, 0.f, 0.f, 0.f);
+                float4 aq = make_float4(0.f, 0.f, 0.f, 0.f);
+                float kreg[RPT];
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) {
+                    const int i = r * RSTEP + w * RPW + rs;
+                    const float a = sa_h[jt * DK + i];
+                    const float kk = sk_h[jt * DK + i];
+                    const float qq = sq_h[jt * DK + i];
+                    kreg[r] = kk;
+                    S[r].x *= a; S[r].y *= a; S[r].z *= a; S[r].w *= a;
+                    ak.x += kk * S[r].x; ak.y += kk * S[r].y;
+                    ak.z += kk * S[r].z; ak.w += kk * S[r].w;
+                    aq.x += qq * S[r].x; aq.y += qq * S[r].y;
+                    aq.z += qq * S[r].z; aq.w += qq * S[r].w;
+                }
+#pragma unroll
+                for (int off = LPR; off < 32; off <<= 1) {
+                    ak.x += __shfl_xor_sync(0xffffffffu, ak.x, off);
+                    ak.y += __shfl_xor_sync(0xffffffffu, ak.y, off);
+                    ak.z += __shfl_xor_sync(0xffffffffu, ak.z, off);
+                    ak.w += __shfl_xor_sync(0xffffffffu, ak.w, off);
+                    aq.x += __shfl_xor_sync(0xffffffffu, aq.x, off);
+                    aq.y += __shfl_xor_sync(0xffffffffu, aq.y, off);
+                    aq.z += __shfl_xor_sync(0xffffffffu, aq.z, off);
+                    aq.w += __shfl_xor_sync(0xffffffffu, aq.w, off);
+                }
+                if (rs == 0) {
+                    *reinterpret_cast<float4*>(&s_red[w][0][4 * cg]) = ak;
+                    *reinterpret_cast<float4*>(&s_red[w][1][4 * cg]) = aq;
+                }
+                __syncthreads();
+                // ---- u and o per value column ----
+                if (tid < DVS) {
+                    float rkj = 0.f, rqj = 0.f;
+#pragma unroll
+                    for (int ww = 0; ww < kWarps; ++ww) {
+                        rkj += s_red[ww][0][tid];
+                        rqj += s_red[ww][1][tid];
+                    }
+                    const float u = sb_h[jt] * (sv_h[jt * DVS + tid] - rkj);
+                    s_u[tid] = u;
+                    store_elem(o, ((size_t)t * H + h) * DV + col0 + tid, rqj + sd_h[jt] * u);
+                }
+                __syncthreads();
+                // ---- rank-1 write ----
+                const float4 u4 = *reinterpret_cast<const float4*>(&s_u[4 * cg]);
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) {
+                    const float kk = kreg[r];
+                    S[r].x += kk * u4.x; S[r].y += kk * u4.y;
+                    S[r].z += kk * u4.z; S[r].w += kk * u4.w;
+                }
+                // ---- state checkpoint after every ckpt_interval tokens of the row ----
+                if constexpr (kCkpt) {
+                    if (t == ck_next) {
+                        const int64_t idx = ck_idx++;
+                        ck_next += p.ckpt_interval;
+                        const int64_t prow = p.ckpt_slots ? (int64_t)p.ckpt_slots[idx] : idx;
+                        if (prow >= 0 && prow < p.ckpt_pool_size) {
+                            float4* cp = reinterpret_cast<float4*>(
+                                p.ckpt_pool + ((size_t)prow * H + h) * DK * DV);
+#pragma unroll
+                            for (int r = 0; r < RPT; ++r) {
+                                const int i = r * RSTEP + w * RPW + rs;
+                                __stcs(cp + (i * DV + col0) / 4 + cg, S[r]);
+                            }
+                        }
+                    }
+                }
             }
         }
+    }
+
+    // decode: one token per row, straight from global memory
+    for (int64_t t = bos; kDecode && t < eos; ++t) {
         // ---- stage 1: token inputs, gate, norm partial sums ----
         const size_t rk = ((size_t)t * H + h) * DK;
         if (tid < DK) {
-            const float qv = kDecode ? load_elem(q, rk + tid) : to_f(cq[jt * DK + tid]);
-            const float kv = kDecode ? load_elem(k, rk + tid) : to_f(ck[jt * DK + tid]);
-            const float zv = kDecode ? load_elem(z, rk + tid) : to_f(cz[jt * DK + tid]);
+            const float qv = load_elem(q, rk + tid);
+            const float kv = load_elem(k, rk + tid);
+            const float zv = load_elem(z, rk + tid);
             s_q[tid] = qv;
             s_k[tid] = kv;
             // alpha = e^g: K3's g = -5 sigmoid(e^A z), or Kimi Linear's
@@ -253,13 +354,11 @@ kda_recurrent_kernel(const RecurrentParams p) {
             }
         } else if (tid < DK + DVS) {
             const int j = tid - DK;
-            s_v[j] = kDecode ? load_elem(v, ((size_t)t * H + h) * DV + col0 + j)
-                             : to_f(cv[jt * DVS + j]);
+            s_v[j] = load_elem(v, ((size_t)t * H + h) * DV + col0 + j);
             if (j == 0) {
-                s_beta = kDecode ? load_elem(beta, (size_t)t * H + h) : to_f(cb[jt]);
+                s_beta = load_elem(beta, (size_t)t * H + h);
             }
         }
-        ++jt;
         __syncthreads();
 
         float sq = 0.f, sk = 0.f, sqk = 0.f;
@@ -330,23 +429,6 @@ kda_recurrent_kernel(const RecurrentParams p) {
             S[r].x += kk * u4.x; S[r].y += kk * u4.y; S[r].z += kk * u4.z; S[r].w += kk * u4.w;
         }
 
-        // ---- state checkpoint after every ckpt_interval tokens of the row ----
-        if constexpr (kCkpt) {
-            if (t == ck_next) {
-                const int64_t idx = ck_idx++;
-                ck_next += p.ckpt_interval;
-                const int64_t prow = p.ckpt_slots ? (int64_t)p.ckpt_slots[idx] : idx;
-                if (prow >= 0 && prow < p.ckpt_pool_size) {
-                    float4* cp = reinterpret_cast<float4*>(p.ckpt_pool +
-                                                           ((size_t)prow * H + h) * DK * DV);
-#pragma unroll
-                    for (int r = 0; r < RPT; ++r) {
-                        const int i = r * RSTEP + w * RPW + rs;
-                        __stcs(cp + (i * DV + col0) / 4 + cg, S[r]);
-                    }
-                }
-            }
-        }
     }
 
     if (p.state_out) {
