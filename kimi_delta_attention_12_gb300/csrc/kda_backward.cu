@@ -25,9 +25,10 @@
 // kernel walks the chunks last to first, recomputes each chunk's states
 // forward into a scratch buffer (S_{t-1} of its 64 tokens), then walks its
 // tokens backwards.  The scratch keeps memory at 64 states per (sequence,
-// head).  Both walks over a chunk read its tokens' inputs (q, k, z, the CTA's
-// v and dO columns, beta) from shared memory, staged once at the chunk start
-// with 16-byte loads, so no token waits on a global load.
+// head).  Both walks over a chunk read its tokens' q_hat, k_hat, alpha, v and
+// dO columns and beta from shared memory, computed once for the chunk by the
+// whole CTA, so the token chain has no global loads, no reductions over the
+// key channels and two barriers per token.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -48,9 +49,6 @@ __device__ __forceinline__ float ldf(const __nv_bfloat16* p, size_t i) {
     return __bfloat162float(p[i]);
 }
 
-// A value of the input dtype as float (any memory space).
-__device__ __forceinline__ float to_f(float x) { return x; }
-__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
 
 __device__ __forceinline__ float bw_sigmoid(float x) {
     if (x >= 0.0f) {
@@ -60,52 +58,22 @@ __device__ __forceinline__ float bw_sigmoid(float x) {
     return e / (1.0f + e);
 }
 
-// Sum over the CTA of one value per thread of warps 0 .. nw-1 (the others
-// pass 0); every thread gets the total.  Uses red[kBwWarps] and two barriers.
-__device__ __forceinline__ float block_sum(float x, float* red) {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        x += __shfl_xor_sync(0xffffffffu, x, off);
-    }
-    if (lane == 0) {
-        red[w] = x;
-    }
-    __syncthreads();
-    float t = 0.0f;
-#pragma unroll
-    for (int i = 0; i < kBwWarps; ++i) {
-        t += red[i];
-    }
-    __syncthreads();
-    return t;
-}
-
 constexpr int kBwCols = 32;   // value columns per CTA
 
-template <int DK>
 struct BwShared {
-    float q[DK];        // raw q, k of the token
-    float k[DK];
-    float a[DK];        // decay a = e^g
-    float v[kBwCols];
-    float dO[kBwCols];
     float u[kBwCols];
     float du[kBwCols];
     float red[kBwWarps][2][kBwCols];
-    float nrm[DK / 32][3];
-    float red1[kBwWarps];
-    float beta;
 };
 
-// Dynamic shared memory of the chunk's token inputs (in the input dtype).
+// Dynamic shared memory of the chunk's prepared token quantities (fp32).
 template <int DK, typename T>
 constexpr size_t chunk_stage_bytes() {
-    return (size_t)kBwChunk * (3 * DK + 2 * kBwCols + 1) * sizeof(T);
+    return (size_t)kBwChunk * (3 * DK + 2 * kBwCols + 2) * sizeof(float);
 }
 
 template <int DK, int DV, typename T>
-__global__ void __launch_bounds__(kBwThreads)
+__global__ void __launch_bounds__(kBwThreads, 2)
 kda_backward_kernel(const BackwardParams p) {
     constexpr int NS = DV / kBwCols;       // CTAs per (sequence, head)
     constexpr int DVS = kBwCols;
@@ -118,7 +86,7 @@ kda_backward_kernel(const BackwardParams p) {
     static_assert(RPT >= 1 && RPT * RSTEP == DK, "bad state tiling");
     static_assert(DK + DVS <= kBwThreads, "token loaders need DK + 32 threads");
 
-    __shared__ BwShared<DK> sh;
+    __shared__ BwShared sh;
 
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     const int cg = lane % LPR, rs = lane / LPR;
@@ -155,99 +123,69 @@ kda_backward_kernel(const BackwardParams p) {
     // float4 index of this thread's part of row r in a full d_k x d_v state
     auto st_idx = [&](int r) { return ((size_t)row_of(r) * DV + col0) / 4 + cg; };
 
-    // ---- the chunk's token inputs, staged in shared memory ----
+    // ---- the chunk's token quantities, prepared in shared memory (fp32) ----
+    // q_hat (normalised, scaled), k_hat, alpha, the CTA's v and dO columns,
+    // beta and q_hat . k_hat depend on the inputs only: the whole CTA computes
+    // them for the chunk (one warp per token) before the two token walks.
     extern __shared__ __align__(16) unsigned char bw_stage[];
-    T* cq = reinterpret_cast<T*>(bw_stage);       // [C][DK]
-    T* ck = cq + C * DK;
-    T* cz = ck + C * DK;
-    T* cv = cz + C * DK;                          // [C][DVS]
-    T* cdo = cv + C * DVS;
-    T* cb = cdo + C * DVS;                        // [C]
-    constexpr int VE = 16 / sizeof(T);            // elements per 16-byte vector
-    int64_t stage_t0 = 0;
-    auto stage_chunk = [&](int64_t t0, int cl) {
-        constexpr int RK = DK / VE, RV = DVS / VE;
-        for (int e = tid; e < cl * RK; e += kBwThreads) {
-            const int j = e / RK, c4 = e - j * RK;
-            const size_t g = ((size_t)(t0 + j) * H + h) * DK + (size_t)c4 * VE;
-            const int l = j * DK + c4 * VE;
-            *reinterpret_cast<uint4*>(cq + l) = __ldg(reinterpret_cast<const uint4*>(q + g));
-            *reinterpret_cast<uint4*>(ck + l) = __ldg(reinterpret_cast<const uint4*>(k + g));
-            *reinterpret_cast<uint4*>(cz + l) = __ldg(reinterpret_cast<const uint4*>(z + g));
-        }
-        for (int e = tid; e < cl * RV; e += kBwThreads) {
-            const int j = e / RV, c4 = e - j * RV;
-            const size_t g = ((size_t)(t0 + j) * H + h) * DV + col0 + (size_t)c4 * VE;
-            const int l = j * DVS + c4 * VE;
-            *reinterpret_cast<uint4*>(cv + l) = __ldg(reinterpret_cast<const uint4*>(v + g));
-            *reinterpret_cast<uint4*>(cdo + l) = __ldg(reinterpret_cast<const uint4*>(dO + g));
-        }
-        if (tid < cl) {
-            cb[tid] = beta[(size_t)(t0 + tid) * H + h];
-        }
-        stage_t0 = t0;
-        __syncthreads();
-    };
-    auto sf = [](const T* a, int i) { return to_f(a[i]); };   // a staged (shared) value
-
-    // ---- one token's inputs into the working arrays, and the norm partials ----
-    auto load_token = [&](int64_t t, bool with_do) {
-        const int jt = (int)(t - stage_t0);
-        if (tid < DK) {
-            const int e = jt * DK + tid;
-            const float qv = sf(cq, e), kv = sf(ck, e), zv = sf(cz, e);
-            sh.q[tid] = qv;
-            sh.k[tid] = kv;
-            const float sg = bw_sigmoid(p.softplus_gate ? -eA * zv : eA * zv);
-            sh.a[tid] = p.softplus_gate ? sg : expf(kBwGmin * sg);
-            float sq = qv * qv, sk = kv * kv, sqk = qv * kv;
+    float* pq = reinterpret_cast<float*>(bw_stage);   // [C][DK]
+    float* pk = pq + C * DK;
+    float* pa = pk + C * DK;
+    float* pv = pa + C * DK;                          // [C][DVS]
+    float* pdo = pv + C * DVS;
+    float* pb = pdo + C * DVS;                        // [C]
+    float* pqk = pb + C;                              // [C]
+    auto prepare = [&](int64_t t0, int cl) {
+        constexpr int CPL = DK / 32;
+        for (int j = w; j < cl; j += kBwWarps) {
+            const int64_t t = t0 + j;
+            const size_t rk = ((size_t)t * H + h) * DK;
+            float qv[CPL], kv[CPL], zv[CPL];
+            float sq = 0.f, sk = 0.f, sqk = 0.f;
+#pragma unroll
+            for (int m = 0; m < CPL; ++m) {
+                qv[m] = ldf(q, rk + lane + 32 * m);
+                kv[m] = ldf(k, rk + lane + 32 * m);
+                zv[m] = ldf(z, rk + lane + 32 * m);
+                sq += qv[m] * qv[m];
+                sk += kv[m] * kv[m];
+                sqk += qv[m] * kv[m];
+            }
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) {
                 sq += __shfl_xor_sync(0xffffffffu, sq, off);
                 sk += __shfl_xor_sync(0xffffffffu, sk, off);
                 sqk += __shfl_xor_sync(0xffffffffu, sqk, off);
             }
-            if (lane == 0) {
-                sh.nrm[w][0] = sq;
-                sh.nrm[w][1] = sk;
-                sh.nrm[w][2] = sqk;
-            }
-        } else if (tid < DK + DVS) {
-            const int j = tid - DK;
-            sh.v[j] = sf(cv, jt * DVS + j);
-            if (with_do) {
-                sh.dO[j] = sf(cdo, jt * DVS + j);
-            }
-            if (j == 0) {
-                sh.beta = sf(cb, jt);
-            }
-        }
-    };
-    struct Norms { float rq, rk, qk; };   // 1/|q|, 1/|k| (or 1), q . k raw
-    auto norms = [&]() {
-        float sq = 0.f, sk = 0.f, sqk = 0.f;
+            const float iq = p.l2norm ? rsqrtf(sq + kBwEps) : 1.0f;
+            const float ik = p.l2norm ? rsqrtf(sk + kBwEps) : 1.0f;
 #pragma unroll
-        for (int i = 0; i < DK / 32; ++i) {
-            sq += sh.nrm[i][0];
-            sk += sh.nrm[i][1];
-            sqk += sh.nrm[i][2];
+            for (int m = 0; m < CPL; ++m) {
+                const int c = lane + 32 * m;
+                pq[j * DK + c] = qv[m] * iq * scale;
+                pk[j * DK + c] = kv[m] * ik;
+                const float sg = bw_sigmoid(p.softplus_gate ? -eA * zv[m] : eA * zv[m]);
+                pa[j * DK + c] = p.softplus_gate ? sg : expf(kBwGmin * sg);
+            }
+            const size_t rv = ((size_t)t * H + h) * DV + col0 + lane;   // lane < 32 = DVS
+            pv[j * DVS + lane] = ldf(v, rv);
+            pdo[j * DVS + lane] = ldf(dO, rv);
+            if (lane == 0) {
+                pb[j] = ldf(beta, (size_t)t * H + h);
+                pqk[j] = sqk * iq * ik * scale;
+            }
         }
-        Norms m;
-        m.rq = p.l2norm ? rsqrtf(sq + kBwEps) : 1.0f;
-        m.rk = p.l2norm ? rsqrtf(sk + kBwEps) : 1.0f;
-        m.qk = sqk;
-        return m;
+        __syncthreads();
     };
 
-    // ---- one forward step on S (registers); token inputs already loaded ----
+    // ---- one forward step on S (registers) for token jt of the chunk ----
     float4 S[RPT];
-    auto forward_step = [&]() {
-        const Norms m = norms();
+    auto forward_step = [&](int jt) {
         float4 ak = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int r = 0; r < RPT; ++r) {
             const int i = row_of(r);
-            const float a = sh.a[i], kk = sh.k[i];
+            const float a = pa[jt * DK + i], kk = pk[jt * DK + i];
             S[r].x *= a; S[r].y *= a; S[r].z *= a; S[r].w *= a;
             ak.x += kk * S[r].x; ak.y += kk * S[r].y; ak.z += kk * S[r].z; ak.w += kk * S[r].w;
         }
@@ -268,13 +206,13 @@ kda_backward_kernel(const BackwardParams p) {
             for (int ww = 0; ww < kBwWarps; ++ww) {
                 r += sh.red[ww][0][tid];
             }
-            sh.u[tid] = sh.beta * (sh.v[tid] - r * m.rk);
+            sh.u[tid] = pb[jt] * (pv[jt * DVS + tid] - r);
         }
         __syncthreads();
         const float4 u4 = *reinterpret_cast<const float4*>(&sh.u[4 * cg]);
 #pragma unroll
         for (int r = 0; r < RPT; ++r) {
-            const float kk = sh.k[row_of(r)] * m.rk;
+            const float kk = pk[jt * DK + row_of(r)];
             S[r].x += kk * u4.x; S[r].y += kk * u4.y; S[r].z += kk * u4.z; S[r].w += kk * u4.w;
         }
     };
@@ -333,8 +271,8 @@ kda_backward_kernel(const BackwardParams p) {
         const int64_t cl = min((int64_t)C, len - i0);
         // 2a: the chunk's states S_{t-1} into the scratch, from the state at
         // the chunk start (the initial state for chunk 0, else checkpoint c)
-        __syncthreads();
-        stage_chunk(bos + i0, (int)cl);
+        __syncthreads();   // the previous chunk's last token has been read
+        prepare(bos + i0, (int)cl);
         if (c > 0) {
             load_state(p.pool + ((size_t)(ck_base + c - 1) * H + h) * SS);
         } else if (p.initial_state) {
@@ -345,31 +283,24 @@ kda_backward_kernel(const BackwardParams p) {
                 S[r] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
-        for (int64_t j = 0; j < cl; ++j) {
+        for (int j = 0; j < (int)cl; ++j) {
             store_state(scratch + (size_t)j * SS, S);
-            if (j + 1 == cl) {
+            if (j + 1 == (int)cl) {
                 break;   // the state after the chunk's last token is not needed
             }
-            load_token(bos + i0 + j, false);
-            __syncthreads();
-            forward_step();
-            __syncthreads();
+            forward_step(j);
         }
-        // 2b: the chunk's tokens in reverse
-        for (int64_t j = cl - 1; j >= 0; --j) {
+        // 2b: the chunk's tokens in reverse (each thread reads back the
+        // scratch elements it wrote: no barrier needed for them)
+        for (int j = (int)cl - 1; j >= 0; --j) {
             const int64_t t = bos + i0 + j;
-            __syncthreads();   // the scratch stores (and the previous token's reads) are done
             load_state(scratch + (size_t)j * SS);        // S = S_{t-1}
-            load_token(t, true);
-            __syncthreads();
-            const Norms m = norms();
-            const float qs = m.rq * scale;
             // column sums: r = S'^T kh and gk = G^T kh (G = dL/dS_t from the future)
             float4 ar = make_float4(0.f, 0.f, 0.f, 0.f), ag = ar;
 #pragma unroll
             for (int r = 0; r < RPT; ++r) {
                 const int i = row_of(r);
-                const float a = sh.a[i], kk = sh.k[i] * m.rk;
+                const float a = pa[j * DK + i], kk = pk[j * DK + i];
                 ar.x += kk * a * S[r].x; ar.y += kk * a * S[r].y;
                 ar.z += kk * a * S[r].z; ar.w += kk * a * S[r].w;
                 ag.x += kk * G[r].x; ag.y += kk * G[r].y; ag.z += kk * G[r].z; ag.w += kk * G[r].w;
@@ -390,8 +321,8 @@ kda_backward_kernel(const BackwardParams p) {
                 *reinterpret_cast<float4*>(&sh.red[w][1][4 * cg]) = ag;
             }
             __syncthreads();
-            // per value column: u, du, dv and the column's share of db
-            float dbj = 0.0f;
+            // per value column (warp 0, one lane per column): u, du, dv and db
+            float* part = p.part + (((size_t)split * p.total_T + t) * H + h) * PW;
             if (tid < DVS) {
                 float rr = 0.f, gk = 0.f;
 #pragma unroll
@@ -399,29 +330,31 @@ kda_backward_kernel(const BackwardParams p) {
                     rr += sh.red[ww][0][tid];
                     gk += sh.red[ww][1][tid];
                 }
-                const float b = sh.beta;
-                const float wv = sh.v[tid] - rr;                   // v - S'^T kh
-                const float qk = m.qk * m.rk * qs;                 // qh . kh
-                const float duj = gk + qk * sh.dO[tid];
+                const float b = pb[j];
+                const float wv = pv[j * DVS + tid] - rr;            // v - S'^T kh
+                const float duj = gk + pqk[j] * pdo[j * DVS + tid];
                 sh.u[tid] = b * wv;
                 sh.du[tid] = duj;
                 p.dv[((size_t)t * H + h) * DV + col0 + tid] = b * duj;
-                dbj = duj * wv;
+                float db = duj * wv;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    db += __shfl_xor_sync(0xffffffffu, db, off);
+                }
+                if (tid == 0) {
+                    part[3 * DK] = db;
+                }
             }
-            const float db = block_sum(dbj, sh.red1);   // two barriers: u, du visible after
-            float* part = p.part + (((size_t)split * p.total_T + t) * H + h) * PW;
-            if (tid == 0) {
-                part[3 * DK] = db;
-            }
+            __syncthreads();
             // per state row: dqh, dkh, da and the new G
             const float4 u4 = *reinterpret_cast<const float4*>(&sh.u[4 * cg]);
             const float4 du4 = *reinterpret_cast<const float4*>(&sh.du[4 * cg]);
-            const float4 do4 = *reinterpret_cast<const float4*>(&sh.dO[4 * cg]);
-            const float b = sh.beta;
+            const float4 do4 = *reinterpret_cast<const float4*>(&pdo[j * DVS + 4 * cg]);
+            const float b = pb[j];
 #pragma unroll
             for (int r = 0; r < RPT; ++r) {
                 const int i = row_of(r);
-                const float a = sh.a[i], kk = sh.k[i] * m.rk, qq = sh.q[i] * qs;
+                const float a = pa[j * DK + i], kk = pk[j * DK + i], qq = pq[j * DK + i];
                 const float4 sp = make_float4(a * S[r].x, a * S[r].y, a * S[r].z, a * S[r].w);
                 const float4 st = make_float4(sp.x + kk * u4.x, sp.y + kk * u4.y,
                                               sp.z + kk * u4.z, sp.w + kk * u4.w);
