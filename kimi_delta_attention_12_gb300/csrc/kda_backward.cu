@@ -291,10 +291,29 @@ kda_backward_kernel(const BackwardParams p) {
             forward_step(j);
         }
         // 2b: the chunk's tokens in reverse (each thread reads back the
-        // scratch elements it wrote: no barrier needed for them)
+        // scratch elements it wrote: no barrier needed for them).  The next
+        // reverse token's S_{t-1} is loaded while this token is worked on.
+        float4 Snext[RPT];
+        {
+            const float4* sp = reinterpret_cast<const float4*>(scratch + (size_t)(cl - 1) * SS);
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) {
+                Snext[r] = sp[st_idx(r)];
+            }
+        }
         for (int j = (int)cl - 1; j >= 0; --j) {
             const int64_t t = bos + i0 + j;
-            load_state(scratch + (size_t)j * SS);        // S = S_{t-1}
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) {
+                S[r] = Snext[r];                           // S = S_{t-1}
+            }
+            if (j > 0) {
+                const float4* sp = reinterpret_cast<const float4*>(scratch + (size_t)(j - 1) * SS);
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) {
+                    Snext[r] = sp[st_idx(r)];
+                }
+            }
             // column sums: r = S'^T kh and gk = G^T kh (G = dL/dS_t from the future)
             float4 ar = make_float4(0.f, 0.f, 0.f, 0.f), ag = ar;
 #pragma unroll
