@@ -47,16 +47,27 @@ __device__ __forceinline__ float load_elem(const __nv_bfloat16* p, size_t i) {
     return __bfloat162float(p[i]);
 }
 __device__ __forceinline__ void store_elem(float* p, size_t i, float x) { p[i] = x; }
+// a value of the input dtype as float, from any memory space (shared included)
+__device__ __forceinline__ float as_float(float x) { return x; }
+__device__ __forceinline__ float as_float(__nv_bfloat16 x) { return __bfloat162float(x); }
 
 // Prefill prepares the next kStage tokens at once, in dynamic shared memory
 // (fp32): the normalised and scaled q_hat, k_hat, the decay alpha, the CTA's
 // v columns, beta and q_hat . k_hat.  These depend on the inputs only, so the
 // whole CTA computes them in parallel (one warp per token); the token-serial
 // loop is then left with the state update and two CTA barriers per token.
+// The stretch's raw inputs are first copied into shared memory with 16-byte
+// loads, all in flight at once; for fp32 inputs they land in the prepared
+// arrays themselves (each warp reads its token's row before overwriting it),
+// for bf16 in a raw area after them.
 constexpr int kStage = 64;
 template <int DK, int DVS, typename T>
+constexpr size_t stage_raw_bytes() {
+    return sizeof(T) == 4 ? 0 : (size_t)kStage * (3 * DK + DVS + 1) * sizeof(T);
+}
+template <int DK, int DVS, typename T>
 constexpr size_t stage_bytes() {
-    return (size_t)kStage * (3 * DK + DVS + 2) * sizeof(float);
+    return (size_t)kStage * (3 * DK + DVS + 2) * sizeof(float) + stage_raw_bytes<DK, DVS, T>();
 }
 __device__ __forceinline__ void store_elem(__nv_bfloat16* p, size_t i, float x) {
     p[i] = __float2bfloat16_rn(x);
@@ -196,24 +207,56 @@ kda_recurrent_kernel(const RecurrentParams p) {
     float* sv_h = sa_h + kStage * DK;                   // [kStage][DVS]
     float* sb_h = sv_h + kStage * DVS;                  // [kStage] beta
     float* sd_h = sb_h + kStage;                        // [kStage] q_hat . k_hat
-    // tokens t0 .. t0+n-1: warp w prepares tokens w, w + 8, ...; lane l holds
-    // channels l, l + 32, ... of q, k, z (and column l of v when l < DVS)
+    // raw inputs of the stretch: in place (fp32) or in the raw area (bf16)
+    unsigned char* raw_area = rc_stage + (size_t)kStage * (3 * DK + DVS + 2) * sizeof(float);
+    T* rq = sizeof(T) == 4 ? reinterpret_cast<T*>(sq_h) : reinterpret_cast<T*>(raw_area);
+    T* rk_ = sizeof(T) == 4 ? reinterpret_cast<T*>(sk_h) : rq + kStage * DK;
+    T* rz = sizeof(T) == 4 ? reinterpret_cast<T*>(sa_h) : rk_ + kStage * DK;
+    T* rv = sizeof(T) == 4 ? reinterpret_cast<T*>(sv_h) : rz + kStage * DK;
+    T* rb = sizeof(T) == 4 ? reinterpret_cast<T*>(sb_h) : rv + kStage * DVS;
+    auto stage_raw = [&](int64_t t0, int n) {
+        constexpr int VE = 16 / sizeof(T);
+        constexpr int RK = DK / VE, RV = DVS / VE;
+        for (int e = tid; e < n * RK; e += kThreads) {
+            const int j = e / RK, c4 = e - j * RK;
+            const size_t g = ((size_t)(t0 + j) * H + h) * DK + (size_t)c4 * VE;
+            const int l = j * DK + c4 * VE;
+            *reinterpret_cast<uint4*>(rq + l) = __ldg(reinterpret_cast<const uint4*>(q + g));
+            *reinterpret_cast<uint4*>(rk_ + l) = __ldg(reinterpret_cast<const uint4*>(k + g));
+            *reinterpret_cast<uint4*>(rz + l) = __ldg(reinterpret_cast<const uint4*>(z + g));
+        }
+        for (int e = tid; e < n * RV; e += kThreads) {
+            const int j = e / RV, c4 = e - j * RV;
+            const size_t g = ((size_t)(t0 + j) * H + h) * DV + col0 + (size_t)c4 * VE;
+            *reinterpret_cast<uint4*>(rv + j * DVS + c4 * VE) =
+                __ldg(reinterpret_cast<const uint4*>(v + g));
+        }
+        if (tid < n) {
+            rb[tid] = beta[(size_t)(t0 + tid) * H + h];
+        }
+        __syncthreads();
+    };
+    // tokens t0 .. t0+n-1 from the raw copy: warp w prepares tokens w, w + 8,
+    // ...; lane l holds channels l, l + 32, ... (and column l of v, l < DVS)
     auto prepare = [&](int64_t t0, int n) {
         constexpr int CPL = DK / 32;
+        stage_raw(t0, n);
         for (int j = w; j < n; j += kWarps) {
-            const int64_t t = t0 + j;
-            const size_t rk = ((size_t)t * H + h) * DK;
             float qv[CPL], kv[CPL], zv[CPL];
             float sq = 0.f, sk = 0.f, sqk = 0.f;
 #pragma unroll
             for (int m = 0; m < CPL; ++m) {
-                qv[m] = load_elem(q, rk + lane + 32 * m);
-                kv[m] = load_elem(k, rk + lane + 32 * m);
-                zv[m] = load_elem(z, rk + lane + 32 * m);
+                const int c = j * DK + lane + 32 * m;
+                qv[m] = as_float(rq[c]);
+                kv[m] = as_float(rk_[c]);
+                zv[m] = as_float(rz[c]);
                 sq += qv[m] * qv[m];
                 sk += kv[m] * kv[m];
                 sqk += qv[m] * kv[m];
             }
+            const float vv = lane < DVS ? as_float(rv[j * DVS + lane]) : 0.0f;
+            const float bv = as_float(rb[j]);
+            __syncwarp();   // (fp32: the row is read before it is overwritten)
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) {
                 sq += __shfl_xor_sync(0xffffffffu, sq, off);
@@ -233,10 +276,10 @@ kda_recurrent_kernel(const RecurrentParams p) {
                 sa_h[j * DK + c] = p.softplus_gate ? sg : expf(kGmin * sg);
             }
             if (lane < DVS) {
-                sv_h[j * DVS + lane] = load_elem(v, ((size_t)t * H + h) * DV + col0 + lane);
+                sv_h[j * DVS + lane] = vv;
             }
             if (lane == 0) {
-                sb_h[j] = load_elem(beta, (size_t)t * H + h);
+                sb_h[j] = bv;
                 sd_h[j] = sqk * iq * ik * scale;
             }
         }
