@@ -50,6 +50,9 @@ __device__ __forceinline__ float ldf(const __nv_bfloat16* p, size_t i) {
 }
 
 
+__device__ __forceinline__ float as_f32(float x) { return x; }
+__device__ __forceinline__ float as_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
 __device__ __forceinline__ float bw_sigmoid(float x) {
     if (x >= 0.0f) {
         return 1.0f / (1.0f + expf(-x));
@@ -66,10 +69,17 @@ struct BwShared {
     float red[kBwWarps][2][kBwCols];
 };
 
-// Dynamic shared memory of the chunk's prepared token quantities (fp32).
+// Dynamic shared memory of the chunk's prepared token quantities (fp32),
+// then, for 16-bit inputs, the chunk's raw inputs (fp32 inputs are copied in
+// place into the prepared arrays).
+template <int DK, typename T>
+constexpr size_t chunk_raw_bytes() {
+    return sizeof(T) == 4 ? 0 : (size_t)kBwChunk * (3 * DK + 2 * kBwCols + 1) * sizeof(T);
+}
 template <int DK, typename T>
 constexpr size_t chunk_stage_bytes() {
-    return (size_t)kBwChunk * (3 * DK + 2 * kBwCols + 2) * sizeof(float);
+    return (size_t)kBwChunk * (3 * DK + 2 * kBwCols + 2) * sizeof(float) +
+           chunk_raw_bytes<DK, T>();
 }
 
 template <int DK, int DV, typename T>
@@ -125,8 +135,9 @@ kda_backward_kernel(const BackwardParams p) {
 
     // ---- the chunk's token quantities, prepared in shared memory (fp32) ----
     // q_hat (normalised, scaled), k_hat, alpha, the CTA's v and dO columns,
-    // beta and q_hat . k_hat depend on the inputs only: the whole CTA computes
-    // them for the chunk (one warp per token) before the two token walks.
+    // beta and q_hat . k_hat depend on the inputs only: the whole CTA first
+    // copies the chunk's raw inputs in with 16-byte loads, all in flight at
+    // once, then computes them (one warp per token) before the two token walks.
     extern __shared__ __align__(16) unsigned char bw_stage[];
     float* pq = reinterpret_cast<float*>(bw_stage);   // [C][DK]
     float* pk = pq + C * DK;
@@ -135,22 +146,71 @@ kda_backward_kernel(const BackwardParams p) {
     float* pdo = pv + C * DVS;
     float* pb = pdo + C * DVS;                        // [C]
     float* pqk = pb + C;                              // [C]
+    // the raw copy: in place for fp32 inputs, after the prepared arrays else
+    T* rq;
+    T* rk_;
+    T* rz;
+    T* rv;
+    T* rdo;
+    T* rb;
+    if constexpr (sizeof(T) == 4) {
+        rq = reinterpret_cast<T*>(pq);
+        rk_ = reinterpret_cast<T*>(pk);
+        rz = reinterpret_cast<T*>(pa);
+        rv = reinterpret_cast<T*>(pv);
+        rdo = reinterpret_cast<T*>(pdo);
+        rb = reinterpret_cast<T*>(pb);
+    } else {
+        rq = reinterpret_cast<T*>(pqk + C);
+        rk_ = rq + C * DK;
+        rz = rk_ + C * DK;
+        rv = rz + C * DK;
+        rdo = rv + C * DVS;
+        rb = rdo + C * DVS;
+    }
+    auto stage_raw = [&](int64_t t0, int cl) {
+        constexpr int VE = 16 / sizeof(T);
+        constexpr int RK = DK / VE, RV = DVS / VE;
+        for (int e = tid; e < cl * RK; e += kBwThreads) {
+            const int j = e / RK, c4 = e - j * RK;
+            const size_t g = ((size_t)(t0 + j) * H + h) * DK + (size_t)c4 * VE;
+            const int l = j * DK + c4 * VE;
+            *reinterpret_cast<uint4*>(rq + l) = __ldg(reinterpret_cast<const uint4*>(q + g));
+            *reinterpret_cast<uint4*>(rk_ + l) = __ldg(reinterpret_cast<const uint4*>(k + g));
+            *reinterpret_cast<uint4*>(rz + l) = __ldg(reinterpret_cast<const uint4*>(z + g));
+        }
+        for (int e = tid; e < cl * RV; e += kBwThreads) {
+            const int j = e / RV, c4 = e - j * RV;
+            const size_t g = ((size_t)(t0 + j) * H + h) * DV + col0 + (size_t)c4 * VE;
+            const int l = j * DVS + c4 * VE;
+            *reinterpret_cast<uint4*>(rv + l) = __ldg(reinterpret_cast<const uint4*>(v + g));
+            *reinterpret_cast<uint4*>(rdo + l) = __ldg(reinterpret_cast<const uint4*>(dO + g));
+        }
+        if (tid < cl) {
+            rb[tid] = beta[(size_t)(t0 + tid) * H + h];
+        }
+        __syncthreads();
+    };
     auto prepare = [&](int64_t t0, int cl) {
         constexpr int CPL = DK / 32;
+        stage_raw(t0, cl);
         for (int j = w; j < cl; j += kBwWarps) {
-            const int64_t t = t0 + j;
-            const size_t rk = ((size_t)t * H + h) * DK;
             float qv[CPL], kv[CPL], zv[CPL];
             float sq = 0.f, sk = 0.f, sqk = 0.f;
 #pragma unroll
             for (int m = 0; m < CPL; ++m) {
-                qv[m] = ldf(q, rk + lane + 32 * m);
-                kv[m] = ldf(k, rk + lane + 32 * m);
-                zv[m] = ldf(z, rk + lane + 32 * m);
+                const int c = j * DK + lane + 32 * m;
+                qv[m] = as_f32(rq[c]);
+                kv[m] = as_f32(rk_[c]);
+                zv[m] = as_f32(rz[c]);
                 sq += qv[m] * qv[m];
                 sk += kv[m] * kv[m];
                 sqk += qv[m] * kv[m];
             }
+            const float vv = as_f32(rv[j * DVS + lane]);   // lane < 32 = DVS
+            const float dov = as_f32(rdo[j * DVS + lane]);
+            const float bv = as_f32(rb[j]);
+            __syncwarp();   // (fp32: the row is read before it is overwritten)
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) {
                 sq += __shfl_xor_sync(0xffffffffu, sq, off);
@@ -167,11 +227,10 @@ kda_backward_kernel(const BackwardParams p) {
                 const float sg = bw_sigmoid(p.softplus_gate ? -eA * zv[m] : eA * zv[m]);
                 pa[j * DK + c] = p.softplus_gate ? sg : expf(kBwGmin * sg);
             }
-            const size_t rv = ((size_t)t * H + h) * DV + col0 + lane;   // lane < 32 = DVS
-            pv[j * DVS + lane] = ldf(v, rv);
-            pdo[j * DVS + lane] = ldf(dO, rv);
+            pv[j * DVS + lane] = vv;
+            pdo[j * DVS + lane] = dov;
             if (lane == 0) {
-                pb[j] = ldf(beta, (size_t)t * H + h);
+                pb[j] = bv;
                 pqk[j] = sqk * iq * ik * scale;
             }
         }
