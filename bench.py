@@ -247,6 +247,64 @@ def cpu_baseline(H: int, T: int, d: int, cpu_seconds: float = 12.0):
     return value, threads, sample
 
 
+def row_cpu_baselines(H: int, T: int, d: int, dec_B: int, dec_H: int):
+    """The oracle timed on each further row's workload (or a stated sample of
+    it), beside the GPU figure of that row.  Returns {row: cpu_baseline}."""
+    import numpy as np
+    import torch
+    import oracle
+    from kimi_delta_attention_12_gb300 import inputs
+    oracle.build()
+    x = inputs.make_prefill_inputs([T], H, d, d, torch.bfloat16, seed=0)
+    rows = {}
+
+    t0 = time.perf_counter()
+    _, _, threads = oracle.kda_reference(x.q, x.k, x.v, x.z, x.beta, x.A, None, x.cu_seqlens,
+                                         softplus_gate=True)
+    dt = time.perf_counter() - t0
+    rows["softplus_gate"] = {
+        "value": T / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+        "sample": f"whole softplus-gate prefill (B=1 T={T}, all {H} heads), fp64 C oracle, "
+                  f"{dt:.2f} s"}
+
+    w, cs0 = inputs.make_conv_params(1, H, d, d, CONV_WIDTH, torch.bfloat16, seed=11)
+    t0 = time.perf_counter()
+    oracle.short_conv_qkv(x.q, x.k, x.v, w, x.cu_seqlens, cs0, True)
+    dt = time.perf_counter() - t0
+    byts = conv_algorithmic(1, H, T, d, CONV_WIDTH)
+    rows["short_conv"] = {
+        "value": byts / dt / 1e9, "unit": "GB/s", "ms": dt * 1e3, "cores": 1, "kind": "oracle",
+        "sample": f"whole conv workload (T={T}, {H} heads, width {CONV_WIDTH}, SiLU, states in "
+                  f"and out; inputs converted to fp64 inside the timed call), fp64 C oracle"}
+
+    Tb = min(T, 1024)
+    xb = inputs.make_prefill_inputs([Tb], H, d, d, torch.bfloat16, seed=0)
+    dO, dSf = inputs.make_upstream_grads(Tb, 1, H, d, d, torch.bfloat16, seed=21)
+    t0 = time.perf_counter()
+    g = oracle.kda_reference_backward(xb.q, xb.k, xb.v, xb.z, xb.beta, xb.A, None,
+                                      xb.cu_seqlens, dO, dSf)
+    dt = time.perf_counter() - t0
+    rows["backward"] = {
+        "value": Tb / dt, "unit": "tokens/s", "cores": g["threads"], "kind": "oracle",
+        "sample": f"backward on the first {Tb} tokens of the workload (all {H} heads), "
+                  f"fp64 C oracle, {dt:.2f} s"}
+
+    Bs = 16
+    A, S0 = inputs.make_decode_state(Bs, dec_H, d, d, seed=5)
+    st = inputs.make_decode_step(Bs, dec_H, d, d, torch.bfloat16, seed=5, step=0)
+    cu = np.arange(Bs + 1, dtype=np.int64)
+    t0 = time.perf_counter()
+    _, _, threads = oracle.kda_reference(st.q, st.k, st.v, st.z, st.beta, A, S0, cu)
+    dt = time.perf_counter() - t0
+    rows["decode"] = {
+        "value": decode_algorithmic(Bs, dec_H, d) / dt / 1e9, "unit": "GB/s",
+        "ms_per_step": dt * 1e3 * dec_B / Bs, "cores": threads, "kind": "oracle",
+        "sample": f"one decode step of {Bs} of the {dec_B} sequences ({dec_H} heads; state "
+                  f"converted to fp64 inside the timed call), fp64 C oracle; ms_per_step "
+                  f"scaled to the full batch"}
+    return rows
+
+
 def reference_arm(args, world, rank, pg):
     if rank != 0:
         return
@@ -663,6 +721,10 @@ def finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops
         return
     # CPU baseline: the oracle on the same workload
     cpu_tps, cpu_threads, cpu_sample = cpu_baseline(H, T, d)
+    row_cpu = row_cpu_baselines(H, T, d, D["B"], D["H"])
+    for key in ("softplus_gate", "short_conv", "backward"):
+        if key in extras:
+            extras[key]["cpu_baseline"] = row_cpu[key]
     traffic = profiled_traffic(kernel_name)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -685,7 +747,7 @@ def finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops
                               "steps": D["steps"]},
                    "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm_gbs"],
                                 "unit": "GB/s", "frac": dec_gbs / peaks["hbm_gbs"]},
-                   "clocks": dclk_summary},
+                   "clocks": dclk_summary, "cpu_baseline": row_cpu["decode"]},
         **extras,
         "cpu_baseline": {"value": cpu_tps, "unit": "tokens/s", "cores": cpu_threads,
                          "kind": "oracle", "sample": cpu_sample, "cpu_model": cpu_model()},

@@ -320,7 +320,8 @@ def kda_reference_backward(q, k, v, z, beta, A, initial_state=None, cu_seqlens=N
 
     Layouts as kda_reference (packed); dO [total_T, H, d_v]; dS_final
     [N, H, d_k, d_v] or None.  Returns a dict with dq, dk, dz [total_T, H, d_k],
-    dv [total_T, H, d_v], dbeta [total_T, H], dA [H], dS0 [N, H, d_k, d_v]."""
+    dv [total_T, H, d_v], dbeta [total_T, H], dA [H], dS0 [N, H, d_k, d_v]
+    and the number of threads used ("threads")."""
     lib = _load()
     q, k, v, z, beta, A = (_f64(t) for t in (q, k, v, z, beta, A))
     total_T, H, dk = q.shape
@@ -345,4 +346,5 @@ def kda_reference_backward(q, k, v, z, beta, A, initial_state=None, cu_seqlens=N
     if rc <= 0:
         raise RuntimeError(f"oracle backward failed with status {rc}")
     out["dA"] = gA.sum(axis=0)
+    out["threads"] = int(rc)
     return out
