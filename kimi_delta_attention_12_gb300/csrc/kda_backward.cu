@@ -63,14 +63,83 @@ __device__ __forceinline__ float bw_sigmoid(float x) {
 
 constexpr int kBwCols = 32;   // value columns per CTA
 
+// The CTA's 32 value columns are spread as 8 lanes x float4 per state row, 4
+// row groups per warp (lane = 8 * row group + column group).
+
+// Sum of a float4 of column partials over the warp's 4 row groups (lane bits 3
+// and 4), transposed: each exchange halves what a lane carries.  Returns
+// component (lane >> 3) of the lane's column group, i.e. the sum for column
+// 4 * (lane & 7) + (lane >> 3).
+__device__ __forceinline__ float rowgroups_sum4(float4 v, int lane) {
+    const bool b4 = lane & 16, b3 = lane & 8;
+    float k0 = (b4 ? v.z : v.x) + __shfl_xor_sync(0xffffffffu, b4 ? v.x : v.z, 16);
+    float k1 = (b4 ? v.w : v.y) + __shfl_xor_sync(0xffffffffu, b4 ? v.y : v.w, 16);
+    return (b3 ? k1 : k0) + __shfl_xor_sync(0xffffffffu, b3 ? k0 : k1, 8);
+}
+
+// Sums the per-row partials dq, dk, da of a thread's RPT state rows over the
+// 8 lanes of its row group (lane bits 0..2), transposed as above, and stores
+// them to part[i], part[DK + i], part[2 DK + i] for each row i = row_of(r).
+template <int RPT, int DK, typename RowOf>
+__device__ __forceinline__ void rows_sum_store(const float (&dq)[RPT], const float (&dk)[RPT],
+                                               const float (&da)[RPT], int lane, RowOf row_of,
+                                               float* part) {
+    constexpr unsigned F = 0xffffffffu;
+    constexpr int E0 = RPT == 4 ? 1 : RPT == 2 ? 2 : 4;   // first lane bit of the endgame
+    static_assert(RPT == 1 || RPT == 2 || RPT == 4, "rows per thread");
+    float q1, k1, a1;
+    int rsel;
+    if constexpr (RPT == 4) {
+        const bool c2 = lane & 4, c1 = lane & 2;
+        float q2[2], k2[2], a2[2];
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            q2[m] = (c2 ? dq[m + 2] : dq[m]) + __shfl_xor_sync(F, c2 ? dq[m] : dq[m + 2], 4);
+            k2[m] = (c2 ? dk[m + 2] : dk[m]) + __shfl_xor_sync(F, c2 ? dk[m] : dk[m + 2], 4);
+            a2[m] = (c2 ? da[m + 2] : da[m]) + __shfl_xor_sync(F, c2 ? da[m] : da[m + 2], 4);
+        }
+        q1 = (c1 ? q2[1] : q2[0]) + __shfl_xor_sync(F, c1 ? q2[0] : q2[1], 2);
+        k1 = (c1 ? k2[1] : k2[0]) + __shfl_xor_sync(F, c1 ? k2[0] : k2[1], 2);
+        a1 = (c1 ? a2[1] : a2[0]) + __shfl_xor_sync(F, c1 ? a2[0] : a2[1], 2);
+        rsel = (c2 ? 2 : 0) + (c1 ? 1 : 0);
+    } else if constexpr (RPT == 2) {
+        const bool c2 = lane & 4;
+        q1 = (c2 ? dq[1] : dq[0]) + __shfl_xor_sync(F, c2 ? dq[0] : dq[1], 4);
+        k1 = (c2 ? dk[1] : dk[0]) + __shfl_xor_sync(F, c2 ? dk[0] : dk[1], 4);
+        a1 = (c2 ? da[1] : da[0]) + __shfl_xor_sync(F, c2 ? da[0] : da[1], 4);
+        rsel = c2 ? 1 : 0;
+    } else {
+        q1 = dq[0];
+        k1 = dk[0];
+        a1 = da[0];
+        rsel = 0;
+    }
+    // endgame: lanes with bit E0 clear finish dq (and da), the others dk
+    const bool cb = lane & E0;
+    float fin = (cb ? k1 : q1) + __shfl_xor_sync(F, cb ? q1 : k1, E0);
+    float dsum = a1 + __shfl_xor_sync(F, a1, E0);
+#pragma unroll
+    for (int off = E0 >> 1; off > 0; off >>= 1) {
+        fin += __shfl_xor_sync(F, fin, off);
+        dsum += __shfl_xor_sync(F, dsum, off);
+    }
+    if ((lane & (E0 - 1)) == 0) {
+        const int i = row_of(rsel);
+        part[(cb ? DK : 0) + i] = fin;
+        if (!cb) {
+            part[2 * DK + i] = dsum;
+        }
+    }
+}
+
 struct BwShared {
     float u[kBwCols];
     float du[kBwCols];
     float red[kBwWarps][2][kBwCols];
 };
 
-// Dynamic shared memory of the chunk's prepared token quantities (fp32),
-// then, for 16-bit inputs, the chunk's raw inputs (fp32 inputs are copied in
+// Dynamic shared memory of the chunk's prepared token quantities and of the
+// forward walk's v - S'^T k_hat per token (fp32), then, for 16-bit inputs, the chunk's raw inputs (fp32 inputs are copied in
 // place into the prepared arrays).
 template <int DK, typename T>
 constexpr size_t chunk_raw_bytes() {
@@ -78,7 +147,7 @@ constexpr size_t chunk_raw_bytes() {
 }
 template <int DK, typename T>
 constexpr size_t chunk_stage_bytes() {
-    return (size_t)kBwChunk * (3 * DK + 2 * kBwCols + 2) * sizeof(float) +
+    return (size_t)kBwChunk * (3 * DK + 3 * kBwCols + 2) * sizeof(float) +
            chunk_raw_bytes<DK, T>();
 }
 
@@ -144,7 +213,8 @@ kda_backward_kernel(const BackwardParams p) {
     float* pa = pk + C * DK;
     float* pv = pa + C * DK;                          // [C][DVS]
     float* pdo = pv + C * DVS;
-    float* pb = pdo + C * DVS;                        // [C]
+    float* pw = pdo + C * DVS;                        // [C][DVS]: v - S'^T k_hat
+    float* pb = pw + C * DVS;                         // [C]
     float* pqk = pb + C;                              // [C]
     // the raw copy: in place for fp32 inputs, after the prepared arrays else
     T* rq;
@@ -237,7 +307,9 @@ kda_backward_kernel(const BackwardParams p) {
         __syncthreads();
     };
 
-    // ---- one forward step on S (registers) for token jt of the chunk ----
+    // ---- one forward step on S (registers) for token jt of the chunk; it
+    // also keeps w = v - S'^T k_hat of the token (S' = Diag(alpha) S_{t-1})
+    // for the reverse walk ----
     float4 S[RPT];
     auto forward_step = [&](int jt) {
         float4 ak = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -248,16 +320,7 @@ kda_backward_kernel(const BackwardParams p) {
             S[r].x *= a; S[r].y *= a; S[r].z *= a; S[r].w *= a;
             ak.x += kk * S[r].x; ak.y += kk * S[r].y; ak.z += kk * S[r].z; ak.w += kk * S[r].w;
         }
-#pragma unroll
-        for (int off = LPR; off < 32; off <<= 1) {
-            ak.x += __shfl_xor_sync(0xffffffffu, ak.x, off);
-            ak.y += __shfl_xor_sync(0xffffffffu, ak.y, off);
-            ak.z += __shfl_xor_sync(0xffffffffu, ak.z, off);
-            ak.w += __shfl_xor_sync(0xffffffffu, ak.w, off);
-        }
-        if (rs == 0) {
-            *reinterpret_cast<float4*>(&sh.red[w][0][4 * cg]) = ak;
-        }
+        sh.red[w][0][4 * cg + rs] = rowgroups_sum4(ak, lane);
         __syncthreads();
         if (tid < DVS) {
             float r = 0.f;
@@ -265,7 +328,9 @@ kda_backward_kernel(const BackwardParams p) {
             for (int ww = 0; ww < kBwWarps; ++ww) {
                 r += sh.red[ww][0][tid];
             }
-            sh.u[tid] = pb[jt] * (pv[jt * DVS + tid] - r);
+            const float wv = pv[jt * DVS + tid] - r;
+            pw[jt * DVS + tid] = wv;
+            sh.u[tid] = pb[jt] * wv;
         }
         __syncthreads();
         const float4 u4 = *reinterpret_cast<const float4*>(&sh.u[4 * cg]);
@@ -344,10 +409,7 @@ kda_backward_kernel(const BackwardParams p) {
         }
         for (int j = 0; j < (int)cl; ++j) {
             store_state(scratch + (size_t)j * SS, S);
-            if (j + 1 == (int)cl) {
-                break;   // the state after the chunk's last token is not needed
-            }
-            forward_step(j);
+            forward_step(j);   // (after the last token only its w is used)
         }
         // 2b: the chunk's tokens in reverse (each thread reads back the
         // scratch elements it wrote: no barrier needed for them).  The next
@@ -373,45 +435,35 @@ kda_backward_kernel(const BackwardParams p) {
                     Snext[r] = sp[st_idx(r)];
                 }
             }
-            // column sums: r = S'^T kh and gk = G^T kh (G = dL/dS_t from the future)
-            float4 ar = make_float4(0.f, 0.f, 0.f, 0.f), ag = ar;
+            // u = beta w (from the forward walk); dq_hat = S_t dO needs no G:
+            // S_t = S' + k_hat u^T, S' = Diag(alpha) S_{t-1}
+            const float b = pb[j];
+            const float4 w4 = *reinterpret_cast<const float4*>(&pw[j * DVS + 4 * cg]);
+            const float4 u4 = make_float4(b * w4.x, b * w4.y, b * w4.z, b * w4.w);
+            const float4 do4 = *reinterpret_cast<const float4*>(&pdo[j * DVS + 4 * cg]);
+            float dqv[RPT], dkv[RPT], dav[RPT];
+            // column sums gk = G^T k_hat (G = dL/dS_t from the future)
+            float4 ag = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int r = 0; r < RPT; ++r) {
                 const int i = row_of(r);
                 const float a = pa[j * DK + i], kk = pk[j * DK + i];
-                ar.x += kk * a * S[r].x; ar.y += kk * a * S[r].y;
-                ar.z += kk * a * S[r].z; ar.w += kk * a * S[r].w;
                 ag.x += kk * G[r].x; ag.y += kk * G[r].y; ag.z += kk * G[r].z; ag.w += kk * G[r].w;
+                dqv[r] = (a * S[r].x + kk * u4.x) * do4.x + (a * S[r].y + kk * u4.y) * do4.y +
+                         (a * S[r].z + kk * u4.z) * do4.z + (a * S[r].w + kk * u4.w) * do4.w;
             }
-#pragma unroll
-            for (int off = LPR; off < 32; off <<= 1) {
-                ar.x += __shfl_xor_sync(0xffffffffu, ar.x, off);
-                ar.y += __shfl_xor_sync(0xffffffffu, ar.y, off);
-                ar.z += __shfl_xor_sync(0xffffffffu, ar.z, off);
-                ar.w += __shfl_xor_sync(0xffffffffu, ar.w, off);
-                ag.x += __shfl_xor_sync(0xffffffffu, ag.x, off);
-                ag.y += __shfl_xor_sync(0xffffffffu, ag.y, off);
-                ag.z += __shfl_xor_sync(0xffffffffu, ag.z, off);
-                ag.w += __shfl_xor_sync(0xffffffffu, ag.w, off);
-            }
-            if (rs == 0) {
-                *reinterpret_cast<float4*>(&sh.red[w][0][4 * cg]) = ar;
-                *reinterpret_cast<float4*>(&sh.red[w][1][4 * cg]) = ag;
-            }
+            sh.red[w][1][4 * cg + rs] = rowgroups_sum4(ag, lane);
             __syncthreads();
-            // per value column (warp 0, one lane per column): u, du, dv and db
+            // per value column (warp 0, one lane per column): du, dv and db
             float* part = p.part + (((size_t)split * p.total_T + t) * H + h) * PW;
             if (tid < DVS) {
-                float rr = 0.f, gk = 0.f;
+                float gk = 0.f;
 #pragma unroll
                 for (int ww = 0; ww < kBwWarps; ++ww) {
-                    rr += sh.red[ww][0][tid];
                     gk += sh.red[ww][1][tid];
                 }
-                const float b = pb[j];
-                const float wv = pv[j * DVS + tid] - rr;            // v - S'^T kh
+                const float wv = pw[j * DVS + tid];                 // v - S'^T kh
                 const float duj = gk + pqk[j] * pdo[j * DVS + tid];
-                sh.u[tid] = b * wv;
                 sh.du[tid] = duj;
                 p.dv[((size_t)t * H + h) * DV + col0 + tid] = b * duj;
                 float db = duj * wv;
@@ -424,39 +476,23 @@ kda_backward_kernel(const BackwardParams p) {
                 }
             }
             __syncthreads();
-            // per state row: dqh, dkh, da and the new G
-            const float4 u4 = *reinterpret_cast<const float4*>(&sh.u[4 * cg]);
+            // per state row: dkh, da and the new G
             const float4 du4 = *reinterpret_cast<const float4*>(&sh.du[4 * cg]);
-            const float4 do4 = *reinterpret_cast<const float4*>(&pdo[j * DVS + 4 * cg]);
-            const float b = pb[j];
 #pragma unroll
             for (int r = 0; r < RPT; ++r) {
                 const int i = row_of(r);
                 const float a = pa[j * DK + i], kk = pk[j * DK + i], qq = pq[j * DK + i];
                 const float4 sp = make_float4(a * S[r].x, a * S[r].y, a * S[r].z, a * S[r].w);
-                const float4 st = make_float4(sp.x + kk * u4.x, sp.y + kk * u4.y,
-                                              sp.z + kk * u4.z, sp.w + kk * u4.w);
-                float dq_i = st.x * do4.x + st.y * do4.y + st.z * do4.z + st.w * do4.w;
                 float4 g = make_float4(G[r].x + qq * do4.x, G[r].y + qq * do4.y,
                                        G[r].z + qq * do4.z, G[r].w + qq * do4.w);
-                float dk_i = g.x * u4.x + g.y * u4.y + g.z * u4.z + g.w * u4.w -
-                             b * (sp.x * du4.x + sp.y * du4.y + sp.z * du4.z + sp.w * du4.w);
+                dkv[r] = g.x * u4.x + g.y * u4.y + g.z * u4.z + g.w * u4.w -
+                         b * (sp.x * du4.x + sp.y * du4.y + sp.z * du4.z + sp.w * du4.w);
                 g.x -= b * kk * du4.x; g.y -= b * kk * du4.y;
                 g.z -= b * kk * du4.z; g.w -= b * kk * du4.w;
-                float da_i = g.x * S[r].x + g.y * S[r].y + g.z * S[r].z + g.w * S[r].w;
+                dav[r] = g.x * S[r].x + g.y * S[r].y + g.z * S[r].z + g.w * S[r].w;
                 G[r] = make_float4(a * g.x, a * g.y, a * g.z, a * g.w);
-#pragma unroll
-                for (int off = 1; off < LPR; off <<= 1) {
-                    dq_i += __shfl_xor_sync(0xffffffffu, dq_i, off);
-                    dk_i += __shfl_xor_sync(0xffffffffu, dk_i, off);
-                    da_i += __shfl_xor_sync(0xffffffffu, da_i, off);
-                }
-                if (cg == 0) {
-                    part[i] = dq_i;
-                    part[DK + i] = dk_i;
-                    part[2 * DK + i] = da_i;
-                }
             }
+            rows_sum_store<RPT, DK>(dqv, dkv, dav, lane, row_of, part);
         }
     }
     // dL/dS_0 (this CTA's columns)
