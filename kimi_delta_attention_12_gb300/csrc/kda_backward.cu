@@ -35,6 +35,7 @@
 #include <stdint.h>
 
 #include "kda_internal.h"
+#include "kda_lanes.cuh"
 
 namespace kda {
 namespace {
@@ -61,21 +62,7 @@ __device__ __forceinline__ float bw_sigmoid(float x) {
     return e / (1.0f + e);
 }
 
-constexpr int kBwCols = 32;   // value columns per CTA
-
-// The CTA's 32 value columns are spread as 8 lanes x float4 per state row, 4
-// row groups per warp (lane = 8 * row group + column group).
-
-// Sum of a float4 of column partials over the warp's 4 row groups (lane bits 3
-// and 4), transposed: each exchange halves what a lane carries.  Returns
-// component (lane >> 3) of the lane's column group, i.e. the sum for column
-// 4 * (lane & 7) + (lane >> 3).
-__device__ __forceinline__ float rowgroups_sum4(float4 v, int lane) {
-    const bool b4 = lane & 16, b3 = lane & 8;
-    float k0 = (b4 ? v.z : v.x) + __shfl_xor_sync(0xffffffffu, b4 ? v.x : v.z, 16);
-    float k1 = (b4 ? v.w : v.y) + __shfl_xor_sync(0xffffffffu, b4 ? v.y : v.w, 16);
-    return (b3 ? k1 : k0) + __shfl_xor_sync(0xffffffffu, b3 ? k0 : k1, 8);
-}
+constexpr int kBwCols = 32;   // value columns per CTA (8 lanes x float4 per state row)
 
 // Sums the per-row partials dq, dk, da of a thread's RPT state rows over the
 // 8 lanes of its row group (lane bits 0..2), transposed as above, and stores

@@ -33,6 +33,7 @@
 #include <stdint.h>
 
 #include "kda_internal.h"
+#include "kda_lanes.cuh"
 
 namespace kda {
 namespace {
@@ -287,7 +288,7 @@ kda_recurrent_kernel(const RecurrentParams p) {
     };
 
     if constexpr (!kDecode) {
-        static_assert(DVS <= 32, "prefill CTAs hold at most 32 value columns");
+        static_assert(DVS == 32, "prefill CTAs hold 32 value columns");
         for (int64_t t0 = bos; t0 < eos; t0 += kStage) {
             const int n = (int)min((int64_t)kStage, eos - t0);
             __syncthreads();   // the previous stretch's last token has been read
@@ -311,21 +312,9 @@ kda_recurrent_kernel(const RecurrentParams p) {
                     aq.x += qq * S[r].x; aq.y += qq * S[r].y;
                     aq.z += qq * S[r].z; aq.w += qq * S[r].w;
                 }
-#pragma unroll
-                for (int off = LPR; off < 32; off <<= 1) {
-                    ak.x += __shfl_xor_sync(0xffffffffu, ak.x, off);
-                    ak.y += __shfl_xor_sync(0xffffffffu, ak.y, off);
-                    ak.z += __shfl_xor_sync(0xffffffffu, ak.z, off);
-                    ak.w += __shfl_xor_sync(0xffffffffu, ak.w, off);
-                    aq.x += __shfl_xor_sync(0xffffffffu, aq.x, off);
-                    aq.y += __shfl_xor_sync(0xffffffffu, aq.y, off);
-                    aq.z += __shfl_xor_sync(0xffffffffu, aq.z, off);
-                    aq.w += __shfl_xor_sync(0xffffffffu, aq.w, off);
-                }
-                if (rs == 0) {
-                    *reinterpret_cast<float4*>(&s_red[w][0][4 * cg]) = ak;
-                    *reinterpret_cast<float4*>(&s_red[w][1][4 * cg]) = aq;
-                }
+                // (32 columns: 8 lanes per row, 4 row groups per warp)
+                s_red[w][0][4 * cg + rs] = rowgroups_sum4(ak, lane);
+                s_red[w][1][4 * cg + rs] = rowgroups_sum4(aq, lane);
                 __syncthreads();
                 // ---- u and o per value column ----
                 if (tid < DVS) {
