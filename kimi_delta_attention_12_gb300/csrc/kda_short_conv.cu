@@ -32,7 +32,21 @@ namespace {
 
 constexpr int kConvThreads = 256;
 constexpr int kConvTB = 32;     // tokens per block
-constexpr int kConvAhead = 8;   // rows loaded ahead
+constexpr int kConvAhead = 8;   // rows per copy group
+constexpr int kConvStages = 3;  // copy groups in the per-thread ring (two ahead)
+
+// 8-byte asynchronous copy global -> shared (the thread's own ring slot).
+__device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
+    const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
 
 // An 8-byte vector of channels: 4 bf16 or 2 fp32.
 template <typename T>
@@ -226,16 +240,40 @@ short_conv_kernel(const ShortConvParams p, int n_token_blocks) {
     void* y = cv.tensor == 0 ? p.y[0] : cv.tensor == 1 ? p.y[1] : p.y[2];
     // row pointers of this vector, advanced one token (H * d elements) at a time
     const size_t row_bytes = (size_t)H * cv.d * EB;
-    const char* xr = static_cast<const char*>(x) + xoff(t0) * EB;
+    const char* xi = static_cast<const char*>(x) + xoff(t0) * EB;   // next row to copy
     char* yr = static_cast<char*>(y) + xoff(t0) * EB;
+    // The block's rows reach each thread through its own ring of copy groups in
+    // shared memory (cp.async, kConvStages - 1 groups ahead of the one being
+    // worked on): more bytes in flight than registers could hold.  A thread
+    // reads only the slots it copied itself, so no barrier is needed.
+    __shared__ __align__(16) uint2 ring[kConvStages][kConvAhead][kConvThreads];
+    int64_t ti = t0;   // first token of the next group to copy
+    auto copy_group = [&](int slot) {
+#pragma unroll
+        for (int i = 0; i < kConvAhead; ++i) {
+            if (ti + i < t1) {
+                cp_async8(&ring[slot][i][threadIdx.x], xi + i * row_bytes);
+            }
+        }
+        cp_async_commit();
+        ti += kConvAhead;
+        xi += kConvAhead * row_bytes;
+    };
+#pragma unroll
+    for (int g = 0; g + 1 < kConvStages; ++g) {
+        copy_group(g);
+    }
+    int slot = 0;
     for (int64_t tb = t0; tb < t1; tb += kConvAhead) {
+        // the group kConvStages - 1 ahead, into the slot worked on last time
+        copy_group(slot == 0 ? kConvStages - 1 : slot - 1);
+        cp_async_wait<kConvStages - 1>();   // this group's rows have landed
         uint2 raw[kConvAhead];
 #pragma unroll
         for (int i = 0; i < kConvAhead; ++i) {
-            if (tb + i < t1) {
-                raw[i] = __ldg(reinterpret_cast<const uint2*>(xr + i * row_bytes));
-            }
+            raw[i] = ring[slot][i][threadIdx.x];
         }
+        slot = slot + 1 == kConvStages ? 0 : slot + 1;
 #pragma unroll
         for (int i = 0; i < kConvAhead; ++i) {
             const int64_t t = tb + i;
@@ -284,9 +322,9 @@ short_conv_kernel(const ShortConvParams p, int n_token_blocks) {
                 }
             }
         }
-        xr += kConvAhead * row_bytes;
         yr += kConvAhead * row_bytes;
     }
+    cp_async_wait<0>();   // (copies past the block's end were never issued)
 }
 
 template <typename T, bool kSilu>
