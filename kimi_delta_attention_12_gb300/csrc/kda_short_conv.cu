@@ -79,14 +79,16 @@ struct VecTraits<__nv_bfloat16> {
     }
 };
 
-// y * sigmoid(y) without a branch: with t = e^-|y| (never overflows),
-// sigmoid(y) = 1 / (1 + t) for y >= 0 and t / (1 + t) otherwise.  The fast
-// exponential and reciprocal keep the relative error near 1e-7, far below
-// the bf16 rounding of the stored result.
+// y * sigmoid(y) = y / (1 + 2^(-y log2 e)), without a branch: below about
+// y = -88 the power overflows to +inf and the approximate reciprocal returns
+// +0, the function's limit (the exact value is below 1e-36 there).  The
+// approximate ex2 and rcp keep the relative error near 1e-7, far below the
+// bf16 rounding of the stored result.
 __device__ __forceinline__ float silu_f(float y) {
-    const float t = __expf(-fabsf(y));
-    const float r = __fdividef(1.0f, 1.0f + t);
-    return y * (y >= 0.0f ? r : t * r);
+    float e, r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-1.4426950408889634f * y));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
+    return y * r;
 }
 
 __device__ __forceinline__ uint2 ld8(const void* base, size_t elem_off, int eb) {
@@ -169,6 +171,43 @@ __device__ __forceinline__ int seq_of(const ShortConvParams& p, int64_t t) {
         }
     }
     return lo;
+}
+
+// One token of one channel vector: y = sum_j wt[j] x_{t-R+j} (x_t the raw row
+// rw, the earlier inputs in the window), then the SiLU if asked, stored at yp;
+// the window of the last R = W - 1 inputs then slides by one.
+template <typename T, int W, bool kSilu>
+__device__ __forceinline__ void conv_token(const float (&wt)[W][VecTraits<T>::kN],
+                                           float (&win)[W > 1 ? W - 1 : 1][VecTraits<T>::kN],
+                                           const uint2& rw, char* yp) {
+    using VT = VecTraits<T>;
+    constexpr int VEC = VT::kN;
+    constexpr int R = W - 1;
+    float cur[VEC], out[VEC];
+    VT::unpack(rw, cur);
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) {
+        float acc = wt[R][c] * cur[c];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            acc = fmaf(wt[r][c], win[r][c], acc);
+        }
+        out[c] = kSilu ? silu_f(acc) : acc;
+    }
+    *reinterpret_cast<uint2*>(yp) = VT::pack(out);
+#pragma unroll
+    for (int r = 0; r + 1 < R; ++r) {
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) {
+            win[r][c] = win[r + 1][c];
+        }
+    }
+    if (R > 0) {
+#pragma unroll
+        for (int c = 0; c < VEC; ++c) {
+            win[R > 0 ? R - 1 : 0][c] = cur[c];
+        }
+    }
 }
 
 template <typename T, int W, bool kSilu>
@@ -268,58 +307,38 @@ short_conv_kernel(const ShortConvParams p, int n_token_blocks) {
         // the group kConvStages - 1 ahead, into the slot worked on last time
         copy_group(slot == 0 ? kConvStages - 1 : slot - 1);
         cp_async_wait<kConvStages - 1>();   // this group's rows have landed
-        uint2 raw[kConvAhead];
-#pragma unroll
-        for (int i = 0; i < kConvAhead; ++i) {
-            raw[i] = ring[slot][i][threadIdx.x];
-        }
+        const uint2 (&raw)[kConvAhead][kConvThreads] = ring[slot];
         slot = slot + 1 == kConvStages ? 0 : slot + 1;
+        if (tb + kConvAhead <= t1 && tb + kConvAhead <= eos) {
+            // the whole group lies in the block and in the current sequence
 #pragma unroll
-        for (int i = 0; i < kConvAhead; ++i) {
-            const int64_t t = tb + i;
-            if (t >= t1) {
-                continue;
+            for (int i = 0; i < kConvAhead; ++i) {
+                conv_token<T, W, kSilu>(wt, win, raw[i][threadIdx.x], yr + i * row_bytes);
             }
-            if (t >= eos) {
-                // first token of a later sequence (skipping empty ones): the
-                // window restarts from that sequence's conv state
-                do {
-                    ++n;
-                    seq_bounds(p, n, &bos, &eos);
-                } while (t >= eos);
+        } else {
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    uint2 s = make_uint2(0u, 0u);
-                    if (p.state_in) {
-                        s = ld8(p.state_in, soff(n, r), EB);
+            for (int i = 0; i < kConvAhead; ++i) {
+                const int64_t t = tb + i;
+                if (t >= t1) {
+                    continue;
+                }
+                if (t >= eos) {
+                    // first token of a later sequence (skipping empty ones):
+                    // the window restarts from that sequence's conv state
+                    do {
+                        ++n;
+                        seq_bounds(p, n, &bos, &eos);
+                    } while (t >= eos);
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        uint2 s = make_uint2(0u, 0u);
+                        if (p.state_in) {
+                            s = ld8(p.state_in, soff(n, r), EB);
+                        }
+                        VT::unpack(s, win[r]);
                     }
-                    VT::unpack(s, win[r]);
                 }
-            }
-            float cur[VEC], out[VEC];
-            VT::unpack(raw[i], cur);
-#pragma unroll
-            for (int c = 0; c < VEC; ++c) {
-                float acc = wt[R][c] * cur[c];
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    acc = fmaf(wt[r][c], win[r][c], acc);
-                }
-                out[c] = kSilu ? silu_f(acc) : acc;
-            }
-            *reinterpret_cast<uint2*>(yr + i * row_bytes) = VT::pack(out);
-#pragma unroll
-            for (int r = 0; r + 1 < R; ++r) {
-#pragma unroll
-                for (int c = 0; c < VEC; ++c) {
-                    win[r][c] = win[r + 1][c];
-                }
-            }
-            if (R > 0) {
-#pragma unroll
-                for (int c = 0; c < VEC; ++c) {
-                    win[R > 0 ? R - 1 : 0][c] = cur[c];
-                }
+                conv_token<T, W, kSilu>(wt, win, raw[i][threadIdx.x], yr + i * row_bytes);
             }
         }
         yr += kConvAhead * row_bytes;
