@@ -21,12 +21,15 @@
 // inputs).
 //
 // Thread layout: the value columns of a head are split over NSPLIT CTAs (the
-// columns of S are independent); a CTA's slice of DVS = d_v/NSPLIT columns
-// is covered by LPR = DVS/4 lanes holding one float4 each; a warp covers
-// RPW = 32/LPR rows per pass; the CTA covers RSTEP = 8*RPW rows per pass and
-// each thread keeps RPT = d_k/RSTEP float4 of the state.  Column sums over
-// the d_k rows (S'^T k, S'^T q) are reduced with warp shuffles inside a warp
-// and through shared memory across the 8 warps.
+// columns of S are independent).  Decode: a CTA's slice of DVS = d_v/NSPLIT
+// columns is covered by LPR = DVS/4 lanes holding one float4 each; a warp
+// covers RPW = 32/LPR rows per pass; the CTA covers RSTEP = 8*RPW rows per
+// pass and each thread keeps RPT = d_k/RSTEP float4 of the state.  Column
+// sums over the d_k rows (S'^T k, S'^T q) are reduced with warp shuffles
+// inside a warp and through shared memory across the 8 warps.  Prefill
+// (32-column CTAs): warp w owns the 4 whole columns 4w .. 4w+3 and lane l the
+// rows l + 32 r, so the column sums, u and o of a token stay inside the warp
+// and the token loop has no CTA barrier.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -56,7 +59,7 @@ __device__ __forceinline__ float as_float(__nv_bfloat16 x) { return __bfloat162f
 // (fp32): the normalised and scaled q_hat, k_hat, the decay alpha, the CTA's
 // v columns, beta and q_hat . k_hat.  These depend on the inputs only, so the
 // whole CTA computes them in parallel (one warp per token); the token-serial
-// loop is then left with the state update and two CTA barriers per token.
+// loop is then left with the state update, warp by warp.
 // The stretch's raw inputs are first copied into shared memory with 16-byte
 // loads, all in flight at once; for fp32 inputs they land in the prepared
 // arrays themselves (each warp reads its token's row before overwriting it),
@@ -157,15 +160,27 @@ kda_recurrent_kernel(const RecurrentParams p) {
         return;
     }
 
-    // ---- state load: 128-bit, each warp pass reads whole rows ----
+    // float4 index, in a d_k x d_v state, of the thread's part of its r-th
+    // state row.  Decode: rows r * RSTEP + w * RPW + rs, the CTA's columns
+    // spread over the lanes (each warp pass reads whole rows).  Prefill: rows
+    // lane + 32 r, warp w owning the 4 columns 4w .. 4w+3 of the CTA's 32, so
+    // that a token's column sums never leave the warp.
+    auto st4 = [=](int r) -> size_t {
+        if constexpr (kDecode) {
+            return ((size_t)(r * RSTEP + w * RPW + rs) * DV + col0) / 4 + cg;
+        } else {
+            return ((size_t)(lane + 32 * r) * DV + col0 + 4 * w) / 4;
+        }
+    };
+
+    // ---- state load (128-bit) ----
     float4 S[RPT];
     const size_t soff = ((size_t)sidx * H + h) * DK * DV;
     if (p.state_in) {
         const float4* sp = reinterpret_cast<const float4*>(p.state_in + soff);
 #pragma unroll
         for (int r = 0; r < RPT; ++r) {
-            const int i = r * RSTEP + w * RPW + rs;
-            S[r] = __ldcs(sp + (i * DV + col0) / 4 + cg);
+            S[r] = __ldcs(sp + st4(r));
         }
     } else {
 #pragma unroll
@@ -295,13 +310,15 @@ kda_recurrent_kernel(const RecurrentParams p) {
             prepare(t0, n);
             for (int jt = 0; jt < n; ++jt) {
                 const int64_t t = t0 + jt;
-                // ---- decay, and the two column sums of S' ----
+                // ---- decay, and the two column sums of S' over the d_k rows
+                // (warp w holds whole columns 4w .. 4w+3: no other warp and no
+                // barrier takes part) ----
                 float4 ak = make_float4(0.f, 0.f, 0.f, 0.f);
                 float4 aq = make_float4(0.f, 0.f, 0.f, 0.f);
                 float kreg[RPT];
 #pragma unroll
                 for (int r = 0; r < RPT; ++r) {
-                    const int i = r * RSTEP + w * RPW + rs;
+                    const int i = lane + 32 * r;
                     const float a = sa_h[jt * DK + i];
                     const float kk = sk_h[jt * DK + i];
                     const float qq = sq_h[jt * DK + i];
@@ -312,25 +329,37 @@ kda_recurrent_kernel(const RecurrentParams p) {
                     aq.x += qq * S[r].x; aq.y += qq * S[r].y;
                     aq.z += qq * S[r].z; aq.w += qq * S[r].w;
                 }
-                // (32 columns: 8 lanes per row, 4 row groups per warp)
-                s_red[w][0][4 * cg + rs] = rowgroups_sum4(ak, lane);
-                s_red[w][1][4 * cg + rs] = rowgroups_sum4(aq, lane);
-                __syncthreads();
-                // ---- u and o per value column ----
-                if (tid < DVS) {
-                    float rkj = 0.f, rqj = 0.f;
-#pragma unroll
-                    for (int ww = 0; ww < kWarps; ++ww) {
-                        rkj += s_red[ww][0][tid];
-                        rqj += s_red[ww][1][tid];
-                    }
-                    const float u = sb_h[jt] * (sv_h[jt * DVS + tid] - rkj);
-                    s_u[tid] = u;
-                    store_elem(o, ((size_t)t * H + h) * DV + col0 + tid, rqj + sd_h[jt] * u);
+                // Transposed sums over the 32 lanes: lane bit 4 picks ak or aq,
+                // bits 3 and 2 the column c = 2 b3 + b2 that the lane finishes;
+                // bits 1 and 0 are then summed by two butterflies (9 shuffles
+                // for the 8 sums).
+                constexpr unsigned F = 0xffffffffu;
+                const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+                const float x0 = (b4 ? aq.x : ak.x) + __shfl_xor_sync(F, b4 ? ak.x : aq.x, 16);
+                const float x1 = (b4 ? aq.y : ak.y) + __shfl_xor_sync(F, b4 ? ak.y : aq.y, 16);
+                const float x2 = (b4 ? aq.z : ak.z) + __shfl_xor_sync(F, b4 ? ak.z : aq.z, 16);
+                const float x3 = (b4 ? aq.w : ak.w) + __shfl_xor_sync(F, b4 ? ak.w : aq.w, 16);
+                const float y0 = (b3 ? x2 : x0) + __shfl_xor_sync(F, b3 ? x0 : x2, 8);
+                const float y1 = (b3 ? x3 : x1) + __shfl_xor_sync(F, b3 ? x1 : x3, 8);
+                float zc = (b2 ? y1 : y0) + __shfl_xor_sync(F, b2 ? y0 : y1, 4);
+                zc += __shfl_xor_sync(F, zc, 2);
+                zc += __shfl_xor_sync(F, zc, 1);
+                const int c = (b3 ? 2 : 0) + (b2 ? 1 : 0);
+                // u_c = beta (v_c - (S'^T k)_c) on the lanes that hold
+                // (S'^T k)_c; o_c = (S'^T q)_c + (q . k) u_c on those that
+                // hold (S'^T q)_c, which take u_c from lane ^ 16
+                const float uc = sb_h[jt] * (sv_h[jt * DVS + 4 * w + c] - zc);
+                const float u_other = __shfl_xor_sync(F, uc, 16);
+                if (b4 && (lane & 3) == 0) {
+                    store_elem(o, ((size_t)t * H + h) * DV + col0 + 4 * w + c,
+                               zc + sd_h[jt] * u_other);
                 }
-                __syncthreads();
-                // ---- rank-1 write ----
-                const float4 u4 = *reinterpret_cast<const float4*>(&s_u[4 * cg]);
+                // ---- rank-1 write (u of the warp's 4 columns from lanes 0, 4, 8, 12) ----
+                float4 u4;
+                u4.x = __shfl_sync(F, uc, 0);
+                u4.y = __shfl_sync(F, uc, 4);
+                u4.z = __shfl_sync(F, uc, 8);
+                u4.w = __shfl_sync(F, uc, 12);
 #pragma unroll
                 for (int r = 0; r < RPT; ++r) {
                     const float kk = kreg[r];
@@ -348,8 +377,7 @@ kda_recurrent_kernel(const RecurrentParams p) {
                                 p.ckpt_pool + ((size_t)prow * H + h) * DK * DV);
 #pragma unroll
                             for (int r = 0; r < RPT; ++r) {
-                                const int i = r * RSTEP + w * RPW + rs;
-                                __stcs(cp + (i * DV + col0) / 4 + cg, S[r]);
+                                __stcs(cp + st4(r), S[r]);
                             }
                         }
                     }
@@ -467,8 +495,7 @@ kda_recurrent_kernel(const RecurrentParams p) {
         float4* sp = reinterpret_cast<float4*>(p.state_out + soff);
 #pragma unroll
         for (int r = 0; r < RPT; ++r) {
-            const int i = r * RSTEP + w * RPW + rs;
-            __stcs(sp + (i * DV + col0) / 4 + cg, S[r]);
+            __stcs(sp + st4(r), S[r]);
         }
     }
 }
