@@ -64,102 +64,53 @@ __device__ __forceinline__ float bw_sigmoid(float x) {
 
 constexpr int kBwCols = 32;   // value columns per CTA (8 lanes x float4 per state row)
 
-// Sums the per-row partials dq, dk, da of a thread's RPT state rows over the
-// 8 lanes of its row group (lane bits 0..2), transposed as above, and stores
-// them to part[i], part[DK + i], part[2 DK + i] for each row i = row_of(r).
-template <int RPT, int DK, typename RowOf>
-__device__ __forceinline__ void rows_sum_store(const float (&dq)[RPT], const float (&dk)[RPT],
-                                               const float (&da)[RPT], int lane, RowOf row_of,
-                                               float* part) {
-    constexpr unsigned F = 0xffffffffu;
-    constexpr int E0 = RPT == 4 ? 1 : RPT == 2 ? 2 : 4;   // first lane bit of the endgame
-    static_assert(RPT == 1 || RPT == 2 || RPT == 4, "rows per thread");
-    float q1, k1, a1;
-    int rsel;
-    if constexpr (RPT == 4) {
-        const bool c2 = lane & 4, c1 = lane & 2;
-        float q2[2], k2[2], a2[2];
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {
-            q2[m] = (c2 ? dq[m + 2] : dq[m]) + __shfl_xor_sync(F, c2 ? dq[m] : dq[m + 2], 4);
-            k2[m] = (c2 ? dk[m + 2] : dk[m]) + __shfl_xor_sync(F, c2 ? dk[m] : dk[m + 2], 4);
-            a2[m] = (c2 ? da[m + 2] : da[m]) + __shfl_xor_sync(F, c2 ? da[m] : da[m + 2], 4);
-        }
-        q1 = (c1 ? q2[1] : q2[0]) + __shfl_xor_sync(F, c1 ? q2[0] : q2[1], 2);
-        k1 = (c1 ? k2[1] : k2[0]) + __shfl_xor_sync(F, c1 ? k2[0] : k2[1], 2);
-        a1 = (c1 ? a2[1] : a2[0]) + __shfl_xor_sync(F, c1 ? a2[0] : a2[1], 2);
-        rsel = (c2 ? 2 : 0) + (c1 ? 1 : 0);
-    } else if constexpr (RPT == 2) {
-        const bool c2 = lane & 4;
-        q1 = (c2 ? dq[1] : dq[0]) + __shfl_xor_sync(F, c2 ? dq[0] : dq[1], 4);
-        k1 = (c2 ? dk[1] : dk[0]) + __shfl_xor_sync(F, c2 ? dk[0] : dk[1], 4);
-        a1 = (c2 ? da[1] : da[0]) + __shfl_xor_sync(F, c2 ? da[0] : da[1], 4);
-        rsel = c2 ? 1 : 0;
-    } else {
-        q1 = dq[0];
-        k1 = dk[0];
-        a1 = da[0];
-        rsel = 0;
-    }
-    // endgame: lanes with bit E0 clear finish dq (and da), the others dk
-    const bool cb = lane & E0;
-    float fin = (cb ? k1 : q1) + __shfl_xor_sync(F, cb ? q1 : k1, E0);
-    float dsum = a1 + __shfl_xor_sync(F, a1, E0);
-#pragma unroll
-    for (int off = E0 >> 1; off > 0; off >>= 1) {
-        fin += __shfl_xor_sync(F, fin, off);
-        dsum += __shfl_xor_sync(F, dsum, off);
-    }
-    if ((lane & (E0 - 1)) == 0) {
-        const int i = row_of(rsel);
-        part[(cb ? DK : 0) + i] = fin;
-        if (!cb) {
-            part[2 * DK + i] = dsum;
-        }
-    }
-}
+// Tokens whose per-warp output partials are staged in shared memory before
+// the CTA sums them over its warps.
+constexpr int kBwRed = 4;
 
-struct BwShared {
-    float u[kBwCols];
-    float du[kBwCols];
-    float red[kBwWarps][2][kBwCols];
-};
-
-// Dynamic shared memory of the chunk's prepared token quantities and of the
-// forward walk's v - S'^T k_hat per token (fp32), then, for 16-bit inputs, the chunk's raw inputs (fp32 inputs are copied in
-// place into the prepared arrays).
+// Dynamic shared memory: the chunk's prepared token quantities and the
+// forward walk's v - S'^T k_hat per token (fp32), then one area used first
+// for the chunk's raw 16-bit inputs (fp32 inputs are copied in place into the
+// prepared arrays) and then, in the reverse walk, for the warps' staged
+// output partials.
 template <int DK, typename T>
 constexpr size_t chunk_raw_bytes() {
     return sizeof(T) == 4 ? 0 : (size_t)kBwChunk * (3 * DK + 2 * kBwCols + 1) * sizeof(T);
 }
+template <int DK>
+constexpr size_t chunk_red_bytes() {
+    return (size_t)kBwRed * kBwWarps * (3 * DK + 1) * sizeof(float);
+}
 template <int DK, typename T>
 constexpr size_t chunk_stage_bytes() {
     return (size_t)kBwChunk * (3 * DK + 3 * kBwCols + 2) * sizeof(float) +
-           chunk_raw_bytes<DK, T>();
+           (chunk_raw_bytes<DK, T>() > chunk_red_bytes<DK>() ? chunk_raw_bytes<DK, T>()
+                                                             : chunk_red_bytes<DK>());
 }
 
+// Thread layout: warp w owns the 4 whole value columns 4w .. 4w+3 of the
+// CTA's 32 and lane l the state rows l + 32 r, so that every column sum of
+// the recurrence (S'^T k_hat forward, G^T k_hat in reverse) and the values
+// formed from it (u, du) stay inside the warp: neither walk needs a CTA
+// barrier for the recurrence.  Only the per-row outputs (dq_hat, dk_hat,
+// dalpha) and dbeta are summed over the 8 warps, kBwRed tokens at a time.
 template <int DK, int DV, typename T>
 __global__ void __launch_bounds__(kBwThreads, 2)
 kda_backward_kernel(const BackwardParams p) {
     constexpr int NS = DV / kBwCols;       // CTAs per (sequence, head)
     constexpr int DVS = kBwCols;
-    constexpr int LPR = DVS / 4;           // lanes per state row (one float4 each)
-    constexpr int RPW = 32 / LPR;          // rows per warp pass
-    constexpr int RSTEP = kBwWarps * RPW;  // rows per CTA pass
-    constexpr int RPT = DK / RSTEP;        // rows per thread
+    constexpr int RPT = DK / 32;           // rows per thread
     constexpr int C = kBwChunk;
     constexpr int PW = 3 * DK + 1;         // partials per (split, token, head)
-    static_assert(RPT >= 1 && RPT * RSTEP == DK, "bad state tiling");
-    static_assert(DK + DVS <= kBwThreads, "token loaders need DK + 32 threads");
-
-    __shared__ BwShared sh;
+    static_assert(RPT >= 1 && RPT * 32 == DK, "bad state tiling");
+    static_assert(DVS == 4 * kBwWarps, "a warp owns 4 value columns");
 
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-    const int cg = lane % LPR, rs = lane / LPR;
     const int split = blockIdx.x % NS;
     const int h = (blockIdx.x / NS) % p.H;
     const int n = blockIdx.x / (NS * p.H);
     const int col0 = split * DVS;
+    const int wc0 = 4 * w;                 // the warp's first column within the CTA's
     const int H = p.H;
     const T* q = static_cast<const T*>(p.q);
     const T* k = static_cast<const T*>(p.k);
@@ -180,14 +131,16 @@ kda_backward_kernel(const BackwardParams p) {
     const int64_t len = eos - bos;
     const int64_t nchunks = (len + C - 1) / C;
     const size_t SS = (size_t)DK * DV;
-    // this pair's chunk scratch
-    float* scratch = p.scratch + ((size_t)n * H + h) * C * SS;
+    // this CTA's part of its pair's chunk scratch, thread-major: the float4 of
+    // token j, row pass r, thread tid at (j * RPT + r) * kBwThreads + tid
+    float4* scratch = reinterpret_cast<float4*>(p.scratch + ((size_t)n * H + h) * C * SS +
+                                                (size_t)split * C * DK * DVS);
     const float eA = expf(p.A[h]);
     const float scale = p.scale;
 
-    auto row_of = [&](int r) { return r * RSTEP + w * RPW + rs; };
-    // float4 index of this thread's part of row r in a full d_k x d_v state
-    auto st_idx = [&](int r) { return ((size_t)row_of(r) * DV + col0) / 4 + cg; };
+    // float4 index of the thread's part of its r-th row in a full d_k x d_v state
+    auto st_idx = [=](int r) { return ((size_t)(lane + 32 * r) * DV + col0 + wc0) / 4; };
+    auto sc_idx = [=](int j, int r) { return ((size_t)j * RPT + r) * kBwThreads + tid; };
 
     // ---- the chunk's token quantities, prepared in shared memory (fp32) ----
     // q_hat (normalised, scaled), k_hat, alpha, the CTA's v and dO columns,
@@ -203,7 +156,9 @@ kda_backward_kernel(const BackwardParams p) {
     float* pw = pdo + C * DVS;                        // [C][DVS]: v - S'^T k_hat
     float* pb = pw + C * DVS;                         // [C]
     float* pqk = pb + C;                              // [C]
-    // the raw copy: in place for fp32 inputs, after the prepared arrays else
+    // the raw copy: in place for fp32 inputs, in the shared area else; the
+    // staged output partials [kBwRed][kBwWarps][PW] in the same area
+    float* red = pqk + C;
     T* rq;
     T* rk_;
     T* rz;
@@ -218,7 +173,7 @@ kda_backward_kernel(const BackwardParams p) {
         rdo = reinterpret_cast<T*>(pdo);
         rb = reinterpret_cast<T*>(pb);
     } else {
-        rq = reinterpret_cast<T*>(pqk + C);
+        rq = reinterpret_cast<T*>(red);
         rk_ = rq + C * DK;
         rz = rk_ + C * DK;
         rv = rz + C * DK;
@@ -296,34 +251,28 @@ kda_backward_kernel(const BackwardParams p) {
 
     // ---- one forward step on S (registers) for token jt of the chunk; it
     // also keeps w = v - S'^T k_hat of the token (S' = Diag(alpha) S_{t-1})
-    // for the reverse walk ----
+    // for the reverse walk.  Warp-local: lanes 8c .. 8c+7 finish column c. ----
     float4 S[RPT];
+    const int cw = lane >> 3;   // the warp column whose sums this lane finishes
     auto forward_step = [&](int jt) {
         float4 ak = make_float4(0.f, 0.f, 0.f, 0.f);
+        float kreg[RPT];
 #pragma unroll
         for (int r = 0; r < RPT; ++r) {
-            const int i = row_of(r);
+            const int i = lane + 32 * r;
             const float a = pa[jt * DK + i], kk = pk[jt * DK + i];
+            kreg[r] = kk;
             S[r].x *= a; S[r].y *= a; S[r].z *= a; S[r].w *= a;
             ak.x += kk * S[r].x; ak.y += kk * S[r].y; ak.z += kk * S[r].z; ak.w += kk * S[r].w;
         }
-        sh.red[w][0][4 * cg + rs] = rowgroups_sum4(ak, lane);
-        __syncthreads();
-        if (tid < DVS) {
-            float r = 0.f;
-#pragma unroll
-            for (int ww = 0; ww < kBwWarps; ++ww) {
-                r += sh.red[ww][0][tid];
-            }
-            const float wv = pv[jt * DVS + tid] - r;
-            pw[jt * DVS + tid] = wv;
-            sh.u[tid] = pb[jt] * wv;
+        const float wv = pv[jt * DVS + wc0 + cw] - warp_colsum4(ak, lane);
+        if ((lane & 7) == 0) {
+            pw[jt * DVS + wc0 + cw] = wv;
         }
-        __syncthreads();
-        const float4 u4 = *reinterpret_cast<const float4*>(&sh.u[4 * cg]);
+        const float4 u4 = gather4(pb[jt] * wv);
 #pragma unroll
         for (int r = 0; r < RPT; ++r) {
-            const float kk = pk[jt * DK + row_of(r)];
+            const float kk = kreg[r];
             S[r].x += kk * u4.x; S[r].y += kk * u4.y; S[r].z += kk * u4.z; S[r].w += kk * u4.w;
         }
     };
@@ -332,13 +281,6 @@ kda_backward_kernel(const BackwardParams p) {
 #pragma unroll
         for (int r = 0; r < RPT; ++r) {
             S[r] = sp[st_idx(r)];
-        }
-    };
-    auto store_state = [&](float* dst, const float4* X) {
-        float4* dp = reinterpret_cast<float4*>(dst);
-#pragma unroll
-        for (int r = 0; r < RPT; ++r) {
-            dp[st_idx(r)] = X[r];
         }
     };
 
@@ -382,7 +324,7 @@ kda_backward_kernel(const BackwardParams p) {
         const int64_t cl = min((int64_t)C, len - i0);
         // 2a: the chunk's states S_{t-1} into the scratch, from the state at
         // the chunk start (the initial state for chunk 0, else checkpoint c)
-        __syncthreads();   // the previous chunk's last token has been read
+        __syncthreads();   // the previous chunk's partials and last token have been read
         prepare(bos + i0, (int)cl);
         if (c > 0) {
             load_state(p.pool + ((size_t)(ck_base + c - 1) * H + h) * SS);
@@ -395,79 +337,61 @@ kda_backward_kernel(const BackwardParams p) {
             }
         }
         for (int j = 0; j < (int)cl; ++j) {
-            store_state(scratch + (size_t)j * SS, S);
-            forward_step(j);   // (after the last token only its w is used)
-        }
-        // 2b: the chunk's tokens in reverse (each thread reads back the
-        // scratch elements it wrote: no barrier needed for them).  The next
-        // reverse token's S_{t-1} is loaded while this token is worked on.
-        float4 Snext[RPT];
-        {
-            const float4* sp = reinterpret_cast<const float4*>(scratch + (size_t)(cl - 1) * SS);
 #pragma unroll
             for (int r = 0; r < RPT; ++r) {
-                Snext[r] = sp[st_idx(r)];
+                scratch[sc_idx(j, r)] = S[r];
             }
+            forward_step(j);   // (after the last token only its w is used)
         }
+        __syncwarp();   // the warp's w entries are visible to all its lanes
+        // 2b: the chunk's tokens in reverse (each thread reads back the
+        // scratch elements it wrote).  The next reverse token's S_{t-1} is
+        // loaded while this token is worked on.
+        float4 Snext[RPT];
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            Snext[r] = scratch[sc_idx((int)cl - 1, r)];
+        }
+        int slot = 0;   // staged tokens j + slot - 1 .. j + 1 (one per slot, in walk order)
         for (int j = (int)cl - 1; j >= 0; --j) {
-            const int64_t t = bos + i0 + j;
 #pragma unroll
             for (int r = 0; r < RPT; ++r) {
                 S[r] = Snext[r];                           // S = S_{t-1}
             }
             if (j > 0) {
-                const float4* sp = reinterpret_cast<const float4*>(scratch + (size_t)(j - 1) * SS);
 #pragma unroll
                 for (int r = 0; r < RPT; ++r) {
-                    Snext[r] = sp[st_idx(r)];
+                    Snext[r] = scratch[sc_idx(j - 1, r)];
                 }
             }
             // u = beta w (from the forward walk); dq_hat = S_t dO needs no G:
             // S_t = S' + k_hat u^T, S' = Diag(alpha) S_{t-1}
             const float b = pb[j];
-            const float4 w4 = *reinterpret_cast<const float4*>(&pw[j * DVS + 4 * cg]);
+            const float4 w4 = *reinterpret_cast<const float4*>(&pw[j * DVS + wc0]);
             const float4 u4 = make_float4(b * w4.x, b * w4.y, b * w4.z, b * w4.w);
-            const float4 do4 = *reinterpret_cast<const float4*>(&pdo[j * DVS + 4 * cg]);
+            const float4 do4 = *reinterpret_cast<const float4*>(&pdo[j * DVS + wc0]);
             float dqv[RPT], dkv[RPT], dav[RPT];
             // column sums gk = G^T k_hat (G = dL/dS_t from the future)
             float4 ag = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int r = 0; r < RPT; ++r) {
-                const int i = row_of(r);
+                const int i = lane + 32 * r;
                 const float a = pa[j * DK + i], kk = pk[j * DK + i];
                 ag.x += kk * G[r].x; ag.y += kk * G[r].y; ag.z += kk * G[r].z; ag.w += kk * G[r].w;
                 dqv[r] = (a * S[r].x + kk * u4.x) * do4.x + (a * S[r].y + kk * u4.y) * do4.y +
                          (a * S[r].z + kk * u4.z) * do4.z + (a * S[r].w + kk * u4.w) * do4.w;
             }
-            sh.red[w][1][4 * cg + rs] = rowgroups_sum4(ag, lane);
-            __syncthreads();
-            // per value column (warp 0, one lane per column): du, dv and db
-            float* part = p.part + (((size_t)split * p.total_T + t) * H + h) * PW;
-            if (tid < DVS) {
-                float gk = 0.f;
-#pragma unroll
-                for (int ww = 0; ww < kBwWarps; ++ww) {
-                    gk += sh.red[ww][1][tid];
-                }
-                const float wv = pw[j * DVS + tid];                 // v - S'^T kh
-                const float duj = gk + pqk[j] * pdo[j * DVS + tid];
-                sh.du[tid] = duj;
-                p.dv[((size_t)t * H + h) * DV + col0 + tid] = b * duj;
-                float db = duj * wv;
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    db += __shfl_xor_sync(0xffffffffu, db, off);
-                }
-                if (tid == 0) {
-                    part[3 * DK] = db;
-                }
+            // du = G^T kh + (qh . kh) dO, finished for column cw on lanes 8cw ..
+            const float duc = warp_colsum4(ag, lane) + pqk[j] * pdo[j * DVS + wc0 + cw];
+            const int64_t t = bos + i0 + j;
+            if ((lane & 7) == 0) {
+                p.dv[((size_t)t * H + h) * DV + col0 + wc0 + cw] = b * duc;
             }
-            __syncthreads();
+            const float4 du4 = gather4(duc);
             // per state row: dkh, da and the new G
-            const float4 du4 = *reinterpret_cast<const float4*>(&sh.du[4 * cg]);
 #pragma unroll
             for (int r = 0; r < RPT; ++r) {
-                const int i = row_of(r);
+                const int i = lane + 32 * r;
                 const float a = pa[j * DK + i], kk = pk[j * DK + i], qq = pq[j * DK + i];
                 const float4 sp = make_float4(a * S[r].x, a * S[r].y, a * S[r].z, a * S[r].w);
                 float4 g = make_float4(G[r].x + qq * do4.x, G[r].y + qq * do4.y,
@@ -479,11 +403,47 @@ kda_backward_kernel(const BackwardParams p) {
                 dav[r] = g.x * S[r].x + g.y * S[r].y + g.z * S[r].z + g.w * S[r].w;
                 G[r] = make_float4(a * g.x, a * g.y, a * g.z, a * g.w);
             }
-            rows_sum_store<RPT, DK>(dqv, dkv, dav, lane, row_of, part);
+            // stage the warp's partials (its 4 columns) of dq_hat, dk_hat,
+            // dalpha and dbeta for this token
+            float* rw = red + ((size_t)slot * kBwWarps + w) * PW;
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) {
+                const int i = lane + 32 * r;
+                rw[i] = dqv[r];
+                rw[DK + i] = dkv[r];
+                rw[2 * DK + i] = dav[r];
+            }
+            if (lane == 0) {
+                rw[3 * DK] = du4.x * w4.x + du4.y * w4.y + du4.z * w4.z + du4.w * w4.w;
+            }
+            ++slot;
+            if (slot == kBwRed || j == 0) {
+                // the CTA's partials of the staged tokens: slot s holds token
+                // j + slot - 1 - s; summed over the warps in a fixed order
+                __syncthreads();
+                for (int e = tid; e < slot * PW; e += kBwThreads) {
+                    const int sl = e / PW, x = e - sl * PW;
+                    float acc = 0.f;
+#pragma unroll
+                    for (int ww = 0; ww < kBwWarps; ++ww) {
+                        acc += red[((size_t)sl * kBwWarps + ww) * PW + x];
+                    }
+                    const int64_t ts = bos + i0 + j + slot - 1 - sl;
+                    p.part[(((size_t)split * p.total_T + ts) * H + h) * PW + x] = acc;
+                }
+                __syncthreads();   // the staging area is free again
+                slot = 0;
+            }
         }
     }
     // dL/dS_0 (this CTA's columns)
-    store_state(p.dS0 + ((size_t)n * H + h) * SS, G);
+    {
+        float4* dp = reinterpret_cast<float4*>(p.dS0 + ((size_t)n * H + h) * SS);
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            dp[st_idx(r)] = G[r];
+        }
+    }
 }
 
 // Per (token, head): the column partials of dqh, dkh, da and db added up,

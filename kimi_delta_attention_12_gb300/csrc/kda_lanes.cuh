@@ -16,4 +16,22 @@ __device__ __forceinline__ float rowgroups_sum4(float4 v, int lane) {
     return (b3 ? k1 : k0) + __shfl_xor_sync(0xffffffffu, b3 ? k0 : k1, 8);
 }
 
+// Sum of a float4 of column partials over all 32 lanes of a warp (rows):
+// transposed over lane bits 4 and 3 as above, then butterflies over bits 2,
+// 1, 0 (6 shuffles).  Returns the sum of component (lane >> 3), on every lane.
+__device__ __forceinline__ float warp_colsum4(float4 v, int lane) {
+    float s = rowgroups_sum4(v, lane);
+    s += __shfl_xor_sync(0xffffffffu, s, 4);
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    return s;
+}
+
+// The float4 whose component c is on lanes 8c .. 8c+7 (the layout
+// warp_colsum4 leaves), on every lane.
+__device__ __forceinline__ float4 gather4(float x) {
+    return make_float4(__shfl_sync(0xffffffffu, x, 0), __shfl_sync(0xffffffffu, x, 8),
+                       __shfl_sync(0xffffffffu, x, 16), __shfl_sync(0xffffffffu, x, 24));
+}
+
 }  // namespace kda
