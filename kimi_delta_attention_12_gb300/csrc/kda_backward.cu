@@ -66,7 +66,7 @@ constexpr int kBwCols = 32;   // value columns per CTA (8 lanes x float4 per sta
 
 // Tokens whose per-warp output partials are staged in shared memory before
 // the CTA sums them over its warps.
-constexpr int kBwRed = 4;
+constexpr int kBwRed = 8;
 
 // Dynamic shared memory: the chunk's prepared token quantities and the
 // forward walk's v - S'^T k_hat per token (fp32), then one area used first
