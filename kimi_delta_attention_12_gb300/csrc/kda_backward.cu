@@ -27,8 +27,11 @@
 // tokens backwards.  The scratch keeps memory at 64 states per (sequence,
 // head).  Both walks over a chunk read its tokens' q_hat, k_hat, alpha, v and
 // dO columns and beta from shared memory, computed once for the chunk by the
-// whole CTA, so the token chain has no global loads, no reductions over the
-// key channels and two barriers per token.
+// whole CTA, so the token chain has no global loads and no reductions over
+// the key channels.  Each warp owns 4 whole value columns, so the
+// recurrence's column sums never leave the warp and neither walk takes a CTA
+// barrier per token; the outputs are summed over the warps every kBwRed
+// tokens.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
