@@ -12,7 +12,8 @@ Sources (page titles and sections):
     g = -5 sigmoid(e^A z), alpha = e^g, and Q/K normalisation inside the op;
     the short convolutions before it and their persistent conv state (the
     prefill and decode bullets of the same section); and the gradients of a
-    loss through the recurrence (reverse mode, for the training form).
+    loss through the recurrence (reverse mode, for the training form), also
+    in the chunked form a chunk-parallel backward computes.
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against closed
 forms, brute force and invariants that do not reuse this code.
@@ -347,4 +348,171 @@ def kda_reference_backward(q, k, v, z, beta, A, initial_state=None, cu_seqlens=N
         raise RuntimeError(f"oracle backward failed with status {rc}")
     out["dA"] = gA.sum(axis=0)
     out["threads"] = int(rc)
+    return out
+
+
+def _sigmoid(x):
+    """Logistic function in fp64, without overflow for any x."""
+    return 0.5 * (1.0 + np.tanh(0.5 * x))
+
+
+def kda_reference_backward_chunked(q, k, v, z, beta, A, initial_state=None, cu_seqlens=None,
+                                   dO=None, dS_final=None, chunk: int = 64, scale: float = 1.0,
+                                   l2norm: bool = True, eps: float = EPS,
+                                   softplus_gate: bool = False):
+    """The gradients of kda_reference_backward by the chunked form of the
+    recurrence (fp64 numpy): the algebra a chunk-parallel backward computes.
+
+    Forward inside a chunk of the sequence (tokens r = 1..L, start state S0),
+    from the recurrence of the section by unrolling it with the in-chunk
+    cumulative gate gamma_r = sum_{j<=r} g_j (per key channel):
+      E[r, i]   = e^(gamma_r - gamma_i)  for i <= r (0 above the diagonal)
+      A_kk[r,i] = beta_r sum_c kh_r kh_i E[r,i]    (i < r)
+      A_qk[r,i] = sum_c qh_r kh_i E[r,i]           (i <= r)
+      K+ = kh e^gamma,  Q+ = qh e^gamma,  K_end = kh e^(gamma_L - gamma)
+      X = V - K+ S0;  (I + A_kk) U = Diag(beta) X
+      O = Q+ S0 + A_qk U;  S_L = Diag(e^gamma_L) S0 + K_end^T U
+    Backward of that chunk, given dO and dS_L (the next chunk's dS0):
+      dU = A_qk^T dO + K_end dS_L;  dY = (I + A_kk)^-T dU;  dA_kk = -dY U^T
+      (strictly lower);  dX = Diag(beta) dY;  dbeta += rowsum(dY * X);
+      dV = dX;  dS0 = Q+^T dO + Diag(e^gamma_L) dS_L - K+^T dX
+    then the elementwise chains of K+, Q+, K_end, A_kk, A_qk into qh, kh,
+    beta and gamma, dg = the reverse cumulative sum of dgamma over the chunk,
+    and, per token, the gate and normalisation derivatives (as
+    kda_reference_backward).  Chunks are walked last to first, the state at
+    each chunk start taken from a forward pass over the chunks.
+
+    Same layouts and return dict as kda_reference_backward (without
+    "threads")."""
+    q, k, v, z, beta, A = (_f64(t) for t in (q, k, v, z, beta, A))
+    total_T, H, dk = q.shape
+    dv = v.shape[-1]
+    cu = _cu(cu_seqlens, total_T)
+    N = cu.size - 1
+    S0all = _f64(initial_state)
+    dO = _f64(dO)
+    dSf = _f64(dS_final)
+    if dO is None or dO.shape != (total_T, H, dv):
+        raise ValueError("dO must be [total_T, H, d_v]")
+    if chunk < 1:
+        raise ValueError("chunk must be >= 1")
+    out = dict(dq=np.zeros((total_T, H, dk)), dk=np.zeros((total_T, H, dk)),
+               dv=np.zeros((total_T, H, dv)), dz=np.zeros((total_T, H, dk)),
+               dbeta=np.zeros((total_T, H)), dA=np.zeros(H), dS0=np.zeros((N, H, dk, dv)))
+    for n in range(N):
+        bos, eos = int(cu[n]), int(cu[n + 1])
+        L = eos - bos
+        for h in range(H):
+            S = np.zeros((dk, dv)) if S0all is None else S0all[n, h].copy()
+            dS = np.zeros((dk, dv)) if dSf is None else dSf[n, h].copy()
+            if L == 0:
+                out["dS0"][n, h] = dS
+                continue
+            qq, kk, vv = q[bos:eos, h], k[bos:eos, h], v[bos:eos, h]
+            zz, bb = z[bos:eos, h], beta[bos:eos, h]
+            if l2norm:
+                rq = 1.0 / np.sqrt((qq * qq).sum(axis=1) + eps)
+                rk = 1.0 / np.sqrt((kk * kk).sum(axis=1) + eps)
+            else:
+                rq = np.ones(L)
+                rk = np.ones(L)
+            qh = scale * qq * rq[:, None]
+            kh = kk * rk[:, None]
+            g = gate_softplus(zz, A[h]) if softplus_gate else gate(zz, A[h])
+
+            def chunk_terms(c0, c1, S0):
+                Qh, Kh, V, B = qh[c0:c1], kh[c0:c1], vv[c0:c1], bb[c0:c1]
+                gam = np.cumsum(g[c0:c1], axis=0)
+                Lc = c1 - c0
+                le = np.tril(np.ones((Lc, Lc), dtype=bool))
+                lt = np.tril(np.ones((Lc, Lc), dtype=bool), -1)
+                D = np.where(le[:, :, None], gam[:, None, :] - gam[None, :, :], -np.inf)
+                E = np.exp(D)
+                Akk = B[:, None] * np.einsum("rc,ic,ric->ri", Kh, Kh, E) * lt
+                Aqk = np.einsum("rc,ic,ric->ri", Qh, Kh, E)
+                eg = np.exp(gam)
+                Kp, Qp = Kh * eg, Qh * eg
+                Kend = Kh * np.exp(gam[-1][None, :] - gam)
+                X = V - Kp @ S0
+                Mt = np.eye(Lc) + Akk
+                U = np.linalg.solve(Mt, B[:, None] * X)
+                return dict(Qh=Qh, Kh=Kh, B=B, gam=gam, le=le, lt=lt, E=E, Akk=Akk, Aqk=Aqk,
+                            eg=eg, Kp=Kp, Qp=Qp, Kend=Kend, X=X, Mt=Mt, U=U)
+
+            starts = list(range(0, L, chunk))
+            S_start = []
+            for c0 in starts:
+                c1 = min(c0 + chunk, L)
+                S_start.append(S.copy())
+                t_ = chunk_terms(c0, c1, S)
+                S = np.exp(t_["gam"][-1])[:, None] * S + t_["Kend"].T @ t_["U"]
+
+            dqh = np.zeros((L, dk))
+            dkh = np.zeros((L, dk))
+            dg = np.zeros((L, dk))
+            for ci in range(len(starts) - 1, -1, -1):
+                c0 = starts[ci]
+                c1 = min(c0 + chunk, L)
+                S0 = S_start[ci]
+                t_ = chunk_terms(c0, c1, S0)
+                Qh, Kh, B, E, U, X = t_["Qh"], t_["Kh"], t_["B"], t_["E"], t_["U"], t_["X"]
+                gam, Kp, Qp, Kend, eg = t_["gam"], t_["Kp"], t_["Qp"], t_["Kend"], t_["eg"]
+                egL = np.exp(gam[-1])
+                dOc = dO[bos + c0:bos + c1, h]
+                dU = t_["Aqk"].T @ dOc + Kend @ dS
+                dAqk = (dOc @ U.T) * t_["le"]
+                dQp = dOc @ S0.T
+                dS0 = Qp.T @ dOc + egL[:, None] * dS
+                dKend = U @ dS.T
+                dgamL = egL * (dS * S0).sum(axis=1)
+                dY = np.linalg.solve(t_["Mt"].T, dU)
+                dAkk = -(dY @ U.T) * t_["lt"]
+                dX = B[:, None] * dY
+                dbc = (dY * X).sum(axis=1)
+                dKp = -dX @ S0.T
+                dS0 = dS0 - Kp.T @ dX
+                dKh = dKp * eg
+                dgam = dKp * Kp
+                dQh = dQp * eg
+                dgam += dQp * Qp
+                dKh += dKend * np.exp(gam[-1][None, :] - gam)
+                dgam -= dKend * Kend
+                dgamL += (dKend * Kend).sum(axis=0)
+                T1 = dAkk[:, :, None] * B[:, None, None] * E
+                dbc += np.einsum("ri,rc,ic,ric->r", dAkk, Kh, Kh, E)
+                dKh += np.einsum("ric,ic->rc", T1, Kh) + np.einsum("ric,rc->ic", T1, Kh)
+                P1 = T1 * Kh[:, None, :] * Kh[None, :, :]
+                dgam += P1.sum(axis=1) - P1.sum(axis=0)
+                T2 = dAqk[:, :, None] * E
+                dQh += np.einsum("ric,ic->rc", T2, Kh)
+                dKh += np.einsum("ric,rc->ic", T2, Qh)
+                P2 = T2 * Qh[:, None, :] * Kh[None, :, :]
+                dgam += P2.sum(axis=1) - P2.sum(axis=0)
+                dgam[-1] += dgamL
+                dg[c0:c1] = np.cumsum(dgam[::-1], axis=0)[::-1]
+                dqh[c0:c1] = dQh
+                dkh[c0:c1] = dKh
+                out["dv"][bos + c0:bos + c1, h] = dX
+                out["dbeta"][bos + c0:bos + c1, h] = dbc
+                dS = dS0
+            out["dS0"][n, h] = dS
+            # gate: g = -5 sigmoid(x) or -softplus(x), x = e^A z
+            eA = np.exp(A[h])
+            x = eA * zz
+            if softplus_gate:
+                dx = -dg * _sigmoid(x)
+            else:
+                s = _sigmoid(x)
+                dx = dg * (G_MIN * s * (1.0 - s))
+            out["dz"][bos:eos, h] = dx * eA
+            out["dA"][h] += float((dx * x).sum())
+            # normalisation: xh = m x rho, rho = (sum x^2 + eps)^-1/2
+            if l2norm:
+                out["dq"][bos:eos, h] = scale * (rq[:, None] * dqh - (rq ** 3 * (qq * dqh).sum(
+                    axis=1))[:, None] * qq)
+                out["dk"][bos:eos, h] = rk[:, None] * dkh - (rk ** 3 * (kk * dkh).sum(
+                    axis=1))[:, None] * kk
+            else:
+                out["dq"][bos:eos, h] = scale * dqh
+                out["dk"][bos:eos, h] = dkh
     return out

@@ -619,3 +619,26 @@ def test_backward_identity_closed_form(oracle_mod):
     assert np.all(g["dv"] == 0.0) and np.all(g["dz"] == 0.0) and g["dA"][0] == 0.0
     for t in range(T):
         assert _close(g["dq"][t, 0], S0[0, 0] @ dO[t, 0], 1e-13)
+
+
+@pytest.mark.parametrize("softplus,l2norm", [(False, True), (True, True), (False, False)])
+@pytest.mark.parametrize("C", [1, 3, 16, 64])
+def test_backward_chunked_form_equals_reverse_mode(oracle_mod, softplus, l2norm, C):
+    """The chunked form of the backward (in-chunk cumulative gate, UT system
+    and its transpose, chunks walked last to first with dL/dS carried between
+    them) gives the reverse-mode gradients of the recurrence for every input:
+    chunk sizes that do and do not divide the lengths, an empty sequence, a
+    sequence shorter than one chunk, nonzero S0 and dL/dS_T, scale != 1."""
+    rng = np.random.default_rng(530 + C + 2 * softplus + l2norm)
+    lens = [70, 0, 5, 33]
+    T, H, dk, dv = sum(lens), 2, 6, 5
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    q, k, v, z, beta, A, S0 = _rand_case(rng, T, H, dk, dv, N=len(lens), zscale=2.0)
+    dO = rng.standard_normal((T, H, dv))
+    dSf = rng.standard_normal((len(lens), H, dk, dv))
+    flags = dict(softplus_gate=softplus, l2norm=l2norm, scale=0.8)
+    ref = oracle_mod.kda_reference_backward(q, k, v, z, beta, A, S0, cu, dO, dSf, **flags)
+    got = oracle_mod.kda_reference_backward_chunked(q, k, v, z, beta, A, S0, cu, dO, dSf,
+                                                    chunk=C, **flags)
+    for key in ("dq", "dk", "dv", "dz", "dbeta", "dA", "dS0"):
+        assert _close(got[key], ref[key], 1e-10), key
