@@ -231,7 +231,9 @@ KDA_API int kda_decode_step(const void* q, const void* k, const void* v, const v
  *  cu_seqlens      as kda_prefill (device [N + 1], or NULL for equal lengths)
  *  W               1 .. 4;  flags: 0 or KDA_FLAG_CONV_SILU
  *  q_out, k_out, v_out   the convolved tensors, layouts of q, k, v, rounded
- *                  to dt (round to nearest even)
+ *                  to dt (round to nearest even); the taps and sums in fp32,
+ *                  the SiLU on the approximate exp2 and reciprocal (relative
+ *                  error near 1e-7 before that rounding)
  * Buffers are device memory owned by the caller, 16-byte aligned (conv_w
  * too).  Errors (nothing is launched): KDA_ERR_INVALID_ARG for a missing
  * buffer, W outside 1 .. 4, an unknown flag, bad cu_seqlens_host, an output
