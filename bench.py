@@ -2,12 +2,17 @@
 """KDA benchmark on GB300: prefill tokens/s and decode state GB/s.
 
 Default workload (one "step" = one pass of the whole hot path):
-  kda_prefill on B=1, H=32, T=4096, d_k=d_v=128 (bf16 q/k/v/z/beta, fp32 A,
-  zero initial state) returning the fp32 final state, then one kda_decode_step
-  for each of the 32 heads from that final state (the decode handoff).
-The headline `value` is prefill tokens/s (B*T / step time).  The `decode`
-object times the decode workload B=256, H=96, d=128 (fp32 state ~1.6 GB resident
-in HBM, bf16 per-step inputs) over 64 consecutive steps, as state GB/s.
+  kda_prefill on the long-prefill workload B=1, H=96, T=65,536, d_k=d_v=128
+  (bf16 q/k/v/z/beta, fp32 A, zero initial state) returning the fp32 final
+  state, then one kda_decode_step for each of the 96 heads from that final
+  state (the decode handoff).  This is the largest single-GPU prefill
+  configuration; the headline `value` is its prefill tokens/s (B*T / step
+  time).  Further keys: the 4K prefill (B=1, H=32, T=4096) and the varlen
+  workload (16 packed sequences, H=64, nonzero initial states), each with its
+  roofline; the further rows (checkpoints, softplus gate, short
+  convolutions, backward) on the 4K workload; and the decode workload
+  B=256, H=96, d=128 (fp32 state ~1.6 GB resident in HBM) over 64
+  consecutive steps, as state GB/s.
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kda|reference]
 Under torchrun each rank runs an independent replica (the path needs no
@@ -27,7 +32,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "KDA prefill tokens/s (% tensor peak); decode state GB/s (% HBM peak), 1 GB300"
-PREFILL_SHAPE = dict(B=1, H=32, T=4096, d=128)
+# the headline: the long prefill with its decode handoff (largest single-GPU config)
+PREFILL_SHAPE = dict(B=1, H=96, T=65536, d=128)
+PREFILL_4K_SHAPE = dict(B=1, H=32, T=4096, d=128)
+# heads of the headline workload the oracle runs for the CPU baseline (the
+# figure is extrapolated to all heads; heads are independent)
+ORACLE_SAMPLE_HEADS = 16
 DECODE_SHAPE = dict(B=256, H=96, d=128, steps=64)
 L2_BYTES = 129 * 1024 * 1024
 
@@ -43,15 +53,18 @@ def _peaks():
                 source="fallback")
 
 
-def prefill_algorithmic(B, H, T, d, C=64):
-    """Algorithmic bytes and flops of one prefill call (d_k = d_v = d, bf16 I/O).
+def prefill_algorithmic(B, H, T, d, C=64, read_state=False, N=None):
+    """Algorithmic bytes and flops of one prefill call over B*T packed tokens
+    in N sequences (default B; d_k = d_v = d, bf16 I/O).
 
-    bytes: q, k, v, z, o at 2 B per element, beta at 2 B per head-token, the fp32
-    final state once (zero initial state is not read).
+    bytes: q, k, v, z, o at 2 B per element, beta at 2 B per head-token, the
+    fp32 final state once per (sequence, head), and the initial state once
+    more when it is read (a zero initial state is not).
     flops: 6 d^2 per head-token for the three state contractions plus
     (C+1)(3d+2d) - d for the causal halves of the intra-chunk products."""
+    N = B if N is None else N
     ht = B * T * H
-    byts = ht * (5 * d * 2 + 2) + B * H * d * d * 4
+    byts = ht * (5 * d * 2 + 2) + (2 if read_state else 1) * N * H * d * d * 4
     flops = ht * (6 * d * d + (C + 1) * 5 * d - d)
     return byts, flops
 
@@ -59,7 +72,7 @@ def prefill_algorithmic(B, H, T, d, C=64):
 # Sources of the chunked prefill kernels; a profile summary records their
 # digest so that its DRAM traffic is only reported for the kernel it measured.
 PREFILL_SOURCES = ("kda_prefill_sm103.cu", "kda_chunk_phases.cuh", "sm103_ptx.cuh",
-                   "kda_chunked.h")
+                   "kda_chunked.h", "kda_seqlens.cuh")
 
 
 def prefill_source_digest() -> str:
@@ -71,10 +84,12 @@ def prefill_source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel: str):
-    """dram bytes read + written per launch of `kernel` from its committed ncu
-    summary, or None when there is none for the current sources."""
-    prof = os.path.join(ROOT, "profiles", f"{kernel}_b1_h32_t4096.md")
+def profiled_traffic(profile: str, units: int):
+    """DRAM bytes read + written per launch from the committed ncu summary
+    profiles/<profile>.md, scaled from the profiled launch's (token, head)
+    units to `units` (the kernel's traffic grows in proportion to them), or
+    None when there is no summary for the current sources."""
+    prof = os.path.join(ROOT, "profiles", f"{profile}.md")
     if not os.path.exists(prof):
         return None
     rows = {}
@@ -85,9 +100,11 @@ def profiled_traffic(kernel: str):
     if rows.get("source_digest") != prefill_source_digest():
         return None
     try:
-        return int(rows["traffic_bytes_per_launch"])
+        per = int(rows["traffic_bytes_per_launch"])
+        prof_units = int(rows.get("head_token_units", "0")) or units
     except (KeyError, ValueError):
         return None
+    return per * units / prof_units
 
 
 def decode_algorithmic(B, H, d):
@@ -197,8 +214,8 @@ def _max_over_ranks(pg, x: float) -> float:
 
 # ------------------------------------------------------------------ oracle arm
 def run_oracle_sample(T_sample: int, H: int, d: int, seed: int = 0):
-    """Time the fp64 CPU oracle on the first T_sample tokens of the prefill
-    workload (all heads).  Returns (tokens/s, seconds, threads)."""
+    """Time the fp64 CPU oracle on one sequence of T_sample tokens and H heads
+    (the prefill recipe's inputs).  Returns (head-tokens/s, seconds, threads)."""
     import torch
     import oracle
     from kimi_delta_attention_12_gb300 import inputs
@@ -207,7 +224,7 @@ def run_oracle_sample(T_sample: int, H: int, d: int, seed: int = 0):
     t0 = time.perf_counter()
     _, _, threads = oracle.kda_reference(x.q, x.k, x.v, x.z, x.beta, x.A, None, x.cu_seqlens)
     dt = time.perf_counter() - t0
-    return T_sample / dt, dt, threads
+    return T_sample * H / dt, dt, threads
 
 
 def cpu_model() -> str:
@@ -234,8 +251,9 @@ def cpu_model() -> str:
 
 
 def cpu_baseline(H: int, T: int, d: int, cpu_seconds: float = 12.0):
-    """The oracle on the whole prefill workload, repeated until about
-    cpu_seconds of CPU work (wall time x threads) are spent."""
+    """The oracle on the whole prefill workload (B=1, T tokens, H heads),
+    repeated until about cpu_seconds of CPU work (wall time x threads) are
+    spent.  Returns (tokens/s, threads, sample)."""
     runs, wall, threads = 0, 0.0, 1
     while runs == 0 or wall * threads < cpu_seconds:
         _, dt, threads = run_oracle_sample(T, H, d)
@@ -244,6 +262,19 @@ def cpu_baseline(H: int, T: int, d: int, cpu_seconds: float = 12.0):
     value = runs * T / wall
     sample = (f"whole prefill workload (B=1 T={T}, all {H} heads) x {runs} runs, "
               f"{wall:.1f} s wall on {threads} threads, fp64 C oracle")
+    return value, threads, sample
+
+
+def headline_cpu_baseline(H: int, T: int, d: int, H_sample: int = ORACLE_SAMPLE_HEADS):
+    """The oracle on H_sample of the H heads of the long-prefill workload, all
+    T tokens (heads are independent, so the whole workload takes H / H_sample
+    times as long): tokens/s of the whole workload, extrapolated.  Returns
+    (tokens/s, threads, sample)."""
+    hts, dt, threads = run_oracle_sample(T, H_sample, d)
+    value = T / (dt * H / H_sample)
+    sample = (f"{H_sample} of the {H} heads of the workload, all {T} tokens (B=1), "
+              f"{dt:.1f} s wall on {threads} threads, fp64 C oracle; tokens/s extrapolated "
+              f"to all {H} heads")
     return value, threads, sample
 
 
@@ -306,30 +337,34 @@ def row_cpu_baselines(H: int, T: int, d: int, dec_B: int, dec_H: int):
 
 
 def reference_arm(args, world, rank, pg):
+    """The oracle arm: each step runs the fp64 oracle on a bounded sample of
+    the headline workload (ORACLE_SAMPLE_HEADS of its heads, its first
+    T_sample tokens) and reports the whole workload's tokens/s extrapolated
+    from it (heads are independent, and the oracle's cost per token does not
+    depend on the position)."""
     if rank != 0:
         return
     P = PREFILL_SHAPE
-    T_sample = P["T"]
-    # one warm-up and K timed steps; each step is the whole prefill workload
-    # (B=1, T=4096, all 32 heads)
+    Hs, T_sample = ORACLE_SAMPLE_HEADS, 8192
     for _ in range(max(0, min(args.warmup, 1))):
-        run_oracle_sample(256, P["H"], P["d"])
+        run_oracle_sample(256, Hs, P["d"])
     vals, secs, threads = [], 0.0, 1
     for _ in range(args.steps):
-        v, dt, threads = run_oracle_sample(T_sample, P["H"], P["d"])
-        vals.append(v)
+        _, dt, threads = run_oracle_sample(T_sample, Hs, P["d"])
+        vals.append(T_sample / (dt * P["H"] / Hs))
         secs += dt
     value = statistics.median(vals)
-    sample = (f"whole workload B=1 T={T_sample} d=128, all 32 heads, per step; "
-              f"{args.steps} steps, fp64 C oracle")
+    sample = (f"per step {Hs} of the {P['H']} heads x the first {T_sample} of the "
+              f"{P['T']} tokens of the workload; tokens/s extrapolated to the whole "
+              f"workload; {args.steps} steps, fp64 C oracle")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * secs / max(args.steps, 1),
+        "ms_per_workload_extrapolated": 1000.0 * P["T"] / value,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded torch CPU generator)",
-        "config": {"workload": "prefill B=1 H=32 T=4096 d_k=d_v=128 bf16 inputs", "B": 1,
-                   "H": 32, "T": 4096, "d": 128},
+        "config": headline_config(),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
                          "kind": "oracle", "sample": sample, "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -338,7 +373,79 @@ def reference_arm(args, world, rank, pg):
     print(json.dumps(line), flush=True)
 
 
+def headline_config():
+    P = PREFILL_SHAPE
+    return {"workload": f"long prefill B={P['B']} H={P['H']} T={P['T']} d_k=d_v={P['d']} "
+                        "bf16 + final state handed to one decode step",
+            "B": P["B"], "H": P["H"], "T": P["T"], "d": P["d"], "chunk": 64,
+            "l2": "inputs larger than L2 (6.4 GB per step)", "parallelism": "replicas"}
+
+
 # ------------------------------------------------------------------- GPU arm
+def device_prefill_inputs(seq_lens, H: int, d: int, seed: int, dev, nonzero_state=False):
+    """The prefill recipe's distributions drawn on the device with a seeded
+    CUDA generator (the benchmark's large workloads; their values are not
+    compared with the oracle -- the parity tests draw on the host)."""
+    import torch
+    from kimi_delta_attention_12_gb300 import inputs
+    g = torch.Generator(device=dev).manual_seed(seed)
+    T = int(sum(seq_lens))
+    unit = lambda t: t / t.norm(dim=-1, keepdim=True)
+    q = unit(torch.randn(T, H, d, device=dev, generator=g)).bfloat16()
+    k = unit(torch.randn(T, H, d, device=dev, generator=g)).bfloat16()
+    v = torch.randn(T, H, d, device=dev, generator=g).bfloat16()
+    z = torch.randn(T, H, d, device=dev, generator=g).bfloat16()
+    beta = torch.sigmoid(torch.randn(T, H, device=dev, generator=g)).bfloat16()
+    A = 0.5 * torch.randn(H, device=dev, generator=g)
+    S0 = None
+    if nonzero_state:
+        S0 = 0.02 * torch.randn(len(seq_lens), H, d, d, device=dev, generator=g)
+    cu = torch.zeros(len(seq_lens) + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(seq_lens, dtype=torch.int64), 0).to(torch.int32)
+    return inputs.PrefillInputs(q, k, v, z, beta, A, S0, cu.to(dev))
+
+
+def check_status(kda, ws, what):
+    st = kda.workspace_status(ws)
+    assert st == kda.KDA_OK, f"{what}: prefill kernel reported {kda.status_string(st)}"
+
+
+def time_prefill(kda, sets, ws, o, S, cu_host, steps, warmup, stream, what, **kw):
+    """Mean CUDA-event time (ms) of kda_prefill over `steps` calls after
+    `warmup`, inputs rotating over `sets`; the status word is checked after
+    the warm-up and after the timed calls."""
+    import torch
+    for i in range(warmup):
+        x = sets[i % len(sets)]
+        kda.kda_prefill(x.q, x.k, x.v, x.z, x.beta, x.A, x.initial_state, x.cu_seqlens,
+                        cu_seqlens_host=cu_host, o=o, final_state=S, workspace=ws, **kw)
+    check_status(kda, ws, what + " (warm-up)")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for i in range(steps):
+        x = sets[(warmup + i) % len(sets)]
+        ev[i][0].record(stream)
+        kda.kda_prefill(x.q, x.k, x.v, x.z, x.beta, x.A, x.initial_state, x.cu_seqlens,
+                        cu_seqlens_host=cu_host, o=o, final_state=S, workspace=ws, **kw)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    check_status(kda, ws, what)
+    return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+
+def roofline(byts, flops, ms, peaks, traffic=None, kernel=None):
+    gbs = byts / (ms / 1e3) / 1e9
+    tf = flops / (ms / 1e3) / 1e12
+    r = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+         "frac": gbs / peaks["hbm_gbs"], "traffic": traffic, "kernel_ms": ms,
+         "algorithmic_bytes": byts, "algorithmic_flops": flops,
+         "peak_source": peaks["source"] + ", of measured copy peak",
+         "tensor_tflops": tf, "tensor_frac": tf / peaks["bf16_tflops"]}
+    if kernel:
+        r["kernel"] = kernel
+    return r
+
+
 def kda_arm(args, world, rank, local, pg):
     import torch
     import kimi_delta_attention_12_gb300 as kda
@@ -351,33 +458,23 @@ def kda_arm(args, world, rank, local, pg):
     peaks = _peaks()
     if args.only == "decode":
         return decode_only(args, rank, local, dev, stream, peaks)
-    P = PREFILL_SHAPE
-    B, H, T, d = P["B"], P["H"], P["T"], P["d"]
-    byts, flops = prefill_algorithmic(B, H, T, d)
+    if args.only in ("softplus", "backward", "conv", "prefill4k"):
+        return four_k_only(args, rank, dev, stream, peaks)
 
-    # rotating input sets so that each step's inputs are not L2-resident
-    x_host = inputs.make_prefill_inputs([T] * B, H, d, d, torch.bfloat16, seed=rank)
-    set_bytes = byts
-    nsets = max(2, -(-3 * L2_BYTES // set_bytes))
-    sets = []
-    for i in range(nsets):
-        xi = x_host.to(dev) if i == 0 else inputs.PrefillInputs(
-            *(t.clone() if t is not None else None for t in
-              (sets[0].q, sets[0].k, sets[0].v, sets[0].z, sets[0].beta, sets[0].A,
-               sets[0].initial_state, sets[0].cu_seqlens)))
-        sets.append(xi)
+    # ---- the headline: long prefill B=1, H=96, T=65536 + decode handoff ----
+    P = PREFILL_SHAPE
+    B, H, T, d = P["B"], args.prefill_heads or P["H"], args.prefill_tokens or P["T"], P["d"]
+    byts, flops = prefill_algorithmic(B, H, T, d)
+    x = device_prefill_inputs([T] * B, H, d, seed=100 + rank, dev=dev)
+    cu_host = x.cu_seqlens.cpu()
     o = torch.empty(B * T, H, d, dtype=torch.bfloat16, device=dev)
     S = torch.empty(B, H, d, d, dtype=torch.float32, device=dev)
     ws = kda.alloc_workspace(B, B * T, H, d, d, torch.bfloat16, dev)
-    # the library asks for more than the minimal workspace (256 B header + one
-    # int32 per sequence-head, rounded to 256 B) exactly when it runs the split kernel
     minimal_ws = 256 + -(-4 * B * H // 256) * 256
     kernel_name = "kda_split_kernel" if ws.numel() > minimal_ws else "kda_chunked_kernel"
     o_dec = torch.empty(B, H, d, dtype=torch.bfloat16, device=dev)
-    cu_host = sets[0].cu_seqlens.cpu()
 
-    def step(i, ev=None):
-        x = sets[i % nsets]
+    def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
         kda.kda_prefill(x.q, x.k, x.v, x.z, x.beta, x.A, None, x.cu_seqlens,
@@ -388,11 +485,10 @@ def kda_arm(args, world, rank, local, pg):
         kda.kda_decode_step(x.q[:B], x.k[:B], x.v[:B], x.z[:B], x.beta[:B], x.A, S, o=o_dec)
 
     launches_per_step = 2
-    for i in range(args.warmup):
-        step(i)
+    for _ in range(args.warmup):
+        step()
     torch.cuda.synchronize()
-    assert kda.workspace_status(ws) == kda.KDA_OK, "prefill kernel reported a timeout"
-
+    check_status(kda, ws, "headline prefill (warm-up)")
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
@@ -402,52 +498,140 @@ def kda_arm(args, world, rank, local, pg):
     with ClockSampler(local) as clk:
         t_start.record(stream)
         for i in range(args.steps):
-            step(args.warmup + i, kev[i])
+            step(kev[i])
         t_end.record(stream)
         torch.cuda.synchronize()
     _barrier(pg)
-    ms_total = t_start.elapsed_time(t_end)
-    ms_total = _max_over_ranks(pg, ms_total)
+    check_status(kda, ws, "headline prefill")
+    ms_total = _max_over_ranks(pg, t_start.elapsed_time(t_end))
     kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
     ms_per_step = ms_total / args.steps
     value = world * B * T / (ms_per_step / 1e3)
-    achieved_gbs = byts / (kernel_ms / 1e3) / 1e9
-    achieved_tf = flops / (kernel_ms / 1e3) / 1e12
-    if args.only == "softplus":
-        sp = measure_softplus(sets, ws, o, S, cu_host, args, stream)
-        if rank == 0:
-            print(json.dumps(dict(sp, only="softplus",
-                                  tokens_per_s=B * T / (sp["kernel_ms"] / 1e3))), flush=True)
-        return
-    if args.only == "backward":
-        bw = measure_backward(sets, B, H, T, d, args, stream)
-        if rank == 0:
-            print(json.dumps(dict(bw, only="backward",
-                                  frac=bw["achieved_gbs"] / peaks["hbm_gbs"])), flush=True)
-        return
-    if args.only == "conv":
-        conv = measure_conv(sets, ws, o, S, cu_host, B, H, T, d, args, stream)
-        if rank == 0:
-            print(json.dumps(dict(conv, only="conv",
-                                  frac=conv["achieved_gbs"] / peaks["hbm_gbs"])), flush=True)
-        return
     if args.only == "prefill":
         if rank == 0:
-            print(json.dumps({"only": "prefill", "value": value, "unit": "tokens/s",
-                              "kernel_ms": kernel_ms, "achieved_gbs": achieved_gbs,
-                              "tensor_tflops": achieved_tf}), flush=True)
+            r = roofline(byts, flops, kernel_ms, peaks, kernel=kernel_name)
+            print(json.dumps({"only": "prefill", "H": H, "T": T, "value": value,
+                              "unit": "tokens/s", "kernel_ms": kernel_ms,
+                              "achieved_gbs": r["achieved"], "frac": r["frac"],
+                              "tensor_tflops": r["tensor_tflops"], "clocks": clk.summary()}),
+                  flush=True)
         return
+    head = {"value": value, "ms_per_step": ms_per_step, "kernel_ms": kernel_ms,
+            "kernel": kernel_name, "byts": byts, "flops": flops, "clk": clk,
+            "launches_per_step": launches_per_step}
+    headline = (x, o, S, ws, cu_host)
+
+    # ---- the 4K prefill and the further rows on it ----
+    four_k = measure_4k(args, dev, stream, peaks, rank)
+    # ---- the varlen workload ----
+    varlen = measure_varlen(args, dev, stream, peaks)
+    return finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, head, headline,
+                  four_k, varlen, pg)
+
+
+def four_k_sets(dev, rank):
+    """Rotating copies of the 4K workload's inputs (host recipe), enough that
+    each step's inputs are not L2-resident."""
+    import torch
+    from kimi_delta_attention_12_gb300 import inputs
+    P = PREFILL_4K_SHAPE
+    x_host = inputs.make_prefill_inputs([P["T"]] * P["B"], P["H"], P["d"], P["d"],
+                                        torch.bfloat16, seed=rank)
+    set_bytes, _ = prefill_algorithmic(P["B"], P["H"], P["T"], P["d"])
+    nsets = max(2, -(-3 * L2_BYTES // set_bytes))
+    sets = [x_host.to(dev)]
+    for _ in range(nsets - 1):
+        s0 = sets[0]
+        sets.append(inputs.PrefillInputs(*(t.clone() if t is not None else None for t in
+                                           (s0.q, s0.k, s0.v, s0.z, s0.beta, s0.A,
+                                            s0.initial_state, s0.cu_seqlens))))
+    return x_host, sets
+
+
+def four_k_only(args, rank, dev, stream, peaks):
+    """--only softplus|backward|conv|prefill4k: one further row (or the 4K
+    prefill alone) for profiler captures."""
+    import torch
+    import kimi_delta_attention_12_gb300 as kda
+    P = PREFILL_4K_SHAPE
+    B, H, T, d = P["B"], P["H"], P["T"], P["d"]
+    x_host, sets = four_k_sets(dev, rank)
+    cu_host = sets[0].cu_seqlens.cpu()
+    o = torch.empty(B * T, H, d, dtype=torch.bfloat16, device=dev)
+    S = torch.empty(B, H, d, d, dtype=torch.float32, device=dev)
+    ws = kda.alloc_workspace(B, B * T, H, d, d, torch.bfloat16, dev)
+    if args.only == "softplus":
+        r = measure_softplus(sets, ws, o, S, cu_host, args, stream)
+        r["tokens_per_s"] = B * T / (r["kernel_ms"] / 1e3)
+    elif args.only == "backward":
+        r = measure_backward(sets, B, H, T, d, args, stream)
+        r["frac"] = r["achieved_gbs"] / peaks["hbm_gbs"]
+    elif args.only == "conv":
+        r = measure_conv(sets, ws, o, S, cu_host, B, H, T, d, args, stream)
+        r["frac"] = r["achieved_gbs"] / peaks["hbm_gbs"]
+    else:
+        ms = time_prefill(kda, sets, ws, o, S, cu_host, args.steps, args.warmup, stream,
+                          "4K prefill")
+        byts, flops = prefill_algorithmic(B, H, T, d)
+        r = {"kernel_ms": ms, "tokens_per_s": B * T / (ms / 1e3),
+             "roofline": roofline(byts, flops, ms, peaks)}
+    if rank == 0:
+        print(json.dumps(dict(r, only=args.only)), flush=True)
+
+
+def measure_4k(args, dev, stream, peaks, rank):
+    """The 4K prefill (B=1, H=32, T=4096) with its roofline, and the further
+    rows measured on it: checkpoints, softplus gate, short convolutions,
+    backward."""
+    import torch
+    import kimi_delta_attention_12_gb300 as kda
+    P = PREFILL_4K_SHAPE
+    B, H, T, d = P["B"], P["H"], P["T"], P["d"]
+    x_host, sets = four_k_sets(dev, rank)
+    cu_host = sets[0].cu_seqlens.cpu()
+    o = torch.empty(B * T, H, d, dtype=torch.bfloat16, device=dev)
+    S = torch.empty(B, H, d, d, dtype=torch.float32, device=dev)
+    ws = kda.alloc_workspace(B, B * T, H, d, d, torch.bfloat16, dev)
+    ms = time_prefill(kda, sets, ws, o, S, cu_host, args.steps, args.warmup, stream, "4K prefill")
+    byts, flops = prefill_algorithmic(B, H, T, d)
+    prefill_4k = {"workload": "prefill B=1 H=32 T=4096 d_k=d_v=128 bf16", "kernel_ms": ms,
+                  "tokens_per_s": B * T / (ms / 1e3),
+                  "roofline": roofline(byts, flops, ms, peaks,
+                                       profiled_traffic("kda_split_kernel_b1_h32_t4096",
+                                                        B * T * H),
+                                       "kda_split_kernel")}
     ckpt = measure_checkpointed(sets, ws, o, S, cu_host, B, H, T, d, args, stream)
+    ckpt["kernel_ms_plain"] = ms
     softplus = measure_softplus(sets, ws, o, S, cu_host, args, stream)
     softplus["tokens_per_s"] = B * T / (softplus["kernel_ms"] / 1e3)
-    extras = {"prefill_checkpointed": dict(ckpt, kernel_ms_plain=kernel_ms),
-              "softplus_gate": softplus,
-              "short_conv": measure_conv(sets, ws, o, S, cu_host, B, H, T, d, args, stream),
-              "backward": measure_backward(sets, B, H, T, d, args, stream)}
+    conv = measure_conv(sets, ws, o, S, cu_host, B, H, T, d, args, stream)
+    conv["frac"] = conv["achieved_gbs"] / peaks["hbm_gbs"]
+    bw = measure_backward(sets, B, H, T, d, args, stream)
+    bw["frac"] = bw["achieved_gbs"] / peaks["hbm_gbs"]
+    return {"prefill_4k": prefill_4k, "prefill_checkpointed": ckpt, "softplus_gate": softplus,
+            "short_conv": conv, "backward": bw}
 
-    return finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops, nsets,
-                  set_bytes, x_host, o, S, ws, cu_host, value, ms_per_step, kernel_ms,
-                  achieved_gbs, achieved_tf, clk, launches_per_step, kernel_name, pg, extras)
+
+def measure_varlen(args, dev, stream, peaks):
+    """The varlen workload: 16 packed sequences with lengths U[512, 16384]
+    (seed 0), H=64, nonzero initial states: kernel time, tokens/s, roofline."""
+    import torch
+    import kimi_delta_attention_12_gb300 as kda
+    from kimi_delta_attention_12_gb300 import inputs
+    w = inputs.VARLEN_16
+    H, d, N, T = w.H, w.d_k, w.N, w.total_T
+    x = device_prefill_inputs(list(w.seq_lens), H, d, seed=200, dev=dev, nonzero_state=True)
+    cu_host = x.cu_seqlens.cpu()
+    o = torch.empty(T, H, d, dtype=torch.bfloat16, device=dev)
+    S = torch.empty(N, H, d, d, dtype=torch.float32, device=dev)
+    ws = kda.alloc_workspace(N, T, H, d, d, torch.bfloat16, dev)
+    ms = time_prefill(kda, [x], ws, o, S, cu_host, args.steps, args.warmup, stream,
+                      "varlen prefill")
+    byts, flops = prefill_algorithmic(1, H, T, d, read_state=True, N=N)
+    return {"workload": f"varlen prefill, {N} sequences U[512,16384] (total {T} tokens), "
+                        f"H={H} d_k=d_v={d} bf16, initial states N(0,0.02)",
+            "seq_lens": list(w.seq_lens), "kernel_ms": ms, "tokens_per_s": T / (ms / 1e3),
+            "roofline": roofline(byts, flops, ms, peaks, kernel="kda_split_kernel")}
 
 
 def measure_checkpointed(sets, ws, o, S, cu_host, B, H, T, d, args, stream, interval=1024):
@@ -469,6 +653,7 @@ def measure_checkpointed(sets, ws, o, S, cu_host, B, H, T, d, args, stream, inte
         if i >= args.warmup:
             ev[i - args.warmup][1].record(stream)
     torch.cuda.synchronize()
+    check_status(kda, ws, "checkpointed prefill")
     ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     return {"interval": interval, "checkpoints": count,
             "checkpoint_bytes": count * H * d * d * 4, "kernel_ms": ms}
@@ -508,6 +693,7 @@ def measure_backward(sets, B, H, T, d, args, stream):
         if i >= 1:
             ev[i - 1][1].record(stream)
     torch.cuda.synchronize()
+    check_status(kda, ws, "backward (its checkpointed forward prefill)")
     ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     byts = backward_algorithmic(B, H, T, d)
     return {"kernel": "kda_backward_kernel", "form": "recurrent, fp32", "kernel_ms": ms,
@@ -544,6 +730,7 @@ def measure_conv(sets, ws, o, S, cu_host, B, H, T, d, args, stream):
         if e:
             e[2].record(stream)
     torch.cuda.synchronize()
+    check_status(kda, ws, "prefill after the short convolutions")
     conv_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     both_ms = statistics.mean(e[0].elapsed_time(e[2]) for e in ev)
     byts = conv_algorithmic(B, H, T, d, W)
@@ -571,6 +758,7 @@ def measure_softplus(sets, ws, o, S, cu_host, args, stream):
         if i >= args.warmup:
             ev[i - args.warmup][1].record(stream)
     torch.cuda.synchronize()
+    check_status(kda, ws, "softplus-gate prefill")
     return {"kernel": "kda_recurrent_kernel",
             "kernel_ms": statistics.mean(a.elapsed_time(b) for a, b in ev), "steps": n}
 
@@ -639,25 +827,24 @@ def decode_only(args, rank, local, dev, stream, peaks):
                           "frac": dec_gbs / peaks["hbm_gbs"], "clocks": clk}), flush=True)
 
 
-def finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops, nsets,
-           set_bytes, x_host, o, S, ws, cu_host, value, ms_per_step, kernel_ms, achieved_gbs,
-           achieved_tf, clk, launches_per_step, kernel_name, pg, extras):
+def finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, head, headline,
+           four_k, varlen, pg):
     import torch
     import kimi_delta_attention_12_gb300 as kda
+    x, o, S, ws, cu_host = headline
     # ---- end to end through the public API with host buffers ----
     # Every step copies its inputs from pinned host memory, runs kda_prefill
     # and reads o and the final state back into pinned host memory.  Steps are
     # pipelined the way a stream of requests would be: copy-in, prefill and
     # copy-out run on three streams with two device buffer sets, so that the
     # copy-in of step i + 1 overlaps the prefill of step i and the copy-out of
-    # step i - 1 (host-to-device copies run at ~210 GB/s and bound the step).
-    pin = lambda t: t.pin_memory()
-    hq, hk, hv, hz, hb = (pin(t) for t in (x_host.q, x_host.k, x_host.v, x_host.z, x_host.beta))
-    hA, hcu = pin(x_host.A), pin(x_host.cu_seqlens)
+    # step i - 1 (host-to-device copies bound the step).
+    pin = lambda t: t.cpu().pin_memory()
+    hosts = tuple(pin(t) for t in (x.q, x.k, x.v, x.z, x.beta, x.A, x.cu_seqlens))
     ho = torch.empty(B * T, H, d, dtype=torch.bfloat16).pin_memory()
     hS = torch.empty(B, H, d, d, dtype=torch.float32).pin_memory()
-    hosts = (hq, hk, hv, hz, hb, hA, hcu)
-    dbufs = [tuple(torch.empty_like(t, device=dev) for t in hosts) for _ in range(2)]
+    dbufs = [tuple(t for t in (x.q, x.k, x.v, x.z, x.beta, x.A, x.cu_seqlens)),
+             tuple(torch.empty_like(t, device=dev) for t in hosts)]
     douts = [(o, S), (torch.empty_like(o), torch.empty_like(S))]
     h2d = sum(t.numel() * t.element_size() for t in hosts)
     d2h = ho.numel() * ho.element_size() + hS.numel() * hS.element_size()
@@ -665,6 +852,8 @@ def finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_cmp = [torch.cuda.Event() for _ in range(2)]
     ev_out = [torch.cuda.Event() for _ in range(2)]
+    ws2 = torch.empty_like(ws)   # one workspace per buffer set (their prefills may overlap)
+    wss = (ws, ws2)
 
     def e2e_step(i):
         b = i % 2
@@ -678,7 +867,7 @@ def finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops
         s_cmp.wait_event(ev_in[b])
         s_cmp.wait_event(ev_out[b])     # and its last outputs have been read out
         kda.kda_prefill(dq, dk_, dv_, dz, db, dA, None, dcu, cu_seqlens_host=cu_host,
-                        o=ob, final_state=Sb, workspace=ws, stream=s_cmp)
+                        o=ob, final_state=Sb, workspace=wss[b], stream=s_cmp)
         ev_cmp[b].record(s_cmp)
         s_out.wait_event(ev_cmp[b])
         with torch.cuda.stream(s_out):
@@ -700,47 +889,47 @@ def finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops
     e1.record(s_out)
     torch.cuda.synchronize()
     _barrier(pg)
+    for w_ in wss:
+        check_status(kda, w_, "end-to-end prefill")
     e2e_ms = _max_over_ranks(pg, e0.elapsed_time(e1)) / args.steps
     e2e_value = world * B * T / (e2e_ms / 1e3)
+    del dbufs, douts, ws2
 
     # ---- decode workload: 64 consecutive steps on a resident 1.6 GB state ----
     D = DECODE_SHAPE
     dec_ms, dec_bytes, dec_gbs, dclk_summary = run_decode(dev, rank, local, stream)
     sp_ms, _, sp_gbs, _ = run_decode(dev, rank, local, stream, softplus_gate=True)
-    extras["softplus_gate"].update({"decode_ms_per_step": sp_ms, "decode_gbs": sp_gbs,
+    four_k["softplus_gate"].update({"decode_ms_per_step": sp_ms, "decode_gbs": sp_gbs,
                                     "decode_frac": sp_gbs / peaks["hbm_gbs"]})
     cv_ms, cv_bytes, cv_gbs, _ = run_decode(dev, rank, local, stream, conv=True)
-    conv = extras["short_conv"]
-    conv["frac"] = conv["achieved_gbs"] / peaks["hbm_gbs"]
-    extras["backward"]["frac"] = extras["backward"]["achieved_gbs"] / peaks["hbm_gbs"]
-    conv.update({"decode_kernels": "short_conv_decode_kernel + kda_recurrent_kernel",
-                 "decode_ms_per_step": cv_ms, "decode_bytes_per_step": cv_bytes,
-                 "decode_gbs": cv_gbs, "decode_frac": cv_gbs / peaks["hbm_gbs"]})
+    four_k["short_conv"].update({"decode_kernels": "short_conv_decode_kernel + kda_recurrent_kernel",
+                                 "decode_ms_per_step": cv_ms, "decode_bytes_per_step": cv_bytes,
+                                 "decode_gbs": cv_gbs, "decode_frac": cv_gbs / peaks["hbm_gbs"]})
 
     if rank != 0:
         return
-    # CPU baseline: the oracle on the same workload
-    cpu_tps, cpu_threads, cpu_sample = cpu_baseline(H, T, d)
-    row_cpu = row_cpu_baselines(H, T, d, D["B"], D["H"])
+    # CPU baselines: the oracle on a sample of the headline workload, on the
+    # whole 4K workload, and on each further row's workload
+    cpu_tps, cpu_threads, cpu_sample = headline_cpu_baseline(H, T, d)
+    P4 = PREFILL_4K_SHAPE
+    c4_tps, c4_threads, c4_sample = cpu_baseline(P4["H"], P4["T"], P4["d"], cpu_seconds=4.0)
+    four_k["prefill_4k"]["cpu_baseline"] = {"value": c4_tps, "unit": "tokens/s",
+                                            "cores": c4_threads, "kind": "oracle",
+                                            "sample": c4_sample}
+    row_cpu = row_cpu_baselines(P4["H"], P4["T"], P4["d"], D["B"], D["H"])
     for key in ("softplus_gate", "short_conv", "backward"):
-        if key in extras:
-            extras[key]["cpu_baseline"] = row_cpu[key]
-    traffic = profiled_traffic(kernel_name)
+        four_k[key]["cpu_baseline"] = row_cpu[key]
+    byts, flops, kernel_ms = head["byts"], head["flops"], head["kernel_ms"]
+    traffic = profiled_traffic("kda_split_kernel_b1_h96_t4096", B * T * H)
+    rl = roofline(byts, flops, kernel_ms, peaks, traffic, head["kernel"])
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded generators; inputs rotated over "
-                f"{nsets} sets of {set_bytes / 1e6:.0f} MB > L2)",
-        "config": {"workload": "prefill B=1 H=32 T=4096 d_k=d_v=128 bf16 + decode handoff",
-                   "B": B, "H": H, "T": T, "d": d, "chunk": 64,
-                   "l2": "inputs larger than L2 (rotating sets)", "parallelism": "replicas"},
-        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"],
-                     "traffic": traffic, "kernel": kernel_name, "kernel_ms": kernel_ms,
-                     "algorithmic_bytes": byts, "peak_source": peaks["source"],
-                     "tensor_tflops": achieved_tf,
-                     "tensor_frac": achieved_tf / peaks["bf16_tflops"]},
+        "data": "synthetic (seeded generators; the long-prefill inputs, 6.4 GB > L2, drawn on "
+                "the device with the recipe's distributions)",
+        "config": headline_config(),
+        "roofline": rl,
         "decode": {"metric": "decode state GB/s", "value": dec_gbs, "unit": "GB/s",
                    "ms_per_step": dec_ms, "bytes_per_step": dec_bytes,
                    "config": {"workload": "decode B=256 H=96 d=128 fp32 state, bf16 inputs",
@@ -748,15 +937,16 @@ def finish(args, world, rank, local, dev, stream, peaks, B, H, T, d, byts, flops
                    "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm_gbs"],
                                 "unit": "GB/s", "frac": dec_gbs / peaks["hbm_gbs"]},
                    "clocks": dclk_summary, "cpu_baseline": row_cpu["decode"]},
-        **extras,
+        "prefill_varlen": varlen,
+        **four_k,
         "cpu_baseline": {"value": cpu_tps, "unit": "tokens/s", "cores": cpu_threads,
                          "kind": "oracle", "sample": cpu_sample, "cpu_model": cpu_model()},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "pipelining": "copy-in, prefill and copy-out of consecutive steps overlap "
                               "(three streams, two device buffer sets)"},
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk.summary(),
+        "gpu_launches": head["launches_per_step"] * args.steps,
+        "clocks": head["clk"].summary(),
     }
     print(json.dumps(line), flush=True)
 
@@ -767,9 +957,15 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["kda", "reference"], default="kda")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "conv", "backward", "softplus"],
+    ap.add_argument("--only", choices=["all", "prefill", "prefill4k", "decode", "conv",
+                                       "backward", "softplus"],
                     default="all",
                     help="run one part only (for profiler captures); the default runs all")
+    ap.add_argument("--prefill-heads", type=int, default=0,
+                    help="--only prefill: heads of the long prefill (default 96; smaller "
+                         "cases for profiler captures)")
+    ap.add_argument("--prefill-tokens", type=int, default=0,
+                    help="--only prefill: tokens of the long prefill (default 65536)")
     ap.add_argument("--decode-batch", type=int, default=DECODE_SHAPE["B"],
                     help="decode batch for --only decode (smaller cases for profiler captures)")
     ap.add_argument("--decode-conv", action="store_true",

@@ -30,8 +30,15 @@
  *     the host, launches, and returns; host-detectable errors return a
  *     negative status and launch nothing.  A CUDA launch failure returns
  *     KDA_ERR_CUDA.  No exception or abort crosses this boundary.
- *   - Calls are re-entrant; the library keeps no mutable global state apart
- *     from lazily resolved driver entry points.
+ *   - Calls are re-entrant.  The library's only mutable global state is
+ *     lazily resolved driver entry points and, for kda_prefill_noalloc, its
+ *     fixed device array and the per-device cache of that array's address
+ *     (see there).
+ *   - A device cu_seqlens array is trusted only as far as the token range:
+ *     kernels clamp every entry to [0, total_T] and end each sequence no
+ *     earlier than it starts, so a malformed array (without the host mirror
+ *     that would have caught it) gives meaningless results but never reads
+ *     or writes outside the caller's buffers.
  *   - Input buffers must not alias output buffers unless stated.
  */
 #ifndef KDA_H_
@@ -74,8 +81,14 @@ enum {
                                    so the 16-token reciprocal tiles of the chunked
                                    kernels do not apply: prefill runs the fused
                                    recurrent kernel (fp32), decode is unchanged. */
-    KDA_FLAG_CONV_SILU = 8      /* kda_short_conv, kda_decode_step_conv: SiLU,
+    KDA_FLAG_CONV_SILU = 8,     /* kda_short_conv, kda_decode_step_conv: SiLU,
                                    y * sigmoid(y), after each short convolution */
+    KDA_FLAG_SHORT_PEER_WAITS = 16 /* kda_prefill, test aid: the split kernel's
+                                   waits on other CTAs give up after one poll,
+                                   so that its bounded-wait exit runs; the call
+                                   then reports KDA_ERR_TIMEOUT through
+                                   kda_workspace_status and its outputs are
+                                   invalid.  No effect on other kernels. */
 };
 #define KDA_DEFAULT_FLAGS KDA_FLAG_L2NORM_QK
 
@@ -85,16 +98,17 @@ enum {
  *
  * Any workspace of at least 256 + 4 * N * H bytes (rounded up to 256) is
  * accepted.  With bf16 and d_k = d_v = 128 (up to 1024 sequences and 256
- * heads), a larger workspace -- the size returned here, about 0.8 MB per
- * consumer CTA (a quarter of the SMs at most, ~30 MB on 152 SMs) whatever the
- * sequence lengths -- selects the split kernel, which spreads each
- * (sequence, head) pair's chunks over all SMs and passes every chunk's
- * operand tiles through a ring of slots in the workspace; a smaller one
- * selects the single-pass kernel.  The split kernel expects one CTA on every
- * SM at once: with other work on the GPU its waits may run out and the call
- * then reports KDA_ERR_TIMEOUT through kda_workspace_status.  The workspace
- * is scratch: its content on entry does not matter and it may be reused by
- * the next call on the same stream.
+ * heads), a larger workspace -- the size returned here, a ring of 16 slots of
+ * 66,048 bytes (about 1.06 MB) per consumer CTA, at most a quarter of the SMs
+ * (about 40 MB on 152 SMs) whatever the sequence lengths -- selects the split
+ * kernel, which spreads each (sequence, head) pair's chunks over all SMs and
+ * passes every chunk's operand tiles through the ring; a smaller one selects
+ * the single-pass kernel.  The split kernel needs one CTA on every SM at once
+ * and is launched cooperatively, which guarantees that; where the device
+ * cannot take it (another context holds SMs, a partitioned GPU) the call runs
+ * the single-pass kernel instead, with the same results.  The workspace is
+ * scratch: its content on entry does not matter and it may be reused by the
+ * next call on the same stream.
  */
 KDA_API size_t kda_prefill_workspace_bytes(int32_t N, int32_t total_T, int32_t H,
                                    int32_t d_k, int32_t d_v, kda_dtype dt);
@@ -114,7 +128,8 @@ KDA_API size_t kda_prefill_workspace_bytes(int32_t N, int32_t total_T, int32_t H
  *                 validated (starts at 0, non-decreasing, ends at total_T)
  *                 and used to schedule long sequences first.
  *  scale          multiplies q_hat (1.0 = none)
- *  flags          KDA_FLAG_L2NORM_QK, KDA_FLAG_RECURRENT, KDA_FLAG_SOFTPLUS_GATE (or 0)
+ *  flags          KDA_FLAG_L2NORM_QK, KDA_FLAG_RECURRENT, KDA_FLAG_SOFTPLUS_GATE,
+ *                 KDA_FLAG_SHORT_PEER_WAITS (or 0)
  *  o              [total_T, H, d_v]  dt, output (o_t for every token)
  *  final_state    [N, H, d_k, d_v] fp32, or NULL.  May alias initial_state
  *                 (in-place update is allowed).
@@ -153,7 +168,12 @@ KDA_API int kda_prefill(const void* q, const void* k, const void* v, const void*
  *                  checkpoints of sequence n follow those of sequences
  *                  0 .. n-1 (see kda_checkpoint_count); checkpoint m of
  *                  sequence n has index (checkpoints before n) + m - 1.  Rows
- *                  outside [0, ckpt_pool_size) are skipped.
+ *                  outside [0, ckpt_pool_size) are skipped.  Checkpoints are
+ *                  written (and ckpt_slots read) only below the count the host
+ *                  can vouch for: kda_checkpoint_count of cu_seqlens_host, or
+ *                  of the equal split without cu_seqlens, or -- with a device
+ *                  cu_seqlens and no host mirror -- floor(total_T /
+ *                  ckpt_interval), the largest count a valid array can give.
  *  ckpt_pool_size  rows in the pool (>= 1)
  * Every other argument and result is that of kda_prefill; ckpt_interval == 0
  * (with a NULL pool) is exactly kda_prefill.  Errors: KDA_ERR_INVALID_ARG for
@@ -341,8 +361,10 @@ KDA_API size_t kda_backward_workspace_bytes(int32_t N, int32_t total_T, int32_t 
  *                     pointers, cudaMemcpyDefault).  slots must be NULL.
  *  KDA_STATE_GATHER   dst[i] = src[slots[i]]   (pool -> batch), i < n
  *  KDA_STATE_SCATTER  dst[slots[i]] = src[i]   (batch -> pool), i < n
- * Out-of-range slots skip their state.  For GATHER/SCATTER/ZERO the
- * pointers are device pointers.
+ * A slot outside [0, pool_size) skips its state, except in GATHER, which
+ * fills dst[i] with NaN for it (as kda_decode_step writes NaN to the o row of
+ * such a slot), so that a bad slot cannot hand a stale state to decode
+ * unnoticed.  For GATHER/SCATTER/ZERO the pointers are device pointers.
  */
 typedef enum {
     KDA_STATE_ZERO = 0,
@@ -370,12 +392,13 @@ KDA_API int kda_state_io(kda_state_op op, float* dst, const float* src,
  * Arguments, layouts and results are those of kda_prefill, which it calls
  * with the array as its workspace (so bf16 d=128 runs the single-pass
  * kernel).  More than 16384 (sequence, head) pairs return KDA_ERR_WORKSPACE
- * without launching.  The first call on a device
- * looks up the array's device address (cudaGetSymbolAddress, with that
- * device current), so make that first call before any stream capture.
+ * without launching.  The first call in a device's CUDA context looks up the
+ * array's device address (cudaGetSymbolAddress, with that device current)
+ * and caches it with the context's unique id, so make that first call -- and
+ * the first call after a cudaDeviceReset -- before any stream capture.
  * Every call shares the one array: calls that overlap on the GPU (other
  * streams, other threads) race on it.  The status word in the array is
- * cleared by each call.
+ * cleared by each call; read it with kda_prefill_noalloc_status.
  */
 KDA_API int kda_prefill_noalloc(const void* q, const void* k, const void* v, const void* z,
                                 const void* beta, const float* A, const float* initial_state,
@@ -383,6 +406,16 @@ KDA_API int kda_prefill_noalloc(const void* q, const void* k, const void* v, con
                                 int32_t N, int32_t total_T, int32_t H, int32_t d_k, int32_t d_v,
                                 kda_dtype dt, float scale, uint32_t flags,
                                 void* o, float* final_state, void* stream);
+
+/*
+ * kda_prefill_noalloc_status -- wait for `stream`, then read the status word
+ * the last kda_prefill_noalloc call on the current device left in the fixed
+ * array: KDA_OK, KDA_ERR_TIMEOUT (a bounded wait inside the kernel ran out;
+ * that call's outputs are invalid) or KDA_ERR_CUDA.  The counterpart of
+ * kda_workspace_status for callers that never see a workspace pointer.
+ * Synchronising; allocates nothing.  No counterpart on the pages.
+ */
+KDA_API int kda_prefill_noalloc_status(void* stream);
 
 /* Human-readable name of a kda_status value (static storage). */
 KDA_API const char* kda_status_string(int status);

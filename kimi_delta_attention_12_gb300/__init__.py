@@ -37,6 +37,7 @@ KDA_FLAG_L2NORM_QK = 1
 KDA_FLAG_RECURRENT = 2
 KDA_FLAG_SOFTPLUS_GATE = 4
 KDA_FLAG_CONV_SILU = 8
+KDA_FLAG_SHORT_PEER_WAITS = 16
 
 KDA_STATE_ZERO = 0
 KDA_STATE_COPY = 1
@@ -49,7 +50,7 @@ EXPORTED_SYMBOLS = (
     "kda_decode_step", "kda_state_io", "kda_status_string", "kda_version",
     "kda_prefill_noalloc", "kda_prefill_checkpointed", "kda_checkpoint_count",
     "kda_short_conv", "kda_decode_step_conv", "kda_decode_conv_workspace_bytes",
-    "kda_backward", "kda_backward_workspace_bytes",
+    "kda_backward", "kda_backward_workspace_bytes", "kda_prefill_noalloc_status",
 )
 
 _lock = threading.Lock()
@@ -95,6 +96,8 @@ def lib() -> ctypes.CDLL:
             L.kda_prefill_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                               i32, i32, i32, i32, i32, ctypes.c_int, f32, u32,
                                               vp, vp, vp]
+            L.kda_prefill_noalloc_status.restype = ctypes.c_int
+            L.kda_prefill_noalloc_status.argtypes = [vp]
             L.kda_prefill_checkpointed.restype = ctypes.c_int
             L.kda_prefill_checkpointed.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                                    i32, i32, i32, i32, i32, ctypes.c_int, f32,
@@ -190,7 +193,7 @@ def kda_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: torch.Tens
                 workspace: Optional[torch.Tensor] = None,
                 ckpt_interval: int = 0, ckpt_pool: Optional[torch.Tensor] = None,
                 ckpt_slots: Optional[torch.Tensor] = None,
-                stream: Optional[torch.cuda.Stream] = None
+                stream: Optional[torch.cuda.Stream] = None, extra_flags: int = 0
                 ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """Chunked KDA prefill.  Packed layout: q, k, z [total_T, H, d_k], v
     [total_T, H, d_v], beta [total_T, H]; a 4-D [B, T, H, d] batch is accepted
@@ -202,7 +205,8 @@ def kda_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: torch.Tens
     checkpoint i (kda_prefill_checkpointed in include/kda.h).
 
     softplus_gate=True selects Kimi Linear's unbounded gate -softplus(e^A z)
-    (KDA_FLAG_SOFTPLUS_GATE; runs the fused recurrent kernel)."""
+    (KDA_FLAG_SOFTPLUS_GATE; runs the fused recurrent kernel).  extra_flags
+    are OR-ed into the call's flags (e.g. KDA_FLAG_SHORT_PEER_WAITS)."""
     batched = q.dim() == 4
     if batched:
         B, T = q.shape[:2]
@@ -237,7 +241,7 @@ def kda_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: torch.Tens
     if cu_seqlens_host is not None:
         host_cu = cu_seqlens_host.to(torch.int32).contiguous()
     flags = ((KDA_FLAG_L2NORM_QK if l2norm else 0) | (KDA_FLAG_RECURRENT if recurrent else 0)
-             | (KDA_FLAG_SOFTPLUS_GATE if softplus_gate else 0))
+             | (KDA_FLAG_SOFTPLUS_GATE if softplus_gate else 0) | int(extra_flags))
     host_ptr = None if host_cu is None else ctypes.c_void_p(host_cu.data_ptr())
     if ckpt_interval:
         _check_cuda(ckpt_pool, ckpt_slots)
@@ -249,7 +253,10 @@ def kda_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: torch.Tens
                 raise TypeError("ckpt_slots must be a 1-D int32 tensor")
             cu_h = host_cu if host_cu is not None else (
                 None if cu_seqlens is None else cu_seqlens.to("cpu", torch.int32))
-            need = checkpoint_count(cu_h, N, total_T, int(ckpt_interval))
+            try:
+                need = checkpoint_count(cu_h, N, total_T, int(ckpt_interval))
+            except KDAError:   # a malformed cu_seqlens: the library bounds the reads itself
+                need = -1
             if need >= 0 and ckpt_slots.numel() < need:
                 raise ValueError(f"ckpt_slots has {ckpt_slots.numel()} entries for {need} "
                                  "checkpoints")
@@ -287,6 +294,11 @@ def checkpoint_count(cu_seqlens_host: Optional[torch.Tensor], N: int, total_T: i
 
 def workspace_status(workspace: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> int:
     return int(lib().kda_workspace_status(_ptr(workspace), _stream_ptr(stream)))
+
+
+def noalloc_status(stream: Optional[torch.cuda.Stream] = None) -> int:
+    """Status word of the last kda_prefill_noalloc call on the current device."""
+    return int(lib().kda_prefill_noalloc_status(_stream_ptr(stream)))
 
 
 def _expect_decode(q, k, v, z, beta, A, state, slots, o):

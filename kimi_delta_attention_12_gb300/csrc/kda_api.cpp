@@ -1,6 +1,6 @@
 // kda_api.cpp -- the C ABI declared in include/kda.h: argument validation,
 // kernel selection and launch on the caller's stream.  No allocation, no
-// exceptions across the boundary, no global mutable state.
+// exceptions across the boundary.
 #include "../../include/kda.h"
 
 #include <cuda_runtime.h>
@@ -20,7 +20,11 @@ inline bool supported_dim(int32_t d) { return d == 32 || d == 64 || d == 128; }
 
 inline size_t elem_bytes(kda_dtype dt) { return dt == KDA_F32 ? 4 : 2; }
 
-constexpr uint32_t kKnownFlags = KDA_FLAG_L2NORM_QK | KDA_FLAG_RECURRENT | KDA_FLAG_SOFTPLUS_GATE;
+constexpr uint32_t kKnownFlags = KDA_FLAG_L2NORM_QK | KDA_FLAG_RECURRENT |
+                                 KDA_FLAG_SOFTPLUS_GATE | KDA_FLAG_SHORT_PEER_WAITS;
+// polls of a split-kernel wait on another CTA before it gives up (~2^25, far
+// longer than any legitimate wait); one poll with KDA_FLAG_SHORT_PEER_WAITS
+constexpr uint32_t kPeerWaitPolls = 1u << 25;
 constexpr uint32_t kFlagRecurrent = KDA_FLAG_RECURRENT;
 constexpr int32_t kCheckpointGrain = 64;  // checkpoints fall on chunk boundaries
 
@@ -180,6 +184,18 @@ int kda_prefill_checkpointed(const void* q, const void* k, const void* v, const 
         return KDA_ERR_ALIGNMENT;
     }
 
+    // Checkpoints (and reads of ckpt_slots) stop at the count the host can
+    // vouch for: from the host mirror, from the equal split, or -- with only
+    // a device cu_seqlens -- floor(total_T / interval), which bounds the count
+    // of every valid array.
+    int64_t ckpt_count = 0;
+    if (ckpt_interval > 0) {
+        ckpt_count = (cu_seqlens_host || !cu_seqlens)
+                         ? kda_checkpoint_count(cu_seqlens_host, N, total_T, ckpt_interval)
+                         : (int64_t)total_T / ckpt_interval;
+        if (ckpt_count < 0) return KDA_ERR_INVALID_ARG;
+    }
+
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int32_t* ws = static_cast<int32_t*>(workspace);
     const bool use_chunked = kda::kChunkedPrefillBuilt && dt == KDA_BF16 && d_k == 128 && d_v == 128 &&
@@ -206,10 +222,16 @@ int kda_prefill_checkpointed(const void* q, const void* k, const void* v, const 
         p.l2norm = (flags & KDA_FLAG_L2NORM_QK) ? 1 : 0;
         p.ckpt_interval = ckpt_interval; p.ckpt_pool = ckpt_pool;
         p.ckpt_slots = ckpt_slots; p.ckpt_pool_size = ckpt_pool_size;
+        p.ckpt_count = ckpt_count;
+        p.peer_wait_polls = (flags & KDA_FLAG_SHORT_PEER_WAITS) ? 1u : kPeerWaitPolls;
+        err = cudaErrorCooperativeLaunchTooLarge;
         if (use_split) {
             kda::split_bind(plan, workspace, &p);
             err = kda::launch_split_prefill(p, sms, s);
-        } else {
+        }
+        // the split kernel needs every SM at once; where a cooperative launch
+        // cannot promise that, the single-pass kernel runs instead
+        if (err == cudaErrorCooperativeLaunchTooLarge) {
             err = kda::launch_chunked_prefill(p, s);
         }
     } else {
@@ -223,6 +245,7 @@ int kda_prefill_checkpointed(const void* q, const void* k, const void* v, const 
         p.softplus_gate = (flags & KDA_FLAG_SOFTPLUS_GATE) ? 1 : 0;
         p.ckpt_interval = ckpt_interval; p.ckpt_pool = ckpt_pool;
         p.ckpt_slots = ckpt_slots; p.ckpt_pool_size = ckpt_pool_size;
+        p.ckpt_count = ckpt_count;
         if (total_T == 0 && !final_state) {
             return KDA_OK;
         }
@@ -488,6 +511,7 @@ int kda_backward(const void* q, const void* k, const void* v, const void* z,
     p.dO = dO; p.dS_final = dS_final;
     p.dq = dq; p.dk = dk; p.dv = dv; p.dz = dz; p.dbeta = dbeta; p.dA = dA; p.dS0 = dS0;
     p.pool = pool;
+    p.pool_rows = pool_rows;
     p.scratch = reinterpret_cast<float*>(ws_o + wl.o + wl.pool);
     p.part = reinterpret_cast<float*>(ws_o + wl.o + wl.pool + wl.scratch);
     p.dA_tok = reinterpret_cast<float*>(ws_o + wl.o + wl.pool + wl.scratch + wl.part);

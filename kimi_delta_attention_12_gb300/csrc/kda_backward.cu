@@ -39,6 +39,7 @@
 
 #include "kda_internal.h"
 #include "kda_lanes.cuh"
+#include "kda_seqlens.cuh"
 
 namespace kda {
 namespace {
@@ -123,14 +124,7 @@ kda_backward_kernel(const BackwardParams p) {
     const T* dO = static_cast<const T*>(p.dO);
 
     int64_t bos, eos;
-    if (p.cu_seqlens) {
-        bos = p.cu_seqlens[n];
-        eos = p.cu_seqlens[n + 1];
-    } else {
-        const int64_t len = p.total_T / p.N;
-        bos = (int64_t)n * len;
-        eos = bos + len;
-    }
+    clamped_seq(p.cu_seqlens, n, p.N, p.total_T, bos, eos);
     const int64_t len = eos - bos;
     const int64_t nchunks = (len + C - 1) / C;
     const size_t SS = (size_t)DK * DV;
@@ -297,9 +291,7 @@ kda_backward_kernel(const BackwardParams p) {
     {
         int part = 0;
         for (int m = tid; m < n; m += kBwThreads) {
-            const int64_t lm = p.cu_seqlens ? (int64_t)(p.cu_seqlens[m + 1] - p.cu_seqlens[m])
-                                            : p.total_T / p.N;
-            part += (int)(lm / C);
+            part += (int)(clamped_len(p.cu_seqlens, m, p.N, p.total_T) / C);
         }
         if (part) {
             atomicAdd(&s_base, part);
@@ -329,8 +321,14 @@ kda_backward_kernel(const BackwardParams p) {
         // the chunk start (the initial state for chunk 0, else checkpoint c)
         __syncthreads();   // the previous chunk's partials and last token have been read
         prepare(bos + i0, (int)cl);
-        if (c > 0) {
+        if (c > 0 && ck_base + c - 1 < p.pool_rows) {
             load_state(p.pool + ((size_t)(ck_base + c - 1) * H + h) * SS);
+        } else if (c > 0) {
+            // only a malformed cu_seqlens gets here (more checkpoints than the pool holds)
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) {
+                S[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         } else if (p.initial_state) {
             load_state(p.initial_state + ((size_t)n * H + h) * SS);
         } else {

@@ -42,6 +42,9 @@ struct ChunkedParams {
     float* ckpt_pool;
     const int32_t* ckpt_slots;
     int32_t ckpt_pool_size;
+    int64_t ckpt_count;          // checkpoints with index >= this are skipped (ckpt_slots bound)
+    // polls of a wait on another CTA (split mode) before it gives up
+    uint32_t peer_wait_polls;
 };
 
 // Split mode: the N*H (sequence, head) units are cut into `batches` batches of

@@ -39,6 +39,7 @@ struct RecurrentParams {
     float* ckpt_pool;
     const int32_t* ckpt_slots;
     int32_t ckpt_pool_size;
+    int64_t ckpt_count;     // checkpoints with index >= this are skipped (ckpt_slots bound)
 };
 
 // Short convolutions of q, k and v (kda_short_conv.cu).  Conv weights and
@@ -107,7 +108,8 @@ struct BackwardParams {
     float* dbeta;                // [total_T, H]
     float* dA;                   // [H]
     float* dS0;                  // [N, H, d_k, d_v]
-    const float* pool;           // workspace
+    const float* pool;           // workspace: the chunk-start states
+    int64_t pool_rows;           // states in the pool (reads beyond it are skipped)
     float* scratch;
     float* part;
     float* dA_tok;               // [total_T, H]

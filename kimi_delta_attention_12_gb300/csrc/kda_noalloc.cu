@@ -11,10 +11,14 @@
 //
 // The array below is a file-scope __device__ variable: every GPU that loads
 // the library holds it until the process exits.  In host code its name is
-// only a host-side stand-in, so its device address is looked up once per
-// device (cudaGetSymbolAddress, with that device current) and cached.
+// only a host-side stand-in, so its device address is looked up per device
+// (cudaGetSymbolAddress, with that device current) and cached together with
+// the unique id of the CUDA context it belongs to; a call from a different
+// context (for example after cudaDeviceReset recreated the primary context)
+// looks it up again instead of using a stale address.
 #include "../../include/kda.h"
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "kda_internal.h"
@@ -30,24 +34,64 @@ __device__ __align__(256) unsigned char g_kda_noalloc_scratch[kNoAllocScratchByt
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
-void* g_scratch_addr[kMaxDevices];
+struct ScratchAddr {
+    unsigned long long ctx_id;  // unique id of the context the address belongs to
+    void* addr;
+};
+ScratchAddr g_scratch[kMaxDevices];
 
-// Device address of the scratch array on the current device (looked up on
-// the first call for that device).  Returns nullptr on failure.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+template <typename Fn>
+Fn driver_fn(const char* name) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+        return nullptr;
+    }
+    return reinterpret_cast<Fn>(f);
+}
+
+// Unique id of the calling thread's current CUDA context; false if there is
+// none (or the driver cannot say).
+bool current_ctx_id(unsigned long long* id) {
+    static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+    CUcontext ctx = nullptr;
+    return get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx &&
+           get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the scratch array in the current context (looked up on
+// the first call in that context).  Returns nullptr on failure.
 void* scratch_on_current_device() {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
         return nullptr;
     }
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_addr[dev]) {
-        void* addr = nullptr;
-        if (cudaGetSymbolAddress(&addr, g_kda_noalloc_scratch) != cudaSuccess || !addr) {
-            return nullptr;
-        }
-        g_scratch_addr[dev] = addr;
+    unsigned long long id = 0;
+    if (g_scratch[dev].addr && current_ctx_id(&id) && id == g_scratch[dev].ctx_id) {
+        return g_scratch[dev].addr;
     }
-    return g_scratch_addr[dev];
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_kda_noalloc_scratch) != cudaSuccess || !addr) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    // the lookup made the device's context current if it was not
+    if (!current_ctx_id(&id)) {
+        id = 0;   // no id: the address is looked up again on every call
+        g_scratch[dev].addr = nullptr;
+        return addr;
+    }
+    g_scratch[dev].ctx_id = id;
+    g_scratch[dev].addr = addr;
+    return addr;
 }
 
 }  // namespace
@@ -73,4 +117,12 @@ extern "C" KDA_API int kda_prefill_noalloc(const void* q, const void* k, const v
     return kda_prefill(q, k, v, z, beta, A, initial_state, cu_seqlens, cu_seqlens_host, N,
                        total_T, H, d_k, d_v, dt, scale, flags, o, final_state, scratch,
                        kNoAllocScratchBytes, stream);
+}
+
+extern "C" KDA_API int kda_prefill_noalloc_status(void* stream) {
+    void* scratch = scratch_on_current_device();
+    if (!scratch) {
+        return KDA_ERR_CUDA;
+    }
+    return kda_workspace_status(scratch, stream);
 }

@@ -51,6 +51,7 @@
 
 #include "kda_chunk_phases.cuh"
 #include "kda_chunked.h"
+#include "kda_seqlens.cuh"
 #include "sm103_ptx.cuh"
 
 namespace kda {
@@ -96,14 +97,7 @@ __device__ __forceinline__ Ctx make_ctx(uint8_t* sm, uint32_t tbase) {
 
 __device__ __forceinline__ void seq_bounds(const ChunkedParams& p, int n, int64_t& bos,
                                            int64_t& eos) {
-    if (p.cu_seqlens) {
-        bos = p.cu_seqlens[n];
-        eos = p.cu_seqlens[n + 1];
-    } else {
-        const int64_t len = p.total_T / p.N;
-        bos = (int64_t)n * len;
-        eos = bos + len;
-    }
+    clamped_seq(p.cu_seqlens, n, p.N, p.total_T, bos, eos);
 }
 
 // ====================================================================== single pass
@@ -115,6 +109,7 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
     __shared__ uint64_t bar_raw;   // raw q, k, z of a chunk landed
     __shared__ uint64_t bar_v;     // v of a chunk landed
     __shared__ uint64_t bar_mma;
+    __shared__ uint64_t bar_fin;   // every MMA of this CTA done
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_flag;
 
@@ -135,6 +130,7 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
         mbar_init(&bar_raw, 1);
         mbar_init(&bar_v, 1);
         mbar_init(&bar_mma, 1);
+        mbar_init(&bar_fin, 1);
         fence_mbar_init();
         prefetch_tmap(&args.tm_q);
         prefetch_tmap(&args.tm_k);
@@ -334,8 +330,8 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
         // state checkpoint after this chunk (S^T in TMEM is the state after it)
         if (p.ckpt_interval > 0) {
             const int64_t done = (int64_t)(ci + 1) * C;
-            if (done % p.ckpt_interval == 0 && done <= len) {
-                const int64_t idx = ck_base + done / p.ckpt_interval - 1;
+            const int64_t idx = ck_base + done / p.ckpt_interval - 1;
+            if (done % p.ckpt_interval == 0 && done <= len && idx < p.ckpt_count) {
                 const int64_t row = p.ckpt_slots ? (int64_t)p.ckpt_slots[idx] : idx;
                 if (row >= 0 && row < p.ckpt_pool_size) {
                     store_state(x, p.ckpt_pool + ((size_t)row * H + h) * D * D);
@@ -355,6 +351,13 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
     if (!abort_flag && p.final_state) {
         store_state(x, p.final_state + state_off);
     }
+    // a loop left early may still have MMAs running: none may be when the
+    // TMEM is freed
+    cta_sync_tc();
+    if (tid == 0) {
+        mma_commit(&bar_fin);
+        mbar_wait(&bar_fin, 0, nullptr);
+    }
     cta_sync_tc();
     if (x.warp == 0) {
         tmem_dealloc(x.tbase, TMEM_COLS);
@@ -372,11 +375,11 @@ __device__ __forceinline__ void st_release(int32_t* ptr, int32_t v) {
     asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
 }
 
-// Bounded wait (one thread) until *ptr >= target.  False on timeout or when
-// another thread of the CTA raised the abort flag.
+// Bounded wait (one thread) until *ptr >= target: at most `polls` polls.
+// False on timeout or when another thread of the CTA raised the abort flag.
 __device__ __forceinline__ bool wait_at_least(const int32_t* ptr, int32_t target,
-                                              const volatile int* abort_flag) {
-    for (uint32_t i = 0; i < (1u << 25); ++i) {
+                                              const volatile int* abort_flag, uint32_t polls) {
+    for (uint32_t i = 0; i < polls; ++i) {
         if (ld_acquire(ptr) >= target) {
             return true;
         }
@@ -411,6 +414,11 @@ struct SplitMeta {
     int32_t g0[kSplitMaxBatches + 1];    // first consumer-stream index of each batch
 };
 
+// Length of sequence n from the clamped starts (never negative).
+__device__ __forceinline__ int32_t split_len(const SplitMeta& m, int n) {
+    return max(0, m.cu[n + 1] - m.cu[n]);
+}
+
 // One producer task: chunk c of unit `unit` (the i-th unit of its batch).
 // Task t of batch b is chunk (t - task0[b]) / nu of unit (t - task0[b]) % nu
 // (chunk-major), nu the batch's units; in consumer i's stream of chunks it is
@@ -443,7 +451,7 @@ __device__ __forceinline__ bool decode_task(const SplitMeta& m, const ChunkedPar
     o.h = o.unit - n * p.H;
     o.c = c;
     const int32_t bos = m.cu[n];
-    const int32_t len = m.cu[n + 1] - bos;
+    const int32_t len = split_len(m, n);
     o.t0 = bos + c * C;
     o.L = min(C, len - c * C);
     o.g = m.g0[lo] + c;
@@ -497,8 +505,11 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
         tmem_relinquish();
     }
     // sequence starts and gate constants
+    // each entry clamped to [0, total_T]; a sequence's length is then
+    // max(0, cu[n + 1] - cu[n]) (split_len), so it stays inside the tokens
     for (int n = tid; n <= p.N; n += kThreads) {
-        meta.cu[n] = p.cu_seqlens ? p.cu_seqlens[n] : n * (p.total_T / p.N);
+        meta.cu[n] = p.cu_seqlens ? (int32_t)clamp_token(p.cu_seqlens[n], p.total_T)
+                                  : n * (p.total_T / p.N);
     }
     for (int h = tid; h < H; h += kThreads) {
         meta.eA[h] = exp2_approx(p.A[h] * kLog2e) * kLog2e;
@@ -510,7 +521,7 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
         const int u1 = min(U, u0 + p.n_cons);
         int maxc = 0;
         for (int n = u0 / H; n <= (u1 - 1) / H; ++n) {
-            maxc = max(maxc, (meta.cu[n + 1] - meta.cu[n] + C - 1) / C);
+            maxc = max(maxc, (split_len(meta, n) + C - 1) / C);
         }
         meta.task0[b + 1] = maxc * (u1 - u0);
         meta.g0[b + 1] = maxc;
@@ -582,7 +593,7 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
             const int n = unit / H;
             const int h = unit - n * H;
             const int32_t bos = meta.cu[n];
-            const int32_t len = meta.cu[n + 1] - bos;
+            const int32_t len = split_len(meta, n);
             const int nch = (len + C - 1) / C;
             const int32_t g0 = meta.g0[bt];
             const size_t state_off = (size_t)unit * D * D;
@@ -592,7 +603,7 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
             const int64_t ck_base =
                 p.ckpt_interval > 0
                     ? ckpt_base(n, p.ckpt_interval,
-                                [&](int m) { return (int)(meta.cu[m + 1] - meta.cu[m]); },
+                                [&](int m) { return (int)split_len(meta, m); },
                                 &s_ck)
                     : 0;
 
@@ -623,7 +634,7 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 const int32_t g = g0 + c;
                 const int32_t slot = i * p.ring + g % p.ring;
                 if (block) {
-                    if (!wait_at_least(p.flags + slot, g + 1, &abort_flag)) {
+                    if (!wait_at_least(p.flags + slot, g + 1, &abort_flag, p.peer_wait_polls)) {
                         record_timeout(p.status, &abort_flag);
                         return false;
                     }
@@ -641,12 +652,15 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 return true;
             };
             // every thread: wait for chunk c's buffer; then its slot may be reused
+            // (a copy whose wait gave up is drained below, before the buffers
+            // are reused or the CTA exits)
             auto wait_full = [&](int c) {
                 const uint32_t r = cnt + c;
-                if (!mbar_wait(&bar_full[r & 1], (r >> 1) & 1, &abort_flag)) {
+                if (mbar_wait(&bar_full[r & 1], (r >> 1) & 1, &abort_flag)) {
+                    waited = c + 1;
+                } else {
                     record_timeout(p.status, &abort_flag);
                 }
-                waited = c + 1;
                 if (tid == 32 && !abort_flag) {
                     st_release(p.cons_done + i, g0 + c + 1);
                 }
@@ -732,8 +746,8 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 // state checkpoint after this chunk (S^T in TMEM is the state after it)
                 if (p.ckpt_interval > 0) {
                     const int64_t done = (int64_t)(c + 1) * C;
-                    if (done % p.ckpt_interval == 0 && done <= len) {
-                        const int64_t idx = ck_base + done / p.ckpt_interval - 1;
+                    const int64_t idx = ck_base + done / p.ckpt_interval - 1;
+                    if (done % p.ckpt_interval == 0 && done <= len && idx < p.ckpt_count) {
                         const int64_t row = p.ckpt_slots ? (int64_t)p.ckpt_slots[idx] : idx;
                         if (row >= 0 && row < p.ckpt_pool_size) {
                             store_state(x, p.ckpt_pool + ((size_t)row * H + h) * D * D);
@@ -805,7 +819,10 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
         if (tid == 0 && t < total) {
             issue_raw(cur);
         }
+        // a raw load issued and not yet waited for, and the parity its
+        // completion will have (drained with it if the loop is left early)
         bool raw_pending = t < total;
+        uint32_t raw_par = 0;
         uint32_t ph_raw = 0, ph_mma = 0;
         float beta_r = 0.0f;   // this thread's beta of the current task (tid < 64)
         GateRegs gr;           // this thread's gate unit of the current task
@@ -852,9 +869,11 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 issue_raw(nt);
             }
             raw_pending = has_next;   // (every thread waits for it below)
+            raw_par = ph_raw;
             if (!s_slot_free) {  // wait for the consumer (no flag is held now)
                 if (tid == kPublisher &&
-                    !wait_at_least(p.cons_done + cur.i, cur.g - p.ring + 1, &abort_flag)) {
+                    !wait_at_least(p.cons_done + cur.i, cur.g - p.ring + 1, &abort_flag,
+                                   p.peer_wait_polls)) {
                     record_timeout(p.status, &abort_flag);
                 }
                 __syncthreads();
@@ -935,7 +954,7 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
         }
         // a loop left early may still have a raw load in flight into this CTA's smem
         if (raw_pending) {
-            mbar_wait(&bar_raw, ph_raw, nullptr);
+            mbar_wait(&bar_raw, raw_par, nullptr);
         }
     }
     // no MMA of this CTA may still be running when its TMEM is freed
@@ -1071,9 +1090,20 @@ cudaError_t launch_split_prefill(const ChunkedParams& p, int num_sms, cudaStream
     if (err != cudaSuccess) {
         return err;
     }
-    // the ring flags and consumer counters were zeroed by the caller on this stream
-    kda_split_kernel<<<(unsigned)num_sms, kThreads, SMEM_BYTES, stream>>>(args);
-    return cudaGetLastError();
+    // The CTAs wait on one another (ring flags, consumer counters), so every
+    // one of them must be resident at once: a cooperative launch guarantees
+    // that, or fails (cudaErrorCooperativeLaunchTooLarge) without running
+    // anything when the grid cannot be co-resident -- the caller then runs the
+    // single-pass kernel instead.  The ring flags and consumer counters were
+    // zeroed by the caller on this stream.
+    void* kargs[] = {&args};
+    err = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(&kda_split_kernel),
+                                      dim3((unsigned)num_sms), dim3(kThreads), kargs,
+                                      SMEM_BYTES, stream);
+    if (err != cudaSuccess) {
+        cudaGetLastError();  // clear the launch error; it is returned instead
+    }
+    return err;
 }
 
 }  // namespace kda

@@ -37,6 +37,7 @@
 
 #include "kda_internal.h"
 #include "kda_lanes.cuh"
+#include "kda_seqlens.cuh"
 
 namespace kda {
 namespace {
@@ -144,13 +145,8 @@ kda_recurrent_kernel(const RecurrentParams p) {
             sidx = p.slots[row];
         }
         valid = sidx >= 0 && sidx < p.pool_size;
-    } else if (p.cu_seqlens) {
-        bos = p.cu_seqlens[row];
-        eos = p.cu_seqlens[row + 1];
     } else {
-        const int64_t len = p.total_T / p.rows;
-        bos = (int64_t)row * len;
-        eos = bos + len;
+        clamped_seq(p.cu_seqlens, row, p.rows, p.total_T, bos, eos);
     }
     if (!valid) {
         // Decode row with an out-of-range slot: state untouched, o = NaN.
@@ -204,9 +200,7 @@ kda_recurrent_kernel(const RecurrentParams p) {
         __syncthreads();
         int part = 0;
         for (int m = tid; m < row; m += kThreads) {
-            const int64_t len = p.cu_seqlens ? (int64_t)(p.cu_seqlens[m + 1] - p.cu_seqlens[m])
-                                             : p.total_T / p.rows;
-            part += (int)(len / p.ckpt_interval);
+            part += (int)(clamped_len(p.cu_seqlens, m, p.rows, p.total_T) / p.ckpt_interval);
         }
         if (part) {
             atomicAdd(&s_ck, part);
@@ -368,7 +362,7 @@ kda_recurrent_kernel(const RecurrentParams p) {
                 }
                 // ---- state checkpoint after every ckpt_interval tokens of the row ----
                 if constexpr (kCkpt) {
-                    if (t == ck_next) {
+                    if (t == ck_next && ck_idx < p.ckpt_count) {
                         const int64_t idx = ck_idx++;
                         ck_next += p.ckpt_interval;
                         const int64_t prow = p.ckpt_slots ? (int64_t)p.ckpt_slots[idx] : idx;

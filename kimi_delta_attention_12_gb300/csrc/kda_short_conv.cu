@@ -26,6 +26,7 @@
 #include <stdint.h>
 
 #include "kda_internal.h"
+#include "kda_seqlens.cuh"
 
 namespace kda {
 namespace {
@@ -146,14 +147,7 @@ __device__ __forceinline__ void load_taps(const float* wbase, float (&wt)[W][VEC
 
 __device__ __forceinline__ void seq_bounds(const ShortConvParams& p, int n, int64_t* bos,
                                            int64_t* eos) {
-    if (p.cu_seqlens) {
-        *bos = p.cu_seqlens[n];
-        *eos = p.cu_seqlens[n + 1];
-    } else {
-        const int64_t len = p.total_T / p.N;
-        *bos = (int64_t)n * len;
-        *eos = *bos + len;
-    }
+    clamped_seq(p.cu_seqlens, n, p.N, p.total_T, *bos, *eos);
 }
 
 // The sequence that holds token t (t < total_T): the last n with start <= t.
@@ -270,7 +264,7 @@ short_conv_kernel(const ShortConvParams p, int n_token_blocks) {
         uint2 raw = make_uint2(0u, 0u);
         if (tau >= bos) {
             raw = ld8(x, xoff(tau), EB);
-        } else if (p.state_in) {
+        } else if (p.state_in && tau >= bos - R) {   // (false only for a malformed cu_seqlens)
             raw = ld8(p.state_in, soff(n, (int)(tau - bos + R)), EB);
         }
         VT::unpack(raw, win[r]);
@@ -325,10 +319,10 @@ short_conv_kernel(const ShortConvParams p, int n_token_blocks) {
                 if (t >= eos) {
                     // first token of a later sequence (skipping empty ones):
                     // the window restarts from that sequence's conv state
-                    do {
+                    while (t >= eos && n + 1 < p.N) {
                         ++n;
                         seq_bounds(p, n, &bos, &eos);
-                    } while (t >= eos);
+                    }
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
                         uint2 s = make_uint2(0u, 0u);

@@ -17,7 +17,10 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// mode 0: dst[slot(i)] = 0;  mode 1: dst[i] = src[slot(i)];  mode 2: dst[slot(i)] = src[i]
+// mode 0: dst[slot(i)] = 0;  mode 1: dst[i] = src[slot(i)];  mode 2: dst[slot(i)] = src[i].
+// A slot outside [0, pool_size) skips its state, except that a gather fills
+// dst[i] with NaN so that a bad slot cannot pass a stale state on unnoticed
+// (as decode writes NaN to the o row of such a slot).
 __global__ void __launch_bounds__(kThreads)
 state_slot_kernel(float* __restrict__ dst, const float* __restrict__ src,
                   const int32_t* __restrict__ slots, int32_t pool_size,
@@ -25,6 +28,13 @@ state_slot_kernel(float* __restrict__ dst, const float* __restrict__ src,
     const int i = blockIdx.x;
     const int32_t s = slots ? slots[i] : i;
     if (s < 0 || s >= pool_size) {
+        if (mode == 1) {
+            const float qnan = __int_as_float(0x7fc00000);
+            float4* d = reinterpret_cast<float4*>(dst) + (size_t)i * state_vec4;
+            for (size_t e = threadIdx.x; e < state_vec4; e += kThreads) {
+                __stcs(d + e, make_float4(qnan, qnan, qnan, qnan));
+            }
+        }
         return;
     }
     float4* d;

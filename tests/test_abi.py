@@ -88,7 +88,7 @@ def _call_prefill(L, a):
     (dict(o=None), kda.KDA_ERR_INVALID_ARG),
     (dict(A=None), kda.KDA_ERR_INVALID_ARG),
     (dict(flags=8), kda.KDA_ERR_INVALID_ARG),
-    (dict(flags=16), kda.KDA_ERR_INVALID_ARG),
+    (dict(flags=32), kda.KDA_ERR_INVALID_ARG),
     (dict(scale=float("nan")), kda.KDA_ERR_INVALID_ARG),
     (dict(N=3, T=64), kda.KDA_ERR_INVALID_ARG),      # 64 % 3 != 0 without cu_seqlens
     (dict(ws=None), kda.KDA_ERR_WORKSPACE),
@@ -282,7 +282,7 @@ def _call_decode_conv(L, **over):
     (dict(w=None), kda.KDA_ERR_INVALID_ARG),
     (dict(cs=None), kda.KDA_ERR_INVALID_ARG),          # W > 1 needs a conv state
     (dict(flags=2), kda.KDA_ERR_INVALID_ARG),          # the recurrent flag is prefill-only
-    (dict(flags=16), kda.KDA_ERR_INVALID_ARG),
+    (dict(flags=32), kda.KDA_ERR_INVALID_ARG),
     (dict(dk=16), kda.KDA_ERR_UNSUPPORTED),
     (dict(pool=2), kda.KDA_ERR_INVALID_ARG),
     (dict(w=BASE + 0x800002), kda.KDA_ERR_ALIGNMENT),

@@ -162,3 +162,27 @@ def test_split_mode_matches_single_pass_bitwise():
     assert torch.equal(outs[0][0], outs[1][0])
     assert torch.equal(outs[0][1], outs[1][1])
     _check(x, outs[0][0], outs[0][1])
+
+
+def test_split_peer_wait_timeout_then_clean_call():
+    """The split kernel's bounded waits on other CTAs, made to run out: with
+    KDA_FLAG_SHORT_PEER_WAITS every such wait gives up after one poll, so the
+    consumers time out on their first chunk.  The call must end by itself and
+    report KDA_ERR_TIMEOUT through the workspace status word; every CTA must
+    have left its loops, drained its copies and freed its TMEM, which the next
+    normal call on the same workspace shows by running the split kernel again
+    to a clean status and oracle parity."""
+    x = inputs.make_prefill_inputs([640, 200], 6, 128, 128, torch.bfloat16, seed=17,
+                                   nonzero_state=True)
+    xd = x.to(DEV)
+    N, T, H = 2, x.q.shape[0], 6
+    ws = kda.alloc_workspace(N, T, H, 128, 128, torch.bfloat16)
+    assert ws.numel() > 256 + 256  # the split kernel runs for these sizes
+    kda.kda_prefill(xd.q, xd.k, xd.v, xd.z, xd.beta, xd.A, xd.initial_state, xd.cu_seqlens,
+                    cu_seqlens_host=x.cu_seqlens, workspace=ws,
+                    extra_flags=kda.KDA_FLAG_SHORT_PEER_WAITS)
+    assert kda.workspace_status(ws) == kda.KDA_ERR_TIMEOUT
+    o, S = kda.kda_prefill(xd.q, xd.k, xd.v, xd.z, xd.beta, xd.A, xd.initial_state,
+                           xd.cu_seqlens, cu_seqlens_host=x.cu_seqlens, workspace=ws)
+    assert kda.workspace_status(ws) == kda.KDA_OK
+    _check(x, o, S)

@@ -6,7 +6,9 @@ allocator after start-up) cannot provide the device workspace kda_prefill
 asks for.  kda_prefill_noalloc takes the same arguments minus the workspace
 and uses a fixed array in the library's own device memory instead.  This
 test calls it through the C ABI and checks that two calls in a row give the
-same o and final state as kda_prefill with a caller workspace.
+same o and final state as kda_prefill with a caller workspace, that both
+agree with the fp64 oracle, and that kda_prefill_noalloc_status (the only
+way such a caller can see a device-side timeout) reads KDA_OK after each.
 
 This file is named so that pytest collects it last.
 """
@@ -45,16 +47,22 @@ def test_noalloc_matches_prefill_twice(dtype, d, tol):
     o_ref, S_ref = kda.kda_prefill(xd.q, xd.k, xd.v, xd.z, xd.beta, xd.A, xd.initial_state,
                                    xd.cu_seqlens)
     torch.cuda.synchronize()
+    import oracle
+    o_or, S_or, _ = oracle.kda_reference(x.q, x.k, x.v, x.z, x.beta, x.A, x.initial_state,
+                                         x.cu_seqlens)
+    err = rel_fro if dtype == torch.bfloat16 else max_rel
     for _ in range(2):
         o = torch.full_like(o_ref, float("nan"))
         S = torch.full_like(S_ref, float("nan"))
         st = _call_noalloc(L, xd, N, d, kda.KDA_BF16 if dtype == torch.bfloat16 else kda.KDA_F32,
                            o, S)
         assert st == kda.KDA_OK, kda.status_string(st)
-        torch.cuda.synchronize()
-        err = rel_fro if dtype == torch.bfloat16 else max_rel
+        assert kda.noalloc_status() == kda.KDA_OK
         assert err(o.float(), o_ref.float()) <= tol
         assert err(S, S_ref) <= tol
+        # and against the fp64 oracle
+        assert err(o.float(), o_or) <= tol
+        assert err(S, S_or) <= tol
 
 
 def test_noalloc_rejects_sizes_beyond_its_array():
