@@ -213,8 +213,12 @@ __device__ __forceinline__ void cta_sync_tc() {
     tc_fence_after();
 }
 
-__device__ __forceinline__ void record_timeout(int32_t* status, volatile int* abort_flag) {
-    atomicExch(status, kStatusTimeout);
+// A bounded wait gave up: the first one to do so records where (a nonzero
+// code, the source line of the wait) in the status word, and the CTA leaves
+// its loops.  Any nonzero status is reported as a timeout.
+__device__ __forceinline__ void record_timeout(int32_t* status, volatile int* abort_flag,
+                                               int site = kStatusTimeout) {
+    atomicCAS(status, 0, site);
     *abort_flag = 1;
 }
 
@@ -540,6 +544,68 @@ __device__ __forceinline__ void phase_state_to_tmem(const Ctx& x) {
     }
     tmem_st16(x.tbase + x.lane_base + TC_SB + cb / 2, w);
     tmem_wait_st();
+}
+
+// S^T (TMEM, fp32) -> bf16 at TC_SB, and S^T *= Gamma in the same pass (the
+// next chunk's products read the bf16 copy of the undecayed state and
+// accumulate onto the decayed one); all 16 warps, 32 c each.  No barrier.
+__device__ __forceinline__ void phase_state_to_tmem_decay(const Ctx& x, const float* gam) {
+    const int cb = 32 * x.sub;
+    const uint32_t taddr = x.tbase + x.lane_base + TC_S + cb;
+    uint32_t r0[16], r1[16];
+    tmem_ld16(taddr, r0);
+    tmem_ld16(taddr + 16, r1);
+    tmem_wait_ld();
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        w[i] = pack_bf16x2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
+        w[8 + i] = pack_bf16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
+    }
+    tmem_st16(x.tbase + x.lane_base + TC_SB + cb / 2, w);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        r0[i] = __float_as_uint(__uint_as_float(r0[i]) * gam[cb + i]);
+        r1[i] = __float_as_uint(__uint_as_float(r1[i]) * gam[cb + 16 + i]);
+    }
+    tmem_st16(taddr, r0);
+    tmem_st16(taddr + 16, r1);
+    tmem_wait_st();
+}
+
+// O^T (TMEM lane j, columns r0 .. r0 + 15 of this warp) -> 8 registers of
+// bf16 pairs, then O^T = 0 for the next chunk's accumulation.  The global
+// stores follow later (phase_ot_store), off the chunk's critical path.  No
+// barrier.
+__device__ __forceinline__ void phase_ot_take(const Ctx& x, uint32_t (&ob)[8]) {
+    const uint32_t taddr = x.tbase + x.lane_base + TC_O + 16 * x.sub;
+    uint32_t r[16];
+    tmem_ld16(taddr, r);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        ob[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) r[i] = 0u;
+    tmem_st16(taddr, r);
+    tmem_wait_st();
+}
+
+// The values phase_ot_take kept -> o (bf16): this warp's 16 tokens of its 32
+// value columns; for a token the warp's lanes cover 64 contiguous bytes of o.
+__device__ __forceinline__ void phase_ot_store(const Ctx& x, __nv_bfloat16* o_g, int64_t t0,
+                                               int L, int h, int H, const uint32_t (&ob)[8]) {
+    const int j = 32 * x.qd + x.lane;
+    const int r0 = 16 * x.sub;
+    uint16_t* dst = reinterpret_cast<uint16_t*>(o_g + ((size_t)(t0 + r0) * H + h) * D + j);
+    const size_t row = (size_t)H * D;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        if (r0 + i < L) {
+            dst[i * row] = (uint16_t)((i & 1) ? (ob[i >> 1] >> 16) : (ob[i >> 1] & 0xffffu));
+        }
+    }
 }
 
 // S^T *= Gamma_C in TMEM; all 16 warps, 32 c each.  No barrier.

@@ -52,6 +52,7 @@
 #include "kda_chunk_phases.cuh"
 #include "kda_chunked.h"
 #include "kda_seqlens.cuh"
+#include "kda_split_phases.cuh"
 #include "sm103_ptx.cuh"
 
 namespace kda {
@@ -73,8 +74,10 @@ struct ChunkedArgs {
 constexpr uint32_t CB_BYTES = 66560;          // one slot buffer (HO_BYTES, 1024-aligned)
 constexpr uint32_t CB_VRING = 2 * CB_BYTES;    // then a ring of v tiles, prefetched ahead
 constexpr int kVRing = 4;
-static_assert(CB_VRING + kVRing * 16384 <= SMEM_USED,
-              "consumer layout exceeds the shared memory budget");
+// dynamic shared memory of the split kernel: the larger of the consumer's
+// and the producer's layouts, plus slack for the 1024-byte alignment
+constexpr uint32_t kSplitSmemBytes =
+    (CB_VRING + kVRing * 16384 > split::P_END ? CB_VRING + kVRing * 16384 : split::P_END) + 1024;
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) &
@@ -205,7 +208,7 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
             ph_raw ^= 1;
             raw_pending = false;
         } else {
-            record_timeout(p.status, &abort_flag);
+            record_timeout(p.status, &abort_flag, 211);
         }
         __syncthreads();
         if (abort_flag) {
@@ -235,7 +238,7 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
             mma_commit(&bar_mma);
         }
         if (!mbar_wait(&bar_mma, ph_mma, &abort_flag)) {
-            record_timeout(p.status, &abort_flag);
+            record_timeout(p.status, &abort_flag, 241);
         }
         ph_mma ^= 1;
         tc_fence_after();
@@ -262,7 +265,7 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
             ph_v ^= 1;
             v_pending = false;
         } else {
-            record_timeout(p.status, &abort_flag);
+            record_timeout(p.status, &abort_flag, 268);
         }
         if (tid == 0 && !abort_flag) {
             issue_w(x);
@@ -270,7 +273,7 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
             mma_commit(&bar_mma);
         }
         if (!mbar_wait(&bar_mma, ph_mma, &abort_flag)) {
-            record_timeout(p.status, &abort_flag);
+            record_timeout(p.status, &abort_flag, 276);
         }
         ph_mma ^= 1;
         tc_fence_after();
@@ -296,7 +299,7 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
             mma_commit(&bar_mma);
         }
         if (!mbar_wait(&bar_mma, ph_mma, &abort_flag)) {
-            record_timeout(p.status, &abort_flag);
+            record_timeout(p.status, &abort_flag, 302);
         }
         ph_mma ^= 1;
         tc_fence_after();
@@ -316,7 +319,7 @@ kda_chunked_kernel(const __grid_constant__ ChunkedArgs args) {
             mma_commit(&bar_mma);
         }
         if (!mbar_wait(&bar_mma, ph_mma, &abort_flag)) {
-            record_timeout(p.status, &abort_flag);
+            record_timeout(p.status, &abort_flag, 322);
         }
         ph_mma ^= 1;
         tc_fence_after();
@@ -373,6 +376,15 @@ __device__ __forceinline__ int32_t ld_acquire(const int32_t* ptr) {
 
 __device__ __forceinline__ void st_release(int32_t* ptr, int32_t v) {
     asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+}
+
+// Tells producers that a ring slot may be rewritten.  The slot's bulk copy
+// into this CTA's shared memory has completed (its mbarrier phase was
+// observed) before this store is issued, so no data needs publishing with it:
+// a relaxed store, which does not wait for this CTA's output stores to drain
+// as a release would.
+__device__ __forceinline__ void st_relaxed(int32_t* ptr, int32_t v) {
+    asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
 }
 
 // Bounded wait (one thread) until *ptr >= target: at most `polls` polls.
@@ -471,6 +483,11 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
     __shared__ uint64_t bar_u;         // consumer: U^T done
     __shared__ uint64_t bar_os;        // consumer: O and the state update done
     __shared__ uint64_t bar_fin;       // every MMA of this CTA done
+    __shared__ uint64_t bar_gram;      // producer: Gram products of a task done (A -> B)
+    __shared__ uint64_t bar_gfree;     // producer: B has read a task's Gram (B -> A)
+    __shared__ uint64_t bar_bdone[2];  // producer: B finished task j (K+, beta buffer j & 1 free)
+    __shared__ uint64_t bar_w;         // producer: W^T of a task done
+    __shared__ uint64_t bar_finb;      // producer: every MMA of group B done
     __shared__ uint32_t tmem_base_s;
     __shared__ int s_issued;
     __shared__ int s_vissued;
@@ -494,6 +511,12 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
         mbar_init(&bar_u, 1);
         mbar_init(&bar_os, 1);
         mbar_init(&bar_fin, 1);
+        mbar_init(&bar_gram, 1);
+        mbar_init(&bar_gfree, 1);
+        mbar_init(&bar_bdone[0], 1);
+        mbar_init(&bar_bdone[1], 1);
+        mbar_init(&bar_w, 1);
+        mbar_init(&bar_finb, 1);
         fence_mbar_init();
         prefetch_tmap(&args.tm_q);
         prefetch_tmap(&args.tm_k);
@@ -629,13 +652,19 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 }
                 return ok;
             };
-            // thread 0: copy chunk c's slot into buffer (cnt + c) & 1
-            auto fetch = [&](int c, bool block) -> bool {
+            // thread 0: the ring flag of chunk c
+            auto flag_of = [&](int c) -> const int32_t* {
+                return p.flags + i * p.ring + (g0 + c) % p.ring;
+            };
+            // thread 0: copy chunk c's slot into buffer (cnt + c) & 1 (block: wait
+            // for its flag; ready: an earlier acquire load of it saw it raised)
+            auto fetch = [&](int c, bool block, bool ready = false) -> bool {
                 const int32_t g = g0 + c;
                 const int32_t slot = i * p.ring + g % p.ring;
-                if (block) {
+                if (ready) {
+                } else if (block) {
                     if (!wait_at_least(p.flags + slot, g + 1, &abort_flag, p.peer_wait_polls)) {
-                        record_timeout(p.status, &abort_flag);
+                        record_timeout(p.status, &abort_flag, 667);
                         return false;
                     }
                 } else if (ld_acquire(p.flags + slot) < g + 1) {
@@ -659,10 +688,10 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 if (mbar_wait(&bar_full[r & 1], (r >> 1) & 1, &abort_flag)) {
                     waited = c + 1;
                 } else {
-                    record_timeout(p.status, &abort_flag);
+                    record_timeout(p.status, &abort_flag, 691);
                 }
                 if (tid == 32 && !abort_flag) {
-                    st_release(p.cons_done + i, g0 + c + 1);
+                    st_relaxed(p.cons_done + i, g0 + c + 1);
                 }
             };
 
@@ -682,26 +711,38 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                         tc_fence_after();
                         issue_u_prime_tc(x, tiles(cnt & 1, vcnt % kVRing));   // U'^T = V^T Tm^T
                     } else {
-                        record_timeout(p.status, &abort_flag);
+                        record_timeout(p.status, &abort_flag, 714);
                     }
                 }
-                phase_state_to_tmem(x);
+                // S^T -> bf16 operand; S^T *= Gamma of chunk 0
+                phase_state_to_tmem_decay(
+                    x, reinterpret_cast<const float*>(sm + tiles(cnt & 1, 0).gam));
                 cta_sync_tc();
             }
+            uint32_t ob[8];   // the last chunk's O^T as bf16 pairs, stored one chunk later
+            // thread 0: flags read during the last chunk's products: of the next
+            // chunk (pf1, when it was not copied yet) and of the one after (pf2)
+            int32_t pf1 = 0, pf2 = 0;
             for (int c = 0; c < nch && !abort_flag; ++c) {
                 const StateTiles st = tiles((cnt + c) & 1, (vcnt + c) % kVRing);
                 // [O^T | U^T] += S^T [Q+^T | -W^T]  (U^T holds U', O^T zero)
                 if (tid == 0) {
                     issue_ou_tc(x, st);
                     mma_commit(&bar_u);
-                    if (fetched == c + 1 && c + 1 < nch) {
-                        fetch(c + 1, false);
+                    // chunk c + 1 into the buffer chunk c - 1 left, if the flag read
+                    // during the last chunk's products showed it published (before
+                    // this thread's output stores below, which the copy's proxy
+                    // fence would otherwise wait for)
+                    if (fetched == c + 1 && c + 1 < nch && pf2 >= g0 + c + 2) {
+                        fetch(c + 1, false, true);
                     }
                 }
-                // S^T *= Gamma_C while the tensor core works
-                phase_state_decay(x, reinterpret_cast<const float*>(sm + st.gam));
+                // the previous chunk's o while the tensor core works
+                if (c > 0) {
+                    phase_ot_store(x, o_g, bos + (c - 1) * C, C, h, H, ob);
+                }
                 if (!mbar_wait(&bar_u, ph_u, &abort_flag)) {
-                    record_timeout(p.status, &abort_flag);
+                    record_timeout(p.status, &abort_flag, 745);
                 }
                 ph_u ^= 1;
                 tc_fence_after();
@@ -710,39 +751,50 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 if (abort_flag) {
                     break;
                 }
-                // [S^T | O^T] += U^T [Kend ; Aqk]; then the next chunk's U'
+                // [S^T | O^T] += U^T [Kend ; Aqk]
                 if (tid == 0) {
                     issue_so_tc(x, st);
                     mma_commit(&bar_os);
-                    // U'(c) is done (before U^T): its v slot takes chunk c + kVRing
-                    if (c + kVRing < nch) {
-                        issue_v(c + kVRing);
+                    // the flag of the chunk after next, read while the tensor core
+                    // works (the acquire load's latency overlaps the products); its
+                    // copy is issued at the top of the next chunk
+                    pf1 = pf2 = 0;
+                    if (c + 1 < nch && fetched == c + 1) {
+                        pf1 = ld_acquire(flag_of(c + 1));
                     }
-                    if (c + 1 < nch && (fetched >= c + 2 || fetch(c + 1, true))) {
-                        const uint32_t r = cnt + c + 1;
-                        if (mbar_wait(&bar_full[r & 1], (r >> 1) & 1, &abort_flag) &&
-                            wait_v(c + 1)) {
-                            tc_fence_after();
-                            issue_u_prime_tc(x, tiles(r & 1, (vcnt + c + 1) % kVRing));
-                        } else {
-                            record_timeout(p.status, &abort_flag);
-                        }
+                    if (c + 2 < nch && fetched <= c + 2) {
+                        pf2 = ld_acquire(flag_of(c + 2));
                     }
                 }
                 if (!mbar_wait(&bar_os, ph_os, &abort_flag)) {
-                    record_timeout(p.status, &abort_flag);
+                    record_timeout(p.status, &abort_flag, 770);
                 }
                 ph_os ^= 1;
                 tc_fence_after();
-                // this chunk's buffer is free: copy chunk c + 2 into it if it is ready
-                if (tid == 0 && c + 2 < nch && fetched == c + 2) {
-                    fetch(c + 2, false);
+                if (tid == 0 && !abort_flag) {
+                    if (c + 1 < nch) {
+                        // the next chunk's U' = V Tm^T (its slot must have landed; a
+                        // chunk the producers have not published yet is waited for)
+                        if (fetched >= c + 2 || fetch(c + 1, pf1 < g0 + c + 2, pf1 >= g0 + c + 2)) {
+                            const uint32_t r = cnt + c + 1;
+                            if (mbar_wait(&bar_full[r & 1], (r >> 1) & 1, &abort_flag) &&
+                                wait_v(c + 1)) {
+                                tc_fence_after();
+                                issue_u_prime_tc(x, tiles(r & 1, (vcnt + c + 1) % kVRing));
+                            } else {
+                                record_timeout(p.status, &abort_flag, 785);
+                            }
+                        }
+                    }
+                    // U'(c) and the products of chunk c are done: its v slot takes
+                    // chunk c + kVRing
+                    if (c + kVRing < nch) {
+                        issue_v(c + kVRing);
+                    }
                 }
                 if (c + 1 < nch) {
                     wait_full(c + 1);
                 }
-                // O^T -> o, and the next chunk's S^T -> bf16 operand (the loop
-                // condition, read after the barrier below, handles an abort)
                 // state checkpoint after this chunk (S^T in TMEM is the state after it)
                 if (p.ckpt_interval > 0) {
                     const int64_t done = (int64_t)(c + 1) * C;
@@ -754,11 +806,18 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                         }
                     }
                 }
-                phase_ot_epilogue_zero(x, o_g, bos + c * C, min(C, len - c * C), h, H);
+                // O^T -> registers (stored during the next chunk's products); the
+                // next chunk's S^T -> bf16 operand and S^T *= its Gamma
+                phase_ot_take(x, ob);
                 if (c + 1 < nch) {
-                    phase_state_to_tmem(x);
+                    phase_state_to_tmem_decay(
+                        x, reinterpret_cast<const float*>(
+                               sm + tiles((cnt + c + 1) & 1, 0).gam));
                 }
                 cta_sync_tc();
+                if (c + 1 == nch) {   // the last chunk's o
+                    phase_ot_store(x, o_g, bos + c * C, len - c * C, h, H, ob);
+                }
             }
             // copies still in flight into this CTA's buffers (a loop left early)
             if (tid == 0) {
@@ -788,26 +847,23 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
     } else {
         // ------------------------------------------------------------ producer
         // Producer k takes tasks k, k + P, k + 2P, ... (P producers; tasks past
-        // the end of their sequence are skipped).  Per task: the operand tiles
-        // (all warps), the Gram products, then warps 0-7 finish the task (Gram
-        // epilogue, UT solve, W) while warps 8-15 run the next task's norms and
-        // gate; warps 0-7 then run their own gate units of the next task.  The
-        // tiles the task does not keep (Q+, Kend, Gamma, Aqk, a copy of Tm,
-        // -W^T) go straight into its ring slot; the slot's flag is raised right
-        // after the next task's gate barrier by one thread's release store,
-        // which is cumulative over the CTA's writes ordered before it by that
-        // barrier, and before any wait for a consumer.
+        // the end of their sequence are skipped), the j-th of them through two
+        // warp groups (kda_split_phases.cuh): group A (warps 0-7) runs the
+        // prologue of task j and issues its Gram products while group B (warps
+        // 8-15) finishes task j - 1 (Gram epilogue, UT solve, W).  Hand-overs,
+        // all mbarriers with one arrival: bar_gram (task j's Gram done, A -> B),
+        // bar_gfree (B has read task j's Gram: A may issue the next into the same
+        // TMEM), bar_bdone[j & 1] (B finished task j: its K+ and beta buffers
+        // are free and its slot writes done).  A thread of group A raises each
+        // slot's flag (release) once both groups' writes to it are done; before
+        // group A waits for a consumer to free a slot it raises every flag it
+        // can, so that no wait depends on an unraised flag.
+        using namespace split;
         const int total = meta.task0[p.n_batches];
         const int P = (int)gridDim.x - p.n_cons;
-        float* s_beta = reinterpret_cast<float*>(sm + OFF_BETA);
-        constexpr int kPublisher = 256;  // a thread of warps 8-15 (idle at the hand-offs)
-        const bool low = x.warp < 8;
-        auto issue_raw = [&](const SplitTask& tk) {
-            mbar_arrive_expect_tx(&bar_raw, 3 * 16384);
-            tma_load_3d(sm + OFF_RAWQ, &args.tm_q, 0, tk.h, tk.t0, &bar_raw);
-            tma_load_3d(sm + OFF_RAWK, &args.tm_k, 0, tk.h, tk.t0, &bar_raw);
-            tma_load_3d(sm + OFF_RAWZ, &args.tm_z, 0, tk.h, tk.t0, &bar_raw);
-        };
+        const bool grpA = x.warp < 8;
+        const int lt = grpA ? tid : tid - 256;   // thread within the group
+        const int lw = lt >> 5;                  // warp within the group
         auto next_task = [&](int t, SplitTask& tk) -> int {
             while (t < total && !decode_task(meta, p, t, tk)) {
                 t += P;
@@ -816,145 +872,195 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
         };
         SplitTask cur;
         int t = next_task((int)blockIdx.x - p.n_cons, cur);
-        if (tid == 0 && t < total) {
-            issue_raw(cur);
-        }
-        // a raw load issued and not yet waited for, and the parity its
-        // completion will have (drained with it if the loop is left early)
-        bool raw_pending = t < total;
-        uint32_t raw_par = 0;
-        uint32_t ph_raw = 0, ph_mma = 0;
-        float beta_r = 0.0f;   // this thread's beta of the current task (tid < 64)
-        GateRegs gr;           // this thread's gate unit of the current task
-        if (t < total) {
-            if (tid < cur.L) {
-                beta_r = __bfloat162float(beta_g[(size_t)(cur.t0 + tid) * H + cur.h]);
+        if (grpA) {
+            // ---------------------------------------------------- group A
+            constexpr int kPublisher = 32;   // lane 0 of warp 1
+            auto issue_raw = [&](const SplitTask& tk) {
+                mbar_arrive_expect_tx(&bar_raw, 3 * 16384);
+                tma_load_3d(sm + P_RAWQ, &args.tm_q, 0, tk.h, tk.t0, &bar_raw);
+                tma_load_3d(sm + P_RAWK, &args.tm_k, 0, tk.h, tk.t0, &bar_raw);
+                tma_load_3d(sm + P_RAWZ, &args.tm_z, 0, tk.h, tk.t0, &bar_raw);
+            };
+            if (tid == 0 && t < total) {
+                issue_raw(cur);
             }
-            if (mbar_wait(&bar_raw, ph_raw, &abort_flag)) {
-                raw_pending = false;
-            } else {
-                record_timeout(p.status, &abort_flag);
-            }
-            ph_raw ^= 1;
-            phase_norms(x, cur.L, p.scale, p.l2norm);
-            phase_prologue_gate(x, cur.L, meta.eA[cur.h], gr);
-        }
-        int32_t pend_slot = -1, pend_val = 0;  // publisher: the last written slot, not yet flagged
-        int32_t cons_seen = 0;                 // publisher: the current task's consumer counter
-        while (t < total) {
-            SplitTask nt;
-            const int tn = next_task(t + P, nt);
-            const bool has_next = tn < total;
-            const int32_t slot = cur.i * p.ring + cur.g % p.ring;
-            uint8_t* pub = p.handoff + (size_t)slot * HO_BYTES;
-            // is the slot free (its consumer has copied out the chunk that was in
-            // it)?  cons_seen was read while warps 8-15 waited for the last task.
-            if (tid == kPublisher) {
-                if (cons_seen < cur.g - p.ring + 1) {
-                    cons_seen = ld_acquire(p.cons_done + cur.i);
+            bool raw_pending = t < total;   // a raw load issued and not waited for
+            uint32_t raw_par = 0;           // (and the parity it completes)
+            // publisher: the flag of the previous task, not raised yet
+            int32_t pend_slot = -1, pend_val = 0;
+            // publisher: consumer cons_i's counter, read earlier (it only grows)
+            int32_t cons_seen = 0;
+            int cons_i = -1;
+            const int c = lt & (D - 1);
+            const int hb = lt >> 7;         // the thread's blocks: 2 hb, 2 hb + 1
+            // publisher: wait for B to finish task jj, then raise its flag
+            auto raise_pending = [&](int jj) {
+                if (pend_slot < 0) {
+                    return;
                 }
-                s_slot_free = cons_seen >= cur.g - p.ring + 1;
-            }
-            // every gate unit and the norms of this task are done; the last
-            // task's slot writes too
-            if (__syncthreads_or(abort_flag != 0)) {
-                break;
-            }
-            // the last task's slot writes are ordered before this barrier
-            if (tid == kPublisher && pend_slot >= 0) {
+                if (!mbar_wait(&bar_bdone[jj & 1], (jj >> 1) & 1, &abort_flag)) {
+                    record_timeout(p.status, &abort_flag, 900);
+                    return;
+                }
                 st_release(p.flags + pend_slot, pend_val);
                 pend_slot = -1;
-            }
-            if (tid == 0 && has_next) {  // the raw tiles are consumed: fetch the next task's
-                issue_raw(nt);
-            }
-            raw_pending = has_next;   // (every thread waits for it below)
-            raw_par = ph_raw;
-            if (!s_slot_free) {  // wait for the consumer (no flag is held now)
-                if (tid == kPublisher &&
-                    !wait_at_least(p.cons_done + cur.i, cur.g - p.ring + 1, &abort_flag,
-                                   p.peer_wait_polls)) {
-                    record_timeout(p.status, &abort_flag);
+            };
+            int j = 0;
+            while (t < total) {
+                SplitTask nt;
+                const int tn = next_task(t + P, nt);
+                const bool has_next = tn < total;
+                const int32_t slot = cur.i * p.ring + cur.g % p.ring;
+                uint8_t* pub = p.handoff + (size_t)slot * HO_BYTES;
+                float* s_beta = reinterpret_cast<float*>(sm + P_BETA) + (j & 1) * 64;
+                uint8_t* kp = sm + P_KP + (j & 1) * 16384;
+                // K+ and beta buffer j & 1 are free once B finished task j - 2
+                bool ok = true;
+                if (j >= 2) {
+                    ok = mbar_wait(&bar_bdone[j & 1], ((j - 2) >> 1) & 1, &abort_flag);
                 }
-                __syncthreads();
-            }
-            phase_prologue_operands<true>(x, cur.L, gr, pub);
-            if (tid < C) {
-                s_beta[tid] = beta_r;
-            }
-            cta_sync_tc();  // (the operands half fenced its shared-memory tiles)
-            if (tid == 0) {
-                issue_gram(x);
-                mma_commit(&bar_mma);
-            }
-            float beta_n = 0.0f;   // beta of the next task, used one task from now
-            if (has_next && tid < nt.L) {
-                beta_n = __bfloat162float(beta_g[(size_t)(nt.t0 + tid) * H + nt.h]);
-            }
-            if (low) {
-                // ---- warps 0-7: the rest of this task
-                if (!mbar_wait(&bar_mma, ph_mma, &abort_flag)) {
-                    record_timeout(p.status, &abort_flag);
-                }
-                ph_mma ^= 1;
-                tc_fence_after();
-                phase_gram_epilogue<true>(x, pub);
-                tc_fence_before();
-                half_sync(kBarLow);
-                phase_solve_half<true>(x, pub);
-                fence_proxy_async();
-                tc_fence_before();
-                half_sync(kBarLow);
-                tc_fence_after();
-                if (tid == 0) {
-                    issue_w(x);
-                    mma_commit(&bar_mma);
-                }
-                if (!mbar_wait(&bar_mma, ph_mma, &abort_flag)) {
-                    record_timeout(p.status, &abort_flag);
-                }
-                ph_mma ^= 1;
-                tc_fence_after();
-                phase_neg_w_tile_half(x, pub + HO_WT);
-                // then this half's gate units of the next task
-                if (has_next) {
-                    if (mbar_wait(&bar_raw, ph_raw, &abort_flag)) {
-                        raw_pending = false;
-                    } else {
-                        record_timeout(p.status, &abort_flag);
-                    }
-                    phase_prologue_gate(x, nt.L, meta.eA[nt.h], gr);
-                }
-            } else if (has_next) {
-                // ---- warps 8-15: the next task's norms and their gate units
-                if (mbar_wait(&bar_raw, ph_raw, &abort_flag)) {
+                if (ok && mbar_wait(&bar_raw, j & 1, &abort_flag)) {
                     raw_pending = false;
                 } else {
-                    record_timeout(p.status, &abort_flag);
+                    record_timeout(p.status, &abort_flag, 923);
                 }
-                phase_norms_half(x, x.warp - 8, nt.L, p.scale, p.l2norm);
-                phase_prologue_gate(x, nt.L, meta.eA[nt.h], gr);
-                if (tid == kPublisher) {
-                    cons_seen = ld_acquire(p.cons_done + nt.i);  // read ahead of use
+                // beta, norms and gate of task j
+                if (lt < C) {
+                    s_beta[lt] = lt < cur.L
+                                     ? __bfloat162float(beta_g[(size_t)(cur.t0 + lt) * H + cur.h])
+                                     : 0.0f;
                 }
+                a_norms(sm, lw, x.lane, cur.L, p.scale, p.l2norm);
+                float al0[16], al1[16];
+                a_gate_block(sm, c, 2 * hb, cur.L, meta.eA[cur.h], al0);
+                a_gate_block(sm, c, 2 * hb + 1, cur.L, meta.eA[cur.h], al1);
+                // is the slot free (its consumer has copied out the chunk that was in it)?
+                if (lt == kPublisher) {
+                    if (cons_i != cur.i || cons_seen < cur.g - p.ring + 1) {
+                        cons_seen = ld_acquire(p.cons_done + cur.i);
+                        cons_i = cur.i;
+                    }
+                    s_slot_free = cons_seen >= cur.g - p.ring + 1;
+                }
+                if (group_sync_or(kBarA, abort_flag != 0)) {
+                    break;
+                }
+                if (!s_slot_free) {
+                    // raise the previous task's flag first (no wait may depend on it)
+                    if (lt == kPublisher) {
+                        raise_pending(j - 1);
+                        if (!wait_at_least(p.cons_done + cur.i, cur.g - p.ring + 1, &abort_flag,
+                                           p.peer_wait_polls)) {
+                            record_timeout(p.status, &abort_flag, 951);
+                        }
+                    }
+                    group_sync(kBarA);
+                }
+                // X~, K~ are free once the previous task's Gram products are done
+                if (j >= 1 && !mbar_wait(&bar_gram, (j - 1) & 1, &abort_flag)) {
+                    record_timeout(p.status, &abort_flag, 958);
+                }
+                // the operand tiles
+                a_operands_block(sm, c, 2 * hb, al0, kp, pub);
+                a_operands_block(sm, c, 2 * hb + 1, al1, kp, pub);
+                fence_proxy_async();
+                tc_fence_before();
+                const bool stop = group_sync_or(kBarA, abort_flag != 0);
+                tc_fence_after();
+                if (stop) {
+                    break;
+                }
+                if (tid == 0) {
+                    if (has_next) {   // the raw tiles are consumed: fetch the next task's
+                        issue_raw(nt);
+                    }
+                    // the Gram accumulator is free once B has read the last one
+                    if (j >= 1 && !mbar_wait(&bar_gfree, (j - 1) & 1, &abort_flag)) {
+                        record_timeout(p.status, &abort_flag, 976);
+                    }
+                    if (!abort_flag) {
+                        tc_fence_after();
+                        a_issue_gram(x.smem_base, x.tbase);
+                        mma_commit(&bar_gram);
+                    }
+                }
+                raw_pending = has_next;
+                raw_par = (j + 1) & 1;
+                // the previous task's flag, while the other warps wait for the next
+                // raw tiles (a release after fresh writes waits for them to drain)
+                if (lt == kPublisher) {
+                    raise_pending(j - 1);
+                    pend_slot = slot;
+                    pend_val = cur.g + 1;
+                    if (has_next && nt.i != cons_i) {   // read ahead of its use
+                        cons_seen = ld_acquire(p.cons_done + nt.i);
+                        cons_i = nt.i;
+                    }
+                }
+                cur = nt;
+                t = tn;
+                ++j;
             }
-            if (has_next) {
-                ph_raw ^= 1;
+            // the last task's flag
+            if (lt == kPublisher && !abort_flag) {
+                raise_pending(j - 1);
             }
-            pend_slot = slot;
-            pend_val = cur.g + 1;
-            beta_r = beta_n;
-            t = tn;
-            cur = nt;
-        }
-        // flag the last slot
-        __syncthreads();
-        if (tid == kPublisher && pend_slot >= 0 && !abort_flag) {
-            st_release(p.flags + pend_slot, pend_val);
-        }
-        // a loop left early may still have a raw load in flight into this CTA's smem
-        if (raw_pending) {
-            mbar_wait(&bar_raw, raw_par, nullptr);
+            // a loop left early may still have a raw load in flight into this CTA's smem
+            if (raw_pending) {
+                mbar_wait(&bar_raw, raw_par, nullptr);
+            }
+        } else {
+            // ---------------------------------------------------- group B
+            int j = 0;
+            while (t < total) {
+                SplitTask nt;
+                const int tn = next_task(t + P, nt);
+                const int32_t slot = cur.i * p.ring + cur.g % p.ring;
+                uint8_t* pub = p.handoff + (size_t)slot * HO_BYTES;
+                const float* s_beta = reinterpret_cast<const float*>(sm + P_BETA) + (j & 1) * 64;
+                // task j's Gram products
+                if (!mbar_wait(&bar_gram, j & 1, &abort_flag)) {
+                    record_timeout(p.status, &abort_flag, 1016);
+                }
+                tc_fence_after();
+                b_gram_epilogue(sm, x.tbase, x.warp, x.lane, lw >> 2, s_beta, pub);
+                tc_fence_before();
+                const bool stop = group_sync_or(kBarB, abort_flag != 0);
+                if (stop) {
+                    break;
+                }
+                if (lt == 0) {
+                    mbar_arrive(&bar_gfree);
+                }
+                b_solve(sm, lt, lw, x.lane, s_beta, pub);
+                fence_proxy_async();
+                tc_fence_before();
+                group_sync(kBarB);
+                tc_fence_after();
+                if (lt == 0) {
+                    b_issue_w(x.smem_base, x.tbase, P_KP + (j & 1) * 16384);
+                    mma_commit(&bar_w);
+                }
+                if (!mbar_wait(&bar_w, j & 1, &abort_flag)) {
+                    record_timeout(p.status, &abort_flag, 1038);
+                }
+                tc_fence_after();
+                b_neg_w(x.tbase, x.warp, lw, x.lane, pub + HO_WT);
+                tc_fence_before();
+                group_sync(kBarB);
+                if (lt == 0) {
+                    mbar_arrive(&bar_bdone[j & 1]);
+                }
+                cur = nt;
+                t = tn;
+                ++j;
+            }
+            // no W^T product of this group may still be running when the TMEM
+            // is freed (a wait above may have given up)
+            if (lt == 0) {
+                mma_commit(&bar_finb);
+                mbar_wait(&bar_finb, 0, nullptr);
+            }
         }
     }
     // no MMA of this CTA may still be running when its TMEM is freed
@@ -1086,7 +1192,7 @@ cudaError_t launch_split_prefill(const ChunkedParams& p, int num_sms, cudaStream
     }
     cudaError_t err = cudaFuncSetAttribute(kda_split_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)SMEM_BYTES);
+                                           (int)kSplitSmemBytes);
     if (err != cudaSuccess) {
         return err;
     }
@@ -1099,7 +1205,7 @@ cudaError_t launch_split_prefill(const ChunkedParams& p, int num_sms, cudaStream
     void* kargs[] = {&args};
     err = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(&kda_split_kernel),
                                       dim3((unsigned)num_sms), dim3(kThreads), kargs,
-                                      SMEM_BYTES, stream);
+                                      kSplitSmemBytes, stream);
     if (err != cudaSuccess) {
         cudaGetLastError();  // clear the launch error; it is returned instead
     }
