@@ -100,8 +100,9 @@ enum {
  * accepted.  With bf16 and d_k = d_v = 128 (up to 1024 sequences and 256
  * heads), a larger workspace -- the size returned here, a ring of 16 slots of
  * 66,048 bytes (about 1.06 MB) per consumer CTA, at most a quarter of the SMs
- * (about 40 MB on 152 SMs) whatever the sequence lengths -- selects the split
- * kernel, which spreads each (sequence, head) pair's chunks over all SMs and
+ * (about 40 MB on 152 SMs; 24 slots on up to a third of the SMs, about 80 MB,
+ * where that halves the batches of units) whatever the sequence lengths --
+ * selects the split kernel, which spreads each (sequence, head) pair's chunks over all SMs and
  * passes every chunk's operand tiles through the ring; a smaller one selects
  * the single-pass kernel.  The split kernel needs one CTA on every SM at once
  * and is launched cooperatively, which guarantees that; where the device

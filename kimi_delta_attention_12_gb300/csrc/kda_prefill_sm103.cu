@@ -484,7 +484,7 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
     __shared__ uint64_t bar_os;        // consumer: O and the state update done
     __shared__ uint64_t bar_fin;       // every MMA of this CTA done
     __shared__ uint64_t bar_gram;      // producer: Gram products of a task done (A -> B)
-    __shared__ uint64_t bar_gfree;     // producer: B has read a task's Gram (B -> A)
+    __shared__ uint64_t bar_opready;   // producer: A wrote task j's Gram operands (A -> B)
     __shared__ uint64_t bar_bdone[2];  // producer: B finished task j (K+, beta buffer j & 1 free)
     __shared__ uint64_t bar_w;         // producer: W^T of a task done
     __shared__ uint64_t bar_finb;      // producer: every MMA of group B done
@@ -512,7 +512,7 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
         mbar_init(&bar_os, 1);
         mbar_init(&bar_fin, 1);
         mbar_init(&bar_gram, 1);
-        mbar_init(&bar_gfree, 1);
+        mbar_init(&bar_opready, 1);
         mbar_init(&bar_bdone[0], 1);
         mbar_init(&bar_bdone[1], 1);
         mbar_init(&bar_w, 1);
@@ -851,13 +851,15 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
         // warp groups (kda_split_phases.cuh): group A (warps 0-7) runs the
         // prologue of task j and issues its Gram products while group B (warps
         // 8-15) finishes task j - 1 (Gram epilogue, UT solve, W).  Hand-overs,
-        // all mbarriers with one arrival: bar_gram (task j's Gram done, A -> B),
-        // bar_gfree (B has read task j's Gram: A may issue the next into the same
-        // TMEM), bar_bdone[j & 1] (B finished task j: its K+ and beta buffers
-        // are free and its slot writes done).  A thread of group A raises each
-        // slot's flag (release) once both groups' writes to it are done; before
-        // group A waits for a consumer to free a slot it raises every flag it
-        // can, so that no wait depends on an unraised flag.
+        // all mbarriers with one arrival: bar_opready (task j's operand tiles are
+        // written, A -> B: B issues the Gram products, so that no thread of group
+        // A stalls on the tensor core's issue queue), bar_gram (task j's Gram
+        // done: B reads it, A may overwrite the operand tiles), bar_bdone[j & 1]
+        // (B finished task j: its K+ and beta buffers are free and its slot
+        // writes done).  A thread of group A raises each slot's flag (release)
+        // once both groups' writes to it are done, one task later; before
+        // group A waits for a consumer to free a slot it raises the flag it
+        // still holds, so that no wait depends on an unraised flag.
         using namespace split;
         const int total = meta.task0[p.n_batches];
         const int P = (int)gridDim.x - p.n_cons;
@@ -884,6 +886,11 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
             if (tid == 0 && t < total) {
                 issue_raw(cur);
             }
+            // beta of the current task, loaded one task ahead (threads < 64)
+            float beta_r = 0.0f;
+            if (t < total && lt < cur.L) {
+                beta_r = __bfloat162float(beta_g[(size_t)(cur.t0 + lt) * H + cur.h]);
+            }
             bool raw_pending = t < total;   // a raw load issued and not waited for
             uint32_t raw_par = 0;           // (and the parity it completes)
             // publisher: the flag of the previous task, not raised yet
@@ -891,20 +898,20 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
             // publisher: consumer cons_i's counter, read earlier (it only grows)
             int32_t cons_seen = 0;
             int cons_i = -1;
-            const int c = lt & (D - 1);
-            const int hb = lt >> 7;         // the thread's blocks: 2 hb, 2 hb + 1
             // publisher: wait for B to finish task jj, then raise its flag
             auto raise_pending = [&](int jj) {
                 if (pend_slot < 0) {
                     return;
                 }
                 if (!mbar_wait(&bar_bdone[jj & 1], (jj >> 1) & 1, &abort_flag)) {
-                    record_timeout(p.status, &abort_flag, 900);
+                    record_timeout(p.status, &abort_flag, 907);
                     return;
                 }
                 st_release(p.flags + pend_slot, pend_val);
                 pend_slot = -1;
             };
+            const int c = lt & (D - 1);
+            const int hb = lt >> 7;         // the thread's blocks: 2 hb, 2 hb + 1
             int j = 0;
             while (t < total) {
                 SplitTask nt;
@@ -922,13 +929,14 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 if (ok && mbar_wait(&bar_raw, j & 1, &abort_flag)) {
                     raw_pending = false;
                 } else {
-                    record_timeout(p.status, &abort_flag, 923);
+                    record_timeout(p.status, &abort_flag, 932);
                 }
                 // beta, norms and gate of task j
                 if (lt < C) {
-                    s_beta[lt] = lt < cur.L
-                                     ? __bfloat162float(beta_g[(size_t)(cur.t0 + lt) * H + cur.h])
-                                     : 0.0f;
+                    s_beta[lt] = beta_r;
+                    beta_r = (has_next && lt < nt.L)
+                                 ? __bfloat162float(beta_g[(size_t)(nt.t0 + lt) * H + nt.h])
+                                 : 0.0f;
                 }
                 a_norms(sm, lw, x.lane, cur.L, p.scale, p.l2norm);
                 float al0[16], al1[16];
@@ -951,14 +959,14 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                         raise_pending(j - 1);
                         if (!wait_at_least(p.cons_done + cur.i, cur.g - p.ring + 1, &abort_flag,
                                            p.peer_wait_polls)) {
-                            record_timeout(p.status, &abort_flag, 951);
+                            record_timeout(p.status, &abort_flag, 962);
                         }
                     }
                     group_sync(kBarA);
                 }
                 // X~, K~ are free once the previous task's Gram products are done
                 if (j >= 1 && !mbar_wait(&bar_gram, (j - 1) & 1, &abort_flag)) {
-                    record_timeout(p.status, &abort_flag, 958);
+                    record_timeout(p.status, &abort_flag, 969);
                 }
                 // the operand tiles
                 a_operands_block(sm, c, 2 * hb, al0, kp, pub);
@@ -974,15 +982,7 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                     if (has_next) {   // the raw tiles are consumed: fetch the next task's
                         issue_raw(nt);
                     }
-                    // the Gram accumulator is free once B has read the last one
-                    if (j >= 1 && !mbar_wait(&bar_gfree, (j - 1) & 1, &abort_flag)) {
-                        record_timeout(p.status, &abort_flag, 976);
-                    }
-                    if (!abort_flag) {
-                        tc_fence_after();
-                        a_issue_gram(x.smem_base, x.tbase);
-                        mma_commit(&bar_gram);
-                    }
+                    mbar_arrive(&bar_opready);   // B issues the Gram products
                 }
                 raw_pending = has_next;
                 raw_par = (j + 1) & 1;
@@ -992,7 +992,7 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                     raise_pending(j - 1);
                     pend_slot = slot;
                     pend_val = cur.g + 1;
-                    if (has_next && nt.i != cons_i) {   // read ahead of its use
+                    if (has_next) {   // read ahead of its use (this warp waits here anyway)
                         cons_seen = ld_acquire(p.cons_done + nt.i);
                         cons_i = nt.i;
                     }
@@ -1018,9 +1018,19 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 const int32_t slot = cur.i * p.ring + cur.g % p.ring;
                 uint8_t* pub = p.handoff + (size_t)slot * HO_BYTES;
                 const float* s_beta = reinterpret_cast<const float*>(sm + P_BETA) + (j & 1) * 64;
-                // task j's Gram products
+                // task j's Gram products: issued here once A has written their
+                // operands (the accumulator is free: this group read the last one)
+                if (lt == 0) {
+                    if (mbar_wait(&bar_opready, j & 1, &abort_flag)) {
+                        tc_fence_after();
+                        a_issue_gram(x.smem_base, x.tbase);
+                        mma_commit(&bar_gram);
+                    } else {
+                        record_timeout(p.status, &abort_flag, 1029);
+                    }
+                }
                 if (!mbar_wait(&bar_gram, j & 1, &abort_flag)) {
-                    record_timeout(p.status, &abort_flag, 1016);
+                    record_timeout(p.status, &abort_flag, 1033);
                 }
                 tc_fence_after();
                 b_gram_epilogue(sm, x.tbase, x.warp, x.lane, lw >> 2, s_beta, pub);
@@ -1028,9 +1038,6 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 const bool stop = group_sync_or(kBarB, abort_flag != 0);
                 if (stop) {
                     break;
-                }
-                if (lt == 0) {
-                    mbar_arrive(&bar_gfree);
                 }
                 b_solve(sm, lt, lw, x.lane, s_beta, pub);
                 fence_proxy_async();
@@ -1042,7 +1049,7 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                     mma_commit(&bar_w);
                 }
                 if (!mbar_wait(&bar_w, j & 1, &abort_flag)) {
-                    record_timeout(p.status, &abort_flag, 1038);
+                    record_timeout(p.status, &abort_flag, 1052);
                 }
                 tc_fence_after();
                 b_neg_w(x.tbase, x.warp, lw, x.lane, pub + HO_WT);
@@ -1051,6 +1058,7 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 if (lt == 0) {
                     mbar_arrive(&bar_bdone[j & 1]);
                 }
+
                 cur = nt;
                 t = tn;
                 ++j;
@@ -1121,7 +1129,8 @@ size_t chunked_workspace_bytes(int32_t N, int32_t H) {
 }
 
 namespace {
-constexpr int32_t kSplitRing = 16;  // slots per consumer
+constexpr int32_t kSplitRing = 16;      // slots per consumer
+constexpr int32_t kSplitRingWide = 24;  // with a third of the SMs as consumers
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 size_t split_flags_offset() { return 256; }
 size_t split_done_offset(const SplitPlan& plan) {
@@ -1133,9 +1142,21 @@ bool split_plan(int32_t N, int32_t H, int num_sms, SplitPlan* plan) {
     if (num_sms < 8 || N < 1 || H < 1 || N > kSplitMaxSeqs || H > kSplitMaxHeads) {
         return false;
     }
-    // producers need most of the GPU: at most a quarter of the SMs are consumers
+    // Producers need most of the GPU: at most a quarter of the SMs are
+    // consumers -- or a third where that cuts the units into at most two
+    // batches instead of three or more (96 heads: two batches of 48 instead
+    // of three of 32), with a deeper ring so that the fewer producers can run
+    // further ahead.  (Measured on a GB300: 7.27 -> 6.82 ms for 96 heads x
+    // 65,536 tokens; for many batches, as with 1,024 units, a third of the
+    // SMs as consumers was slower, 9.7 -> 11.9 ms.)
     const int64_t U = (int64_t)N * H;
-    const int64_t max_cons = num_sms / 4;
+    int64_t max_cons = num_sms / 4;
+    int32_t ring = kSplitRing;
+    const int64_t wide = num_sms / 3;
+    if ((U + max_cons - 1) / max_cons > 2 && (U + wide - 1) / wide <= 2) {
+        max_cons = wide;
+        ring = kSplitRingWide;
+    }
     int64_t batches = (U + max_cons - 1) / max_cons;
     if (batches > kSplitMaxBatches) {
         return false;
@@ -1144,7 +1165,7 @@ bool split_plan(int32_t N, int32_t H, int num_sms, SplitPlan* plan) {
     batches = (U + cons - 1) / cons;                    // none left empty
     plan->consumers = (int32_t)cons;
     plan->batches = (int32_t)batches;
-    plan->ring = kSplitRing;
+    plan->ring = ring;
     return true;
 }
 
