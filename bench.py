@@ -71,8 +71,8 @@ def prefill_algorithmic(B, H, T, d, C=64, read_state=False, N=None):
 
 # Sources of the chunked prefill kernels; a profile summary records their
 # digest so that its DRAM traffic is only reported for the kernel it measured.
-PREFILL_SOURCES = ("kda_prefill_sm103.cu", "kda_chunk_phases.cuh", "sm103_ptx.cuh",
-                   "kda_chunked.h", "kda_seqlens.cuh")
+PREFILL_SOURCES = ("kda_prefill_sm103.cu", "kda_chunk_phases.cuh", "kda_split_phases.cuh",
+                   "sm103_ptx.cuh", "kda_chunked.h", "kda_seqlens.cuh")
 
 
 def prefill_source_digest() -> str:
