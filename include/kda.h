@@ -312,13 +312,23 @@ KDA_API size_t kda_decode_conv_workspace_bytes(int32_t B, int32_t H, int32_t d_k
  * Linear's) and the Q/K normalisation (section 1 of the K3 architecture
  * page gives the forward step; the backward is its reverse mode).
  *
- * Recurrent form, fp32 arithmetic, d_v / 32 CTAs per (sequence, head): the
- * states at every 64-token chunk start come from the forward prefill
- * (kda_prefill_checkpointed, on the chunked tensor-core kernel where it
- * applies, launched by this call on `stream`); the chunks are then walked
- * last to first, each recomputed forward in fp32 into a scratch and its
- * tokens walked in reverse; a second kernel adds the per-CTA column sums and
- * applies the gate and normalisation derivatives.
+ * Two forms, both launched by this call on `stream`:
+ *  - chunked, on the tensor cores: bf16 inputs, d_k = d_v = 128, K3's gate,
+ *    and sequence lengths the host can vouch for (cu_seqlens_host given, or
+ *    no cu_seqlens), when the split prefill can run.  That prefill keeps a
+ *    record of every 64-token chunk (its operand tiles and start state); a
+ *    reverse chain then carries dL/dS through the chunks of each (sequence,
+ *    head), last to first, and one CTA per (chunk, head) forms every
+ *    gradient of its tokens (the chunk's adjoint products on the tensor
+ *    core, the decay chains in fp32 on the CUDA cores).  bf16 operands, fp32
+ *    accumulation: the bf16 accuracy of the forward.
+ *  - recurrent, fp32 arithmetic, d_v / 32 CTAs per (sequence, head), for
+ *    every other case: the states at every 64-token chunk start come from the
+ *    checkpointed forward prefill; the chunks are walked last to first, each
+ *    recomputed forward in fp32 into a scratch and its tokens walked in
+ *    reverse; a second kernel adds the per-CTA column sums and applies the
+ *    gate and normalisation derivatives.
+ * Both are deterministic (no atomics in any sum).
  *
  *  q, k, v, z, beta, A, initial_state, cu_seqlens, cu_seqlens_host, N,
  *  total_T, H, d_k, d_v, dt, scale: as kda_prefill (the forward's inputs)
@@ -345,10 +355,13 @@ KDA_API int kda_backward(const void* q, const void* k, const void* v, const void
                          float* dq, float* dk, float* dv, float* dz, float* dbeta, float* dA,
                          float* dS0, void* workspace, size_t workspace_bytes, void* stream);
 
-/* kda_backward_workspace_bytes -- the workspace kda_backward needs: the
- * forward prefill's workspace and outputs, the chunk-start states, a 64-state
- * scratch per (sequence, head), the column partials and per-token dA shares
- * (0 for invalid sizes). */
+/* kda_backward_workspace_bytes -- the workspace kda_backward needs, for
+ * either form: the forward prefill's workspace and outputs, the chunk-start
+ * states, then the larger of the recurrent form's scratch (64 states per
+ * (sequence, head) and the column partials) and the chunked form's chunk
+ * records (132 KB per chunk and head, at most total_T / 64 + N chunks) and
+ * dL/dS tiles (32 KB each), and the per-token dA shares (0 for invalid
+ * sizes). */
 KDA_API size_t kda_backward_workspace_bytes(int32_t N, int32_t total_T, int32_t H, int32_t d_k,
                                             int32_t d_v, kda_dtype dt);
 

@@ -23,7 +23,7 @@ NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC]
 SOURCES = ["kda_api.cpp", "kda_recurrent.cu", "kda_state_io.cu", "kda_prefill_sm103.cu",
            "kda_noalloc.cu", "kda_short_conv.cu",
-           "kda_backward.cu"]
+           "kda_backward.cu", "kda_bwd_chunked.cu"]
 
 
 def _nvcc() -> str:

@@ -422,12 +422,22 @@ int kda_decode_step_conv(const void* q, const void* k, const void* v, const void
 // Backward workspace, in order: the workspace of the checkpointed prefill
 // that provides the chunk-start states (first, so that kda_workspace_status
 // reads its status word), that prefill's output o (not used), the checkpoint
-// pool (at most floor(total_T / 64) states), the per-pair scratch, the
-// per-CTA column partials and the per-token dA shares.
+// pool (at most floor(total_T / 64) states), one area used by whichever
+// backward runs -- the recurrent one's per-pair scratch and per-CTA column
+// partials, or the chunked one's chunk records, per-chunk dL/dS tiles and
+// chunk map (at most total_T / 64 + N chunks) -- and the per-token dA shares.
 struct BackwardLayout {
-    size_t prefill, o, pool, scratch, part, dA_tok;
-    size_t total() const { return prefill + o + pool + scratch + part + dA_tok; }
+    size_t prefill, o, pool, scratch, part, records, dsl, map, dA_tok;
+    size_t area() const {
+        const size_t rec = scratch + part, chk = records + dsl + map;
+        return rec > chk ? rec : chk;
+    }
+    size_t total() const { return prefill + o + pool + area() + dA_tok; }
 };
+
+static int64_t bwd_max_chunks(int32_t N, int32_t total_T) {
+    return (int64_t)total_T / kda::kBwChunk + N;
+}
 
 static BackwardLayout backward_layout(int32_t N, int32_t total_T, int32_t H, int32_t d_k,
                                       int32_t d_v, kda_dtype dt) {
@@ -438,6 +448,13 @@ static BackwardLayout backward_layout(int32_t N, int32_t total_T, int32_t H, int
     l.pool = round_up((size_t)(total_T / kda::kBwChunk) * H * SS, 256);
     l.scratch = round_up((size_t)N * H * kda::kBwChunk * SS, 256);
     l.part = round_up((size_t)(d_v / 32) * total_T * H * (3 * d_k + 1) * sizeof(float), 256);
+    l.records = l.dsl = l.map = 0;
+    if (dt == KDA_BF16 && d_k == 128 && d_v == 128) {
+        const size_t mc = (size_t)bwd_max_chunks(N, total_T);
+        l.records = round_up(mc * H * kda::kChunkRecordBytes, 1024);
+        l.dsl = round_up(mc * H * kda::kBwdDslBytes, 1024);
+        l.map = round_up(mc * 4 * sizeof(int32_t), 256);
+    }
     l.dA_tok = round_up((size_t)total_T * H * sizeof(float), 256);
     return l;
 }
@@ -495,8 +512,74 @@ int kda_backward(const void* q, const void* k, const void* v, const void* z,
     char* ws = static_cast<char*>(workspace);
     char* ws_o = ws + wl.prefill;
     float* pool = reinterpret_cast<float*>(ws_o + wl.o);
-    // the states after every 64 tokens of each sequence, from the forward
+    char* area = ws_o + wl.o + wl.pool;
+    float* dA_tok = reinterpret_cast<float*>(area + wl.area());
     const int32_t pool_rows = total_T / kda::kBwChunk;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    // The chunked backward (bf16, d = 128, the bounded gate, sequence lengths
+    // the host has checked or the equal split): the split prefill keeps a
+    // chunk record of every chunk (its operand tiles and start state), then
+    // the reverse state chain and the chunk-parallel assembly.  Where the split kernel cannot run
+    // (its tables, or co-residency) the recurrent backward below runs instead.
+    if (dt == KDA_BF16 && d_k == 128 && d_v == 128 && total_T > 0 &&
+        (flags & KDA_FLAG_SOFTPLUS_GATE) == 0 && (cu_seqlens_host || !cu_seqlens) &&
+        wl.records > 0) {
+        const int sms = current_sm_count();
+        kda::SplitPlan plan;
+        if (split_eligible(N, H, dt, d_k, d_v, sms, &plan) &&
+            wl.prefill >= kda::split_workspace_bytes(plan)) {
+            const int64_t max_chunks = bwd_max_chunks(N, total_T);
+            uint8_t* records = reinterpret_cast<uint8_t*>(area);
+            uint8_t* dsl = records + wl.records;
+            int32_t* cmap = reinterpret_cast<int32_t*>(dsl + wl.dsl);
+            if (cudaMemsetAsync(ws, 0, kda::split_zeroed_bytes(plan), s) != cudaSuccess) {
+                return KDA_ERR_CUDA;
+            }
+            kda::ChunkedParams fp;
+            memset(&fp, 0, sizeof(fp));
+            fp.q = q; fp.k = k; fp.v = v; fp.z = z; fp.beta = beta; fp.A = A;
+            fp.initial_state = initial_state; fp.final_state = nullptr;
+            fp.cu_seqlens = cu_seqlens; fp.o = ws_o;
+            fp.status = reinterpret_cast<int32_t*>(ws);
+            fp.work_counter = reinterpret_cast<int32_t*>(ws) + 1;
+            fp.N = N; fp.total_T = total_T; fp.H = H; fp.scale = scale;
+            fp.l2norm = (flags & KDA_FLAG_L2NORM_QK) ? 1 : 0;
+            fp.ckpt_interval = 0;   // the records carry the chunk-start states
+            fp.peer_wait_polls = kPeerWaitPolls;
+            fp.records = records;
+            fp.rec_chunks = max_chunks;
+            kda::split_bind(plan, ws, &fp);
+            cudaError_t err = kda::launch_split_prefill(fp, sms, s);
+            if (err == cudaSuccess) {
+                if (cudaMemsetAsync(cmap, 0xff, (size_t)max_chunks * 4 * sizeof(int32_t), s) !=
+                    cudaSuccess) {
+                    return KDA_ERR_CUDA;
+                }
+                kda::BwdChunkedParams bp;
+                memset(&bp, 0, sizeof(bp));
+                bp.q = q; bp.k = k; bp.v = v; bp.z = z; bp.beta = beta; bp.A = A; bp.dO = dO;
+                bp.dS_final = dS_final;
+                bp.cu_seqlens = cu_seqlens; bp.records = records;
+                bp.dsl = dsl; bp.chunk_map = cmap; bp.max_chunks = (int32_t)max_chunks;
+                bp.dq = dq; bp.dk = dk; bp.dv = dv; bp.dz = dz; bp.dbeta = dbeta;
+                bp.dA_tok = dA_tok; bp.dS0 = dS0;
+                bp.status = reinterpret_cast<int32_t*>(ws);
+                bp.N = N; bp.total_T = total_T; bp.H = H; bp.scale = scale;
+                bp.l2norm = fp.l2norm;
+                err = kda::launch_bwd_chunked(bp, s);
+                if (err == cudaSuccess) {
+                    err = kda::launch_backward_dA(dA_tok, dA, total_T, H, s);
+                }
+                return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+            }
+            if (err != cudaErrorCooperativeLaunchTooLarge) {
+                return KDA_ERR_CUDA;
+            }
+        }
+    }
+
+    // the states after every 64 tokens of each sequence, from the forward
     if (pool_rows > 0) {
         const int st = kda_prefill_checkpointed(
             q, k, v, z, beta, A, initial_state, cu_seqlens, cu_seqlens_host, N, total_T, H,
@@ -512,14 +595,13 @@ int kda_backward(const void* q, const void* k, const void* v, const void* z,
     p.dq = dq; p.dk = dk; p.dv = dv; p.dz = dz; p.dbeta = dbeta; p.dA = dA; p.dS0 = dS0;
     p.pool = pool;
     p.pool_rows = pool_rows;
-    p.scratch = reinterpret_cast<float*>(ws_o + wl.o + wl.pool);
-    p.part = reinterpret_cast<float*>(ws_o + wl.o + wl.pool + wl.scratch);
-    p.dA_tok = reinterpret_cast<float*>(ws_o + wl.o + wl.pool + wl.scratch + wl.part);
+    p.scratch = reinterpret_cast<float*>(area);
+    p.part = reinterpret_cast<float*>(area + wl.scratch);
+    p.dA_tok = dA_tok;
     p.N = N; p.total_T = total_T; p.H = H; p.scale = scale;
     p.l2norm = (flags & KDA_FLAG_L2NORM_QK) ? 1 : 0;
     p.softplus_gate = (flags & KDA_FLAG_SOFTPLUS_GATE) ? 1 : 0;
-    const cudaError_t err = kda::launch_backward(p, d_k, d_v, dt == KDA_F32 ? 0 : 1,
-                                                 static_cast<cudaStream_t>(stream));
+    const cudaError_t err = kda::launch_backward(p, d_k, d_v, dt == KDA_F32 ? 0 : 1, s);
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

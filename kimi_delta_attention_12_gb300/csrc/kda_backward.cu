@@ -600,6 +600,12 @@ cudaError_t launch_dk(const BackwardParams& p, int d_v, int dtype, cudaStream_t 
 
 }  // namespace
 
+cudaError_t launch_backward_dA(const float* dA_tok, float* dA, int64_t total_T, int H,
+                               cudaStream_t stream) {
+    kda_backward_dA_kernel<<<H, 256, 0, stream>>>(dA_tok, dA, total_T, H);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_backward(const BackwardParams& p, int d_k, int d_v, int dtype,
                             cudaStream_t stream) {
     if (p.N > 0) {

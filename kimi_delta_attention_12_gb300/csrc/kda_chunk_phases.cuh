@@ -41,6 +41,7 @@ constexpr int kThreads = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNormEps = 1e-6f;
 constexpr int kStatusTimeout = 1;
+constexpr int kStatusRecords = 2;   // more chunks than the chunk records hold
 
 // ---- shared memory map of a chunk's intra work (byte offsets from a 1024-aligned base) ----
 // Region 1 (48 KB): raw q, k, z tiles.
@@ -83,6 +84,17 @@ constexpr uint32_t HO_AQK = 49152;   // Aqk   bf16 [64 r][64 i]
 constexpr uint32_t HO_TM = 57344;    // Tm    bf16 [64 r][64 i]
 constexpr uint32_t HO_GAM = 65536;   // Gamma_C fp32 [128]
 constexpr uint32_t HO_BYTES = 66048; // multiple of 256
+
+// A chunk record (the training backward keeps one per (chunk, head)): the
+// published tiles above, then K+ and the two matrices of the UT transform
+// that the gradient assembly needs.  Every tile starts on a 1024-byte
+// boundary, so a byte copy of it into 1024-aligned shared memory is a valid
+// 128B-swizzled operand.
+constexpr uint32_t REC_KP = 66560;    // K+    bf16 [128 c][64 i]
+constexpr uint32_t REC_G = 82944;     // Gkk   bf16 [64 r][64 i]: <k_r e^{gamma_r - gamma_i}, k_i>, i < r
+constexpr uint32_t REC_MINV = 91136;  // (I + Akk)^-1 bf16 [64 r][64 i] (lower, unit diagonal)
+constexpr uint32_t REC_S0 = 99328;    // the chunk's start state S, bf16, per v-half [128 c][64 v]
+constexpr uint32_t REC_BYTES = 132096; // multiple of 1024
 
 // TMEM columns
 constexpr uint32_t TM_S = 0;      // S^T  [128 j lanes][128 c]
@@ -549,7 +561,10 @@ __device__ __forceinline__ void phase_state_to_tmem(const Ctx& x) {
 // S^T (TMEM, fp32) -> bf16 at TC_SB, and S^T *= Gamma in the same pass (the
 // next chunk's products read the bf16 copy of the undecayed state and
 // accumulate onto the decayed one); all 16 warps, 32 c each.  No barrier.
-__device__ __forceinline__ void phase_state_to_tmem_decay(const Ctx& x, const float* gam) {
+// With `dump` (global memory) the bf16 state also goes there as an operand
+// tile S [c][v]: v-half v / 64 at 16384 (v / 64), row c, 128-byte swizzle.
+__device__ __forceinline__ void phase_state_to_tmem_decay(const Ctx& x, const float* gam,
+                                                          uint8_t* dump = nullptr) {
     const int cb = 32 * x.sub;
     const uint32_t taddr = x.tbase + x.lane_base + TC_S + cb;
     uint32_t r0[16], r1[16];
@@ -563,6 +578,17 @@ __device__ __forceinline__ void phase_state_to_tmem_decay(const Ctx& x, const fl
         w[8 + i] = pack_bf16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
     }
     tmem_st16(x.tbase + x.lane_base + TC_SB + cb / 2, w);
+    if (dump) {
+        const int v = 32 * x.qd + x.lane;
+        uint8_t* half = dump + (v >> 6) * 16384;
+        const uint32_t vb = 2 * (v & 63);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const uint32_t pr = w[i >> 1];
+            *reinterpret_cast<uint16_t*>(half + sw128(cb + i, vb)) =
+                (i & 1) ? (uint16_t)(pr >> 16) : (uint16_t)(pr & 0xffffu);
+        }
+    }
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         r0[i] = __float_as_uint(__uint_as_float(r0[i]) * gam[cb + i]);

@@ -122,6 +122,9 @@ struct BackwardParams {
 };
 cudaError_t launch_backward(const BackwardParams& p, int d_k, int d_v, int dtype,
                             cudaStream_t stream);
+// dA[h] = the sum over tokens of dA_tok[t][h] (fixed order).
+cudaError_t launch_backward_dA(const float* dA_tok, float* dA, int64_t total_T, int H,
+                               cudaStream_t stream);
 
 // Launches the recurrent kernel for (d_k, d_v) in {32, 64, 128}^2 and
 // dtype (0 = fp32, 1 = bf16).  Returns a cudaError_t.

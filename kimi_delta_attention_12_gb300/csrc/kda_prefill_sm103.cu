@@ -409,14 +409,6 @@ __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes,
-                                          uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-            "r"(smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
 
 // Sequence and batch tables, built by every CTA at start.
 struct SplitMeta {
@@ -424,7 +416,17 @@ struct SplitMeta {
     float eA[kSplitMaxHeads];            // e^{A_h} log2(e)
     int32_t task0[kSplitMaxBatches + 1]; // first task of each batch
     int32_t g0[kSplitMaxBatches + 1];    // first consumer-stream index of each batch
+    int32_t ch0[kSplitMaxSeqs + 1];      // chunk records only: first chunk of each sequence
+    uint8_t* rec;                        // the chunk records, or null (none, or too few)
 };
+
+static_assert(REC_BYTES == kChunkRecordBytes, "chunk record size");
+
+// The chunk record of chunk c of sequence n, head h.
+__device__ __forceinline__ uint8_t* chunk_record(const SplitMeta& m, const ChunkedParams& p,
+                                                 int n, int c, int h) {
+    return m.rec + ((size_t)(m.ch0[n] + c) * p.H + h) * REC_BYTES;
+}
 
 // Length of sequence n from the clamped starts (never negative).
 __device__ __forceinline__ int32_t split_len(const SplitMeta& m, int n) {
@@ -548,6 +550,40 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
         }
         meta.task0[b + 1] = maxc * (u1 - u0);
         meta.g0[b + 1] = maxc;
+    }
+    if (tid == 0 && !p.records) {
+        meta.rec = nullptr;
+    }
+    if (p.records && (tid >> 5) == 1) {   // chunk bases of the sequences (one warp)
+        const int l = tid & 31;
+        const int per = (p.N + 31) >> 5;
+        const int n0 = min(l * per, p.N), n1 = min(n0 + per, p.N);
+        int32_t a = 0;
+        for (int n = n0; n < n1; ++n) {
+            a += (split_len(meta, n) + C - 1) / C;
+        }
+        int32_t incl = a;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int32_t t = __shfl_up_sync(0xffffffffu, incl, off);
+            if (l >= off) {
+                incl += t;
+            }
+        }
+        int32_t run = incl - a;
+        for (int n = n0; n < n1; ++n) {
+            meta.ch0[n] = run;
+            run += (split_len(meta, n) + C - 1) / C;
+        }
+        if (l == 31) {
+            meta.ch0[p.N] = incl;
+            // more chunks than the records hold (only a cu_seqlens the host has
+            // not checked): an error, and the chunks go through the ring
+            meta.rec = incl <= p.rec_chunks ? p.records : nullptr;
+            if (!meta.rec) {
+                atomicCAS(p.status, 0, kStatusRecords);
+            }
+        }
     }
     __syncthreads();
     if (tid < 32) {  // exclusive prefix sums over the batches (one warp)
@@ -676,7 +712,10 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 const uint32_t b = (cnt + c) & 1;
                 uint8_t* buf = sm + b * CB_BYTES;
                 mbar_arrive_expect_tx(&bar_full[b], HO_BYTES);
-                bulk_load(buf, p.handoff + (size_t)slot * HO_BYTES, HO_BYTES, &bar_full[b]);
+                bulk_load(buf,
+                          meta.rec ? chunk_record(meta, p, n, c, h)
+                                    : p.handoff + (size_t)slot * HO_BYTES,
+                          HO_BYTES, &bar_full[b]);
                 fetched = c + 1;
                 return true;
             };
@@ -714,9 +753,10 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                         record_timeout(p.status, &abort_flag, 714);
                     }
                 }
-                // S^T -> bf16 operand; S^T *= Gamma of chunk 0
+                // S^T -> bf16 operand (and chunk 0's record); S^T *= Gamma of chunk 0
                 phase_state_to_tmem_decay(
-                    x, reinterpret_cast<const float*>(sm + tiles(cnt & 1, 0).gam));
+                    x, reinterpret_cast<const float*>(sm + tiles(cnt & 1, 0).gam),
+                    meta.rec ? chunk_record(meta, p, n, 0, h) + REC_S0 : nullptr);
                 cta_sync_tc();
             }
             uint32_t ob[8];   // the last chunk's O^T as bf16 pairs, stored one chunk later
@@ -812,7 +852,8 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 if (c + 1 < nch) {
                     phase_state_to_tmem_decay(
                         x, reinterpret_cast<const float*>(
-                               sm + tiles((cnt + c + 1) & 1, 0).gam));
+                               sm + tiles((cnt + c + 1) & 1, 0).gam),
+                        meta.rec ? chunk_record(meta, p, n, c + 1, h) + REC_S0 : nullptr);
                 }
                 cta_sync_tc();
                 if (c + 1 == nch) {   // the last chunk's o
@@ -918,7 +959,9 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 const int tn = next_task(t + P, nt);
                 const bool has_next = tn < total;
                 const int32_t slot = cur.i * p.ring + cur.g % p.ring;
-                uint8_t* pub = p.handoff + (size_t)slot * HO_BYTES;
+                uint8_t* rec =
+                    meta.rec ? chunk_record(meta, p, cur.unit / H, cur.c, cur.h) : nullptr;
+                uint8_t* pub = rec ? rec : p.handoff + (size_t)slot * HO_BYTES;
                 float* s_beta = reinterpret_cast<float*>(sm + P_BETA) + (j & 1) * 64;
                 uint8_t* kp = sm + P_KP + (j & 1) * 16384;
                 // K+ and beta buffer j & 1 are free once B finished task j - 2
@@ -969,8 +1012,8 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                     record_timeout(p.status, &abort_flag, 969);
                 }
                 // the operand tiles
-                a_operands_block(sm, c, 2 * hb, al0, kp, pub);
-                a_operands_block(sm, c, 2 * hb + 1, al1, kp, pub);
+                a_operands_block(sm, c, 2 * hb, al0, kp, pub, rec);
+                a_operands_block(sm, c, 2 * hb + 1, al1, kp, pub, rec);
                 fence_proxy_async();
                 tc_fence_before();
                 const bool stop = group_sync_or(kBarA, abort_flag != 0);
@@ -1016,7 +1059,9 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 SplitTask nt;
                 const int tn = next_task(t + P, nt);
                 const int32_t slot = cur.i * p.ring + cur.g % p.ring;
-                uint8_t* pub = p.handoff + (size_t)slot * HO_BYTES;
+                uint8_t* rec =
+                    meta.rec ? chunk_record(meta, p, cur.unit / H, cur.c, cur.h) : nullptr;
+                uint8_t* pub = rec ? rec : p.handoff + (size_t)slot * HO_BYTES;
                 const float* s_beta = reinterpret_cast<const float*>(sm + P_BETA) + (j & 1) * 64;
                 // task j's Gram products: issued here once A has written their
                 // operands (the accumulator is free: this group read the last one)
@@ -1033,13 +1078,13 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                     record_timeout(p.status, &abort_flag, 1033);
                 }
                 tc_fence_after();
-                b_gram_epilogue(sm, x.tbase, x.warp, x.lane, lw >> 2, s_beta, pub);
+                b_gram_epilogue(sm, x.tbase, x.warp, x.lane, lw >> 2, s_beta, pub, rec);
                 tc_fence_before();
                 const bool stop = group_sync_or(kBarB, abort_flag != 0);
                 if (stop) {
                     break;
                 }
-                b_solve(sm, lt, lw, x.lane, s_beta, pub);
+                b_solve(sm, lt, lw, x.lane, s_beta, pub, rec);
                 fence_proxy_async();
                 tc_fence_before();
                 group_sync(kBarB);
@@ -1098,8 +1143,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-bool make_map(CUtensorMap* map, const void* base, int total_T, int H, int box_c,
-              CUtensorMapSwizzle swz) {
+bool make_map_impl(CUtensorMap* map, const void* base, int total_T, int H, int box_c,
+                   CUtensorMapSwizzle swz) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) {
         return false;
@@ -1113,13 +1158,22 @@ bool make_map(CUtensorMap* map, const void* base, int total_T, int H, int box_c,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+}  // namespace
+
+bool make_token_map(CUtensorMap* map, const void* base, int total_T, int H, bool swizzled) {
+    return make_map_impl(map, base, total_T, H, swizzled ? 64 : 128,
+                         swizzled ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+namespace {
+
 bool make_args(ChunkedArgs* args, const ChunkedParams& p) {
     memset(args, 0, sizeof(*args));
     args->p = p;
-    return make_map(&args->tm_q, p.q, p.total_T, p.H, 128, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-           make_map(&args->tm_k, p.k, p.total_T, p.H, 128, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-           make_map(&args->tm_z, p.z, p.total_T, p.H, 128, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-           make_map(&args->tm_v, p.v, p.total_T, p.H, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+    return make_token_map(&args->tm_q, p.q, p.total_T, p.H, false) &&
+           make_token_map(&args->tm_k, p.k, p.total_T, p.H, false) &&
+           make_token_map(&args->tm_z, p.z, p.total_T, p.H, false) &&
+           make_token_map(&args->tm_v, p.v, p.total_T, p.H, true);
 }
 
 }  // namespace

@@ -151,11 +151,12 @@ __device__ __forceinline__ void a_gate_block(uint8_t* sm, int c, int ab, int L, 
 // The operand tiles of token block ab for channel c, from its alpha (al, 16
 // tokens) and the raw q, k in shared memory: X~ and K~^(a) (all a >= ab) for
 // the Gram, K+ into kp, and Q+, Kend (and, for block 0, Gamma_C) straight
-// into the published chunk at pub.  The arithmetic is that of
-// chunk::phase_prologue_operands.
+// into the published chunk at pub; with `rec` (a chunk record, which pub
+// then points into) K+ goes to its REC_KP tile as well.  The arithmetic is
+// that of chunk::phase_prologue_operands.
 __device__ __forceinline__ void a_operands_block(uint8_t* sm, int c, int ab,
                                                  const float (&al)[16], uint8_t* kp,
-                                                 uint8_t* pub) {
+                                                 uint8_t* pub, uint8_t* rec) {
     const float* s_invq = reinterpret_cast<const float*>(sm + P_INVQ);
     const float* s_invk = reinterpret_cast<const float*>(sm + P_INVK);
     const float* s_tot = reinterpret_cast<const float*>(sm + P_TOT);
@@ -218,6 +219,9 @@ __device__ __forceinline__ void a_operands_block(uint8_t* sm, int c, int ab,
 #pragma unroll
     for (int rr = 0; rr < 16; ++rr) v[rr] *= eRa;
     chunk::store_row16(kp, c, 32 * ab, v);
+    if (rec) {
+        chunk::store_row16(rec + chunk::REC_KP, c, 32 * ab, v);
+    }
     // key side with the end-of-block reference: k e^{rho_{a+1} - gamma_r} <= 1
 #pragma unroll
     for (int rr = 0; rr < 16; ++rr) G[rr] *= kh[rr];
@@ -260,9 +264,11 @@ __device__ __forceinline__ void a_issue_gram(uint32_t smem_base, uint32_t tbase)
 // Gram epilogue: warp quadrant q holds the rows of block a = 3 - q (lanes
 // 0-15 the q rows, 16-31 the k rows); part (0, 1) selects 32 of the block's
 // 64 key tokens.  Aqk (bf16, i <= r) goes to the published chunk, Akk (fp32,
-// beta_r-scaled, i < r) to P_AKK.  No barrier.
+// beta_r-scaled, i < r) to P_AKK and, with a chunk record `rec`, the key
+// Gram without beta (bf16, i < r) to its REC_G tile.  No barrier.
 __device__ __forceinline__ void b_gram_epilogue(uint8_t* sm, uint32_t tbase, int warp, int lane,
-                                                int part, const float* s_beta, uint8_t* pub) {
+                                                int part, const float* s_beta, uint8_t* pub,
+                                                uint8_t* rec) {
     const int q = warp & 3;
     const int a = 3 - q;
     const int row = 16 * a + (lane & 15);
@@ -297,16 +303,34 @@ __device__ __forceinline__ void b_gram_epilogue(uint8_t* sm, uint32_t tbase, int
             akk[k] = i0 + k < row ? br * __uint_as_float(r0[k]) : 0.0f;
             akk[16 + k] = i0 + 16 + k < row ? br * __uint_as_float(r1[k]) : 0.0f;
         }
+        if (rec) {
+            uint32_t w[16];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int i = i0 + 2 * k;
+                w[k] = chunk::pack_bf16x2(i < row ? __uint_as_float(r0[2 * k]) : 0.0f,
+                                          i + 1 < row ? __uint_as_float(r0[2 * k + 1]) : 0.0f);
+                w[8 + k] = chunk::pack_bf16x2(i + 16 < row ? __uint_as_float(r1[2 * k]) : 0.0f,
+                                              i + 17 < row ? __uint_as_float(r1[2 * k + 1]) : 0.0f);
+            }
+            uint8_t* t = rec + chunk::REC_G;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                *reinterpret_cast<uint4*>(t + sw128(row, 2 * i0 + 16 * k)) =
+                    make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+            }
+        }
     }
 }
 
 // UT solve Tm = (I + Akk)^-1 Diag(beta) on group B (lt = thread, lw = warp in
 // the group; named barrier kBarB), Tm -> P_TM (over Akk) and the published
-// chunk.  The blocked forward substitution of chunk::phase_solve.  The group
+// chunk; with a chunk record `rec`, (I + Akk)^-1 itself to its REC_MINV
+// tile.  The blocked forward substitution of chunk::phase_solve.  The group
 // must have synchronised after the Gram epilogue; ends with Tm written (no
 // barrier after it).
 __device__ __forceinline__ void b_solve(uint8_t* sm, int lt, int lw, int lane,
-                                        const float* s_beta, uint8_t* pub) {
+                                        const float* s_beta, uint8_t* pub, uint8_t* rec) {
     float* Lm = reinterpret_cast<float*>(sm + P_AKK);
     float* Nm = reinterpret_cast<float*>(sm + P_NMAT);
     if (lt < 64) {
@@ -350,16 +374,22 @@ __device__ __forceinline__ void b_solve(uint8_t* sm, int lt, int lw, int lane,
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         const int r = (lt >> 3) + 32 * h, i0 = (lt & 7) * 8;
-        float v[8];
+        float v[8], nv[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const int i = i0 + u;
-            v[u] = i <= r ? Nm[r * 65 + i] * s_beta[i] : 0.0f;
+            nv[u] = i <= r ? Nm[r * 65 + i] : 0.0f;
+            v[u] = nv[u] * s_beta[i];
         }
         const uint4 w = make_uint4(chunk::pack_bf16x2(v[0], v[1]), chunk::pack_bf16x2(v[2], v[3]),
                                    chunk::pack_bf16x2(v[4], v[5]), chunk::pack_bf16x2(v[6], v[7]));
         *reinterpret_cast<uint4*>(sm + P_TM + sw128(r, 2 * i0)) = w;
         *reinterpret_cast<uint4*>(pub + chunk::HO_TM + sw128(r, 2 * i0)) = w;
+        if (rec) {
+            *reinterpret_cast<uint4*>(rec + chunk::REC_MINV + sw128(r, 2 * i0)) =
+                make_uint4(chunk::pack_bf16x2(nv[0], nv[1]), chunk::pack_bf16x2(nv[2], nv[3]),
+                           chunk::pack_bf16x2(nv[4], nv[5]), chunk::pack_bf16x2(nv[6], nv[7]));
+        }
     }
 }
 
