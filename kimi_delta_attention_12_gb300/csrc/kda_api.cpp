@@ -540,7 +540,7 @@ int kda_backward(const void* q, const void* k, const void* v, const void* z,
             memset(&fp, 0, sizeof(fp));
             fp.q = q; fp.k = k; fp.v = v; fp.z = z; fp.beta = beta; fp.A = A;
             fp.initial_state = initial_state; fp.final_state = nullptr;
-            fp.cu_seqlens = cu_seqlens; fp.o = ws_o;
+            fp.cu_seqlens = cu_seqlens; fp.o = nullptr;   // (the forward's o is not needed)
             fp.status = reinterpret_cast<int32_t*>(ws);
             fp.work_counter = reinterpret_cast<int32_t*>(ws) + 1;
             fp.N = N; fp.total_T = total_T; fp.H = H; fp.scale = scale;

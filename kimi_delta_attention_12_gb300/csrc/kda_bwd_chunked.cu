@@ -707,8 +707,10 @@ kda_bwd_assemble_kernel(const __grid_constant__ BwdArgs args) {
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
             const int t = 16 * pb + j;
+            // (the forward's arithmetic: sigmoid(x) = 1 / (1 + 2^{-x log2 e}))
             const float xv = eA * bf16_at(sm + AS_Z + t * 256 + 2 * cc);
-            const float g = t < L ? -5.0f * kLog2e / (1.0f + expf(-xv)) : 0.0f;
+            const float sg = rcp_approx(1.0f + exp2_approx(-kLog2e * xv));
+            const float g = t < L ? -5.0f * kLog2e * sg : 0.0f;
             run += g;
             g2[j] = run;
         }
@@ -944,7 +946,7 @@ kda_bwd_assemble_kernel(const __grid_constant__ BwdArgs args) {
             float dxx = 0.f;
             if (t < L) {
                 const float zx = __uint_as_float(xr[j]);
-                const float sg = 1.0f / (1.0f + expf(-zx));
+                const float sg = rcp_approx(1.0f + exp2_approx(-kLog2e * zx));
                 const float dx = run * (-5.0f) * sg * (1.0f - sg);
                 p.dz[((size_t)(t0 + t) * H + h) * D + cc] = dx * eA;
                 dxx = dx * zx;

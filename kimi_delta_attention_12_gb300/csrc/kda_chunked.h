@@ -22,7 +22,7 @@ struct ChunkedParams {
     const float* initial_state;
     float* final_state;
     const int32_t* cu_seqlens;   // device, [N+1]; null -> equal split
-    void* o;
+    void* o;                     // (split mode: null skips the output stores)
     int32_t* status;             // device status word (workspace)
     int32_t* work_counter;       // device work counter (workspace)
     const int32_t* schedule;     // optional device list of unit ids (workspace), or null

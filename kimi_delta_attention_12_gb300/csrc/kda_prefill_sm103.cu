@@ -778,7 +778,7 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                     }
                 }
                 // the previous chunk's o while the tensor core works
-                if (c > 0) {
+                if (c > 0 && o_g) {
                     phase_ot_store(x, o_g, bos + (c - 1) * C, C, h, H, ob);
                 }
                 if (!mbar_wait(&bar_u, ph_u, &abort_flag)) {
@@ -856,7 +856,7 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                         meta.rec ? chunk_record(meta, p, n, c + 1, h) + REC_S0 : nullptr);
                 }
                 cta_sync_tc();
-                if (c + 1 == nch) {   // the last chunk's o
+                if (c + 1 == nch && o_g) {   // the last chunk's o
                     phase_ot_store(x, o_g, bos + c * C, len - c * C, h, H, ob);
                 }
             }

@@ -4,7 +4,8 @@ the chunk-parallel gradient assembly) against the fp64 reverse-mode oracle,
 through the C ABI.
 
 Every gradient is compared by relative Frobenius error (the bf16 bar,
-2e-2): dq, dk, dv, dz, dbeta, dS0 and, per head, dA by its relative error.
+2e-2): dq, dk, dv, dz, dbeta, dS0, and per head dA through its per-token
+shares (metrics.check_dA).
 The cases cover ragged last chunks, empty and one-token sequences, several
 full chunks, a nonzero initial state and dL/dS_T, scale != 1, no in-op
 normalisation, and the equal split without cu_seqlens; every call's status
@@ -15,7 +16,7 @@ import torch
 
 import kimi_delta_attention_12_gb300 as kda
 from kimi_delta_attention_12_gb300 import inputs
-from metrics import BF16_TOL, rel_fro
+from metrics import BF16_TOL, check_dA, rel_fro
 
 pytestmark = pytest.mark.gpu
 
@@ -47,24 +48,22 @@ def _run(oracle_mod, lens, H, seed, with_state=True, equal_split=False, **flags)
     assert kda.workspace_status(ws) == kda.KDA_OK
     ref = oracle_mod.kda_reference_backward(x.q, x.k, x.v, x.z, x.beta, x.A, x.initial_state,
                                             x.cu_seqlens, dO, dSf, **flags)
-    return g, ref
+    return g, ref, x
 
 
-def _check(g, ref, H):
+def _check(g, ref, x):
     for key in KEYS:
         assert torch.isfinite(g[key]).all(), key
         assert rel_fro(g[key], ref[key]) <= BF16_TOL, (key, rel_fro(g[key], ref[key]))
-    for h in range(H):
-        got, want = float(g["dA"][h]), float(ref["dA"][h])
-        assert abs(got - want) <= BF16_TOL * abs(want), (h, got, want)
+    check_dA(g["dA"], g["dz"], ref["dA"], ref["dz"], x.z)
 
 
 def test_chunked_backward_varlen_ragged(oracle_mod):
     """Five sequences: ragged (200 = 3 x 64 + 8), empty, exactly one chunk,
     two chunks and a tail of 2, and a single token; three heads, scale 0.9."""
     lens = [200, 0, 64, 130, 1]
-    g, ref = _run(oracle_mod, lens, 3, seed=500, scale=0.9)
-    _check(g, ref, 3)
+    g, ref, x = _run(oracle_mod, lens, 3, seed=500, scale=0.9)
+    _check(g, ref, x)
     # the empty sequence's dL/dS0 is its dL/dS_T
     _, dSf = inputs.make_upstream_grads(sum(lens), len(lens), 3, 128, 128, torch.bfloat16,
                                         seed=500)
@@ -73,21 +72,21 @@ def test_chunked_backward_varlen_ragged(oracle_mod):
 
 def test_chunked_backward_no_norm_no_state(oracle_mod):
     """No in-op normalisation, no initial state, no dL/dS_T."""
-    g, ref = _run(oracle_mod, [96, 33], 2, seed=510, with_state=False, l2norm=False)
-    _check(g, ref, 2)
+    g, ref, x = _run(oracle_mod, [96, 33], 2, seed=510, with_state=False, l2norm=False)
+    _check(g, ref, x)
 
 
 def test_chunked_backward_equal_split_long(oracle_mod):
     """One sequence of 1,000 tokens (16 chunks, ragged tail) without
     cu_seqlens: the chain carries dL/dS through every chunk."""
-    g, ref = _run(oracle_mod, [1000], 2, seed=520, equal_split=True)
-    _check(g, ref, 2)
+    g, ref, x = _run(oracle_mod, [1000], 2, seed=520, equal_split=True)
+    _check(g, ref, x)
 
 
 def test_chunked_backward_short_single_chunk(oracle_mod):
     """A sequence shorter than one chunk, a single head."""
-    g, ref = _run(oracle_mod, [37], 1, seed=530)
-    _check(g, ref, 1)
+    g, ref, x = _run(oracle_mod, [37], 1, seed=530)
+    _check(g, ref, x)
 
 
 def test_chunked_backward_deterministic(oracle_mod):
