@@ -745,11 +745,31 @@ def measure_conv(sets, ws, o, S, cu_host, B, H, T, d, args, stream):
     check_status(kda, ws, "prefill after the short convolutions")
     conv_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     both_ms = statistics.mean(e[0].elapsed_time(e[2]) for e in ev)
+    # the same, fused: kda_prefill_conv (the convolutions inside the split
+    # kernel's producers, the convolved tensors never in HBM)
+    wsf = torch.empty(kda.prefill_conv_workspace_bytes(B, B * T, H, d, d, torch.bfloat16),
+                      dtype=torch.uint8, device=dev)
+    fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    for i in range(args.warmup + n):
+        x = sets[i % len(sets)]
+        if i >= args.warmup:
+            fev[i - args.warmup][0].record(stream)
+        kda.kda_prefill_conv(x.q, x.k, x.v, x.z, x.beta, x.A, w, cs_in, cs_out,
+                             cu_seqlens=x.cu_seqlens, cu_seqlens_host=cu_host, silu=True,
+                             o=o, final_state=S, workspace=wsf)
+        if i >= args.warmup:
+            fev[i - args.warmup][1].record(stream)
+    torch.cuda.synchronize()
+    check_status(kda, wsf, "prefill with the short convolutions fused")
+    fused_ms = statistics.mean(a.elapsed_time(b) for a, b in fev)
     byts = conv_algorithmic(B, H, T, d, W)
     return {"kernel": "short_conv_kernel", "width": W, "silu": True, "kernel_ms": conv_ms,
             "algorithmic_bytes": byts, "achieved_gbs": byts / (conv_ms / 1e3) / 1e9,
             "conv_then_prefill_ms": both_ms,
-            "conv_then_prefill_tokens_per_s": B * T / (both_ms / 1e3)}
+            "conv_then_prefill_tokens_per_s": B * T / (both_ms / 1e3),
+            "fused_conv_prefill_ms": fused_ms,
+            "fused_conv_prefill_tokens_per_s": B * T / (fused_ms / 1e3)}
 
 
 def measure_softplus(sets, ws, o, S, cu_host, args, stream):

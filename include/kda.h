@@ -269,6 +269,49 @@ KDA_API int kda_short_conv(const void* q, const void* k, const void* v, const fl
                            void* q_out, void* k_out, void* v_out, void* stream);
 
 /*
+ * kda_prefill_conv -- kda_short_conv followed by kda_prefill on its outputs,
+ * in one call: the same o, final state and conv_state_out, bit for bit.
+ *
+ * With bf16, d_k = d_v = 128 and K3's gate, where the split kernel runs with
+ * all (sequence, head) pairs in one batch (at most one pair per four SMs: 38
+ * on 152 SMs), the convolutions are fused into it: its producers
+ * convolve each chunk's q and k in shared memory before the Q/K
+ * normalisation and its v into the chunk's operand tiles, with the same
+ * arithmetic and rounding to bf16 as kda_short_conv, and the consumers write
+ * each sequence's final conv state; the convolved tensors never go to HBM.
+ * Otherwise (more pairs, whose producers have no slack for the extra work;
+ * other dtypes or sizes; the softplus gate; KDA_FLAG_RECURRENT; a device
+ * that cannot take the split kernel's cooperative launch) the call runs
+ * kda_short_conv into the workspace and then kda_prefill.
+ *
+ *  q, k, v, z, beta, A, initial_state, cu_seqlens, cu_seqlens_host, N,
+ *  total_T, H, d_k, d_v, dt, scale, o, final_state: as kda_prefill (q, k, v
+ *                  the convolutions' inputs)
+ *  flags           kda_prefill's flags, plus KDA_FLAG_CONV_SILU
+ *  conv_w, conv_state_in, conv_state_out, W: as kda_short_conv
+ *  workspace       kda_prefill_conv_workspace_bytes(...) bytes, 256-byte
+ *                  aligned; it begins with the prefill's workspace, so
+ *                  kda_workspace_status on it reports the split kernel's
+ *                  bounded waits
+ * Errors: as kda_prefill and kda_short_conv.
+ */
+KDA_API int kda_prefill_conv(const void* q, const void* k, const void* v, const void* z,
+                             const void* beta, const float* A, const float* initial_state,
+                             const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                             int32_t N, int32_t total_T, int32_t H, int32_t d_k, int32_t d_v,
+                             kda_dtype dt, float scale, uint32_t flags,
+                             const float* conv_w, const void* conv_state_in,
+                             void* conv_state_out, int32_t W, void* o, float* final_state,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* kda_prefill_conv_workspace_bytes -- the workspace kda_prefill_conv needs:
+ * the prefill's (with the larger slots of the fused kernel, which also carry
+ * the convolved v of each chunk) and room for the convolved q, k, v of the
+ * two-pass path (0 for invalid sizes). */
+KDA_API size_t kda_prefill_conv_workspace_bytes(int32_t N, int32_t total_T, int32_t H,
+                                                int32_t d_k, int32_t d_v, kda_dtype dt);
+
+/*
  * kda_decode_step_conv -- kda_decode_step preceded by the token's short
  * convolutions of q, k and v (as kda_short_conv, width W) with the conv
  * state kept persistent beside the recurrent state (section 1, decode

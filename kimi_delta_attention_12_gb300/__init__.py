@@ -51,6 +51,7 @@ EXPORTED_SYMBOLS = (
     "kda_prefill_noalloc", "kda_prefill_checkpointed", "kda_checkpoint_count",
     "kda_short_conv", "kda_decode_step_conv", "kda_decode_conv_workspace_bytes",
     "kda_backward", "kda_backward_workspace_bytes", "kda_prefill_noalloc_status",
+    "kda_prefill_conv", "kda_prefill_conv_workspace_bytes",
 )
 
 _lock = threading.Lock()
@@ -118,6 +119,13 @@ def lib() -> ctypes.CDLL:
                                        vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
             L.kda_backward_workspace_bytes.restype = sz
             L.kda_backward_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, ctypes.c_int]
+            L.kda_prefill_conv.restype = ctypes.c_int
+            L.kda_prefill_conv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                           i32, i32, i32, i32, i32, ctypes.c_int, f32, u32,
+                                           vp, vp, vp, i32, vp, vp, vp, sz, vp]
+            L.kda_prefill_conv_workspace_bytes.restype = sz
+            L.kda_prefill_conv_workspace_bytes.argtypes = [i32, i32, i32, i32, i32,
+                                                           ctypes.c_int]
             L.kda_checkpoint_count.restype = ctypes.c_int64
             L.kda_checkpoint_count.argtypes = [vp, i32, i32, i32]
             _lib = L
@@ -495,6 +503,78 @@ def kda_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: torch.Ten
     if st != KDA_OK:
         raise KDAError(st, "kda_backward")
     return g
+
+
+def prefill_conv_workspace_bytes(N: int, total_T: int, H: int, d_k: int, d_v: int,
+                                 dtype: torch.dtype) -> int:
+    return int(lib().kda_prefill_conv_workspace_bytes(N, total_T, H, d_k, d_v,
+                                                      _dtype_code(dtype)))
+
+
+def kda_prefill_conv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, z: torch.Tensor,
+                     beta: torch.Tensor, A: torch.Tensor, conv_w: torch.Tensor,
+                     conv_state_in: Optional[torch.Tensor] = None,
+                     conv_state_out: Optional[torch.Tensor] = None,
+                     initial_state: Optional[torch.Tensor] = None,
+                     cu_seqlens: Optional[torch.Tensor] = None,
+                     cu_seqlens_host: Optional[torch.Tensor] = None,
+                     scale: float = 1.0, l2norm: bool = True, silu: bool = False,
+                     softplus_gate: bool = False, output_final_state: bool = True,
+                     o: Optional[torch.Tensor] = None,
+                     final_state: Optional[torch.Tensor] = None,
+                     workspace: Optional[torch.Tensor] = None,
+                     stream: Optional[torch.cuda.Stream] = None, extra_flags: int = 0
+                     ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """kda_short_conv followed by kda_prefill on its outputs, in one call
+    (kda_prefill_conv in include/kda.h: the convolutions fused into the split
+    kernel where it runs).  Packed layouts as kda_prefill; conv_w
+    [H, 2 d_k + d_v, W] fp32; conv states [N, H, W-1, 2 d_k + d_v] in the
+    dtype of q (the final ones go to conv_state_out when given).  Returns
+    (o, final_state)."""
+    N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    total_T, H, d_k = q.shape
+    d_v = v.shape[-1]
+    dt = q.dtype
+    for t in (k, v, z, beta):
+        if t.dtype != dt:
+            raise TypeError("q, k, v, z and beta must share one dtype")
+    _check_cuda(q, k, v, z, beta, A, conv_w, conv_state_in, conv_state_out, initial_state,
+                cu_seqlens, o, final_state)
+    if conv_w.dtype != torch.float32 or conv_w.dim() != 3:
+        raise TypeError("conv_w must be a float32 [H, 2 d_k + d_v, W] tensor")
+    W = conv_w.shape[-1]
+    Cc = 2 * d_k + d_v
+    for name, t in (("k", k), ("z", z)):
+        _expect(t, (total_T, H, d_k), name)
+    _expect(v, (total_T, H, d_v), "v")
+    _expect(beta, (total_T, H), "beta")
+    _expect(A, (H,), "A", torch.float32)
+    _expect(conv_w, (H, Cc, W), "conv_w", torch.float32)
+    _expect(conv_state_in, (N, H, W - 1, Cc), "conv_state_in", dt)
+    _expect(conv_state_out, (N, H, W - 1, Cc), "conv_state_out", dt)
+    _expect(cu_seqlens, (N + 1,), "cu_seqlens", torch.int32)
+    _expect(initial_state, (N, H, d_k, d_v), "initial_state", torch.float32)
+    _expect(o, (total_T, H, d_v), "o", dt)
+    _expect(final_state, (N, H, d_k, d_v), "final_state", torch.float32)
+    if o is None:
+        o = torch.empty(total_T, H, d_v, dtype=dt, device=q.device)
+    if final_state is None and output_final_state:
+        final_state = torch.empty(N, H, d_k, d_v, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(prefill_conv_workspace_bytes(N, total_T, H, d_k, d_v, dt),
+                                dtype=torch.uint8, device=q.device)
+    host_cu = None if cu_seqlens_host is None else cu_seqlens_host.to(torch.int32).contiguous()
+    host_ptr = None if host_cu is None else ctypes.c_void_p(host_cu.data_ptr())
+    flags = ((KDA_FLAG_L2NORM_QK if l2norm else 0) | (KDA_FLAG_CONV_SILU if silu else 0)
+             | (KDA_FLAG_SOFTPLUS_GATE if softplus_gate else 0) | int(extra_flags))
+    st = lib().kda_prefill_conv(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A), _ptr(initial_state),
+        _ptr(cu_seqlens), host_ptr, N, total_T, H, d_k, d_v, _dtype_code(dt), float(scale),
+        flags, _ptr(conv_w), _ptr(conv_state_in), _ptr(conv_state_out), W, _ptr(o),
+        _ptr(final_state), _ptr(workspace), _nbytes(workspace), _stream_ptr(stream))
+    if st != KDA_OK:
+        raise KDAError(st, "kda_prefill_conv")
+    return o, final_state
 
 
 def kda_state_io(op: int, dst: torch.Tensor, src: Optional[torch.Tensor] = None,

@@ -314,6 +314,120 @@ int kda_short_conv(const void* q, const void* k, const void* v, const float* con
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+// kda_prefill_conv's workspace: the prefill's part (large enough for the split
+// kernel with the convolutions fused, whose slots also carry the convolved v)
+// then, for the two-pass path, the convolved q, k, v.
+static size_t prefill_conv_part(int32_t N, int32_t total_T, int32_t H, int32_t d_k, int32_t d_v,
+                                kda_dtype dt) {
+    size_t part = kda_prefill_workspace_bytes(N, total_T, H, d_k, d_v, dt);
+    kda::SplitPlan plan;
+    if (N > 0 && H > 0 && total_T > 0 &&
+        split_eligible(N, H, dt, d_k, d_v, current_sm_count(), &plan)) {
+        const size_t fused = kda::split_workspace_bytes(plan, true);
+        part = fused > part ? fused : part;
+    }
+    return round_up(part, 256);
+}
+
+size_t kda_prefill_conv_workspace_bytes(int32_t N, int32_t total_T, int32_t H, int32_t d_k,
+                                        int32_t d_v, kda_dtype dt) {
+    if (N < 1 || H < 1 || total_T < 0 || !supported_dim(d_k) || !supported_dim(d_v) ||
+        (dt != KDA_F32 && dt != KDA_BF16)) {
+        return 0;
+    }
+    const size_t eb = elem_bytes(dt);
+    return prefill_conv_part(N, total_T, H, d_k, d_v, dt) +
+           2 * round_up((size_t)total_T * H * d_k * eb, 256) +
+           round_up((size_t)total_T * H * d_v * eb, 256);
+}
+
+int kda_prefill_conv(const void* q, const void* k, const void* v, const void* z,
+                     const void* beta, const float* A, const float* initial_state,
+                     const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                     int32_t N, int32_t total_T, int32_t H, int32_t d_k, int32_t d_v,
+                     kda_dtype dt, float scale, uint32_t flags,
+                     const float* conv_w, const void* conv_state_in, void* conv_state_out,
+                     int32_t W, void* o, float* final_state,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+    if (dt != KDA_F32 && dt != KDA_BF16) return KDA_ERR_UNSUPPORTED;
+    if (!supported_dim(d_k) || !supported_dim(d_v)) return KDA_ERR_UNSUPPORTED;
+    if (N < 1 || H < 1 || total_T < 0) return KDA_ERR_INVALID_ARG;
+    if ((flags & ~(kKnownFlags | (uint32_t)KDA_FLAG_CONV_SILU)) != 0) return KDA_ERR_INVALID_ARG;
+    if (W < 1 || W > kMaxConvWidth || !conv_w) return KDA_ERR_INVALID_ARG;
+    if (!isfinite(scale) || !A) return KDA_ERR_INVALID_ARG;
+    if (total_T > 0 && (!q || !k || !v || !z || !beta || !o)) return KDA_ERR_INVALID_ARG;
+    if (!cu_seqlens && total_T % N != 0) return KDA_ERR_INVALID_ARG;
+    if (cu_seqlens_host) {
+        if (cu_seqlens_host[0] != 0 || cu_seqlens_host[N] != total_T) return KDA_ERR_INVALID_ARG;
+        for (int32_t n = 0; n < N; ++n) {
+            if (cu_seqlens_host[n + 1] < cu_seqlens_host[n]) return KDA_ERR_INVALID_ARG;
+        }
+    }
+    const size_t need = kda_prefill_conv_workspace_bytes(N, total_T, H, d_k, d_v, dt);
+    if (!workspace || workspace_bytes < need) return KDA_ERR_WORKSPACE;
+    const size_t eb = elem_bytes(dt);
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(z, 16) ||
+        !aligned(o, 16) || !aligned(beta, eb) || !aligned(A, 4) ||
+        !aligned(initial_state, 16) || !aligned(final_state, 16) || !aligned(conv_w, 16) ||
+        !aligned(conv_state_in, 16) || !aligned(conv_state_out, 16) ||
+        !aligned(cu_seqlens, 4) || !aligned(workspace, 256)) {
+        return KDA_ERR_ALIGNMENT;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* ws = static_cast<char*>(workspace);
+    const size_t part = prefill_conv_part(N, total_T, H, d_k, d_v, dt);
+    const uint32_t pflags = flags & ~(uint32_t)KDA_FLAG_CONV_SILU;
+
+    // fused: the split kernel convolves q, k and v in its producers -- where
+    // its units fit one batch.  The convolutions add about a third to a
+    // producer's work per chunk; with one batch the producers have that slack
+    // (4K workload, 32 heads: 0.243 ms fused against 0.275 ms for the two
+    // passes, 0.228 ms prefill alone), with several batches they are the
+    // binding resource and the two passes are faster (96 heads x 65,536
+    // tokens, two batches: 10.8 against 8.45 ms).
+    kda::SplitPlan plan;
+    const int sms = (dt == KDA_BF16 && d_k == 128 && d_v == 128 && total_T > 0 &&
+                     (flags & (kFlagRecurrent | KDA_FLAG_SOFTPLUS_GATE)) == 0)
+                        ? current_sm_count()
+                        : 0;
+    if (sms > 0 && split_eligible(N, H, dt, d_k, d_v, sms, &plan) && plan.batches == 1 &&
+        part >= kda::split_workspace_bytes(plan, true)) {
+        if (cudaMemsetAsync(ws, 0, kda::split_zeroed_bytes(plan), s) != cudaSuccess) {
+            return KDA_ERR_CUDA;
+        }
+        kda::ChunkedParams p;
+        memset(&p, 0, sizeof(p));
+        p.q = q; p.k = k; p.v = v; p.z = z; p.beta = beta; p.A = A;
+        p.initial_state = initial_state; p.final_state = final_state;
+        p.cu_seqlens = cu_seqlens; p.o = o;
+        p.status = reinterpret_cast<int32_t*>(ws);
+        p.work_counter = reinterpret_cast<int32_t*>(ws) + 1;
+        p.N = N; p.total_T = total_T; p.H = H; p.scale = scale;
+        p.l2norm = (flags & KDA_FLAG_L2NORM_QK) ? 1 : 0;
+        p.peer_wait_polls = (flags & KDA_FLAG_SHORT_PEER_WAITS) ? 1u : kPeerWaitPolls;
+        p.conv_w = conv_w;
+        p.conv_state_in = W > 1 ? conv_state_in : nullptr;
+        p.conv_state_out = W > 1 ? conv_state_out : nullptr;
+        p.conv_W = W;
+        p.conv_silu = (flags & KDA_FLAG_CONV_SILU) ? 1 : 0;
+        kda::split_bind(plan, ws, &p);
+        const cudaError_t err = kda::launch_split_prefill(p, sms, s);
+        if (err == cudaSuccess) return KDA_OK;
+        if (err != cudaErrorCooperativeLaunchTooLarge) return KDA_ERR_CUDA;
+    }
+    // two passes: the convolutions into the workspace, then the prefill on them
+    char* qc = ws + part;
+    char* kc = qc + round_up((size_t)total_T * H * d_k * eb, 256);
+    char* vc = kc + round_up((size_t)total_T * H * d_k * eb, 256);
+    int st = kda_short_conv(q, k, v, conv_w, conv_state_in, conv_state_out, cu_seqlens,
+                            cu_seqlens_host, N, total_T, H, d_k, d_v, W, dt,
+                            flags & (uint32_t)KDA_FLAG_CONV_SILU, qc, kc, vc, stream);
+    if (st != KDA_OK) return st;
+    return kda_prefill(qc, kc, vc, z, beta, A, initial_state, cu_seqlens, cu_seqlens_host, N,
+                       total_T, H, d_k, d_v, dt, scale, pflags, o, final_state, ws, part,
+                       stream);
+}
+
 // One of the three convolved tensors in the decode-conv workspace.
 static size_t conv_ws_part(int32_t B, int32_t H, int32_t d, kda_dtype dt) {
     return round_up((size_t)B * H * d * elem_bytes(dt), 256);

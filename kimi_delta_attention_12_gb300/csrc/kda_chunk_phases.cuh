@@ -84,6 +84,11 @@ constexpr uint32_t HO_AQK = 49152;   // Aqk   bf16 [64 r][64 i]
 constexpr uint32_t HO_TM = 57344;    // Tm    bf16 [64 r][64 i]
 constexpr uint32_t HO_GAM = 65536;   // Gamma_C fp32 [128]
 constexpr uint32_t HO_BYTES = 66048; // multiple of 256
+// With the short convolutions fused (split kernel), a slot also carries the
+// chunk's convolved v tile, as the consumer's V operand (two halves
+// [64 i][64 j], 128-byte swizzle: the layout TMA gives the plain kernel).
+constexpr uint32_t HO_V = 66560;
+constexpr uint32_t HO_BYTES_CONV = HO_V + 16384;
 
 // A chunk record (the training backward keeps one per (chunk, head)): the
 // published tiles above, then K+ and the two matrices of the UT transform

@@ -54,6 +54,15 @@ struct ChunkedParams {
     // copies it from there
     uint8_t* records;
     int64_t rec_chunks;          // records per head the buffer holds (a bound on the chunk count)
+    // split mode only: the short convolutions of q, k, v fused in (conv_w
+    // non-null), as kda_short_conv computes them: taps [H][2*128+128][W] fp32,
+    // conv states [N][H][W-1][384] bf16 in (or null: zeros) and out (or null);
+    // the slots then carry the convolved v tile (HO_BYTES_CONV each)
+    const float* conv_w;
+    const void* conv_state_in;
+    void* conv_state_out;
+    int32_t conv_W;
+    int32_t conv_silu;
 };
 constexpr uint32_t kChunkRecordBytes = 132096;  // one chunk record (REC_BYTES)
 
@@ -122,7 +131,8 @@ size_t min_prefill_workspace_bytes(int32_t N, int32_t H);
 // not run in split mode.
 bool split_plan(int32_t N, int32_t H, int num_sms, SplitPlan* plan);
 size_t split_zeroed_bytes(const SplitPlan& plan);
-size_t split_workspace_bytes(const SplitPlan& plan);
+// (conv: slots with the convolved v tile, for the fused short convolutions)
+size_t split_workspace_bytes(const SplitPlan& plan, bool conv = false);
 // Points p's split-mode fields into a workspace laid out for plan.
 void split_bind(const SplitPlan& plan, void* workspace, ChunkedParams* p);
 // TMA map of a packed [total_T][H][128] bf16 tensor with a box of 64 tokens

@@ -472,6 +472,29 @@ __device__ __forceinline__ bool decode_task(const SplitMeta& m, const ChunkedPar
     return c * C < len;
 }
 
+// With the convolutions fused: the conv state after sequence n of head h --
+// its last W-1 inputs of q, k and v, oldest first (from its conv state in
+// where the sequence is shorter), as kda_short_conv writes it.  Every thread
+// of the CTA; no barrier.
+__device__ __forceinline__ void conv_state_tail(const ChunkedParams& p, int n, int h,
+                                                int64_t bos, int64_t eos) {
+    const int R = p.conv_W - 1;
+    const __nv_bfloat16* st_in = static_cast<const __nv_bfloat16*>(p.conv_state_in);
+    __nv_bfloat16* st_out = static_cast<__nv_bfloat16*>(p.conv_state_out);
+    for (int e = threadIdx.x; e < R * 3 * D; e += blockDim.x) {
+        const int r = e / (3 * D), ch = e - r * 3 * D;
+        const int64_t tau = eos - R + r;
+        __nv_bfloat16 val = __float2bfloat16_rn(0.0f);
+        if (tau >= bos) {
+            const void* x = ch < D ? p.q : ch < 2 * D ? p.k : p.v;
+            val = static_cast<const __nv_bfloat16*>(x)[((size_t)tau * p.H + h) * D + (ch & (D - 1))];
+        } else if (st_in) {
+            val = st_in[(((size_t)n * p.H + h) * R + (tau - bos + R)) * 3 * D + ch];
+        }
+        st_out[(((size_t)n * p.H + h) * R + r) * 3 * D + ch] = val;
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
     const ChunkedParams& p = args.p;
@@ -629,10 +652,14 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
         // ------------------------------------------------------------ consumer
         const int i = blockIdx.x;
         __nv_bfloat16* o_g = static_cast<__nv_bfloat16*>(p.o);
+        // with the convolutions fused, the convolved v tile comes in the slot
+        // (buffers of HO_BYTES_CONV) and the v ring is not used
+        const bool conv = p.conv_w != nullptr;
+        const uint32_t cbuf = conv ? HO_BYTES_CONV : CB_BYTES;
         auto tiles = [&](uint32_t b, uint32_t vb) -> StateTiles {
-            const uint32_t cb = b * CB_BYTES;
+            const uint32_t cb = b * cbuf;
             return StateTiles{cb + HO_WT, cb + HO_QP,  cb + HO_KE, cb + HO_AQK, cb + HO_TM,
-                              cb + HO_GAM, CB_VRING + vb * 16384, 0, 0};
+                              cb + HO_GAM, conv ? cb + HO_V : CB_VRING + vb * 16384, 0, 0};
         };
         uint32_t cnt = 0;  // buffer fills so far (buffer = count & 1, parity = (count >> 1) & 1)
         uint32_t vcnt = 0; // v tiles loaded so far (ring slot = count % 4, parity = (count / 4) & 1)
@@ -672,6 +699,9 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
             // thread 0: load chunk c's v tile (an input, independent of the
             // producers) into the v ring, up to kVRing chunks ahead of use
             auto issue_v = [&](int c) {
+                if (conv) {
+                    return;
+                }
                 const uint32_t vb = (vcnt + c) % kVRing;
                 uint8_t* vbuf = sm + CB_VRING + vb * 16384;
                 mbar_arrive_expect_tx(&bar_v[vb], 16384);
@@ -681,6 +711,9 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
             };
             // thread 0: wait for chunk c's v tile
             auto wait_v = [&](int c) -> bool {
+                if (conv) {
+                    return true;
+                }
                 const uint32_t r = vcnt + c;
                 const bool ok = mbar_wait(&bar_v[r % kVRing], (r / kVRing) & 1, &abort_flag);
                 if (ok) {
@@ -710,12 +743,13 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 fence_proxy_async_global();
                 fence_proxy_async();
                 const uint32_t b = (cnt + c) & 1;
-                uint8_t* buf = sm + b * CB_BYTES;
-                mbar_arrive_expect_tx(&bar_full[b], HO_BYTES);
+                uint8_t* buf = sm + b * cbuf;
+                const uint32_t bytes = conv ? HO_BYTES_CONV : HO_BYTES;
+                mbar_arrive_expect_tx(&bar_full[b], bytes);
                 bulk_load(buf,
                           meta.rec ? chunk_record(meta, p, n, c, h)
-                                    : p.handoff + (size_t)slot * HO_BYTES,
-                          HO_BYTES, &bar_full[b]);
+                                    : p.handoff + (size_t)slot * bytes,
+                          bytes, &bar_full[b]);
                 fetched = c + 1;
                 return true;
             };
@@ -880,6 +914,9 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
             if (!abort_flag && p.final_state) {
                 store_state(x, p.final_state + state_off);
             }
+            if (conv && p.conv_state_out) {
+                conv_state_tail(p, n, h, meta.cu[n], meta.cu[n] + len);
+            }
             cta_sync_tc();
             if (tid == 32 && !abort_flag) {  // skip the stream positions this unit leaves unused
                 st_release(p.cons_done + i, meta.g0[bt + 1]);
@@ -903,6 +940,17 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
         // still holds, so that no wait depends on an unraised flag.
         using namespace split;
         const int total = meta.task0[p.n_batches];
+        const bool conv = p.conv_w != nullptr;
+        const uint32_t slot_bytes = conv ? HO_BYTES_CONV : HO_BYTES;
+        ConvSrc cs;
+        cs.w = p.conv_w;
+        cs.q = static_cast<const __nv_bfloat16*>(p.q);
+        cs.k = static_cast<const __nv_bfloat16*>(p.k);
+        cs.v = static_cast<const __nv_bfloat16*>(p.v);
+        cs.st = static_cast<const __nv_bfloat16*>(p.conv_state_in);
+        cs.R = p.conv_W - 1;
+        cs.silu = p.conv_silu != 0;
+        cs.H = H;
         const int P = (int)gridDim.x - p.n_cons;
         const bool grpA = x.warp < 8;
         const int lt = grpA ? tid : tid - 256;   // thread within the group
@@ -961,7 +1009,7 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 const int32_t slot = cur.i * p.ring + cur.g % p.ring;
                 uint8_t* rec =
                     meta.rec ? chunk_record(meta, p, cur.unit / H, cur.c, cur.h) : nullptr;
-                uint8_t* pub = rec ? rec : p.handoff + (size_t)slot * HO_BYTES;
+                uint8_t* pub = rec ? rec : p.handoff + (size_t)slot * slot_bytes;
                 float* s_beta = reinterpret_cast<float*>(sm + P_BETA) + (j & 1) * 64;
                 uint8_t* kp = sm + P_KP + (j & 1) * 16384;
                 // K+ and beta buffer j & 1 are free once B finished task j - 2
@@ -980,6 +1028,13 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                     beta_r = (has_next && lt < nt.L)
                                  ? __bfloat162float(beta_g[(size_t)(nt.t0 + lt) * H + nt.h])
                                  : 0.0f;
+                }
+                if (conv) {   // the short convolutions of q and k, in place
+                    float hq[3], hk[3];
+                    a_conv_halo(sm, lt, cs, cur.t0, cur.c, cur.unit / H, cur.h, hq, hk);
+                    group_sync(kBarA);
+                    a_conv_apply(sm, lt, cs, cur.h, hq, hk);
+                    group_sync(kBarA);
                 }
                 a_norms(sm, lw, x.lane, cur.L, p.scale, p.l2norm);
                 float al0[16], al1[16];
@@ -1061,7 +1116,7 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 const int32_t slot = cur.i * p.ring + cur.g % p.ring;
                 uint8_t* rec =
                     meta.rec ? chunk_record(meta, p, cur.unit / H, cur.c, cur.h) : nullptr;
-                uint8_t* pub = rec ? rec : p.handoff + (size_t)slot * HO_BYTES;
+                uint8_t* pub = rec ? rec : p.handoff + (size_t)slot * slot_bytes;
                 const float* s_beta = reinterpret_cast<const float*>(sm + P_BETA) + (j & 1) * 64;
                 // task j's Gram products: issued here once A has written their
                 // operands (the accumulator is free: this group read the last one)
@@ -1073,6 +1128,12 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                     } else {
                         record_timeout(p.status, &abort_flag, 1029);
                     }
+                }
+                if (conv) {
+                    // the slot is free once A has written task j's operands into
+                    // it; the convolved v goes in while the Gram products run
+                    group_sync(kBarB);
+                    b_conv_v(pub + HO_V, lt, cs, cur.t0, cur.L, cur.c, cur.unit / H, cur.h);
                 }
                 if (!mbar_wait(&bar_gram, j & 1, &abort_flag)) {
                     record_timeout(p.status, &abort_flag, 1033);
@@ -1227,8 +1288,9 @@ size_t split_zeroed_bytes(const SplitPlan& plan) {
     return split_done_offset(plan) + round256((size_t)plan.consumers * sizeof(int32_t));
 }
 
-size_t split_workspace_bytes(const SplitPlan& plan) {
-    return split_zeroed_bytes(plan) + (size_t)plan.consumers * plan.ring * HO_BYTES;
+size_t split_workspace_bytes(const SplitPlan& plan, bool conv) {
+    return split_zeroed_bytes(plan) +
+           (size_t)plan.consumers * plan.ring * (conv ? HO_BYTES_CONV : HO_BYTES);
 }
 
 void split_bind(const SplitPlan& plan, void* workspace, ChunkedParams* p) {

@@ -25,6 +25,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "kda_conv_math.cuh"
 #include "kda_internal.h"
 #include "kda_seqlens.cuh"
 
@@ -80,17 +81,6 @@ struct VecTraits<__nv_bfloat16> {
     }
 };
 
-// y * sigmoid(y) = y / (1 + 2^(-y log2 e)), without a branch: below about
-// y = -88 the power overflows to +inf and the approximate reciprocal returns
-// +0, the function's limit (the exact value is below 1e-36 there).  The
-// approximate ex2 and rcp keep the relative error near 1e-7, far below the
-// bf16 rounding of the stored result.
-__device__ __forceinline__ float silu_f(float y) {
-    float e, r;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-1.4426950408889634f * y));
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
-    return y * r;
-}
 
 __device__ __forceinline__ uint2 ld8(const void* base, size_t elem_off, int eb) {
     return __ldg(reinterpret_cast<const uint2*>(static_cast<const char*>(base) +

@@ -31,6 +31,7 @@
 #include <stdint.h>
 
 #include "kda_chunk_phases.cuh"
+#include "kda_conv_math.cuh"
 #include "sm103_ptx.cuh"
 
 namespace kda {
@@ -82,6 +83,162 @@ __device__ __forceinline__ bool group_sync_or(int id, bool pred) {
         : "r"((uint32_t)pred), "r"(id), "r"(kGroupThreads)
         : "memory");
     return r != 0;
+}
+
+// ---------------------------------------------------------- fused convolutions
+// The short convolutions of kda_short_conv.cu (conv_step, the same arithmetic
+// and rounding), fused into the producers: q and k in place in the raw tiles
+// (group A, before the norms), v into the published chunk (group B).  The
+// inputs before a chunk's first token are the previous chunk's last ones, or
+// for a sequence's first chunk the rows of its conv state (zeros without one).
+
+// Where a convolution finds a chunk's inputs.
+struct ConvSrc {
+    const float* w;            // taps [H][384][W] fp32
+    const __nv_bfloat16* q;    // raw inputs [total_T][H][128]
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* v;
+    const __nv_bfloat16* st;   // conv states in [N][H][W-1][384], or null
+    int R;                     // W - 1 (0 .. 3)
+    bool silu;
+    int H;
+};
+
+// Taps of channel ch (of the 384) of head h: w[0 .. R] (the rest 0).
+__device__ __forceinline__ void conv_taps(const ConvSrc& cs, int h, int ch, float (&w)[4]) {
+    const float* src = cs.w + ((size_t)h * 384 + ch) * (cs.R + 1);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w[j] = j <= cs.R ? __ldg(src + j) : 0.0f;
+}
+
+// Group A, step 1 (before a barrier of the group): thread lt takes channel
+// c = lt % 128 of tokens 32 hb .. 32 hb + 31 (hb = lt / 128) of q and k; its
+// window gets the R inputs before its first token (win[3 - R + r]: the r-th of
+// them, oldest first), read before the thread ahead of it overwrites them.
+__device__ __forceinline__ void a_conv_halo(const uint8_t* sm, int lt, const ConvSrc& cs,
+                                            int64_t t0, int chunk, int n, int h,
+                                            float (&wq)[3], float (&wk)[3]) {
+    const int c = lt & (D - 1), hb = lt >> 7;
+#pragma unroll
+    for (int r = 0; r < 3; ++r) {
+        wq[r] = 0.0f;
+        wk[r] = 0.0f;
+    }
+    for (int r = 0; r < cs.R; ++r) {
+        const int rel = 32 * hb - cs.R + r;   // token within the chunk (< 0: before it)
+        float a = 0.0f, b = 0.0f;
+        if (rel >= 0) {
+            a = __bfloat162float(
+                *reinterpret_cast<const __nv_bfloat16*>(sm + P_RAWQ + rel * 256 + 2 * c));
+            b = __bfloat162float(
+                *reinterpret_cast<const __nv_bfloat16*>(sm + P_RAWK + rel * 256 + 2 * c));
+        } else if (chunk > 0) {
+            const size_t o = ((size_t)(t0 + rel) * cs.H + h) * D + c;
+            a = __bfloat162float(cs.q[o]);
+            b = __bfloat162float(cs.k[o]);
+        } else if (cs.st) {
+            const size_t o = (((size_t)n * cs.H + h) * cs.R + (rel + cs.R)) * 384 + c;
+            a = __bfloat162float(cs.st[o]);
+            b = __bfloat162float(cs.st[o + D]);
+        }
+        wq[3 - cs.R + r] = a;
+        wk[3 - cs.R + r] = b;
+    }
+}
+
+template <int R>
+__device__ __forceinline__ void a_conv_rows(uint8_t* sm, int c, int hb, const float (&tq)[4],
+                                            const float (&tk)[4], float (&wq)[3],
+                                            float (&wk)[3], bool silu) {
+    __nv_bfloat16* rq = reinterpret_cast<__nv_bfloat16*>(sm + P_RAWQ);
+    __nv_bfloat16* rk = reinterpret_cast<__nv_bfloat16*>(sm + P_RAWK);
+#pragma unroll 4
+    for (int j = 0; j < 32; ++j) {
+        const int e = (32 * hb + j) * D + c;
+        const float xq = __bfloat162float(rq[e]), xk = __bfloat162float(rk[e]);
+        rq[e] = __float2bfloat16_rn(conv_step<R>(tq, wq, xq, silu));
+        rk[e] = __float2bfloat16_rn(conv_step<R>(tk, wk, xk, silu));
+        wq[0] = wq[1]; wq[1] = wq[2]; wq[2] = xq;
+        wk[0] = wk[1]; wk[1] = wk[2]; wk[2] = xk;
+    }
+}
+
+// Group A, step 2 (after that barrier): the thread's 32 outputs of q and k,
+// rounded to bf16, over its inputs in the raw tiles.  No barrier.
+__device__ __forceinline__ void a_conv_apply(uint8_t* sm, int lt, const ConvSrc& cs, int h,
+                                             float (&wq)[3], float (&wk)[3]) {
+    const int c = lt & (D - 1), hb = lt >> 7;
+    float tq[4], tk[4];
+    conv_taps(cs, h, c, tq);
+    conv_taps(cs, h, D + c, tk);
+    switch (cs.R) {
+        case 0: a_conv_rows<0>(sm, c, hb, tq, tk, wq, wk, cs.silu); break;
+        case 1: a_conv_rows<1>(sm, c, hb, tq, tk, wq, wk, cs.silu); break;
+        case 2: a_conv_rows<2>(sm, c, hb, tq, tk, wq, wk, cs.silu); break;
+        default: a_conv_rows<3>(sm, c, hb, tq, tk, wq, wk, cs.silu); break;
+    }
+}
+
+template <int R>
+__device__ __forceinline__ void b_conv_rows(uint8_t* tile, int c0, int tq, const float (&t0w)[4],
+                                            const float (&t1w)[4], const uint32_t (&raw)[19],
+                                            bool silu) {
+    float w0[3], w1[3];
+#pragma unroll
+    for (int r = 0; r < 3; ++r) {   // raw[r]: the input 3 - r tokens before the first
+        w0[r] = chunk::bf16lo(raw[r]);
+        w1[r] = chunk::bf16hi(raw[r]);
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const float x0 = chunk::bf16lo(raw[3 + j]), x1 = chunk::bf16hi(raw[3 + j]);
+        const uint32_t y = chunk::pack_bf16x2(conv_step<R>(t0w, w0, x0, silu),
+                                              conv_step<R>(t1w, w1, x1, silu));
+        *reinterpret_cast<uint32_t*>(tile + (c0 >> 6) * 8192 + sw128(16 * tq + j, 2 * (c0 & 63))) =
+            y;
+        w0[0] = w0[1]; w0[1] = w0[2]; w0[2] = x0;
+        w1[0] = w1[1]; w1[1] = w1[2]; w1[2] = x1;
+    }
+}
+
+// Group B: the chunk's convolved v into the published chunk's V tile (the
+// consumer's operand layout).  Thread lt: channels c0 = 2 (lt % 64), c0 + 1
+// of tokens 16 tq .. 16 tq + 15 (tq = lt / 64); its 16 + 3 input pairs are
+// loaded first, all in flight at once.  Tokens at or past the chunk's end L
+// read as 0.  No barrier.
+__device__ __forceinline__ void b_conv_v(uint8_t* tile, int lt, const ConvSrc& cs, int64_t t0,
+                                         int L, int chunk, int n, int h) {
+    const int c0 = 2 * (lt & 63), tq = lt >> 6;
+    uint32_t raw[19];
+#pragma unroll
+    for (int i = 0; i < 19; ++i) {
+        const int rel = 16 * tq - 3 + i;   // token within the chunk
+        uint32_t val = 0u;
+        if (rel >= 0) {
+            if (rel < L) {
+                val = __ldg(reinterpret_cast<const uint32_t*>(
+                    cs.v + ((size_t)(t0 + rel) * cs.H + h) * D + c0));
+            }
+        } else if (rel >= -cs.R) {
+            if (chunk > 0) {
+                val = __ldg(reinterpret_cast<const uint32_t*>(
+                    cs.v + ((size_t)(t0 + rel) * cs.H + h) * D + c0));
+            } else if (cs.st) {
+                val = __ldg(reinterpret_cast<const uint32_t*>(
+                    cs.st + (((size_t)n * cs.H + h) * cs.R + (rel + cs.R)) * 384 + 2 * D + c0));
+            }
+        }
+        raw[i] = val;
+    }
+    float t0w[4], t1w[4];
+    conv_taps(cs, h, 2 * D + c0, t0w);
+    conv_taps(cs, h, 2 * D + c0 + 1, t1w);
+    switch (cs.R) {
+        case 0: b_conv_rows<0>(tile, c0, tq, t0w, t1w, raw, cs.silu); break;
+        case 1: b_conv_rows<1>(tile, c0, tq, t0w, t1w, raw, cs.silu); break;
+        case 2: b_conv_rows<2>(tile, c0, tq, t0w, t1w, raw, cs.silu); break;
+        default: b_conv_rows<3>(tile, c0, tq, t0w, t1w, raw, cs.silu); break;
+    }
 }
 
 // ---------------------------------------------------------------- group A
