@@ -410,26 +410,34 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 }
 
 
-// Sequence and batch tables, built by every CTA at start.
-struct SplitMeta {
+// Sequence and batch tables, built by every CTA at start (the chunk bases
+// only with chunk records).
+template <bool kRec>
+struct SplitMetaT {
     int32_t cu[kSplitMaxSeqs + 1];       // token start of each sequence (and total_T)
     float eA[kSplitMaxHeads];            // e^{A_h} log2(e)
     int32_t task0[kSplitMaxBatches + 1]; // first task of each batch
     int32_t g0[kSplitMaxBatches + 1];    // first consumer-stream index of each batch
-    int32_t ch0[kSplitMaxSeqs + 1];      // chunk records only: first chunk of each sequence
+    int32_t ch0[kRec ? kSplitMaxSeqs + 1 : 1];   // records: first chunk of each sequence
     uint8_t* rec;                        // the chunk records, or null (none, or too few)
 };
 
 static_assert(REC_BYTES == kChunkRecordBytes, "chunk record size");
 
-// The chunk record of chunk c of sequence n, head h.
-__device__ __forceinline__ uint8_t* chunk_record(const SplitMeta& m, const ChunkedParams& p,
-                                                 int n, int c, int h) {
-    return m.rec + ((size_t)(m.ch0[n] + c) * p.H + h) * REC_BYTES;
+// The chunk record of chunk c of sequence n, head h (none without records).
+template <bool kRec>
+__device__ __forceinline__ uint8_t* chunk_record(const SplitMetaT<kRec>& m,
+                                                 const ChunkedParams& p, int n, int c, int h) {
+    if constexpr (kRec) {
+        return m.rec + ((size_t)(m.ch0[n] + c) * p.H + h) * REC_BYTES;
+    } else {
+        return nullptr;
+    }
 }
 
 // Length of sequence n from the clamped starts (never negative).
-__device__ __forceinline__ int32_t split_len(const SplitMeta& m, int n) {
+template <bool kRec>
+__device__ __forceinline__ int32_t split_len(const SplitMetaT<kRec>& m, int n) {
     return max(0, m.cu[n + 1] - m.cu[n]);
 }
 
@@ -443,7 +451,8 @@ struct SplitTask {
 };
 
 // False if the task's chunk lies past the end of its sequence.
-__device__ __forceinline__ bool decode_task(const SplitMeta& m, const ChunkedParams& p, int t,
+template <bool kRec>
+__device__ __forceinline__ bool decode_task(const SplitMetaT<kRec>& m, const ChunkedParams& p, int t,
                                             SplitTask& o) {
     int lo = 0, hi = p.n_batches - 1;
     while (lo < hi) {
@@ -495,12 +504,23 @@ __device__ __forceinline__ void conv_state_tail(const ChunkedParams& p, int n, i
     }
 }
 
+// kMode: kSplitPlain, kSplitRecords (chunk records for the training
+// backward) or kSplitConv (the short convolutions fused in); one
+// instantiation each, so that the plain prefill carries none of the others'
+// code.
+constexpr int kSplitPlain = 0;
+constexpr int kSplitRecords = 1;
+constexpr int kSplitConv = 2;
+
+template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
+    constexpr bool kRec = kMode == kSplitRecords;
+    constexpr bool kConv = kMode == kSplitConv;
     const ChunkedParams& p = args.p;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
-    __shared__ SplitMeta meta;
+    __shared__ SplitMetaT<kRec> meta;
     __shared__ uint64_t bar_raw;       // producer: raw q, k, z landed
     __shared__ uint64_t bar_mma;       // producer: MMA group done
     __shared__ uint64_t bar_full[2];   // consumer: a buffer's slot landed
@@ -574,10 +594,10 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
         meta.task0[b + 1] = maxc * (u1 - u0);
         meta.g0[b + 1] = maxc;
     }
-    if (tid == 0 && !p.records) {
+    if (tid == 0 && !kRec) {
         meta.rec = nullptr;
     }
-    if (p.records && (tid >> 5) == 1) {   // chunk bases of the sequences (one warp)
+    if (kRec && (tid >> 5) == 1) {   // chunk bases of the sequences (one warp)
         const int l = tid & 31;
         const int per = (p.N + 31) >> 5;
         const int n0 = min(l * per, p.N), n1 = min(n0 + per, p.N);
@@ -654,8 +674,8 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
         __nv_bfloat16* o_g = static_cast<__nv_bfloat16*>(p.o);
         // with the convolutions fused, the convolved v tile comes in the slot
         // (buffers of HO_BYTES_CONV) and the v ring is not used
-        const bool conv = p.conv_w != nullptr;
-        const uint32_t cbuf = conv ? HO_BYTES_CONV : CB_BYTES;
+        constexpr bool conv = kConv;
+        constexpr uint32_t cbuf = conv ? HO_BYTES_CONV : CB_BYTES;
         auto tiles = [&](uint32_t b, uint32_t vb) -> StateTiles {
             const uint32_t cb = b * cbuf;
             return StateTiles{cb + HO_WT, cb + HO_QP,  cb + HO_KE, cb + HO_AQK, cb + HO_TM,
@@ -747,7 +767,7 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 const uint32_t bytes = conv ? HO_BYTES_CONV : HO_BYTES;
                 mbar_arrive_expect_tx(&bar_full[b], bytes);
                 bulk_load(buf,
-                          meta.rec ? chunk_record(meta, p, n, c, h)
+                          kRec && meta.rec ? chunk_record(meta, p, n, c, h)
                                     : p.handoff + (size_t)slot * bytes,
                           bytes, &bar_full[b]);
                 fetched = c + 1;
@@ -790,7 +810,7 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 // S^T -> bf16 operand (and chunk 0's record); S^T *= Gamma of chunk 0
                 phase_state_to_tmem_decay(
                     x, reinterpret_cast<const float*>(sm + tiles(cnt & 1, 0).gam),
-                    meta.rec ? chunk_record(meta, p, n, 0, h) + REC_S0 : nullptr);
+                    kRec && meta.rec ? chunk_record(meta, p, n, 0, h) + REC_S0 : nullptr);
                 cta_sync_tc();
             }
             uint32_t ob[8];   // the last chunk's O^T as bf16 pairs, stored one chunk later
@@ -887,7 +907,8 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                     phase_state_to_tmem_decay(
                         x, reinterpret_cast<const float*>(
                                sm + tiles((cnt + c + 1) & 1, 0).gam),
-                        meta.rec ? chunk_record(meta, p, n, c + 1, h) + REC_S0 : nullptr);
+                        kRec && meta.rec ? chunk_record(meta, p, n, c + 1, h) + REC_S0
+                                         : nullptr);
                 }
                 cta_sync_tc();
                 if (c + 1 == nch && o_g) {   // the last chunk's o
@@ -940,8 +961,8 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
         // still holds, so that no wait depends on an unraised flag.
         using namespace split;
         const int total = meta.task0[p.n_batches];
-        const bool conv = p.conv_w != nullptr;
-        const uint32_t slot_bytes = conv ? HO_BYTES_CONV : HO_BYTES;
+        constexpr bool conv = kConv;
+        constexpr uint32_t slot_bytes = conv ? HO_BYTES_CONV : HO_BYTES;
         ConvSrc cs;
         cs.w = p.conv_w;
         cs.q = static_cast<const __nv_bfloat16*>(p.q);
@@ -1008,7 +1029,8 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 const bool has_next = tn < total;
                 const int32_t slot = cur.i * p.ring + cur.g % p.ring;
                 uint8_t* rec =
-                    meta.rec ? chunk_record(meta, p, cur.unit / H, cur.c, cur.h) : nullptr;
+                    kRec && meta.rec ? chunk_record(meta, p, cur.unit / H, cur.c, cur.h)
+                                     : nullptr;
                 uint8_t* pub = rec ? rec : p.handoff + (size_t)slot * slot_bytes;
                 float* s_beta = reinterpret_cast<float*>(sm + P_BETA) + (j & 1) * 64;
                 uint8_t* kp = sm + P_KP + (j & 1) * 16384;
@@ -1115,7 +1137,8 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 const int tn = next_task(t + P, nt);
                 const int32_t slot = cur.i * p.ring + cur.g % p.ring;
                 uint8_t* rec =
-                    meta.rec ? chunk_record(meta, p, cur.unit / H, cur.c, cur.h) : nullptr;
+                    kRec && meta.rec ? chunk_record(meta, p, cur.unit / H, cur.c, cur.h)
+                                     : nullptr;
                 uint8_t* pub = rec ? rec : p.handoff + (size_t)slot * slot_bytes;
                 const float* s_beta = reinterpret_cast<const float*>(sm + P_BETA) + (j & 1) * 64;
                 // task j's Gram products: issued here once A has written their
@@ -1322,12 +1345,10 @@ cudaError_t launch_chunked_prefill(const ChunkedParams& p, cudaStream_t stream) 
     return cudaGetLastError();
 }
 
-cudaError_t launch_split_prefill(const ChunkedParams& p, int num_sms, cudaStream_t stream) {
-    ChunkedArgs args;
-    if (!make_args(&args, p)) {
-        return cudaErrorInvalidValue;
-    }
-    cudaError_t err = cudaFuncSetAttribute(kda_split_kernel,
+namespace {
+template <int kMode>
+cudaError_t launch_split_mode(ChunkedArgs& args, int num_sms, cudaStream_t stream) {
+    cudaError_t err = cudaFuncSetAttribute(kda_split_kernel<kMode>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)kSplitSmemBytes);
     if (err != cudaSuccess) {
@@ -1340,13 +1361,28 @@ cudaError_t launch_split_prefill(const ChunkedParams& p, int num_sms, cudaStream
     // single-pass kernel instead.  The ring flags and consumer counters were
     // zeroed by the caller on this stream.
     void* kargs[] = {&args};
-    err = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(&kda_split_kernel),
+    err = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(&kda_split_kernel<kMode>),
                                       dim3((unsigned)num_sms), dim3(kThreads), kargs,
                                       kSplitSmemBytes, stream);
     if (err != cudaSuccess) {
         cudaGetLastError();  // clear the launch error; it is returned instead
     }
     return err;
+}
+}  // namespace
+
+cudaError_t launch_split_prefill(const ChunkedParams& p, int num_sms, cudaStream_t stream) {
+    ChunkedArgs args;
+    if (!make_args(&args, p)) {
+        return cudaErrorInvalidValue;
+    }
+    if (p.records) {
+        return launch_split_mode<kSplitRecords>(args, num_sms, stream);
+    }
+    if (p.conv_w) {
+        return launch_split_mode<kSplitConv>(args, num_sms, stream);
+    }
+    return launch_split_mode<kSplitPlain>(args, num_sms, stream);
 }
 
 }  // namespace kda
