@@ -528,8 +528,7 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
     __shared__ uint64_t bar_u;         // consumer: U^T done
     __shared__ uint64_t bar_os;        // consumer: O and the state update done
     __shared__ uint64_t bar_fin;       // every MMA of this CTA done
-    __shared__ uint64_t bar_gram;      // producer: Gram products of a task done (A -> B)
-    __shared__ uint64_t bar_opready;   // producer: A wrote task j's Gram operands (A -> B)
+    __shared__ uint64_t bar_gram[2];   // producer: Gram products of task j done (buffer j & 1)
     __shared__ uint64_t bar_bdone[2];  // producer: B finished task j (K+, beta buffer j & 1 free)
     __shared__ uint64_t bar_w;         // producer: W^T of a task done
     __shared__ uint64_t bar_finb;      // producer: every MMA of group B done
@@ -556,8 +555,8 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
         mbar_init(&bar_u, 1);
         mbar_init(&bar_os, 1);
         mbar_init(&bar_fin, 1);
-        mbar_init(&bar_gram, 1);
-        mbar_init(&bar_opready, 1);
+        mbar_init(&bar_gram[0], 1);
+        mbar_init(&bar_gram[1], 1);
         mbar_init(&bar_bdone[0], 1);
         mbar_init(&bar_bdone[1], 1);
         mbar_init(&bar_w, 1);
@@ -948,13 +947,13 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
         // Producer k takes tasks k, k + P, k + 2P, ... (P producers; tasks past
         // the end of their sequence are skipped), the j-th of them through two
         // warp groups (kda_split_phases.cuh): group A (warps 0-7) runs the
-        // prologue of task j and issues its Gram products while group B (warps
-        // 8-15) finishes task j - 1 (Gram epilogue, UT solve, W).  Hand-overs,
-        // all mbarriers with one arrival: bar_opready (task j's operand tiles are
-        // written, A -> B: B issues the Gram products, so that no thread of group
-        // A stalls on the tensor core's issue queue), bar_gram (task j's Gram
-        // done: B reads it, A may overwrite the operand tiles), bar_bdone[j & 1]
-        // (B finished task j: its K+ and beta buffers are free and its slot
+        // prologue of task j and issues its Gram products into TMEM buffer
+        // j & 1 while group B (warps 8-15) finishes task j - 1 (Gram epilogue,
+        // UT solve, W) out of the other buffer.  Hand-overs, all mbarriers with
+        // one arrival: bar_gram[j & 1] (task j's Gram done: B reads it, A may
+        // overwrite the operand tiles; one barrier per buffer, so that a waiter
+        // never faces a phase two tasks ahead), bar_bdone[j & 1] (B finished
+        // task j: its TMEM buffer, K+ and beta buffers are free and its slot
         // writes done).  A thread of group A raises each slot's flag (release)
         // once both groups' writes to it are done, one task later; before
         // group A waits for a consumer to free a slot it raises the flag it
@@ -1085,7 +1084,8 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                     group_sync(kBarA);
                 }
                 // X~, K~ are free once the previous task's Gram products are done
-                if (j >= 1 && !mbar_wait(&bar_gram, (j - 1) & 1, &abort_flag)) {
+                if (j >= 1 &&
+                    !mbar_wait(&bar_gram[(j - 1) & 1], ((j - 1) >> 1) & 1, &abort_flag)) {
                     record_timeout(p.status, &abort_flag, 969);
                 }
                 // the operand tiles
@@ -1102,7 +1102,10 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                     if (has_next) {   // the raw tiles are consumed: fetch the next task's
                         issue_raw(nt);
                     }
-                    mbar_arrive(&bar_opready);   // B issues the Gram products
+                    // task j's Gram products into TMEM buffer j & 1 (free: B
+                    // finished task j - 2, waited for at the top of this task)
+                    a_issue_gram(x.smem_base, x.tbase + (j & 1) * kGramBufCols);
+                    mma_commit(&bar_gram[j & 1]);
                 }
                 raw_pending = has_next;
                 raw_par = (j + 1) & 1;
@@ -1141,28 +1144,17 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                                      : nullptr;
                 uint8_t* pub = rec ? rec : p.handoff + (size_t)slot * slot_bytes;
                 const float* s_beta = reinterpret_cast<const float*>(sm + P_BETA) + (j & 1) * 64;
-                // task j's Gram products: issued here once A has written their
-                // operands (the accumulator is free: this group read the last one)
-                if (lt == 0) {
-                    if (mbar_wait(&bar_opready, j & 1, &abort_flag)) {
-                        tc_fence_after();
-                        a_issue_gram(x.smem_base, x.tbase);
-                        mma_commit(&bar_gram);
-                    } else {
-                        record_timeout(p.status, &abort_flag, 1029);
-                    }
-                }
-                if (conv) {
-                    // the slot is free once A has written task j's operands into
-                    // it; the convolved v goes in while the Gram products run
-                    group_sync(kBarB);
-                    b_conv_v(pub + HO_V, lt, cs, cur.t0, cur.L, cur.c, cur.unit / H, cur.h);
-                }
-                if (!mbar_wait(&bar_gram, j & 1, &abort_flag)) {
+                // task j's Gram products, issued by group A once it has written
+                // their operands (the slot is then free: A checked it first)
+                const uint32_t tg = x.tbase + (j & 1) * kGramBufCols;
+                if (!mbar_wait(&bar_gram[j & 1], (j >> 1) & 1, &abort_flag)) {
                     record_timeout(p.status, &abort_flag, 1033);
                 }
+                if (conv) {   // the convolved v into the slot
+                    b_conv_v(pub + HO_V, lt, cs, cur.t0, cur.L, cur.c, cur.unit / H, cur.h);
+                }
                 tc_fence_after();
-                b_gram_epilogue(sm, x.tbase, x.warp, x.lane, lw >> 2, s_beta, pub, rec);
+                b_gram_epilogue(sm, tg, x.warp, x.lane, lw >> 2, s_beta, pub, rec);
                 tc_fence_before();
                 const bool stop = group_sync_or(kBarB, abort_flag != 0);
                 if (stop) {
@@ -1174,14 +1166,14 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 group_sync(kBarB);
                 tc_fence_after();
                 if (lt == 0) {
-                    b_issue_w(x.smem_base, x.tbase, P_KP + (j & 1) * 16384);
+                    b_issue_w(x.smem_base, tg, P_KP + (j & 1) * 16384);
                     mma_commit(&bar_w);
                 }
                 if (!mbar_wait(&bar_w, j & 1, &abort_flag)) {
                     record_timeout(p.status, &abort_flag, 1052);
                 }
                 tc_fence_after();
-                b_neg_w(x.tbase, x.warp, lw, x.lane, pub + HO_WT);
+                b_neg_w(tg, x.warp, lw, x.lane, pub + HO_WT);
                 tc_fence_before();
                 group_sync(kBarB);
                 if (lt == 0) {

@@ -10,10 +10,11 @@
 //   group B (warps 8-15): the Gram epilogue (Akk fp32 in shared memory, Aqk
 //     into the slot), the UT solve Tm = (I + Akk)^-1 Diag(beta) (Tm into the
 //     slot), W^T = K+^T Tm^T on the tensor core and -W^T into the slot.
-// Group A runs task j + 1 while group B finishes task j.  The two groups
-// share no barrier: they hand the Gram accumulator, K+ and beta over through
-// mbarriers (see the kernel), so each group synchronises with a named barrier
-// of its own 256 threads.
+// Group A runs task j + 1 (and issues its Gram products into the other TMEM
+// buffer) while group B finishes task j.  The two groups share no barrier:
+// they hand the Gram accumulator, K+ and beta over through mbarriers (see
+// the kernel), so each group synchronises with a named barrier of its own
+// 256 threads.
 //
 // The Gram products are one M = 128 x N = 256 x K = 128 product: A = X~ (the
 // q and k rows of the four 16-token blocks, [Q3 K3 Q2 K2 Q1 K1 Q0 K0], stored
@@ -59,9 +60,13 @@ constexpr uint32_t P_BETA = 214016;     // 2 buffers [64] beta (0 past the chunk
 constexpr uint32_t P_TOT = 214528;      // [4][128] block totals of g (log2 units)
 constexpr uint32_t P_END = 216576;
 
-// TMEM columns of a producer
+// TMEM columns of a producer: two buffers of 256 columns, task j in buffer
+// j & 1 -- its Gram products, then (once the epilogue has read them) W^T in
+// its first 64 columns -- so that group A can issue the next task's Gram
+// products while group B still works on this one.  Offsets within a buffer:
 constexpr uint32_t TG_G = 0;            // Gram: 256 columns
-constexpr uint32_t TG_W = 256;          // W^T [128 c][64 r]
+constexpr uint32_t TG_W = 0;            // W^T [128 c][64 r]
+constexpr uint32_t kGramBufCols = 256;
 
 constexpr int kGroupThreads = 256;
 constexpr int kBarA = 1;                // named barrier of group A
@@ -406,7 +411,8 @@ __device__ __forceinline__ void a_operands_block(uint8_t* sm, int c, int ab,
     }
 }
 
-// (one thread) the Gram products into TG_G: [X~ rows] x [4 key copies].
+// (one thread) the Gram products into TG_G of the buffer at tbase: [X~ rows]
+// x [4 key copies].
 __device__ __forceinline__ void a_issue_gram(uint32_t smem_base, uint32_t tbase) {
     const uint32_t id = idesc_bf16(128, 256, 1, 1);
 #pragma unroll
@@ -550,7 +556,7 @@ __device__ __forceinline__ void b_solve(uint8_t* sm, int lt, int lw, int lane,
     }
 }
 
-// (one thread) W^T = K+^T Tm^T into TG_W (K+ at kp_off).
+// (one thread) W^T = K+^T Tm^T into TG_W of the buffer at tbase (K+ at kp_off).
 __device__ __forceinline__ void b_issue_w(uint32_t smem_base, uint32_t tbase, uint32_t kp_off) {
     const uint32_t idw = idesc_bf16(128, 64, 0, 0);
 #pragma unroll
