@@ -530,6 +530,7 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
     __shared__ uint64_t bar_fin;       // every MMA of this CTA done
     __shared__ uint64_t bar_gram[2];   // producer: Gram products of task j done (buffer j & 1)
     __shared__ uint64_t bar_bdone[2];  // producer: B finished task j (K+, beta buffer j & 1 free)
+    __shared__ uint64_t bar_aw[2];     // producer: A's writes of task j into its slot done
     __shared__ uint64_t bar_w;         // producer: W^T of a task done
     __shared__ uint64_t bar_finb;      // producer: every MMA of group B done
     __shared__ uint32_t tmem_base_s;
@@ -559,6 +560,8 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
         mbar_init(&bar_gram[1], 1);
         mbar_init(&bar_bdone[0], 1);
         mbar_init(&bar_bdone[1], 1);
+        mbar_init(&bar_aw[0], 1);
+        mbar_init(&bar_aw[1], 1);
         mbar_init(&bar_w, 1);
         mbar_init(&bar_finb, 1);
         fence_mbar_init();
@@ -952,12 +955,13 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
         // UT solve, W) out of the other buffer.  Hand-overs, all mbarriers with
         // one arrival: bar_gram[j & 1] (task j's Gram done: B reads it, A may
         // overwrite the operand tiles; one barrier per buffer, so that a waiter
-        // never faces a phase two tasks ahead), bar_bdone[j & 1] (B finished
-        // task j: its TMEM buffer, K+ and beta buffers are free and its slot
-        // writes done).  A thread of group A raises each slot's flag (release)
-        // once both groups' writes to it are done, one task later; before
-        // group A waits for a consumer to free a slot it raises the flag it
-        // still holds, so that no wait depends on an unraised flag.
+        // never faces a phase two tasks ahead), bar_aw[j & 1] (A's writes of
+        // task j into its slot done), bar_bdone[j & 1] (B finished task j: its
+        // TMEM buffer, K+ and beta buffers are free).  Group B raises each
+        // slot's flag (release) once it has finished the task: B waits on
+        // nothing outside the CTA, so every flag is raised without depending on
+        // a consumer, and the release's wait for the slot writes to drain falls
+        // in B's idle time instead of holding up group A's barriers.
         using namespace split;
         const int total = meta.task0[p.n_batches];
         constexpr bool conv = kConv;
@@ -985,7 +989,7 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
         int t = next_task((int)blockIdx.x - p.n_cons, cur);
         if (grpA) {
             // ---------------------------------------------------- group A
-            constexpr int kPublisher = 32;   // lane 0 of warp 1
+            constexpr int kChecker = 32;     // lane 0 of warp 1: the slot checks
             auto issue_raw = [&](const SplitTask& tk) {
                 mbar_arrive_expect_tx(&bar_raw, 3 * 16384);
                 tma_load_3d(sm + P_RAWQ, &args.tm_q, 0, tk.h, tk.t0, &bar_raw);
@@ -1002,25 +1006,15 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
             }
             bool raw_pending = t < total;   // a raw load issued and not waited for
             uint32_t raw_par = 0;           // (and the parity it completes)
-            // publisher: the flag of the previous task, not raised yet
-            int32_t pend_slot = -1, pend_val = 0;
-            // publisher: consumer cons_i's counter, read earlier (it only grows)
+            // slot checker: consumer cons_i's counter, read earlier (it only grows)
             int32_t cons_seen = 0;
             int cons_i = -1;
-            // publisher: wait for B to finish task jj, then raise its flag
-            auto raise_pending = [&](int jj) {
-                if (pend_slot < 0) {
-                    return;
-                }
-                if (!mbar_wait(&bar_bdone[jj & 1], (jj >> 1) & 1, &abort_flag)) {
-                    record_timeout(p.status, &abort_flag, 907);
-                    return;
-                }
-                st_release(p.flags + pend_slot, pend_val);
-                pend_slot = -1;
-            };
             const int c = lt & (D - 1);
-            const int hb = lt >> 7;         // the thread's blocks: 2 hb, 2 hb + 1
+            // the thread's two 16-token blocks: {0, 3} or {1, 2}, so that both
+            // halves of the group write the same number of key copies (block a
+            // is in the copies a..3)
+            const int hb = lt >> 7;
+            const int blk0 = hb ? 1 : 0, blk1 = hb ? 2 : 3;
             int j = 0;
             while (t < total) {
                 SplitTask nt;
@@ -1059,10 +1053,10 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 }
                 a_norms(sm, lw, x.lane, cur.L, p.scale, p.l2norm);
                 float al0[16], al1[16];
-                a_gate_block(sm, c, 2 * hb, cur.L, meta.eA[cur.h], al0);
-                a_gate_block(sm, c, 2 * hb + 1, cur.L, meta.eA[cur.h], al1);
+                a_gate_block(sm, c, blk0, cur.L, meta.eA[cur.h], al0);
+                a_gate_block(sm, c, blk1, cur.L, meta.eA[cur.h], al1);
                 // is the slot free (its consumer has copied out the chunk that was in it)?
-                if (lt == kPublisher) {
+                if (lt == kChecker) {
                     if (cons_i != cur.i || cons_seen < cur.g - p.ring + 1) {
                         cons_seen = ld_acquire(p.cons_done + cur.i);
                         cons_i = cur.i;
@@ -1073,13 +1067,10 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                     break;
                 }
                 if (!s_slot_free) {
-                    // raise the previous task's flag first (no wait may depend on it)
-                    if (lt == kPublisher) {
-                        raise_pending(j - 1);
-                        if (!wait_at_least(p.cons_done + cur.i, cur.g - p.ring + 1, &abort_flag,
-                                           p.peer_wait_polls)) {
-                            record_timeout(p.status, &abort_flag, 962);
-                        }
+                    if (lt == kChecker &&
+                        !wait_at_least(p.cons_done + cur.i, cur.g - p.ring + 1, &abort_flag,
+                                       p.peer_wait_polls)) {
+                        record_timeout(p.status, &abort_flag, 962);
                     }
                     group_sync(kBarA);
                 }
@@ -1089,8 +1080,8 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                     record_timeout(p.status, &abort_flag, 969);
                 }
                 // the operand tiles
-                a_operands_block(sm, c, 2 * hb, al0, kp, pub, rec);
-                a_operands_block(sm, c, 2 * hb + 1, al1, kp, pub, rec);
+                a_operands_block(sm, c, blk0, al0, kp, pub, rec);
+                a_operands_block(sm, c, blk1, al1, kp, pub, rec);
                 fence_proxy_async();
                 tc_fence_before();
                 const bool stop = group_sync_or(kBarA, abort_flag != 0);
@@ -1099,6 +1090,8 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                     break;
                 }
                 if (tid == 0) {
+                    // every thread of A has written its part of task j's slot
+                    mbar_arrive(&bar_aw[j & 1]);
                     if (has_next) {   // the raw tiles are consumed: fetch the next task's
                         issue_raw(nt);
                     }
@@ -1109,24 +1102,14 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 }
                 raw_pending = has_next;
                 raw_par = (j + 1) & 1;
-                // the previous task's flag, while the other warps wait for the next
-                // raw tiles (a release after fresh writes waits for them to drain)
-                if (lt == kPublisher) {
-                    raise_pending(j - 1);
-                    pend_slot = slot;
-                    pend_val = cur.g + 1;
-                    if (has_next) {   // read ahead of its use (this warp waits here anyway)
-                        cons_seen = ld_acquire(p.cons_done + nt.i);
-                        cons_i = nt.i;
-                    }
+                // the next slot's consumer counter, read ahead of its use
+                if (lt == kChecker && has_next) {
+                    cons_seen = ld_acquire(p.cons_done + nt.i);
+                    cons_i = nt.i;
                 }
                 cur = nt;
                 t = tn;
                 ++j;
-            }
-            // the last task's flag
-            if (lt == kPublisher && !abort_flag) {
-                raise_pending(j - 1);
             }
             // a loop left early may still have a raw load in flight into this CTA's smem
             if (raw_pending) {
@@ -1177,7 +1160,18 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 tc_fence_before();
                 group_sync(kBarB);
                 if (lt == 0) {
+                    // A's writes of task j (ordered before its arrival, which came
+                    // before the Gram products B waited for) and B's (ordered by
+                    // the group barrier) are all done: raise the slot's flag.
+                    // bar_aw[j & 1] cannot complete again before this wait: A
+                    // arrives for task j + 2 only after B finished task j.
+                    const bool aw = mbar_wait(&bar_aw[j & 1], (j >> 1) & 1, &abort_flag);
                     mbar_arrive(&bar_bdone[j & 1]);
+                    if (aw) {
+                        st_release(p.flags + slot, cur.g + 1);
+                    } else {
+                        record_timeout(p.status, &abort_flag, 1064);
+                    }
                 }
 
                 cur = nt;
