@@ -268,27 +268,36 @@ __device__ __forceinline__ void a_norms(uint8_t* sm, int lw, int lane, int L, fl
         sq[tt] = q0 * q0 + q1 * q1 + q2 * q2 + q3 * q3;
         sk[tt] = k0 * k0 + k1 * k1 + k2 * k2 + k3 * k3;
     }
+    // The 16 sums (8 tokens of q, then of k) over the 32 lanes, halving the
+    // values at each step: at offset o a lane keeps the half of its values
+    // that its lane bit o selects and adds the partner's copy of that half.
+    // Afterwards lanes 2m and 2m + 1 hold sum number ((m >> 3) & 1) * 8 +
+    // (m & 7) -- tensor bit 4 of the lane, token bits 3..1.
+    float v16[16];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
+    for (int tt = 0; tt < 8; ++tt) {
+        v16[tt] = sq[tt];
+        v16[8 + tt] = sk[tt];
+    }
 #pragma unroll
-        for (int tt = 0; tt < 8; ++tt) {
-            sq[tt] += __shfl_xor_sync(0xffffffffu, sq[tt], off);
-            sk[tt] += __shfl_xor_sync(0xffffffffu, sk[tt], off);
+    for (int off = 16, n = 16; off >= 2; off >>= 1, n >>= 1) {
+        const bool hi = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float keep = hi ? v16[n / 2 + i] : v16[i];
+            const float send = hi ? v16[i] : v16[n / 2 + i];
+            v16[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
         }
     }
-    if (lane < 8) {
-        float a = sq[0], b = sk[0];
-#pragma unroll
-        for (int tt = 1; tt < 8; ++tt) {
-            if (lane == tt) {
-                a = sq[tt];
-                b = sk[tt];
-            }
-        }
-        const int r = lw * 8 + lane;
+    const float tot = v16[0] + __shfl_xor_sync(0xffffffffu, v16[0], 1);
+    if ((lane & 1) == 0) {
+        const int r = lw * 8 + ((lane >> 1) & 7);
         const bool valid = r < L;
-        s_invq[r] = valid ? (l2norm ? rsqrtf(a + kNormEps) : 1.0f) * scale : 0.0f;
-        s_invk[r] = valid ? (l2norm ? rsqrtf(b + kNormEps) : 1.0f) : 0.0f;
+        if (lane & 16) {
+            s_invk[r] = valid ? (l2norm ? rsqrtf(tot + kNormEps) : 1.0f) : 0.0f;
+        } else {
+            s_invq[r] = valid ? (l2norm ? rsqrtf(tot + kNormEps) : 1.0f) * scale : 0.0f;
+        }
     }
 }
 
