@@ -546,23 +546,6 @@ constexpr uint32_t TC_U = 192;    // U^T  fp32 [128 j][64 r]
 constexpr uint32_t TC_SB = 256;   // S^T  bf16, 64 columns
 constexpr uint32_t TC_UB = 320;   // U^T  bf16, 32 columns
 
-// S^T (TMEM, fp32) -> bf16 at TC_SB; all 16 warps, 32 c each.  No barrier.
-__device__ __forceinline__ void phase_state_to_tmem(const Ctx& x) {
-    const int cb = 32 * x.sub;
-    uint32_t r0[16], r1[16];
-    tmem_ld16(x.tbase + x.lane_base + TC_S + cb, r0);
-    tmem_ld16(x.tbase + x.lane_base + TC_S + cb + 16, r1);
-    tmem_wait_ld();
-    uint32_t w[16];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        w[i] = pack_bf16x2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
-        w[8 + i] = pack_bf16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
-    }
-    tmem_st16(x.tbase + x.lane_base + TC_SB + cb / 2, w);
-    tmem_wait_st();
-}
-
 // S^T (TMEM, fp32) -> bf16 at TC_SB, and S^T *= Gamma in the same pass (the
 // next chunk's products read the bf16 copy of the undecayed state and
 // accumulate onto the decayed one); all 16 warps, 32 c each.  No barrier.
@@ -639,24 +622,6 @@ __device__ __forceinline__ void phase_ot_store(const Ctx& x, __nv_bfloat16* o_g,
     }
 }
 
-// S^T *= Gamma_C in TMEM; all 16 warps, 32 c each.  No barrier.
-__device__ __forceinline__ void phase_state_decay(const Ctx& x, const float* gam) {
-    const int cb = 32 * x.sub;
-    const uint32_t taddr = x.tbase + x.lane_base + TC_S + cb;
-    uint32_t r0[16], r1[16];
-    tmem_ld16(taddr, r0);
-    tmem_ld16(taddr + 16, r1);
-    tmem_wait_ld();
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        r0[i] = __float_as_uint(__uint_as_float(r0[i]) * gam[cb + i]);
-        r1[i] = __float_as_uint(__uint_as_float(r1[i]) * gam[cb + 16 + i]);
-    }
-    tmem_st16(taddr, r0);
-    tmem_st16(taddr + 16, r1);
-    tmem_wait_st();
-}
-
 // U^T (TMEM, fp32) -> bf16 at TC_UB; all 16 warps, 16 r each.  No barrier.
 __device__ __forceinline__ void phase_u_to_tmem(const Ctx& x) {
     uint32_t r[16];
@@ -668,30 +633,6 @@ __device__ __forceinline__ void phase_u_to_tmem(const Ctx& x) {
         w[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
     }
     tmem_st8(x.tbase + x.lane_base + TC_UB + 8 * x.sub, w);
-    tmem_wait_st();
-}
-
-// O^T (TMEM lane j, column r) -> o (bf16), then O^T = 0 for the next chunk's
-// accumulation.  Each warp handles 16 tokens of its 32 value columns; for a
-// token the warp's lanes cover 64 contiguous bytes of o.  No barrier.
-__device__ __forceinline__ void phase_ot_epilogue_zero(const Ctx& x, __nv_bfloat16* o_g,
-                                                       int64_t t0, int L, int h, int H) {
-    const int j = 32 * x.qd + x.lane;
-    const int r0 = 16 * x.sub;
-    const uint32_t taddr = x.tbase + x.lane_base + TC_O + r0;
-    uint32_t r[16];
-    tmem_ld16(taddr, r);
-    tmem_wait_ld();
-    __nv_bfloat16* dst = o_g + ((size_t)(t0 + r0) * H + h) * D + j;
-    const size_t row = (size_t)H * D;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        if (r0 + i < L) {
-            dst[i * row] = __float2bfloat16_rn(__uint_as_float(r[i]));
-        }
-        r[i] = 0u;
-    }
-    tmem_st16(taddr, r);
     tmem_wait_st();
 }
 
@@ -826,17 +767,6 @@ __device__ __forceinline__ void issue_u_prime(const Ctx& x, const StateTiles& st
 // ---------------------------------------------------------------- P6 / P8
 // A 128-lane x 64-token fp32 TMEM block -> bf16 tile rows (lane = row), 16
 // tokens per warp (all 16 warps).  No barrier.
-__device__ __forceinline__ void phase_tile_from_tmem_to(const Ctx& x, uint32_t tm_col,
-                                                        uint8_t* tile, float sign = 1.0f) {
-    uint32_t r[16];
-    tmem_ld16(x.tbase + x.lane_base + tm_col + 16 * x.sub, r);
-    tmem_wait_ld();
-    float v[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = sign * __uint_as_float(r[i]);
-    store_row16(tile, 32 * x.qd + x.lane, 32 * x.sub, v);
-}
-
 __device__ __forceinline__ void phase_tile_from_tmem(const Ctx& x, uint32_t tm_col, uint32_t tile) {
     uint32_t r[16];
     tmem_ld16(x.tbase + x.lane_base + tm_col + 16 * x.sub, r);
@@ -915,140 +845,6 @@ __device__ __forceinline__ void phase_o_epilogue(const Ctx& x, __nv_bfloat16* o_
         if (r0 + i < L) {
             dst[i * row] = __float2bfloat16_rn(__uint_as_float(r[i]));
         }
-    }
-}
-
-// ---------------------------------------------------------------- half-CTA variants
-// The split kernel's producer runs the tail of a chunk (Gram epilogue, UT
-// solve, W) on warps 0-7 while warps 8-15 start the next chunk (norms, gate).
-// These variants cover one half (256 threads) and synchronise it with a
-// named barrier; their arithmetic is that of the full-CTA phases.
-constexpr int kHalfThreads = 256;
-constexpr int kBarLow = 1;   // named barrier of warps 0-7
-
-__device__ __forceinline__ void half_sync(int id) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(kHalfThreads) : "memory");
-}
-
-// Per-token L2 norms, 8 tokens per warp; lw = warp index within the half.
-__device__ __forceinline__ void phase_norms_half(const Ctx& x, int lw, int L, float scale,
-                                                 int l2norm) {
-    const uint8_t* rq = x.sm + OFF_RAWQ;
-    const uint8_t* rk = x.sm + OFF_RAWK;
-    float* s_invq = reinterpret_cast<float*>(x.sm + OFF_INVQ);
-    float* s_invk = reinterpret_cast<float*>(x.sm + OFF_INVK);
-    float sq[8], sk[8];
-#pragma unroll
-    for (int tt = 0; tt < 8; ++tt) {
-        const int r = lw * 8 + tt;
-        const uint2 qv = *reinterpret_cast<const uint2*>(rq + r * 256 + x.lane * 8);
-        const uint2 kv = *reinterpret_cast<const uint2*>(rk + r * 256 + x.lane * 8);
-        const float q0 = bf16lo(qv.x), q1 = bf16hi(qv.x), q2 = bf16lo(qv.y), q3 = bf16hi(qv.y);
-        const float k0 = bf16lo(kv.x), k1 = bf16hi(kv.x), k2 = bf16lo(kv.y), k3 = bf16hi(kv.y);
-        sq[tt] = q0 * q0 + q1 * q1 + q2 * q2 + q3 * q3;
-        sk[tt] = k0 * k0 + k1 * k1 + k2 * k2 + k3 * k3;
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-#pragma unroll
-        for (int tt = 0; tt < 8; ++tt) {
-            sq[tt] += __shfl_xor_sync(0xffffffffu, sq[tt], off);
-            sk[tt] += __shfl_xor_sync(0xffffffffu, sk[tt], off);
-        }
-    }
-    if (x.lane < 8) {
-        float a = sq[0], b = sk[0];
-#pragma unroll
-        for (int tt = 1; tt < 8; ++tt) {
-            if (x.lane == tt) {
-                a = sq[tt];
-                b = sk[tt];
-            }
-        }
-        const int r = lw * 8 + x.lane;
-        const bool valid = r < L;
-        s_invq[r] = valid ? (l2norm ? rsqrtf(a + kNormEps) : 1.0f) * scale : 0.0f;
-        s_invk[r] = valid ? (l2norm ? rsqrtf(b + kNormEps) : 1.0f) : 0.0f;
-    }
-}
-
-// phase_solve on warps 0-7 (named barrier kBarLow); Tm also to `pub` when
-// kPub.  The caller must have synchronised the half after the Gram epilogue.
-template <bool kPub>
-__device__ __forceinline__ void phase_solve_half(const Ctx& x, uint8_t* pub) {
-    const float* s_beta = reinterpret_cast<const float*>(x.sm + OFF_BETA);
-    float* Lm = reinterpret_cast<float*>(x.sm + OFF_AKK);
-    float* Nm = reinterpret_cast<float*>(x.sm + OFF_NMAT);
-    if (x.tid < 64) {
-        const int a = x.tid >> 4, jj = x.tid & 15;
-        const float* Lb = Lm + (16 * a) * 65 + 16 * a;
-        float acc[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) acc[r] = (r == jj) ? 1.0f : 0.0f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float xi = (i < jj) ? 0.0f : acc[i];
-            acc[i] = xi;
-#pragma unroll
-            for (int r = i + 1; r < 16; ++r) acc[r] -= Lb[r * 65 + i] * xi;
-        }
-#pragma unroll
-        for (int r = 0; r < 16; ++r) Nm[(16 * a + r) * 65 + 16 * a + jj] = acc[r];
-    }
-    half_sync(kBarLow);
-    if (x.warp < 6) {
-        // (a, c) = (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
-        const int a = x.warp < 1 ? 1 : x.warp < 3 ? 2 : 3;
-        const int c = x.warp < 1 ? 0 : x.warp < 3 ? x.warp - 1 : x.warp - 3;
-        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        warp_gemm16(acc, Nm, 16 * a, 16 * a, Lm, 16 * a, 16 * c, x.lane);
-        warp_store16(acc, Lm, 16 * a, 16 * c, 1.0f, x.lane);
-    }
-    half_sync(kBarLow);
-#pragma unroll 1
-    for (int wave = 1; wave < 4; ++wave) {
-        if (x.warp < 4 - wave) {
-            const int a = x.warp + wave, b = x.warp;
-            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            for (int cc = b; cc < a; ++cc) {
-                warp_gemm16(acc, Lm, 16 * a, 16 * cc, Nm, 16 * cc, 16 * b, x.lane);
-            }
-            warp_store16(acc, Nm, 16 * a, 16 * b, -1.0f, x.lane);
-        }
-        half_sync(kBarLow);
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int r = (x.tid >> 3) + 32 * h, i0 = (x.tid & 7) * 8;
-        uint4 w;
-        float v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int i = i0 + u;
-            v[u] = i <= r ? Nm[r * 65 + i] * s_beta[i] : 0.0f;
-        }
-        w.x = pack_bf16x2(v[0], v[1]); w.y = pack_bf16x2(v[2], v[3]);
-        w.z = pack_bf16x2(v[4], v[5]); w.w = pack_bf16x2(v[6], v[7]);
-        *reinterpret_cast<uint4*>(x.sm + OFF_TM + sw128(r, 2 * i0)) = w;
-        if (kPub) {
-            *reinterpret_cast<uint4*>(pub + HO_TM + sw128(r, 2 * i0)) = w;
-        }
-    }
-}
-
-// -W^T (TMEM TM_W) -> tile, warps 0-7: each covers 32 of the 64 token
-// columns of its lane quadrant.  No barrier.
-__device__ __forceinline__ void phase_neg_w_tile_half(const Ctx& x, uint8_t* tile) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int sub = 2 * (x.warp >> 2) + h;
-        uint32_t r[16];
-        tmem_ld16(x.tbase + x.lane_base + TM_W + 16 * sub, r);
-        tmem_wait_ld();
-        float v[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = -1.0f * __uint_as_float(r[i]);
-        store_row16(tile, 32 * x.qd + x.lane, 32 * sub, v);
     }
 }
 
