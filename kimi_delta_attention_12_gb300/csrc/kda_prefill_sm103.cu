@@ -715,7 +715,10 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                                 &s_ck)
                     : 0;
 
-            int fetched = 0;  // thread 0: chunks of this unit whose copies are issued
+            // Thread 0 issues the tensor-core products and the v tiles; thread 32
+            // polls the ring flags and issues the slot copies, so that their
+            // acquire loads and proxy fences do not hold up the next products.
+            int fetched = 0;  // thread 32: chunks of this unit whose copies are issued
             int waited = 0;   // chunks of this unit every thread has waited for
             int v_issued = 0, v_waited = 0;   // thread 0: v tiles of this unit
             // thread 0: load chunk c's v tile (an input, independent of the
@@ -743,11 +746,11 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 }
                 return ok;
             };
-            // thread 0: the ring flag of chunk c
+            // thread 32: the ring flag of chunk c
             auto flag_of = [&](int c) -> const int32_t* {
                 return p.flags + i * p.ring + (g0 + c) % p.ring;
             };
-            // thread 0: copy chunk c's slot into buffer (cnt + c) & 1 (block: wait
+            // thread 32: copy chunk c's slot into buffer (cnt + c) & 1 (block: wait
             // for its flag; ready: an earlier acquire load of it saw it raised)
             auto fetch = [&](int c, bool block, bool ready = false) -> bool {
                 const int32_t g = g0 + c;
@@ -795,6 +798,8 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                     for (int c = 0; c < nch && c < kVRing; ++c) {
                         issue_v(c);
                     }
+                }
+                if (tid == 32) {
                     if (fetch(0, true) && nch > 1) {
                         fetch(1, false);
                     }
@@ -816,7 +821,7 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 cta_sync_tc();
             }
             uint32_t ob[8];   // the last chunk's O^T as bf16 pairs, stored one chunk later
-            // thread 0: flags read during the last chunk's products: of the next
+            // thread 32: flags read during the last chunk's products: of the next
             // chunk (pf1, when it was not copied yet) and of the one after (pf2)
             int32_t pf1 = 0, pf2 = 0;
             for (int c = 0; c < nch && !abort_flag; ++c) {
@@ -825,13 +830,13 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 if (tid == 0) {
                     issue_ou_tc(x, st);
                     mma_commit(&bar_u);
-                    // chunk c + 1 into the buffer chunk c - 1 left, if the flag read
-                    // during the last chunk's products showed it published (before
-                    // this thread's output stores below, which the copy's proxy
-                    // fence would otherwise wait for)
-                    if (fetched == c + 1 && c + 1 < nch && pf2 >= g0 + c + 2) {
-                        fetch(c + 1, false, true);
-                    }
+                }
+                // chunk c + 1 into the buffer chunk c - 1 left, if the flag read
+                // during the last chunk's products showed it published (before
+                // this thread's output stores below, which the copy's proxy
+                // fence would otherwise wait for)
+                if (tid == 32 && fetched == c + 1 && c + 1 < nch && pf2 >= g0 + c + 2) {
+                    fetch(c + 1, false, true);
                 }
                 // the previous chunk's o while the tensor core works
                 if (c > 0 && o_g) {
@@ -851,6 +856,8 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 if (tid == 0) {
                     issue_so_tc(x, st);
                     mma_commit(&bar_os);
+                }
+                if (tid == 32) {
                     // the flag of the chunk after next, read while the tensor core
                     // works (the acquire load's latency overlaps the products); its
                     // copy is issued at the top of the next chunk
@@ -867,19 +874,21 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 }
                 ph_os ^= 1;
                 tc_fence_after();
+                // the next chunk's slot, if not copied yet (a chunk the producers
+                // have not published yet is waited for)
+                if (tid == 32 && !abort_flag && c + 1 < nch && fetched < c + 2) {
+                    fetch(c + 1, pf1 < g0 + c + 2, pf1 >= g0 + c + 2);
+                }
                 if (tid == 0 && !abort_flag) {
                     if (c + 1 < nch) {
-                        // the next chunk's U' = V Tm^T (its slot must have landed; a
-                        // chunk the producers have not published yet is waited for)
-                        if (fetched >= c + 2 || fetch(c + 1, pf1 < g0 + c + 2, pf1 >= g0 + c + 2)) {
-                            const uint32_t r = cnt + c + 1;
-                            if (mbar_wait(&bar_full[r & 1], (r >> 1) & 1, &abort_flag) &&
-                                wait_v(c + 1)) {
-                                tc_fence_after();
-                                issue_u_prime_tc(x, tiles(r & 1, (vcnt + c + 1) % kVRing));
-                            } else {
-                                record_timeout(p.status, &abort_flag, 785);
-                            }
+                        // the next chunk's U' = V Tm^T, once its slot has landed
+                        const uint32_t r = cnt + c + 1;
+                        if (mbar_wait(&bar_full[r & 1], (r >> 1) & 1, &abort_flag) &&
+                            wait_v(c + 1)) {
+                            tc_fence_after();
+                            issue_u_prime_tc(x, tiles(r & 1, (vcnt + c + 1) % kVRing));
+                        } else {
+                            record_timeout(p.status, &abort_flag, 785);
                         }
                     }
                     // U'(c) and the products of chunk c are done: its v slot takes
@@ -918,8 +927,10 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 }
             }
             // copies still in flight into this CTA's buffers (a loop left early)
-            if (tid == 0) {
+            if (tid == 32) {
                 s_issued = fetched;
+            }
+            if (tid == 0) {
                 for (int c = v_waited; c < v_issued; ++c) {
                     const uint32_t r = vcnt + c;
                     mbar_wait(&bar_v[r % kVRing], (r / kVRing) & 1, nullptr);
