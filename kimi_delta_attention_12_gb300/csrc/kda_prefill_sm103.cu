@@ -876,8 +876,15 @@ kda_split_kernel(const __grid_constant__ ChunkedArgs args) {
                 tc_fence_after();
                 // the next chunk's slot, if not copied yet (a chunk the producers
                 // have not published yet is waited for)
-                if (tid == 32 && !abort_flag && c + 1 < nch && fetched < c + 2) {
-                    fetch(c + 1, pf1 < g0 + c + 2, pf1 >= g0 + c + 2);
+                if (tid == 32 && !abort_flag) {
+                    if (c + 1 < nch && fetched < c + 2) {
+                        fetch(c + 1, pf1 < g0 + c + 2, pf1 >= g0 + c + 2);
+                    }
+                    // chunk c's buffer is free once its products are done: the chunk
+                    // after next goes into it now if its flag showed it published
+                    if (c + 2 < nch && fetched == c + 2 && pf2 >= g0 + c + 3) {
+                        fetch(c + 2, false, true);
+                    }
                 }
                 if (tid == 0 && !abort_flag) {
                     if (c + 1 < nch) {
